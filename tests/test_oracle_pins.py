@@ -1,0 +1,348 @@
+"""Pins for the CPU oracle: checks against the pages, closed forms and exact arithmetic.
+
+Each ``pin_*`` function takes the oracle module so that ``test_planted_*``
+can run it against a copy with a deliberate mistake and show that the pin
+notices. All tests here are CPU-only.
+"""
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import torch
+
+import oracle.nvfp4_oracle as O
+from nvfp4_quantized_matmul_gb300 import synth
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _read_table(name):
+    rows = []
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if line and not line.startswith("#"):
+                rows.append(line.split())
+    return rows
+
+
+# ---------------------------------------------------------------- independent decoders
+
+def frac_e2m1(c: int) -> Fraction:
+    """E2M1 from its bit layout: sign(1) exponent(2, bias 1) mantissa(1)."""
+    s, e, m = (c >> 3) & 1, (c >> 1) & 3, c & 1
+    mag = Fraction(m, 2) if e == 0 else Fraction(2) ** (e - 1) * (1 + Fraction(m, 2))
+    return -mag if s else mag
+
+
+def frac_e4m3(b: int):
+    """E4M3FN from its bit layout (None for NaN)."""
+    s, e, m = (b >> 7) & 1, (b >> 3) & 15, b & 7
+    if e == 15 and m == 7:
+        return None
+    mag = Fraction(m, 8) * Fraction(2) ** -6 if e == 0 else (1 + Fraction(m, 8)) * Fraction(2) ** (e - 7)
+    return -mag if s else mag
+
+
+def pack_codes(codes: np.ndarray) -> np.ndarray:
+    """Pack codes [.., K] into words [.., K/8], column 8j+i in nibble i (test's own packer)."""
+    codes = np.asarray(codes, dtype=np.int64)
+    k = codes.shape[-1]
+    c = codes.reshape(*codes.shape[:-1], k // 8, 8)
+    w = np.zeros(c.shape[:-1], dtype=np.int64)
+    for i in range(8):
+        w |= c[..., i] << (4 * i)
+    return w.astype(np.uint32)
+
+
+# ---------------------------------------------------------------- pins
+
+def pin_e2m1_table(orc):
+    table = {int(c): float(v) for c, v in _read_table("e2m1_table.txt")}
+    got = orc.e2m1_value(np.arange(16))
+    for c in range(16):
+        assert got[c] == table[c], (c, got[c], table[c])
+        # the sign of zero matters: code 8 is -0.0
+        assert np.signbit(got[c]) == (c >= 8), c
+        assert got[c] == float(frac_e2m1(c))
+
+
+def pin_e4m3_all_bytes(orc):
+    b = np.arange(256)
+    got = orc.e4m3_value(b)
+    lib = torch.from_numpy(b.astype(np.uint8)).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    nan = np.isnan(lib)
+    assert np.array_equal(np.isnan(got), nan)
+    assert set(np.nonzero(nan)[0].tolist()) == {0x7F, 0xFF}
+    assert np.array_equal(got[~nan], lib[~nan])
+    assert np.array_equal(np.signbit(got[~nan]), np.signbit(lib[~nan]))
+    for v in range(256):
+        f = frac_e4m3(v)
+        assert (f is None) == np.isnan(got[v])
+        if f is not None:
+            assert got[v] == float(f)
+    assert got[0x7E] == 448.0 and got[0x01] == 2.0**-9 and got[0x38] == 1.0
+
+
+def pin_packing(orc):
+    w = np.array([[0x76543210, 0xFEDCBA98]], dtype=np.uint32)
+    assert orc.unpack_codes(w).tolist() == [list(range(16))]
+    g = synth.rng(11)
+    codes = g.integers(0, 16, size=(3, 64))
+    assert np.array_equal(orc.unpack_codes(pack_codes(codes)), codes)
+
+
+def pin_block_scale_broadcast(orc):
+    # every code 2 (= 1.0); scale of group j is 2^(j-2): value at column k is 2^(k//16 - 2)
+    n, k = 2, 64
+    w = pack_codes(np.full((n, k), 2))
+    sbytes = synth.e4m3_bytes(np.array([[2.0 ** (j - 2) for j in range(k // 16)]] * n))
+    v = orc.block_values(w, sbytes)
+    expect = np.array([2.0 ** (c // 16 - 2) for c in range(k)])
+    assert np.array_equal(v, np.broadcast_to(expect, (n, k)))
+
+
+def _brute_force_qmm(x, codes, sbytes, gs):
+    """Exact-rational y = factor * x @ (fp4 * e4m3).T, factor = RN_f32(gs/2688)."""
+    m_, k = x.shape
+    n = codes.shape[0]
+    fac = Fraction(1) if gs is None else Fraction(float(np.float32(np.float32(gs) / np.float32(2688))))
+    y = np.empty((m_, n), dtype=np.float64)
+    for m in range(m_):
+        for j in range(n):
+            acc = Fraction(0)
+            for c in range(k):
+                acc += Fraction(float(x[m, c])) * frac_e2m1(int(codes[j, c])) * frac_e4m3(int(sbytes[j, c // 16]))
+            y[m, j] = float(acc * fac)
+    return y
+
+
+def pin_brute_force_matmul(orc):
+    g = synth.rng(5)
+    for gs in (None, np.float32(26.88)):
+        m, n, k = 3, 5, 48
+        codes = g.integers(0, 16, size=(n, k))
+        sbytes = synth.log_uniform_scales(g, (n, k // 16), 2.0**-4, 2.0**4)
+        x = synth.activations(g, (m, k), "bf16").double().numpy()
+        got = orc.qmm(x, pack_codes(codes), sbytes, gs)
+        ref = _brute_force_qmm(x, codes, sbytes, gs)
+        # float64 accumulation of at most 48 dyadic terms: well inside 1e-12 of max
+        assert np.max(np.abs(got - ref)) <= 1e-12 * max(1.0, np.max(np.abs(ref)))
+
+
+def pin_one_hot(orc):
+    # unit scales and one-hot activations pick out single table entries
+    n, k = 16, 32
+    codes = np.arange(n * k).reshape(n, k) % 16
+    sbytes = np.full((n, k // 16), 0x38, dtype=np.uint8)
+    for col in (0, 7, 8, 31):
+        x = np.zeros((1, k))
+        x[0, col] = 1.0
+        y = orc.qmm(x, pack_codes(codes), sbytes, None)
+        table = {int(c): float(v) for c, v in _read_table("e2m1_table.txt")}
+        assert y[0].tolist() == [table[int(codes[j, col])] for j in range(n)]
+
+
+def pin_global_factor(orc):
+    divisor = int(_read_table("global_scale_convention.txt")[0][0])
+    g = synth.rng(3)
+    for gs in list(synth.global_scales(g, 200)) + [np.float32(2688.0), np.float32(26.88)]:
+        f = orc.global_factor(gs)
+        assert f.dtype == np.float32
+        exact = Fraction(float(gs)) / divisor
+        # round-to-nearest float32: error at most half an ulp of the result
+        ulp = Fraction(float(np.spacing(np.float32(f))))
+        assert abs(Fraction(float(f)) - exact) <= ulp / 2
+    assert orc.global_factor(np.float32(2688.0)) == 1.0
+    assert orc.global_factor(None) == 1.0
+
+
+def _bf16_rne_bits(f32: np.ndarray) -> np.ndarray:
+    """float32 -> bfloat16 bits, round to nearest even, written with integer ops."""
+    u = f32.astype(np.float32).view(np.uint32).astype(np.uint64)
+    r = (u + 0x7FFF + ((u >> 16) & 1)) >> 16
+    nan = np.isnan(f32)
+    r = np.where(nan, (u >> 16) | 0x40, r)
+    return r.astype(np.uint16)
+
+
+def pin_dequantize_rounding(orc):
+    g = synth.rng(9)
+    n, k = 8, 64
+    w = synth.packed_weight(g, n, k)
+    s = synth.log_uniform_scales(g, (n, k // 16), 2.0**-6, 4.0)
+    exact = orc.block_values(w, s)
+    # without gs the dequantize is exact in every dtype
+    for dt in ("f32", "f16", "bf16"):
+        d = orc.dequantize(w, s, None, dt).double().numpy()
+        assert np.array_equal(d, exact)
+        assert np.array_equal(np.signbit(d), np.signbit(exact))
+    gs = np.float32(1234.5)
+    fac = np.float32(gs) / np.float32(2688)
+    f32 = (exact.astype(np.float32) * fac).astype(np.float32)
+    assert np.array_equal(orc.dequantize(w, s, gs, "f32").numpy().view(np.uint32), f32.view(np.uint32))
+    assert np.array_equal(orc.dequantize(w, s, gs, "f16").numpy().view(np.uint16),
+                          f32.astype(np.float16).view(np.uint16))
+    assert np.array_equal(orc.dequantize(w, s, gs, "bf16").view(torch.uint16).numpy(), _bf16_rne_bits(f32))
+
+
+def pin_sidecar_identity(orc):
+    """native-with-sidecar dequantize reproduces ModelOpt's fp4 * e4m3(ws) * ws2."""
+    g = synth.rng(21)
+    exact_hits = total = 0
+    for _ in range(40):
+        mo_w, mo_ws, ws2 = synth.modelopt_triplet(g, 4, 64)
+        w, s, gs = orc.transcode(mo_w, mo_ws, ws2)
+        native = orc.dequantize(w, s, gs, "f32").numpy()
+        ref = orc.modelopt_values(mo_w, mo_ws, ws2)  # float64
+        ref32 = ref.astype(np.float32)
+        roundtrip = np.float32(gs) / np.float32(2688) == np.float32(ws2)
+        total += 1
+        if roundtrip:
+            exact_hits += 1
+            assert np.array_equal(native.view(np.uint32), ref32.view(np.uint32))
+        else:
+            ulp = np.spacing(np.abs(ref32)).astype(np.float64)
+            assert np.all(np.abs(native.astype(np.float64) - ref) <= 2 * ulp + 0.0)
+    assert exact_hits > 0
+
+
+def pin_transcode_layout(orc):
+    mo_w = np.array([[0x10, 0x32, 0x54, 0x76, 0x98, 0xBA, 0xDC, 0xFE]], dtype=np.uint8)
+    mo_ws = np.array([[0x38]], dtype=np.uint8)
+    w, s, gs = orc.transcode(mo_w, mo_ws, np.float32(0.01))
+    assert w.dtype == np.uint32 and w.tolist() == [[0x76543210, 0xFEDCBA98]]
+    assert s.tolist() == [[0x38]]
+    assert gs == np.float32(np.float32(0.01) * np.float32(2688))
+    # ModelOpt byte j holds columns 2j (low nibble) and 2j+1 (high nibble)
+    assert orc.unpack_codes(w).tolist() == [list(range(16))]
+
+
+def pin_gather_zero_rows(orc):
+    g = synth.rng(4)
+    E, N, K, B = 3, 16, 32, 4
+    w = synth.packed_weight(g, E, N, K)
+    s = synth.log_uniform_scales(g, (E, N, K // 16), 0.25, 4.0)
+    gs = synth.global_scales(g, E)
+    x = synth.activations(g, (B, K), "f32").double().numpy()
+    rhs = np.array([0, 2, E, E + 1, 2**31 - 1, 2**32 - 1, 1, 1], dtype=np.uint32)
+    lhs = np.array([3, 0, 1, 2, 0, 1, B, 2**32 - 1], dtype=np.uint32)
+    y = orc.gather_qmm(x, lhs, rhs, w, s, gs)
+    for r in (2, 3, 4, 5, 6, 7):
+        assert np.all(y[r] == 0.0) and not np.any(np.signbit(y[r]))
+    for r in (0, 1):
+        e = int(rhs[r])
+        ref = orc.qmm(x[lhs[r]:lhs[r] + 1], w[e], s[e], gs[e])[0]
+        assert np.array_equal(y[r], ref)
+
+
+def pin_plane_check(orc):
+    w = np.zeros((4, 8), dtype=np.uint32)
+    orc.check_planes(w, np.zeros((4, 4), dtype=np.uint8))
+    for bad in ((4, 3), (4, 5), (3, 4), (4, 4, 1)):
+        with pytest.raises(ValueError):
+            orc.check_planes(w, np.zeros(bad, dtype=np.uint8))
+
+
+def pin_error_metric(orc):
+    assert orc.rel_to_max_error([1.0, 2.0], [1.0, 4.0]) == 0.5
+    assert orc.rel_to_max_error([0.0], [0.0]) == 0.0
+
+
+PINS = [pin_e2m1_table, pin_e4m3_all_bytes, pin_packing, pin_block_scale_broadcast,
+        pin_brute_force_matmul, pin_one_hot, pin_global_factor, pin_dequantize_rounding,
+        pin_sidecar_identity, pin_transcode_layout, pin_gather_zero_rows, pin_plane_check,
+        pin_error_metric]
+
+
+@pytest.mark.parametrize("pin", PINS, ids=lambda p: p.__name__)
+def test_pin(pin):
+    pin(O)
+
+
+# ---------------------------------------------------------------- planted mistakes
+
+def _planted(monkeypatch, name, fn):
+    monkeypatch.setattr(O, name, fn)
+    return O
+
+
+def test_planted_wrong_table_entry(monkeypatch):
+    monkeypatch.setattr(O, "E2M1_MAGNITUDES", (0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 5.0))
+    with pytest.raises(AssertionError):
+        pin_e2m1_table(O)
+
+
+def test_planted_high_nibble_first(monkeypatch):
+    orig = O.unpack_codes
+
+    def swapped(w):
+        c = orig(w)
+        return c.reshape(*c.shape[:-1], -1, 8)[..., ::-1].reshape(c.shape)
+    _planted(monkeypatch, "unpack_codes", swapped)
+    with pytest.raises(AssertionError):
+        pin_packing(O)
+
+
+def test_planted_e4m3_bias(monkeypatch):
+    orig = O.e4m3_value
+    _planted(monkeypatch, "e4m3_value", lambda b: orig(b) * 2.0)
+    with pytest.raises(AssertionError):
+        pin_e4m3_all_bytes(O)
+
+
+def test_planted_transposed_operand(monkeypatch):
+    orig = O.block_values
+
+    def transposed(w, s):
+        v = orig(w, s)
+        return v[::-1]  # rows in the wrong order
+    _planted(monkeypatch, "block_values", transposed)
+    with pytest.raises(AssertionError):
+        pin_brute_force_matmul(O)
+
+
+def test_planted_factor_inverted(monkeypatch):
+    _planted(monkeypatch, "global_factor",
+             lambda gs: np.float32(1.0) if gs is None else np.float32(2688) / np.float32(gs))
+    with pytest.raises(AssertionError):
+        pin_global_factor(O)
+
+
+def test_planted_gather_ignores_bounds(monkeypatch):
+    def unbounded(x, lhs, rhs, w, scales, gs=None):
+        rhs = np.minimum(np.asarray(rhs, dtype=np.int64), w.shape[0] - 1)
+        lhs = np.minimum(np.asarray(lhs, dtype=np.int64), np.asarray(x).shape[0] - 1)
+        rows = [O.qmm(np.asarray(x)[l:l + 1], w[e], scales[e], None if gs is None else gs[e])[0]
+                for l, e in zip(lhs, rhs)]
+        return np.stack(rows)
+    _planted(monkeypatch, "gather_qmm", unbounded)
+    with pytest.raises(AssertionError):
+        pin_gather_zero_rows(O)
+
+
+def test_planted_scale_per_8_columns(monkeypatch):
+    orig_repeat = np.repeat
+
+    def block_values(w, scales):
+        O.check_planes(w, scales)
+        vals = O.e2m1_value(O.unpack_codes(w))
+        s = O.e4m3_value(scales)
+        s = orig_repeat(s, 8, axis=-1)
+        s = np.concatenate([s, s], axis=-1)
+        return vals * s
+    _planted(monkeypatch, "block_values", block_values)
+    with pytest.raises(AssertionError):
+        pin_block_scale_broadcast(O)
+
+
+def test_planted_sidecar_without_2688(monkeypatch):
+    orig = O.transcode
+
+    def bad(mo_w, mo_ws, ws2):
+        w, s, _ = orig(mo_w, mo_ws, ws2)
+        return w, s, np.float32(ws2)
+    _planted(monkeypatch, "transcode", bad)
+    with pytest.raises(AssertionError):
+        pin_sidecar_identity(O)
