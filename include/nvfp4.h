@@ -1,0 +1,131 @@
+/*
+ * nvfp4.h - C ABI of libnvfp4.so, NVFP4 quantized matmul for NVIDIA GB300 (sm_103a).
+ *
+ * Weight format (mlxcel issue #693 "direct-transcode ModelOpt triplets to MLX
+ * native", Technical notes):
+ *   w       uint32 [E, N, K/8]  eight E2M1 codes per word along K; column
+ *                               8*j+i of a row is nibble i of word j, counted
+ *                               from the least significant nibble. E2M1 code
+ *                               c has magnitude {0,.5,1,1.5,2,3,4,6}[c & 7]
+ *                               and is negative when bit 3 is set.
+ *   scales  uint8  [E, N, K/16] one E4M3 (OCP E4M3FN) byte per 16 columns.
+ *   gs      float  [E] or none  optional global scale; outputs (and
+ *                               dequantized elements) are multiplied by
+ *                               gs[e] / (448 * 6) once (mlxcel PR #2629
+ *                               "ROCm native NVFP4", Summary).
+ * For a single linear E = 1. The scale plane must hold exactly
+ * w.shape[:-1] + [w.shape[-1] / 2] bytes (PR #2629, Changes during review);
+ * lengths are passed so the library can refuse a mismatched plane.
+ *
+ * Conventions for every entry point:
+ *   - All data pointers are DEVICE pointers owned by the caller; the library
+ *     keeps no reference after the call returns. Lengths are element counts.
+ *   - Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL is the
+ *     legacy default stream). Nothing is synchronised, nothing is allocated.
+ *   - Data pointers must be 16-byte aligned; index arrays and gs 4-byte.
+ *   - K must be a multiple of 16. Any N >= 1 is accepted.
+ *   - Empty outputs (M, N or R equal to 0) return NVFP4_OK without a launch.
+ *   - On failure nothing is launched (validation errors) or the CUDA launch
+ *     error is returned as NVFP4_ERR_CUDA; nvfp4_last_error() then holds a
+ *     message for the calling thread.
+ */
+#ifndef NVFP4_H
+#define NVFP4_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  NVFP4_OK = 0,
+  NVFP4_ERR_NULL = 1,    /* a required pointer is NULL */
+  NVFP4_ERR_SHAPE = 2,   /* negative size, K % 16 != 0, size overflow */
+  NVFP4_ERR_PLANE = 3,   /* weight or scale plane length does not match the shape */
+  NVFP4_ERR_DTYPE = 4,   /* unknown dtype or route */
+  NVFP4_ERR_ALIGN = 5,   /* pointer not aligned as required */
+  NVFP4_ERR_GSCALE = 6,  /* gs given with the wrong length (or a length without gs) */
+  NVFP4_ERR_LIMIT = 7,   /* launch dimensions beyond what the kernels support */
+  NVFP4_ERR_CUDA = 8     /* CUDA reported an error at launch */
+} nvfp4_status;
+
+typedef enum { NVFP4_F32 = 0, NVFP4_F16 = 1, NVFP4_BF16 = 2 } nvfp4_dtype;
+
+/* Route for nvfp4_qmm_routed: AUTO picks by the measured M crossover. */
+typedef enum { NVFP4_ROUTE_AUTO = 0, NVFP4_ROUTE_QMV = 1, NVFP4_ROUTE_TC = 2 } nvfp4_route;
+
+/*
+ * ModelOpt triplet -> native planes (issue #693, Goal and Implementation plan
+ * step 3): four source bytes become one little-endian uint32, the E4M3 block
+ * scales are kept byte for byte, and weight_scale_2 becomes the global-scale
+ * sidecar gs = ws2 * 2688 (float32 multiply), so that the native factor
+ * gs / 2688 stands for ws2. No dense intermediate is formed.
+ *   mo_weight        uint8 [N, K/2]   two E2M1 codes per byte, low nibble = even column
+ *   mo_weight_scale  uint8 [N, K/16]  E4M3
+ *   weight_scale_2   float [1]        device scalar
+ *   w_out [N, K/8] uint32, scales_out [N, K/16] uint8, gs_out float [1]
+ * Lengths must equal N*K/2 and N*K/16 (NVFP4_ERR_PLANE otherwise).
+ */
+nvfp4_status nvfp4_transcode(const uint8_t* mo_weight, int64_t mo_weight_len, const uint8_t* mo_weight_scale,
+                             int64_t mo_weight_scale_len, const float* weight_scale_2, int64_t N, int64_t K,
+                             uint32_t* w_out, uint8_t* scales_out, float* gs_out, void* stream);
+
+/*
+ * Exact dequantize (PR #2629, Summary; Changes during review: sized from the
+ * weight plane). out[e, n, k] = cast_rne(f32(fp4 * e4m3) * f32(gs[e] / 2688)),
+ * or the exact product when gs is NULL. out is [E, N, K] of out_dtype.
+ * gs_len must be 0 (gs NULL) or E.
+ */
+nvfp4_status nvfp4_dequantize(const uint32_t* w, int64_t w_len, const uint8_t* scales, int64_t scales_len,
+                              const float* gs, int64_t gs_len, int64_t E, int64_t N, int64_t K,
+                              nvfp4_dtype out_dtype, void* out, void* stream);
+
+/*
+ * QuantizedMatmul (PR #2629, Summary): y = x @ dequantize(w).T, with the
+ * global factor gs / 2688 applied once per output after the f32 sum.
+ *   x [M, K] of x_dtype (f32, f16 or bf16), w [N, K/8], scales [N, K/16],
+ *   gs NULL (gs_len 0) or one float (gs_len 1), y [M, N] of x_dtype.
+ * The route (decode-shape qmv or the tcgen05 tensor-core path) is chosen by
+ * comparing M with nvfp4_qmm_crossover().
+ */
+nvfp4_status nvfp4_qmm(const void* x, nvfp4_dtype x_dtype, int64_t M, int64_t K, const uint32_t* w,
+                       int64_t w_len, const uint8_t* scales, int64_t scales_len, const float* gs,
+                       int64_t gs_len, int64_t N, void* y, void* stream);
+
+/* nvfp4_qmm with an explicit route (tests and crossover sweeps). */
+nvfp4_status nvfp4_qmm_routed(const void* x, nvfp4_dtype x_dtype, int64_t M, int64_t K, const uint32_t* w,
+                              int64_t w_len, const uint8_t* scales, int64_t scales_len, const float* gs,
+                              int64_t gs_len, int64_t N, void* y, nvfp4_route route, void* stream);
+
+/* Smallest M routed to the tensor-core path for this shape and dtype. The
+ * environment variable NVFP4_QMM_CROSSOVER overrides it. */
+int64_t nvfp4_qmm_crossover(nvfp4_dtype x_dtype, int64_t N, int64_t K);
+
+/*
+ * GatherQMM (PR #2629, Summary; Changes during review):
+ *   y[r] = x[lhs[r]] @ dequantize(w[rhs[r]]).T * gs[rhs[r]] / 2688
+ *   x [B, K] of x_dtype; lhs_indices uint32 [R] or NULL (row r uses x[r]);
+ *   rhs_indices uint32 [R]; w [E, N, K/8]; scales [E, N, K/16];
+ *   gs NULL (gs_len 0) or [E] (gs_len E); y [R, N] of x_dtype.
+ * A row whose expert index is >= E, or whose activation index is >= B, is
+ * written as exact +0.0 (no read outside x or w). `sorted_indices` != 0
+ * promises rows grouped by expert (a sorted MoE prefill) and enables the
+ * expert-batched path; results do not depend on it.
+ */
+nvfp4_status nvfp4_gather_qmm(const void* x, nvfp4_dtype x_dtype, int64_t B, int64_t K, const uint32_t* lhs_indices,
+                              const uint32_t* rhs_indices, int64_t R, int sorted_indices, const uint32_t* w,
+                              int64_t w_len, const uint8_t* scales, int64_t scales_len, const float* gs,
+                              int64_t gs_len, int64_t E, int64_t N, void* y, void* stream);
+
+/* Message for the calling thread's last non-OK status ("" if none). */
+const char* nvfp4_last_error(void);
+
+/* Library version string. */
+const char* nvfp4_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NVFP4_H */

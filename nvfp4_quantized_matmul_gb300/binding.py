@@ -1,0 +1,165 @@
+"""ctypes binding over libnvfp4.so: argument marshalling only.
+
+Every function here checks that the tensors live on the GPU, passes their
+device pointers, element counts and the current CUDA stream to the C ABI
+(``include/nvfp4.h``) and raises ``Nvfp4Error`` with the library's message on
+a non-OK status. All arithmetic runs in the library's CUDA kernels; there is
+no CPU fallback. If the library has not been built the import fails.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libnvfp4.so")
+
+STATUS = ("OK", "ERR_NULL", "ERR_SHAPE", "ERR_PLANE", "ERR_DTYPE", "ERR_ALIGN", "ERR_GSCALE",
+          "ERR_LIMIT", "ERR_CUDA")
+DTYPE_CODE = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}
+ROUTE_CODE = {"auto": 0, "qmv": 1, "tc": 2}
+
+_P = ctypes.c_void_p
+_I64 = ctypes.c_int64
+_INT = ctypes.c_int
+
+# name -> (restype, argtypes); mirrors include/nvfp4.h
+SIGNATURES = {
+    "nvfp4_transcode": (_INT, [_P, _I64, _P, _I64, _P, _I64, _I64, _P, _P, _P, _P]),
+    "nvfp4_dequantize": (_INT, [_P, _I64, _P, _I64, _P, _I64, _I64, _I64, _I64, _INT, _P, _P]),
+    "nvfp4_qmm": (_INT, [_P, _INT, _I64, _I64, _P, _I64, _P, _I64, _P, _I64, _I64, _P, _P]),
+    "nvfp4_qmm_routed": (_INT, [_P, _INT, _I64, _I64, _P, _I64, _P, _I64, _P, _I64, _I64, _P, _INT, _P]),
+    "nvfp4_qmm_crossover": (_I64, [_INT, _I64, _I64]),
+    "nvfp4_gather_qmm": (_INT, [_P, _INT, _I64, _I64, _P, _P, _I64, _INT, _P, _I64, _P, _I64, _P, _I64,
+                                _I64, _I64, _P, _P]),
+    "nvfp4_last_error": (ctypes.c_char_p, []),
+    "nvfp4_version": (ctypes.c_char_p, []),
+}
+
+
+class Nvfp4Error(RuntimeError):
+    def __init__(self, status: int, message: str):
+        name = STATUS[status] if 0 <= status < len(STATUS) else str(status)
+        super().__init__(f"NVFP4_{name}: {message}")
+        self.status = status
+        self.name = name
+
+
+def _load():
+    if not os.path.exists(_LIB_PATH):
+        raise ImportError(f"{_LIB_PATH} is missing: build it with `python -c 'import __graft_entry__ as g; g.build()'`")
+    lib = ctypes.CDLL(_LIB_PATH)
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    return lib
+
+
+_lib = _load()
+
+
+def library():
+    """The loaded ctypes library (for direct C-ABI calls)."""
+    return _lib
+
+
+def check(status: int) -> None:
+    if status != 0:
+        raise Nvfp4Error(status, _lib.nvfp4_last_error().decode())
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _n(t):
+    return 0 if t is None else t.numel()
+
+
+def _cuda(*ts):
+    for t in ts:
+        if t is not None:
+            if not t.is_cuda:
+                raise ValueError("nvfp4 ops take CUDA tensors (the library has no CPU path)")
+            if not t.is_contiguous():
+                raise ValueError("nvfp4 ops take contiguous tensors")
+
+
+def _stream(t):
+    return torch.cuda.current_stream(t.device).cuda_stream
+
+
+def _gs_tensor(gs, device):
+    if gs is None:
+        return None
+    if not torch.is_tensor(gs):
+        gs = torch.tensor([float(gs)], dtype=torch.float32, device=device)
+    if gs.dtype != torch.float32:
+        raise ValueError("gs must be float32")
+    return gs.reshape(-1)
+
+
+def transcode(mo_weight, mo_weight_scale, weight_scale_2, out=None):
+    """ModelOpt triplet -> (w uint32 [N,K/8] as int32 storage, scales uint8 [N,K/16], gs float32 [1])."""
+    _cuda(mo_weight, mo_weight_scale)
+    n, half_k = mo_weight.shape
+    k = half_k * 2
+    ws2 = _gs_tensor(weight_scale_2, mo_weight.device)
+    if out is None:
+        w = torch.empty((n, k // 8), dtype=torch.int32, device=mo_weight.device)
+        s = torch.empty((n, k // 16), dtype=torch.uint8, device=mo_weight.device)
+        gs = torch.empty((1,), dtype=torch.float32, device=mo_weight.device)
+    else:
+        w, s, gs = out
+    check(_lib.nvfp4_transcode(_ptr(mo_weight), mo_weight.numel(), _ptr(mo_weight_scale), mo_weight_scale.numel(),
+                               _ptr(ws2), n, k, _ptr(w), _ptr(s), _ptr(gs), _stream(mo_weight)))
+    return w, s, gs
+
+
+def dequantize(w, scales, gs=None, out_dtype=torch.bfloat16, out=None):
+    """Exact dequantize of ``w`` [E?, N, K/8] -> [E?, N, K] of ``out_dtype``."""
+    _cuda(w, scales)
+    lead = tuple(w.shape[:-1])
+    k = w.shape[-1] * 8
+    e = lead[0] if len(lead) == 2 else 1
+    n = lead[-1]
+    gs = _gs_tensor(gs, w.device)
+    if out is None:
+        out = torch.empty((*lead, k), dtype=out_dtype, device=w.device)
+    check(_lib.nvfp4_dequantize(_ptr(w), w.numel(), _ptr(scales), scales.numel(), _ptr(gs), _n(gs), e, n, k,
+                                DTYPE_CODE[out.dtype], _ptr(out), _stream(w)))
+    return out
+
+
+def qmm(x, w, scales, gs=None, route="auto", out=None):
+    """QuantizedMatmul: ``x`` [M, K] @ dequantize(w [N, K/8]).T -> [M, N] in x's dtype."""
+    _cuda(x, w, scales)
+    m, k = x.shape
+    n = w.shape[0]
+    gs = _gs_tensor(gs, x.device)
+    if out is None:
+        out = torch.empty((m, n), dtype=x.dtype, device=x.device)
+    check(_lib.nvfp4_qmm_routed(_ptr(x), DTYPE_CODE[x.dtype], m, k, _ptr(w), w.numel(), _ptr(scales),
+                                scales.numel(), _ptr(gs), _n(gs), n, _ptr(out), ROUTE_CODE[route], _stream(x)))
+    return out
+
+
+def gather_qmm(x, w, scales, rhs, lhs=None, gs=None, sorted_indices=False, out=None):
+    """GatherQMM: row r = x[lhs[r]] @ dequantize(w[rhs[r]]).T * gs[rhs[r]]/2688 (zero row if out of range)."""
+    _cuda(x, w, scales, rhs, lhs)
+    b, k = x.shape
+    e, n = w.shape[0], w.shape[1]
+    r = rhs.numel()
+    gs = _gs_tensor(gs, x.device)
+    if out is None:
+        out = torch.empty((r, n), dtype=x.dtype, device=x.device)
+    check(_lib.nvfp4_gather_qmm(_ptr(x), DTYPE_CODE[x.dtype], b, k, _ptr(lhs), _ptr(rhs), r, int(bool(sorted_indices)),
+                                _ptr(w), w.numel(), _ptr(scales), scales.numel(), _ptr(gs), _n(gs), e, n,
+                                _ptr(out), _stream(x)))
+    return out
+
+
+def qmm_crossover(dtype, n, k):
+    return int(_lib.nvfp4_qmm_crossover(DTYPE_CODE[dtype], n, k))

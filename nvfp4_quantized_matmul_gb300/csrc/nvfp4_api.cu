@@ -1,0 +1,240 @@
+// C-ABI layer of libnvfp4.so: argument validation, route selection, launch.
+//
+// Validation follows the refusals on the pages (mlxcel PR #2629 "ROCm native
+// NVFP4", Summary and Changes during review): a scale plane must hold exactly
+// w.shape[:-1] + [w.shape[-1] / 2] bytes, K must be a multiple of 16, a
+// global scale must have one entry per expert, an unexpected global-scale
+// input is refused rather than ignored, launch limits are refused with a
+// clear error, and empty outputs return before any launch.
+#include <cinttypes>
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <string>
+
+#include "../../include/nvfp4.h"
+#include "nvfp4_internal.h"
+
+namespace {
+
+thread_local std::string g_last_error;
+
+nvfp4_status fail(nvfp4_status s, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return s;
+}
+
+nvfp4_status ok() {
+  g_last_error.clear();
+  return NVFP4_OK;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// a * b without signed overflow, for non-negative operands.
+bool mul_ok(int64_t a, int64_t b, int64_t* out) {
+  if (a < 0 || b < 0) return false;
+  if (a != 0 && b > INT64_MAX / a) return false;
+  *out = a * b;
+  return true;
+}
+
+int dtype_size(nvfp4_dtype d) { return d == NVFP4_F32 ? 4 : 2; }
+bool dtype_ok(nvfp4_dtype d) { return d == NVFP4_F32 || d == NVFP4_F16 || d == NVFP4_BF16; }
+
+// Shared checks for a weight plane [E, N, K/8] with scales [E, N, K/16].
+nvfp4_status check_planes(const char* fn, const uint32_t* w, int64_t w_len, const uint8_t* scales,
+                          int64_t scales_len, int64_t E, int64_t N, int64_t K) {
+  if (E < 0 || N < 0 || K < 0) return fail(NVFP4_ERR_SHAPE, "%s: negative size (E=%" PRId64 ", N=%" PRId64 ", K=%" PRId64 ")", fn, E, N, K);
+  if (K % 16) return fail(NVFP4_ERR_SHAPE, "%s: K=%" PRId64 " is not a multiple of 16", fn, K);
+  int64_t en, words, groups, elems;
+  if (!mul_ok(E, N, &en) || !mul_ok(en, K, &elems) || !mul_ok(elems, 4, &elems))
+    return fail(NVFP4_ERR_SHAPE, "%s: E*N*K overflows", fn);
+  words = en * (K / 8);
+  groups = en * (K / 16);
+  if (w_len != words)
+    return fail(NVFP4_ERR_PLANE, "%s: weight plane has %" PRId64 " words, expected E*N*K/8 = %" PRId64, fn, w_len, words);
+  if (scales_len != groups)
+    return fail(NVFP4_ERR_PLANE,
+                "%s: scale plane has %" PRId64 " bytes, expected E*N*K/16 = %" PRId64
+                " (scales.shape must be w.shape[:-1] + [w.shape[-1]/2])",
+                fn, scales_len, groups);
+  if (words > 0 && (!w || !scales)) return fail(NVFP4_ERR_NULL, "%s: weight or scale plane is NULL", fn);
+  if (!aligned(w, 16) || !aligned(scales, 16)) return fail(NVFP4_ERR_ALIGN, "%s: weight/scale planes must be 16-byte aligned", fn);
+  return NVFP4_OK;
+}
+
+nvfp4_status check_gs(const char* fn, const float* gs, int64_t gs_len, int64_t expect) {
+  if (!gs) {
+    if (gs_len != 0) return fail(NVFP4_ERR_GSCALE, "%s: gs is NULL but gs_len=%" PRId64, fn, gs_len);
+    return NVFP4_OK;
+  }
+  if (gs_len != expect)
+    return fail(NVFP4_ERR_GSCALE, "%s: gs has %" PRId64 " entries, expected %" PRId64, fn, gs_len, expect);
+  if (!aligned(gs, 4)) return fail(NVFP4_ERR_ALIGN, "%s: gs must be 4-byte aligned", fn);
+  return NVFP4_OK;
+}
+
+nvfp4_status cuda_status(const char* fn, cudaError_t e) {
+  if (e != cudaSuccess) return fail(NVFP4_ERR_CUDA, "%s: CUDA error %s (%s)", fn, cudaGetErrorName(e), cudaGetErrorString(e));
+  return ok();
+}
+
+constexpr int64_t kMaxGridX = 0x7FFFFFFF;
+constexpr int64_t kMaxGridY = 65535;
+
+nvfp4_status check_qmv_grid(const char* fn, int64_t R, int64_t N) {
+  if ((N + 15) / 16 > kMaxGridX || (R + 7) / 8 > kMaxGridY * 64)
+    return fail(NVFP4_ERR_LIMIT, "%s: R=%" PRId64 ", N=%" PRId64 " exceed the launch limits", fn, R, N);
+  return NVFP4_OK;
+}
+
+// Launch the decode-shape kernel in row blocks so grid.y stays within 65535.
+cudaError_t run_qmv(nvfp4::QmvArgs a, int xdt, cudaStream_t st) {
+  const int64_t chunk = kMaxGridY * 8;  // rows per launch: a multiple of every row tile
+  const int64_t R = a.R;
+  if (R <= chunk) return nvfp4::launch_qmv(a, xdt, st);
+  const int64_t xsz = xdt == NVFP4_F32 ? 4 : 2;
+  for (int64_t r = 0; r < R; r += chunk) {
+    nvfp4::QmvArgs b = a;
+    b.R = R - r < chunk ? R - r : chunk;
+    b.y = static_cast<char*>(a.y) + r * a.N * xsz;
+    if (a.lhs) b.lhs = a.lhs + r;
+    if (a.rhs) b.rhs = a.rhs + r;
+    if (!a.lhs) {  // identity activation rows: shift x instead
+      b.x = static_cast<const char*>(a.x) + r * a.K * xsz;
+      b.B = a.B - r;
+    }
+    cudaError_t e = nvfp4::launch_qmv(b, xdt, st);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+int64_t env_crossover() {
+  const char* s = std::getenv("NVFP4_QMM_CROSSOVER");
+  if (!s || !*s) return -1;
+  char* end = nullptr;
+  const long long v = std::strtoll(s, &end, 10);
+  return (end && *end == 0 && v >= 0) ? (int64_t)v : -1;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* nvfp4_last_error(void) { return g_last_error.c_str(); }
+
+const char* nvfp4_version(void) { return "nvfp4-gb300 0.1 (sm_103a)"; }
+
+nvfp4_status nvfp4_transcode(const uint8_t* mo_weight, int64_t mo_weight_len, const uint8_t* mo_weight_scale,
+                             int64_t mo_weight_scale_len, const float* weight_scale_2, int64_t N, int64_t K,
+                             uint32_t* w_out, uint8_t* scales_out, float* gs_out, void* stream) {
+  const char* fn = "nvfp4_transcode";
+  if (N < 0 || K < 0) return fail(NVFP4_ERR_SHAPE, "%s: negative size", fn);
+  if (K % 16) return fail(NVFP4_ERR_SHAPE, "%s: K=%" PRId64 " is not a multiple of 16", fn, K);
+  int64_t wb, sb;
+  if (!mul_ok(N, K / 2, &wb) || !mul_ok(N, K / 16, &sb)) return fail(NVFP4_ERR_SHAPE, "%s: N*K overflows", fn);
+  if (mo_weight_len != wb)
+    return fail(NVFP4_ERR_PLANE, "%s: weight has %" PRId64 " bytes, expected N*K/2 = %" PRId64, fn, mo_weight_len, wb);
+  if (mo_weight_scale_len != sb)
+    return fail(NVFP4_ERR_PLANE, "%s: weight_scale has %" PRId64 " bytes, expected N*K/16 = %" PRId64, fn,
+                mo_weight_scale_len, sb);
+  if (!weight_scale_2 || !gs_out) return fail(NVFP4_ERR_NULL, "%s: weight_scale_2 and gs_out are required", fn);
+  if (wb > 0 && (!mo_weight || !mo_weight_scale || !w_out || !scales_out))
+    return fail(NVFP4_ERR_NULL, "%s: a plane pointer is NULL", fn);
+  if (!aligned(mo_weight, 16) || !aligned(mo_weight_scale, 16) || !aligned(w_out, 16) || !aligned(scales_out, 16) ||
+      !aligned(weight_scale_2, 4) || !aligned(gs_out, 4))
+    return fail(NVFP4_ERR_ALIGN, "%s: planes must be 16-byte aligned, scalars 4-byte", fn);
+  return cuda_status(fn, nvfp4::launch_transcode(mo_weight, wb, mo_weight_scale, sb, weight_scale_2, w_out,
+                                                 scales_out, gs_out, static_cast<cudaStream_t>(stream)));
+}
+
+nvfp4_status nvfp4_dequantize(const uint32_t* w, int64_t w_len, const uint8_t* scales, int64_t scales_len,
+                              const float* gs, int64_t gs_len, int64_t E, int64_t N, int64_t K,
+                              nvfp4_dtype out_dtype, void* out, void* stream) {
+  const char* fn = "nvfp4_dequantize";
+  if (!dtype_ok(out_dtype)) return fail(NVFP4_ERR_DTYPE, "%s: unknown output dtype %d", fn, (int)out_dtype);
+  nvfp4_status s = check_planes(fn, w, w_len, scales, scales_len, E, N, K);
+  if (s) return s;
+  if ((s = check_gs(fn, gs, gs_len, E))) return s;
+  if (w_len == 0) return ok();
+  if (!out) return fail(NVFP4_ERR_NULL, "%s: out is NULL", fn);
+  if (!aligned(out, 16)) return fail(NVFP4_ERR_ALIGN, "%s: out must be 16-byte aligned", fn);
+  return cuda_status(fn, nvfp4::launch_dequantize(w, scales, gs, E, N, K, (int)out_dtype, out,
+                                                  static_cast<cudaStream_t>(stream)));
+}
+
+int64_t nvfp4_qmm_crossover(nvfp4_dtype x_dtype, int64_t N, int64_t K) {
+  (void)N;
+  (void)K;
+  const int64_t env = env_crossover();
+  if (env >= 0) return env;
+  if (x_dtype == NVFP4_F32) return INT64_MAX;  // f32 activations stay on the exact SIMT path
+  return INT64_MAX;  // no tensor-core route built yet
+}
+
+nvfp4_status nvfp4_qmm_routed(const void* x, nvfp4_dtype x_dtype, int64_t M, int64_t K, const uint32_t* w,
+                              int64_t w_len, const uint8_t* scales, int64_t scales_len, const float* gs,
+                              int64_t gs_len, int64_t N, void* y, nvfp4_route route, void* stream) {
+  const char* fn = "nvfp4_qmm";
+  if (!dtype_ok(x_dtype)) return fail(NVFP4_ERR_DTYPE, "%s: unknown activation dtype %d", fn, (int)x_dtype);
+  if (route != NVFP4_ROUTE_AUTO && route != NVFP4_ROUTE_QMV && route != NVFP4_ROUTE_TC)
+    return fail(NVFP4_ERR_DTYPE, "%s: unknown route %d", fn, (int)route);
+  if (M < 0) return fail(NVFP4_ERR_SHAPE, "%s: negative M", fn);
+  nvfp4_status s = check_planes(fn, w, w_len, scales, scales_len, 1, N, K);
+  if (s) return s;
+  if ((s = check_gs(fn, gs, gs_len, 1))) return s;
+  int64_t xe;
+  if (!mul_ok(M, K, &xe) || !mul_ok(M, N, &xe)) return fail(NVFP4_ERR_SHAPE, "%s: M*K or M*N overflows", fn);
+  if (M == 0 || N == 0) return ok();
+  if (!y || (K > 0 && !x)) return fail(NVFP4_ERR_NULL, "%s: x or y is NULL", fn);
+  if (!aligned(x, 16) || !aligned(y, 16)) return fail(NVFP4_ERR_ALIGN, "%s: x and y must be 16-byte aligned", fn);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (K == 0) return cuda_status(fn, cudaMemsetAsync(y, 0, (size_t)(M * N * dtype_size(x_dtype)), st));
+  if (route == NVFP4_ROUTE_TC && x_dtype == NVFP4_F32)
+    return fail(NVFP4_ERR_DTYPE, "%s: the tensor-core route takes f16 or bf16 activations", fn);
+  if ((s = check_qmv_grid(fn, M, N))) return s;
+  nvfp4::QmvArgs a{x, w, scales, gs, nullptr, nullptr, M, M, K, N, 1, y};
+  return cuda_status(fn, run_qmv(a, (int)x_dtype, st));
+}
+
+nvfp4_status nvfp4_qmm(const void* x, nvfp4_dtype x_dtype, int64_t M, int64_t K, const uint32_t* w,
+                       int64_t w_len, const uint8_t* scales, int64_t scales_len, const float* gs,
+                       int64_t gs_len, int64_t N, void* y, void* stream) {
+  return nvfp4_qmm_routed(x, x_dtype, M, K, w, w_len, scales, scales_len, gs, gs_len, N, y, NVFP4_ROUTE_AUTO,
+                          stream);
+}
+
+nvfp4_status nvfp4_gather_qmm(const void* x, nvfp4_dtype x_dtype, int64_t B, int64_t K, const uint32_t* lhs_indices,
+                              const uint32_t* rhs_indices, int64_t R, int sorted_indices, const uint32_t* w,
+                              int64_t w_len, const uint8_t* scales, int64_t scales_len, const float* gs,
+                              int64_t gs_len, int64_t E, int64_t N, void* y, void* stream) {
+  const char* fn = "nvfp4_gather_qmm";
+  (void)sorted_indices;
+  if (!dtype_ok(x_dtype)) return fail(NVFP4_ERR_DTYPE, "%s: unknown activation dtype %d", fn, (int)x_dtype);
+  if (B < 0 || R < 0) return fail(NVFP4_ERR_SHAPE, "%s: negative B or R", fn);
+  nvfp4_status s = check_planes(fn, w, w_len, scales, scales_len, E, N, K);
+  if (s) return s;
+  if ((s = check_gs(fn, gs, gs_len, E))) return s;
+  int64_t xe;
+  if (!mul_ok(B, K, &xe) || !mul_ok(R, N, &xe)) return fail(NVFP4_ERR_SHAPE, "%s: B*K or R*N overflows", fn);
+  if (R == 0 || N == 0) return ok();
+  if (!y || !rhs_indices) return fail(NVFP4_ERR_NULL, "%s: y and rhs_indices are required", fn);
+  if (B > 0 && K > 0 && !x) return fail(NVFP4_ERR_NULL, "%s: x is NULL", fn);
+  if (!aligned(x, 16) || !aligned(y, 16)) return fail(NVFP4_ERR_ALIGN, "%s: x and y must be 16-byte aligned", fn);
+  if (!aligned(rhs_indices, 4) || !aligned(lhs_indices, 4))
+    return fail(NVFP4_ERR_ALIGN, "%s: index arrays must be 4-byte aligned", fn);
+  if ((s = check_qmv_grid(fn, R, N))) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (K == 0) return cuda_status(fn, cudaMemsetAsync(y, 0, (size_t)(R * N * dtype_size(x_dtype)), st));
+  nvfp4::QmvArgs a{x, w, scales, gs, lhs_indices, rhs_indices, B, R, K, N, E, y};
+  return cuda_status(fn, run_qmv(a, (int)x_dtype, st));
+}
+
+}  // extern "C"

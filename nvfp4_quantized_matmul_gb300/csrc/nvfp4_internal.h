@@ -1,0 +1,33 @@
+// Internal launchers shared between the C-ABI layer and the kernel files.
+// Arguments are already validated by the caller (nvfp4_api.cu).
+#pragma once
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace nvfp4 {
+
+enum XType : int { kF32 = 0, kF16 = 1, kBF16 = 2 };
+
+cudaError_t launch_transcode(const uint8_t* mo_w, int64_t w_bytes, const uint8_t* mo_ws, int64_t s_bytes,
+                             const float* ws2, uint32_t* w_out, uint8_t* s_out, float* gs_out,
+                             cudaStream_t st);
+
+cudaError_t launch_dequantize(const uint32_t* w, const uint8_t* scales, const float* gs, int64_t E,
+                              int64_t N, int64_t K, int out_dtype, void* out, cudaStream_t st);
+
+// Decode-shape product on the SIMT/mma.sync path. Row r of the output uses
+// activation row lhs[r] (r when lhs is null) and expert rhs[r] (0 when rhs is
+// null); rows whose expert is >= E or whose activation row is >= B are zero.
+struct QmvArgs {
+  const void* x;          // [B, K], dtype xdt
+  const uint32_t* w;      // [E, N, K/8]
+  const uint8_t* scales;  // [E, N, K/16]
+  const float* gs;        // null or [E]
+  const uint32_t* lhs;    // null or [R]
+  const uint32_t* rhs;    // null or [R]
+  int64_t B, R, K, N, E;
+  void* y;                // [R, N], dtype xdt
+};
+cudaError_t launch_qmv(const QmvArgs& a, int xdt, cudaStream_t st);
+
+}  // namespace nvfp4

@@ -1,0 +1,183 @@
+// Bandwidth-bound kernels: ModelOpt-triplet transcode and exact dequantize.
+#include "nvfp4_common.cuh"
+#include "nvfp4_internal.h"
+
+namespace nvfp4 {
+namespace {
+
+constexpr int kStreamThreads = 256;
+
+int stream_grid(int64_t units) {
+  int dev = 0, sms = 152;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int64_t want = (units + kStreamThreads - 1) / kStreamThreads;
+  const int64_t cap = (int64_t)sms * 8;  // 8 resident 256-thread blocks per SM
+  return (int)(want < cap ? (want < 1 ? 1 : want) : cap);
+}
+
+// Transcode (issue #693 "direct-transcode ModelOpt triplets to MLX native",
+// Implementation plan step 3). ModelOpt's U8 plane stores column 2j in the
+// low nibble of byte j; packing four consecutive bytes little-endian into one
+// uint32 therefore yields the native word with column 8i+k in nibble k. That
+// repack is the identity on the byte stream, so the kernel is a 16-byte
+// vectorised copy of both planes; the E4M3 block scales are kept byte for
+// byte and the sidecar is f32(ws2) * 2688 so that gs / 2688 stands for ws2.
+// Both planes are read and written exactly once; no dense intermediate.
+__global__ void __launch_bounds__(kStreamThreads)
+transcode_kernel(const uint8_t* __restrict__ mo_w, int64_t w_bytes, const uint8_t* __restrict__ mo_ws,
+                 int64_t s_bytes, const float* __restrict__ ws2, uint8_t* __restrict__ w_out,
+                 uint8_t* __restrict__ s_out, float* __restrict__ gs_out) {
+  const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  if (tid == 0) gs_out[0] = __fmul_rn(__ldg(ws2), kGlobalScaleDivisor);
+  const int64_t wv = w_bytes >> 4, sv = s_bytes >> 4;
+  // Main body: 16-byte chunks of the weight plane then the scale plane;
+  // four independent loads in flight per thread.
+  const uint4* wi = reinterpret_cast<const uint4*>(mo_w);
+  uint4* wo = reinterpret_cast<uint4*>(w_out);
+  int64_t i = tid;
+  for (; i + 3 * stride < wv; i += 4 * stride) {
+    const uint4 a = ld_stream_v4(wi + i), b = ld_stream_v4(wi + i + stride);
+    const uint4 c = ld_stream_v4(wi + i + 2 * stride), d = ld_stream_v4(wi + i + 3 * stride);
+    __stcs(wo + i, a);
+    __stcs(wo + i + stride, b);
+    __stcs(wo + i + 2 * stride, c);
+    __stcs(wo + i + 3 * stride, d);
+  }
+  for (; i < wv; i += stride) __stcs(wo + i, ld_stream_v4(wi + i));
+  const uint4* si = reinterpret_cast<const uint4*>(mo_ws);
+  uint4* so = reinterpret_cast<uint4*>(s_out);
+  for (int64_t j = tid; j < sv; j += stride) __stcs(so + j, ld_stream_v4(si + j));
+  // Byte tails (fewer than 16 bytes each).
+  const int64_t wt = w_bytes - (wv << 4), st = s_bytes - (sv << 4);
+  if (tid < wt) w_out[(wv << 4) + tid] = mo_w[(wv << 4) + tid];
+  if (tid < st) s_out[(sv << 4) + tid] = mo_ws[(sv << 4) + tid];
+}
+
+// Exact dequantize (PR #2629 "ROCm native NVFP4", Summary: the dequantize
+// kernel expands a plane exactly; Changes during review: the grid is sized
+// from the weight plane). One thread-iteration expands one 16-column block:
+// two packed words and one scale byte in, sixteen outputs out. Element value
+// = cast(f32(fp4 * e4m3) * factor) with factor = gs[e] / 2688 (absent gs:
+// the product itself, exact in every output type).
+template <typename OutT>
+__device__ __forceinline__ void store16(OutT* dst, const uint32_t (&h)[8], float fac, bool has_gs);
+
+__device__ __forceinline__ float h_lo(uint32_t v) { return __half2float(__ushort_as_half((unsigned short)(v & 0xFFFF))); }
+__device__ __forceinline__ float h_hi(uint32_t v) { return __half2float(__ushort_as_half((unsigned short)(v >> 16))); }
+
+template <>
+__device__ __forceinline__ void store16<float>(float* dst, const uint32_t (&h)[8], float fac, bool has_gs) {
+  float v[16];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    v[2 * i] = h_lo(h[i]);
+    v[2 * i + 1] = h_hi(h[i]);
+  }
+  if (has_gs) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __fmul_rn(v[i], fac);
+  }
+  uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int q = 0; q < 4; ++q)
+    __stcs(d + q, make_uint4(__float_as_uint(v[4 * q]), __float_as_uint(v[4 * q + 1]),
+                             __float_as_uint(v[4 * q + 2]), __float_as_uint(v[4 * q + 3])));
+}
+
+template <>
+__device__ __forceinline__ void store16<__half>(__half* dst, const uint32_t (&h)[8], float fac, bool has_gs) {
+  uint32_t o[8];
+  if (!has_gs) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) o[i] = h[i];
+  } else {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const __half lo = __float2half_rn(__fmul_rn(h_lo(h[i]), fac));
+      const __half hi = __float2half_rn(__fmul_rn(h_hi(h[i]), fac));
+      o[i] = (uint32_t)__half_as_ushort(lo) | ((uint32_t)__half_as_ushort(hi) << 16);
+    }
+  }
+  uint4* d = reinterpret_cast<uint4*>(dst);
+  __stcs(d, make_uint4(o[0], o[1], o[2], o[3]));
+  __stcs(d + 1, make_uint4(o[4], o[5], o[6], o[7]));
+}
+
+template <>
+__device__ __forceinline__ void store16<__nv_bfloat16>(__nv_bfloat16* dst, const uint32_t (&h)[8], float fac,
+                                                       bool has_gs) {
+  uint32_t o[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    float a = h_lo(h[i]), b = h_hi(h[i]);
+    if (has_gs) {
+      a = __fmul_rn(a, fac);
+      b = __fmul_rn(b, fac);
+    }
+    o[i] = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(a)) |
+           ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(b)) << 16);
+  }
+  uint4* d = reinterpret_cast<uint4*>(dst);
+  __stcs(d, make_uint4(o[0], o[1], o[2], o[3]));
+  __stcs(d + 1, make_uint4(o[4], o[5], o[6], o[7]));
+}
+
+template <typename OutT>
+__global__ void __launch_bounds__(kStreamThreads)
+dequantize_kernel(const uint32_t* __restrict__ w, const uint8_t* __restrict__ scales,
+                  const float* __restrict__ gs, int64_t E, int64_t groups_per_expert,
+                  OutT* __restrict__ out) {
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t e = blockIdx.y; e < E; e += gridDim.y) {
+    const float fac = global_factor(gs, e);
+    const bool has_gs = gs != nullptr;
+    const int64_t base = e * groups_per_expert;
+    for (int64_t gi = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; gi < groups_per_expert; gi += stride) {
+      const int64_t g = base + gi;
+      const uint2 ww = ld_stream_v2(w + 2 * g);
+      const uint32_t sc = e4m3_to_f16x2_bcast(__ldcs(scales + g));
+      uint32_t h[8];
+      decode8_scaled_f16(ww.x, sc, *reinterpret_cast<uint32_t(*)[4]>(&h[0]));
+      decode8_scaled_f16(ww.y, sc, *reinterpret_cast<uint32_t(*)[4]>(&h[4]));
+      store16<OutT>(out + 16 * g, h, fac, has_gs);
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_transcode(const uint8_t* mo_w, int64_t w_bytes, const uint8_t* mo_ws, int64_t s_bytes,
+                             const float* ws2, uint32_t* w_out, uint8_t* s_out, float* gs_out,
+                             cudaStream_t st) {
+  const int64_t units = (w_bytes >> 4) / 4 + 16;
+  transcode_kernel<<<stream_grid(units), kStreamThreads, 0, st>>>(
+      mo_w, w_bytes, mo_ws, s_bytes, ws2, reinterpret_cast<uint8_t*>(w_out), s_out, gs_out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dequantize(const uint32_t* w, const uint8_t* scales, const float* gs, int64_t E,
+                              int64_t N, int64_t K, int out_dtype, void* out, cudaStream_t st) {
+  const int64_t gpe = N * (K / 16);
+  int gx = stream_grid(gpe * E);
+  const int64_t per_expert = (gpe + kStreamThreads - 1) / kStreamThreads;
+  if (gx > per_expert) gx = (int)(per_expert < 1 ? 1 : per_expert);
+  int gy = (int)(E < 65535 ? E : 65535);
+  const dim3 grid(gx, gy);
+  switch (out_dtype) {
+    case kF32:
+      dequantize_kernel<float><<<grid, kStreamThreads, 0, st>>>(w, scales, gs, E, gpe, (float*)out);
+      break;
+    case kF16:
+      dequantize_kernel<__half><<<grid, kStreamThreads, 0, st>>>(w, scales, gs, E, gpe, (__half*)out);
+      break;
+    default:
+      dequantize_kernel<__nv_bfloat16><<<grid, kStreamThreads, 0, st>>>(w, scales, gs, E, gpe,
+                                                                          (__nv_bfloat16*)out);
+      break;
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace nvfp4

@@ -1,0 +1,197 @@
+"""GPU parity: every route of libnvfp4.so against the CPU oracle.
+
+Bit-exact for transcode and dequantize; max|y - ref| / max|ref| within the
+per-dtype bound for the matmul routes (1e-5 f32, 1e-3 f16, 8e-3 bf16).
+"""
+import numpy as np
+import pytest
+import torch
+
+from oracle import nvfp4_oracle as O
+from nvfp4_quantized_matmul_gb300 import synth
+
+from nvutil import TOL, TORCH, f32_to_dev, guarded_empty, guards_intact, rel_err, u32_to_dev, u8_to_dev, weights
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def nv():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import __graft_entry__ as ge
+
+    ge.build()
+    import nvfp4_quantized_matmul_gb300 as pkg
+
+    return pkg
+
+
+def _bits(t: torch.Tensor) -> np.ndarray:
+    t = t.cpu()
+    if t.dtype == torch.float32:
+        return t.view(torch.int32).numpy()
+    return t.view(torch.int16).numpy()
+
+
+def _assert_bit_exact(got: torch.Tensor, ref: torch.Tensor):
+    g, r = got.cpu(), ref.cpu()
+    gn, rn = torch.isnan(g.float()), torch.isnan(r.float())
+    assert torch.equal(gn, rn), "NaN positions differ"
+    gb, rb = _bits(g), _bits(r)
+    keep = ~rn.numpy()
+    bad = np.nonzero((gb != rb) & keep)
+    assert bad[0].size == 0, f"{bad[0].size} elements differ, first at {tuple(b[0] for b in bad)}"
+
+
+# ------------------------------------------------------------------ dequantize
+
+@pytest.mark.parametrize("shape", [(1, 272, 256), (1, 1, 16), (3, 17, 48), (2, 64, 5376), (1, 5, 32)])
+@pytest.mark.parametrize("dt", ["f32", "f16", "bf16"])
+@pytest.mark.parametrize("with_gs", [False, True])
+def test_dequantize_bit_exact(nv, shape, dt, with_gs):
+    E, N, K = shape
+    w, s = weights(100 + N + K, E, N, K)
+    # exercise special scale bytes: NaN, signed zeros, negatives, subnormals, max
+    flat = s.reshape(-1)
+    specials = np.array([0x7F, 0xFF, 0x00, 0x80, 0x01, 0x81, 0x7E, 0xFE, 0x38, 0xB8], dtype=np.uint8)
+    flat[: min(flat.size, specials.size)] = specials[: flat.size]
+    gs = synth.global_scales(synth.rng(7), E) if with_gs else None
+    if E == 1:  # a single linear: [N, K/8] planes and a scalar global scale
+        w, s = w[0], s[0]
+        gs = None if gs is None else gs[0]
+    out = nv.dequantize(u32_to_dev(w), u8_to_dev(s), None if gs is None else f32_to_dev(gs), TORCH[dt])
+    torch.cuda.synchronize()
+    ref = O.dequantize(w, s, gs, dt)
+    _assert_bit_exact(out, ref)
+
+
+def test_dequantize_guard_bands(nv):
+    N, K = 33, 48
+    w, s = weights(5, N, K)
+    out, backing, guard = guarded_empty((N, K), torch.bfloat16)
+    nv.dequantize(u32_to_dev(w), u8_to_dev(s), None, torch.bfloat16, out=out)
+    torch.cuda.synchronize()
+    assert guards_intact(backing, guard)
+    _assert_bit_exact(out, O.dequantize(w, s, None, "bf16"))
+
+
+# ------------------------------------------------------------------ transcode
+
+@pytest.mark.parametrize("nk", [(3, 16), (272, 256), (33, 5376), (1, 48)])
+def test_transcode_bit_exact(nv, nk):
+    N, K = nk
+    g = synth.rng(N * 7 + K)
+    mo_w, mo_ws, ws2 = synth.modelopt_triplet(g, N, K)
+    w, s, gs = nv.transcode(u8_to_dev(mo_w), u8_to_dev(mo_ws), float(ws2))
+    rw, rs, rg = O.transcode(mo_w, mo_ws, ws2)
+    assert np.array_equal(w.cpu().numpy().view(np.uint32), rw)
+    assert np.array_equal(s.cpu().numpy(), rs)
+    assert gs.cpu().numpy().view(np.uint32)[0] == np.float32(rg).view(np.uint32)
+
+
+def test_transcode_then_dequantize_matches_modelopt(nv):
+    """Sidecar identity on the GPU: native dequantize of the transcoded planes
+    reproduces ModelOpt's fp4 * e4m3(weight_scale) * weight_scale_2."""
+    g = synth.rng(77)
+    N, K = 64, 256
+    mo_w, mo_ws, ws2 = synth.modelopt_triplet(g, N, K)
+    w, s, gs = nv.transcode(u8_to_dev(mo_w), u8_to_dev(mo_ws), float(ws2))
+    deq = nv.dequantize(w, s, gs, torch.float32).cpu().numpy().astype(np.float64)
+    ref = O.modelopt_values(mo_w, mo_ws, ws2)
+    ulp = np.spacing(np.abs(ref.astype(np.float32))).astype(np.float64)
+    assert np.all(np.abs(deq - ref) <= 2 * ulp)
+    rw, rs, rg = O.transcode(mo_w, mo_ws, ws2)
+    _assert_bit_exact(torch.from_numpy(deq.astype(np.float32)), O.dequantize(rw, rs, rg, "f32"))
+
+
+# ------------------------------------------------------------------ QuantizedMatmul
+
+QMM_SHAPES = [(512, 256), (272, 48), (1, 16), (17, 5376), (96, 1040)]
+
+
+@pytest.mark.parametrize("nk", QMM_SHAPES)
+@pytest.mark.parametrize("M", [1, 2, 3, 8, 9, 16, 33])
+@pytest.mark.parametrize("dt", ["f32", "f16", "bf16"])
+def test_qmm_qmv_route(nv, nk, M, dt):
+    N, K = nk
+    w, s = weights(N * 31 + K, N, K, lo=2.0**-4, hi=16.0)
+    g = synth.rng(M * 1000 + N + K)
+    x = synth.activations(g, (M, K), dt)
+    for gs in (None, np.float32(2688 * 0.01)):
+        y, backing, guard = guarded_empty((M, N), TORCH[dt], fill=-7.0)
+        nv.qmm(x.cuda(), u32_to_dev(w), u8_to_dev(s), gs=None if gs is None else float(gs), route="qmv", out=y)
+        torch.cuda.synchronize()
+        ref = O.qmm(x.double().numpy(), w, s, gs)
+        err = rel_err(y, ref)
+        assert err <= TOL[dt], f"rel-to-max error {err:.3g} > {TOL[dt]}"
+        assert guards_intact(backing, guard)
+
+
+def test_qmm_unit_scales_one_hot(nv):
+    """Unit scales and one-hot activations reproduce E2M1 table entries exactly."""
+    N, K = 16, 32
+    codes = (np.arange(N * K).reshape(N, K) % 16).astype(np.int64)
+    w = np.zeros((N, K // 8), dtype=np.uint32)
+    for i in range(8):
+        w |= (codes[:, i::8].astype(np.uint32) << (4 * i))
+    s = np.full((N, K // 16), 0x38, dtype=np.uint8)
+    x = torch.eye(K, dtype=torch.bfloat16)
+    y = nv.qmm(x.cuda(), u32_to_dev(w), u8_to_dev(s), route="qmv").float().cpu().numpy()
+    ref = O.qmm(x.double().numpy(), w, s)
+    assert np.array_equal(y, ref)
+
+
+def test_qmm_empty(nv):
+    w, s = weights(1, 32, 64)
+    y = nv.qmm(torch.zeros(0, 64, dtype=torch.bfloat16, device="cuda"), u32_to_dev(w), u8_to_dev(s))
+    assert y.shape == (0, 32)
+
+
+# ------------------------------------------------------------------ GatherQMM
+
+@pytest.mark.parametrize("dt", ["f32", "f16", "bf16"])
+@pytest.mark.parametrize("with_gs", [False, True])
+def test_gather_unsorted_decode_with_zero_rows(nv, dt, with_gs):
+    E, N, K, B = 8, 96, 256, 10
+    w, s = weights(9, E, N, K)
+    g = synth.rng(91)
+    gs = synth.global_scales(g, E) if with_gs else None
+    x = synth.activations(g, (B, K), dt)
+    rhs = np.concatenate([synth.zipf_experts(g, 20, E), np.array([E, E + 1, 2**31 - 1, 2**32 - 1, 3, 5], dtype=np.uint32)])
+    lhs = np.concatenate([g.integers(0, B, size=20).astype(np.uint32), np.array([0, 1, 2, 3, B, 2**32 - 1], dtype=np.uint32)])
+    y = nv.gather_qmm(x.cuda(), u32_to_dev(w), u8_to_dev(s), u32_to_dev(rhs), u32_to_dev(lhs),
+                      gs=None if gs is None else f32_to_dev(gs))
+    torch.cuda.synchronize()
+    ref = O.gather_qmm(x.double().numpy(), lhs, rhs, w, s, gs)
+    yc = y.float().cpu().numpy()
+    for r in range(20, 26):
+        assert np.all(yc[r] == 0.0) and not np.any(np.signbit(yc[r])), f"row {r} must be +0.0"
+    assert rel_err(y, ref) <= TOL[dt]
+
+
+@pytest.mark.parametrize("dt", ["f16", "bf16"])
+def test_gather_sorted_prefill(nv, dt):
+    E, N, K, T, topk = 16, 64, 512, 40, 4
+    w, s = weights(19, E, N, K)
+    g = synth.rng(191)
+    gs = synth.global_scales(g, E)
+    x = synth.activations(g, (T, K), dt)
+    lhs, rhs = synth.zipf_routing(g, T, E, topk)
+    y = nv.gather_qmm(x.cuda(), u32_to_dev(w), u8_to_dev(s), u32_to_dev(rhs), u32_to_dev(lhs), gs=f32_to_dev(gs),
+                      sorted_indices=True)
+    torch.cuda.synchronize()
+    ref = O.gather_qmm(x.double().numpy(), lhs, rhs, w, s, gs)
+    assert rel_err(y, ref) <= TOL[dt]
+
+
+def test_gather_identity_lhs(nv):
+    E, N, K = 4, 40, 64
+    w, s = weights(29, E, N, K)
+    g = synth.rng(292)
+    x = synth.activations(g, (6, K), "bf16")
+    rhs = np.array([3, 0, 0, 2, 9, 1], dtype=np.uint32)
+    y = nv.gather_qmm(x.cuda(), u32_to_dev(w), u8_to_dev(s), u32_to_dev(rhs))
+    ref = O.gather_qmm(x.double().numpy(), None, rhs, w, s)
+    assert rel_err(y, ref) <= TOL["bf16"]
+    assert np.all(y[4].float().cpu().numpy() == 0.0)

@@ -1,0 +1,138 @@
+"""Host-side tests of libnvfp4.so (no GPU): it loads, exports what the header
+declares, and refuses malformed calls before touching CUDA."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def nv():
+    import __graft_entry__ as ge
+
+    ge.build()
+    from nvfp4_quantized_matmul_gb300 import binding
+
+    return binding
+
+
+def declared_functions():
+    with open(os.path.join(ROOT, "include", "nvfp4.h")) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(nvfp4_\w+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(nv):
+    names = declared_functions()
+    assert "nvfp4_qmm" in names and "nvfp4_gather_qmm" in names
+    lib = nv.library()
+    for name in names:
+        assert hasattr(lib, name), name
+        assert name in nv.SIGNATURES, f"binding lacks {name}"
+
+
+def test_version(nv):
+    assert b"sm_103a" in nv.library().nvfp4_version()
+
+
+# Fake, never-dereferenced device addresses: validation rejects before launch.
+A = 0x10000  # 16-byte aligned
+U = 0x10004  # 4-byte aligned only
+
+
+def qmm_call(nv, **kw):
+    args = dict(x=A, xdt=2, M=4, K=256, w=A, w_len=512 * 32, s=A, s_len=512 * 16, gs=None, gs_len=0, N=512,
+                y=A, route=0)
+    args.update(kw)
+    lib = nv.library()
+    return lib.nvfp4_qmm_routed(args["x"], args["xdt"], args["M"], args["K"], args["w"], args["w_len"], args["s"],
+                                args["s_len"], args["gs"], args["gs_len"], args["N"], args["y"], args["route"], None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(K=24, w_len=512 * 3, s_len=512), "ERR_SHAPE"),          # K % 16 != 0
+    (dict(s_len=512 * 16 - 1), "ERR_PLANE"),                      # short scale plane
+    (dict(s_len=512 * 16 + 16), "ERR_PLANE"),                     # oversized scale plane
+    (dict(w_len=512 * 32 + 1), "ERR_PLANE"),
+    (dict(gs=A, gs_len=2), "ERR_GSCALE"),                         # qmm takes one global scale
+    (dict(gs=None, gs_len=1), "ERR_GSCALE"),                      # length without a pointer
+    (dict(xdt=7), "ERR_DTYPE"),
+    (dict(route=9), "ERR_DTYPE"),
+    (dict(x=U), "ERR_ALIGN"),
+    (dict(w=U), "ERR_ALIGN"),
+    (dict(y=None), "ERR_NULL"),
+    (dict(w=None), "ERR_NULL"),
+    (dict(M=-1), "ERR_SHAPE"),
+    (dict(N=-1, w_len=0, s_len=0), "ERR_SHAPE"),
+    (dict(N=2**62, w_len=0, s_len=0), "ERR_SHAPE"),               # overflow
+])
+def test_qmm_refusals(nv, kw, status):
+    st = qmm_call(nv, **kw)
+    assert nv.STATUS[st] == status, (st, nv.library().nvfp4_last_error())
+    assert nv.library().nvfp4_last_error()
+
+
+def test_empty_outputs_return_ok_without_launch(nv):
+    assert qmm_call(nv, M=0) == 0
+    assert qmm_call(nv, N=0, w_len=0, s_len=0) == 0
+    lib = nv.library()
+    st = lib.nvfp4_gather_qmm(A, 2, 4, 256, None, A, 0, 0, A, 3 * 64 * 32, A, 3 * 64 * 16, None, 0, 3, 64, A, None)
+    assert st == 0
+    st = lib.nvfp4_dequantize(A, 0, A, 0, None, 0, 1, 0, 256, 2, A, None)
+    assert st == 0
+
+
+def test_gather_refusals(nv):
+    lib = nv.library()
+    E, N, K = 3, 64, 256
+
+    def call(**kw):
+        a = dict(x=A, xdt=2, B=4, K=K, lhs=None, rhs=A, R=5, w=A, w_len=E * N * K // 8, s=A, s_len=E * N * K // 16,
+                 gs=None, gs_len=0, E=E, N=N, y=A)
+        a.update(kw)
+        return nv.STATUS[lib.nvfp4_gather_qmm(a["x"], a["xdt"], a["B"], a["K"], a["lhs"], a["rhs"], a["R"], 0, a["w"],
+                                              a["w_len"], a["s"], a["s_len"], a["gs"], a["gs_len"], a["E"], a["N"],
+                                              a["y"], None)]
+
+    assert call(gs=A, gs_len=E - 1) == "ERR_GSCALE"  # one global scale per expert
+    assert call(gs=A, gs_len=1) == "ERR_GSCALE"
+    assert call(s_len=E * N * K // 16 - N * K // 16) == "ERR_PLANE"  # missing expert in scales
+    assert call(rhs=None) == "ERR_NULL"
+    assert call(rhs=A + 2) == "ERR_ALIGN"
+    assert call(B=-1) == "ERR_SHAPE"
+
+
+def test_transcode_and_dequantize_refusals(nv):
+    lib = nv.library()
+    N, K = 8, 64
+    st = lib.nvfp4_transcode(A, N * K // 2 - 1, A, N * K // 16, A, N, K, A, A, A, None)
+    assert nv.STATUS[st] == "ERR_PLANE"
+    st = lib.nvfp4_transcode(A, N * K // 2, A, N * K // 16, None, N, K, A, A, A, None)
+    assert nv.STATUS[st] == "ERR_NULL"
+    st = lib.nvfp4_transcode(A, N * 8, A, N, A, N, 17, A, A, A, None)
+    assert nv.STATUS[st] == "ERR_SHAPE"
+    st = lib.nvfp4_dequantize(A, N * K // 8, A, N * K // 16 + 4, None, 0, 1, N, K, 0, A, None)
+    assert nv.STATUS[st] == "ERR_PLANE"
+    st = lib.nvfp4_dequantize(A, N * K // 8, A, N * K // 16, A, 2, 1, N, K, 0, A, None)
+    assert nv.STATUS[st] == "ERR_GSCALE"
+    st = lib.nvfp4_dequantize(A, N * K // 8, A, N * K // 16, None, 0, 1, N, K, 3, A, None)
+    assert nv.STATUS[st] == "ERR_DTYPE"
+
+
+def test_crossover_env_override(nv, monkeypatch):
+    monkeypatch.setenv("NVFP4_QMM_CROSSOVER", "96")
+    assert nv.library().nvfp4_qmm_crossover(2, 21504, 5376) == 96
+
+
+def test_binding_rejects_cpu_tensors(nv):
+    import torch
+
+    x = torch.zeros(2, 32, dtype=torch.bfloat16)
+    w = torch.zeros(4, 4, dtype=torch.int32)
+    s = torch.zeros(4, 2, dtype=torch.uint8)
+    with pytest.raises(ValueError):
+        nv.qmm(x, w, s)
