@@ -1,0 +1,546 @@
+"""Benchmark of the NVFP4 hot path on GB300; prints one JSON line.
+
+Step (the headline): one decode-layer pass of the decode-shape workload. For
+each token count M in {1, 2, 4, 8, 16}, bf16 activations x [M, K] go through
+the three NVFP4 linears of a 31B-class layer (fused gate/up [43008, 5376],
+down [5376, 21504], qkv [8192, 5376]), each with an E4M3/16 scale plane and a
+per-linear float32 global scale: 15 `nvfp4_qmm` calls (the public API, route
+chosen by the library: all of them are on the decode-shape qmv route).
+`value` is the algorithmic HBM traffic of those calls (9/16 byte per weight
+element + activations + outputs + one global scale) divided by the step time,
+in GB/s. Five rotating weight copies (1.1 GB per step) keep every call's
+weights out of L2.
+
+`routes` reports the other configurations measured the same way (prefill
+QuantizedMatmul TFLOP/s, MoE GatherQMM, transcode, dequantize) for context.
+
+`--impl reference` times the CPU oracle on a bounded sample instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+K_HIDDEN = 5376
+LINEARS = (("gate_up", 43008, 5376), ("down", 5376, 21504), ("qkv", 8192, 5376))
+DECODE_M = (1, 2, 4, 8, 16)
+ROTATE = 5
+WORKLOAD = ("decode-shape qmv: bf16 x [M in {1,2,4,8,16}, K] through NVFP4 gate/up [43008,5376], "
+            "down [5376,21504], qkv [8192,5376]; E4M3/16 scales log-uniform in [2^-6,2^2]; "
+            "per-linear f32 global scale in [0.5,2]*2688; bf16 out, f32 accumulate")
+METRIC = "qmv HBM GB/s & µs/call, qmm TFLOP/s; fraction of GB300 roofline (1 GPU)"
+
+# dram bytes per launch of the dominant kernel from one ncu capture, and the
+# digest of the kernel source it was taken on (stale -> reported as null).
+TRAFFIC = {"source": None, "kernel_sha": None, "bytes_per_step": None}
+
+
+def qmv_bytes(m, n, k):
+    return 0.5625 * n * k + 2 * m * k + 2 * m * n + 4
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d.get("hbm_gbs", 6800.0), d.get("bf16_tflops", 1900.0), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples during the timed region."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            p = [v.strip() for v in line.split(",")]
+            if len(p) < 9:
+                continue
+            try:
+                sm.append(float(p[1]))
+                mx.append(float(p[2]))
+            except ValueError:
+                continue
+            for name, v in zip(names, p[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def source_sha(name):
+    with open(os.path.join(ROOT, "nvfp4_quantized_matmul_gb300", "csrc", name), "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+# ----------------------------------------------------------------------------- our arm
+
+def build_decode(nv, synth, torch, dev, rank):
+    """Weights (ROTATE copies), activations and outputs for the decode step."""
+    g = synth.rng(1000 + rank)
+    lin = []
+    for name, n, k in LINEARS:
+        copies = []
+        for c in range(ROTATE):
+            w = torch.randint(-2**31, 2**31 - 1, (n, k // 8), dtype=torch.int32, device=dev,
+                              generator=torch.Generator(device=dev).manual_seed(17 * c + n))
+            s = torch.from_numpy(synth.log_uniform_scales(g, (n, k // 16), 2.0**-6, 4.0)).to(dev)
+            gs = torch.from_numpy(synth.global_scales(g, 1)).to(dev)
+            copies.append((w, s, gs))
+        lin.append((name, n, k, copies))
+    xs = {}
+    for m in DECODE_M:
+        for name, n, k, _ in lin:
+            xs[(m, name)] = synth.activations(g, (m, k), "bf16").to(dev)
+    ys = {(m, name): torch.empty((m, n), dtype=torch.bfloat16, device=dev) for m in DECODE_M for name, n, _, _ in lin}
+    return lin, xs, ys
+
+
+def decode_step_calls(nv, lin, xs, ys, copy_shift=0):
+    calls = []
+    for mi, m in enumerate(DECODE_M):
+        for name, n, k, copies in lin:
+            w, s, gs = copies[(mi + copy_shift) % ROTATE]
+            calls.append((m, n, k, xs[(m, name)], w, s, gs, ys[(m, name)]))
+    return calls
+
+
+def run_ours(args):
+    import torch
+
+    import nvfp4_quantized_matmul_gb300 as nv
+    from nvfp4_quantized_matmul_gb300 import synth
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    hbm_peak, bf16_peak, peak_kind = peaks()
+
+    lin, xs, ys = build_decode(nv, synth, torch, dev, rank)
+    step_bytes = sum(qmv_bytes(m, n, k) for m in DECODE_M for _, n, k, _ in lin)
+    launches_per_step = len(DECODE_M) * len(LINEARS)
+
+    # One CUDA graph per rotation phase: the 15 calls of a step, weights
+    # rotated so consecutive steps never touch the same copy.
+    stream = torch.cuda.Stream(device=dev)
+    graphs = []
+    with torch.cuda.stream(stream):
+        for shift in range(ROTATE):
+            for (m, n, k, x, w, s, gs, y) in decode_step_calls(nv, lin, xs, ys, shift):
+                nv.qmm(x, w, s, gs=gs, out=y)  # warm the path outside capture
+        torch.cuda.synchronize(dev)
+        for shift in range(ROTATE):
+            gph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gph, stream=stream):
+                for (m, n, k, x, w, s, gs, y) in decode_step_calls(nv, lin, xs, ys, shift):
+                    nv.qmm(x, w, s, gs=gs, out=y)
+            graphs.append(gph)
+    torch.cuda.synchronize(dev)
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            graphs[i % ROTATE].replay()
+    barrier()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        with torch.cuda.stream(stream):
+            ev0.record(stream)
+            for i in range(args.steps):
+                graphs[i % ROTATE].replay()
+            ev1.record(stream)
+        torch.cuda.synchronize(dev)
+    barrier()
+    ms_total = ev0.elapsed_time(ev1)
+    if dist is not None:
+        t = torch.tensor([ms_total], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_total = float(t.item())
+    ms_step = ms_total / args.steps
+    value = step_bytes * world / (ms_step * 1e-3) / 1e9
+
+    # Per-call latency (µs/call) per shape: each call timed alone on the
+    # stream, weights rotated, after the step measurement.
+    per_call = {}
+    with torch.cuda.stream(stream):
+        for mi, m in enumerate(DECODE_M):
+            for name, n, k, copies in lin:
+                evs = []
+                for rep in range(2 * ROTATE):
+                    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    w, s, gs = copies[rep % ROTATE]
+                    a.record(stream)
+                    nv.qmm(xs[(m, name)], w, s, gs=gs, out=ys[(m, name)])
+                    b.record(stream)
+                    evs.append((a, b))
+                torch.cuda.synchronize(dev)
+                us = statistics.median(a.elapsed_time(b) * 1e3 for a, b in evs[ROTATE:])
+                per_call[f"{name}_M{m}"] = {"us": round(us, 2),
+                                            "GBps": round(qmv_bytes(m, n, k) / (us * 1e-6) / 1e9, 1)}
+
+    # End to end through the public API: pinned host activations in, bf16
+    # outputs back to pinned host memory, every step.
+    e2e = run_e2e(nv, torch, dev, stream, lin, xs, ys, args, step_bytes)
+
+    routes = {} if args.no_routes else run_routes(nv, synth, torch, dev, stream, args)
+    kernel_sha = source_sha("nvfp4_qmv.cu")
+    traffic = TRAFFIC["bytes_per_step"] if TRAFFIC["kernel_sha"] == kernel_sha else None
+
+    if rank == 0:
+        cpu = run_cpu_baseline(args) if world == 1 and not args.no_cpu else None
+        achieved = step_bytes / (ms_step * 1e-3) / 1e9
+        line = {
+            "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "M": list(DECODE_M), "calls_per_step": launches_per_step,
+                       "bytes_per_step": step_bytes, "l2": "inputs larger than L2: 5 rotating weight copies "
+                       "(1.1 GB per step)", "graph": "one CUDA graph per step"},
+            "us_per_call": per_call,
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
+                         "frac": round(achieved / hbm_peak, 4), "peak_kind": f"{peak_kind} copy bandwidth",
+                         "frac_of_8TBps": round(achieved / 8000.0, 4),
+                         "kernel": "qmv_mma_kernel (all 15 launches of the step)",
+                         "traffic": None if traffic is None else round(traffic / launches_per_step)},
+            "gpu_launches": launches_per_step * args.steps,
+            "e2e": e2e,
+            "clocks": clk.summary(),
+            "routes": routes,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line))
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def run_e2e(nv, torch, dev, stream, lin, xs, ys, args, step_bytes):
+    host_x = {key: x.cpu().pin_memory() for key, x in xs.items()}
+    host_y = {key: torch.empty(y.shape, dtype=y.dtype).pin_memory() for key, y in ys.items()}
+    dev_x = {key: torch.empty_like(x) for key, x in xs.items()}
+    h2d = sum(t.numel() * t.element_size() for t in host_x.values())
+    d2h = sum(t.numel() * t.element_size() for t in host_y.values())
+
+    def step(i):
+        for key in dev_x:
+            dev_x[key].copy_(host_x[key], non_blocking=True)
+        for mi, m in enumerate(DECODE_M):
+            for name, n, k, copies in lin:
+                w, s, gs = copies[(mi + i) % ROTATE]
+                nv.qmm(dev_x[(m, name)], w, s, gs=gs, out=ys[(m, name)])
+        for key in host_y:
+            host_y[key].copy_(ys[key], non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            step(i)
+        torch.cuda.synchronize(dev)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for i in range(args.steps):
+            step(i)
+        b.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = a.elapsed_time(b) / args.steps
+    return {"value": round(step_bytes / (ms * 1e-3) / 1e9, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": round(ms, 4),
+            "path": "nvfp4_qmm per call (no graph), pinned host x in, host y out"}
+
+
+def time_calls(torch, dev, stream, fn, reps):
+    with torch.cuda.stream(stream):
+        fn(0)
+        torch.cuda.synchronize(dev)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for i in range(reps):
+            fn(i)
+        b.record(stream)
+    torch.cuda.synchronize(dev)
+    return a.elapsed_time(b) / reps
+
+
+def run_routes(nv, synth, torch, dev, stream, args):
+    hbm_peak, bf16_peak, _ = peaks()
+    out = {}
+    g = synth.rng(3000)
+
+    def rand_w(n, k, copies=1, seed=0):
+        ws = []
+        for c in range(copies):
+            w = torch.randint(-2**31, 2**31 - 1, (n, k // 8), dtype=torch.int32, device=dev,
+                              generator=torch.Generator(device=dev).manual_seed(seed + c))
+            s = torch.from_numpy(synth.log_uniform_scales(g, (n, k // 16), 2.0**-6, 4.0)).to(dev)
+            ws.append((w, s))
+        return ws
+
+    # Prefill QuantizedMatmul (tensor-core route where the library picks it).
+    pre = {}
+    for (m, n, k) in ((512, 21504, 5376), (2048, 21504, 5376), (8192, 21504, 5376), (2048, 5376, 21504)):
+        ws = rand_w(n, k, 2, seed=n + k)
+        gs = torch.from_numpy(synth.global_scales(g, 1)).to(dev)
+        x = synth.activations(g, (m, k), "bf16").to(dev)
+        y = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
+        reps = 3 if m >= 8192 else 5
+        ms = time_calls(torch, dev, stream, lambda i: nv.qmm(x, ws[i % 2][0], ws[i % 2][1], gs=gs, out=y), reps)
+        tf = 2.0 * m * n * k / (ms * 1e-3) / 1e12
+        pre[f"M{m}_N{n}_K{k}"] = {"us": round(ms * 1e3, 1), "TFLOPs": round(tf, 1),
+                                  "frac_bf16": round(tf / bf16_peak, 4),
+                                  "route": "tc" if m >= nv.qmm_crossover(torch.bfloat16, n, k) else "qmv"}
+        del ws, x, y
+    out["qmm_prefill"] = pre
+
+    # Transcode: one layer's three ModelOpt triplets -> native planes.
+    tr = {}
+    tot_b, tot_ms = 0.0, 0.0
+    for name, n, k in LINEARS:
+        mo_w = torch.randint(0, 256, (n, k // 2), dtype=torch.uint8, device=dev)
+        mo_s = torch.randint(0, 127, (n, k // 16), dtype=torch.uint8, device=dev)
+        ws2 = torch.tensor([0.005], dtype=torch.float32, device=dev)
+        outp = (torch.empty((n, k // 8), dtype=torch.int32, device=dev),
+                torch.empty((n, k // 16), dtype=torch.uint8, device=dev),
+                torch.empty((1,), dtype=torch.float32, device=dev))
+        ms = time_calls(torch, dev, stream, lambda i: nv.transcode(mo_w, mo_s, ws2, out=outp), 5)
+        b = 2 * 0.5625 * n * k + 8
+        tr[name] = {"us": round(ms * 1e3, 1), "GBps": round(b / (ms * 1e-3) / 1e9, 1)}
+        tot_b += b
+        tot_ms += ms
+        del mo_w, mo_s, outp
+    tr["layer_GBps"] = round(tot_b / (tot_ms * 1e-3) / 1e9, 1)
+    tr["60_layers_ms_est"] = round(60 * tot_ms, 2)
+    out["transcode"] = tr
+
+    # Dequantize the gate/up weight to bf16.
+    n, k = 43008, 5376
+    (w, s), = rand_w(n, k, 1, seed=5)
+    d = torch.empty((n, k), dtype=torch.bfloat16, device=dev)
+    ms = time_calls(torch, dev, stream, lambda i: nv.dequantize(w, s, None, torch.bfloat16, out=d), 5)
+    b = 0.5625 * n * k + 2 * n * k
+    out["dequantize_bf16_43008x5376"] = {"us": round(ms * 1e3, 1), "GBps": round(b / (ms * 1e-3) / 1e9, 1),
+                                         "frac_hbm": round(b / (ms * 1e-3) / 1e9 / hbm_peak, 4)}
+    del d, w, s
+
+    # MoE GatherQMM: 128 experts, gate/up [1536, 2048], down [2048, 768].
+    E = 128
+    moe = {}
+    for name, n, k in (("gate_up", 1536, 2048), ("down", 2048, 768)):
+        w = torch.randint(-2**31, 2**31 - 1, (E, n, k // 8), dtype=torch.int32, device=dev)
+        s = torch.from_numpy(synth.log_uniform_scales(g, (E, n, k // 16), 2.0**-6, 4.0)).to(dev)
+        gs = torch.from_numpy(synth.global_scales(g, E)).to(dev)
+        # decode: 64 unsorted rows + experts E and E+1 (zero rows)
+        rhs = np.concatenate([synth.zipf_experts(g, 64, E), np.array([E, E + 1], dtype=np.uint32)])
+        rhs_d = torch.from_numpy(rhs.view(np.int32)).to(dev)
+        x = synth.activations(g, (66, k), "bf16").to(dev)
+        y = torch.empty((66, n), dtype=torch.bfloat16, device=dev)
+        ms = time_calls(torch, dev, stream, lambda i: nv.gather_qmm(x, w, s, rhs_d, None, gs=gs, out=y), 10)
+        uniq = len(set(int(v) for v in rhs if v < E))
+        b = uniq * 0.5625 * n * k + 66 * 2 * (k + n)
+        moe[f"decode_{name}"] = {"us": round(ms * 1e3, 1), "unique_experts": uniq,
+                                 "GBps_unique": round(b / (ms * 1e-3) / 1e9, 1)}
+        # prefill: 4096 tokens, top-8 Zipf(1.1) routing, rows sorted by expert;
+        # the down projection takes the 32768 gate/up output rows in order.
+        if name == "gate_up":
+            lhs_p, rhs_p = synth.zipf_routing(g, 4096, E, 8)
+            lhs, rhs = lhs_p, rhs_p
+            xp = synth.activations(g, (4096, k), "bf16").to(dev)
+        else:
+            lhs, rhs = np.arange(rhs_p.size, dtype=np.uint32), rhs_p
+            xp = synth.activations(g, (rhs_p.size, k), "bf16").to(dev)
+        lhs_d = torch.from_numpy(lhs.view(np.int32)).to(dev)
+        rhs_d = torch.from_numpy(rhs.view(np.int32)).to(dev)
+        yp = torch.empty((rhs.size, n), dtype=torch.bfloat16, device=dev)
+        ms = time_calls(torch, dev, stream,
+                        lambda i: nv.gather_qmm(xp, w, s, rhs_d, lhs_d, gs=gs, sorted_indices=True, out=yp), 3)
+        tf = 2.0 * rhs.size * n * k / (ms * 1e-3) / 1e12
+        moe[f"prefill_{name}"] = {"rows": int(rhs.size), "us": round(ms * 1e3, 1), "TFLOPs": round(tf, 1),
+                                  "frac_bf16": round(tf / bf16_peak, 4)}
+        del w, s, x, y, xp, yp
+    out["gather_moe"] = moe
+    torch.cuda.empty_cache()
+    return out
+
+
+# ----------------------------------------------------------------------------- CPU oracle
+
+def oracle_sample(rows_per_linear=192, seed=4000):
+    """A bounded sample of the decode step for the CPU oracle: the first
+    `rows_per_linear` output columns of every (M, linear) call."""
+    from nvfp4_quantized_matmul_gb300 import synth
+
+    g = synth.rng(seed)
+    items = []
+    for m in DECODE_M:
+        for name, n, k in LINEARS:
+            w = synth.packed_weight(g, rows_per_linear, k)
+            s = synth.log_uniform_scales(g, (rows_per_linear, k // 16), 2.0**-6, 4.0)
+            gs = synth.global_scales(g, 1)[0]
+            x = synth.activations(g, (m, k), "bf16").double().numpy()
+            items.append((m, rows_per_linear, k, x, w, s, gs))
+    return items
+
+
+def time_oracle(items):
+    from oracle import nvfp4_oracle as O
+
+    t0 = time.perf_counter()
+    nbytes = 0.0
+    for (m, n, k, x, w, s, gs) in items:
+        O.qmm(x, w, s, gs)
+        nbytes += qmv_bytes(m, n, k)
+    return nbytes, time.perf_counter() - t0
+
+
+def cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count()
+
+
+def run_cpu_baseline(args):
+    items = oracle_sample(args.cpu_rows)
+    nbytes, secs = time_oracle(items)
+    return {"value": round(nbytes / secs / 1e9, 4), "unit": "GB/s", "cores": cores(), "kind": "oracle",
+            "seconds": round(secs, 2),
+            "sample": f"first {args.cpu_rows} weight rows of each of the 15 decode calls "
+                      f"({nbytes / 1e6:.1f} MB algorithmic), numpy float64 oracle"}
+
+
+def run_case(args):
+    """Small profiling case: gate/up [43008, 5376] (two copies, 260 MB, larger
+    than L2), three warm-up calls then one call each at M = 1, 8 and 16."""
+    import torch
+
+    import nvfp4_quantized_matmul_gb300 as nv
+    from nvfp4_quantized_matmul_gb300 import synth
+
+    dev = torch.device("cuda", 0)
+    g = synth.rng(5000)
+    n, k = 43008, 5376
+    ws = []
+    for c in range(2):
+        w = torch.randint(-2**31, 2**31 - 1, (n, k // 8), dtype=torch.int32, device=dev,
+                          generator=torch.Generator(device=dev).manual_seed(c))
+        s = torch.from_numpy(synth.log_uniform_scales(g, (n, k // 16), 2.0**-6, 4.0)).to(dev)
+        ws.append((w, s))
+    gs = torch.from_numpy(synth.global_scales(g, 1)).to(dev)
+    for i, m in enumerate((1, 1, 1, 1, 8, 16)):
+        x = synth.activations(g, (m, k), "bf16").to(dev)
+        nv.qmm(x, ws[i % 2][0], ws[i % 2][1], gs=gs)
+    torch.cuda.synchronize(dev)
+    print("case qmv_small ok")
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    items = oracle_sample(args.ref_rows)
+    for _ in range(args.warmup):
+        time_oracle(items[:3])
+    tot_b, tot_s = 0.0, 0.0
+    for _ in range(args.steps):
+        b, s = time_oracle(items)
+        tot_b += b
+        tot_s += s
+    value = tot_b / tot_s / 1e9
+    ms_step = tot_s / args.steps * 1e3
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+        "n_gpus": int(os.environ.get("WORLD_SIZE", "1")), "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 2), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "M": list(DECODE_M), "sample_rows_per_linear": args.ref_rows},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores(), "kind": "oracle",
+                         "sample": f"first {args.ref_rows} weight rows of each of the 15 decode calls per step"},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-routes", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--cpu-rows", type=int, default=640)
+    ap.add_argument("--ref-rows", type=int, default=32)
+    ap.add_argument("--case", choices=["qmv_small"], default=None,
+                    help="run one small profiling case instead of the benchmark")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.case:
+        run_case(args)
+    elif args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -118,6 +118,15 @@ nvfp4_status nvfp4_gather_qmm(const void* x, nvfp4_dtype x_dtype, int64_t B, int
                               int64_t w_len, const uint8_t* scales, int64_t scales_len, const float* gs,
                               int64_t gs_len, int64_t E, int64_t N, void* y, void* stream);
 
+/* Error code recorded on the device by a tensor-core kernel whose bounded
+ * wait on a pipeline barrier ran out (each wait gives up after 2 s instead of
+ * hanging, and the kernel then returns without finishing its tiles); the
+ * call reads and clears it. Blocks until all prior work on the current device
+ * has finished. Returns 0 when no wait gave up, -1 if the read failed. Not
+ * part of the pages' interface: it exists so that a kernel can report a stall
+ * instead of holding the GPU. */
+int32_t nvfp4_take_device_error(void);
+
 /* Message for the calling thread's last non-OK status ("" if none). */
 const char* nvfp4_last_error(void);
 

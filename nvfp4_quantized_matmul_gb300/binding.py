@@ -35,6 +35,7 @@ SIGNATURES = {
                                 _I64, _I64, _P, _P]),
     "nvfp4_last_error": (ctypes.c_char_p, []),
     "nvfp4_version": (ctypes.c_char_p, []),
+    "nvfp4_take_device_error": (ctypes.c_int32, []),
 }
 
 
@@ -159,6 +160,11 @@ def gather_qmm(x, w, scales, rhs, lhs=None, gs=None, sorted_indices=False, out=N
                                 _ptr(w), w.numel(), _ptr(scales), scales.numel(), _ptr(gs), _n(gs), e, n,
                                 _ptr(out), _stream(x)))
     return out
+
+
+def take_device_error():
+    """Device error code from a tensor-core kernel's bounded wait (0 = none); synchronises."""
+    return int(_lib.nvfp4_take_device_error())
 
 
 def qmm_crossover(dtype, n, k):

@@ -116,6 +116,9 @@ cudaError_t run_qmv(nvfp4::QmvArgs a, int xdt, cudaStream_t st) {
   return cudaSuccess;
 }
 
+// Smallest M sent to the tensor-core route by default (measured sweep).
+constexpr int64_t kDefaultCrossover = 128;
+
 int64_t env_crossover() {
   const char* s = std::getenv("NVFP4_QMM_CROSSOVER");
   if (!s || !*s) return -1;
@@ -131,6 +134,8 @@ extern "C" {
 const char* nvfp4_last_error(void) { return g_last_error.c_str(); }
 
 const char* nvfp4_version(void) { return "nvfp4-gb300 0.1 (sm_103a)"; }
+
+int32_t nvfp4_take_device_error(void) { return nvfp4::read_tc_error(); }
 
 nvfp4_status nvfp4_transcode(const uint8_t* mo_weight, int64_t mo_weight_len, const uint8_t* mo_weight_scale,
                              int64_t mo_weight_scale_len, const float* weight_scale_2, int64_t N, int64_t K,
@@ -176,7 +181,7 @@ int64_t nvfp4_qmm_crossover(nvfp4_dtype x_dtype, int64_t N, int64_t K) {
   const int64_t env = env_crossover();
   if (env >= 0) return env;
   if (x_dtype == NVFP4_F32) return INT64_MAX;  // f32 activations stay on the exact SIMT path
-  return INT64_MAX;  // no tensor-core route built yet
+  return kDefaultCrossover;
 }
 
 nvfp4_status nvfp4_qmm_routed(const void* x, nvfp4_dtype x_dtype, int64_t M, int64_t K, const uint32_t* w,
@@ -199,7 +204,15 @@ nvfp4_status nvfp4_qmm_routed(const void* x, nvfp4_dtype x_dtype, int64_t M, int
   if (K == 0) return cuda_status(fn, cudaMemsetAsync(y, 0, (size_t)(M * N * dtype_size(x_dtype)), st));
   if (route == NVFP4_ROUTE_TC && x_dtype == NVFP4_F32)
     return fail(NVFP4_ERR_DTYPE, "%s: the tensor-core route takes f16 or bf16 activations", fn);
+  if (route == NVFP4_ROUTE_TC && !nvfp4::qmm_tc_supported(M, N, K))
+    return fail(NVFP4_ERR_SHAPE, "%s: the tensor-core route needs K %% 32 == 0 and K >= 32 (K=%" PRId64 ")", fn, K);
+  const bool use_tc = x_dtype != NVFP4_F32 && nvfp4::qmm_tc_supported(M, N, K) &&
+                      (route == NVFP4_ROUTE_TC || (route == NVFP4_ROUTE_AUTO && M >= nvfp4_qmm_crossover(x_dtype, N, K)));
+  if (use_tc)
+    return cuda_status(fn, nvfp4::launch_qmm_tc(x, (int)x_dtype, M, K, w, scales, gs, N, y, st));
   if ((s = check_qmv_grid(fn, M, N))) return s;
+  if (x_dtype != NVFP4_F32 && !nvfp4::qmv_supported_k(K))
+    return fail(NVFP4_ERR_LIMIT, "%s: K=%" PRId64 " exceeds %" PRId64 " for 16-bit activations", fn, K, nvfp4::kQmvMaxK);
   nvfp4::QmvArgs a{x, w, scales, gs, nullptr, nullptr, M, M, K, N, 1, y};
   return cuda_status(fn, run_qmv(a, (int)x_dtype, st));
 }
@@ -231,6 +244,9 @@ nvfp4_status nvfp4_gather_qmm(const void* x, nvfp4_dtype x_dtype, int64_t B, int
   if (!aligned(rhs_indices, 4) || !aligned(lhs_indices, 4))
     return fail(NVFP4_ERR_ALIGN, "%s: index arrays must be 4-byte aligned", fn);
   if ((s = check_qmv_grid(fn, R, N))) return s;
+  if (x_dtype != NVFP4_F32 && !nvfp4::qmv_supported_k(K))
+    return fail(NVFP4_ERR_LIMIT, "%s: K=%" PRId64 " exceeds %" PRId64 " for 16-bit activations", fn, K, nvfp4::kQmvMaxK);
+  if (E > INT32_MAX) return fail(NVFP4_ERR_LIMIT, "%s: E=%" PRId64 " exceeds 2^31-1", fn, E);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (K == 0) return cuda_status(fn, cudaMemsetAsync(y, 0, (size_t)(R * N * dtype_size(x_dtype)), st));
   nvfp4::QmvArgs a{x, w, scales, gs, lhs_indices, rhs_indices, B, R, K, N, E, y};

@@ -30,4 +30,17 @@ struct QmvArgs {
 };
 cudaError_t launch_qmv(const QmvArgs& a, int xdt, cudaStream_t st);
 
+// Largest K the 16-bit decode-shape route stages in shared memory (eight
+// CTAs per cluster, eight rows per tile).
+constexpr int64_t kQmvMaxK = 98304;
+bool qmv_supported_k(int64_t K);
+
+// Prefill-shape tensor-core route (tcgen05, TMEM accumulators).
+bool qmm_tc_supported(int64_t M, int64_t N, int64_t K);
+cudaError_t launch_qmm_tc(const void* x, int xdt, int64_t M, int64_t K, const uint32_t* w, const uint8_t* scales,
+                          const float* gs, int64_t N, void* y, cudaStream_t st);
+// Reads and clears the error code left by a bounded wait in the tensor-core
+// kernels (synchronises with the device); 0 = none, -1 = read failed.
+int read_tc_error();
+
 }  // namespace nvfp4

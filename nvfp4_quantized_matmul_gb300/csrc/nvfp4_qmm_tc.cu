@@ -1,0 +1,492 @@
+// Prefill-shape NVFP4 QuantizedMatmul on the 5th-generation tensor cores.
+//
+// y[m, n] = factor * sum_k x[m, k] * (fp4 * e4m3)[n, k] for large M (mlxcel PR
+// #2629 "ROCm native NVFP4", Summary: prefill-size products take a dense GEMM
+// route; the global scale multiplies each output once, after the sum).
+//
+// The pages' route dequantizes the whole plane and calls a vendor GEMM. Here
+// the dequantization is fused into a persistent tcgen05 GEMM: the weights are
+// read packed (9/16 byte per element) and expanded tile by tile in shared
+// memory, so the dense plane never exists in HBM. The products fp4 * e4m3 are
+// exact in bf16/f16, so the tensor core sees exactly the dequantized weights.
+//
+// Per CTA (one per SM, 16 warps):
+//   warp 0      TMA producer of the activation tiles x[128 x 64] (SW128)
+//   warp 1      MMA issuer: tcgen05.mma.cta_group::1.kind::f16, M=128 N=256
+//               K=16, accumulator in TMEM (two 256-column buffers)
+//   warp 2      TMEM allocator
+//   warps 4-7   epilogue: tcgen05.ld 32x32b, global factor, cast, store
+//   warps 8-15  weight producers: 128-bit loads of the packed words and
+//               scale bytes (prefetched three stages ahead in registers),
+//               exact decode to bf16/f16, stores in the canonical K-major
+//               128-byte-swizzled layout the MMA descriptor reads
+// Stages hand off through mbarriers; every wait is bounded and records an
+// error code instead of hanging.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+#include <type_traits>
+
+#include "nvfp4_common.cuh"
+#include "nvfp4_internal.h"
+
+namespace nvfp4 {
+
+__device__ int g_tc_error = 0;  // first error code recorded by a bounded wait
+
+namespace {
+
+constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
+constexpr uint32_t A_BYTES = BM * BK * 2;  // 16 KB
+constexpr uint32_t B_BYTES = BN * BK * 2;  // 32 KB
+constexpr int kThreads = 512;
+constexpr int kProducerWarps = 8;
+constexpr int kEpiWarps = 4;
+constexpr int kWarpTma = 0, kWarpMma = 1, kWarpAlloc = 2, kWarpEpi0 = 4, kWarpProd0 = 8;
+constexpr uint32_t kTmemCols = 512;  // two 256-column f32 accumulators
+constexpr int kBarBytes = 8 * (3 * STAGES + 4) + 16;
+constexpr size_t kSmemBytes = 1024 + STAGES * (A_BYTES + B_BYTES) + kBarBytes;
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+
+struct TcParams {
+  const uint32_t* w;
+  const uint8_t* scales;
+  const float* gs;
+  void* y;
+  int64_t M, N, K;
+  int num_m_tiles, num_tiles, num_kb;
+};
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ uint64_t gtimer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+// Bounded wait: false (and the abort flag set) after kWaitLimitNs, or as soon
+// as another role has aborted.
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag, int code) {
+  if (mbar_try(bar, parity)) return true;
+  const uint64_t t0 = gtimer();
+  for (uint32_t n = 1;; ++n) {
+    if (mbar_try(bar, parity)) return true;
+    if ((n & 63) == 0) {
+      if (*abort_flag) return false;
+      if (gtimer() - t0 > kWaitLimitNs) {
+        *abort_flag = 1;
+        atomicCAS(&g_tc_error, 0, code);
+        return false;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int c0, int c1, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// Shared-memory matrix descriptor, K-major, 128-byte swizzle: rows of 128
+// bytes, eight-row groups 1024 bytes apart (stride byte offset), descriptor
+// version 1 (bits 46-48), swizzle mode 2 (bits 61-63).
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+  return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
+         ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+
+// Instruction descriptor for kind::f16: f32 accumulator, A/B bf16 or f16,
+// both K-major, N = BN, M = BM.
+template <bool BF16>
+__host__ __device__ constexpr uint32_t make_idesc() {
+  return (1u << 4) | ((BF16 ? 1u : 0u) << 7) | ((BF16 ? 1u : 0u) << 10) | ((uint32_t)(BN >> 3) << 17) |
+         ((uint32_t)(BM >> 4) << 24);
+}
+
+__device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void umma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+#define NVFP4_R8(i) "=r"(r[i]), "=r"(r[i + 1]), "=r"(r[i + 2]), "=r"(r[i + 3]), "=r"(r[i + 4]), "=r"(r[i + 5]), "=r"(r[i + 6]), "=r"(r[i + 7])
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,"
+      "%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : NVFP4_R8(0), NVFP4_R8(8), NVFP4_R8(16), NVFP4_R8(24)
+      : "r"(taddr));
+}
+#undef NVFP4_R8
+__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// ---------------------------------------------------------------- producer of decoded weights
+
+struct WTask {
+  uint4 w0, w1;      // packed words 4h..4h+3 of the k-block for rows r and r+128
+  uint32_t s0, s1;   // the four scale bytes of the k-block for rows r and r+128
+};
+
+struct WCursor {
+  int tile, kb;
+  bool done;
+};
+
+__device__ __forceinline__ void w_load(WTask& t, const WCursor& cur, const TcParams& p, int r, int h) {
+  if (cur.done) return;
+  const int n_tile = cur.tile / p.num_m_tiles;
+  const int64_t kwords = p.K / 8, kgroups = p.K / 16;
+  const int64_t n0 = (int64_t)n_tile * BN + r, n1 = n0 + 128;
+  const int64_t kw = (int64_t)cur.kb * 8 + 4 * h;  // first of this task's four words
+  const bool kok = kw < kwords;                     // K % 32 == 0 keeps the four words together
+  const int64_t g4 = (int64_t)cur.kb * 4;
+  t.w0 = (kok && n0 < p.N) ? __ldg(reinterpret_cast<const uint4*>(p.w + n0 * kwords + kw)) : make_uint4(0, 0, 0, 0);
+  t.w1 = (kok && n1 < p.N) ? __ldg(reinterpret_cast<const uint4*>(p.w + n1 * kwords + kw)) : make_uint4(0, 0, 0, 0);
+  if (kgroups % 4 == 0) {
+    t.s0 = (kok && n0 < p.N) ? __ldg(reinterpret_cast<const uint32_t*>(p.scales + n0 * kgroups + g4)) : 0u;
+    t.s1 = (kok && n1 < p.N) ? __ldg(reinterpret_cast<const uint32_t*>(p.scales + n1 * kgroups + g4)) : 0u;
+  } else {
+    uint32_t a = 0, b = 0;
+    for (int i = 0; i < 4; ++i) {
+      if (g4 + i < kgroups) {
+        if (n0 < p.N) a |= (uint32_t)p.scales[n0 * kgroups + g4 + i] << (8 * i);
+        if (n1 < p.N) b |= (uint32_t)p.scales[n1 * kgroups + g4 + i] << (8 * i);
+      }
+    }
+    t.s0 = a;
+    t.s1 = b;
+  }
+}
+
+__device__ __forceinline__ void w_advance(WCursor& cur, const TcParams& p) {
+  if (++cur.kb >= p.num_kb) {
+    cur.kb = 0;
+    cur.tile += gridDim.x;
+    if (cur.tile >= p.num_tiles) cur.done = true;
+  }
+}
+
+// Decode one row's four words (columns 32h..32h+31 of the k-block) and store
+// them as four 16-byte chunks of the swizzled row.
+template <typename T>
+__device__ __forceinline__ void w_store_row(uint32_t stage_base, int row, int h, const uint4& w, uint32_t sbytes) {
+  const uint32_t sc0 = Dt<T>::scale((sbytes >> (16 * h)) & 0xFF);
+  const uint32_t sc1 = Dt<T>::scale((sbytes >> (16 * h + 8)) & 0xFF);
+  const uint32_t rbase = stage_base + (uint32_t)(row >> 3) * 1024u + (uint32_t)(row & 7) * 128u;
+  const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    uint32_t o[4];
+    Dt<T>::decode(ws[i], i < 2 ? sc0 : sc1, o);
+    const uint32_t chunk = (uint32_t)(4 * h + i) ^ (uint32_t)(row & 7);
+    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(rbase + chunk * 16u), "r"(o[0]), "r"(o[1]),
+                 "r"(o[2]), "r"(o[3])
+                 : "memory");
+  }
+}
+
+template <typename T>
+__device__ void producer_role(const TcParams& p, uint32_t sB, uint32_t bars, volatile int* abort_flag) {
+  const int pid = threadIdx.x - kWarpProd0 * 32;  // 0..255
+  const int r = pid >> 1, h = pid & 1;            // rows r and r+128, words 4h..4h+3 of the k-block
+  const int lane = threadIdx.x & 31;
+  WCursor ld{(int)blockIdx.x, 0, (int)blockIdx.x >= p.num_tiles};
+  WTask b0, b1, b2;
+  w_load(b0, ld, p, r, h);
+  w_advance(ld, p);
+  w_load(b1, ld, p, r, h);
+  w_advance(ld, p);
+  uint32_t u = 0;
+  const int total = ((p.num_tiles - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x) * p.num_kb;
+  auto consume = [&](const WTask& t) -> bool {
+    const int s = (int)(u % STAGES);
+    const uint32_t ph = (u / STAGES) & 1;
+    if (!wait_bar(bars + 8 * (2 * STAGES + s), ph ^ 1, abort_flag, 3)) return false;  // stage empty
+    const uint32_t stage = sB + (uint32_t)s * B_BYTES;
+    w_store_row<T>(stage, r, h, t.w0, t.s0);
+    w_store_row<T>(stage, r + 128, h, t.w1, t.s1);
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bars + 8 * (STAGES + s));  // fullB
+    ++u;
+    return true;
+  };
+  for (int i = 0; i < total; i += 3) {
+    w_load(b2, ld, p, r, h);
+    w_advance(ld, p);
+    if (!consume(b0)) return;
+    if (i + 1 >= total) break;
+    w_load(b0, ld, p, r, h);
+    w_advance(ld, p);
+    if (!consume(b1)) return;
+    if (i + 2 >= total) break;
+    w_load(b1, ld, p, r, h);
+    w_advance(ld, p);
+    if (!consume(b2)) return;
+  }
+}
+
+// ---------------------------------------------------------------- kernel
+
+template <typename T>
+__global__ void __launch_bounds__(kThreads, 1)
+qmm_tc_kernel(const __grid_constant__ CUtensorMap xmap, const TcParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* base_ptr = smem_raw + (base - raw);
+  const uint32_t sA = base, sB = base + STAGES * A_BYTES;
+  const uint32_t bars = sB + STAGES * B_BYTES;
+  // barriers: fullA[S] fullB[S] empty[S] accFull[2] accEmpty[2]
+  uint32_t* holder = reinterpret_cast<uint32_t*>(base_ptr + STAGES * (A_BYTES + B_BYTES) + 8 * (3 * STAGES + 4));
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(holder + 1);
+  auto fullA = [&](int s) { return bars + 8 * s; };
+  auto fullB = [&](int s) { return bars + 8 * (STAGES + s); };
+  auto emptyB = [&](int s) { return bars + 8 * (2 * STAGES + s); };
+  auto accFull = [&](int b) { return bars + 8 * (3 * STAGES + b); };
+  auto accEmpty = [&](int b) { return bars + 8 * (3 * STAGES + 2 + b); };
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(fullA(s), 1);
+      mbar_init(fullB(s), kProducerWarps);
+      mbar_init(emptyB(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(accFull(b), 1);
+      mbar_init(accEmpty(b), kEpiWarps);
+    }
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == kWarpTma && lane == 0)
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&xmap)) : "memory");
+  if (warp == kWarpAlloc) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(holder)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *holder;
+  const int my_tiles = (int)blockIdx.x < p.num_tiles
+                           ? (p.num_tiles - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x
+                           : 0;
+
+  if (warp == kWarpTma) {
+    if (lane == 0) {
+      uint32_t u = 0;
+      bool ok = true;
+      for (int i = 0; i < my_tiles && ok; ++i) {
+        const int tile = (int)blockIdx.x + i * (int)gridDim.x;
+        const int m_tile = tile % p.num_m_tiles;
+        for (int kb = 0; kb < p.num_kb; ++kb, ++u) {
+          const int s = (int)(u % STAGES);
+          const uint32_t ph = (u / STAGES) & 1;
+          if (!wait_bar(emptyB(s), ph ^ 1, abort_flag, 1)) { ok = false; break; }
+          mbar_arrive_tx(fullA(s), A_BYTES);
+          tma_load_2d(sA + (uint32_t)s * A_BYTES, &xmap, kb * BK, m_tile * BM, fullA(s));
+        }
+      }
+      // Leave no copy in flight: wait (bounded) for the last stages issued.
+      const uint32_t first = u > STAGES ? u - STAGES : 0;
+      for (uint32_t v = first; v < u; ++v) {
+        const uint32_t limit_ph = (v / STAGES) & 1;
+        const uint64_t t0 = gtimer();
+        while (!mbar_try(fullA((int)(v % STAGES)), limit_ph) && gtimer() - t0 < kWaitLimitNs) {
+        }
+      }
+    }
+  } else if (warp == kWarpMma) {
+    if (lane == 0) {
+      constexpr uint32_t idesc = make_idesc<std::is_same<T, __nv_bfloat16>::value>();
+      uint32_t u = 0;
+      bool ok = true;
+      for (int i = 0; i < my_tiles && ok; ++i) {
+        const int b = i & 1;
+        if (!wait_bar(accEmpty(b), ((i >> 1) & 1) ^ 1, abort_flag, 4)) break;
+        tc_fence_after();
+        const uint32_t d = tmem + (uint32_t)(b * BN);
+        for (int kb = 0; kb < p.num_kb; ++kb, ++u) {
+          const int s = (int)(u % STAGES);
+          const uint32_t ph = (u / STAGES) & 1;
+          if (!wait_bar(fullA(s), ph, abort_flag, 5) || !wait_bar(fullB(s), ph, abort_flag, 6)) { ok = false; break; }
+          tc_fence_after();
+          const uint64_t ad = sw128_desc(sA + (uint32_t)s * A_BYTES);
+          const uint64_t bd = sw128_desc(sB + (uint32_t)s * B_BYTES);
+#pragma unroll
+          for (int j = 0; j < BK / 16; ++j)
+            umma_f16(d, ad + (uint64_t)(2 * j), bd + (uint64_t)(2 * j), idesc, (kb | j) != 0);
+          umma_commit(emptyB(s));
+        }
+        if (ok) umma_commit(accFull(b));
+      }
+    }
+  } else if (warp >= kWarpEpi0 && warp < kWarpEpi0 + kEpiWarps) {
+    const int q = warp - kWarpEpi0;  // TMEM lane quarter
+    const float fac = global_factor(p.gs, 0);
+    T* y = static_cast<T*>(p.y);
+    for (int i = 0; i < my_tiles; ++i) {
+      const int tile = (int)blockIdx.x + i * (int)gridDim.x;
+      const int m_tile = tile % p.num_m_tiles, n_tile = tile / p.num_m_tiles;
+      const int b = i & 1;
+      if (!wait_bar(accFull(b), (i >> 1) & 1, abort_flag, 7)) break;
+      tc_fence_after();
+      const int64_t m = (int64_t)m_tile * BM + 32 * q + lane;
+      const int64_t n_base = (int64_t)n_tile * BN;
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(b * BN + 32 * c), r);
+        tmem_ld_wait();
+        if (m >= p.M) continue;
+        const int64_t n0 = n_base + 32 * c;
+        uint32_t packed[16];
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+          float v0 = __uint_as_float(r[2 * k]), v1 = __uint_as_float(r[2 * k + 1]);
+          if (p.gs) {
+            v0 = __fmul_rn(v0, fac);
+            v1 = __fmul_rn(v1, fac);
+          }
+          const T t0 = Dt<T>::from_f32(v0), t1 = Dt<T>::from_f32(v1);
+          packed[k] = (uint32_t)(*reinterpret_cast<const uint16_t*>(&t0)) |
+                      ((uint32_t)(*reinterpret_cast<const uint16_t*>(&t1)) << 16);
+        }
+        T* dst = y + m * p.N + n0;
+        if (n0 + 32 <= p.N && (p.N % 8) == 0) {
+          uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            d4[k] = make_uint4(packed[4 * k], packed[4 * k + 1], packed[4 * k + 2], packed[4 * k + 3]);
+        } else {
+          uint16_t* d16 = reinterpret_cast<uint16_t*>(dst);
+          for (int k = 0; k < 32 && n0 + k < p.N; ++k)
+            d16[k] = (uint16_t)(packed[k >> 1] >> (16 * (k & 1)));
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(accEmpty(b));
+    }
+  } else if (warp >= kWarpProd0) {
+    producer_role<T>(p, sB, bars, abort_flag);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kWarpAlloc) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
+  }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+template <typename T>
+cudaError_t launch_tc(const void* x, int64_t M, int64_t K, const uint32_t* w, const uint8_t* scales, const float* gs,
+                      int64_t N, void* y, cudaStream_t st) {
+  auto enc = encode_fn();
+  if (!enc) return cudaErrorNotSupported;
+  CUtensorMap map;
+  const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)M};
+  const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+  const cuuint32_t box[2] = {BK, BM};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUtensorMapDataType dt =
+      std::is_same<T, __nv_bfloat16>::value ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  CUresult r = enc(&map, dt, 2, const_cast<void*>(x), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  TcParams p;
+  p.w = w;
+  p.scales = scales;
+  p.gs = gs;
+  p.y = y;
+  p.M = M;
+  p.N = N;
+  p.K = K;
+  p.num_m_tiles = (int)((M + BM - 1) / BM);
+  const int num_n_tiles = (int)((N + BN - 1) / BN);
+  p.num_tiles = p.num_m_tiles * num_n_tiles;
+  p.num_kb = (int)((K + BK - 1) / BK);
+  int dev = 0, sms = 152;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int grid = p.num_tiles < sms ? p.num_tiles : sms;
+  cudaError_t e = cudaFuncSetAttribute(qmm_tc_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+  if (e != cudaSuccess) return e;
+  qmm_tc_kernel<T><<<grid, kThreads, kSmemBytes, st>>>(map, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool qmm_tc_supported(int64_t M, int64_t N, int64_t K) {
+  // TMA coordinates are 32-bit; K must keep each 128-bit weight load within
+  // one k-block row segment (K % 32 == 0).
+  return M > 0 && N > 0 && K >= 32 && K % 32 == 0 && M < (1ll << 31) && K < (1ll << 31) &&
+         (M + BM - 1) / BM * ((N + BN - 1) / BN) < (1ll << 31);
+}
+
+cudaError_t launch_qmm_tc(const void* x, int xdt, int64_t M, int64_t K, const uint32_t* w, const uint8_t* scales,
+                          const float* gs, int64_t N, void* y, cudaStream_t st) {
+  if (xdt == kBF16) return launch_tc<__nv_bfloat16>(x, M, K, w, scales, gs, N, y, st);
+  return launch_tc<__half>(x, M, K, w, scales, gs, N, y, st);
+}
+
+int read_tc_error() {
+  int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_tc_error, sizeof(int)) != cudaSuccess) return -1;
+  const int zero = 0;
+  cudaMemcpyToSymbol(g_tc_error, &zero, sizeof(int));
+  return v;
+}
+
+}  // namespace nvfp4

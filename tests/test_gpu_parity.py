@@ -195,3 +195,55 @@ def test_gather_identity_lhs(nv):
     ref = O.gather_qmm(x.double().numpy(), None, rhs, w, s)
     assert rel_err(y, ref) <= TOL["bf16"]
     assert np.all(y[4].float().cpu().numpy() == 0.0)
+
+
+# ------------------------------------------------------------------ tensor-core (tcgen05) route
+
+TC_SHAPES = [(1, 256, 64), (100, 272, 96), (128, 512, 256), (129, 40, 64), (300, 520, 320), (256, 256, 5376)]
+
+
+@pytest.mark.parametrize("mnk", TC_SHAPES, ids=lambda v: "M%d_N%d_K%d" % v)
+@pytest.mark.parametrize("dt", ["f16", "bf16"])
+def test_qmm_tc_route(nv, mnk, dt):
+    M, N, K = mnk
+    w, s = weights(M + 7 * N + K, N, K, lo=2.0**-4, hi=16.0)
+    g = synth.rng(M * 77 + N + K)
+    x = synth.activations(g, (M, K), dt)
+    for gs in (None, np.float32(2688 * 0.37)):
+        y, backing, guard = guarded_empty((M, N), TORCH[dt], fill=-7.0)
+        nv.qmm(x.cuda(), u32_to_dev(w), u8_to_dev(s), gs=None if gs is None else float(gs), route="tc", out=y)
+        torch.cuda.synchronize()
+        assert nv.take_device_error() == 0
+        ref = O.qmm(x.double().numpy(), w, s, gs)
+        err = rel_err(y, ref)
+        assert err <= TOL[dt], f"rel-to-max error {err:.3g} > {TOL[dt]}"
+        assert guards_intact(backing, guard)
+
+
+def test_qmm_tc_matches_qmv_route(nv):
+    """Both routes compute the same sums: outputs agree to bf16 rounding."""
+    M, N, K = 192, 384, 1024
+    w, s = weights(3, N, K)
+    x = synth.activations(synth.rng(33), (M, K), "bf16").cuda()
+    a = nv.qmm(x, u32_to_dev(w), u8_to_dev(s), route="tc").float()
+    b = nv.qmm(x, u32_to_dev(w), u8_to_dev(s), route="qmv").float()
+    assert nv.take_device_error() == 0
+    assert (a - b).abs().max().item() <= 2 * 2.0**-8 * b.abs().max().item()
+
+
+@pytest.mark.parametrize("special", [1e-30, 1e5, -3e30, 2.0**-20])
+def test_qmm_qmv_bf16_values_outside_f16(nv, special):
+    """bf16 activations that f16 cannot hold exactly take the bf16 decode path;
+    the result still matches the oracle (the f16 fast path is only taken when
+    every staged activation converts exactly)."""
+    M, N, K = 3, 272, 512
+    w, s = weights(11, N, K)
+    x = synth.activations(synth.rng(12), (M, K), "bf16")
+    x[1, 5] = special
+    x[2, 300] = special
+    y = nv.qmm(x.cuda(), u32_to_dev(w), u8_to_dev(s), route="qmv")
+    ref = O.qmm(x.double().numpy(), w, s, None)
+    assert rel_err(y, ref) <= TOL["bf16"]
+    # rows without the special value are unaffected by it
+    ref0 = O.qmm(x[:1].double().numpy(), w, s, None)
+    assert rel_err(y[:1], ref0) <= TOL["bf16"]
