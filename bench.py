@@ -221,24 +221,29 @@ def run_ours(args):
     ms_step = ms_total / args.steps
     value = step_bytes * world / (ms_step * 1e-3) / 1e9
 
-    # Per-call latency (µs/call) per shape: each call timed alone on the
-    # stream, weights rotated, after the step measurement.
+    # Per-call latency (µs/call) per shape: ten calls (rotating weight copies)
+    # captured in one CUDA graph, replayed, device time / 10.
     per_call = {}
     with torch.cuda.stream(stream):
         for mi, m in enumerate(DECODE_M):
             for name, n, k, copies in lin:
-                evs = []
-                for rep in range(2 * ROTATE):
-                    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                    w, s, gs = copies[rep % ROTATE]
-                    a.record(stream)
-                    nv.qmm(xs[(m, name)], w, s, gs=gs, out=ys[(m, name)])
-                    b.record(stream)
-                    evs.append((a, b))
+                gph = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(gph, stream=stream):
+                    for rep in range(2 * ROTATE):
+                        w, s, gs = copies[rep % ROTATE]
+                        nv.qmm(xs[(m, name)], w, s, gs=gs, out=ys[(m, name)])
+                gph.replay()
                 torch.cuda.synchronize(dev)
-                us = statistics.median(a.elapsed_time(b) * 1e3 for a, b in evs[ROTATE:])
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                for _ in range(3):
+                    gph.replay()
+                b.record(stream)
+                torch.cuda.synchronize(dev)
+                us = a.elapsed_time(b) * 1e3 / (3 * 2 * ROTATE)
                 per_call[f"{name}_M{m}"] = {"us": round(us, 2),
                                             "GBps": round(qmv_bytes(m, n, k) / (us * 1e-6) / 1e9, 1)}
+                del gph
 
     # End to end through the public API: pinned host activations in, bf16
     # outputs back to pinned host memory, every step.
@@ -468,14 +473,36 @@ def run_cpu_baseline(args):
 
 
 def run_case(args):
-    """Small profiling case: gate/up [43008, 5376] (two copies, 260 MB, larger
-    than L2), three warm-up calls then one call each at M = 1, 8 and 16."""
+    """Small profiling cases.
+
+    qmv_small: gate/up [43008, 5376] (two copies, 260 MB, larger than L2),
+    three warm-up calls then one call each at M = 1, 8 and 16.
+    qmv_shapes: each decode linear (gate/up, down, qkv; 220 MB) once at M = 1
+    and once at M = 16, after one warm-up call each.
+    """
     import torch
 
     import nvfp4_quantized_matmul_gb300 as nv
     from nvfp4_quantized_matmul_gb300 import synth
 
     dev = torch.device("cuda", 0)
+    if args.case == "qmv_shapes":
+        g = synth.rng(5100)
+        lin = []
+        for name, n, k in LINEARS:
+            w = torch.randint(-2**31, 2**31 - 1, (n, k // 8), dtype=torch.int32, device=dev,
+                              generator=torch.Generator(device=dev).manual_seed(n))
+            s = torch.from_numpy(synth.log_uniform_scales(g, (n, k // 16), 2.0**-6, 4.0)).to(dev)
+            gs = torch.from_numpy(synth.global_scales(g, 1)).to(dev)
+            lin.append((w, s, gs, k))
+        for w, s, gs, k in lin:
+            nv.qmm(synth.activations(g, (1, k), "bf16").to(dev), w, s, gs=gs)
+        for m in (1, 16):
+            for w, s, gs, k in lin:
+                nv.qmm(synth.activations(g, (m, k), "bf16").to(dev), w, s, gs=gs)
+        torch.cuda.synchronize(dev)
+        print("case qmv_shapes ok")
+        return
     g = synth.rng(5000)
     n, k = 43008, 5376
     ws = []
@@ -529,7 +556,7 @@ def main():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-rows", type=int, default=640)
     ap.add_argument("--ref-rows", type=int, default=32)
-    ap.add_argument("--case", choices=["qmv_small"], default=None,
+    ap.add_argument("--case", choices=["qmv_small", "qmv_shapes"], default=None,
                     help="run one small profiling case instead of the benchmark")
     args = ap.parse_args()
     if args.warmup < 3:

@@ -135,7 +135,11 @@ const char* nvfp4_last_error(void) { return g_last_error.c_str(); }
 
 const char* nvfp4_version(void) { return "nvfp4-gb300 0.1 (sm_103a)"; }
 
-int32_t nvfp4_take_device_error(void) { return nvfp4::read_tc_error(); }
+int32_t nvfp4_take_device_error(void) {
+  const int a = nvfp4::read_tc_error(), b = nvfp4::read_qmv_error();
+  if (a < 0 || b < 0) return -1;
+  return a ? a : b;
+}
 
 nvfp4_status nvfp4_transcode(const uint8_t* mo_weight, int64_t mo_weight_len, const uint8_t* mo_weight_scale,
                              int64_t mo_weight_scale_len, const float* weight_scale_2, int64_t N, int64_t K,

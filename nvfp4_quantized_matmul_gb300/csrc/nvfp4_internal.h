@@ -30,10 +30,14 @@ struct QmvArgs {
 };
 cudaError_t launch_qmv(const QmvArgs& a, int xdt, cudaStream_t st);
 
-// Largest K the 16-bit decode-shape route stages in shared memory (eight
+// Largest K the 16-bit decode-shape route stages in shared memory (sixteen
 // CTAs per cluster, eight rows per tile).
-constexpr int64_t kQmvMaxK = 98304;
+constexpr int64_t kQmvMaxK = 196608;
 bool qmv_supported_k(int64_t K);
+// TMA-fed variant of the decode-shape route (16-bit activations, K % 256 == 0).
+bool qmv_tma_supported(const QmvArgs& a, int xdt);
+cudaError_t launch_qmv_tma(const QmvArgs& a, int xdt, cudaStream_t st);
+int read_qmv_error();
 
 // Prefill-shape tensor-core route (tcgen05, TMEM accumulators).
 bool qmm_tc_supported(int64_t M, int64_t N, int64_t K);

@@ -69,13 +69,17 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
 __device__ __forceinline__ void mbar_arrive_tx(uint32_t bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
 }
+// A waiting thread may be suspended by the hardware for up to this long per
+// try (it resumes as soon as the phase completes), so waits do not burn issue
+// slots that the working warps need.
+constexpr uint32_t kSuspendHintNs = 1000;
 __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
-      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(bar), "r"(parity)
+      : "r"(bar), "r"(parity), "r"(kSuspendHintNs)
       : "memory");
   return ok != 0;
 }
@@ -102,6 +106,26 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
   }
 }
 
+// Bounded wait executed by all 32 lanes of a warp together: every lane polls
+// the barrier (so each has acquired the phase), and the decision to stop is
+// taken warp-wide, so the lanes never diverge on a timeout.
+__device__ __forceinline__ bool wait_bar_warp(uint32_t bar, uint32_t parity, volatile int* abort_flag, int code, int* err) {
+  if (__all_sync(0xffffffffu, mbar_try(bar, parity))) return true;
+  const uint64_t t0 = gtimer();
+  for (uint32_t n = 1;; ++n) {
+    if (__all_sync(0xffffffffu, mbar_try(bar, parity))) return true;
+    if ((n & 63) == 0) {
+      const bool stop = __any_sync(0xffffffffu, *abort_flag != 0 || gtimer() - t0 > kWaitLimitNs);
+      if (stop) {
+        if ((threadIdx.x & 31) == 0) {
+          if (!*abort_flag) atomicCAS(err, 0, code);
+          *abort_flag = 1;
+        }
+        return false;
+      }
+    }
+  }
+}
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int c0, int c1, uint32_t bar) {
   asm volatile(
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
@@ -233,7 +257,7 @@ __device__ void producer_role(const TcParams& p, uint32_t sB, uint32_t bars, vol
   auto consume = [&](const WTask& t) -> bool {
     const int s = (int)(u % STAGES);
     const uint32_t ph = (u / STAGES) & 1;
-    if (!wait_bar(bars + 8 * (2 * STAGES + s), ph ^ 1, abort_flag, 3)) return false;  // stage empty
+    if (!wait_bar_warp(bars + 8 * (2 * STAGES + s), ph ^ 1, abort_flag, 3, &g_tc_error)) return false;  // stage empty
     const uint32_t stage = sB + (uint32_t)s * B_BYTES;
     w_store_row<T>(stage, r, h, t.w0, t.s0);
     w_store_row<T>(stage, r + 128, h, t.w1, t.s1);
@@ -365,7 +389,7 @@ qmm_tc_kernel(const __grid_constant__ CUtensorMap xmap, const TcParams p) {
       const int tile = (int)blockIdx.x + i * (int)gridDim.x;
       const int m_tile = tile % p.num_m_tiles, n_tile = tile / p.num_m_tiles;
       const int b = i & 1;
-      if (!wait_bar(accFull(b), (i >> 1) & 1, abort_flag, 7)) break;
+      if (!wait_bar_warp(accFull(b), (i >> 1) & 1, abort_flag, 7, &g_tc_error)) break;
       tc_fence_after();
       const int64_t m = (int64_t)m_tile * BM + 32 * q + lane;
       const int64_t n_base = (int64_t)n_tile * BN;

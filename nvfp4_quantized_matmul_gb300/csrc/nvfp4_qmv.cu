@@ -25,90 +25,30 @@
 //    the bf16 values and decodes the weights to bf16 instead. Either way the
 //    products entering the tensor core equal x * fp4 * e4m3 exactly and the
 //    sum is accumulated in f32.
-//  * K order inside one MMA is a permutation of the chunk's columns: in
-//    k16-step s lane t's A slots {2t, 2t+1, 2t+8, 2t+9} hold columns
-//    32t+4s+0..3 of its rows. A lane therefore streams four consecutive packed
-//    words (one 128-bit load) per row and chunk, and the staged activations
-//    are stored in the matching order so that its B operands for a chunk are
-//    four conflict-free 128-bit shared loads.
-#include "nvfp4_common.cuh"
-#include "nvfp4_internal.h"
+//  * K order inside one MMA is a permutation of the chunk's columns: with
+//    256-column chunks, in k16-step s lane t's A slots {2t, 2t+1, 2t+8, 2t+9}
+//    hold columns 64t+4s+0..3 of its rows. A lane therefore streams eight
+//    consecutive packed words (two 128-bit loads) per row and chunk, and the
+//    staged activations are stored in the matching order so that its B
+//    operands are conflict-free 128-bit shared loads.
+#include "nvfp4_qmv_common.cuh"
 
 namespace nvfp4 {
 namespace {
+using namespace qmv;
 
-constexpr int kWarps = 8;
-constexpr int kThreads = kWarps * 32;
-constexpr int kSlabRows = kWarps * 16;  // 128 weight rows per slab
-
-template <typename T> struct MmaOp;
-template <> struct MmaOp<__half> {
-  __device__ static __forceinline__ void run(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                             uint32_t b0, uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-        "{%0,%1,%2,%3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-  }
-};
-template <> struct MmaOp<__nv_bfloat16> {
-  __device__ static __forceinline__ void run(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                             uint32_t b0, uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-        "{%0,%1,%2,%3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-  }
-};
-
-__device__ __forceinline__ uint32_t cluster_rank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-__device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory"); }
-__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
-__device__ __forceinline__ uint32_t map_rank(uint32_t saddr, uint32_t rank) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
-  return r;
-}
-__device__ __forceinline__ float ld_dsmem(uint32_t addr) {
-  float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
-  return v;
-}
-__device__ __forceinline__ uint4 lds128(uint32_t addr) {
-  uint4 v;
-  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
-  return v;
-}
-
-// Launch plan, computed on the host.
-struct Plan {
-  int C;            // cluster size = K split
-  int nchunk;       // 128-column chunks in K
-  int64_t slabs;    // 128-row slabs of N
-  int spc;          // slabs per cluster (persistent loop)
-  int TR;           // output rows (token slots) per CTA row tile
-  int xs_stride;    // staged activation row stride in 16-bit elements
-  int x_is_bf16;    // activation input is bf16 (else f16)
-};
-
-struct Chunk {
-  uint4 wa, wb;     // words 4t..4t+3 of rows g and g+8
-  uint32_t sa, sb;  // scale bytes of groups 2t, 2t+1 of rows g and g+8 (low 16 bits)
-};
-
-// Iterator over this warp's chunk jobs: slab-major, then expert pass, then chunk.
-struct JobIter {
+// Load-side iterator over this warp's jobs: slab-major, then expert pass,
+// then chunk. Only the loads need addresses; the compute side counts.
+struct LoadIter {
   int slab_i, pass, chunk;
-  const uint32_t* pa;
-  const uint32_t* pb;
+  const uint32_t* pa;  // row n0+g of the current expert, at the chunk (null if n >= N)
+  const uint32_t* pb;  // row n0+g+8
   const uint8_t* qa;
   const uint8_t* qb;
+  bool done;
+};
+struct CountIter {
+  int slab_i, pass, chunk;
   bool done;
 };
 
@@ -123,225 +63,217 @@ struct Ctx {
   int row_g;                 // warp*16 + g
 };
 
-__device__ __forceinline__ void iter_point(JobIter& it, const Ctx& c) {
+__device__ __forceinline__ void iter_point(LoadIter& it, const Ctx& c) {
   const int64_t slab = c.slab0 + (int64_t)it.slab_i * c.slab_step;
   const int64_t e = c.pass_e[it.pass];
   const int64_t na = slab * kSlabRows + c.row_g, nb = na + 8;
   const uint32_t* we = c.w + e * c.N * c.kwords;
   const uint8_t* se = c.scales + e * c.N * c.kgroups;
-  it.pa = na < c.N ? we + na * c.kwords + (int64_t)it.chunk * 16 : nullptr;
-  it.pb = nb < c.N ? we + nb * c.kwords + (int64_t)it.chunk * 16 : nullptr;
-  it.qa = se + na * c.kgroups + (int64_t)it.chunk * 8;
-  it.qb = se + nb * c.kgroups + (int64_t)it.chunk * 8;
+  const int64_t kw = (int64_t)it.chunk * kChunkWords, kg = (int64_t)it.chunk * (kChunkCols / 16);
+  it.pa = na < c.N ? we + na * c.kwords + kw : nullptr;
+  it.pb = nb < c.N ? we + nb * c.kwords + kw : nullptr;
+  it.qa = se + na * c.kgroups + kg;
+  it.qb = se + nb * c.kgroups + kg;
 }
 
-__device__ __forceinline__ void iter_begin(JobIter& it, const Ctx& c) {
+template <typename It>
+__device__ __forceinline__ bool empty_job_list(const Ctx& c) {
+  return c.nslab <= 0 || c.cb >= c.ce || c.npass == 0;
+}
+
+__device__ __forceinline__ void iter_begin(LoadIter& it, const Ctx& c) {
   it.slab_i = 0;
   it.pass = 0;
   it.chunk = c.cb;
-  it.done = c.nslab <= 0 || c.cb >= c.ce || c.npass == 0;
+  it.done = empty_job_list<LoadIter>(c);
   if (!it.done) iter_point(it, c);
 }
+__device__ __forceinline__ void iter_begin(CountIter& it, const Ctx& c) {
+  it.slab_i = 0;
+  it.pass = 0;
+  it.chunk = c.cb;
+  it.done = empty_job_list<CountIter>(c);
+}
 
-// Advance; returns true when the job just left was the last of its slab.
-__device__ __forceinline__ bool iter_next(JobIter& it, const Ctx& c) {
+__device__ __forceinline__ void iter_next(LoadIter& it, const Ctx& c) {
   if (++it.chunk < c.ce) {
-    if (it.pa) it.pa += 16;
-    if (it.pb) it.pb += 16;
-    it.qa += 8;
-    it.qb += 8;
-    return false;
+    if (it.pa) it.pa += kChunkWords;
+    if (it.pb) it.pb += kChunkWords;
+    it.qa += kChunkCols / 16;
+    it.qb += kChunkCols / 16;
+    return;
   }
   it.chunk = c.cb;
-  bool slab_end = false;
   if (++it.pass >= c.npass) {
     it.pass = 0;
-    slab_end = true;
     if (++it.slab_i >= c.nslab) {
       it.done = true;
-      return true;
+      return;
     }
   }
   iter_point(it, c);
-  return slab_end;
+}
+// Advance; returns true when the job just left was the last of its slab.
+__device__ __forceinline__ bool iter_next(CountIter& it, const Ctx& c) {
+  if (++it.chunk < c.ce) return false;
+  it.chunk = c.cb;
+  if (++it.pass < c.npass) return false;
+  it.pass = 0;
+  if (++it.slab_i >= c.nslab) it.done = true;
+  return true;
 }
 
-template <bool VEC>
-__device__ __forceinline__ void load_chunk(Chunk& ch, const JobIter& it, const Ctx& c, int t) {
-  if (it.done) return;
-  const int64_t kw = (int64_t)it.chunk * 16 + 4 * t;  // word index within the row
-  if (VEC) {  // K % 32 == 0: a lane's four words (and two scales) are all in range or all out
-    const bool ok = kw < c.kwords;
-    ch.wa = (ok && it.pa) ? ld_stream_v4(it.pa + 4 * t) : make_uint4(0, 0, 0, 0);
-    ch.wb = (ok && it.pb) ? ld_stream_v4(it.pb + 4 * t) : make_uint4(0, 0, 0, 0);
-    ch.sa = (ok && it.pa) ? (uint32_t)__ldcs(reinterpret_cast<const unsigned short*>(it.qa + 2 * t)) : 0u;
-    ch.sb = (ok && it.pb) ? (uint32_t)__ldcs(reinterpret_cast<const unsigned short*>(it.qb + 2 * t)) : 0u;
-  } else {  // K % 32 == 16: words come in in-range pairs (one 16-column block each)
-    const bool ok0 = kw < c.kwords, ok1 = kw + 2 < c.kwords;
-    uint2 a0 = make_uint2(0, 0), a1 = a0, b0 = a0, b1 = a0;
-    uint32_t sa = 0, sb = 0;
-    if (it.pa) {
-      if (ok0) { a0 = ld_stream_v2(it.pa + 4 * t); sa = it.qa[2 * t]; }
-      if (ok1) { a1 = ld_stream_v2(it.pa + 4 * t + 2); sa |= (uint32_t)it.qa[2 * t + 1] << 8; }
+// KV = 2: K % 64 == 0 (two 128-bit loads and one 32-bit scale load per row);
+// KV = 1: K % 32 == 0 (scales as two 16-bit halves); KV = 0: K % 16 == 0
+// (words in 64-bit pairs, scales bytewise).
+template <int KV>
+__device__ __forceinline__ void load_row(const uint32_t* p, const uint8_t* q, int64_t kw0, int64_t kwords, int t,
+                                         uint4& lo, uint4& hi, uint32_t& sc) {
+  lo = make_uint4(0, 0, 0, 0);
+  hi = lo;
+  sc = 0;
+  if (!p) return;
+  if (KV >= 1) {
+    const bool ok0 = kw0 < kwords, ok1 = kw0 + 4 < kwords;
+    if (ok0) lo = ld_stream_v4(p + 8 * t);
+    if (ok1) hi = ld_stream_v4(p + 8 * t + 4);
+    if (KV == 2) {
+      if (ok1) sc = __ldcs(reinterpret_cast<const unsigned int*>(q + 4 * t));
+      else if (ok0) sc = __ldcs(reinterpret_cast<const unsigned short*>(q + 4 * t));
+    } else {
+      if (ok0) sc = __ldcs(reinterpret_cast<const unsigned short*>(q + 4 * t));
+      if (ok1) sc |= (uint32_t)__ldcs(reinterpret_cast<const unsigned short*>(q + 4 * t + 2)) << 16;
     }
-    if (it.pb) {
-      if (ok0) { b0 = ld_stream_v2(it.pb + 4 * t); sb = it.qb[2 * t]; }
-      if (ok1) { b1 = ld_stream_v2(it.pb + 4 * t + 2); sb |= (uint32_t)it.qb[2 * t + 1] << 8; }
-    }
-    ch.wa = make_uint4(a0.x, a0.y, a1.x, a1.y);
-    ch.wb = make_uint4(b0.x, b0.y, b1.x, b1.y);
-    ch.sa = sa;
-    ch.sb = sb;
-  }
-}
-
-__device__ __forceinline__ uint32_t u4get(const uint4& v, int i) {
-  return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
-}
-
-// One chunk: decode eight words per lane and run 8 k16-steps per token tile.
-// xaddr[mt] is the shared address of this lane's first staged activation
-// group for the chunk (slot g+8mt), or 0 when the slot is not in the current
-// pass. Column 32t+8q+i of a chunk is staged at offset (4q+t)*8+i, so the
-// lane's q-th 16-byte group lies 64*q bytes after its base.
-template <typename T, int MT>
-__device__ __forceinline__ void compute_chunk(const Chunk& ch, const uint32_t (&xaddr)[MT], float (&acc)[MT][4]) {
-  uint4 xv[MT][4];
+  } else {
+    uint32_t wv[8] = {0, 0, 0, 0, 0, 0, 0, 0};
 #pragma unroll
-  for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-    for (int q = 0; q < 4; ++q) xv[mt][q] = xaddr[mt] ? lds128(xaddr[mt] + 64 * q) : make_uint4(0, 0, 0, 0);
-  const uint32_t sa0 = Dt<T>::scale(ch.sa & 0xFF), sa1 = Dt<T>::scale((ch.sa >> 8) & 0xFF);
-  const uint32_t sb0 = Dt<T>::scale(ch.sb & 0xFF), sb1 = Dt<T>::scale((ch.sb >> 8) & 0xFF);
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {  // word j of the lane: columns 32t+8j..+7, k16-steps 2j and 2j+1
-    uint32_t da[4], db[4];
-    Dt<T>::decode(u4get(ch.wa, j), j < 2 ? sa0 : sa1, da);
-    Dt<T>::decode(u4get(ch.wb, j), j < 2 ? sb0 : sb1, db);
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int s = 2 * j + h;  // bytes 2h, 2h+1 of the word feed step s
-#pragma unroll
-      for (int mt = 0; mt < MT; ++mt) {
-        const uint32_t b0 = u4get(xv[mt][s >> 1], (2 * s) & 3);
-        const uint32_t b1 = u4get(xv[mt][s >> 1], (2 * s + 1) & 3);
-        MmaOp<T>::run(acc[mt], da[2 * h], db[2 * h], da[2 * h + 1], db[2 * h + 1], b0, b1);
+    for (int pr = 0; pr < 4; ++pr) {
+      if (kw0 + 2 * pr < kwords) {
+        const uint2 v = ld_stream_v2(p + 8 * t + 2 * pr);
+        wv[2 * pr] = v.x;
+        wv[2 * pr + 1] = v.y;
+        sc |= (uint32_t)q[4 * t + pr] << (8 * pr);
       }
     }
+    lo = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+    hi = make_uint4(wv[4], wv[5], wv[6], wv[7]);
   }
+}
+
+template <int KV>
+__device__ __forceinline__ void load_chunk(Chunk& ch, const LoadIter& it, const Ctx& c, int t) {
+  if (it.done) return;
+  const int64_t kw0 = (int64_t)it.chunk * kChunkWords + 8 * t;
+  load_row<KV>(it.pa, it.qa, kw0, c.kwords, t, ch.a0, ch.a1, ch.sa);
+  load_row<KV>(it.pb, it.qb, kw0, c.kwords, t, ch.b0, ch.b1, ch.sb);
 }
 
 // Shared-memory layout (dynamic):
 //   s_e[TR], s_xr[TR] (int64)      slot expert (-1 = zero row) and activation row
 //   s_pe[TR] (int), s_pm[TR] (u32) expert and slot mask of each pass
+//   lut_bf[256] (u32)              bf16x2 of scale * 2^112 per E4M3 byte
 //   xs[TR][xs_stride] (16-bit)     staged activations of this CTA's K slice
 //   red[2][128][TR] (f32)          partial sums, double-buffered per slab
-template <typename T, int MT, bool VEC>
+template <typename T, int MT, int KV>
 __device__ __forceinline__ void run_slabs(const QmvArgs& a, const Plan& pl, const Ctx& c, uint32_t xs_base,
-                                          uint32_t red_base, const int64_t* s_e, const uint32_t* s_pm,
-                                          int64_t r0, uint32_t rank) {
+                                          uint32_t red_base, uint32_t lut_bf, const int64_t* s_e,
+                                          const uint32_t* s_pm, int64_t r0, uint32_t rank) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
   const int TR = pl.TR;
-  JobIter ld, cp;
+  LoadIter ld;
+  CountIter cp;
   iter_begin(ld, c);
   iter_begin(cp, c);
-  Chunk b0, b1, b2;
-  load_chunk<VEC>(b0, ld, c, t);
-  if (!ld.done) iter_next(ld, c);
-  load_chunk<VEC>(b1, ld, c, t);
+  Chunk b0, b1;
+  load_chunk<KV>(b0, ld, c, t);
   if (!ld.done) iter_next(ld, c);
 
-  float acc[MT][4];
+  constexpr int NA = NAcc<MT>::value;
+  float acc[NA][MT][4];
 #pragma unroll
-  for (int mt = 0; mt < MT; ++mt)
+  for (int k = 0; k < NA; ++k)
 #pragma unroll
-    for (int i = 0; i < 4; ++i) acc[mt][i] = 0.f;
+    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) acc[k][mt][i] = 0.f;
   int buf = 0;
+  int pending = -1;  // slab whose cluster reduction is still to do
 
-  // staged activation address of this lane for chunk `chunk` of pass mask `pm`
   auto xaddrs = [&](uint32_t (&xa)[MT], int chunk, uint32_t pm) {
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt) {
       const int slot = g + 8 * mt;
       xa[mt] = (slot < TR && ((pm >> slot) & 1))
-                   ? xs_base + 2u * (uint32_t)(slot * pl.xs_stride + (chunk - c.cb) * 128 + 8 * t) : 0u;
+                   ? xs_base + 2u * (uint32_t)(slot * pl.xs_stride + (chunk - c.cb) * kChunkCols + 8 * t)
+                   : 0u;
     }
   };
-  // Per slab: partials -> shared, cluster barrier, reduce own rows over the cluster.
-  auto flush = [&](int slab_i) {
-    const uint32_t rb = red_base + (uint32_t)buf * (kSlabRows * TR * 4);
+  // Sum slab `si`'s partials (buffer `rb`) over the cluster for this CTA's rows.
+  auto reduce = [&](int si, uint32_t rb) {
+    cluster_reduce(a, pl.C, TR, pl.x_is_bf16, rank, c.slab0 + (int64_t)si * c.slab_step, rb, s_e, r0, kThreads);
+  };
+  const uint32_t buf_bytes = (uint32_t)(kSlabRows * TR * 4);
+  // End of slab `si`: reduce the previous slab (one cluster barrier behind, so
+  // no CTA waits for the others while it still has work), then publish this
+  // slab's partials.
+  auto flush = [&](int si) {
+    if (pending >= 0) {
+      cluster_wait();
+      reduce(pending, red_base + (uint32_t)(buf ^ 1) * buf_bytes);
+    }
+    const uint32_t rb = red_base + (uint32_t)buf * buf_bytes;
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const int row = warp * 16 + g + ((i & 2) ? 8 : 0);
         const int slot = 8 * mt + 2 * t + (i & 1);
-        if (slot < TR) asm volatile("st.shared.f32 [%0], %1;" ::"r"(rb + 4u * (row * TR + slot)), "f"(acc[mt][i]));
-        acc[mt][i] = 0.f;
+        float v = 0.f;
+#pragma unroll
+        for (int k = 0; k < NA; ++k) {
+          v += acc[k][mt][i];
+          acc[k][mt][i] = 0.f;
+        }
+        if (slot < TR) asm volatile("st.shared.f32 [%0], %1;" ::"r"(rb + 4u * (row * TR + slot)), "f"(v));
       }
     cluster_arrive();
-    cluster_wait();
-    const int64_t slab = c.slab0 + (int64_t)slab_i * c.slab_step;
-    const int rlo = (int)(rank * kSlabRows / pl.C), rhi = (int)((rank + 1) * kSlabRows / pl.C);
-    const int nrow = rhi - rlo;
-    for (int idx = threadIdx.x; idx < nrow * TR; idx += kThreads) {
-      const int slot = idx / nrow, row = rlo + idx % nrow;
-      const int64_t n = slab * kSlabRows + row, r = r0 + slot;
-      if (n >= a.N || r >= a.R) continue;
-      float v = 0.f;
-      const uint32_t off = rb + 4u * (row * TR + slot);
-      for (int q = 0; q < pl.C; ++q) v += ld_dsmem(map_rank(off, (uint32_t)q));
-      const int64_t e = s_e[slot];
-      const float out = e < 0 ? 0.f : (a.gs ? __fmul_rn(v, global_factor(a.gs, e)) : v);
-      // the output has the activation input's dtype, whatever the MMA used
-      if (pl.x_is_bf16)
-        static_cast<__nv_bfloat16*>(a.y)[r * a.N + n] = __float2bfloat16_rn(out);
-      else
-        static_cast<__half*>(a.y)[r * a.N + n] = __float2half_rn(out);
-    }
+    pending = si;
     buf ^= 1;
   };
 
   if (cp.done) {  // no weight to read (all rows zero): write the zero rows, join the barriers
     for (int s = 0; s < c.nslab; ++s) flush(s);
-    return;
+  } else {
+    while (true) {  // two register stages: one chunk in flight while one is decoded
+      {
+        load_chunk<KV>(b1, ld, c, t);
+        if (!ld.done) iter_next(ld, c);
+        uint32_t xa[MT];
+        xaddrs(xa, cp.chunk, s_pm[cp.pass]);
+        compute_chunk<T, MT>(b0, xa, acc, lut_bf);
+        const int si = cp.slab_i;
+        if (iter_next(cp, c)) flush(si);
+        if (cp.done) break;
+      }
+      {
+        load_chunk<KV>(b0, ld, c, t);
+        if (!ld.done) iter_next(ld, c);
+        uint32_t xa[MT];
+        xaddrs(xa, cp.chunk, s_pm[cp.pass]);
+        compute_chunk<T, MT>(b1, xa, acc, lut_bf);
+        const int si = cp.slab_i;
+        if (iter_next(cp, c)) flush(si);
+        if (cp.done) break;
+      }
+    }
   }
-  while (true) {
-    // three register stages: two chunks in flight while one is decoded
-    {
-      load_chunk<VEC>(b2, ld, c, t);
-      if (!ld.done) iter_next(ld, c);
-      uint32_t xa[MT];
-      xaddrs(xa, cp.chunk, s_pm[cp.pass]);
-      compute_chunk<T, MT>(b0, xa, acc);
-      const int si = cp.slab_i;
-      if (iter_next(cp, c)) flush(si);
-      if (cp.done) break;
-    }
-    {
-      load_chunk<VEC>(b0, ld, c, t);
-      if (!ld.done) iter_next(ld, c);
-      uint32_t xa[MT];
-      xaddrs(xa, cp.chunk, s_pm[cp.pass]);
-      compute_chunk<T, MT>(b1, xa, acc);
-      const int si = cp.slab_i;
-      if (iter_next(cp, c)) flush(si);
-      if (cp.done) break;
-    }
-    {
-      load_chunk<VEC>(b1, ld, c, t);
-      if (!ld.done) iter_next(ld, c);
-      uint32_t xa[MT];
-      xaddrs(xa, cp.chunk, s_pm[cp.pass]);
-      compute_chunk<T, MT>(b2, xa, acc);
-      const int si = cp.slab_i;
-      if (iter_next(cp, c)) flush(si);
-      if (cp.done) break;
-    }
+  if (pending >= 0) {
+    cluster_wait();
+    reduce(pending, red_base + (uint32_t)(buf ^ 1) * buf_bytes);
   }
 }
 
-template <int MT, bool VEC>
+template <int MT, int KV>
 __global__ void __launch_bounds__(kThreads, 2)
 qmv_cluster_kernel(const QmvArgs a, const Plan pl) {
   extern __shared__ __align__(16) uint8_t smem[];
@@ -352,7 +284,9 @@ qmv_cluster_kernel(const QmvArgs a, const Plan pl) {
   uint32_t* s_pm = reinterpret_cast<uint32_t*>(s_pe + TR);
   __shared__ int s_npass;
   const size_t meta = ((size_t)TR * 24 + 15) & ~(size_t)15;
-  uint8_t* xs = smem + meta;
+  uint32_t* lut = reinterpret_cast<uint32_t*>(smem + meta);
+  const uint32_t lut_bf = (uint32_t)__cvta_generic_to_shared(lut);
+  uint8_t* xs = smem + meta + 1024;
   const size_t xs_bytes = (size_t)TR * pl.xs_stride * 2;
   const uint32_t xs_base = (uint32_t)__cvta_generic_to_shared(xs);
   const uint32_t red_base = xs_base + (uint32_t)((xs_bytes + 15) & ~(size_t)15);
@@ -362,84 +296,11 @@ qmv_cluster_kernel(const QmvArgs a, const Plan pl) {
   const int64_t nclusters = gridDim.x / pl.C;
   const int64_t r0 = (int64_t)blockIdx.y * TR;
 
-  if (threadIdx.x < TR) {
-    const int64_t r = r0 + threadIdx.x;
-    int64_t e = -1, xr = -1;
-    if (r < a.R) {
-      e = a.rhs ? (int64_t)a.rhs[r] : 0;
-      xr = a.lhs ? (int64_t)a.lhs[r] : r;
-      if (e >= a.E || xr >= a.B) e = -1;  // zero row
-    }
-    s_e[threadIdx.x] = e;
-    s_xr[threadIdx.x] = xr;
-  }
-  __syncthreads();
-  if (threadIdx.x == 0) {  // group the slots by expert: one pass per distinct expert
-    uint32_t pending = 0;
-    for (int j = 0; j < TR; ++j)
-      if (s_e[j] >= 0) pending |= 1u << j;
-    int np = 0;
-    while (pending) {
-      const int first = __ffs(pending) - 1;
-      const int64_t e = s_e[first];
-      uint32_t m = 0;
-      for (int j = first; j < TR; ++j)
-        if (((pending >> j) & 1) && s_e[j] == e) m |= 1u << j;
-      pending &= ~m;
-      s_pe[np] = (int)e;
-      s_pm[np] = m;
-      ++np;
-    }
-    s_npass = np;  // 0 when every row of the tile is a zero row: no weight is read
-  }
-
+  lut[threadIdx.x] = e4m3_to_bf16x2_bcast_x2p112(threadIdx.x);  // kThreads == 256 entries
+  setup_slots(a, TR, r0, s_e, s_xr, s_pe, s_pm, &s_npass);
   // This CTA's K slice.
   const int cb = (int)((int64_t)pl.nchunk * rank / pl.C), ce = (int)((int64_t)pl.nchunk * (rank + 1) / pl.C);
-  // Stage activations of the slice: element at column 32t+8q+i of a chunk is
-  // stored at chunk offset (4q+t)*8+i so a lane's four 16-byte reads are
-  // contiguous with its neighbours'.
-  const int units = TR * (ce - cb) * 16;  // 8-element units
-  int inexact = 0;
-  for (int u = threadIdx.x; u < units; u += kThreads) {
-    const int slot = u / ((ce - cb) * 16);
-    const int rem = u % ((ce - cb) * 16);
-    const int ch = rem >> 4, w8 = rem & 15;  // unit within chunk: columns 8*w8 .. 8*w8+7
-    const int tq = w8 >> 2, qq = w8 & 3;     // t = w8/4, q = w8%4
-    const int64_t col = (int64_t)(cb + ch) * 128 + 8 * w8;
-    const int64_t xr = s_xr[slot];
-    uint4 v = make_uint4(0, 0, 0, 0);
-    if (s_e[slot] >= 0 && col < a.K)
-      v = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.x) + xr * a.K + col));
-    if (pl.x_is_bf16) {  // bf16 -> f16, exactness checked
-      uint32_t in[4] = {v.x, v.y, v.z, v.w}, o[4];
-#pragma unroll
-      for (int p = 0; p < 4; ++p) {
-        const float lo = __uint_as_float(in[p] << 16), hi = __uint_as_float(in[p] & 0xFFFF0000u);
-        const __half2 h = __floats2half2_rn(lo, hi);
-        const float2 back = __half22float2(h);
-        inexact |= (back.x != lo) | (back.y != hi);
-        o[p] = *reinterpret_cast<const uint32_t*>(&h);
-      }
-      v = make_uint4(o[0], o[1], o[2], o[3]);
-    }
-    const uint32_t dst = xs_base + 2u * (uint32_t)(slot * pl.xs_stride + ch * 128 + (4 * qq + tq) * 8);
-    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w));
-  }
-  const bool use_bf16 = __syncthreads_or(inexact) != 0;
-  if (use_bf16) {  // keep the exact bf16 activations instead
-    for (int u = threadIdx.x; u < units; u += kThreads) {
-      const int slot = u / ((ce - cb) * 16);
-      const int rem = u % ((ce - cb) * 16);
-      const int ch = rem >> 4, w8 = rem & 15, tq = w8 >> 2, qq = w8 & 3;
-      const int64_t col = (int64_t)(cb + ch) * 128 + 8 * w8;
-      uint4 v = make_uint4(0, 0, 0, 0);
-      if (s_e[slot] >= 0 && col < a.K)
-        v = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.x) + s_xr[slot] * a.K + col));
-      const uint32_t dst = xs_base + 2u * (uint32_t)(slot * pl.xs_stride + ch * 128 + (4 * qq + tq) * 8);
-      asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w));
-    }
-    __syncthreads();
-  }
+  const bool use_bf16 = stage_x(a, pl, cb, ce, xs_base, s_e, s_xr);
 
   Ctx c;
   c.w = a.w;
@@ -456,9 +317,9 @@ qmv_cluster_kernel(const QmvArgs a, const Plan pl) {
   c.pass_e = s_pe;
   c.row_g = (threadIdx.x >> 5) * 16 + ((threadIdx.x & 31) >> 2);
   if (use_bf16)
-    run_slabs<__nv_bfloat16, MT, VEC>(a, pl, c, xs_base, red_base, s_e, s_pm, r0, rank);
+    run_slabs<__nv_bfloat16, MT, KV>(a, pl, c, xs_base, red_base, lut_bf, s_e, s_pm, r0, rank);
   else
-    run_slabs<__half, MT, VEC>(a, pl, c, xs_base, red_base, s_e, s_pm, r0, rank);
+    run_slabs<__half, MT, KV>(a, pl, c, xs_base, red_base, lut_bf, s_e, s_pm, r0, rank);
   // Peers may still read this CTA's partials: leave together.
   cluster_arrive();
   cluster_wait();
@@ -519,7 +380,6 @@ qmv_f32_kernel(const QmvArgs a) {
     }
   }
 }
-
 int sm_count() {
   int dev = 0, sms = 152;
   cudaGetDevice(&dev);
@@ -527,60 +387,81 @@ int sm_count() {
   return sms;
 }
 
-constexpr size_t kSmemBudget = 110 * 1024;  // two CTAs per SM
+constexpr size_t kSmemPerCta = 72 * 1024;  // three CTAs per SM
+constexpr int kMaxCluster = 16;            // non-portable cluster sizes above 8
 
 size_t smem_bytes(const Plan& p) {
   const size_t meta = ((size_t)p.TR * 24 + 15) & ~(size_t)15;
   const size_t xs = (((size_t)p.TR * p.xs_stride * 2) + 15) & ~(size_t)15;
   const size_t red = (size_t)2 * kSlabRows * p.TR * 4;
-  return meta + xs + red;
+  return meta + 1024 + xs + red;
+}
+
+// Pick the K split C and the slabs per cluster. Time is modelled as (CTAs per
+// SM) x (chunks per CTA + one chunk of per-slab synchronisation), with SMs
+// holding fewer than two CTAs counted at half speed (too few warps to keep the
+// memory system busy); slices must fit the shared-memory budget.
+Plan choose_plan(Plan pl, int64_t row_tiles) {
+  const int sms = sm_count();
+  double best = 1e300;
+  Plan out = pl;
+  for (int C = 1; C <= kMaxCluster && C <= pl.nchunk; ++C) {
+    const int per = (pl.nchunk + C - 1) / C;
+    Plan p = pl;
+    p.C = C;
+    p.xs_stride = per * kChunkCols + 32;  // 512-byte multiple plus 64 bytes
+    if (smem_bytes(p) > kSmemPerCta && C < kMaxCluster && C < pl.nchunk) continue;
+    for (int64_t spc = 1; spc <= pl.slabs && spc <= 64; ++spc) {
+      const int64_t nclusters = (pl.slabs + spc - 1) / spc;
+      const int64_t ctas = nclusters * C * row_tiles;
+      const double per_sm = (double)((ctas + sms - 1) / sms);
+      const double eff = per_sm >= 2 ? 1.0 : 0.5;
+      const double tm = per_sm * (double)spc * (per + 1) / eff;
+      if (tm < best - 1e-9) {
+        best = tm;
+        out = p;
+        out.spc = (int)spc;
+      }
+    }
+  }
+  return out;
+}
+
+template <int MT, int KV>
+cudaError_t launch_kv(const QmvArgs& a, const Plan& pl, int64_t row_tiles, size_t smem, cudaStream_t st) {
+  auto kern = qmv_cluster_kernel<MT, KV>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  if (pl.C > 8) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return e;
+  }
+  const int64_t nclusters = (pl.slabs + pl.spc - 1) / pl.spc;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(nclusters * pl.C), (unsigned)row_tiles, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)pl.C;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, a, pl);
 }
 
 template <int MT>
 cudaError_t launch_cluster(const QmvArgs& a, Plan pl, cudaStream_t st) {
   pl.TR = 8 * MT;
   const int64_t row_tiles = (a.R + pl.TR - 1) / pl.TR;
-  // K split: a divisor of the chunk count up to 8 when one exists, at least
-  // four chunks per CTA.
-  int C = 1;
-  for (int c = 8; c >= 1; --c) {
-    if (pl.nchunk >= 4 * c && pl.nchunk % c == 0) { C = c; break; }
-  }
-  if (C == 1 && pl.nchunk >= 16) C = 8;
-  pl.C = C;
-  const int max_slice = (pl.nchunk + C - 1) / C;
-  // staged row stride: 128-byte multiple plus 64 bytes (conflict-free LDS.128)
-  pl.xs_stride = max_slice * 128 + 32;
-  // persistent clusters: enough CTAs to fill the GPU twice, slabs spread evenly
-  const int64_t cap = (int64_t)sm_count() * 2;
-  const int64_t want_clusters = cap / (C * row_tiles) > 0 ? cap / (C * row_tiles) : 1;
-  int64_t spc = (pl.slabs + want_clusters - 1) / want_clusters;
-  if (spc < 1) spc = 1;
-  const int64_t nclusters = (pl.slabs + spc - 1) / spc;
-  pl.spc = (int)spc;
+  pl = choose_plan(pl, row_tiles);
   const size_t smem = smem_bytes(pl);
   if (smem > 227 * 1024) return cudaErrorInvalidValue;  // excluded by qmv_supported_k
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(nclusters * C), (unsigned)row_tiles, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = (unsigned)C;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  cudaError_t e;
-  if (a.K % 32 == 0) {
-    e = cudaFuncSetAttribute(qmv_cluster_kernel<MT, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    return cudaLaunchKernelEx(&cfg, qmv_cluster_kernel<MT, true>, a, pl);
-  }
-  e = cudaFuncSetAttribute(qmv_cluster_kernel<MT, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
-  return cudaLaunchKernelEx(&cfg, qmv_cluster_kernel<MT, false>, a, pl);
+  if (a.K % 64 == 0) return launch_kv<MT, 2>(a, pl, row_tiles, smem, st);
+  if (a.K % 32 == 0) return launch_kv<MT, 1>(a, pl, row_tiles, smem, st);
+  return launch_kv<MT, 0>(a, pl, row_tiles, smem, st);
 }
 
 }  // namespace
@@ -591,20 +472,20 @@ cudaError_t launch_qmv(const QmvArgs& a, int xdt, cudaStream_t st) {
     qmv_f32_kernel<<<grid, kThreads, 0, st>>>(a);
     return cudaGetLastError();
   }
+  if (qmv_tma_supported(a, xdt)) return launch_qmv_tma(a, xdt, st);
   Plan pl{};
-  pl.nchunk = (int)((a.K + 127) / 128);
+  pl.nchunk = (int)((a.K + kChunkCols - 1) / kChunkCols);
   pl.slabs = (a.N + kSlabRows - 1) / kSlabRows;
   pl.x_is_bf16 = xdt == kBF16;
   // Rows per CTA tile: 8 for one- to eight-row calls and for gather calls,
-  // 16 otherwise, unless the staged slice would not fit.
+  // 16 otherwise.
   const bool wide = a.rhs == nullptr && a.R > 8;
-  Plan probe = pl;
-  probe.TR = 16;
-  probe.xs_stride = ((pl.nchunk + 7) / 8) * 128 + 32;
-  if (wide && smem_bytes(probe) <= kSmemBudget) return launch_cluster<2>(a, pl, st);
+  if (wide) return launch_cluster<2>(a, pl, st);
   return launch_cluster<1>(a, pl, st);
 }
 
+// The staged slice (eight rows, K / 16 columns per CTA of a 16-CTA cluster)
+// must fit one CTA's shared memory.
 bool qmv_supported_k(int64_t K) { return K <= kQmvMaxK; }
 
 }  // namespace nvfp4

@@ -247,3 +247,42 @@ def test_qmm_qmv_bf16_values_outside_f16(nv, special):
     # rows without the special value are unaffected by it
     ref0 = O.qmm(x[:1].double().numpy(), w, s, None)
     assert rel_err(y[:1], ref0) <= TOL["bf16"]
+
+
+@pytest.mark.parametrize("count", [1, 40, 200])
+def test_qmm_qmv_tiny_activations_exact(nv, count):
+    """Rows whose only nonzero activations are below f16's normal range.
+
+    With up to 64 such values in a CTA's slice the f16 path adds their exact
+    residuals (x - f16(x)) times the weights in f32; with more it stages bf16.
+    Either way the output must match the oracle to output rounding; rounding x
+    to f16 alone would be tens of percent off here.
+    """
+    M, N, K = 2, 384, 512
+    w, s = weights(41, N, K)
+    g = synth.rng(42 + count)
+    x = torch.zeros((M, K), dtype=torch.bfloat16)
+    cols = g.choice(K, size=min(count, K), replace=False)
+    mags = np.exp2(g.uniform(-40, -18, size=cols.size)) * g.choice([-1.0, 1.0], size=cols.size)
+    x[0, torch.from_numpy(cols)] = torch.from_numpy(mags.astype(np.float32)).to(torch.bfloat16)
+    x[1] = synth.activations(g, (1, K), "bf16")[0]
+    y = nv.qmm(x.cuda(), u32_to_dev(w), u8_to_dev(s), route="qmv")
+    ref = O.qmm(x.double().numpy(), w, s, None)
+    assert rel_err(y[:1], ref[:1]) <= TOL["bf16"], "tiny-only row"
+    assert rel_err(y[1:], ref[1:]) <= TOL["bf16"], "normal row"
+
+
+def test_gather_tiny_activations_exact(nv):
+    E, N, K, B = 4, 128, 512, 6
+    w, s = weights(43, E, N, K)
+    g = synth.rng(44)
+    x = synth.activations(g, (B, K), "bf16")
+    x[2] = 0
+    cols = g.choice(K, size=30, replace=False)
+    x[2, torch.from_numpy(cols)] = torch.from_numpy(np.exp2(g.uniform(-35, -20, size=30)).astype(np.float32)).to(torch.bfloat16)
+    rhs = np.array([1, 3, 1, 0, 2, 3, 1], dtype=np.uint32)
+    lhs = np.array([2, 2, 0, 2, 5, 1, 2], dtype=np.uint32)
+    y = nv.gather_qmm(x.cuda(), u32_to_dev(w), u8_to_dev(s), u32_to_dev(rhs), u32_to_dev(lhs))
+    ref = O.gather_qmm(x.double().numpy(), lhs, rhs, w, s)
+    for r in range(len(rhs)):
+        assert rel_err(y[r:r + 1], ref[r:r + 1]) <= TOL["bf16"], f"row {r}"
