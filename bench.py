@@ -554,7 +554,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-routes", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
-    ap.add_argument("--cpu-rows", type=int, default=640)
+    ap.add_argument("--cpu-rows", type=int, default=6144)
     ap.add_argument("--ref-rows", type=int, default=32)
     ap.add_argument("--case", choices=["qmv_small", "qmv_shapes"], default=None,
                     help="run one small profiling case instead of the benchmark")

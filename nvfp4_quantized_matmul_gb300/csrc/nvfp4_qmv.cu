@@ -176,7 +176,7 @@ __device__ __forceinline__ void load_chunk(Chunk& ch, const LoadIter& it, const 
 //   red[2][128][TR] (f32)          partial sums, double-buffered per slab
 template <typename T, int MT, int KV>
 __device__ __forceinline__ void run_slabs(const QmvArgs& a, const Plan& pl, const Ctx& c, uint32_t xs_base,
-                                          uint32_t red_base, uint32_t lut_bf, const int64_t* s_e,
+                                          uint32_t red_base, uint32_t lut_bf, uint32_t zero_base, const int64_t* s_e,
                                           const uint32_t* s_pm, int64_t r0, uint32_t rank) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
   const int TR = pl.TR;
@@ -205,12 +205,14 @@ __device__ __forceinline__ void run_slabs(const QmvArgs& a, const Plan& pl, cons
       const int slot = g + 8 * mt;
       xa[mt] = (slot < TR && ((pm >> slot) & 1))
                    ? xs_base + 2u * (uint32_t)(slot * pl.xs_stride + (chunk - c.cb) * kChunkCols + 8 * t)
-                   : 0u;
+                   : zero_base + 16u * (uint32_t)t;
     }
   };
   // Sum slab `si`'s partials (buffer `rb`) over the cluster for this CTA's rows.
-  auto reduce = [&](int si, uint32_t rb) {
-    cluster_reduce(a, pl.C, TR, pl.x_is_bf16, rank, c.slab0 + (int64_t)si * c.slab_step, rb, s_e, r0, kThreads);
+  ReduceOut red_out;
+  auto gather = [&](uint32_t rb) { cluster_gather(pl.C, TR, rank, rb, kThreads, red_out); };
+  auto store = [&](int si) {
+    cluster_store(a, pl.C, TR, pl.x_is_bf16, rank, c.slab0 + (int64_t)si * c.slab_step, s_e, r0, kThreads, red_out);
   };
   const uint32_t buf_bytes = (uint32_t)(kSlabRows * TR * 4);
   // End of slab `si`: reduce the previous slab (one cluster barrier behind, so
@@ -219,7 +221,7 @@ __device__ __forceinline__ void run_slabs(const QmvArgs& a, const Plan& pl, cons
   auto flush = [&](int si) {
     if (pending >= 0) {
       cluster_wait();
-      reduce(pending, red_base + (uint32_t)(buf ^ 1) * buf_bytes);
+      gather(red_base + (uint32_t)(buf ^ 1) * buf_bytes);
     }
     const uint32_t rb = red_base + (uint32_t)buf * buf_bytes;
 #pragma unroll
@@ -237,6 +239,7 @@ __device__ __forceinline__ void run_slabs(const QmvArgs& a, const Plan& pl, cons
         if (slot < TR) asm volatile("st.shared.f32 [%0], %1;" ::"r"(rb + 4u * (row * TR + slot)), "f"(v));
       }
     cluster_arrive();
+    if (pending >= 0) store(pending);  // after the arrive: its release does not wait for these stores
     pending = si;
     buf ^= 1;
   };
@@ -269,7 +272,8 @@ __device__ __forceinline__ void run_slabs(const QmvArgs& a, const Plan& pl, cons
   }
   if (pending >= 0) {
     cluster_wait();
-    reduce(pending, red_base + (uint32_t)(buf ^ 1) * buf_bytes);
+    gather(red_base + (uint32_t)(buf ^ 1) * buf_bytes);
+    store(pending);
   }
 }
 
@@ -286,7 +290,8 @@ qmv_cluster_kernel(const QmvArgs a, const Plan pl) {
   const size_t meta = ((size_t)TR * 24 + 15) & ~(size_t)15;
   uint32_t* lut = reinterpret_cast<uint32_t*>(smem + meta);
   const uint32_t lut_bf = (uint32_t)__cvta_generic_to_shared(lut);
-  uint8_t* xs = smem + meta + 1024;
+  const uint32_t zero_base = lut_bf + 1024;  // 512 zero bytes: activations of slots outside a pass
+  uint8_t* xs = smem + meta + 1024 + 512;
   const size_t xs_bytes = (size_t)TR * pl.xs_stride * 2;
   const uint32_t xs_base = (uint32_t)__cvta_generic_to_shared(xs);
   const uint32_t red_base = xs_base + (uint32_t)((xs_bytes + 15) & ~(size_t)15);
@@ -297,6 +302,7 @@ qmv_cluster_kernel(const QmvArgs a, const Plan pl) {
   const int64_t r0 = (int64_t)blockIdx.y * TR;
 
   lut[threadIdx.x] = e4m3_to_bf16x2_bcast_x2p112(threadIdx.x);  // kThreads == 256 entries
+  if (threadIdx.x < 128) lut[256 + threadIdx.x] = 0u;            // the zero block follows the table
   setup_slots(a, TR, r0, s_e, s_xr, s_pe, s_pm, &s_npass);
   // This CTA's K slice.
   const int cb = (int)((int64_t)pl.nchunk * rank / pl.C), ce = (int)((int64_t)pl.nchunk * (rank + 1) / pl.C);
@@ -317,9 +323,9 @@ qmv_cluster_kernel(const QmvArgs a, const Plan pl) {
   c.pass_e = s_pe;
   c.row_g = (threadIdx.x >> 5) * 16 + ((threadIdx.x & 31) >> 2);
   if (use_bf16)
-    run_slabs<__nv_bfloat16, MT, KV>(a, pl, c, xs_base, red_base, lut_bf, s_e, s_pm, r0, rank);
+    run_slabs<__nv_bfloat16, MT, KV>(a, pl, c, xs_base, red_base, lut_bf, zero_base, s_e, s_pm, r0, rank);
   else
-    run_slabs<__half, MT, KV>(a, pl, c, xs_base, red_base, lut_bf, s_e, s_pm, r0, rank);
+    run_slabs<__half, MT, KV>(a, pl, c, xs_base, red_base, lut_bf, zero_base, s_e, s_pm, r0, rank);
   // Peers may still read this CTA's partials: leave together.
   cluster_arrive();
   cluster_wait();
@@ -394,7 +400,7 @@ size_t smem_bytes(const Plan& p) {
   const size_t meta = ((size_t)p.TR * 24 + 15) & ~(size_t)15;
   const size_t xs = (((size_t)p.TR * p.xs_stride * 2) + 15) & ~(size_t)15;
   const size_t red = (size_t)2 * kSlabRows * p.TR * 4;
-  return meta + 1024 + xs + red;
+  return meta + 1024 + 512 + xs + red;
 }
 
 // Pick the K split C and the slabs per cluster. Time is modelled as (CTAs per

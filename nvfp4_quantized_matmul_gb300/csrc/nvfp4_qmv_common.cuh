@@ -59,23 +59,25 @@ __device__ __forceinline__ float4 ld_dsmem4(uint32_t addr) {
   return v;
 }
 
-// Cluster reduction of one slab: this CTA (rank `rank` of C) owns rows
-// [rank*128/C, (rank+1)*128/C) of the slab; partial sums sit at
-// rb + 4*(row*TR + slot) in every CTA of the cluster. Each item is one row and
-// four consecutive slots: all C remote 16-byte loads are issued before any is
-// summed (in groups of four peers), so the distributed-shared-memory latency
-// is paid once per group. Writes factor * sum (or +0.0 for zero rows) in the
-// activation dtype. Kept out of line: it runs once per slab and must not add
-// its registers to the main loop's.
-static __device__ __noinline__ void cluster_reduce(const QmvArgs& a, int C, int TR, int x_is_bf16, uint32_t rank,
-                                               int64_t slab, uint32_t rb, const int64_t* s_e, int64_t r0,
-                                               int nthreads) {
+// Cluster reduction of one slab, split in two so that the output stores can
+// be issued after the next cluster arrive (a release fence would otherwise
+// wait for them). This CTA (rank `rank` of C) owns rows [rank*128/C,
+// (rank+1)*128/C) of the slab; partial sums sit at rb + 4*(row*TR + slot) in
+// every CTA of the cluster. An item is one row and four consecutive slots; a
+// thread holds at most two items (nrow * TR/4 <= 512 for 256 threads). All
+// remote 16-byte loads of a group of four peers are issued before any is
+// summed, so the distributed-shared-memory latency is paid once per group.
+struct ReduceOut {
+  float v[2][4];
+  int n;
+};
+static __device__ __noinline__ void cluster_gather(int C, int TR, uint32_t rank, uint32_t rb, int nthreads,
+                                                   ReduceOut& o) {
   const int rlo = (int)(rank * kSlabRows / C), rhi = (int)((rank + 1) * kSlabRows / C);
   const int nrow = rhi - rlo, nq = TR / 4;
-  for (int idx = threadIdx.x; idx < nrow * nq; idx += nthreads) {
+  o.n = 0;
+  for (int idx = threadIdx.x, k = 0; idx < nrow * nq && k < 2; idx += nthreads, ++k) {
     const int quad = idx / nrow, row = rlo + idx % nrow;
-    const int64_t n = slab * kSlabRows + row;
-    if (n >= a.N) continue;
     const uint32_t off = rb + 4u * (uint32_t)(row * TR + 4 * quad);
     float v[4] = {0.f, 0.f, 0.f, 0.f};
     for (int q0 = 0; q0 < C; q0 += 4) {
@@ -93,12 +95,28 @@ static __device__ __noinline__ void cluster_reduce(const QmvArgs& a, int C, int 
         }
     }
 #pragma unroll
+    for (int j = 0; j < 4; ++j) o.v[k][j] = v[j];
+    o.n = k + 1;
+  }
+}
+// Writes factor * sum (or +0.0 for zero rows) in the activation dtype.
+static __device__ __noinline__ void cluster_store(const QmvArgs& a, int C, int TR, int x_is_bf16, uint32_t rank,
+                                                  int64_t slab, const int64_t* s_e, int64_t r0, int nthreads,
+                                                  const ReduceOut& o) {
+  const int rlo = (int)(rank * kSlabRows / C), rhi = (int)((rank + 1) * kSlabRows / C);
+  const int nrow = rhi - rlo;
+  for (int k = 0; k < o.n; ++k) {
+    const int idx = threadIdx.x + k * nthreads;
+    const int quad = idx / nrow, row = rlo + idx % nrow;
+    const int64_t n = slab * kSlabRows + row;
+    if (n >= a.N) continue;
+#pragma unroll
     for (int j = 0; j < 4; ++j) {
       const int slot = 4 * quad + j;
       const int64_t r = r0 + slot;
       if (r >= a.R) continue;
       const int64_t e = s_e[slot];
-      const float out = e < 0 ? 0.f : (a.gs ? __fmul_rn(v[j], global_factor(a.gs, e)) : v[j]);
+      const float out = e < 0 ? 0.f : (a.gs ? __fmul_rn(o.v[k][j], global_factor(a.gs, e)) : o.v[k][j]);
       // the output has the activation input's dtype, whatever the MMA used
       if (x_is_bf16)
         static_cast<__nv_bfloat16*>(a.y)[r * a.N + n] = __float2bfloat16_rn(out);
@@ -128,6 +146,7 @@ struct Plan {
   int xs_stride;    // staged activation row stride in 16-bit elements
   int x_is_bf16;    // activation input is bf16 (else f16)
   int stages;       // depth of the TMA stage ring (TMA-fed kernel only)
+  int xs_slots;     // staged activation rows actually allocated (min(TR, R))
 };
 
 // One lane's share of a chunk: words 8t..8t+7 of rows g and g+8, and the
@@ -154,6 +173,25 @@ template <> __device__ __forceinline__ uint32_t scale_op<__nv_bfloat16>(uint32_t
   return v;
 }
 
+// Block-scale operands for the two 16-column groups of one half-chunk
+// (scale bytes 2*half and 2*half+1 of the lane's scale word), each broadcast
+// to both halves of a packed register. f16: one two-byte conversion and two
+// byte permutes; bf16: two lookups of scale * 2^112 in the shared table.
+template <typename T>
+__device__ __forceinline__ void scale_pair(uint32_t sbytes, int half, uint32_t lut_bf, uint32_t& s0, uint32_t& s1);
+template <>
+__device__ __forceinline__ void scale_pair<__half>(uint32_t sbytes, int half, uint32_t, uint32_t& s0, uint32_t& s1) {
+  const uint32_t h = e4m3x2_to_f16x2(sbytes >> (16 * half));
+  s0 = __byte_perm(h, 0, 0x1010);
+  s1 = __byte_perm(h, 0, 0x3232);
+}
+template <>
+__device__ __forceinline__ void scale_pair<__nv_bfloat16>(uint32_t sbytes, int half, uint32_t lut_bf, uint32_t& s0,
+                                                          uint32_t& s1) {
+  s0 = scale_op<__nv_bfloat16>(sbytes, 2 * half, lut_bf);
+  s1 = scale_op<__nv_bfloat16>(sbytes, 2 * half + 1, lut_bf);
+}
+
 // One chunk: 16 k16-steps. Lane t's word j holds columns 64t+8j..+7; step s
 // uses bytes 2h, 2h+1 (h = s & 1) of word s/2, i.e. columns 64t+4s+0..3 in
 // A slots {2t, 2t+1, 2t+8, 2t+9}. The staged activations put column
@@ -170,16 +208,18 @@ __device__ __forceinline__ void compute_chunk(const Chunk& ch, const uint32_t (&
   constexpr int NA = NAcc<MT>::value;
 #pragma unroll
   for (int half = 0; half < 2; ++half) {  // words 4*half .. 4*half+3
+    // xaddr points at a zeroed block for slots outside the pass, so the
+    // loads are unconditional
     uint4 xv[MT][4];
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
-      for (int q = 0; q < 4; ++q)
-        xv[mt][q] = xaddr[mt] ? lds128(xaddr[mt] + 64 * (4 * half + q)) : make_uint4(0, 0, 0, 0);
+      for (int q = 0; q < 4; ++q) xv[mt][q] = lds128(xaddr[mt] + 64 * (4 * half + q));
     const uint4& wa = half ? ch.a1 : ch.a0;
     const uint4& wb = half ? ch.b1 : ch.b0;
-    const uint32_t sa0 = scale_op<T>(ch.sa, 2 * half, lut_bf), sa1 = scale_op<T>(ch.sa, 2 * half + 1, lut_bf);
-    const uint32_t sb0 = scale_op<T>(ch.sb, 2 * half, lut_bf), sb1 = scale_op<T>(ch.sb, 2 * half + 1, lut_bf);
+    uint32_t sa0, sa1, sb0, sb1;
+    scale_pair<T>(ch.sa, half, lut_bf, sa0, sa1);
+    scale_pair<T>(ch.sb, half, lut_bf, sb0, sb1);
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       uint32_t da[4], db[4];
@@ -331,9 +371,10 @@ constexpr int kMaxCorr = 64;
 template <bool kNamed>
 __device__ __forceinline__ int stage_x_corr(const QmvArgs& a, const Plan& pl, int cb, int ce, uint32_t xs_base,
                                             const int64_t* s_e, const int64_t* s_xr, Corr* corr, int* n_corr) {
-  const int TR = pl.TR;
+  // only the allocated slots (min(TR, R)) are staged; the others never hold
+  // a row of this tile and are never read
   const int upc = kChunkCols / 8;
-  const int units = TR * (ce - cb) * upc;
+  const int units = pl.xs_slots * (ce - cb) * upc;
   const int nthr = kNamed ? 256 : (int)blockDim.x;
   int hard = 0;
   for (int u = threadIdx.x; u < units; u += nthr) {

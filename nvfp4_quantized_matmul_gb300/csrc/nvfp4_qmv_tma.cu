@@ -28,7 +28,7 @@ using namespace qmv;
 
 constexpr int kConsumerWarps = kWarps;                     // 8 warps x 16 rows = one 128-row slab
 constexpr int kTmaThreads = (kConsumerWarps + 1) * 32;     // plus one producer warp
-constexpr int kMaxStages = 3;  // ring depth: the plan picks 2 or 3
+constexpr int kMaxStages = 4;  // ring depth: the plan picks 2 to 4
 constexpr uint32_t kWStage = kSlabRows * kChunkWords * 4;  // 16 KB of packed words
 constexpr uint32_t kSStage = kSlabRows * (kChunkCols / 16);  // 2 KB of scale bytes
 constexpr uint64_t kWaitLimitNs = 2000000000ull;          // 2 s
@@ -169,8 +169,9 @@ __device__ void produce(const TmaCtx& c, const CUtensorMap* wmap, const CUtensor
 
 template <typename T, int MT>
 __device__ void consume(const QmvArgs& a, const Plan& pl, const TmaCtx& c, uint32_t wst, uint32_t sst, uint32_t bars,
-                        volatile int* abort_flag, uint32_t xs_base, uint32_t red_base, uint32_t lut_bf,
-                        const int64_t* s_e, int64_t r0, uint32_t rank, const Corr* corr, int ncorr) {
+                        volatile int* abort_flag, uint32_t xs_base, uint32_t zero_base, uint32_t red_base,
+                        uint32_t lut_bf, const int64_t* s_e, int64_t r0, uint32_t rank, const Corr* corr,
+                        int ncorr) {
   const int kStages = pl.stages;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
   const int TR = pl.TR;
@@ -195,19 +196,23 @@ __device__ void consume(const QmvArgs& a, const Plan& pl, const TmaCtx& c, uint3
   int s = 0;        // ring stage of the next job
   uint32_t ph = 0;  // its phase parity
 
-  auto reduce = [&](int si, uint32_t rb) {
-    cluster_reduce(a, pl.C, TR, pl.x_is_bf16, rank, c.slab0 + (int64_t)si * c.slab_step, rb, s_e, r0, kConsumerWarps * 32);
+  ReduceOut red_out;
+  auto gather = [&](uint32_t rb) { cluster_gather(pl.C, TR, rank, rb, kConsumerWarps * 32, red_out); };
+  auto store = [&](int si) {
+    cluster_store(a, pl.C, TR, pl.x_is_bf16, rank, c.slab0 + (int64_t)si * c.slab_step, s_e, r0, kConsumerWarps * 32, red_out);
   };
 
   for (int si = 0; si < c.nslab; ++si) {
     for (int p = 0; p < c.npass; ++p) {
       const uint32_t pm = c.pass_m[p];
-      uint32_t xa[MT];
+      uint32_t xa[MT], xstep[MT];
       int cur = 0;  // next residual correction (sorted by column)
 #pragma unroll
       for (int mt = 0; mt < MT; ++mt) {
         const int slot = g + 8 * mt;
-        xa[mt] = (slot < TR && ((pm >> slot) & 1)) ? xs_base + 2u * (uint32_t)(slot * pl.xs_stride + 8 * t) : 0u;
+        const bool in = slot < TR && ((pm >> slot) & 1);
+        xa[mt] = in ? xs_base + 2u * (uint32_t)(slot * pl.xs_stride + 8 * t) : zero_base + 16u * (uint32_t)t;
+        xstep[mt] = in ? 2u * kChunkCols : 0u;  // bytes per chunk (0: stay on the zero block)
       }
       for (int ch = c.cb; ch < c.ce; ++ch) {
         const int cs = s;          // this job's stage
@@ -218,7 +223,7 @@ __device__ void consume(const QmvArgs& a, const Plan& pl, const TmaCtx& c, uint3
         }
         uint32_t xc[MT];
 #pragma unroll
-        for (int mt = 0; mt < MT; ++mt) xc[mt] = xa[mt] ? xa[mt] + 2u * (uint32_t)((ch - c.cb) * kChunkCols) : 0u;
+        for (int mt = 0; mt < MT; ++mt) xc[mt] = xa[mt] + xstep[mt] * (uint32_t)(ch - c.cb);
         if (!wait_bar_warp(bars + 8 * cs, cph, abort_flag, 12, &g_qmv_error)) continue;  // stage full
         const uint32_t w = wst + (uint32_t)cs * kWStage, q = sst + (uint32_t)cs * kSStage;
         Chunk chk;
@@ -263,7 +268,7 @@ __device__ void consume(const QmvArgs& a, const Plan& pl, const TmaCtx& c, uint3
     // end of slab: reduce the previous slab over the cluster, publish this one
     if (pending >= 0) {
       cluster_wait();
-      reduce(pending, red_base + (uint32_t)(buf ^ 1) * buf_bytes);
+      gather(red_base + (uint32_t)(buf ^ 1) * buf_bytes);
     }
     const uint32_t rb = red_base + (uint32_t)buf * buf_bytes;
 #pragma unroll
@@ -281,12 +286,14 @@ __device__ void consume(const QmvArgs& a, const Plan& pl, const TmaCtx& c, uint3
         if (slot < TR) asm volatile("st.shared.f32 [%0], %1;" ::"r"(rb + 4u * (row * TR + slot)), "f"(v));
       }
     cluster_arrive();
+    if (pending >= 0) store(pending);  // after the arrive: its release does not wait for these stores
     pending = si;
     buf ^= 1;
   }
   if (pending >= 0) {
     cluster_wait();
-    reduce(pending, red_base + (uint32_t)(buf ^ 1) * buf_bytes);
+    gather(red_base + (uint32_t)(buf ^ 1) * buf_bytes);
+    store(pending);
   }
 }
 
@@ -295,9 +302,9 @@ __device__ void consume(const QmvArgs& a, const Plan& pl, const TmaCtx& c, uint3
 size_t tma_smem_bytes(const Plan& p) {
   const size_t ring = (size_t)p.stages * (kWStage + kSStage) + 8 * 2 * kMaxStages + 16;
   const size_t meta = ((size_t)p.TR * 24 + 15) & ~(size_t)15;
-  const size_t xs = (((size_t)p.TR * p.xs_stride * 2) + 15) & ~(size_t)15;
+  const size_t xs = (((size_t)p.xs_slots * p.xs_stride * 2) + 15) & ~(size_t)15;
   const size_t red = (size_t)2 * kSlabRows * p.TR * 4;
-  return 1024 + ring + meta + 1024 + xs + red;
+  return 1024 + ring + meta + 1024 + 512 + xs + red;
 }
 
 template <int MT>
@@ -322,8 +329,9 @@ qmv_tma_kernel(const QmvArgs a, const Plan pl, const __grid_constant__ CUtensorM
   const size_t meta = ((size_t)TR * 24 + 15) & ~(size_t)15;
   uint32_t* lut = reinterpret_cast<uint32_t*>(after + meta);
   const uint32_t lut_bf = (uint32_t)__cvta_generic_to_shared(lut);
-  const uint32_t xs_base = lut_bf + 1024;
-  const size_t xs_bytes = (size_t)TR * pl.xs_stride * 2;
+  const uint32_t zero_base = lut_bf + 1024;  // 512 zero bytes: activations of slots outside a pass
+  const uint32_t xs_base = zero_base + 512;
+  const size_t xs_bytes = (size_t)pl.xs_slots * pl.xs_stride * 2;
   const uint32_t red_base = xs_base + (uint32_t)((xs_bytes + 15) & ~(size_t)15);
   __shared__ Corr s_corr[kMaxCorr];
   __shared__ int s_ncorr;
@@ -348,6 +356,7 @@ qmv_tma_kernel(const QmvArgs a, const Plan pl, const __grid_constant__ CUtensorM
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&smap)) : "memory");
   }
   if (threadIdx.x < 256) lut[threadIdx.x] = e4m3_to_bf16x2_bcast_x2p112(threadIdx.x);
+  if (threadIdx.x < 128) lut[256 + threadIdx.x] = 0u;  // the zero block follows the table
   setup_slots(a, TR, r0, s_e, s_xr, s_pe, s_pm, &s_npass);  // ends with __syncthreads
 
   const int cb = (int)((int64_t)pl.nchunk * rank / pl.C), ce = (int)((int64_t)pl.nchunk * (rank + 1) / pl.C);
@@ -374,11 +383,11 @@ qmv_tma_kernel(const QmvArgs a, const Plan pl, const __grid_constant__ CUtensorM
   const bool use_bf16 = mode == 2;
   const int ncorr = mode == 1 ? s_ncorr : 0;
   if (use_bf16) {
-    consume<__nv_bfloat16, MT>(a, pl, c, wst, sst, bars, abort_flag, xs_base, red_base, lut_bf, s_e, r0, rank,
-                               s_corr, 0);
+    consume<__nv_bfloat16, MT>(a, pl, c, wst, sst, bars, abort_flag, xs_base, zero_base, red_base, lut_bf, s_e, r0,
+                               rank, s_corr, 0);
   } else {
-    consume<__half, MT>(a, pl, c, wst, sst, bars, abort_flag, xs_base, red_base, lut_bf, s_e, r0, rank, s_corr,
-                        ncorr);
+    consume<__half, MT>(a, pl, c, wst, sst, bars, abort_flag, xs_base, zero_base, red_base, lut_bf, s_e, r0, rank,
+                        s_corr, ncorr);
   }
   // Peers may still read this CTA's partials: leave together.
   cluster_arrive();
@@ -428,7 +437,7 @@ Plan tma_plan(Plan pl, int64_t row_tiles, OccFn occupancy) {
     const size_t smem = tma_smem_bytes(p);
     const int occ = occupancy(smem);  // 0 when it does not fit at all
     if (occ < 1) continue;
-    const double depth = stages >= 3 ? 1.0 : 1.1;  // a shallower ring hides less latency
+    const double depth = stages >= 4 ? 1.0 : stages == 3 ? 1.05 : 1.15;  // shallower rings hide less latency
     for (int64_t spc = 1; spc <= pl.slabs && spc <= 64; ++spc) {
       const int64_t ctas = (pl.slabs + spc - 1) / spc * C * row_tiles;
       // per slab: the chunks, a cluster sync worth one chunk (two with 16
@@ -488,7 +497,7 @@ cudaError_t launch_mt(const QmvArgs& a, Plan pl, int64_t row_tiles, cudaStream_t
   static std::mutex mu;
   static std::map<Key, Plan> cache;
   static std::map<int, int> max_dyn_of_dev;
-  const Key key{dev, a.K, a.N, a.E, row_tiles, pl.x_is_bf16};
+  const Key key{dev, a.K, a.N, a.E, row_tiles * 64 + pl.xs_slots, pl.x_is_bf16};
   {
     std::lock_guard<std::mutex> lock(mu);
     auto it = cache.find(key);
@@ -554,11 +563,14 @@ cudaError_t launch_qmv_tma(const QmvArgs& a, int xdt, cudaStream_t st) {
   pl.slabs = (a.N + kSlabRows - 1) / kSlabRows;
   pl.x_is_bf16 = xdt == kBF16;
   const bool wide = a.rhs == nullptr && a.R > 8;
+  // Only the slots that exist get staging space (a one-row call stages one row).
   if (wide) {
     pl.TR = 16;
+    pl.xs_slots = (int)(a.R < 16 ? a.R : 16);
     return launch_mt<2>(a, pl, (a.R + 15) / 16, st);
   }
   pl.TR = 8;
+  pl.xs_slots = (int)(a.R < 8 ? a.R : 8);
   return launch_mt<1>(a, pl, (a.R + 7) / 8, st);
 }
 
