@@ -210,9 +210,10 @@ __device__ __forceinline__ void run_slabs(const QmvArgs& a, const Plan& pl, cons
   };
   // Sum slab `si`'s partials (buffer `rb`) over the cluster for this CTA's rows.
   ReduceOut red_out;
-  auto gather = [&](uint32_t rb) { cluster_gather(pl.C, TR, rank, rb, kThreads, red_out); };
+  auto gather = [&](uint32_t rb) { cluster_gather(pl.C, TR, rank, rb, threadIdx.x, kThreads, red_out); };
   auto store = [&](int si) {
-    cluster_store(a, pl.C, TR, pl.x_is_bf16, rank, c.slab0 + (int64_t)si * c.slab_step, s_e, r0, kThreads, red_out);
+    cluster_store(a, pl.C, TR, pl.x_is_bf16, rank, c.slab0 + (int64_t)si * c.slab_step, s_e, r0, threadIdx.x,
+                  kThreads, red_out);
   };
   const uint32_t buf_bytes = (uint32_t)(kSlabRows * TR * 4);
   // End of slab `si`: reduce the previous slab (one cluster barrier behind, so

@@ -71,12 +71,12 @@ struct ReduceOut {
   float v[2][4];
   int n;
 };
-static __device__ __noinline__ void cluster_gather(int C, int TR, uint32_t rank, uint32_t rb, int nthreads,
+static __device__ __noinline__ void cluster_gather(int C, int TR, uint32_t rank, uint32_t rb, int tid, int nthreads,
                                                    ReduceOut& o) {
   const int rlo = (int)(rank * kSlabRows / C), rhi = (int)((rank + 1) * kSlabRows / C);
   const int nrow = rhi - rlo, nq = TR / 4;
   o.n = 0;
-  for (int idx = threadIdx.x, k = 0; idx < nrow * nq && k < 2; idx += nthreads, ++k) {
+  for (int idx = tid, k = 0; idx < nrow * nq && k < 2; idx += nthreads, ++k) {
     const int quad = idx / nrow, row = rlo + idx % nrow;
     const uint32_t off = rb + 4u * (uint32_t)(row * TR + 4 * quad);
     float v[4] = {0.f, 0.f, 0.f, 0.f};
@@ -101,12 +101,12 @@ static __device__ __noinline__ void cluster_gather(int C, int TR, uint32_t rank,
 }
 // Writes factor * sum (or +0.0 for zero rows) in the activation dtype.
 static __device__ __noinline__ void cluster_store(const QmvArgs& a, int C, int TR, int x_is_bf16, uint32_t rank,
-                                                  int64_t slab, const int64_t* s_e, int64_t r0, int nthreads,
+                                                  int64_t slab, const int64_t* s_e, int64_t r0, int tid, int nthreads,
                                                   const ReduceOut& o) {
   const int rlo = (int)(rank * kSlabRows / C), rhi = (int)((rank + 1) * kSlabRows / C);
   const int nrow = rhi - rlo;
   for (int k = 0; k < o.n; ++k) {
-    const int idx = threadIdx.x + k * nthreads;
+    const int idx = tid + k * nthreads;
     const int quad = idx / nrow, row = rlo + idx % nrow;
     const int64_t n = slab * kSlabRows + row;
     if (n >= a.N) continue;
@@ -333,24 +333,22 @@ __device__ __forceinline__ bool stage_x(const QmvArgs& a, const Plan& pl, int cb
   return use_bf16;
 }
 
-// Block-wide (kNamed == false) or consumer-warps-only (named barrier 1 over
-// the first 256 threads) synchronisation for the staging step.
-template <bool kNamed>
+// Synchronisation of the staging threads: named barrier 1 over kCount
+// threads (the staging group), with an OR-reduction variant.
+template <int kCount>
 __device__ __forceinline__ int sync_or(int pred) {
-  if (!kNamed) return __syncthreads_or(pred);
   uint32_t r;
   asm volatile(
-      "{\n\t.reg .pred p, q;\n\tsetp.ne.s32 p, %1, 0;\n\tbarrier.red.or.pred q, 1, 256, p;\n\t"
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.s32 p, %1, 0;\n\tbarrier.red.or.pred q, 1, %2, p;\n\t"
       "selp.u32 %0, 1, 0, q;\n\t}"
       : "=r"(r)
-      : "r"(pred)
+      : "r"(pred), "n"(kCount)
       : "memory");
   return (int)r;
 }
-template <bool kNamed>
+template <int kCount>
 __device__ __forceinline__ void sync_all() {
-  if (!kNamed) __syncthreads();
-  else asm volatile("barrier.sync 1, 256;" ::: "memory");
+  asm volatile("barrier.sync 1, %0;" ::"n"(kCount) : "memory");
 }
 
 // Exact residual of one staged activation that f16 cannot hold (a bf16 value
@@ -367,21 +365,22 @@ constexpr int kMaxCorr = 64;
 // `*n_corr` corrections, sorted by column) or 2 (bf16 staged: some value
 // overflows f16 or is NaN, or more than kMaxCorr values need a residual).
 // `*n_corr` must be zero on entry (and visible to the block).
-// kNamed: only the first 256 threads (the consumer warps) take part.
-template <bool kNamed>
-__device__ __forceinline__ int stage_x_corr(const QmvArgs& a, const Plan& pl, int cb, int ce, uint32_t xs_base,
+// Threads kFirst .. kFirst+kCount-1 (whole warps) take part.
+// dst(slot, ch, w8) gives the shared address of the 16-byte unit holding
+// columns 8*w8 .. 8*w8+7 of chunk ch (relative to the slice) of a slot.
+template <int kFirst, int kCount, typename Dst>
+__device__ __forceinline__ int stage_x_corr(const QmvArgs& a, const Plan& pl, int cb, int ce, Dst dst_of,
                                             const int64_t* s_e, const int64_t* s_xr, Corr* corr, int* n_corr) {
   // only the allocated slots (min(TR, R)) are staged; the others never hold
   // a row of this tile and are never read
   const int upc = kChunkCols / 8;
   const int units = pl.xs_slots * (ce - cb) * upc;
-  const int nthr = kNamed ? 256 : (int)blockDim.x;
+  const int nthr = kCount, tid = (int)threadIdx.x - kFirst;
   int hard = 0;
-  for (int u = threadIdx.x; u < units; u += nthr) {
+  for (int u = tid; u < units; u += nthr) {
     const int slot = u / ((ce - cb) * upc);
     const int rem = u % ((ce - cb) * upc);
     const int ch = rem / upc, w8 = rem % upc;
-    const int tq = w8 >> 3, qq = w8 & 7;
     const int64_t col = (int64_t)(cb + ch) * kChunkCols + 8 * w8;
     uint4 v = make_uint4(0, 0, 0, 0);
     if (s_e[slot] >= 0 && col < a.K)
@@ -410,27 +409,27 @@ __device__ __forceinline__ int stage_x_corr(const QmvArgs& a, const Plan& pl, in
       }
       v = make_uint4(o[0], o[1], o[2], o[3]);
     }
-    const uint32_t dst = xs_base + 2u * (uint32_t)(slot * pl.xs_stride + ch * kChunkCols + (4 * qq + tq) * 8);
+    const uint32_t dst = dst_of(slot, ch, w8);
     asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w));
   }
-  if (sync_or<kNamed>(hard)) {  // keep the exact bf16 activations instead
-    for (int u = threadIdx.x; u < units; u += nthr) {
+  if (sync_or<kCount>(hard)) {  // keep the exact bf16 activations instead
+    for (int u = tid; u < units; u += nthr) {
       const int slot = u / ((ce - cb) * upc);
       const int rem = u % ((ce - cb) * upc);
-      const int ch = rem / upc, w8 = rem % upc, tq = w8 >> 3, qq = w8 & 7;
+      const int ch = rem / upc, w8 = rem % upc;
       const int64_t col = (int64_t)(cb + ch) * kChunkCols + 8 * w8;
       uint4 v = make_uint4(0, 0, 0, 0);
       if (s_e[slot] >= 0 && col < a.K)
         v = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.x) + s_xr[slot] * a.K + col));
-      const uint32_t dst = xs_base + 2u * (uint32_t)(slot * pl.xs_stride + ch * kChunkCols + (4 * qq + tq) * 8);
+      const uint32_t dst = dst_of(slot, ch, w8);
       asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w));
     }
-    sync_all<kNamed>();
+    sync_all<kCount>();
     return 2;
   }
   const int nc = *n_corr;
   if (nc == 0) return 0;
-  if (threadIdx.x == 0) {  // sort by column (at most kMaxCorr entries)
+  if (tid == 0) {  // sort by column (at most kMaxCorr entries)
     for (int i = 1; i < nc; ++i) {
       const Corr k = corr[i];
       int j = i - 1;
@@ -441,7 +440,7 @@ __device__ __forceinline__ int stage_x_corr(const QmvArgs& a, const Plan& pl, in
       corr[j + 1] = k;
     }
   }
-  sync_all<kNamed>();
+  sync_all<kCount>();
   return 1;
 }
 

@@ -197,9 +197,10 @@ __device__ void consume(const QmvArgs& a, const Plan& pl, const TmaCtx& c, uint3
   uint32_t ph = 0;  // its phase parity
 
   ReduceOut red_out;
-  auto gather = [&](uint32_t rb) { cluster_gather(pl.C, TR, rank, rb, kConsumerWarps * 32, red_out); };
+  auto gather = [&](uint32_t rb) { cluster_gather(pl.C, TR, rank, rb, threadIdx.x, kConsumerWarps * 32, red_out); };
   auto store = [&](int si) {
-    cluster_store(a, pl.C, TR, pl.x_is_bf16, rank, c.slab0 + (int64_t)si * c.slab_step, s_e, r0, kConsumerWarps * 32, red_out);
+    cluster_store(a, pl.C, TR, pl.x_is_bf16, rank, c.slab0 + (int64_t)si * c.slab_step, s_e, r0, threadIdx.x,
+                  kConsumerWarps * 32, red_out);
   };
 
   for (int si = 0; si < c.nslab; ++si) {
@@ -379,7 +380,11 @@ qmv_tma_kernel(const QmvArgs a, const Plan pl, const __grid_constant__ CUtensorM
     cluster_wait();
     return;
   }
-  const int mode = stage_x_corr<true>(a, pl, cb, ce, xs_base, s_e, s_xr, s_corr, &s_ncorr);
+  // column 64t+8q+i of a chunk is staged at chunk offset (4q+t)*8+i
+  auto dst_of = [&](int slot, int ch, int w8) {
+    return xs_base + 2u * (uint32_t)(slot * pl.xs_stride + ch * kChunkCols + (4 * (w8 & 7) + (w8 >> 3)) * 8);
+  };
+  const int mode = stage_x_corr<0, kConsumerWarps * 32>(a, pl, cb, ce, dst_of, s_e, s_xr, s_corr, &s_ncorr);
   const bool use_bf16 = mode == 2;
   const int ncorr = mode == 1 ? s_ncorr : 0;
   if (use_bf16) {
