@@ -10,21 +10,28 @@
 // memory, so the dense plane never exists in HBM. The products fp4 * e4m3 are
 // exact in bf16/f16, so the tensor core sees exactly the dequantized weights.
 //
-// Per CTA (one per SM, 16 warps):
-//   warp 0      TMA producer of the activation tiles x[128 x 64] (SW128)
-//   warp 1      MMA issuer: tcgen05.mma.cta_group::1.kind::f16, M=128 N=256
-//               K=16, accumulator in TMEM (two 256-column buffers)
+// Per CTA (one per SM), for a BM x BN output tile with BM = 128 * MH:
+//   warp 0      TMA producer of the activation tiles x[BM x 64] (SW128), one
+//               128-row box per M half
+//   warp 1      MMA issuer: tcgen05.mma.cta_group::1.kind::f16, M=128 per M
+//               half, N=BN, K=16; accumulators in TMEM
 //   warp 2      TMEM allocator
-//   warps 4-7   epilogue: tcgen05.ld 32x32b, global factor, cast, store
-//   warps 8-15  weight producers: 128-bit loads of the packed words and
-//               scale bytes (prefetched three stages ahead in registers),
-//               exact decode to bf16/f16, stores in the canonical K-major
+//   warps 4..   epilogue, four warps per M half: tcgen05.ld 32x32b, global
+//               factor, cast, store
+//   last 8      weight producers: 128-bit loads of the packed words and scale
+//               bytes (prefetched three stages ahead in registers), exact
+//               decode to bf16/f16, stores in the canonical K-major
 //               128-byte-swizzled layout the MMA descriptor reads
+// Every decoded weight tile feeds MH M=128 MMAs, so a 256-row tile (MH = 2)
+// halves the decode work per flop, which is what bounds the bf16 route.
 // Stages hand off through mbarriers; every wait is bounded and records an
 // error code instead of hanging.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <cmath>
+#include <cstdlib>
+#include <cstring>
 #include <mutex>
 #include <type_traits>
 
@@ -37,17 +44,32 @@ __device__ int g_tc_error = 0;  // first error code recorded by a bounded wait
 
 namespace {
 
-constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
-constexpr uint32_t A_BYTES = BM * BK * 2;  // 16 KB
-constexpr uint32_t B_BYTES = BN * BK * 2;  // 32 KB
-constexpr int kThreads = 512;
+constexpr int BK = 64;
+constexpr uint32_t kHalfA = 128 * BK * 2;  // one 128-row activation box: 16 KB
+constexpr uint32_t kRingBudget = 192 * 1024;
 constexpr int kProducerWarps = 8;
-constexpr int kEpiWarps = 4;
-constexpr int kWarpTma = 0, kWarpMma = 1, kWarpAlloc = 2, kWarpEpi0 = 4, kWarpProd0 = 8;
-constexpr uint32_t kTmemCols = 512;  // two 256-column f32 accumulators
-constexpr int kBarBytes = 8 * (3 * STAGES + 4) + 16;
-constexpr size_t kSmemBytes = 1024 + STAGES * (A_BYTES + B_BYTES) + kBarBytes;
+constexpr int kWarpTma = 0, kWarpMma = 1, kWarpAlloc = 2, kWarpEpi0 = 4;
+constexpr uint32_t kTmemCols = 512;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+
+// Tile configuration: MH M halves of 128 rows, BN weight rows per tile.
+template <int MH_, int BN_>
+struct Cfg {
+  static constexpr int MH = MH_, BN = BN_, BM = 128 * MH_;
+  static constexpr uint32_t A_BYTES = MH_ * kHalfA;
+  static constexpr uint32_t B_BYTES = BN_ * BK * 2;
+  static constexpr int STAGES = (int)(kRingBudget / (A_BYTES + B_BYTES));
+  static constexpr int ACC_BUFS = (int)kTmemCols / (MH_ * BN_) >= 2 ? 2 : 1;  // accumulator buffers in TMEM
+  static constexpr int EPI_WARPS = 4 * MH_;
+  static constexpr int kWarpProd0 = kWarpEpi0 + EPI_WARPS;
+  static constexpr int THREADS = 32 * (kWarpProd0 + kProducerWarps);
+  static constexpr int RPT = BN_ / 128;  // weight rows per producer thread
+  static constexpr int BAR_BYTES = 8 * (3 * STAGES + 2 * ACC_BUFS) + 16;
+  static constexpr size_t SMEM = 1024 + (size_t)STAGES * (A_BYTES + B_BYTES) + BAR_BYTES;
+  static_assert(STAGES >= 3, "ring too shallow");
+  static_assert(ACC_BUFS * MH_ * BN_ <= (int)kTmemCols, "accumulators exceed TMEM");
+  static_assert(SMEM <= 227 * 1024, "shared memory");
+};
 
 struct TcParams {
   const uint32_t* w;
@@ -146,11 +168,11 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
 }
 
 // Instruction descriptor for kind::f16: f32 accumulator, A/B bf16 or f16,
-// both K-major, N = BN, M = BM.
-template <bool BF16>
+// both K-major, N = BN, M = 128.
+template <bool BF16, int BN>
 __host__ __device__ constexpr uint32_t make_idesc() {
   return (1u << 4) | ((BF16 ? 1u : 0u) << 7) | ((BF16 ? 1u : 0u) << 10) | ((uint32_t)(BN >> 3) << 17) |
-         ((uint32_t)(BM >> 4) << 24);
+         ((uint32_t)(128 >> 4) << 24);
 }
 
 __device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
@@ -178,9 +200,10 @@ __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.
 
 // ---------------------------------------------------------------- producer of decoded weights
 
+template <int RPT>
 struct WTask {
-  uint4 w0, w1;      // packed words 4h..4h+3 of the k-block for rows r and r+128
-  uint32_t s0, s1;   // the four scale bytes of the k-block for rows r and r+128
+  uint4 w[RPT];      // packed words 4h..4h+3 of the k-block for rows r + 128 i
+  uint32_t s[RPT];   // the four scale bytes of the k-block for those rows
 };
 
 struct WCursor {
@@ -188,29 +211,27 @@ struct WCursor {
   bool done;
 };
 
-__device__ __forceinline__ void w_load(WTask& t, const WCursor& cur, const TcParams& p, int r, int h) {
+template <int BN, int RPT>
+__device__ __forceinline__ void w_load(WTask<RPT>& t, const WCursor& cur, const TcParams& p, int r, int h) {
   if (cur.done) return;
   const int n_tile = cur.tile / p.num_m_tiles;
   const int64_t kwords = p.K / 8, kgroups = p.K / 16;
-  const int64_t n0 = (int64_t)n_tile * BN + r, n1 = n0 + 128;
   const int64_t kw = (int64_t)cur.kb * 8 + 4 * h;  // first of this task's four words
   const bool kok = kw < kwords;                     // K % 32 == 0 keeps the four words together
   const int64_t g4 = (int64_t)cur.kb * 4;
-  t.w0 = (kok && n0 < p.N) ? __ldg(reinterpret_cast<const uint4*>(p.w + n0 * kwords + kw)) : make_uint4(0, 0, 0, 0);
-  t.w1 = (kok && n1 < p.N) ? __ldg(reinterpret_cast<const uint4*>(p.w + n1 * kwords + kw)) : make_uint4(0, 0, 0, 0);
-  if (kgroups % 4 == 0) {
-    t.s0 = (kok && n0 < p.N) ? __ldg(reinterpret_cast<const uint32_t*>(p.scales + n0 * kgroups + g4)) : 0u;
-    t.s1 = (kok && n1 < p.N) ? __ldg(reinterpret_cast<const uint32_t*>(p.scales + n1 * kgroups + g4)) : 0u;
-  } else {
-    uint32_t a = 0, b = 0;
-    for (int i = 0; i < 4; ++i) {
-      if (g4 + i < kgroups) {
-        if (n0 < p.N) a |= (uint32_t)p.scales[n0 * kgroups + g4 + i] << (8 * i);
-        if (n1 < p.N) b |= (uint32_t)p.scales[n1 * kgroups + g4 + i] << (8 * i);
-      }
+#pragma unroll
+  for (int i = 0; i < RPT; ++i) {
+    const int64_t n = (int64_t)n_tile * BN + r + 128 * i;
+    const bool ok = kok && n < p.N;
+    t.w[i] = ok ? __ldg(reinterpret_cast<const uint4*>(p.w + n * kwords + kw)) : make_uint4(0, 0, 0, 0);
+    if (kgroups % 4 == 0) {
+      t.s[i] = ok ? __ldg(reinterpret_cast<const uint32_t*>(p.scales + n * kgroups + g4)) : 0u;
+    } else {
+      uint32_t v = 0;
+      for (int j = 0; j < 4; ++j)
+        if (ok && g4 + j < kgroups) v |= (uint32_t)p.scales[n * kgroups + g4 + j] << (8 * j);
+      t.s[i] = v;
     }
-    t.s0 = a;
-    t.s1 = b;
   }
 }
 
@@ -241,26 +262,27 @@ __device__ __forceinline__ void w_store_row(uint32_t stage_base, int row, int h,
   }
 }
 
-template <typename T>
+template <typename T, typename C>
 __device__ void producer_role(const TcParams& p, uint32_t sB, uint32_t bars, volatile int* abort_flag) {
-  const int pid = threadIdx.x - kWarpProd0 * 32;  // 0..255
-  const int r = pid >> 1, h = pid & 1;            // rows r and r+128, words 4h..4h+3 of the k-block
+  constexpr int STAGES = C::STAGES, RPT = C::RPT;
+  const int pid = threadIdx.x - C::kWarpProd0 * 32;  // 0..255
+  const int r = pid >> 1, h = pid & 1;               // rows r + 128 i, words 4h..4h+3 of the k-block
   const int lane = threadIdx.x & 31;
   WCursor ld{(int)blockIdx.x, 0, (int)blockIdx.x >= p.num_tiles};
-  WTask b0, b1, b2;
-  w_load(b0, ld, p, r, h);
+  WTask<RPT> b0, b1, b2;
+  w_load<C::BN>(b0, ld, p, r, h);
   w_advance(ld, p);
-  w_load(b1, ld, p, r, h);
+  w_load<C::BN>(b1, ld, p, r, h);
   w_advance(ld, p);
   uint32_t u = 0;
   const int total = ((p.num_tiles - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x) * p.num_kb;
-  auto consume = [&](const WTask& t) -> bool {
+  auto consume = [&](const WTask<RPT>& t) -> bool {
     const int s = (int)(u % STAGES);
     const uint32_t ph = (u / STAGES) & 1;
     if (!wait_bar_warp(bars + 8 * (2 * STAGES + s), ph ^ 1, abort_flag, 3, &g_tc_error)) return false;  // stage empty
-    const uint32_t stage = sB + (uint32_t)s * B_BYTES;
-    w_store_row<T>(stage, r, h, t.w0, t.s0);
-    w_store_row<T>(stage, r + 128, h, t.w1, t.s1);
+    const uint32_t stage = sB + (uint32_t)s * C::B_BYTES;
+#pragma unroll
+    for (int i = 0; i < RPT; ++i) w_store_row<T>(stage, r + 128 * i, h, t.w[i], t.s[i]);
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     __syncwarp();
     if (lane == 0) mbar_arrive(bars + 8 * (STAGES + s));  // fullB
@@ -268,15 +290,15 @@ __device__ void producer_role(const TcParams& p, uint32_t sB, uint32_t bars, vol
     return true;
   };
   for (int i = 0; i < total; i += 3) {
-    w_load(b2, ld, p, r, h);
+    w_load<C::BN>(b2, ld, p, r, h);
     w_advance(ld, p);
     if (!consume(b0)) return;
     if (i + 1 >= total) break;
-    w_load(b0, ld, p, r, h);
+    w_load<C::BN>(b0, ld, p, r, h);
     w_advance(ld, p);
     if (!consume(b1)) return;
     if (i + 2 >= total) break;
-    w_load(b1, ld, p, r, h);
+    w_load<C::BN>(b1, ld, p, r, h);
     w_advance(ld, p);
     if (!consume(b2)) return;
   }
@@ -284,23 +306,25 @@ __device__ void producer_role(const TcParams& p, uint32_t sB, uint32_t bars, vol
 
 // ---------------------------------------------------------------- kernel
 
-template <typename T>
-__global__ void __launch_bounds__(kThreads, 1)
+template <typename T, typename C>
+__global__ void __launch_bounds__(C::THREADS, 1)
 qmm_tc_kernel(const __grid_constant__ CUtensorMap xmap, const TcParams p) {
+  constexpr int STAGES = C::STAGES, MH = C::MH, BN = C::BN, BM = C::BM, NBUF = C::ACC_BUFS;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* base_ptr = smem_raw + (base - raw);
-  const uint32_t sA = base, sB = base + STAGES * A_BYTES;
-  const uint32_t bars = sB + STAGES * B_BYTES;
-  // barriers: fullA[S] fullB[S] empty[S] accFull[2] accEmpty[2]
-  uint32_t* holder = reinterpret_cast<uint32_t*>(base_ptr + STAGES * (A_BYTES + B_BYTES) + 8 * (3 * STAGES + 4));
+  const uint32_t sA = base, sB = base + STAGES * C::A_BYTES;
+  const uint32_t bars = sB + STAGES * C::B_BYTES;
+  // barriers: fullA[S] fullB[S] empty[S] accFull[NBUF] accEmpty[NBUF]
+  uint32_t* holder =
+      reinterpret_cast<uint32_t*>(base_ptr + STAGES * (C::A_BYTES + C::B_BYTES) + 8 * (3 * STAGES + 2 * NBUF));
   volatile int* abort_flag = reinterpret_cast<volatile int*>(holder + 1);
   auto fullA = [&](int s) { return bars + 8 * s; };
   auto fullB = [&](int s) { return bars + 8 * (STAGES + s); };
   auto emptyB = [&](int s) { return bars + 8 * (2 * STAGES + s); };
   auto accFull = [&](int b) { return bars + 8 * (3 * STAGES + b); };
-  auto accEmpty = [&](int b) { return bars + 8 * (3 * STAGES + 2 + b); };
+  auto accEmpty = [&](int b) { return bars + 8 * (3 * STAGES + NBUF + b); };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -309,9 +333,9 @@ qmm_tc_kernel(const __grid_constant__ CUtensorMap xmap, const TcParams p) {
       mbar_init(fullB(s), kProducerWarps);
       mbar_init(emptyB(s), 1);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < NBUF; ++b) {
       mbar_init(accFull(b), 1);
-      mbar_init(accEmpty(b), kEpiWarps);
+      mbar_init(accEmpty(b), C::EPI_WARPS);
     }
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -343,12 +367,15 @@ qmm_tc_kernel(const __grid_constant__ CUtensorMap xmap, const TcParams p) {
           const int s = (int)(u % STAGES);
           const uint32_t ph = (u / STAGES) & 1;
           if (!wait_bar(emptyB(s), ph ^ 1, abort_flag, 1)) { ok = false; break; }
-          mbar_arrive_tx(fullA(s), A_BYTES);
-          tma_load_2d(sA + (uint32_t)s * A_BYTES, &xmap, kb * BK, m_tile * BM, fullA(s));
+          mbar_arrive_tx(fullA(s), C::A_BYTES);
+#pragma unroll
+          for (int h = 0; h < MH; ++h)
+            tma_load_2d(sA + (uint32_t)s * C::A_BYTES + (uint32_t)h * kHalfA, &xmap, kb * BK, m_tile * BM + 128 * h,
+                        fullA(s));
         }
       }
       // Leave no copy in flight: wait (bounded) for the last stages issued.
-      const uint32_t first = u > STAGES ? u - STAGES : 0;
+      const uint32_t first = u > (uint32_t)STAGES ? u - STAGES : 0;
       for (uint32_t v = first; v < u; ++v) {
         const uint32_t limit_ph = (v / STAGES) & 1;
         const uint64_t t0 = gtimer();
@@ -358,45 +385,50 @@ qmm_tc_kernel(const __grid_constant__ CUtensorMap xmap, const TcParams p) {
     }
   } else if (warp == kWarpMma) {
     if (lane == 0) {
-      constexpr uint32_t idesc = make_idesc<std::is_same<T, __nv_bfloat16>::value>();
+      constexpr uint32_t idesc = make_idesc<std::is_same<T, __nv_bfloat16>::value, BN>();
       uint32_t u = 0;
       bool ok = true;
       for (int i = 0; i < my_tiles && ok; ++i) {
-        const int b = i & 1;
-        if (!wait_bar(accEmpty(b), ((i >> 1) & 1) ^ 1, abort_flag, 4)) break;
+        const int b = i % NBUF;
+        if (!wait_bar(accEmpty(b), ((i / NBUF) & 1) ^ 1, abort_flag, 4)) break;
         tc_fence_after();
-        const uint32_t d = tmem + (uint32_t)(b * BN);
+        const uint32_t d = tmem + (uint32_t)(b * MH * BN);
         for (int kb = 0; kb < p.num_kb; ++kb, ++u) {
           const int s = (int)(u % STAGES);
           const uint32_t ph = (u / STAGES) & 1;
           if (!wait_bar(fullA(s), ph, abort_flag, 5) || !wait_bar(fullB(s), ph, abort_flag, 6)) { ok = false; break; }
           tc_fence_after();
-          const uint64_t ad = sw128_desc(sA + (uint32_t)s * A_BYTES);
-          const uint64_t bd = sw128_desc(sB + (uint32_t)s * B_BYTES);
+          const uint64_t bd = sw128_desc(sB + (uint32_t)s * C::B_BYTES);
 #pragma unroll
           for (int j = 0; j < BK / 16; ++j)
-            umma_f16(d, ad + (uint64_t)(2 * j), bd + (uint64_t)(2 * j), idesc, (kb | j) != 0);
+#pragma unroll
+            for (int h = 0; h < MH; ++h) {
+              const uint64_t ad = sw128_desc(sA + (uint32_t)s * C::A_BYTES + (uint32_t)h * kHalfA);
+              umma_f16(d + (uint32_t)(h * BN), ad + (uint64_t)(2 * j), bd + (uint64_t)(2 * j), idesc, (kb | j) != 0);
+            }
           umma_commit(emptyB(s));
         }
         if (ok) umma_commit(accFull(b));
       }
     }
-  } else if (warp >= kWarpEpi0 && warp < kWarpEpi0 + kEpiWarps) {
-    const int q = warp - kWarpEpi0;  // TMEM lane quarter
+  } else if (warp >= kWarpEpi0 && warp < kWarpEpi0 + C::EPI_WARPS) {
+    const int q = warp & 3;                 // TMEM lane quarter this warp may read
+    const int hm = (warp - kWarpEpi0) >> 2;  // M half it drains
     const float fac = global_factor(p.gs, 0);
     T* y = static_cast<T*>(p.y);
     for (int i = 0; i < my_tiles; ++i) {
       const int tile = (int)blockIdx.x + i * (int)gridDim.x;
       const int m_tile = tile % p.num_m_tiles, n_tile = tile / p.num_m_tiles;
-      const int b = i & 1;
-      if (!wait_bar_warp(accFull(b), (i >> 1) & 1, abort_flag, 7, &g_tc_error)) break;
+      const int b = i % NBUF;
+      if (!wait_bar_warp(accFull(b), (i / NBUF) & 1, abort_flag, 7, &g_tc_error)) break;
       tc_fence_after();
-      const int64_t m = (int64_t)m_tile * BM + 32 * q + lane;
+      const int64_t m = (int64_t)m_tile * BM + 128 * hm + 32 * q + lane;
       const int64_t n_base = (int64_t)n_tile * BN;
+      const uint32_t tcol = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(b * MH * BN + hm * BN);
 #pragma unroll 1
       for (int c = 0; c < BN / 32; ++c) {
         uint32_t r[32];
-        tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(b * BN + 32 * c), r);
+        tmem_ld32(tcol + (uint32_t)(32 * c), r);
         tmem_ld_wait();
         if (m >= p.M) continue;
         const int64_t n0 = n_base + 32 * c;
@@ -428,8 +460,8 @@ qmm_tc_kernel(const __grid_constant__ CUtensorMap xmap, const TcParams p) {
       __syncwarp();
       if (lane == 0) mbar_arrive(accEmpty(b));
     }
-  } else if (warp >= kWarpProd0) {
-    producer_role<T>(p, sB, bars, abort_flag);
+  } else if (warp >= C::kWarpProd0) {
+    producer_role<T, C>(p, sB, bars, abort_flag);
   }
 
   tc_fence_before();
@@ -453,15 +485,15 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-template <typename T>
-cudaError_t launch_tc(const void* x, int64_t M, int64_t K, const uint32_t* w, const uint8_t* scales, const float* gs,
-                      int64_t N, void* y, cudaStream_t st) {
+template <typename T, typename C>
+cudaError_t launch_cfg(const void* x, int64_t M, int64_t K, const uint32_t* w, const uint8_t* scales, const float* gs,
+                       int64_t N, void* y, int sms, cudaStream_t st) {
   auto enc = encode_fn();
   if (!enc) return cudaErrorNotSupported;
   CUtensorMap map;
   const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)M};
   const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
-  const cuuint32_t box[2] = {BK, BM};
+  const cuuint32_t box[2] = {BK, 128};
   const cuuint32_t estr[2] = {1, 1};
   const CUtensorMapDataType dt =
       std::is_same<T, __nv_bfloat16>::value ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
@@ -476,18 +508,61 @@ cudaError_t launch_tc(const void* x, int64_t M, int64_t K, const uint32_t* w, co
   p.M = M;
   p.N = N;
   p.K = K;
-  p.num_m_tiles = (int)((M + BM - 1) / BM);
-  const int num_n_tiles = (int)((N + BN - 1) / BN);
+  p.num_m_tiles = (int)((M + C::BM - 1) / C::BM);
+  const int num_n_tiles = (int)((N + C::BN - 1) / C::BN);
   p.num_tiles = p.num_m_tiles * num_n_tiles;
   p.num_kb = (int)((K + BK - 1) / BK);
+  const int grid = p.num_tiles < sms ? p.num_tiles : sms;
+  auto kern = qmm_tc_kernel<T, C>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
+  if (e != cudaSuccess) return e;
+  kern<<<grid, C::THREADS, C::SMEM, st>>>(map, p);
+  return cudaGetLastError();
+}
+
+using Tile256x256 = Cfg<2, 256>;
+using Tile256x128 = Cfg<2, 128>;
+using Tile128x256 = Cfg<1, 256>;
+
+// Tile shape by modelled time: whole waves of persistent tiles, each tile's
+// cost its area over the shape's relative throughput (one 128-row half per
+// decoded weight tile runs decode-bound at about 0.6 of the two-half rate;
+// 128-wide tiles re-read the activations twice as often). The environment
+// variable NVFP4_TC_TILE ("256x256", "256x128" or "128x256") overrides it.
+int pick_tile(int64_t M, int64_t N, int sms) {
+  const char* forced = std::getenv("NVFP4_TC_TILE");
+  if (forced) {
+    if (!std::strcmp(forced, "256x256")) return 0;
+    if (!std::strcmp(forced, "256x128")) return 1;
+    if (!std::strcmp(forced, "128x256")) return 2;
+  }
+  const int bm[3] = {256, 256, 128}, bn[3] = {256, 128, 256};
+  const double rate[3] = {1.0, 0.92, 0.6};
+  int best = 0;
+  double best_t = 1e300;
+  for (int c = 0; c < 3; ++c) {
+    const double tiles = (double)((M + bm[c] - 1) / bm[c]) * (double)((N + bn[c] - 1) / bn[c]);
+    const double waves = std::ceil(tiles / sms);
+    const double t = waves * bm[c] * bn[c] / rate[c];
+    if (t < best_t - 1e-9) {
+      best_t = t;
+      best = c;
+    }
+  }
+  return best;
+}
+
+template <typename T>
+cudaError_t launch_tc(const void* x, int64_t M, int64_t K, const uint32_t* w, const uint8_t* scales, const float* gs,
+                      int64_t N, void* y, cudaStream_t st) {
   int dev = 0, sms = 152;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const int grid = p.num_tiles < sms ? p.num_tiles : sms;
-  cudaError_t e = cudaFuncSetAttribute(qmm_tc_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
-  if (e != cudaSuccess) return e;
-  qmm_tc_kernel<T><<<grid, kThreads, kSmemBytes, st>>>(map, p);
-  return cudaGetLastError();
+  switch (pick_tile(M, N, sms)) {
+    case 0: return launch_cfg<T, Tile256x256>(x, M, K, w, scales, gs, N, y, sms, st);
+    case 1: return launch_cfg<T, Tile256x128>(x, M, K, w, scales, gs, N, y, sms, st);
+    default: return launch_cfg<T, Tile128x256>(x, M, K, w, scales, gs, N, y, sms, st);
+  }
 }
 
 }  // namespace
@@ -496,7 +571,7 @@ bool qmm_tc_supported(int64_t M, int64_t N, int64_t K) {
   // TMA coordinates are 32-bit; K must keep each 128-bit weight load within
   // one k-block row segment (K % 32 == 0).
   return M > 0 && N > 0 && K >= 32 && K % 32 == 0 && M < (1ll << 31) && K < (1ll << 31) &&
-         (M + BM - 1) / BM * ((N + BN - 1) / BN) < (1ll << 31);
+         (M + 127) / 128 * ((N + 127) / 128) < (1ll << 31);
 }
 
 cudaError_t launch_qmm_tc(const void* x, int xdt, int64_t M, int64_t K, const uint32_t* w, const uint8_t* scales,

@@ -41,6 +41,11 @@ __device__ __forceinline__ uint32_t cluster_rank() {
   return r;
 }
 __device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory"); }
+// Arrival that publishes nothing (a warp whose writes no peer reads): it does
+// not wait for the thread's outstanding memory operations.
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
 __device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
 __device__ __forceinline__ uint32_t map_rank(uint32_t saddr, uint32_t rank) {
   uint32_t r;

@@ -151,7 +151,7 @@ __device__ void produce(const TmaCtx& c, const CUtensorMap* wmap, const CUtensor
     }
     __syncwarp();
     if (pending) cluster_wait();
-    cluster_arrive();
+    cluster_arrive_relaxed();
     pending = true;
   }
   if (pending) cluster_wait();
@@ -376,7 +376,7 @@ qmv_tma_kernel(const QmvArgs a, const Plan pl, const __grid_constant__ CUtensorM
   // the activations meanwhile (named barrier 1, 256 threads).
   if (warp == kConsumerWarps) {
     produce(c, &wmap, &smap, wst, sst, bars, abort_flag, kStages);
-    cluster_arrive();
+    cluster_arrive_relaxed();
     cluster_wait();
     return;
   }

@@ -199,12 +199,18 @@ def test_gather_identity_lhs(nv):
 
 # ------------------------------------------------------------------ tensor-core (tcgen05) route
 
-TC_SHAPES = [(1, 256, 64), (100, 272, 96), (128, 512, 256), (129, 40, 64), (300, 520, 320), (256, 256, 5376)]
+# (4096, 8192, 64) gives every persistent CTA several tiles, so accumulator
+# reuse and barrier phase wrap-around are exercised for each tile shape.
+TC_SHAPES = [(1, 256, 64), (100, 272, 96), (128, 512, 256), (129, 40, 64), (300, 520, 320), (256, 256, 5376),
+             (4096, 8192, 64)]
 
 
+@pytest.mark.parametrize("tile", ["auto", "256x256", "256x128", "128x256"])
 @pytest.mark.parametrize("mnk", TC_SHAPES, ids=lambda v: "M%d_N%d_K%d" % v)
 @pytest.mark.parametrize("dt", ["f16", "bf16"])
-def test_qmm_tc_route(nv, mnk, dt):
+def test_qmm_tc_route(nv, mnk, dt, tile, monkeypatch):
+    if tile != "auto":
+        monkeypatch.setenv("NVFP4_TC_TILE", tile)
     M, N, K = mnk
     w, s = weights(M + 7 * N + K, N, K, lo=2.0**-4, hi=16.0)
     g = synth.rng(M * 77 + N + K)
