@@ -127,6 +127,19 @@ nvfp4_status nvfp4_gather_qmm(const void* x, nvfp4_dtype x_dtype, int64_t B, int
  * instead of holding the GPU. */
 int32_t nvfp4_take_device_error(void);
 
+/* Launch overlap for the weight-streaming calls (nvfp4_qmm below the
+ * tensor-core crossover, nvfp4_gather_qmm). When enabled (non-zero) they are
+ * launched as programmatic dependents of the kernel before them on the
+ * stream: their CTAs may start, and begin streaming the weight and scale
+ * planes, while that kernel is still finishing. Activations, indices and
+ * outputs are touched only after it has completed and its writes are visible.
+ * The caller promises that no kernel still running on the stream writes the
+ * weight or scale planes (for example a transcode of those planes issued just
+ * before). Off by default; process-wide. Returns the previous setting. Not
+ * part of the pages' interface: it removes the idle gap between consecutive
+ * decode-step matmuls, whose weights are constant. */
+int nvfp4_set_launch_overlap(int enable);
+
 /* Message for the calling thread's last non-OK status ("" if none). */
 const char* nvfp4_last_error(void);
 

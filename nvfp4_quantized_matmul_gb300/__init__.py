@@ -4,7 +4,8 @@ The compute path lives in ``libnvfp4.so`` (CUDA kernels behind a C ABI); the
 ``ops`` attributes below are thin ctypes marshalling over it and are loaded on
 first use, so ``synth`` can be imported on machines without the library.
 """
-_LAZY = ("transcode", "dequantize", "qmm", "gather_qmm", "library", "qmm_crossover", "take_device_error")
+_LAZY = ("transcode", "dequantize", "qmm", "gather_qmm", "library", "qmm_crossover", "take_device_error",
+         "set_launch_overlap")
 
 
 def __getattr__(name):

@@ -36,6 +36,7 @@ SIGNATURES = {
     "nvfp4_last_error": (ctypes.c_char_p, []),
     "nvfp4_version": (ctypes.c_char_p, []),
     "nvfp4_take_device_error": (ctypes.c_int32, []),
+    "nvfp4_set_launch_overlap": (_INT, [_INT]),
 }
 
 
@@ -165,6 +166,13 @@ def gather_qmm(x, w, scales, rhs, lhs=None, gs=None, sorted_indices=False, out=N
 def take_device_error():
     """Device error code from a tensor-core kernel's bounded wait (0 = none); synchronises."""
     return int(_lib.nvfp4_take_device_error())
+
+
+def set_launch_overlap(enable):
+    """Let weight-streaming calls start while the previous kernel on the stream
+    finishes (the weight planes must not be written by a kernel still running).
+    Returns the previous setting."""
+    return bool(_lib.nvfp4_set_launch_overlap(int(bool(enable))))
 
 
 def qmm_crossover(dtype, n, k):

@@ -6,6 +6,7 @@
 // global scale must have one entry per expert, an unexpected global-scale
 // input is refused rather than ignored, launch limits are refused with a
 // clear error, and empty outputs return before any launch.
+#include <atomic>
 #include <cinttypes>
 #include <cstdarg>
 #include <cstdio>
@@ -129,11 +130,18 @@ int64_t env_crossover() {
 
 }  // namespace
 
+namespace nvfp4 {
+std::atomic<int> g_launch_overlap{0};
+bool launch_overlap() { return g_launch_overlap.load(std::memory_order_relaxed) != 0; }
+}  // namespace nvfp4
+
 extern "C" {
 
 const char* nvfp4_last_error(void) { return g_last_error.c_str(); }
 
 const char* nvfp4_version(void) { return "nvfp4-gb300 0.1 (sm_103a)"; }
+
+int nvfp4_set_launch_overlap(int enable) { return nvfp4::g_launch_overlap.exchange(enable ? 1 : 0); }
 
 int32_t nvfp4_take_device_error(void) {
   const int a = nvfp4::read_tc_error(), b = nvfp4::read_qmv_error();

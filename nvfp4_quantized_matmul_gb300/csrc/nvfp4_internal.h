@@ -39,6 +39,10 @@ bool qmv_tma_supported(const QmvArgs& a, int xdt);
 cudaError_t launch_qmv_tma(const QmvArgs& a, int xdt, cudaStream_t st);
 int read_qmv_error();
 
+// Whether weight-streaming launches may overlap the previous kernel on the
+// stream (programmatic dependent launch; see nvfp4_set_launch_overlap).
+bool launch_overlap();
+
 // Prefill-shape tensor-core route (tcgen05, TMEM accumulators).
 bool qmm_tc_supported(int64_t M, int64_t N, int64_t K);
 cudaError_t launch_qmm_tc(const void* x, int xdt, int64_t M, int64_t K, const uint32_t* w, const uint8_t* scales,

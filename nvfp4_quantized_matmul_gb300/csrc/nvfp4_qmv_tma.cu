@@ -13,6 +13,8 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <cstdio>
+#include <cstdlib>
 #include <map>
 #include <mutex>
 #include <tuple>
@@ -30,7 +32,15 @@ constexpr int kConsumerWarps = kWarps;                     // 8 warps x 16 rows 
 constexpr int kTmaThreads = (kConsumerWarps + 1) * 32;     // plus one producer warp
 constexpr int kMaxStages = 4;  // ring depth: the plan picks 2 to 4
 constexpr uint32_t kWStage = kSlabRows * kChunkWords * 4;  // 16 KB of packed words
-constexpr uint32_t kSStage = kSlabRows * (kChunkCols / 16);  // 2 KB of scale bytes
+// Scale bytes arrive in blocks of eight chunks: one 128-byte-wide box of the
+// scale plane per block (a 16-byte-wide box per chunk would cost the copy
+// engine about as much as the chunk's 16 KB of words), 128-byte swizzled so
+// the per-row 4-byte reads stay conflict-free; two blocks in flight.
+constexpr int kScaleChunks = 8;
+constexpr uint32_t kSBlock = kSlabRows * kScaleChunks * (kChunkCols / 16);  // 16 KB
+constexpr int kSBlocks = 2;
+// barriers: full[kMaxStages] empty[kMaxStages] sfull[kSBlocks] sempty[kSBlocks]
+constexpr uint32_t kBarBytes = 8 * (2 * kMaxStages + 2 * kSBlocks);
 constexpr uint64_t kWaitLimitNs = 2000000000ull;          // 2 s
 
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
@@ -134,17 +144,26 @@ __device__ void produce(const TmaCtx& c, const CUtensorMap* wmap, const CUtensor
   uint32_t u = 0;
   int s = 0;
   uint32_t ph = 0;
+  uint32_t su = 0;  // scale blocks issued
   bool pending = false;
+  const uint32_t sbars = bars + 8 * (2 * kMaxStages);
   for (int si = 0; si < c.nslab; ++si) {
     const int64_t slab = c.slab0 + (int64_t)si * c.slab_step;
     for (int p = 0; p < c.npass; ++p) {
       const int row = (int)((int64_t)c.pass_e[p] * c.N + slab * kSlabRows);
       for (int ch = c.cb; ch < c.ce; ++ch, ++u, s = (s + 1 == kStages ? 0 : s + 1), ph ^= (s == 0 ? 1u : 0u)) {
         if (lane == 0 && !*abort_flag) {
+          if (((ch - c.cb) & (kScaleChunks - 1)) == 0) {  // scale block of chunks ch .. ch+7
+            const uint32_t ss = su & 1u, sph = (su >> 1) & 1u;
+            ++su;
+            if (wait_bar(sbars + 8 * (kSBlocks + ss), sph ^ 1, abort_flag, 13)) {
+              mbar_arrive_tx(sbars + 8 * ss, kSBlock);
+              tma_load_2d(sst + ss * kSBlock, smap, ch * (kChunkCols / 16), row, sbars + 8 * ss);
+            }
+          }
           if (wait_bar(bars + 8 * (kStages + s), ph ^ 1, abort_flag, 11)) {  // stage empty
-            mbar_arrive_tx(bars + 8 * s, kWStage + kSStage);
+            mbar_arrive_tx(bars + 8 * s, kWStage);
             tma_load_2d(wst + (uint32_t)s * kWStage, wmap, ch * kChunkWords, row, bars + 8 * s);
-            tma_load_2d(sst + (uint32_t)s * kSStage, smap, ch * (kChunkCols / 16), row, bars + 8 * s);
           }
         }
       }
@@ -156,12 +175,18 @@ __device__ void produce(const TmaCtx& c, const CUtensorMap* wmap, const CUtensor
   }
   if (pending) cluster_wait();
   // No copy may still be in flight when the CTA leaves: wait (bounded) for
-  // the last stages issued.
+  // the last stages and scale blocks issued.
   if (lane == 0) {
     const uint32_t first = u > (uint32_t)kStages ? u - kStages : 0;
     for (uint32_t v = first; v < u; ++v) {
       const uint64_t t0 = gtimer();
       while (!mbar_try(bars + 8 * (v % kStages), (v / kStages) & 1) && gtimer() - t0 < kWaitLimitNs) {
+      }
+    }
+    const uint32_t sfirst = su > (uint32_t)kSBlocks ? su - kSBlocks : 0;
+    for (uint32_t v = sfirst; v < su; ++v) {
+      const uint64_t t0 = gtimer();
+      while (!mbar_try(sbars + 8 * (v & 1u), (v >> 1) & 1u) && gtimer() - t0 < kWaitLimitNs) {
       }
     }
   }
@@ -181,7 +206,9 @@ __device__ void consume(const QmvArgs& a, const Plan& pl, const TmaCtx& c, uint3
   const uint32_t oa1 = (uint32_t)rg * 128u + ((uint32_t)((2 * t + 1) ^ (rg & 7)) << 4);
   const uint32_t ob0 = (uint32_t)rg8 * 128u + ((uint32_t)((2 * t) ^ (rg8 & 7)) << 4);
   const uint32_t ob1 = (uint32_t)rg8 * 128u + ((uint32_t)((2 * t + 1) ^ (rg8 & 7)) << 4);
-  const uint32_t osa = (uint32_t)rg * 16u + 4u * t, osb = (uint32_t)rg8 * 16u + 4u * t;
+  // this lane's scale word in a scale block: row rg (rg8), 16-byte chunk
+  // (chunk index within the block) ^ (row & 7), bytes 4t..4t+3
+  const uint32_t osa = (uint32_t)rg * 128u + 4u * t, osb = (uint32_t)rg8 * 128u + 4u * t;
 
   constexpr int NA = NAcc<MT>::value;
   float acc[NA][MT][4];
@@ -195,6 +222,8 @@ __device__ void consume(const QmvArgs& a, const Plan& pl, const TmaCtx& c, uint3
   int buf = 0, pending = -1;
   int s = 0;        // ring stage of the next job
   uint32_t ph = 0;  // its phase parity
+  uint32_t su = 0;  // scale blocks consumed
+  const uint32_t sbars = bars + 8 * (2 * kMaxStages);
 
   ReduceOut red_out;
   auto gather = [&](uint32_t rb) { cluster_gather(pl.C, TR, rank, rb, threadIdx.x, kConsumerWarps * 32, red_out); };
@@ -222,18 +251,26 @@ __device__ void consume(const QmvArgs& a, const Plan& pl, const TmaCtx& c, uint3
           s = 0;
           ph ^= 1u;
         }
+        const int kb = (ch - c.cb) & (kScaleChunks - 1);  // chunk within its scale block
+        const uint32_t sblk = su;                          // this chunk's scale block (running count)
+        const uint32_t ss = sblk & 1u;
+        const bool last_of_block = kb == kScaleChunks - 1 || ch + 1 == c.ce;
+        if (last_of_block) ++su;
         uint32_t xc[MT];
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt) xc[mt] = xa[mt] + xstep[mt] * (uint32_t)(ch - c.cb);
+        if (kb == 0 && !wait_bar_warp(sbars + 8 * ss, (sblk >> 1) & 1u, abort_flag, 14, &g_qmv_error))
+          continue;  // scale block full
         if (!wait_bar_warp(bars + 8 * cs, cph, abort_flag, 12, &g_qmv_error)) continue;  // stage full
-        const uint32_t w = wst + (uint32_t)cs * kWStage, q = sst + (uint32_t)cs * kSStage;
+        const uint32_t w = wst + (uint32_t)cs * kWStage, q = sst + ss * kSBlock;
+        const uint32_t qa = q + osa + ((uint32_t)(kb ^ (rg & 7)) << 4), qb = q + osb + ((uint32_t)(kb ^ (rg8 & 7)) << 4);
         Chunk chk;
         chk.a0 = lds128(w + oa0);
         chk.a1 = lds128(w + oa1);
         chk.b0 = lds128(w + ob0);
         chk.b1 = lds128(w + ob1);
-        chk.sa = lds32(q + osa);
-        chk.sb = lds32(q + osb);
+        chk.sa = lds32(qa);
+        chk.sb = lds32(qb);
         compute_chunk<T, MT>(chk, xc, acc, lut_bf);
         // residuals of activations that f16 could not hold exactly
         const int cend = (ch - c.cb + 1) * kChunkCols;
@@ -244,8 +281,8 @@ __device__ void consume(const QmvArgs& a, const Plan& pl, const TmaCtx& c, uint3
           const uint32_t wq = (uint32_t)(kc >> 5), wi = (uint32_t)((kc >> 3) & 3), sh = 4u * (uint32_t)(kc & 7);
           const uint32_t wa = lds32(w + (uint32_t)rg * 128u + ((wq ^ (uint32_t)(rg & 7)) << 4) + 4u * wi);
           const uint32_t wb = lds32(w + (uint32_t)rg8 * 128u + ((wq ^ (uint32_t)(rg8 & 7)) << 4) + 4u * wi);
-          const uint32_t sa_w = lds32(q + (uint32_t)rg * 16u + (uint32_t)(kc >> 4) / 4u * 4u);
-          const uint32_t sb_w = lds32(q + (uint32_t)rg8 * 16u + (uint32_t)(kc >> 4) / 4u * 4u);
+          const uint32_t sa_w = lds32(qa - 4u * t + (uint32_t)(kc >> 4) / 4u * 4u);
+          const uint32_t sb_w = lds32(qb - 4u * t + (uint32_t)(kc >> 4) / 4u * 4u);
           const uint32_t sbyte = 8u * ((uint32_t)(kc >> 4) & 3u);
           const float va = e2m1_to_f32((wa >> sh) & 0xF) * e4m3_to_f32((sa_w >> sbyte) & 0xFF);
           const float vb = e2m1_to_f32((wb >> sh) & 0xF) * e4m3_to_f32((sb_w >> sbyte) & 0xFF);
@@ -263,7 +300,10 @@ __device__ void consume(const QmvArgs& a, const Plan& pl, const TmaCtx& c, uint3
           }
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive_relaxed(bars + 8 * (kStages + cs));  // stage empty
+        if (lane == 0) {
+          mbar_arrive_relaxed(bars + 8 * (kStages + cs));                   // stage empty
+          if (last_of_block) mbar_arrive_relaxed(sbars + 8 * (kSBlocks + ss));  // scale block empty
+        }
       }
     }
     // end of slab: reduce the previous slab over the cluster, publish this one
@@ -301,7 +341,7 @@ __device__ void consume(const QmvArgs& a, const Plan& pl, const TmaCtx& c, uint3
 // Dynamic shared memory: [1024-aligned] W stages | S stages | barriers (full[S],
 // empty[S], abort) | meta | bf16 scale table | staged activations | partials.
 size_t tma_smem_bytes(const Plan& p) {
-  const size_t ring = (size_t)p.stages * (kWStage + kSStage) + 8 * 2 * kMaxStages + 16;
+  const size_t ring = (size_t)p.stages * kWStage + kSBlocks * kSBlock + kBarBytes + 16;
   const size_t meta = ((size_t)p.TR * 24 + 15) & ~(size_t)15;
   const size_t xs = (((size_t)p.xs_slots * p.xs_stride * 2) + 15) & ~(size_t)15;
   const size_t red = (size_t)2 * kSlabRows * p.TR * 4;
@@ -317,10 +357,11 @@ qmv_tma_kernel(const QmvArgs a, const Plan pl, const __grid_constant__ CUtensorM
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* bp = smem_raw + (base - raw);
   const int kStages = pl.stages;
-  const uint32_t wst = base, sst = base + kStages * kWStage;
-  const uint32_t bars = sst + kStages * kSStage;
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(bp + kStages * (kWStage + kSStage) + 8 * 2 * kMaxStages);
-  uint8_t* after = bp + kStages * (kWStage + kSStage) + 8 * 2 * kMaxStages + 16;
+  const uint32_t wst = base, sst = base + kStages * kWStage;  // both 1024-byte aligned (16 KB units)
+  const uint32_t bars = sst + kSBlocks * kSBlock;
+  const uint32_t ring_bytes = kStages * kWStage + kSBlocks * kSBlock;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bp + ring_bytes + kBarBytes);
+  uint8_t* after = bp + ring_bytes + kBarBytes + 16;
   const int TR = pl.TR;
   int64_t* s_e = reinterpret_cast<int64_t*>(after);
   int64_t* s_xr = s_e + TR;
@@ -348,6 +389,10 @@ qmv_tma_kernel(const QmvArgs a, const Plan pl, const __grid_constant__ CUtensorM
       mbar_init(bars + 8 * s, 1);                            // full: producer arrive + TMA bytes
       mbar_init(bars + 8 * (kStages + s), kConsumerWarps);  // empty: one arrive per consumer warp
     }
+    for (int b = 0; b < kSBlocks; ++b) {
+      mbar_init(bars + 8 * (2 * kMaxStages + b), 1);
+      mbar_init(bars + 8 * (2 * kMaxStages + kSBlocks + b), kConsumerWarps);
+    }
     *abort_flag = 0;
     s_ncorr = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -358,6 +403,14 @@ qmv_tma_kernel(const QmvArgs a, const Plan pl, const __grid_constant__ CUtensorM
   }
   if (threadIdx.x < 256) lut[threadIdx.x] = e4m3_to_bf16x2_bcast_x2p112(threadIdx.x);
   if (threadIdx.x < 128) lut[256 + threadIdx.x] = 0u;  // the zero block follows the table
+  // Launched as a programmatic dependent (launch overlap on), this CTA may be
+  // running while the previous kernel on the stream finishes. The next kernel
+  // may start as soon as every CTA here has started; the weight planes are
+  // read at once (the caller guarantees no running kernel writes them), the
+  // gather indices and the activations only after the wait below (a no-op
+  // without a programmatic dependency).
+  if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  if (a.rhs != nullptr || a.lhs != nullptr) asm volatile("griddepcontrol.wait;" ::: "memory");
   setup_slots(a, TR, r0, s_e, s_xr, s_pe, s_pm, &s_npass);  // ends with __syncthreads
 
   const int cb = (int)((int64_t)pl.nchunk * rank / pl.C), ce = (int)((int64_t)pl.nchunk * (rank + 1) / pl.C);
@@ -384,6 +437,7 @@ qmv_tma_kernel(const QmvArgs a, const Plan pl, const __grid_constant__ CUtensorM
   auto dst_of = [&](int slot, int ch, int w8) {
     return xs_base + 2u * (uint32_t)(slot * pl.xs_stride + ch * kChunkCols + (4 * (w8 & 7) + (w8 >> 3)) * 8);
   };
+  asm volatile("griddepcontrol.wait;" ::: "memory");  // activations and outputs follow the previous kernel
   const int mode = stage_x_corr<0, kConsumerWarps * 32>(a, pl, cb, ce, dst_of, s_e, s_xr, s_corr, &s_ncorr);
   const bool use_bf16 = mode == 2;
   const int ncorr = mode == 1 ? s_ncorr : 0;
@@ -419,49 +473,51 @@ int sm_count() {
   return sms;
 }
 
-// K split C and slabs per cluster (spc). A CTA's work is spc slabs of
-// (its chunks + one chunk's worth of per-slab cluster synchronisation). One
-// CTA alone keeps an SM only about half busy (eight consumer warps cannot hide
-// the decode latency), two fill it; so the time of a single wave is modelled
-// as (CTAs on the busiest SM) x (CTA work) / min(that count, 2) x 2, and
-// plans that need a second wave as total work / (SMs x rate) plus one CTA of
-// tail. Each CTA also pays about two chunks of staging and set-up.
-template <typename OccFn>
-Plan tma_plan(Plan pl, int64_t row_tiles, OccFn occupancy) {
+// Launch plan: K split C (cluster size), slabs per cluster, ring depth.
+// Modelled time (microseconds of one CTA's wall clock), its constants fitted
+// to plan sweeps of the three decode shapes at 1, 4 and 16 tokens on GB300:
+//   (waves + 0.3 (waves - 1)) * slabs_per_cluster * (chunks_per_slab * w(k) + sync(C, k))
+// `capacity(C, smem)` is the number of CTAs that can be resident at once
+// (clusters must fit a GPC, so a 7-CTA cluster packs worse than a 6-CTA
+// one); k is the most CTAs an SM holds in a wave; w(1) = 0.4 and
+// w(k) = 0.3 k per 16 KB chunk (CTAs on one SM share its copy engine and
+// issue slots); a slab boundary costs a cluster barrier and the exchange of
+// partial sums, 0.2 (1 + 0.1 C) k, doubled for sixteen token slots (0.2
+// without peers). Sixteen token slots cost 1.6x per chunk, each further
+// staged token 2% more.
+template <typename CapFn>
+Plan tma_plan(Plan pl, int64_t row_tiles, CapFn capacity) {
   const int sms = sm_count();
   double best = 1e300;
   Plan out = pl;
   out.C = 0;
+  const double mt_factor = pl.TR > 8 ? 1.6 : 1.0 + 0.02 * (pl.xs_slots - 1);
   for (int C = 1; C <= 16 && C <= pl.nchunk; ++C)
-  for (int stages = kMaxStages; stages >= 2; --stages) {
-    const int per = (pl.nchunk + C - 1) / C;
-    Plan p = pl;
-    p.C = C;
-    p.stages = stages;
-    p.xs_stride = per * kChunkCols + 32;  // 512-byte multiple plus 64 bytes
-    const size_t smem = tma_smem_bytes(p);
-    const int occ = occupancy(smem);  // 0 when it does not fit at all
-    if (occ < 1) continue;
-    const double depth = stages >= 4 ? 1.0 : stages == 3 ? 1.05 : 1.15;  // shallower rings hide less latency
-    for (int64_t spc = 1; spc <= pl.slabs && spc <= 64; ++spc) {
-      const int64_t ctas = (pl.slabs + spc - 1) / spc * C * row_tiles;
-      // per slab: the chunks, a cluster sync worth one chunk (two with 16
-      // token slots, whose reduction is twice as large); plus staging
-      const double work = depth * (double)spc * (per + (p.TR > 8 ? 2 : 1)) + 2.0;
-      double tm;
-      if (ctas <= (int64_t)sms * occ) {
-        const double n = (double)((ctas + sms - 1) / sms);
-        tm = n * work * 2.0 / (n < 2 ? n : 2.0);
-      } else {
-        tm = (double)ctas * work / sms * (occ >= 2 ? 1.0 : 2.0) + work;
-      }
-      if (tm < best - 1e-9) {
-        best = tm;
-        out = p;
-        out.spc = (int)spc;
+    for (int stages = kMaxStages; stages >= 2; --stages) {
+      const int per = (pl.nchunk + C - 1) / C;
+      Plan p = pl;
+      p.C = C;
+      p.stages = stages;
+      p.xs_stride = per * kChunkCols + 32;  // 512-byte multiple plus 64 bytes
+      const int64_t cap = capacity(C, tma_smem_bytes(p));
+      if (cap < 1) continue;
+      const double depth = stages >= 4 ? 1.0 : stages == 3 ? 1.04 : 1.12;  // shallower rings hide less latency
+      const double sync_c = C > 1 ? 0.2 * (1.0 + 0.1 * C) * (pl.TR > 8 ? 2.0 : 1.0) : 0.2;
+      for (int64_t spc = 1; spc <= pl.slabs && spc <= 64; ++spc) {
+        const int64_t ctas = (pl.slabs + spc - 1) / spc * C * row_tiles;
+        const int64_t waves = (ctas + cap - 1) / cap;
+        const int64_t wave_ctas = ctas < cap ? ctas : cap;
+        const int64_t k = (wave_ctas + sms - 1) / sms;
+        const double w = (k <= 1 ? 0.4 : 0.3 * (double)k) * depth * mt_factor;
+        const double sync = C > 1 ? sync_c * (double)(k > 1 ? k : 1) : sync_c;
+        const double tm = ((double)waves + 0.3 * (double)(waves - 1)) * (double)spc * ((double)per * w + sync);
+        if (tm < best - 1e-9) {
+          best = tm;
+          out = p;
+          out.spc = (int)spc;
+        }
       }
     }
-  }
   return out;
 }
 
@@ -484,10 +540,10 @@ cudaError_t launch_mt(const QmvArgs& a, Plan pl, int64_t row_tiles, cudaStream_t
   {
     const cuuint64_t dims[2] = {(cuuint64_t)(a.K / 16), (cuuint64_t)rows};
     const cuuint64_t strides[1] = {(cuuint64_t)(a.K / 16)};
-    const cuuint32_t box[2] = {kChunkCols / 16, kSlabRows};
+    const cuuint32_t box[2] = {kScaleChunks * (kChunkCols / 16), kSlabRows};
     const cuuint32_t es[2] = {1, 1};
     if (enc(&smap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(a.scales), dims, strides, box, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
@@ -526,14 +582,55 @@ cudaError_t launch_mt(const QmvArgs& a, Plan pl, int64_t row_tiles, cudaStream_t
       } else {
         max_dyn = md->second;
       }
-      auto occupancy = [&](size_t smem) {
-        int n = 0;
+      // CTAs of a C-CTA cluster launch that can be resident at once
+      auto capacity = [&](int C, size_t smem) -> int64_t {
         if (smem > (size_t)max_dyn) return 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kTmaThreads, smem) != cudaSuccess) return 0;
-        return n;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)(C * 64), 1, 1);
+        cfg.blockDim = dim3(kTmaThreads, 1, 1);
+        cfg.dynamicSmemBytes = smem;
+        cudaLaunchAttribute at[1];
+        at[0].id = cudaLaunchAttributeClusterDimension;
+        at[0].val.clusterDim.x = (unsigned)C;
+        at[0].val.clusterDim.y = 1;
+        at[0].val.clusterDim.z = 1;
+        cfg.attrs = at;
+        cfg.numAttrs = 1;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
+          cudaGetLastError();
+          return 0;
+        }
+        return (int64_t)n * C;
       };
-      pl = tma_plan(pl, row_tiles, occupancy);
+      pl = tma_plan(pl, row_tiles, capacity);
       cache[key] = pl;
+      if (std::getenv("NVFP4_QMV_PLAN_LOG")) {
+        std::fprintf(stderr, "nvfp4 qmv plan N=%lld K=%lld E=%lld rows=%lld: C=%d slabs/cluster=%d stages=%d; resident CTAs by C:",
+                     (long long)a.N, (long long)a.K, (long long)a.E, (long long)a.R, pl.C, pl.spc, pl.stages);
+        for (int C = 1; C <= 16 && C <= pl.nchunk; ++C) {
+          Plan q = pl;
+          q.C = C;
+          q.xs_stride = ((pl.nchunk + C - 1) / C) * kChunkCols + 32;
+          std::fprintf(stderr, " %d:%lld", C, (long long)capacity(C, tma_smem_bytes(q)));
+        }
+        std::fprintf(stderr, "\n");
+      }
+    }
+  }
+  // NVFP4_QMV_PLAN="C,slabs_per_cluster,stages" overrides the plan (tuning).
+  if (const char* ev = std::getenv("NVFP4_QMV_PLAN")) {
+    int C = 0, spc = 0, stages = 0;
+    if (std::sscanf(ev, "%d,%d,%d", &C, &spc, &stages) == 3 && C >= 1 && C <= 16 && C <= pl.nchunk && spc >= 1 &&
+        stages >= 2 && stages <= kMaxStages) {
+      Plan q = pl;
+      q.C = C;
+      q.spc = spc;
+      q.stages = stages;
+      q.xs_stride = ((pl.nchunk + C - 1) / C) * kChunkCols + 32;
+      std::lock_guard<std::mutex> lock(mu);
+      if (tma_smem_bytes(q) > (size_t)max_dyn_of_dev[dev]) return cudaErrorInvalidConfiguration;
+      pl = q;
     }
   }
   if (pl.C == 0) return cudaErrorInvalidValue;
@@ -544,13 +641,15 @@ cudaError_t launch_mt(const QmvArgs& a, Plan pl, int64_t row_tiles, cudaStream_t
   cfg.blockDim = dim3(kTmaThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = (unsigned)pl.C;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = launch_overlap() ? 2 : 1;
   return cudaLaunchKernelEx(&cfg, kern, a, pl, wmap, smap);
 }
 

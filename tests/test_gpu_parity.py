@@ -292,3 +292,76 @@ def test_gather_tiny_activations_exact(nv):
     ref = O.gather_qmm(x.double().numpy(), lhs, rhs, w, s)
     for r in range(len(rhs)):
         assert rel_err(y[r:r + 1], ref[r:r + 1]) <= TOL["bf16"], f"row {r}"
+
+
+# ------------------------------------------------------------------ launch overlap (programmatic dependent launch)
+
+@pytest.fixture
+def overlap(nv):
+    prev = nv.set_launch_overlap(True)
+    yield
+    nv.set_launch_overlap(prev)
+
+
+@pytest.mark.parametrize("graph", [False, True])
+def test_launch_overlap_chained_calls(nv, overlap, graph):
+    """With launch overlap on, a call whose activations are the previous
+    call's output still reads them only after that call has finished, and a
+    call writing a buffer the previous call reads waits for that read."""
+    K1, N1, N2 = 4096, 8192, 1536
+    w1, s1 = weights(61, N1, K1)
+    w2, s2 = weights(62, N2, N1)
+    g = synth.rng(63)
+    x0 = synth.activations(g, (4, K1), "bf16").cuda()
+    dw1, ds1, dw2, ds2 = u32_to_dev(w1), u8_to_dev(s1), u32_to_dev(w2), u8_to_dev(s2)
+    y1 = torch.empty((4, N1), dtype=torch.bfloat16, device="cuda")
+    y2 = torch.empty((4, N2), dtype=torch.bfloat16, device="cuda")
+
+    def step():
+        nv.qmm(x0, dw1, ds1, out=y1)  # long call
+        nv.qmm(y1, dw2, ds2, out=y2)  # reads y1 (read after write)
+        nv.qmm(x0, dw1, ds1, out=y1)  # rewrites y1 after the second call read it (write after read)
+
+    torch.cuda.synchronize()
+    if graph:
+        step()  # warm up plans outside capture
+        torch.cuda.synchronize()
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr):
+            step()
+        y1.zero_()
+        y2.zero_()
+        gr.replay()
+    else:
+        step()
+    torch.cuda.synchronize()
+    assert nv.take_device_error() == 0
+    ref1 = O.qmm(x0.cpu().double().numpy(), w1, s1, None)
+    assert rel_err(y1, ref1) <= TOL["bf16"]
+    # the second call's reference takes the first call's (bf16) output as input
+    ref2 = O.qmm(y1.cpu().double().numpy(), w2, s2, None)
+    assert rel_err(y2, ref2) <= TOL["bf16"]
+
+
+def test_launch_overlap_gather_indices_from_previous_kernel(nv, overlap):
+    """Indices produced by the kernel just before the gather are read only
+    after it has finished."""
+    E, N, K, B, R = 32, 1536, 2048, 16, 64
+    w, s = weights(71, E, N, K)
+    g = synth.rng(72)
+    x = synth.activations(g, (B, K), "bf16").cuda()
+    base = torch.from_numpy(synth.zipf_experts(g, R, E).astype(np.int64)).cuda()
+    lhs_src = torch.from_numpy(g.integers(0, B, size=R).astype(np.int64)).cuda()
+    dw, ds = u32_to_dev(w), u8_to_dev(s)
+    rhs = torch.zeros(R, dtype=torch.int32, device="cuda")
+    lhs = torch.zeros(R, dtype=torch.int32, device="cuda")
+    for shift in range(1, 4):
+        torch.cuda.synchronize()
+        # elementwise kernels write the indices immediately before the gather
+        rhs.copy_(((base + shift) % E).to(torch.int32))
+        lhs.copy_(((lhs_src + shift) % B).to(torch.int32))
+        y = nv.gather_qmm(x, dw, ds, rhs, lhs)
+        torch.cuda.synchronize()
+        ref = O.gather_qmm(x.cpu().double().numpy(), lhs.cpu().numpy().astype(np.uint32),
+                           rhs.cpu().numpy().astype(np.uint32), w, s)
+        assert rel_err(y, ref) <= TOL["bf16"], f"shift {shift}"
