@@ -45,7 +45,13 @@ METRIC = "qmv HBM GB/s & µs/call, qmm TFLOP/s; fraction of GB300 roofline (1 GP
 
 # dram bytes per launch of the dominant kernel from one ncu capture, and the
 # digest of the kernel source it was taken on (stale -> reported as null).
-TRAFFIC = {"source": None, "kernel_sha": None, "bytes_per_step": None}
+# DRAM bytes (read + write) of the decode kernel per step, from the ncu capture
+# in profiles/qmv_tma_kernel_decode_shapes.md (the three linears at M = 1, whose
+# traffic is the weight planes, times the five token counts); reported only
+# while the kernel sources still hash to kernel_sha.
+TRAFFIC = {"source": "profiles/qmv_tma_kernel_decode_shapes.md", "kernel_sha": "ecacee53173f29f4",
+           "bytes_per_step": 1157903360}
+TRAFFIC_FILES = ("nvfp4_qmv_tma.cu", "nvfp4_qmv_common.cuh", "nvfp4_common.cuh")
 
 
 def qmv_bytes(m, n, k):
@@ -119,9 +125,12 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
-def source_sha(name):
-    with open(os.path.join(ROOT, "nvfp4_quantized_matmul_gb300", "csrc", name), "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+def source_sha(names):
+    h = hashlib.sha256()
+    for name in names:
+        with open(os.path.join(ROOT, "nvfp4_quantized_matmul_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
 # ----------------------------------------------------------------------------- our arm
@@ -254,7 +263,7 @@ def run_ours(args):
     e2e = run_e2e(nv, torch, dev, stream, lin, xs, ys, args, step_bytes)
 
     routes = {} if args.no_routes else run_routes(nv, synth, torch, dev, stream, args)
-    kernel_sha = source_sha("nvfp4_qmv.cu")
+    kernel_sha = source_sha(TRAFFIC_FILES)
     traffic = TRAFFIC["bytes_per_step"] if TRAFFIC["kernel_sha"] == kernel_sha else None
 
     if rank == 0:
@@ -484,6 +493,8 @@ def run_case(args):
     three warm-up calls then one call each at M = 1, 8 and 16.
     qmv_shapes: each decode linear (gate/up, down, qkv; 220 MB) once at M = 1
     and once at M = 16, after one warm-up call each.
+    prefill: the tensor-core route at M = 2048 on the [21504, 5376] plane, one
+    warm-up call then one call.
     """
     import torch
 
@@ -491,6 +502,19 @@ def run_case(args):
     from nvfp4_quantized_matmul_gb300 import synth
 
     dev = torch.device("cuda", 0)
+    if args.case == "prefill":
+        g = synth.rng(5200)
+        n, k, m = 21504, 5376, 2048
+        w = torch.randint(-2**31, 2**31 - 1, (n, k // 8), dtype=torch.int32, device=dev,
+                          generator=torch.Generator(device=dev).manual_seed(7))
+        s = torch.from_numpy(synth.log_uniform_scales(g, (n, k // 16), 2.0**-6, 4.0)).to(dev)
+        gs = torch.from_numpy(synth.global_scales(g, 1)).to(dev)
+        x = synth.activations(g, (m, k), "bf16").to(dev)
+        for _ in range(2):
+            nv.qmm(x, w, s, gs=gs, route="tc")
+        torch.cuda.synchronize(dev)
+        print("case prefill ok")
+        return
     if args.case == "qmv_shapes":
         g = synth.rng(5100)
         lin = []
@@ -563,7 +587,7 @@ def main():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-rows", type=int, default=6144)
     ap.add_argument("--ref-rows", type=int, default=32)
-    ap.add_argument("--case", choices=["qmv_small", "qmv_shapes"], default=None,
+    ap.add_argument("--case", choices=["qmv_small", "qmv_shapes", "prefill"], default=None,
                     help="run one small profiling case instead of the benchmark")
     args = ap.parse_args()
     if args.warmup < 3:

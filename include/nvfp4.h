@@ -110,8 +110,13 @@ int64_t nvfp4_qmm_crossover(nvfp4_dtype x_dtype, int64_t N, int64_t K);
  *   gs NULL (gs_len 0) or [E] (gs_len E); y [R, N] of x_dtype.
  * A row whose expert index is >= E, or whose activation index is >= B, is
  * written as exact +0.0 (no read outside x or w). `sorted_indices` != 0
- * promises rows grouped by expert (a sorted MoE prefill) and enables the
- * expert-batched path; results do not depend on it.
+ * promises expert indices in non-decreasing order (a sorted MoE prefill) and
+ * lets 16-bit calls with enough rows per expert (R >= 512 and R >= 16 E, E <=
+ * 1024, K % 32 == 0) take the expert-batched tensor-core route; the
+ * environment variable NVFP4_GATHER_TC (1/0) forces or disables that route.
+ * If the promise is broken on that route, every output row is still written
+ * once and nothing outside the inputs is read, but rows are computed with
+ * the expert of the sorted segment they fall in.
  */
 nvfp4_status nvfp4_gather_qmm(const void* x, nvfp4_dtype x_dtype, int64_t B, int64_t K, const uint32_t* lhs_indices,
                               const uint32_t* rhs_indices, int64_t R, int sorted_indices, const uint32_t* w,

@@ -241,7 +241,6 @@ nvfp4_status nvfp4_gather_qmm(const void* x, nvfp4_dtype x_dtype, int64_t B, int
                               int64_t w_len, const uint8_t* scales, int64_t scales_len, const float* gs,
                               int64_t gs_len, int64_t E, int64_t N, void* y, void* stream) {
   const char* fn = "nvfp4_gather_qmm";
-  (void)sorted_indices;
   if (!dtype_ok(x_dtype)) return fail(NVFP4_ERR_DTYPE, "%s: unknown activation dtype %d", fn, (int)x_dtype);
   if (B < 0 || R < 0) return fail(NVFP4_ERR_SHAPE, "%s: negative B or R", fn);
   nvfp4_status s = check_planes(fn, w, w_len, scales, scales_len, E, N, K);
@@ -261,6 +260,17 @@ nvfp4_status nvfp4_gather_qmm(const void* x, nvfp4_dtype x_dtype, int64_t B, int
   if (E > INT32_MAX) return fail(NVFP4_ERR_LIMIT, "%s: E=%" PRId64 " exceeds 2^31-1", fn, E);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (K == 0) return cuda_status(fn, cudaMemsetAsync(y, 0, (size_t)(R * N * dtype_size(x_dtype)), st));
+  // Sorted rows with enough of them per expert take the expert-batched
+  // tensor-core route (128-row tiles; below about 16 rows per expert the tiles
+  // would mostly be padding). NVFP4_GATHER_TC=1 forces it where supported,
+  // =0 disables it.
+  if (sorted_indices && x_dtype != NVFP4_F32 && nvfp4::gather_tc_supported(B, K, R, E, N)) {
+    const char* force = std::getenv("NVFP4_GATHER_TC");
+    const bool use = force ? force[0] == '1' : (R >= 512 && R >= 16 * E);
+    if (use)
+      return cuda_status(fn, nvfp4::launch_gather_tc(x, (int)x_dtype, B, K, lhs_indices, rhs_indices, R, w, scales, gs,
+                                                     E, N, y, st));
+  }
   nvfp4::QmvArgs a{x, w, scales, gs, lhs_indices, rhs_indices, B, R, K, N, E, y};
   return cuda_status(fn, run_qmv(a, (int)x_dtype, st));
 }

@@ -76,9 +76,59 @@ struct TcParams {
   const uint8_t* scales;
   const float* gs;
   void* y;
-  int64_t M, N, K;
-  int num_m_tiles, num_tiles, num_kb;
+  int64_t M, N, K;  // M = output rows (R for a gather)
+  int num_m_tiles, num_tiles, num_kb, num_n_tiles;
+  // Expert-batched gather (GatherQMM with rows sorted by expert): output row
+  // r is x[lhs[r]] (x[r] without lhs) times expert rhs[r]'s weights.
+  const uint32_t* lhs;
+  const uint32_t* rhs;
+  int64_t B;  // activation rows
+  int E;      // experts
 };
+
+// One output tile: expert, weight tile, first output row and row count.
+struct Tile {
+  int e, nt, rows;
+  int64_t m0;
+};
+
+// Shared-memory tables of the gather mode: seg[e] = first row of expert e
+// (seg[E] = first row whose expert is out of range), pre[e] = tiles of the
+// experts before e (pre[E] = all tiles).
+constexpr int kGatherMaxE = 1024;
+constexpr int kGatherSamples = 4096;
+constexpr size_t kGatherSmem = (size_t)kGatherSamples * 4 + 2 * (size_t)(kGatherMaxE + 1) * 4 + 16;
+
+template <bool GATHER, int BM>
+__device__ __forceinline__ Tile tile_of(const TcParams& p, int t, const int* seg, const int* pre) {
+  Tile r;
+  if (!GATHER) {
+    const int mt = t % p.num_m_tiles;
+    r.e = 0;
+    r.nt = t / p.num_m_tiles;
+    r.m0 = (int64_t)mt * BM;
+    const int64_t left = p.M - r.m0;
+    r.rows = left < BM ? (int)left : BM;
+    return r;
+  }
+  // largest e with pre[e] <= t; experts without rows have no tiles, so the
+  // search never lands on one
+  int lo = 0, hi = p.E;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (pre[mid] <= t) lo = mid; else hi = mid;
+  }
+  const int e = lo;
+  const int cnt = seg[e + 1] - seg[e];
+  const int mtiles = (cnt + BM - 1) / BM;
+  const int rem = t - pre[e];
+  r.e = e;
+  r.nt = rem / mtiles;  // m tiles fastest: consecutive tiles share a weight tile
+  r.m0 = seg[e] + (int64_t)(rem % mtiles) * BM;
+  const int64_t left = seg[e + 1] - r.m0;
+  r.rows = left < BM ? (int)left : BM;
+  return r;
+}
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
@@ -209,37 +259,51 @@ struct WTask {
 struct WCursor {
   int tile, kb;
   bool done;
+  int e, nt;  // expert and weight tile of `tile`
 };
+
+template <bool GATHER, int BM>
+__device__ __forceinline__ void w_seek(WCursor& cur, const TcParams& p, int num_tiles, const int* seg, const int* pre) {
+  cur.done = cur.tile >= num_tiles;
+  if (!cur.done) {
+    const Tile t = tile_of<GATHER, BM>(p, cur.tile, seg, pre);
+    cur.e = t.e;
+    cur.nt = t.nt;
+  }
+}
 
 template <int BN, int RPT>
 __device__ __forceinline__ void w_load(WTask<RPT>& t, const WCursor& cur, const TcParams& p, int r, int h) {
   if (cur.done) return;
-  const int n_tile = cur.tile / p.num_m_tiles;
   const int64_t kwords = p.K / 8, kgroups = p.K / 16;
+  const uint32_t* w = p.w + (int64_t)cur.e * p.N * kwords;
+  const uint8_t* sc = p.scales + (int64_t)cur.e * p.N * kgroups;
   const int64_t kw = (int64_t)cur.kb * 8 + 4 * h;  // first of this task's four words
   const bool kok = kw < kwords;                     // K % 32 == 0 keeps the four words together
   const int64_t g4 = (int64_t)cur.kb * 4;
 #pragma unroll
   for (int i = 0; i < RPT; ++i) {
-    const int64_t n = (int64_t)n_tile * BN + r + 128 * i;
+    const int64_t n = (int64_t)cur.nt * BN + r + 128 * i;
     const bool ok = kok && n < p.N;
-    t.w[i] = ok ? __ldg(reinterpret_cast<const uint4*>(p.w + n * kwords + kw)) : make_uint4(0, 0, 0, 0);
+    t.w[i] = ok ? __ldg(reinterpret_cast<const uint4*>(w + n * kwords + kw)) : make_uint4(0, 0, 0, 0);
     if (kgroups % 4 == 0) {
-      t.s[i] = ok ? __ldg(reinterpret_cast<const uint32_t*>(p.scales + n * kgroups + g4)) : 0u;
+      t.s[i] = ok ? __ldg(reinterpret_cast<const uint32_t*>(sc + n * kgroups + g4)) : 0u;
     } else {
       uint32_t v = 0;
       for (int j = 0; j < 4; ++j)
-        if (ok && g4 + j < kgroups) v |= (uint32_t)p.scales[n * kgroups + g4 + j] << (8 * j);
+        if (ok && g4 + j < kgroups) v |= (uint32_t)sc[n * kgroups + g4 + j] << (8 * j);
       t.s[i] = v;
     }
   }
 }
 
-__device__ __forceinline__ void w_advance(WCursor& cur, const TcParams& p) {
+template <bool GATHER, int BM>
+__device__ __forceinline__ void w_advance(WCursor& cur, const TcParams& p, int num_tiles, const int* seg,
+                                          const int* pre) {
   if (++cur.kb >= p.num_kb) {
     cur.kb = 0;
     cur.tile += gridDim.x;
-    if (cur.tile >= p.num_tiles) cur.done = true;
+    w_seek<GATHER, BM>(cur, p, num_tiles, seg, pre);
   }
 }
 
@@ -262,20 +326,22 @@ __device__ __forceinline__ void w_store_row(uint32_t stage_base, int row, int h,
   }
 }
 
-template <typename T, typename C>
-__device__ void producer_role(const TcParams& p, uint32_t sB, uint32_t bars, volatile int* abort_flag) {
-  constexpr int STAGES = C::STAGES, RPT = C::RPT;
+template <typename T, typename C, bool GATHER>
+__device__ void producer_role(const TcParams& p, uint32_t sB, uint32_t bars, volatile int* abort_flag, int num_tiles,
+                              const int* seg, const int* pre) {
+  constexpr int STAGES = C::STAGES, RPT = C::RPT, BM = C::BM;
   const int pid = threadIdx.x - C::kWarpProd0 * 32;  // 0..255
   const int r = pid >> 1, h = pid & 1;               // rows r + 128 i, words 4h..4h+3 of the k-block
   const int lane = threadIdx.x & 31;
-  WCursor ld{(int)blockIdx.x, 0, (int)blockIdx.x >= p.num_tiles};
+  WCursor ld{(int)blockIdx.x, 0, true, 0, 0};
+  w_seek<GATHER, BM>(ld, p, num_tiles, seg, pre);
   WTask<RPT> b0, b1, b2;
   w_load<C::BN>(b0, ld, p, r, h);
-  w_advance(ld, p);
+  w_advance<GATHER, BM>(ld, p, num_tiles, seg, pre);
   w_load<C::BN>(b1, ld, p, r, h);
-  w_advance(ld, p);
+  w_advance<GATHER, BM>(ld, p, num_tiles, seg, pre);
   uint32_t u = 0;
-  const int total = ((p.num_tiles - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x) * p.num_kb;
+  const int total = ((num_tiles - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x) * p.num_kb;
   auto consume = [&](const WTask<RPT>& t) -> bool {
     const int s = (int)(u % STAGES);
     const uint32_t ph = (u / STAGES) & 1;
@@ -291,22 +357,97 @@ __device__ void producer_role(const TcParams& p, uint32_t sB, uint32_t bars, vol
   };
   for (int i = 0; i < total; i += 3) {
     w_load<C::BN>(b2, ld, p, r, h);
-    w_advance(ld, p);
+    w_advance<GATHER, BM>(ld, p, num_tiles, seg, pre);
     if (!consume(b0)) return;
     if (i + 1 >= total) break;
     w_load<C::BN>(b0, ld, p, r, h);
-    w_advance(ld, p);
+    w_advance<GATHER, BM>(ld, p, num_tiles, seg, pre);
     if (!consume(b1)) return;
     if (i + 2 >= total) break;
     w_load<C::BN>(b1, ld, p, r, h);
-    w_advance(ld, p);
+    w_advance<GATHER, BM>(ld, p, num_tiles, seg, pre);
     if (!consume(b2)) return;
   }
 }
 
+// Gather mode: builds seg[] and pre[] from the expert indices (all threads of
+// the CTA; ends with __syncthreads). A sample of every L-th index narrows each
+// expert's lower-bound search to at most L rows of global memory. Indices
+// that are not sorted still give non-decreasing segments covering every row
+// below seg[E] exactly once, so no row is written twice or read out of range.
+template <int BM>
+__device__ void build_gather_tables(const TcParams& p, uint32_t* samp, int* seg, int* pre) {
+  const int tid = threadIdx.x, nth = blockDim.x;
+  const int64_t R = p.M;
+  const int64_t L = (R + kGatherSamples - 1) / kGatherSamples;  // >= 1
+  const int ns = (int)((R + L - 1) / L);
+  for (int j = tid; j < ns; j += nth) samp[j] = __ldg(p.rhs + (int64_t)j * L);
+  __syncthreads();
+  for (int e = tid; e <= p.E; e += nth) {
+    const uint32_t ev = (uint32_t)e;
+    int lo = 0, hi = ns;  // first sample >= e
+    while (lo < hi) {
+      const int mid = (lo + hi) >> 1;
+      if (samp[mid] < ev) lo = mid + 1; else hi = mid;
+    }
+    int64_t a = lo == 0 ? 0 : (int64_t)(lo - 1) * L + 1;
+    int64_t b = lo == ns ? R : (int64_t)lo * L;
+    while (a < b) {
+      const int64_t mid = (a + b) >> 1;
+      if (__ldg(p.rhs + mid) < ev) a = mid + 1; else b = mid;
+    }
+    seg[e] = (int)a;
+  }
+  __syncthreads();
+  if (tid < 32) {
+    const int lane = tid;
+    // non-decreasing segment starts (already so for sorted indices)
+    const int n = p.E + 1, per = (n + 31) / 32, b = lane * per, en = min(b + per, n);
+    int run = 0;
+    for (int i = b; i < en; ++i) {
+      run = max(run, seg[i]);
+      seg[i] = run;
+    }
+    int m = run;
+    for (int off = 1; off < 32; off <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, m, off);
+      if (lane >= off) m = max(m, v);
+    }
+    int excl = __shfl_up_sync(0xffffffffu, m, 1);
+    if (lane == 0) excl = 0;
+    for (int i = b; i < en; ++i) seg[i] = max(seg[i], excl);
+    __syncwarp();
+    // tiles of each expert (row tiles times weight tiles), exclusive prefix sum
+    const int ne = p.E, pe = (ne + 31) / 32, b2 = lane * pe, en2 = min(b2 + pe, ne);
+    int sum = 0;
+    for (int i = b2; i < en2; ++i) sum += ((seg[i + 1] - seg[i] + BM - 1) / BM) * p.num_n_tiles;
+    int inc = sum;
+    for (int off = 1; off < 32; off <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, inc, off);
+      if (lane >= off) inc += v;
+    }
+    int base = inc - sum;
+    for (int i = b2; i < en2; ++i) {
+      pre[i] = base;
+      base += ((seg[i + 1] - seg[i] + BM - 1) / BM) * p.num_n_tiles;
+    }
+    if (lane == 31) pre[ne] = inc;
+  }
+  __syncthreads();
+}
+
+__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* map, int c0, int r0, int r1, int r2, int r3,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, "
+      "%4, %5, %6}], [%7];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(bar)
+      : "memory");
+}
+
 // ---------------------------------------------------------------- kernel
 
-template <typename T, typename C>
+template <typename T, typename C, bool GATHER>
 __global__ void __launch_bounds__(C::THREADS, 1)
 qmm_tc_kernel(const __grid_constant__ CUtensorMap xmap, const TcParams p) {
   constexpr int STAGES = C::STAGES, MH = C::MH, BN = C::BN, BM = C::BM, NBUF = C::ACC_BUFS;
@@ -320,6 +461,10 @@ qmm_tc_kernel(const __grid_constant__ CUtensorMap xmap, const TcParams p) {
   uint32_t* holder =
       reinterpret_cast<uint32_t*>(base_ptr + STAGES * (C::A_BYTES + C::B_BYTES) + 8 * (3 * STAGES + 2 * NBUF));
   volatile int* abort_flag = reinterpret_cast<volatile int*>(holder + 1);
+  // gather tables follow the barrier block (16-byte aligned)
+  uint32_t* samp = reinterpret_cast<uint32_t*>(base_ptr + C::SMEM - 1024);
+  int* seg = reinterpret_cast<int*>(samp + kGatherSamples);
+  int* pre = seg + (kGatherMaxE + 1);
   auto fullA = [&](int s) { return bars + 8 * s; };
   auto fullB = [&](int s) { return bars + 8 * (STAGES + s); };
   auto emptyB = [&](int s) { return bars + 8 * (2 * STAGES + s); };
@@ -348,33 +493,73 @@ qmm_tc_kernel(const __grid_constant__ CUtensorMap xmap, const TcParams p) {
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
+  if (GATHER) build_gather_tables<BM>(p, samp, seg, pre);  // ends with __syncthreads
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *holder;
-  const int my_tiles = (int)blockIdx.x < p.num_tiles
-                           ? (p.num_tiles - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x
+  const int num_tiles = GATHER ? pre[p.E] : p.num_tiles;
+  const int my_tiles = (int)blockIdx.x < num_tiles
+                           ? (num_tiles - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x
                            : 0;
 
   if (warp == kWarpTma) {
-    if (lane == 0) {
-      uint32_t u = 0;
+    uint32_t u = 0;
+    if (!GATHER) {
+      if (lane == 0) {
+        bool ok = true;
+        for (int i = 0; i < my_tiles && ok; ++i) {
+          const int tile = (int)blockIdx.x + i * (int)gridDim.x;
+          const int m_tile = tile % p.num_m_tiles;
+          for (int kb = 0; kb < p.num_kb; ++kb, ++u) {
+            const int s = (int)(u % STAGES);
+            const uint32_t ph = (u / STAGES) & 1;
+            if (!wait_bar(emptyB(s), ph ^ 1, abort_flag, 1)) { ok = false; break; }
+            mbar_arrive_tx(fullA(s), C::A_BYTES);
+#pragma unroll
+            for (int h = 0; h < MH; ++h)
+              tma_load_2d(sA + (uint32_t)s * C::A_BYTES + (uint32_t)h * kHalfA, &xmap, kb * BK, m_tile * BM + 128 * h,
+                          fullA(s));
+          }
+        }
+      }
+    } else {
+      // Each lane fetches four activation rows of every 128-row half with one
+      // tile::gather4 copy per k-block; rows past the tile's end or with an
+      // out-of-range activation index read row 0 (their outputs are not
+      // taken from the accumulator).
       bool ok = true;
       for (int i = 0; i < my_tiles && ok; ++i) {
-        const int tile = (int)blockIdx.x + i * (int)gridDim.x;
-        const int m_tile = tile % p.num_m_tiles;
+        const Tile tl = tile_of<true, BM>(p, (int)blockIdx.x + i * (int)gridDim.x, seg, pre);
+        int xr[MH][4];
+#pragma unroll
+        for (int h = 0; h < MH; ++h)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int rr = 128 * h + 4 * lane + j;
+            int64_t v = 0;
+            if (rr < tl.rows) {
+              const int64_t r = tl.m0 + rr;
+              v = p.lhs ? (int64_t)__ldg(p.lhs + r) : r;
+              if (v >= p.B) v = 0;
+            }
+            xr[h][j] = (int)v;
+          }
         for (int kb = 0; kb < p.num_kb; ++kb, ++u) {
           const int s = (int)(u % STAGES);
           const uint32_t ph = (u / STAGES) & 1;
-          if (!wait_bar(emptyB(s), ph ^ 1, abort_flag, 1)) { ok = false; break; }
-          mbar_arrive_tx(fullA(s), C::A_BYTES);
+          if (!wait_bar_warp(emptyB(s), ph ^ 1, abort_flag, 1, &g_tc_error)) { ok = false; break; }
+          if (lane == 0) mbar_arrive_tx(fullA(s), C::A_BYTES);
+          __syncwarp();
 #pragma unroll
           for (int h = 0; h < MH; ++h)
-            tma_load_2d(sA + (uint32_t)s * C::A_BYTES + (uint32_t)h * kHalfA, &xmap, kb * BK, m_tile * BM + 128 * h,
-                        fullA(s));
+            tma_gather4(sA + (uint32_t)s * C::A_BYTES + (uint32_t)h * kHalfA + 512u * (uint32_t)lane, &xmap, kb * BK,
+                        xr[h][0], xr[h][1], xr[h][2], xr[h][3], fullA(s));
         }
       }
-      // Leave no copy in flight: wait (bounded) for the last stages issued.
+    }
+    // Leave no copy in flight: wait (bounded) for the last stages issued.
+    if (lane == 0) {
       const uint32_t first = u > (uint32_t)STAGES ? u - STAGES : 0;
       for (uint32_t v = first; v < u; ++v) {
         const uint32_t limit_ph = (v / STAGES) & 1;
@@ -412,26 +597,41 @@ qmm_tc_kernel(const __grid_constant__ CUtensorMap xmap, const TcParams p) {
       }
     }
   } else if (warp >= kWarpEpi0 && warp < kWarpEpi0 + C::EPI_WARPS) {
-    const int q = warp & 3;                 // TMEM lane quarter this warp may read
+    const int q = warp & 3;                  // TMEM lane quarter this warp may read
     const int hm = (warp - kWarpEpi0) >> 2;  // M half it drains
-    const float fac = global_factor(p.gs, 0);
     T* y = static_cast<T*>(p.y);
+    if (GATHER) {
+      // rows whose expert index is out of range (sorted last) are exact +0
+      const int64_t z0 = seg[p.E];
+      const int64_t total = (p.M - z0) * p.N;
+      const int ethreads = 32 * C::EPI_WARPS, etid = threadIdx.x - 32 * kWarpEpi0;
+      uint16_t* yz = reinterpret_cast<uint16_t*>(y) + z0 * p.N;
+      for (int64_t i = (int64_t)blockIdx.x * ethreads + etid; i < total; i += (int64_t)gridDim.x * ethreads) yz[i] = 0;
+    }
     for (int i = 0; i < my_tiles; ++i) {
-      const int tile = (int)blockIdx.x + i * (int)gridDim.x;
-      const int m_tile = tile % p.num_m_tiles, n_tile = tile / p.num_m_tiles;
+      const Tile tl = tile_of<GATHER, BM>(p, (int)blockIdx.x + i * (int)gridDim.x, seg, pre);
       const int b = i % NBUF;
       if (!wait_bar_warp(accFull(b), (i / NBUF) & 1, abort_flag, 7, &g_tc_error)) break;
       tc_fence_after();
-      const int64_t m = (int64_t)m_tile * BM + 128 * hm + 32 * q + lane;
-      const int64_t n_base = (int64_t)n_tile * BN;
+      const int rr = 128 * hm + 32 * q + lane;  // row within the tile
+      const int64_t m = tl.m0 + rr;
+      const bool live = rr < tl.rows;
+      bool zero = false;
+      if (GATHER && live) {
+        const int64_t xr = p.lhs ? (int64_t)__ldg(p.lhs + m) : m;
+        zero = xr >= p.B;
+      }
+      const float fac = global_factor(p.gs, tl.e);
+      const int64_t n_base = (int64_t)tl.nt * BN;
       const uint32_t tcol = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(b * MH * BN + hm * BN);
 #pragma unroll 1
       for (int c = 0; c < BN / 32; ++c) {
         uint32_t r[32];
         tmem_ld32(tcol + (uint32_t)(32 * c), r);
         tmem_ld_wait();
-        if (m >= p.M) continue;
+        if (!live) continue;
         const int64_t n0 = n_base + 32 * c;
+        if (n0 >= p.N) continue;
         uint32_t packed[16];
 #pragma unroll
         for (int k = 0; k < 16; ++k) {
@@ -441,8 +641,9 @@ qmm_tc_kernel(const __grid_constant__ CUtensorMap xmap, const TcParams p) {
             v1 = __fmul_rn(v1, fac);
           }
           const T t0 = Dt<T>::from_f32(v0), t1 = Dt<T>::from_f32(v1);
-          packed[k] = (uint32_t)(*reinterpret_cast<const uint16_t*>(&t0)) |
-                      ((uint32_t)(*reinterpret_cast<const uint16_t*>(&t1)) << 16);
+          packed[k] = zero ? 0u
+                           : (uint32_t)(*reinterpret_cast<const uint16_t*>(&t0)) |
+                                 ((uint32_t)(*reinterpret_cast<const uint16_t*>(&t1)) << 16);
         }
         T* dst = y + m * p.N + n0;
         if (n0 + 32 <= p.N && (p.N % 8) == 0) {
@@ -461,7 +662,7 @@ qmm_tc_kernel(const __grid_constant__ CUtensorMap xmap, const TcParams p) {
       if (lane == 0) mbar_arrive(accEmpty(b));
     }
   } else if (warp >= C::kWarpProd0) {
-    producer_role<T, C>(p, sB, bars, abort_flag);
+    producer_role<T, C, GATHER>(p, sB, bars, abort_flag, num_tiles, seg, pre);
   }
 
   tc_fence_before();
@@ -509,11 +710,15 @@ cudaError_t launch_cfg(const void* x, int64_t M, int64_t K, const uint32_t* w, c
   p.N = N;
   p.K = K;
   p.num_m_tiles = (int)((M + C::BM - 1) / C::BM);
-  const int num_n_tiles = (int)((N + C::BN - 1) / C::BN);
-  p.num_tiles = p.num_m_tiles * num_n_tiles;
+  p.num_n_tiles = (int)((N + C::BN - 1) / C::BN);
+  p.num_tiles = p.num_m_tiles * p.num_n_tiles;
   p.num_kb = (int)((K + BK - 1) / BK);
+  p.lhs = nullptr;
+  p.rhs = nullptr;
+  p.B = M;
+  p.E = 1;
   const int grid = p.num_tiles < sms ? p.num_tiles : sms;
-  auto kern = qmm_tc_kernel<T, C>;
+  auto kern = qmm_tc_kernel<T, C, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
   if (e != cudaSuccess) return e;
   kern<<<grid, C::THREADS, C::SMEM, st>>>(map, p);
@@ -565,7 +770,67 @@ cudaError_t launch_tc(const void* x, int64_t M, int64_t K, const uint32_t* w, co
   }
 }
 
+// Expert-batched GatherQMM: 128-row tiles (expert segments are short enough
+// that 256-row tiles would mostly compute padding), persistent grid of one
+// CTA per SM; the tile count is known only on the device.
+template <typename T>
+cudaError_t launch_gather(const void* x, int64_t B, int64_t K, const uint32_t* lhs, const uint32_t* rhs, int64_t R,
+                          const uint32_t* w, const uint8_t* scales, const float* gs, int64_t E, int64_t N, void* y,
+                          cudaStream_t st) {
+  using C = Tile128x256;
+  auto enc = encode_fn();
+  if (!enc) return cudaErrorNotSupported;
+  CUtensorMap map;
+  const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)B};
+  const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+  const cuuint32_t box[2] = {BK, 1};  // tile::gather4 takes a one-row box
+  const cuuint32_t estr[2] = {1, 1};
+  const CUtensorMapDataType dt =
+      std::is_same<T, __nv_bfloat16>::value ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  CUresult r = enc(&map, dt, 2, const_cast<void*>(x), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  TcParams p;
+  p.w = w;
+  p.scales = scales;
+  p.gs = gs;
+  p.y = y;
+  p.M = R;
+  p.N = N;
+  p.K = K;
+  p.num_m_tiles = 0;
+  p.num_n_tiles = (int)((N + C::BN - 1) / C::BN);
+  p.num_tiles = 0;  // counted on the device
+  p.num_kb = (int)((K + BK - 1) / BK);
+  p.lhs = lhs;
+  p.rhs = rhs;
+  p.B = B;
+  p.E = (int)E;
+  int dev = 0, sms = 152;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const size_t smem = C::SMEM + kGatherSmem;
+  auto kern = qmm_tc_kernel<T, C, true>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  kern<<<sms, C::THREADS, smem, st>>>(map, p);
+  return cudaGetLastError();
+}
+
 }  // namespace
+
+bool gather_tc_supported(int64_t B, int64_t K, int64_t R, int64_t E, int64_t N) {
+  // 32-bit activation-row coordinates and row counts; K as for the dense route
+  return B > 0 && B < (1ll << 31) && R > 0 && R < (1ll << 31) && E >= 1 && E <= kGatherMaxE && N > 0 && K >= 32 &&
+         K % 32 == 0 && K < (1ll << 31) && ((R + 127) / 128 + E) * ((N + 255) / 256) < (1ll << 31);
+}
+
+cudaError_t launch_gather_tc(const void* x, int xdt, int64_t B, int64_t K, const uint32_t* lhs, const uint32_t* rhs,
+                             int64_t R, const uint32_t* w, const uint8_t* scales, const float* gs, int64_t E, int64_t N,
+                             void* y, cudaStream_t st) {
+  if (xdt == kBF16) return launch_gather<__nv_bfloat16>(x, B, K, lhs, rhs, R, w, scales, gs, E, N, y, st);
+  return launch_gather<__half>(x, B, K, lhs, rhs, R, w, scales, gs, E, N, y, st);
+}
 
 bool qmm_tc_supported(int64_t M, int64_t N, int64_t K) {
   // TMA coordinates are 32-bit; K must keep each 128-bit weight load within

@@ -365,3 +365,91 @@ def test_launch_overlap_gather_indices_from_previous_kernel(nv, overlap):
         ref = O.gather_qmm(x.cpu().double().numpy(), lhs.cpu().numpy().astype(np.uint32),
                            rhs.cpu().numpy().astype(np.uint32), w, s)
         assert rel_err(y, ref) <= TOL["bf16"], f"shift {shift}"
+
+
+# ------------------------------------------------------------------ expert-batched tensor-core gather
+
+# (E, N, K, tokens, top_k): ragged N and K with short segments; R = 16384 so
+# every persistent CTA takes many tiles; 128 Zipf experts, some without rows.
+GATHER_TC_CASES = [(16, 272, 96, 300, 4), (8, 1024, 64, 4096, 4), (128, 256, 256, 512, 8)]
+
+
+@pytest.mark.parametrize("case", GATHER_TC_CASES, ids=lambda v: "E%d_N%d_K%d_T%d_k%d" % v)
+@pytest.mark.parametrize("dt", ["f16", "bf16"])
+def test_gather_sorted_tc_route(nv, monkeypatch, case, dt):
+    monkeypatch.setenv("NVFP4_GATHER_TC", "1")
+    E, N, K, T, topk = case
+    w, s = weights(7 * E + N, E, N, K)
+    g = synth.rng(E + N + K + T)
+    gs = synth.global_scales(g, E)
+    x = synth.activations(g, (T, K), dt)
+    lhs, rhs = synth.zipf_routing(g, T, E, topk)
+    lhs = lhs.copy()
+    bad = g.choice(len(lhs), size=7, replace=False)
+    lhs[bad[:6]] = T + np.arange(6, dtype=np.uint32)  # activation rows out of range inside segments
+    lhs[bad[6]] = 2**32 - 1
+    rhs = np.concatenate([rhs, np.array([E, E, E + 1, 2**32 - 1], dtype=np.uint32)])  # sorted last
+    lhs = np.concatenate([lhs, np.array([0, 1, 2, 3], dtype=np.uint32)])
+    R = len(rhs)
+    y, backing, guard = guarded_empty((R, N), TORCH[dt], fill=-7.0)
+    nv.gather_qmm(x.cuda(), u32_to_dev(w), u8_to_dev(s), u32_to_dev(rhs), u32_to_dev(lhs), gs=f32_to_dev(gs),
+                  sorted_indices=True, out=y)
+    torch.cuda.synchronize()
+    assert nv.take_device_error() == 0
+    ref = O.gather_qmm(x.double().numpy(), lhs, rhs, w, s, gs)
+    yc = y.float().cpu().numpy()
+    zero = (rhs >= E) | (lhs >= T)
+    assert np.all(yc[zero] == 0.0) and not np.any(np.signbit(yc[zero])), "out-of-range rows must be +0.0"
+    assert rel_err(y, ref) <= TOL[dt]
+    assert guards_intact(backing, guard)
+
+
+def test_gather_sorted_tc_identity_lhs(nv, monkeypatch):
+    """Without lhs, row r reads x[r]; rows at or past B are +0.0."""
+    monkeypatch.setenv("NVFP4_GATHER_TC", "1")
+    E, N, K, R = 32, 256, 128, 2048
+    w, s = weights(81, E, N, K)
+    g = synth.rng(82)
+    B = R - 3
+    x = synth.activations(g, (B, K), "bf16")
+    rhs = np.sort(synth.zipf_experts(g, R, E))
+    y = nv.gather_qmm(x.cuda(), u32_to_dev(w), u8_to_dev(s), u32_to_dev(rhs), sorted_indices=True)
+    torch.cuda.synchronize()
+    assert nv.take_device_error() == 0
+    ref = O.gather_qmm(x.double().numpy(), None, rhs, w, s)
+    assert rel_err(y, ref) <= TOL["bf16"]
+    assert np.all(y[B:].float().cpu().numpy() == 0.0)
+
+
+def test_gather_sorted_tc_matches_decode_route(nv, monkeypatch):
+    """The expert-batched and the decode-shape gather compute the same sums."""
+    E, N, K, T, topk = 64, 512, 512, 1024, 4
+    w, s = weights(91, E, N, K)
+    g = synth.rng(92)
+    x = synth.activations(g, (T, K), "bf16").cuda()
+    lhs, rhs = synth.zipf_routing(g, T, E, topk)
+    args = (x, u32_to_dev(w), u8_to_dev(s), u32_to_dev(rhs), u32_to_dev(lhs))
+    monkeypatch.setenv("NVFP4_GATHER_TC", "1")
+    a = nv.gather_qmm(*args, sorted_indices=True).float()
+    monkeypatch.setenv("NVFP4_GATHER_TC", "0")
+    b = nv.gather_qmm(*args, sorted_indices=True).float()
+    assert nv.take_device_error() == 0
+    assert (a - b).abs().max().item() <= 2 * 2.0**-8 * b.abs().max().item()
+
+
+def test_gather_tc_unsorted_promise_is_memory_safe(nv, monkeypatch):
+    """Indices that break the sorted promise still write every row once and
+    read nothing out of range (values are then unspecified)."""
+    monkeypatch.setenv("NVFP4_GATHER_TC", "1")
+    E, N, K, T = 8, 256, 64, 600
+    w, s = weights(95, E, N, K)
+    g = synth.rng(96)
+    x = synth.activations(g, (T, K), "bf16")
+    rhs = g.integers(0, E + 2, size=T).astype(np.uint32)  # unsorted, some out of range
+    y, backing, guard = guarded_empty((T, N), torch.bfloat16, fill=-7.0)
+    nv.gather_qmm(x.cuda(), u32_to_dev(w), u8_to_dev(s), u32_to_dev(rhs), sorted_indices=True, out=y)
+    torch.cuda.synchronize()
+    assert nv.take_device_error() == 0
+    assert guards_intact(backing, guard)
+    assert torch.isfinite(y.float()).all()
+    assert not (y.float() == -7.0).all(dim=1).any(), "a row was left unwritten"
