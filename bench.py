@@ -370,6 +370,33 @@ def run_routes(nv, synth, torch, dev, stream, args):
         del ws, x, y
     out["qmm_prefill"] = pre
 
+    # Route crossover: the decode-shape route against the tensor-core route
+    # for growing M on each decode linear (two weight copies alternate, so the
+    # weights come from HBM); M* is the first M where the tensor cores win.
+    cross = {}
+    for name, n, k in LINEARS:
+        ws = rand_w(n, k, 2, seed=7 * n + k)
+        row = {"M": [], "qmv_us": [], "tc_us": []}
+        first = None
+        for m in (16, 24, 32, 48, 64, 96, 128, 192, 256):
+            x = synth.activations(g, (m, k), "bf16").to(dev)
+            y = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
+            t = {}
+            for route in ("qmv", "tc"):
+                t[route] = time_calls(torch, dev, stream,
+                                      lambda i: nv.qmm(x, ws[i % 2][0], ws[i % 2][1], route=route, out=y), 6)
+            row["M"].append(m)
+            row["qmv_us"].append(round(t["qmv"] * 1e3, 1))
+            row["tc_us"].append(round(t["tc"] * 1e3, 1))
+            if first is None and t["tc"] < t["qmv"]:
+                first = m
+            del x, y
+        row["first_M_tc_faster"] = first
+        row["library_crossover"] = nv.qmm_crossover(torch.bfloat16, n, k)
+        cross[name] = row
+        del ws
+    out["route_crossover"] = cross
+
     # Transcode: one layer's three ModelOpt triplets -> native planes.
     tr = {}
     tot_b, tot_ms = 0.0, 0.0

@@ -128,6 +128,21 @@ def test_crossover_env_override(nv, monkeypatch):
     assert nv.library().nvfp4_qmm_crossover(2, 21504, 5376) == 96
 
 
+def test_crossover_model(nv, monkeypatch):
+    """The default crossover follows the route sweep on GB300: gate/up and
+    qkv switch to the tensor cores within 48-64 token rows, the down
+    projection (21 weight tiles for 152 SMs) only at 96-128; f32 never."""
+    monkeypatch.delenv("NVFP4_QMM_CROSSOVER", raising=False)
+    lib = nv.library()
+    assert lib.nvfp4_qmm_crossover(2, 43008, 5376) == 48
+    assert lib.nvfp4_qmm_crossover(2, 8192, 5376) == 64
+    assert lib.nvfp4_qmm_crossover(2, 5376, 21504) == 128
+    assert lib.nvfp4_qmm_crossover(1, 43008, 5376) == 48
+    assert lib.nvfp4_qmm_crossover(0, 43008, 5376) > 2**62
+    for n, k in ((256, 256), (1 << 20, 64), (64, 1 << 20)):
+        assert 16 <= lib.nvfp4_qmm_crossover(2, n, k) <= 128
+
+
 def test_binding_rejects_cpu_tensors(nv):
     import torch
 
