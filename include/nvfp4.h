@@ -21,7 +21,12 @@
  *   - All data pointers are DEVICE pointers owned by the caller; the library
  *     keeps no reference after the call returns. Lengths are element counts.
  *   - Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL is the
- *     legacy default stream). Nothing is synchronised, nothing is allocated.
+ *     legacy default stream). Nothing is synchronised. The only allocation is
+ *     the decode route's workspace (see nvfp4_qmm): made on the first such
+ *     call on a stream, or the first that needs more, and kept until
+ *     nvfp4_shutdown(). Made while the stream is being captured into a CUDA
+ *     graph, the allocation is done outside the capture (the thread's capture
+ *     mode relaxed for it) and the graph uses that workspace on every replay.
  *   - Data pointers must be 16-byte aligned; index arrays and gs 4-byte.
  *   - K must be a multiple of 16. Any N >= 1 is accepted.
  *   - Empty outputs (M, N or R equal to 0) return NVFP4_OK without a launch.
@@ -88,6 +93,14 @@ nvfp4_status nvfp4_dequantize(const uint32_t* w, int64_t w_len, const uint8_t* s
  *   gs NULL (gs_len 0) or one float (gs_len 1), y [M, N] of x_dtype.
  * The route (decode-shape qmv or the tcgen05 tensor-core path) is chosen by
  * comparing M with nvfp4_qmm_crossover().
+ * With 16-bit activations, 1 <= M <= 16 and K % 256 == 0 the decode route
+ * splits the weight plane evenly over the SMs; a 256-row block of outputs
+ * computed by several CTAs is summed in a float32 workspace owned by the
+ * library, one per (device, stream): 64 bytes per weight row plus a counter
+ * per 256 rows, returned to zero by every call that completes. Calls on one
+ * stream are ordered, so they never share it concurrently. The environment
+ * variable NVFP4_QMV_STREAM=0 selects the cluster-split decode kernel instead
+ * (no workspace).
  */
 nvfp4_status nvfp4_qmm(const void* x, nvfp4_dtype x_dtype, int64_t M, int64_t K, const uint32_t* w,
                        int64_t w_len, const uint8_t* scales, int64_t scales_len, const float* gs,
@@ -123,10 +136,11 @@ nvfp4_status nvfp4_gather_qmm(const void* x, nvfp4_dtype x_dtype, int64_t B, int
                               int64_t w_len, const uint8_t* scales, int64_t scales_len, const float* gs,
                               int64_t gs_len, int64_t E, int64_t N, void* y, void* stream);
 
-/* Error code recorded on the device by a tensor-core kernel whose bounded
+/* Error code recorded on the device by a pipelined kernel whose bounded
  * wait on a pipeline barrier ran out (each wait gives up after 2 s instead of
  * hanging, and the kernel then returns without finishing its tiles); the
- * call reads and clears it. Blocks until all prior work on the current device
+ * call reads and clears it (and, after an error, clears the decode
+ * workspaces). Blocks until all prior work on the current device
  * has finished. Returns 0 when no wait gave up, -1 if the read failed. Not
  * part of the pages' interface: it exists so that a kernel can report a stall
  * instead of holding the GPU. */
@@ -144,6 +158,11 @@ int32_t nvfp4_take_device_error(void);
  * part of the pages' interface: it removes the idle gap between consecutive
  * decode-step matmuls, whose weights are constant. */
 int nvfp4_set_launch_overlap(int enable);
+
+/* Frees the decode route's workspaces on every device. Call only when no
+ * library work is queued or running; a later call allocates again. Not part
+ * of the pages' interface. */
+void nvfp4_shutdown(void);
 
 /* Message for the calling thread's last non-OK status ("" if none). */
 const char* nvfp4_last_error(void);

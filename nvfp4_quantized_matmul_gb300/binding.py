@@ -37,6 +37,7 @@ SIGNATURES = {
     "nvfp4_version": (ctypes.c_char_p, []),
     "nvfp4_take_device_error": (ctypes.c_int32, []),
     "nvfp4_set_launch_overlap": (_INT, [_INT]),
+    "nvfp4_shutdown": (None, []),
 }
 
 
@@ -173,6 +174,11 @@ def set_launch_overlap(enable):
     finishes (the weight planes must not be written by a kernel still running).
     Returns the previous setting."""
     return bool(_lib.nvfp4_set_launch_overlap(int(bool(enable))))
+
+
+def shutdown():
+    """Free the library's workspaces (call with no library work in flight)."""
+    _lib.nvfp4_shutdown()
 
 
 def qmm_crossover(dtype, n, k):

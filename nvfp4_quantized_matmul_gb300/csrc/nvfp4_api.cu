@@ -144,10 +144,12 @@ const char* nvfp4_version(void) { return "nvfp4-gb300 0.1 (sm_103a)"; }
 int nvfp4_set_launch_overlap(int enable) { return nvfp4::g_launch_overlap.exchange(enable ? 1 : 0); }
 
 int32_t nvfp4_take_device_error(void) {
-  const int a = nvfp4::read_tc_error(), b = nvfp4::read_qmv_error();
-  if (a < 0 || b < 0) return -1;
-  return a ? a : b;
+  const int a = nvfp4::read_tc_error(), b = nvfp4::read_qmv_error(), c = nvfp4::read_stream_error();
+  if (a < 0 || b < 0 || c < 0) return -1;
+  return a ? a : b ? b : c;
 }
+
+void nvfp4_shutdown(void) { nvfp4::release_stream_workspaces(); }
 
 nvfp4_status nvfp4_transcode(const uint8_t* mo_weight, int64_t mo_weight_len, const uint8_t* mo_weight_scale,
                              int64_t mo_weight_scale_len, const float* weight_scale_2, int64_t N, int64_t K,

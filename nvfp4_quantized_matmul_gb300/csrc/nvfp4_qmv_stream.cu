@@ -1,0 +1,763 @@
+// Decode-shape NVFP4 QuantizedMatmul as one persistent, evenly split weight
+// stream: y = x @ dequantize(w).T * gs / 2688 for 1 to 16 token rows
+// (mlxcel PR #2629 "ROCm native NVFP4", Summary: qmv for small M, the global
+// scale applied once per output after the f32 sum).
+//
+// GB300 design.
+//  * The product is bound by streaming the packed planes (9/16 byte per
+//    weight). One CTA per SM, each with 16 consumer warps, one TMA producer
+//    warp and one epilogue warp, holds a ring of 32 KB stages (256 weight rows
+//    x 256 columns of packed words, 128-byte swizzled) plus 16 KB scale blocks
+//    (256 rows x 4 chunks of E4M3 bytes, 64-byte swizzled): about 160 KB in
+//    flight per SM, which is what HBM3e needs at its latency.
+//  * Work split. The plane is a grid of tiles (256-row tile, 256-column
+//    chunk). K is cut into S groups only as far as needed for the group's
+//    activations to fit in shared memory (staged once per CTA, f16 when every
+//    value converts exactly); each group's tiles, in row-major order, are
+//    divided evenly over its CTAs (stream-K). A CTA therefore streams a
+//    contiguous run of rows, every SM gets the same number of tiles to within
+//    one, and no cluster or inter-CTA wait is involved.
+//  * A row tile covered by one CTA is finished in place. A row tile split
+//    between CTAs (by the even division or by the K groups) is finished by
+//    whichever contributor arrives last: each adds its partial sums to a f32
+//    workspace row block with vector atomics, then adds its chunk count to the
+//    tile's counter; the one that completes the count (K / 256 chunks) reads
+//    the sums, writes y and zeroes the workspace rows and the counter for the
+//    next call. Nobody waits on another CTA.
+//  * Math (shared with the other decode kernels): each weight word is decoded
+//    exactly into f16 pairs that feed mma.sync m16n8k16 A fragments (weights
+//    are the 16-row A operand, token rows the 8-wide B operand, f32
+//    accumulation on the tensor pipe).
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <cstdio>
+#include <cstdlib>
+#include <map>
+#include <mutex>
+#include <tuple>
+#include <utility>
+#include <vector>
+
+#include "nvfp4_pipe.cuh"
+#include "nvfp4_qmv_common.cuh"
+
+namespace nvfp4 {
+
+__device__ int g_stream_error = 0;  // first error code recorded by a bounded wait
+
+namespace {
+using namespace qmv;
+using namespace pipe;
+
+constexpr int kCW = 16;                      // consumer warps, 16 weight rows each
+constexpr int kProducer = kCW;               // warp issuing the TMA copies
+constexpr int kEpilogue = kCW + 1;           // warp finishing row tiles
+constexpr int kSThreads = (kCW + 2) * 32;    // 576
+constexpr int kTileRows = kCW * 16;          // 256 weight rows per tile
+constexpr uint32_t kWBox = kTileRows * 128;  // one chunk of words: 256 rows x 128 B
+constexpr int kSChunks = 4;                  // chunks per scale block
+constexpr uint32_t kSBox = kTileRows * 64;   // one scale block: 256 rows x 64 B
+constexpr int kMaxStages = 4;
+constexpr int kAccSlots = 16;  // workspace floats per weight row (token slots)
+// A partial-sum buffer holds, per token slot, the 256 row sums of a tile
+// (1 KB, contiguous for the bulk copies) at a stride of 260 floats, which
+// spreads the consumers' stores over the banks.
+constexpr uint32_t kPStride = 260;
+// barriers: full[kMaxStages] empty[kMaxStages] sfull[2] sempty[2] pfull[2]
+// pempty[2] back[1], rounded to 16 bytes (what follows is read 16 B at a time)
+constexpr uint32_t kBarBytes = ((2 * kMaxStages + 9) * 8 + 15) / 16 * 16;
+
+// Launch plan (host).
+struct SPlan {
+  int M;          // token rows, 1..16
+  int nc;         // 256-column chunks in K
+  int ncg;        // chunks per K group
+  int S;          // K groups
+  int gs;         // CTAs per group
+  int64_t nrt;    // 256-row tiles
+  int stages;     // word stages in the ring
+  int xs_stride;  // staged activation row stride, elements (= 32 mod 256)
+  int x_is_bf16;  // activation (and output) dtype is bf16, else f16
+  int pslots;     // token slots held in a partial-sum buffer (8 per MMA tile)
+};
+
+struct Seg {
+  int64_t r;  // row tile
+  int c0, c1;  // chunks [c0, c1) of the CTA's K group
+};
+// A CTA's work within its K group, as tile ranges in row-major tile order
+// (tile = row tile * ncg + chunk). The group's row tiles are dealt out whole,
+// W = nrt / gs consecutive ones per CTA; the nrt mod gs left over are split
+// evenly over all the group's CTAs by tiles. Each CTA does its share of the
+// split rows first, so that finishing those (shared with other CTAs) overlaps
+// the streaming of its whole rows, which it completes alone.
+struct Work {
+  int64_t a0, a1;  // share of the split rows
+  int64_t b0, b1;  // whole rows
+  int ncg;
+  __device__ __forceinline__ static Work of(const SPlan& p, int gi) {
+    Work w;
+    const int64_t W = p.nrt / p.gs, whole = W * p.gs * p.ncg, rest = (p.nrt - W * p.gs) * p.ncg;
+    w.a0 = whole + rest * gi / p.gs;
+    w.a1 = whole + rest * (gi + 1) / p.gs;
+    w.b0 = (int64_t)gi * W * p.ncg;
+    w.b1 = w.b0 + W * p.ncg;
+    w.ncg = p.ncg;
+    return w;
+  }
+  __device__ __forceinline__ bool next(Seg& s) {
+    const bool first = a0 < a1;
+    if (!first && b0 >= b1) return false;
+    const int64_t t = first ? a0 : b0, t1 = first ? a1 : b1;
+    s.r = t / ncg;
+    s.c0 = (int)(t % ncg);
+    const int64_t left = t1 - t;
+    s.c1 = left < (int64_t)(ncg - s.c0) ? s.c0 + (int)left : ncg;
+    if (first)
+      a0 = t + (s.c1 - s.c0);
+    else
+      b0 = t + (s.c1 - s.c0);
+    return true;
+  }
+};
+
+struct Bars {
+  uint32_t base;
+  int ns;
+  __device__ __forceinline__ uint32_t full(uint32_t s) const { return base + 8u * s; }
+  __device__ __forceinline__ uint32_t empty(uint32_t s) const { return base + 8u * (kMaxStages + s); }
+  __device__ __forceinline__ uint32_t sfull(uint32_t b) const { return base + 8u * (2 * kMaxStages + b); }
+  __device__ __forceinline__ uint32_t sempty(uint32_t b) const { return base + 8u * (2 * kMaxStages + 2 + b); }
+  __device__ __forceinline__ uint32_t pfull(uint32_t b) const { return base + 8u * (2 * kMaxStages + 4 + b); }
+  __device__ __forceinline__ uint32_t pempty(uint32_t b) const { return base + 8u * (2 * kMaxStages + 6 + b); }
+  __device__ __forceinline__ uint32_t back() const { return base + 8u * (2 * kMaxStages + 8); }
+};
+
+// Producer (lane 0 of the producer warp): the same tile walk as the
+// consumers; a scale block at the start of each segment and at every fourth
+// chunk, a word stage per chunk.
+__device__ void produce(const SPlan& p, int grp, Work wk, const CUtensorMap* wmap,
+                        const CUtensorMap* smap, uint32_t wst, uint32_t sst, const Bars& bar,
+                        volatile int* abort_flag) {
+  uint32_t u = 0, s = 0, ph = 0, su = 0;  // copies issued, next stage and its phase, scale blocks
+  bool stop = false;
+  Seg sg;
+  while (!stop && wk.next(sg)) {
+    const int row = (int)(sg.r * kTileRows);
+    for (int c = sg.c0; c < sg.c1; ++c) {
+      const int ac = grp * p.ncg + c;  // absolute chunk
+      if (c == sg.c0 || ac % kSChunks == 0) {
+        const uint32_t b = su & 1u, ph = (su >> 1) & 1u;
+        if (!wait_bar(bar.sempty(b), ph ^ 1u, abort_flag, 21, &g_stream_error)) {
+          stop = true;
+          break;
+        }
+        ++su;
+        mbar_arrive_tx(bar.sfull(b), kSBox);
+        tma_load_2d(sst + b * kSBox, smap, (ac / kSChunks) * (kSChunks * 16), row, bar.sfull(b));
+      }
+      if (!wait_bar(bar.empty(s), ph ^ 1u, abort_flag, 22, &g_stream_error)) {
+        stop = true;
+        break;
+      }
+      ++u;
+      mbar_arrive_tx(bar.full(s), kWBox);
+      tma_load_2d(wst + s * kWBox, wmap, ac * kChunkWords, row, bar.full(s));
+      if (++s == (uint32_t)p.stages) {
+        s = 0;
+        ph ^= 1u;
+      }
+    }
+  }
+  // No copy may still be in flight when the CTA exits.
+  const uint32_t first = u > (uint32_t)p.stages ? u - p.stages : 0;
+  for (uint32_t v = first; v < u; ++v) wait_bar_quiet(bar.full(v % p.stages), (v / p.stages) & 1u);
+  const uint32_t sfirst = su > 2u ? su - 2u : 0;
+  for (uint32_t v = sfirst; v < su; ++v) wait_bar_quiet(bar.sfull(v & 1u), (v >> 1) & 1u);
+}
+
+template <typename T, int MT>
+__device__ void consume(const SPlan& p, int grp, Work wk, uint32_t wst, uint32_t sst,
+                        uint32_t pbuf, uint32_t pbuf_bytes, const Bars& bar, volatile int* abort_flag,
+                        uint32_t xs_base, uint32_t zero_base, uint32_t lut_bf, const Corr* corr, int ncorr) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+  const int rg = warp * 16 + g, rg8 = rg + 8;
+  // 128-byte swizzle of the word stage: 16-byte granule j of row r sits at
+  // j ^ (r & 7). This lane reads granules 2t and 2t+1 of rows rg and rg8.
+  const uint32_t oa0 = (uint32_t)rg * 128u + ((uint32_t)((2 * t) ^ (rg & 7)) << 4);
+  const uint32_t oa1 = (uint32_t)rg * 128u + ((uint32_t)((2 * t + 1) ^ (rg & 7)) << 4);
+  const uint32_t ob0 = (uint32_t)rg8 * 128u + ((uint32_t)((2 * t) ^ (rg8 & 7)) << 4);
+  const uint32_t ob1 = (uint32_t)rg8 * 128u + ((uint32_t)((2 * t + 1) ^ (rg8 & 7)) << 4);
+  // 64-byte swizzle of a scale block: granule kb (chunk kb of the block) of
+  // row r sits at kb ^ ((r >> 1) & 3); this lane reads its word t (groups
+  // 4t..4t+3 of the chunk).
+  const uint32_t osa = (uint32_t)rg * 64u + 4u * t, osb = (uint32_t)rg8 * 64u + 4u * t;
+  const uint32_t swa = (uint32_t)((rg >> 1) & 3), swb = (uint32_t)((rg8 >> 1) & 3);
+
+  uint32_t xa[MT], xstep[MT];
+#pragma unroll
+  for (int mt = 0; mt < MT; ++mt) {
+    const int slot = g + 8 * mt;
+    const bool in = slot < p.M;
+    xa[mt] = in ? xs_base + 2u * (uint32_t)(slot * p.xs_stride + 8 * t) : zero_base + 16u * (uint32_t)t;
+    xstep[mt] = in ? 2u * kChunkCols : 0u;
+  }
+
+  constexpr int NA = NAcc<MT>::value;
+  float acc[NA][MT][4];
+  uint32_t s = 0, ph = 0, su = 0, pc = 0;  // word stage and its phase, scale blocks, partial buffers
+  Seg sg;
+  while (wk.next(sg)) {
+#pragma unroll
+    for (int k = 0; k < NA; ++k)
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc[k][mt][i] = 0.f;
+    int cur = 0;  // next residual correction (sorted by column)
+    while (cur < ncorr && corr[cur].col < sg.c0 * kChunkCols) ++cur;
+    for (int c = sg.c0; c < sg.c1; ++c) {
+      const int ac = grp * p.ncg + c, kb = ac % kSChunks;
+      const uint32_t cs = s, cph = ph;  // this chunk's stage
+      if (++s == (uint32_t)p.stages) {
+        s = 0;
+        ph ^= 1u;
+      }
+      const uint32_t sb = su & 1u, sph = (su >> 1) & 1u;
+      const bool first_of_block = c == sg.c0 || kb == 0;
+      const bool last_of_block = c + 1 == sg.c1 || kb == kSChunks - 1;
+      if (last_of_block) ++su;
+      if (first_of_block && !wait_bar_warp(bar.sfull(sb), sph, abort_flag, 23, &g_stream_error)) continue;
+      if (!wait_bar_warp(bar.full(cs), cph, abort_flag, 24, &g_stream_error)) continue;
+      const uint32_t w = wst + cs * kWBox, q = sst + sb * kSBox;
+      const uint32_t qa = q + osa + (((uint32_t)kb ^ swa) << 4), qb = q + osb + (((uint32_t)kb ^ swb) << 4);
+      Chunk chk;
+      chk.a0 = lds128(w + oa0);
+      chk.a1 = lds128(w + oa1);
+      chk.b0 = lds128(w + ob0);
+      chk.b1 = lds128(w + ob1);
+      chk.sa = lds32(qa);
+      chk.sb = lds32(qb);
+      uint32_t xc[MT];
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) xc[mt] = xa[mt] + xstep[mt] * (uint32_t)c;
+      compute_chunk<T, MT>(chk, xc, acc, lut_bf);
+      // residuals of activations that f16 could not hold exactly
+      const int cend = (c + 1) * kChunkCols;
+      for (; cur < ncorr && corr[cur].col < cend; ++cur) {
+        const Corr e = corr[cur];
+        if (((e.slot & 7) >> 1) != t) continue;
+        const int kc = e.col - c * kChunkCols;  // column within the chunk
+        const uint32_t wq = (uint32_t)(kc >> 5), wi = (uint32_t)((kc >> 3) & 3), sh = 4u * (uint32_t)(kc & 7);
+        const uint32_t wa = lds32(w + (uint32_t)rg * 128u + ((wq ^ (uint32_t)(rg & 7)) << 4) + 4u * wi);
+        const uint32_t wb = lds32(w + (uint32_t)rg8 * 128u + ((wq ^ (uint32_t)(rg8 & 7)) << 4) + 4u * wi);
+        const uint32_t grpb = (uint32_t)(kc >> 4);  // 16-column group within the chunk: byte of the granule
+        const uint32_t sa_w = lds32(qa - 4u * t + 4u * (grpb >> 2));
+        const uint32_t sb_w = lds32(qb - 4u * t + 4u * (grpb >> 2));
+        const uint32_t sbyte = 8u * (grpb & 3u);
+        // fp4 * e4m3 * residual is exact in f32 (at most 6 + 8 significant bits)
+        const float da = e2m1_to_f32((wa >> sh) & 0xF) * e4m3_to_f32((sa_w >> sbyte) & 0xFF) * e.r;
+        const float db = e2m1_to_f32((wb >> sh) & 0xF) * e4m3_to_f32((sb_w >> sbyte) & 0xFF) * e.r;
+        const bool odd = e.slot & 1;
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {  // selects, not indexing: the accumulators stay in registers
+          const bool on = (e.slot >> 3) == mt;
+          acc[0][mt][0] += on && !odd ? da : 0.f;
+          acc[0][mt][1] += on && odd ? da : 0.f;
+          acc[0][mt][2] += on && !odd ? db : 0.f;
+          acc[0][mt][3] += on && odd ? db : 0.f;
+        }
+      }
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive_relaxed(bar.empty(cs));
+        if (last_of_block) mbar_arrive_relaxed(bar.sempty(sb));
+      }
+    }
+    // hand the segment's sums to the epilogue warp
+    const uint32_t b = pc & 1u, bph = (pc >> 1) & 1u;
+    ++pc;
+    if (!wait_bar_warp(bar.pempty(b), bph ^ 1u, abort_flag, 25, &g_stream_error)) continue;
+    const uint32_t pb = pbuf + b * pbuf_bytes;
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int row = rg + ((i & 2) ? 8 : 0);
+        const int slot = 8 * mt + 2 * t + (i & 1);
+        float v = 0.f;
+#pragma unroll
+        for (int k = 0; k < NA; ++k) v += acc[k][mt][i];
+        sts_f32(pb + 4u * ((uint32_t)slot * kPStride + (uint32_t)row), v);
+      }
+    mbar_arrive(bar.pfull(b));  // every lane: releases its own stores
+  }
+}
+
+__device__ __forceinline__ void store_out(void* y, int is_bf16, int64_t idx, float v) {
+  if (is_bf16)
+    static_cast<__nv_bfloat16*>(y)[idx] = __float2bfloat16_rn(v);
+  else
+    static_cast<__half*>(y)[idx] = __float2half_rn(v);
+}
+
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(bar)
+               : "memory");
+}
+// Element-wise float add of `bytes` of shared memory into global memory,
+// performed by the copy engine at L2 (the split-tile reduction).
+__device__ __forceinline__ void bulk_add_s2g(float* dst, uint32_t src, uint32_t bytes) {
+  asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.add.f32 [%0], [%1], %2;" ::"l"(dst), "r"(src),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_s2g(void* dst, uint32_t src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(src), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+// Epilogue warp: finishes each segment the consumers hand over. The
+// workspace holds, per token slot, one float per weight row (slot-major, so
+// that a tile's sums for one slot are 1 KB contiguous).
+__device__ void finish(const QmvArgs& a, const SPlan& p, Work wk, uint32_t pbuf, uint32_t pbuf_bytes,
+                       const Bars& bar, volatile int* abort_flag, uint32_t zero_base, float* __restrict__ acc,
+                       uint32_t* __restrict__ cnt) {
+  const int lane = threadIdx.x & 31;
+  const float factor = global_factor(a.gs, 0);
+  const bool has_gs = a.gs != nullptr;
+  const int M = p.M;
+  const int64_t npad = p.nrt * kTileRows;
+  constexpr uint32_t kSlotBytes = kTileRows * 4u;
+  // the zero block (written by generic stores at set-up) is a bulk-copy source
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  uint32_t pc = 0, bc = 0;
+  Seg sg;
+  while (wk.next(sg)) {
+    const uint32_t b = pc & 1u, bph = (pc >> 1) & 1u;
+    ++pc;
+    if (!wait_bar_warp(bar.pfull(b), bph, abort_flag, 26, &g_stream_error)) break;
+    const uint32_t pb = pbuf + b * pbuf_bytes;
+    const int64_t n0 = sg.r * kTileRows;
+    const int rows = (int)(a.N - n0 < kTileRows ? a.N - n0 : kTileRows);
+    bool own = p.S == 1 && sg.c0 == 0 && sg.c1 == p.ncg;  // the whole row tile is this CTA's
+    if (!own) {
+      // Add this piece to the tile's workspace sums (one bulk add per slot;
+      // rows past N add zeros), then count its chunks in.
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // consumers' stores -> copy engine
+      if (lane == 0) {
+        for (int slot = 0; slot < M; ++slot)
+          bulk_add_s2g(acc + slot * npad + n0, pb + (uint32_t)slot * kPStride * 4u, kSlotBytes);
+        bulk_commit();
+        bulk_wait_all();
+        asm volatile("fence.proxy.async.global;" ::: "memory");
+        __threadfence();
+        const uint32_t add = (uint32_t)(sg.c1 - sg.c0);
+        own = atomicAdd(cnt + sg.r, add) + add == (uint32_t)p.nc;  // the last contribution finishes the tile
+      }
+      own = __shfl_sync(0xffffffffu, (int)own, 0) != 0;
+      if (own) {
+        // Bring the completed sums into this buffer, clear the workspace rows
+        // and the counter for the next call.
+        __threadfence();
+        asm volatile("fence.proxy.async.global;" ::: "memory");
+        if (lane == 0) {
+          mbar_arrive_tx(bar.back(), (uint32_t)M * kSlotBytes);
+          for (int slot = 0; slot < M; ++slot)
+            bulk_g2s(pb + (uint32_t)slot * kPStride * 4u, acc + slot * npad + n0, kSlotBytes, bar.back());
+        }
+        const bool ok = wait_bar_warp(bar.back(), bc & 1u, abort_flag, 27, &g_stream_error);
+        ++bc;
+        if (!ok) {
+          wait_bar_quiet(bar.back(), (bc - 1) & 1u);  // the copies must land before the CTA leaves
+          break;
+        }
+        if (lane == 0) {
+          for (int slot = 0; slot < M; ++slot) {
+            bulk_s2g(acc + slot * npad + n0, zero_base, kSlotBytes / 2);
+            bulk_s2g(acc + slot * npad + n0 + kTileRows / 2, zero_base, kSlotBytes / 2);
+          }
+          bulk_commit();
+          atomicExch(cnt + sg.r, 0u);
+        }
+      }
+    }
+    if (own) {  // write y = factor * sum for the tile's rows
+      for (int idx = lane; idx < M * kTileRows; idx += 32) {
+        const int slot = idx / kTileRows, row = idx % kTileRows;
+        if (row >= rows) continue;
+        const float v = lds_f32(pb + 4u * ((uint32_t)slot * kPStride + (uint32_t)row));
+        store_out(a.y, p.x_is_bf16, (int64_t)slot * a.N + n0 + row, has_gs ? __fmul_rn(v, factor) : v);
+      }
+    }
+    __syncwarp();
+    if (lane == 0) {
+      bulk_wait_all();  // nothing of this buffer may still be read by the copy engine
+      mbar_arrive(bar.pempty(b));
+    }
+  }
+  if (lane == 0) bulk_wait_all();
+}
+
+// Dynamic shared memory: [1024-aligned] word stages | scale blocks | partial
+// buffers | barriers, abort flag | slot table | bf16 scale table, zero block |
+// staged activations.
+size_t stream_smem_bytes(const SPlan& p) {
+  const size_t pbuf = (size_t)2 * p.pslots * kPStride * 4;
+  const size_t xs = (((size_t)p.M * p.xs_stride * 2) + 15) & ~(size_t)15;
+  return 1024 + (size_t)p.stages * kWBox + 2 * kSBox + pbuf + kBarBytes + 16 + 256 + 1024 + 512 + 64 + xs;
+}
+
+template <int MT>
+__global__ void __launch_bounds__(kSThreads, 1)
+qmv_stream_kernel(const QmvArgs a, const SPlan p, float* __restrict__ acc, uint32_t* __restrict__ cnt,
+                  const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap smap) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_addr(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* bp = smem_raw + (base - raw);
+  const uint32_t wst = base;                       // stages x 32 KB (1024-aligned)
+  const uint32_t sst = wst + p.stages * kWBox;     // 2 x 16 KB
+  const uint32_t pbuf = sst + 2 * kSBox;           // 2 partial buffers
+  const uint32_t pbuf_bytes = (uint32_t)(p.pslots * kPStride * 4);
+  const Bars bar{pbuf + 2 * pbuf_bytes, p.stages};
+  uint8_t* after_bars = bp + (bar.base - base) + kBarBytes;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(after_bars);
+  int64_t* s_e = reinterpret_cast<int64_t*>(after_bars + 16);  // 16 slots: expert (0 or -1 = no row)
+  int64_t* s_xr = s_e + 16;                                     // and activation row
+  uint32_t* lut = reinterpret_cast<uint32_t*>(after_bars + 16 + 256);
+  const uint32_t lut_bf = smem_addr(lut);
+  // 512 zero bytes stand in for the activations of absent token slots; they
+  // sit 64 bytes (mod 128) before the staged rows so that a lane reading them
+  // and a lane reading row 0 in the same phase use different banks.
+  const uint32_t zero_base = lut_bf + 1024;
+  const uint32_t xs_base = zero_base + 512 + 64;
+  __shared__ Corr s_corr[kMaxCorr];
+  __shared__ int s_ncorr;
+
+  const int warp = threadIdx.x >> 5;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < p.stages; ++s) {
+      mbar_init(bar.full(s), 1);     // producer arrive + TMA bytes
+      mbar_init(bar.empty(s), kCW);  // one arrive per consumer warp
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar.sfull(b), 1);
+      mbar_init(bar.sempty(b), kCW);
+      mbar_init(bar.pfull(b), kCW * 32);  // every consumer lane
+      mbar_init(bar.pempty(b), 1);
+    }
+    mbar_init(bar.back(), 1);
+    *abort_flag = 0;
+    s_ncorr = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (threadIdx.x == kProducer * 32) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&wmap)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&smap)) : "memory");
+  }
+  if (threadIdx.x < 256) lut[threadIdx.x] = e4m3_to_bf16x2_bcast_x2p112(threadIdx.x);
+  if (threadIdx.x < 128) lut[256 + threadIdx.x] = 0u;  // the zero block
+  if (threadIdx.x < 16) {
+    s_e[threadIdx.x] = threadIdx.x < p.M ? 0 : -1;
+    s_xr[threadIdx.x] = threadIdx.x;
+  }
+  // Launched with launch overlap on, this grid may start while the previous
+  // kernel on the stream finishes: the weight planes are streamed at once
+  // (the caller guarantees no running kernel writes them); activations,
+  // outputs and the workspace are touched only after griddepcontrol.wait.
+  if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  __syncthreads();
+
+  const int grp = blockIdx.x / p.gs, gi = blockIdx.x % p.gs;
+  const Work wk = Work::of(p, gi);
+
+  if (warp == kProducer) {
+    if ((threadIdx.x & 31) == 0) produce(p, grp, wk, &wmap, &smap, wst, sst, bar, abort_flag);
+    return;
+  }
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (warp == kEpilogue) {
+    finish(a, p, wk, pbuf, pbuf_bytes, bar, abort_flag, zero_base, acc, cnt);
+    return;
+  }
+  // Consumers: stage this group's activation columns (named barrier 1, 512
+  // threads); column 64t+8q+i of a chunk goes to chunk offset (4q+t)*8+i.
+  Plan sp{};
+  sp.xs_slots = p.M;
+  sp.x_is_bf16 = p.x_is_bf16;
+  auto dst_of = [&](int slot, int ch, int w8) {
+    return xs_base + 2u * (uint32_t)(slot * p.xs_stride + ch * kChunkCols + (4 * (w8 & 7) + (w8 >> 3)) * 8);
+  };
+  const int cb = grp * p.ncg;
+  const int mode = stage_x_corr<0, kCW * 32>(a, sp, cb, cb + p.ncg, dst_of, s_e, s_xr, s_corr, &s_ncorr);
+  if (mode == 2)
+    consume<__nv_bfloat16, MT>(p, grp, wk, wst, sst, pbuf, pbuf_bytes, bar, abort_flag, xs_base, zero_base,
+                               lut_bf, s_corr, 0);
+  else
+    consume<__half, MT>(p, grp, wk, wst, sst, pbuf, pbuf_bytes, bar, abort_flag, xs_base, zero_base, lut_bf,
+                        s_corr, mode == 1 ? s_ncorr : 0);
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+// ---- workspace: one per (device, stream), grown on demand ----
+struct Ws {
+  float* acc = nullptr;
+  uint32_t* cnt = nullptr;
+  int64_t acc_floats = 0, cnt_words = 0;
+};
+std::mutex g_ws_mu;
+std::map<std::pair<int, uintptr_t>, Ws> g_ws;
+std::vector<void*> g_ws_retired;  // replaced buffers, freed by nvfp4_shutdown
+
+// Zeroes device memory on a library-owned stream and waits for it, so the
+// clearing is never part of the caller's stream or of a graph capture.
+cudaError_t zero_now(void* ptr, size_t bytes) {
+  cudaStream_t z = nullptr;
+  cudaError_t e = cudaStreamCreateWithFlags(&z, cudaStreamNonBlocking);
+  if (e != cudaSuccess) return e;
+  e = cudaMemsetAsync(ptr, 0, bytes, z);
+  const cudaError_t e2 = cudaStreamSynchronize(z);
+  cudaStreamDestroy(z);
+  return e != cudaSuccess ? e : e2;
+}
+
+// The workspace of (dev, st), allocated (zeroed) or grown on first need. A
+// stream being captured into a graph (torch.cuda.graph captures on a stream
+// of its own) gets its workspace with the thread's capture mode relaxed for
+// the allocation, the way a stream-ordered allocator does it; the buffer is
+// ready before the graph is ever replayed.
+cudaError_t get_workspace(int dev, cudaStream_t st, int64_t nrt, Ws* out) {
+  std::lock_guard<std::mutex> lock(g_ws_mu);
+  Ws& w = g_ws[{dev, reinterpret_cast<uintptr_t>(st)}];
+  const int64_t need_acc = nrt * kTileRows * kAccSlots, need_cnt = nrt;
+  if (w.acc_floats < need_acc || w.cnt_words < need_cnt) {
+    cudaStreamCaptureMode mode = cudaStreamCaptureModeRelaxed;
+    cudaError_t e = cudaThreadExchangeStreamCaptureMode(&mode);
+    if (e != cudaSuccess) return e;
+    const int64_t acc_n = need_acc > w.acc_floats * 2 ? need_acc : w.acc_floats * 2;
+    const int64_t cnt_n = need_cnt > w.cnt_words * 2 ? need_cnt : w.cnt_words * 2;
+    float* acc = nullptr;
+    uint32_t* cnt = nullptr;
+    e = cudaMalloc(&acc, (size_t)acc_n * sizeof(float));
+    if (e == cudaSuccess) e = cudaMalloc(&cnt, (size_t)cnt_n * sizeof(uint32_t));
+    if (e == cudaSuccess) e = zero_now(acc, (size_t)acc_n * sizeof(float));
+    if (e == cudaSuccess) e = zero_now(cnt, (size_t)cnt_n * sizeof(uint32_t));
+    cudaStreamCaptureMode back = mode;
+    cudaThreadExchangeStreamCaptureMode(&back);
+    if (e != cudaSuccess) {
+      cudaFree(acc);
+      cudaFree(cnt);
+      return e;
+    }
+    if (w.acc) g_ws_retired.push_back(w.acc);
+    if (w.cnt) g_ws_retired.push_back(w.cnt);
+    w.acc = acc;
+    w.cnt = cnt;
+    w.acc_floats = acc_n;
+    w.cnt_words = cnt_n;
+  }
+  *out = w;
+  return cudaSuccess;
+}
+
+int sms_of(int dev) {
+  int sms = 152;
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  return sms;
+}
+
+// Plan: for each ring depth (4, else 3 stages) the fewest K groups whose
+// activation slice fits next to the ring; the depth with fewer groups wins
+// (fewer groups means fewer row tiles finished through the workspace), ties
+// go to the deeper ring. CTAs per group fill the SMs.
+bool make_plan(SPlan& p, int sms, int64_t max_dyn) {
+  const int mt = p.M > 8 ? 2 : 1;
+  p.pslots = 8 * mt;
+  bool found = false;
+  SPlan best{};
+  for (int stages = kMaxStages; stages >= 3; --stages) {
+    for (int S = 1; S <= p.nc && S <= sms; ++S) {
+      if (p.nc % S) continue;
+      SPlan q = p;
+      q.stages = stages;
+      q.S = S;
+      q.ncg = p.nc / S;
+      q.xs_stride = q.ncg * kChunkCols + 32;
+      if ((int64_t)stream_smem_bytes(q) > max_dyn) continue;
+      const int64_t tg = q.nrt * q.ncg;
+      const int64_t per = sms / S;
+      q.gs = (int)(per < tg ? per : tg);
+      if (q.gs < 1) continue;
+      if (!found || q.S < best.S) best = q;
+      found = true;
+      break;
+    }
+  }
+  if (found) p = best;
+  return found;
+}
+
+template <int MT>
+cudaError_t launch_mt(const QmvArgs& a, int xdt, cudaStream_t st) {
+  auto enc = encode_fn();
+  if (!enc) return cudaErrorNotSupported;
+  auto kern = qmv_stream_kernel<MT>;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  using Key = std::tuple<int, int64_t, int64_t, int64_t, int>;
+  static std::mutex mu;
+  static std::map<Key, SPlan> cache;
+  static std::map<int, int64_t> max_dyn_of_dev;
+  SPlan p{};
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    const Key key{dev, a.N, a.K, a.R, xdt};
+    auto it = cache.find(key);
+    if (it != cache.end()) {
+      p = it->second;
+    } else {
+      auto md = max_dyn_of_dev.find(dev);
+      int64_t max_dyn;
+      if (md == max_dyn_of_dev.end()) {
+        int optin = 0;
+        cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+        cudaFuncAttributes fa;
+        if ((e = cudaFuncGetAttributes(&fa, kern)) != cudaSuccess) return e;
+        max_dyn = optin - (int64_t)fa.sharedSizeBytes;
+        if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)max_dyn)) != cudaSuccess)
+          return e;
+        max_dyn_of_dev[dev] = max_dyn;
+      } else {
+        max_dyn = md->second;
+      }
+      p.M = (int)a.R;
+      p.nc = (int)(a.K / kChunkCols);
+      p.nrt = (a.N + kTileRows - 1) / kTileRows;
+      p.x_is_bf16 = xdt == kBF16;
+      if (!make_plan(p, sms_of(dev), max_dyn)) return cudaErrorInvalidConfiguration;
+      cache[key] = p;
+      if (std::getenv("NVFP4_QMV_PLAN_LOG"))
+        std::fprintf(stderr, "nvfp4 qmv stream plan N=%lld K=%lld M=%d: stages=%d S=%d CTAs/group=%d tiles/group=%lld\n",
+                     (long long)a.N, (long long)a.K, p.M, p.stages, p.S, p.gs, (long long)(p.nrt * p.ncg));
+    }
+  }
+  // NVFP4_QMV_STREAM_PLAN="stages,groups" overrides the plan (tuning).
+  if (const char* ev = std::getenv("NVFP4_QMV_STREAM_PLAN")) {
+    int stages = 0, S = 0;
+    if (std::sscanf(ev, "%d,%d", &stages, &S) == 2 && stages >= 2 && stages <= kMaxStages && S >= 1 && S <= p.nc &&
+        p.nc % S == 0) {
+      SPlan q = p;
+      q.stages = stages;
+      q.S = S;
+      q.ncg = p.nc / S;
+      q.xs_stride = q.ncg * kChunkCols + 32;
+      const int64_t per = sms_of(dev) / S, tg = q.nrt * q.ncg;
+      q.gs = (int)(per < tg ? per : tg);
+      std::lock_guard<std::mutex> lock(mu);
+      if (q.gs < 1 || (int64_t)stream_smem_bytes(q) > max_dyn_of_dev[dev]) return cudaErrorInvalidConfiguration;
+      p = q;
+    }
+  }
+  Ws ws;
+  if ((e = get_workspace(dev, st, p.nrt, &ws)) != cudaSuccess) return e;
+  CUtensorMap wmap, smap;
+  {
+    const cuuint64_t dims[2] = {(cuuint64_t)(a.K / 8), (cuuint64_t)a.N};
+    const cuuint64_t strides[1] = {(cuuint64_t)(a.K / 2)};
+    const cuuint32_t box[2] = {kChunkWords, kTileRows};
+    const cuuint32_t es[2] = {1, 1};
+    if (enc(&wmap, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<uint32_t*>(a.w), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  {
+    const cuuint64_t dims[2] = {(cuuint64_t)(a.K / 16), (cuuint64_t)a.N};
+    const cuuint64_t strides[1] = {(cuuint64_t)(a.K / 16)};
+    const cuuint32_t box[2] = {kSChunks * 16, kTileRows};
+    const cuuint32_t es[2] = {1, 1};
+    if (enc(&smap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(a.scales), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(p.S * p.gs), 1, 1);
+  cfg.blockDim = dim3(kSThreads, 1, 1);
+  cfg.dynamicSmemBytes = stream_smem_bytes(p);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = launch_overlap() ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, a, p, ws.acc, ws.cnt, wmap, smap);
+}
+
+}  // namespace
+
+bool qmv_stream_supported(const QmvArgs& a, int xdt) {
+  if (const char* ev = std::getenv("NVFP4_QMV_STREAM"))
+    if (ev[0] == '0') return false;
+  return xdt != kF32 && a.rhs == nullptr && a.lhs == nullptr && a.E == 1 && a.R >= 1 && a.R <= 16 &&
+         a.K % kChunkCols == 0 && a.K > 0 && a.N > 0 && a.N < (1ll << 31) && a.K / kChunkCols <= 4096;
+}
+
+cudaError_t launch_qmv_stream(const QmvArgs& a, int xdt, cudaStream_t st) {
+  return a.R > 8 ? launch_mt<2>(a, xdt, st) : launch_mt<1>(a, xdt, st);
+}
+
+int read_stream_error() {
+  int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_stream_error, sizeof(int)) != cudaSuccess) return -1;
+  if (v) {
+    const int zero = 0;
+    cudaMemcpyToSymbol(g_stream_error, &zero, sizeof(int));
+    // An aborted kernel may have left partial sums and counts behind: clear
+    // every workspace once all work has finished.
+    cudaDeviceSynchronize();
+    std::lock_guard<std::mutex> lock(g_ws_mu);
+    int cur = 0;
+    cudaGetDevice(&cur);
+    for (auto& kv : g_ws) {
+      cudaSetDevice(kv.first.first);
+      cudaDeviceSynchronize();
+      zero_now(kv.second.acc, (size_t)kv.second.acc_floats * sizeof(float));
+      zero_now(kv.second.cnt, (size_t)kv.second.cnt_words * sizeof(uint32_t));
+    }
+    cudaSetDevice(cur);
+  }
+  return v;
+}
+
+void release_stream_workspaces() {
+  std::lock_guard<std::mutex> lock(g_ws_mu);
+  for (auto& kv : g_ws) {
+    cudaFree(kv.second.acc);
+    cudaFree(kv.second.cnt);
+  }
+  g_ws.clear();
+  for (void* ptr : g_ws_retired) cudaFree(ptr);
+  g_ws_retired.clear();
+}
+
+}  // namespace nvfp4
