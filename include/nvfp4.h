@@ -111,6 +111,26 @@ nvfp4_status nvfp4_qmm_routed(const void* x, nvfp4_dtype x_dtype, int64_t M, int
                               int64_t w_len, const uint8_t* scales, int64_t scales_len, const float* gs,
                               int64_t gs_len, int64_t N, void* y, nvfp4_route route, void* stream);
 
+/*
+ * nvfp4_qmm for callers that must not allocate device memory: a runtime whose
+ * memory is planned once at start-up, or code that runs while a CUDA graph is
+ * captured in the strict mode, where an allocation would break the capture.
+ * Same arguments and result as nvfp4_qmm, always on the decode route; its
+ * scratch is a fixed array inside the library (4 MB plus 1 KB, held on every
+ * GPU that loads the library until the process exits). Limits: f16 or bf16
+ * activations, 1 <= M <= 16, K a multiple of 256 (at most 2^20), N at most
+ * 65536; other shapes are refused (NVFP4_ERR_DTYPE / _SHAPE / _LIMIT) before
+ * anything is queued. Nothing is allocated: the first call on a device looks
+ * up the array's device address (make that call before any stream capture),
+ * and every call clears the part of the array it uses on `stream` before its
+ * kernel. All calls share the one array, so calls whose work overlaps on the
+ * GPU (on different streams) race and give wrong results: order them. The
+ * pages have no counterpart of this entry point.
+ */
+nvfp4_status nvfp4_qmm_noalloc(const void* x, nvfp4_dtype x_dtype, int64_t M, int64_t K, const uint32_t* w,
+                               int64_t w_len, const uint8_t* scales, int64_t scales_len, const float* gs,
+                               int64_t gs_len, int64_t N, void* y, void* stream);
+
 /* Smallest M routed to the tensor-core path for this shape and dtype. The
  * environment variable NVFP4_QMM_CROSSOVER overrides it. */
 int64_t nvfp4_qmm_crossover(nvfp4_dtype x_dtype, int64_t N, int64_t K);

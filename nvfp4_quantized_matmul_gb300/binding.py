@@ -31,6 +31,7 @@ SIGNATURES = {
     "nvfp4_qmm": (_INT, [_P, _INT, _I64, _I64, _P, _I64, _P, _I64, _P, _I64, _I64, _P, _P]),
     "nvfp4_qmm_routed": (_INT, [_P, _INT, _I64, _I64, _P, _I64, _P, _I64, _P, _I64, _I64, _P, _INT, _P]),
     "nvfp4_qmm_crossover": (_I64, [_INT, _I64, _I64]),
+    "nvfp4_qmm_noalloc": (_INT, [_P, _INT, _I64, _I64, _P, _I64, _P, _I64, _P, _I64, _I64, _P, _P]),
     "nvfp4_gather_qmm": (_INT, [_P, _INT, _I64, _I64, _P, _P, _I64, _INT, _P, _I64, _P, _I64, _P, _I64,
                                 _I64, _I64, _P, _P]),
     "nvfp4_last_error": (ctypes.c_char_p, []),
@@ -146,6 +147,21 @@ def qmm(x, w, scales, gs=None, route="auto", out=None):
         out = torch.empty((m, n), dtype=x.dtype, device=x.device)
     check(_lib.nvfp4_qmm_routed(_ptr(x), DTYPE_CODE[x.dtype], m, k, _ptr(w), w.numel(), _ptr(scales),
                                 scales.numel(), _ptr(gs), _n(gs), n, _ptr(out), ROUTE_CODE[route], _stream(x)))
+    return out
+
+
+def qmm_noalloc(x, w, scales, gs=None, out=None):
+    """nvfp4_qmm without any device allocation by the library (fixed scratch
+    inside it; 16-bit x, M <= 16, K % 256 == 0, N <= 65536). Calls that could
+    overlap on the GPU must be ordered: they share that scratch."""
+    _cuda(x, w, scales)
+    m, k = x.shape
+    n = w.shape[0]
+    gs = _gs_tensor(gs, x.device)
+    if out is None:
+        out = torch.empty((m, n), dtype=x.dtype, device=x.device)
+    check(_lib.nvfp4_qmm_noalloc(_ptr(x), DTYPE_CODE[x.dtype], m, k, _ptr(w), w.numel(), _ptr(scales),
+                                 scales.numel(), _ptr(gs), _n(gs), n, _ptr(out), _stream(x)))
     return out
 
 

@@ -254,6 +254,33 @@ nvfp4_status nvfp4_qmm(const void* x, nvfp4_dtype x_dtype, int64_t M, int64_t K,
                           stream);
 }
 
+nvfp4_status nvfp4_qmm_noalloc(const void* x, nvfp4_dtype x_dtype, int64_t M, int64_t K, const uint32_t* w,
+                               int64_t w_len, const uint8_t* scales, int64_t scales_len, const float* gs,
+                               int64_t gs_len, int64_t N, void* y, void* stream) {
+  const char* fn = "nvfp4_qmm_noalloc";
+  if (x_dtype != NVFP4_F16 && x_dtype != NVFP4_BF16)
+    return fail(NVFP4_ERR_DTYPE, "%s: takes f16 or bf16 activations (dtype %d)", fn, (int)x_dtype);
+  if (M < 0) return fail(NVFP4_ERR_SHAPE, "%s: negative M", fn);
+  nvfp4_status s = check_planes(fn, w, w_len, scales, scales_len, 1, N, K);
+  if (s) return s;
+  if ((s = check_gs(fn, gs, gs_len, 1))) return s;
+  int64_t xe;
+  if (!mul_ok(M, K, &xe) || !mul_ok(M, N, &xe)) return fail(NVFP4_ERR_SHAPE, "%s: M*K or M*N overflows", fn);
+  if (M == 0 || N == 0) return ok();
+  if (!y || (K > 0 && !x)) return fail(NVFP4_ERR_NULL, "%s: x or y is NULL", fn);
+  if (!aligned(x, 16) || !aligned(y, 16)) return fail(NVFP4_ERR_ALIGN, "%s: x and y must be 16-byte aligned", fn);
+  if (M > 16) return fail(NVFP4_ERR_LIMIT, "%s: M=%" PRId64 " exceeds 16 token rows", fn, M);
+  if (K % 256) return fail(NVFP4_ERR_SHAPE, "%s: K=%" PRId64 " is not a multiple of 256", fn, K);
+  if (K > (int64_t)1 << 20) return fail(NVFP4_ERR_LIMIT, "%s: K=%" PRId64 " exceeds 2^20", fn, K);
+  if (N > nvfp4::kNoAllocMaxRows)
+    return fail(NVFP4_ERR_LIMIT, "%s: N=%" PRId64 " exceeds the %" PRId64 " weight rows its fixed scratch covers", fn, N,
+                nvfp4::kNoAllocMaxRows);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (K == 0) return cuda_status(fn, cudaMemsetAsync(y, 0, (size_t)(M * N * dtype_size(x_dtype)), st));
+  nvfp4::QmvArgs a{x, w, scales, gs, nullptr, nullptr, M, M, K, N, 1, y};
+  return cuda_status(fn, nvfp4::launch_qmv_stream_noalloc(a, (int)x_dtype, st));
+}
+
 nvfp4_status nvfp4_gather_qmm(const void* x, nvfp4_dtype x_dtype, int64_t B, int64_t K, const uint32_t* lhs_indices,
                               const uint32_t* rhs_indices, int64_t R, int sorted_indices, const uint32_t* w,
                               int64_t w_len, const uint8_t* scales, int64_t scales_len, const float* gs,

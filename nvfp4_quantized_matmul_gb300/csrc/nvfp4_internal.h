@@ -46,6 +46,10 @@ bool qmv_stream_supported(const QmvArgs& a, int xdt);
 cudaError_t launch_qmv_stream(const QmvArgs& a, int xdt, cudaStream_t st);
 int read_stream_error();
 void release_stream_workspaces();
+// The same route with its scratch in a fixed array inside the library (no
+// allocation); at most kNoAllocMaxRows weight rows.
+constexpr int64_t kNoAllocMaxRows = 65536;
+cudaError_t launch_qmv_stream_noalloc(const QmvArgs& a, int xdt, cudaStream_t st);
 
 // Whether weight-streaming launches may overlap the previous kernel on the
 // stream (programmatic dependent launch; see nvfp4_set_launch_overlap).

@@ -616,7 +616,7 @@ bool make_plan(SPlan& p, int sms, int64_t max_dyn) {
 }
 
 template <int MT>
-cudaError_t launch_mt(const QmvArgs& a, int xdt, cudaStream_t st) {
+cudaError_t launch_mt(const QmvArgs& a, int xdt, cudaStream_t st, const Ws* given = nullptr) {
   auto enc = encode_fn();
   if (!enc) return cudaErrorNotSupported;
   auto kern = qmv_stream_kernel<MT>;
@@ -678,7 +678,10 @@ cudaError_t launch_mt(const QmvArgs& a, int xdt, cudaStream_t st) {
     }
   }
   Ws ws;
-  if ((e = get_workspace(dev, st, p.nrt, &ws)) != cudaSuccess) return e;
+  if (given)
+    ws = *given;
+  else if ((e = get_workspace(dev, st, p.nrt, &ws)) != cudaSuccess)
+    return e;
   CUtensorMap wmap, smap;
   {
     const cuuint64_t dims[2] = {(cuuint64_t)(a.K / 8), (cuuint64_t)a.N};
@@ -747,6 +750,63 @@ int read_stream_error() {
     cudaSetDevice(cur);
   }
   return v;
+}
+
+// ---- allocation-free variant --------------------------------------------
+//
+// The same decode kernel, with its scratch (the split-tile sums and the tile
+// counters) in a fixed array compiled into the library instead of a
+// workspace from cudaMalloc. It serves callers that must not allocate device
+// memory: a runtime whose memory is planned once at start-up, or code that
+// runs while a CUDA graph is being captured in the strict mode, where an
+// allocation would break the capture. The array costs every GPU that loads
+// the library kNoAllocBytes until the process exits.
+namespace {
+constexpr int64_t kNoAllocAccFloats = (int64_t)kAccSlots * kNoAllocMaxRows;  // 4 MB of sums
+constexpr int64_t kNoAllocCounters = kNoAllocMaxRows / kTileRows;           // one per 256-row tile
+static __device__ __align__(256) float g_noalloc_scratch[kNoAllocAccFloats + kNoAllocCounters];
+
+struct NoAllocDev {
+  float* base = nullptr;  // device address of g_noalloc_scratch on this device
+  bool ready = false;
+};
+std::mutex g_noalloc_mu;
+std::map<int, NoAllocDev> g_noalloc;
+
+// Device address of the array on the current device (its host-side name is
+// only a stand-in), looked up once per device.
+cudaError_t noalloc_base(int dev, float** out) {
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  NoAllocDev& d = g_noalloc[dev];
+  if (!d.ready) {
+    void* ptr = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+    if (e != cudaSuccess) return e;
+    d.base = static_cast<float*>(ptr);
+    d.ready = true;
+  }
+  *out = d.base;
+  return cudaSuccess;
+}
+}  // namespace
+
+cudaError_t launch_qmv_stream_noalloc(const QmvArgs& a, int xdt, cudaStream_t st) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  float* base = nullptr;
+  if ((e = noalloc_base(dev, &base)) != cudaSuccess) return e;
+  const int64_t nrt = (a.N + kTileRows - 1) / kTileRows;
+  Ws ws;
+  ws.acc = base;
+  ws.cnt = reinterpret_cast<uint32_t*>(base + kNoAllocAccFloats);
+  ws.acc_floats = kNoAllocAccFloats;
+  ws.cnt_words = kNoAllocCounters;
+  // The kernel indexes the sums as [slot][nrt * 256]: clear the slots this
+  // call uses and its tile counters (a previous call may have been cut short).
+  if ((e = cudaMemsetAsync(ws.cnt, 0, (size_t)nrt * sizeof(uint32_t), st)) != cudaSuccess) return e;
+  if ((e = cudaMemsetAsync(ws.acc, 0, (size_t)a.R * nrt * kTileRows * sizeof(float), st)) != cudaSuccess) return e;
+  return a.R > 8 ? launch_mt<2>(a, xdt, st, &ws) : launch_mt<1>(a, xdt, st, &ws);
 }
 
 void release_stream_workspaces() {
