@@ -58,7 +58,7 @@ constexpr int kTileRows = kCW * 16;          // 256 weight rows per tile
 constexpr uint32_t kWBox = kTileRows * 128;  // one chunk of words: 256 rows x 128 B
 constexpr int kSChunks = 4;                  // chunks per scale block
 constexpr uint32_t kSBox = kTileRows * 64;   // one scale block: 256 rows x 64 B
-constexpr int kMaxStages = 4;
+constexpr int kMaxStages = 6;
 constexpr int kAccSlots = 16;  // workspace floats per weight row (token slots)
 // A partial-sum buffer holds, per token slot, the 256 row sums of a tile
 // (1 KB, contiguous for the bulk copies) at a stride of 260 floats, which
@@ -77,6 +77,7 @@ struct SPlan {
   int gs;         // CTAs per group
   int64_t nrt;    // 256-row tiles
   int stages;     // word stages in the ring
+  int xs_chunks;  // most chunks of activations a CTA stages
   int xs_stride;  // staged activation row stride, elements (= 32 mod 256)
   int x_is_bf16;  // activation (and output) dtype is bf16, else f16
   int pslots;     // token slots held in a partial-sum buffer (8 per MMA tile)
@@ -134,40 +135,189 @@ struct Bars {
   __device__ __forceinline__ uint32_t back() const { return base + 8u * (2 * kMaxStages + 8); }
 };
 
-// Producer (lane 0 of the producer warp): the same tile walk as the
+// The chunks of its K group a CTA visits form a circular run: staged chunk j
+// holds group chunk (first + j) mod ncg, j < count. Whole rows visit them all.
+struct XRun {
+  int first, count;
+};
+__device__ __forceinline__ XRun x_run(const SPlan& p, const Work& wk) {
+  if (wk.b1 > wk.b0 || wk.a1 - wk.a0 >= p.ncg) return XRun{0, p.ncg};
+  return XRun{(int)(wk.a0 % p.ncg), (int)(wk.a1 - wk.a0)};
+}
+
+// Stages the CTA's run of activation columns for every token row, 8 columns
+// per 16-byte unit, column 64t+8q+i of a chunk at chunk offset (4q+t)*8+i.
+// bf16 inputs are staged as f16 when that is exact; a value f16 cannot hold
+// exactly but within its range is split into its f16 part and an f32
+// residual (up to kMaxCorr of them, recorded by group-relative column and
+// sorted); otherwise the bf16 values are staged. Returns 0 (f16), 1 (f16 with
+// residuals) or 2 (bf16). Threads 0 .. kN-1 (the consumer warps) take part;
+// *n_corr must be zero and visible on entry. Loads are issued four at a time
+// per thread so that their latencies overlap.
+template <int kN>
+__device__ int stage_run(const QmvArgs& a, const SPlan& p, int chunk0, XRun run, uint32_t xs_base, Corr* corr,
+                         int* n_corr) {
+  constexpr int kBatch = 4;
+  const int per_slot = run.count * (kChunkCols / 8), units = p.M * per_slot;
+  const int tid = (int)threadIdx.x;
+  const uint16_t* xg = static_cast<const uint16_t*>(a.x);
+  auto locate = [&](int u, int64_t& src, uint32_t& dst, int& gcol) {
+    const int slot = u / per_slot, rem = u % per_slot, j = rem >> 5, w8 = rem & 31;
+    int gc = run.first + j;
+    if (gc >= p.ncg) gc -= p.ncg;
+    gcol = gc * kChunkCols + 8 * w8;  // group-relative column
+    src = (int64_t)slot * a.K + (int64_t)chunk0 * kChunkCols + gcol;
+    dst = xs_base + 2u * (uint32_t)(slot * p.xs_stride + j * kChunkCols + (4 * (w8 & 7) + (w8 >> 3)) * 8);
+  };
+  int hard = 0;
+  for (int u0 = tid; u0 < units; u0 += kBatch * kN) {
+    uint4 v[kBatch];
+#pragma unroll
+    for (int b = 0; b < kBatch; ++b) {
+      const int u = u0 + b * kN;
+      v[b] = make_uint4(0, 0, 0, 0);
+      if (u < units) {
+        int64_t src;
+        uint32_t dst;
+        int gcol;
+        locate(u, src, dst, gcol);
+        v[b] = __ldg(reinterpret_cast<const uint4*>(xg + src));
+      }
+    }
+#pragma unroll
+    for (int b = 0; b < kBatch; ++b) {
+      const int u = u0 + b * kN;
+      if (u >= units) continue;
+      int64_t src;
+      uint32_t dst;
+      int gcol;
+      locate(u, src, dst, gcol);
+      uint4 o = v[b];
+      if (p.x_is_bf16) {
+        const uint32_t in[4] = {v[b].x, v[b].y, v[b].z, v[b].w};
+        uint32_t h2[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float lo = __uint_as_float(in[q] << 16), hi = __uint_as_float(in[q] & 0xFFFF0000u);
+          const __half2 h = __floats2half2_rn(lo, hi);
+          const float2 back = __half22float2(h);
+          h2[q] = *reinterpret_cast<const uint32_t*>(&h);
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const float xv = e ? hi : lo, bv = e ? back.y : back.x;
+            if (bv != xv) {
+              if (!(fabsf(xv) <= 65504.f)) {  // beyond f16's range, or NaN
+                hard = 1;
+              } else {
+                const int i = atomicAdd(n_corr, 1);
+                if (i < kMaxCorr)
+                  corr[i] = Corr{u / per_slot, gcol + 2 * q + e, xv - bv};
+                else
+                  hard = 1;
+              }
+            }
+          }
+        }
+        o = make_uint4(h2[0], h2[1], h2[2], h2[3]);
+      }
+      asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(o.x), "r"(o.y), "r"(o.z), "r"(o.w));
+    }
+  }
+  if (sync_or<kN>(hard)) {  // keep the exact bf16 activations instead
+    for (int u0 = tid; u0 < units; u0 += kBatch * kN) {
+      uint4 v[kBatch];
+#pragma unroll
+      for (int b = 0; b < kBatch; ++b) {
+        const int u = u0 + b * kN;
+        v[b] = make_uint4(0, 0, 0, 0);
+        if (u < units) {
+          int64_t src;
+          uint32_t dst;
+          int gcol;
+          locate(u, src, dst, gcol);
+          v[b] = __ldg(reinterpret_cast<const uint4*>(xg + src));
+        }
+      }
+#pragma unroll
+      for (int b = 0; b < kBatch; ++b) {
+        const int u = u0 + b * kN;
+        if (u >= units) continue;
+        int64_t src;
+        uint32_t dst;
+        int gcol;
+        locate(u, src, dst, gcol);
+        asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(v[b].x), "r"(v[b].y), "r"(v[b].z),
+                     "r"(v[b].w));
+      }
+    }
+    sync_all<kN>();
+    return 2;
+  }
+  const int nc = *n_corr;
+  if (nc == 0) return 0;
+  if (tid == 0) {  // sort by column (at most kMaxCorr entries)
+    for (int i = 1; i < nc; ++i) {
+      const Corr k = corr[i];
+      int j = i - 1;
+      while (j >= 0 && corr[j].col > k.col) {
+        corr[j + 1] = corr[j];
+        --j;
+      }
+      corr[j + 1] = k;
+    }
+  }
+  sync_all<kN>();
+  return 1;
+}
+
+// Position in a CTA's chunk sequence (the order every role walks).
+struct ChunkPos {
+  Work wk;
+  Seg sg;
+  int c;
+  bool valid;
+  __device__ __forceinline__ void start(const Work& w) {
+    wk = w;
+    valid = wk.next(sg);
+    c = valid ? sg.c0 : 0;
+  }
+  __device__ __forceinline__ void advance() {
+    if (valid && ++c >= sg.c1) {
+      valid = wk.next(sg);
+      if (valid) c = sg.c0;
+    }
+  }
+  // the scale block covering this chunk is loaded here (segment start or a
+  // block boundary)
+  __device__ __forceinline__ bool block_start(int ac) const { return c == sg.c0 || ac % kSChunks == 0; }
+};
+
+// Producer (lane 0 of the producer warp): the same chunk walk as the
 // consumers; a scale block at the start of each segment and at every fourth
 // chunk, a word stage per chunk.
 __device__ void produce(const SPlan& p, int grp, Work wk, const CUtensorMap* wmap,
                         const CUtensorMap* smap, uint32_t wst, uint32_t sst, const Bars& bar,
                         volatile int* abort_flag) {
   uint32_t u = 0, s = 0, ph = 0, su = 0;  // copies issued, next stage and its phase, scale blocks
-  bool stop = false;
-  Seg sg;
-  while (!stop && wk.next(sg)) {
-    const int row = (int)(sg.r * kTileRows);
-    for (int c = sg.c0; c < sg.c1; ++c) {
-      const int ac = grp * p.ncg + c;  // absolute chunk
-      if (c == sg.c0 || ac % kSChunks == 0) {
-        const uint32_t b = su & 1u, ph = (su >> 1) & 1u;
-        if (!wait_bar(bar.sempty(b), ph ^ 1u, abort_flag, 21, &g_stream_error)) {
-          stop = true;
-          break;
-        }
-        ++su;
-        mbar_arrive_tx(bar.sfull(b), kSBox);
-        tma_load_2d(sst + b * kSBox, smap, (ac / kSChunks) * (kSChunks * 16), row, bar.sfull(b));
-      }
-      if (!wait_bar(bar.empty(s), ph ^ 1u, abort_flag, 22, &g_stream_error)) {
-        stop = true;
-        break;
-      }
-      ++u;
-      mbar_arrive_tx(bar.full(s), kWBox);
-      tma_load_2d(wst + s * kWBox, wmap, ac * kChunkWords, row, bar.full(s));
-      if (++s == (uint32_t)p.stages) {
-        s = 0;
-        ph ^= 1u;
-      }
+  ChunkPos pos;
+  pos.start(wk);
+  for (; pos.valid; pos.advance()) {
+    const int ac = grp * p.ncg + pos.c;  // absolute chunk
+    const int row = (int)(pos.sg.r * kTileRows);
+    if (pos.block_start(ac)) {
+      const uint32_t b = su & 1u, bph = (su >> 1) & 1u;
+      if (!wait_bar(bar.sempty(b), bph ^ 1u, abort_flag, 21, &g_stream_error)) break;
+      ++su;
+      mbar_arrive_tx(bar.sfull(b), kSBox);
+      tma_load_2d(sst + b * kSBox, smap, (ac / kSChunks) * (kSChunks * 16), row, bar.sfull(b));
+    }
+    if (!wait_bar(bar.empty(s), ph ^ 1u, abort_flag, 22, &g_stream_error)) break;
+    ++u;
+    mbar_arrive_tx(bar.full(s), kWBox);
+    tma_load_2d(wst + s * kWBox, wmap, ac * kChunkWords, row, bar.full(s));
+    if (++s == (uint32_t)p.stages) {
+      s = 0;
+      ph ^= 1u;
     }
   }
   // No copy may still be in flight when the CTA exits.
@@ -178,7 +328,7 @@ __device__ void produce(const SPlan& p, int grp, Work wk, const CUtensorMap* wma
 }
 
 template <typename T, int MT>
-__device__ void consume(const SPlan& p, int grp, Work wk, uint32_t wst, uint32_t sst,
+__device__ void consume(const SPlan& p, int grp, Work wk, XRun run, uint32_t wst, uint32_t sst,
                         uint32_t pbuf, uint32_t pbuf_bytes, const Bars& bar, volatile int* abort_flag,
                         uint32_t xs_base, uint32_t zero_base, uint32_t lut_bf, const Corr* corr, int ncorr) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
@@ -240,8 +390,9 @@ __device__ void consume(const SPlan& p, int grp, Work wk, uint32_t wst, uint32_t
       chk.sa = lds32(qa);
       chk.sb = lds32(qb);
       uint32_t xc[MT];
+      const int jx = c >= run.first ? c - run.first : c - run.first + p.ncg;  // staged chunk
 #pragma unroll
-      for (int mt = 0; mt < MT; ++mt) xc[mt] = xa[mt] + xstep[mt] * (uint32_t)c;
+      for (int mt = 0; mt < MT; ++mt) xc[mt] = xa[mt] + xstep[mt] * (uint32_t)jx;
       compute_chunk<T, MT>(chk, xc, acc, lut_bf);
       // residuals of activations that f16 could not hold exactly
       const int cend = (c + 1) * kChunkCols;
@@ -321,6 +472,22 @@ __device__ __forceinline__ void bulk_s2g(void* dst, uint32_t src, uint32_t bytes
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
+// Eight consecutive outputs (idx a multiple of 8, so 16-byte aligned).
+__device__ __forceinline__ void store_out8(void* y, int is_bf16, int64_t idx, const float (&v)[8]) {
+  uint32_t o[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    if (is_bf16) {
+      const __nv_bfloat162 h = __floats2bfloat162_rn(v[2 * q], v[2 * q + 1]);
+      o[q] = *reinterpret_cast<const uint32_t*>(&h);
+    } else {
+      const __half2 h = __floats2half2_rn(v[2 * q], v[2 * q + 1]);
+      o[q] = *reinterpret_cast<const uint32_t*>(&h);
+    }
+  }
+  *reinterpret_cast<uint4*>(static_cast<uint16_t*>(y) + idx) = make_uint4(o[0], o[1], o[2], o[3]);
+}
+
 // Epilogue warp: finishes each segment the consumers hand over. The
 // workspace holds, per token slot, one float per weight row (slot-major, so
 // that a tile's sums for one slot are 1 KB contiguous).
@@ -387,20 +554,35 @@ __device__ void finish(const QmvArgs& a, const SPlan& p, Work wk, uint32_t pbuf,
       }
     }
     if (own) {  // write y = factor * sum for the tile's rows
-      for (int idx = lane; idx < M * kTileRows; idx += 32) {
-        const int slot = idx / kTileRows, row = idx % kTileRows;
-        if (row >= rows) continue;
-        const float v = lds_f32(pb + 4u * ((uint32_t)slot * kPStride + (uint32_t)row));
-        store_out(a.y, p.x_is_bf16, (int64_t)slot * a.N + n0 + row, has_gs ? __fmul_rn(v, factor) : v);
+      if ((a.N & 7) == 0) {
+        // eight outputs (16 bytes) per store: a warp's narrow 2-byte stores
+        // cost about as much each as a wide one
+        for (int idx = lane; idx < M * (kTileRows / 8); idx += 32) {
+          const int slot = idx / (kTileRows / 8), r8 = (idx % (kTileRows / 8)) * 8;
+          if (r8 >= rows) continue;
+          float v[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            v[i] = lds_f32(pb + 4u * ((uint32_t)slot * kPStride + (uint32_t)(r8 + i)));
+            if (has_gs) v[i] = __fmul_rn(v[i], factor);
+          }
+          store_out8(a.y, p.x_is_bf16, (int64_t)slot * a.N + n0 + r8, v);
+        }
+      } else {
+        for (int idx = lane; idx < M * kTileRows; idx += 32) {
+          const int slot = idx / kTileRows, row = idx % kTileRows;
+          if (row >= rows) continue;
+          const float v = lds_f32(pb + 4u * ((uint32_t)slot * kPStride + (uint32_t)row));
+          store_out(a.y, p.x_is_bf16, (int64_t)slot * a.N + n0 + row, has_gs ? __fmul_rn(v, factor) : v);
+        }
       }
     }
+    // The buffer is free: its bulk add completed before the count, its
+    // read-back landed, and the zeroing copies read the zero block instead.
     __syncwarp();
-    if (lane == 0) {
-      bulk_wait_all();  // nothing of this buffer may still be read by the copy engine
-      mbar_arrive(bar.pempty(b));
-    }
+    if (lane == 0) mbar_arrive(bar.pempty(b));
   }
-  if (lane == 0) bulk_wait_all();
+  if (lane == 0) bulk_wait_all();  // the zeroing copies finish before the CTA exits
 }
 
 // Dynamic shared memory: [1024-aligned] word stages | scale blocks | partial
@@ -485,21 +667,15 @@ qmv_stream_kernel(const QmvArgs a, const SPlan p, float* __restrict__ acc, uint3
     finish(a, p, wk, pbuf, pbuf_bytes, bar, abort_flag, zero_base, acc, cnt);
     return;
   }
-  // Consumers: stage this group's activation columns (named barrier 1, 512
-  // threads); column 64t+8q+i of a chunk goes to chunk offset (4q+t)*8+i.
-  Plan sp{};
-  sp.xs_slots = p.M;
-  sp.x_is_bf16 = p.x_is_bf16;
-  auto dst_of = [&](int slot, int ch, int w8) {
-    return xs_base + 2u * (uint32_t)(slot * p.xs_stride + ch * kChunkCols + (4 * (w8 & 7) + (w8 >> 3)) * 8);
-  };
-  const int cb = grp * p.ncg;
-  const int mode = stage_x_corr<0, kCW * 32>(a, sp, cb, cb + p.ncg, dst_of, s_e, s_xr, s_corr, &s_ncorr);
+  // Consumers: stage the activation columns this CTA visits (named barrier
+  // 1, 512 threads), then stream.
+  const XRun run = x_run(p, wk);
+  const int mode = stage_run<kCW * 32>(a, p, grp * p.ncg, run, xs_base, s_corr, &s_ncorr);
   if (mode == 2)
-    consume<__nv_bfloat16, MT>(p, grp, wk, wst, sst, pbuf, pbuf_bytes, bar, abort_flag, xs_base, zero_base,
+    consume<__nv_bfloat16, MT>(p, grp, wk, run, wst, sst, pbuf, pbuf_bytes, bar, abort_flag, xs_base, zero_base,
                                lut_bf, s_corr, 0);
   else
-    consume<__half, MT>(p, grp, wk, wst, sst, pbuf, pbuf_bytes, bar, abort_flag, xs_base, zero_base, lut_bf,
+    consume<__half, MT>(p, grp, wk, run, wst, sst, pbuf, pbuf_bytes, bar, abort_flag, xs_base, zero_base, lut_bf,
                         s_corr, mode == 1 ? s_ncorr : 0);
 }
 
@@ -600,12 +776,15 @@ bool make_plan(SPlan& p, int sms, int64_t max_dyn) {
       q.stages = stages;
       q.S = S;
       q.ncg = p.nc / S;
-      q.xs_stride = q.ncg * kChunkCols + 32;
-      if ((int64_t)stream_smem_bytes(q) > max_dyn) continue;
       const int64_t tg = q.nrt * q.ncg;
       const int64_t per = sms / S;
       q.gs = (int)(per < tg ? per : tg);
       if (q.gs < 1) continue;
+      // a CTA with whole rows stages the group's chunks; otherwise its run
+      const int64_t run = (tg + q.gs - 1) / q.gs;
+      q.xs_chunks = q.nrt / q.gs >= 1 || run >= q.ncg ? q.ncg : (int)run;
+      q.xs_stride = q.xs_chunks * kChunkCols + 32;
+      if ((int64_t)stream_smem_bytes(q) > max_dyn) continue;
       if (!found || q.S < best.S) best = q;
       found = true;
       break;
@@ -669,9 +848,11 @@ cudaError_t launch_mt(const QmvArgs& a, int xdt, cudaStream_t st, const Ws* give
       q.stages = stages;
       q.S = S;
       q.ncg = p.nc / S;
-      q.xs_stride = q.ncg * kChunkCols + 32;
       const int64_t per = sms_of(dev) / S, tg = q.nrt * q.ncg;
       q.gs = (int)(per < tg ? per : tg);
+      const int64_t run = q.gs > 0 ? (tg + q.gs - 1) / q.gs : 0;
+      q.xs_chunks = q.gs > 0 && (q.nrt / q.gs >= 1 || run >= q.ncg) ? q.ncg : (int)run;
+      q.xs_stride = q.xs_chunks * kChunkCols + 32;
       std::lock_guard<std::mutex> lock(mu);
       if (q.gs < 1 || (int64_t)stream_smem_bytes(q) > max_dyn_of_dev[dev]) return cudaErrorInvalidConfiguration;
       p = q;
