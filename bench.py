@@ -43,15 +43,13 @@ WORKLOAD = ("decode-shape qmv: bf16 x [M in {1,2,4,8,16}, K] through NVFP4 gate/
             "per-linear f32 global scale in [0.5,2]*2688; bf16 out, f32 accumulate")
 METRIC = "qmv HBM GB/s & µs/call, qmm TFLOP/s; fraction of GB300 roofline (1 GPU)"
 
-# dram bytes per launch of the dominant kernel from one ncu capture, and the
-# digest of the kernel source it was taken on (stale -> reported as null).
-# DRAM bytes (read + write) of the decode kernel per step, from the ncu capture
-# in profiles/qmv_tma_kernel_decode_shapes.md (the three linears at M = 1, whose
-# traffic is the weight planes, times the five token counts); reported only
-# while the kernel sources still hash to kernel_sha.
-TRAFFIC = {"source": "profiles/qmv_tma_kernel_decode_shapes.md", "kernel_sha": "ecacee53173f29f4",
-           "bytes_per_step": 1157903360}
-TRAFFIC_FILES = ("nvfp4_qmv_tma.cu", "nvfp4_qmv_common.cuh", "nvfp4_common.cuh")
+# DRAM bytes (read + write) of the decode kernel over the 15 launches of one
+# step, from the ncu capture summarised in
+# profiles/qmv_stream_kernel_decode_step.md (`--case decode_step`); reported
+# per launch, and only while the kernel sources still hash to kernel_sha.
+TRAFFIC = {"source": "profiles/qmv_stream_kernel_decode_step.md", "kernel_sha": "9ad4690bd9e03ee0",
+           "bytes_per_step": 1123853568}
+TRAFFIC_FILES = ("nvfp4_qmv_stream.cu", "nvfp4_qmv_common.cuh", "nvfp4_common.cuh", "nvfp4_pipe.cuh")
 
 
 def qmv_bytes(m, n, k):
@@ -135,13 +133,14 @@ def source_sha(names):
 
 # ----------------------------------------------------------------------------- our arm
 
-def build_decode(nv, synth, torch, dev, rank):
-    """Weights (ROTATE copies), activations and outputs for the decode step."""
+def build_decode(nv, synth, torch, dev, rank, copies=ROTATE):
+    """Weights (`copies` rotating copies), activations and outputs for the decode step."""
     g = synth.rng(1000 + rank)
+    ncopies = copies
     lin = []
     for name, n, k in LINEARS:
         copies = []
-        for c in range(ROTATE):
+        for c in range(ncopies):
             w = torch.randint(-2**31, 2**31 - 1, (n, k // 8), dtype=torch.int32, device=dev,
                               generator=torch.Generator(device=dev).manual_seed(17 * c + n))
             s = torch.from_numpy(synth.log_uniform_scales(g, (n, k // 16), 2.0**-6, 4.0)).to(dev)
@@ -160,7 +159,7 @@ def decode_step_calls(nv, lin, xs, ys, copy_shift=0):
     calls = []
     for mi, m in enumerate(DECODE_M):
         for name, n, k, copies in lin:
-            w, s, gs = copies[(mi + copy_shift) % ROTATE]
+            w, s, gs = copies[(mi + copy_shift) % len(copies)]
             calls.append((m, n, k, xs[(m, name)], w, s, gs, ys[(m, name)]))
     return calls
 
@@ -281,7 +280,7 @@ def run_ours(args):
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
                          "frac": round(achieved / hbm_peak, 4), "peak_kind": f"{peak_kind} copy bandwidth",
                          "frac_of_8TBps": round(achieved / 8000.0, 4),
-                         "kernel": "qmv_tma_kernel (all 15 launches of the step)",
+                         "kernel": "qmv_stream_kernel (all 15 launches of the step)",
                          "traffic": None if traffic is None else round(traffic / launches_per_step)},
             "gpu_launches": launches_per_step * args.steps,
             "e2e": e2e,
@@ -520,6 +519,8 @@ def run_case(args):
     three warm-up calls then one call each at M = 1, 8 and 16.
     qmv_shapes: each decode linear (gate/up, down, qkv; 220 MB) once at M = 1
     and once at M = 16, after one warm-up call each.
+    decode_step: the 15 calls of one decode step (one weight copy per linear),
+    once as warm-up and once more.
     prefill: the tensor-core route at M = 2048 on the [21504, 5376] plane, one
     warm-up call then one call.
     """
@@ -541,6 +542,14 @@ def run_case(args):
             nv.qmm(x, w, s, gs=gs, route="tc")
         torch.cuda.synchronize(dev)
         print("case prefill ok")
+        return
+    if args.case == "decode_step":
+        lin, xs, ys = build_decode(nv, synth, torch, dev, 0, copies=1)
+        for _ in range(2):
+            for (m, n, k, x, w, s, gs, y) in decode_step_calls(nv, lin, xs, ys, 0):
+                nv.qmm(x, w, s, gs=gs, out=y)
+        torch.cuda.synchronize(dev)
+        print("case decode_step ok")
         return
     if args.case == "qmv_shapes":
         g = synth.rng(5100)
@@ -614,7 +623,7 @@ def main():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-rows", type=int, default=6144)
     ap.add_argument("--ref-rows", type=int, default=32)
-    ap.add_argument("--case", choices=["qmv_small", "qmv_shapes", "prefill"], default=None,
+    ap.add_argument("--case", choices=["qmv_small", "qmv_shapes", "decode_step", "prefill"], default=None,
                     help="run one small profiling case instead of the benchmark")
     args = ap.parse_args()
     if args.warmup < 3:
