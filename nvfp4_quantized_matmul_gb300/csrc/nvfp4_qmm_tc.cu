@@ -64,6 +64,7 @@ struct Cfg {
   static constexpr int kWarpProd0 = kWarpEpi0 + EPI_WARPS;
   static constexpr int THREADS = 32 * (kWarpProd0 + kProducerWarps);
   static constexpr int RPT = BN_ / 128;  // weight rows per producer thread
+  static constexpr int PF = RPT == 1 ? 6 : 4;  // k-blocks of packed weights in flight per producer thread
   static constexpr int BAR_BYTES = 8 * (3 * STAGES + 2 * ACC_BUFS) + 16;
   static constexpr size_t SMEM = 1024 + (size_t)STAGES * (A_BYTES + B_BYTES) + BAR_BYTES;
   static_assert(STAGES >= 3, "ring too shallow");
@@ -335,11 +336,15 @@ __device__ void producer_role(const TcParams& p, uint32_t sB, uint32_t bars, vol
   const int lane = threadIdx.x & 31;
   WCursor ld{(int)blockIdx.x, 0, true, 0, 0};
   w_seek<GATHER, BM>(ld, p, num_tiles, seg, pre);
-  WTask<RPT> b0, b1, b2;
-  w_load<C::BN>(b0, ld, p, r, h);
-  w_advance<GATHER, BM>(ld, p, num_tiles, seg, pre);
-  w_load<C::BN>(b1, ld, p, r, h);
-  w_advance<GATHER, BM>(ld, p, num_tiles, seg, pre);
+  // PF k-blocks of packed weights in flight per thread (registers), so that
+  // the L2 latency of the loads is covered by PF - 1 blocks of decoding.
+  constexpr int PF = C::PF;
+  WTask<RPT> buf[PF];
+#pragma unroll
+  for (int j = 0; j < PF - 1; ++j) {
+    w_load<C::BN>(buf[j], ld, p, r, h);
+    w_advance<GATHER, BM>(ld, p, num_tiles, seg, pre);
+  }
   uint32_t u = 0;
   const int total = ((num_tiles - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x) * p.num_kb;
   auto consume = [&](const WTask<RPT>& t) -> bool {
@@ -355,18 +360,16 @@ __device__ void producer_role(const TcParams& p, uint32_t sB, uint32_t bars, vol
     ++u;
     return true;
   };
-  for (int i = 0; i < total; i += 3) {
-    w_load<C::BN>(b2, ld, p, r, h);
-    w_advance<GATHER, BM>(ld, p, num_tiles, seg, pre);
-    if (!consume(b0)) return;
-    if (i + 1 >= total) break;
-    w_load<C::BN>(b0, ld, p, r, h);
-    w_advance<GATHER, BM>(ld, p, num_tiles, seg, pre);
-    if (!consume(b1)) return;
-    if (i + 2 >= total) break;
-    w_load<C::BN>(b1, ld, p, r, h);
-    w_advance<GATHER, BM>(ld, p, num_tiles, seg, pre);
-    if (!consume(b2)) return;
+  // the ring of buffers is indexed by compile-time positions only (unrolled),
+  // so it stays in registers
+  for (int i = 0; i < total; i += PF) {
+#pragma unroll
+    for (int j = 0; j < PF; ++j) {
+      if (i + j >= total) return;
+      w_load<C::BN>(buf[(j + PF - 1) % PF], ld, p, r, h);
+      w_advance<GATHER, BM>(ld, p, num_tiles, seg, pre);
+      if (!consume(buf[j])) return;
+    }
   }
 }
 
