@@ -521,6 +521,8 @@ def run_case(args):
     and once at M = 16, after one warm-up call each.
     decode_step: the 15 calls of one decode step (one weight copy per linear),
     once as warm-up and once more.
+    gather_prefill: the sorted MoE gate/up GatherQMM (4096 tokens, top-8 of
+    128 experts), one warm-up call then one call.
     prefill: the tensor-core route at M = 2048 on the [21504, 5376] plane, one
     warm-up call then one call.
     """
@@ -542,6 +544,22 @@ def run_case(args):
             nv.qmm(x, w, s, gs=gs, route="tc")
         torch.cuda.synchronize(dev)
         print("case prefill ok")
+        return
+    if args.case == "gather_prefill":
+        g = synth.rng(5300)
+        E, n, k, T = 128, 1536, 2048, 4096
+        w = torch.randint(-2**31, 2**31 - 1, (E, n, k // 8), dtype=torch.int32, device=dev,
+                          generator=torch.Generator(device=dev).manual_seed(11))
+        s = torch.from_numpy(synth.log_uniform_scales(g, (E, n, k // 16), 2.0**-6, 4.0)).to(dev)
+        gs = torch.from_numpy(synth.global_scales(g, E)).to(dev)
+        lhs, rhs = synth.zipf_routing(g, T, E, 8)
+        x = synth.activations(g, (T, k), "bf16").to(dev)
+        lhs_d = torch.from_numpy(lhs.view(np.int32)).to(dev)
+        rhs_d = torch.from_numpy(rhs.view(np.int32)).to(dev)
+        for _ in range(2):
+            nv.gather_qmm(x, w, s, rhs_d, lhs_d, gs=gs, sorted_indices=True)
+        torch.cuda.synchronize(dev)
+        print("case gather_prefill ok")
         return
     if args.case == "decode_step":
         lin, xs, ys = build_decode(nv, synth, torch, dev, 0, copies=1)
@@ -623,7 +641,8 @@ def main():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-rows", type=int, default=6144)
     ap.add_argument("--ref-rows", type=int, default=32)
-    ap.add_argument("--case", choices=["qmv_small", "qmv_shapes", "decode_step", "prefill"], default=None,
+    ap.add_argument("--case", choices=["qmv_small", "qmv_shapes", "decode_step", "prefill", "gather_prefill"],
+                    default=None,
                     help="run one small profiling case instead of the benchmark")
     args = ap.parse_args()
     if args.warmup < 3:

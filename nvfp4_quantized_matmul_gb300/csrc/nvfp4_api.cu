@@ -195,22 +195,28 @@ int64_t nvfp4_qmm_crossover(nvfp4_dtype x_dtype, int64_t N, int64_t K) {
   if (x_dtype == NVFP4_F32) return INT64_MAX;  // f32 activations stay on the exact SIMT path
   if (N <= 0 || K <= 0) return kDefaultCrossover;
   // Times in microseconds, fitted to a route sweep (M = 16 .. 256) of the
-  // three decode linears on GB300. The decode-shape route streams the planes
-  // once per 16 token rows: about 8 + bytes / 1.7 MB for the first 16 rows
-  // and 0.55 of that for each further 16. Below 128 rows the tensor-core
-  // route costs one pass of weight decoding over ceil(N / 256) tiles, about
-  // 0.6 us per 64-column k-block while the tiles fit one wave of SMs (0.95
-  // beyond). M* is the first multiple of 16 where the decode route is slower.
+  // three decode linears on GB300. The decode route (K % 256 == 0) runs one
+  // launch per 16 token rows, about 12 + bytes / 3.9 MB each (other K: the
+  // cluster kernel, about 8 + bytes / 1.7 MB for the first 16 rows and 0.55
+  // of that for each further 16). Below 256 rows the tensor-core route costs
+  // one pass of weight decoding over ceil(N / 256) tiles: about 0.55 us per
+  // 64-column k-block while the tiles fit one wave of SMs, 0.8 beyond. M* is
+  // the first multiple of 16 where the decode route is slower.
   int dev = 0, sms = 152;
   if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     sms = 152;
   const double bytes = 0.5625 * (double)N * (double)K;
-  const double t16 = 8.0 + bytes / 1.7e6;
+  const bool stream = K % 256 == 0;
+  const double t16 = stream ? 12.0 + bytes / 3.9e6 : 8.0 + bytes / 1.7e6;
   const int64_t tiles = (N + 255) / 256;
   const double waves = (double)((tiles + sms - 1) / sms);
-  const double t_tc = waves * (double)((K + 63) / 64) * (tiles <= sms ? 0.6 : 0.95);
+  const double t_tc = waves * (double)((K + 63) / 64) * (tiles <= sms ? 0.55 : 0.8);
+  auto t_qmv = [&](int64_t m) {
+    const double blocks = (double)((m + 15) / 16);
+    return stream ? blocks * t16 : t16 * (1.0 + 0.55 * (blocks - 1.0));
+  };
   int64_t m = 16;
-  while (m < kDefaultCrossover && t16 * (1.0 + 0.55 * (double)(m / 16 - 1)) <= t_tc) m += 16;
+  while (m < kDefaultCrossover && t_qmv(m) <= t_tc) m += 16;
   return m;
 }
 

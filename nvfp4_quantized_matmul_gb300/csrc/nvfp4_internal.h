@@ -39,7 +39,7 @@ bool qmv_tma_supported(const QmvArgs& a, int xdt);
 cudaError_t launch_qmv_tma(const QmvArgs& a, int xdt, cudaStream_t st);
 int read_qmv_error();
 // Persistent stream-K decode route for dense QuantizedMatmul (16-bit
-// activations, 1 to 16 token rows, K % 256 == 0). It finishes row tiles split
+// activations, K % 256 == 0; one launch per 16 token rows). It finishes row tiles split
 // between CTAs through a per-(device, stream) workspace that the library
 // allocates on the first call on a stream (and grows on demand).
 bool qmv_stream_supported(const QmvArgs& a, int xdt);

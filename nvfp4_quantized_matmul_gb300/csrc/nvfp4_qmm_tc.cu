@@ -298,6 +298,33 @@ __device__ __forceinline__ void w_load(WTask<RPT>& t, const WCursor& cur, const 
   }
 }
 
+// Gather mode: an expert's weight tile serves only the few row tiles of that
+// expert, so its packed rows mostly come from DRAM, 32 bytes per row per
+// k-block. When the load cursor enters a tile, the producer threads ask L2 to
+// prefetch whole rows (words and scale bytes) of the tile after it, which
+// turns those scattered reads into L2 hits.
+__device__ __forceinline__ void l2_prefetch_bulk(const void* ptr, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(ptr), "r"(bytes) : "memory");
+}
+template <int BN, int RPT, int BM>
+__device__ __forceinline__ void w_prefetch_next(const WCursor& cur, const TcParams& p, int num_tiles, const int* seg,
+                                                const int* pre, int r, int h) {
+  const int nxt = cur.tile + (int)gridDim.x;
+  if (nxt >= num_tiles) return;
+  const Tile t = tile_of<true, BM>(p, nxt, seg, pre);
+  const int64_t kwords = p.K / 8, kgroups = p.K / 16;
+#pragma unroll
+  for (int i = 0; i < RPT; ++i) {
+    const int64_t n = (int64_t)t.nt * BN + r + 128 * i;
+    if (n >= p.N) continue;
+    const int64_t row = (int64_t)t.e * p.N + n;
+    if (h == 0)
+      l2_prefetch_bulk(p.w + row * kwords, (uint32_t)(kwords * 4));
+    else if (kgroups % 16 == 0)
+      l2_prefetch_bulk(p.scales + row * kgroups, (uint32_t)kgroups);
+  }
+}
+
 template <bool GATHER, int BM>
 __device__ __forceinline__ void w_advance(WCursor& cur, const TcParams& p, int num_tiles, const int* seg,
                                           const int* pre) {
@@ -340,10 +367,19 @@ __device__ void producer_role(const TcParams& p, uint32_t sB, uint32_t bars, vol
   // the L2 latency of the loads is covered by PF - 1 blocks of decoding.
   constexpr int PF = C::PF;
   WTask<RPT> buf[PF];
+  int prefetched = -1;  // last tile whose successor was prefetched (gather mode)
+  auto prefetch = [&]() {
+    if (GATHER && !ld.done && ld.tile != prefetched && (p.K / 8) * 4 < (1ll << 20)) {
+      w_prefetch_next<C::BN, RPT, BM>(ld, p, num_tiles, seg, pre, r, h);
+      prefetched = ld.tile;
+    }
+  };
+  prefetch();
 #pragma unroll
   for (int j = 0; j < PF - 1; ++j) {
     w_load<C::BN>(buf[j], ld, p, r, h);
     w_advance<GATHER, BM>(ld, p, num_tiles, seg, pre);
+    prefetch();
   }
   uint32_t u = 0;
   const int total = ((num_tiles - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x) * p.num_kb;
@@ -368,6 +404,7 @@ __device__ void producer_role(const TcParams& p, uint32_t sB, uint32_t bars, vol
       if (i + j >= total) return;
       w_load<C::BN>(buf[(j + PF - 1) % PF], ld, p, r, h);
       w_advance<GATHER, BM>(ld, p, num_tiles, seg, pre);
+      prefetch();
       if (!consume(buf[j])) return;
     }
   }
@@ -733,10 +770,12 @@ using Tile256x128 = Cfg<2, 128>;
 using Tile128x256 = Cfg<1, 256>;
 
 // Tile shape by modelled time: whole waves of persistent tiles, each tile's
-// cost its area over the shape's relative throughput (one 128-row half per
-// decoded weight tile runs decode-bound at about 0.6 of the two-half rate;
-// 128-wide tiles re-read the activations twice as often). The environment
-// variable NVFP4_TC_TILE ("256x256", "256x128" or "128x256") overrides it.
+// cost its area over the shape's relative throughput. The rates are measured
+// on GB300 with full waves (M = 8192, [21504, 5376]): 256x128 tiles run at
+// 0.81 of 256x256, whose decoded weight tile feeds twice the MMA work, and
+// 128x256 tiles at 0.54. With them the model picks the fastest shape on a
+// sweep of M = 512 .. 8192 and of K = 21504. The environment variable
+// NVFP4_TC_TILE ("256x256", "256x128" or "128x256") overrides it.
 int pick_tile(int64_t M, int64_t N, int sms) {
   const char* forced = std::getenv("NVFP4_TC_TILE");
   if (forced) {
@@ -745,7 +784,7 @@ int pick_tile(int64_t M, int64_t N, int sms) {
     if (!std::strcmp(forced, "128x256")) return 2;
   }
   const int bm[3] = {256, 256, 128}, bn[3] = {256, 128, 256};
-  const double rate[3] = {1.0, 0.92, 0.6};
+  const double rate[3] = {1.0, 0.81, 0.54};
   int best = 0;
   double best_t = 1e300;
   for (int c = 0; c < 3; ++c) {

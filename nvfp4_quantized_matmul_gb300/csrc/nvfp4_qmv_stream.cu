@@ -902,12 +902,22 @@ cudaError_t launch_mt(const QmvArgs& a, int xdt, cudaStream_t st, const Ws* give
 bool qmv_stream_supported(const QmvArgs& a, int xdt) {
   if (const char* ev = std::getenv("NVFP4_QMV_STREAM"))
     if (ev[0] == '0') return false;
-  return xdt != kF32 && a.rhs == nullptr && a.lhs == nullptr && a.E == 1 && a.R >= 1 && a.R <= 16 &&
-         a.K % kChunkCols == 0 && a.K > 0 && a.N > 0 && a.N < (1ll << 31) && a.K / kChunkCols <= 4096;
+  return xdt != kF32 && a.rhs == nullptr && a.lhs == nullptr && a.E == 1 && a.R >= 1 && a.K % kChunkCols == 0 &&
+         a.K > 0 && a.N > 0 && a.N < (1ll << 31) && a.K / kChunkCols <= 4096;
 }
 
+// More than 16 token rows run as consecutive launches of 16 rows each (the
+// weights are streamed once per launch).
 cudaError_t launch_qmv_stream(const QmvArgs& a, int xdt, cudaStream_t st) {
-  return a.R > 8 ? launch_mt<2>(a, xdt, st) : launch_mt<1>(a, xdt, st);
+  for (int64_t r0 = 0; r0 < a.R; r0 += 16) {
+    QmvArgs b = a;
+    b.R = b.B = a.R - r0 < 16 ? a.R - r0 : 16;
+    b.x = static_cast<const uint16_t*>(a.x) + r0 * a.K;
+    b.y = static_cast<uint16_t*>(a.y) + r0 * a.N;
+    const cudaError_t e = b.R > 8 ? launch_mt<2>(b, xdt, st) : launch_mt<1>(b, xdt, st);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 int read_stream_error() {

@@ -36,7 +36,7 @@ STREAM_SHAPES = [(1000, 4096), (300, 21504), (4100, 768), (2304, 2560), (257, 25
 
 
 @pytest.mark.parametrize("nk", STREAM_SHAPES, ids=lambda v: "N%d_K%d" % v)
-@pytest.mark.parametrize("M", [1, 2, 4, 5, 8, 9, 16])
+@pytest.mark.parametrize("M", [1, 2, 4, 5, 8, 9, 16, 17, 40])
 @pytest.mark.parametrize("dt", ["f16", "bf16"])
 def test_stream_route_parity(nv, nk, M, dt):
     N, K = nk
