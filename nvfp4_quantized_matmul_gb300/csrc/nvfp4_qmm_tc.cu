@@ -19,7 +19,7 @@
 //   warps 4..   epilogue, four warps per M half: tcgen05.ld 32x32b, global
 //               factor, cast, store
 //   last 8      weight producers: 128-bit loads of the packed words and scale
-//               bytes (prefetched three stages ahead in registers), exact
+//               bytes (four to six k-blocks ahead in registers), exact
 //               decode to bf16/f16, stores in the canonical K-major
 //               128-byte-swizzled layout the MMA descriptor reads
 // Every decoded weight tile feeds MH M=128 MMAs, so a 256-row tile (MH = 2)
@@ -298,33 +298,6 @@ __device__ __forceinline__ void w_load(WTask<RPT>& t, const WCursor& cur, const 
   }
 }
 
-// Gather mode: an expert's weight tile serves only the few row tiles of that
-// expert, so its packed rows mostly come from DRAM, 32 bytes per row per
-// k-block. When the load cursor enters a tile, the producer threads ask L2 to
-// prefetch whole rows (words and scale bytes) of the tile after it, which
-// turns those scattered reads into L2 hits.
-__device__ __forceinline__ void l2_prefetch_bulk(const void* ptr, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(ptr), "r"(bytes) : "memory");
-}
-template <int BN, int RPT, int BM>
-__device__ __forceinline__ void w_prefetch_next(const WCursor& cur, const TcParams& p, int num_tiles, const int* seg,
-                                                const int* pre, int r, int h) {
-  const int nxt = cur.tile + (int)gridDim.x;
-  if (nxt >= num_tiles) return;
-  const Tile t = tile_of<true, BM>(p, nxt, seg, pre);
-  const int64_t kwords = p.K / 8, kgroups = p.K / 16;
-#pragma unroll
-  for (int i = 0; i < RPT; ++i) {
-    const int64_t n = (int64_t)t.nt * BN + r + 128 * i;
-    if (n >= p.N) continue;
-    const int64_t row = (int64_t)t.e * p.N + n;
-    if (h == 0)
-      l2_prefetch_bulk(p.w + row * kwords, (uint32_t)(kwords * 4));
-    else if (kgroups % 16 == 0)
-      l2_prefetch_bulk(p.scales + row * kgroups, (uint32_t)kgroups);
-  }
-}
-
 template <bool GATHER, int BM>
 __device__ __forceinline__ void w_advance(WCursor& cur, const TcParams& p, int num_tiles, const int* seg,
                                           const int* pre) {
@@ -367,19 +340,10 @@ __device__ void producer_role(const TcParams& p, uint32_t sB, uint32_t bars, vol
   // the L2 latency of the loads is covered by PF - 1 blocks of decoding.
   constexpr int PF = C::PF;
   WTask<RPT> buf[PF];
-  int prefetched = -1;  // last tile whose successor was prefetched (gather mode)
-  auto prefetch = [&]() {
-    if (GATHER && !ld.done && ld.tile != prefetched && (p.K / 8) * 4 < (1ll << 20)) {
-      w_prefetch_next<C::BN, RPT, BM>(ld, p, num_tiles, seg, pre, r, h);
-      prefetched = ld.tile;
-    }
-  };
-  prefetch();
 #pragma unroll
   for (int j = 0; j < PF - 1; ++j) {
     w_load<C::BN>(buf[j], ld, p, r, h);
     w_advance<GATHER, BM>(ld, p, num_tiles, seg, pre);
-    prefetch();
   }
   uint32_t u = 0;
   const int total = ((num_tiles - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x) * p.num_kb;
@@ -404,7 +368,6 @@ __device__ void producer_role(const TcParams& p, uint32_t sB, uint32_t bars, vol
       if (i + j >= total) return;
       w_load<C::BN>(buf[(j + PF - 1) % PF], ld, p, r, h);
       w_advance<GATHER, BM>(ld, p, num_tiles, seg, pre);
-      prefetch();
       if (!consume(buf[j])) return;
     }
   }

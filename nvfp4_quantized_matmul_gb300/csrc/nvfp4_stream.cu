@@ -7,12 +7,18 @@ namespace {
 
 constexpr int kStreamThreads = 256;
 
-int stream_grid(int64_t units) {
-  int dev = 0, sms = 152;
+// Grid for a grid-stride kernel: enough blocks for `units` thread-iterations,
+// at most what is resident at once (a second wave of equal blocks would run
+// after the first instead of beside it).
+template <typename Kern>
+int stream_grid(Kern kern, int64_t units) {
+  int dev = 0, sms = 152, per_sm = 1;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kStreamThreads, 0) != cudaSuccess || per_sm < 1)
+    per_sm = 1;
   const int64_t want = (units + kStreamThreads - 1) / kStreamThreads;
-  const int64_t cap = (int64_t)sms * 8;  // 8 resident 256-thread blocks per SM
+  const int64_t cap = (int64_t)sms * per_sm;
   return (int)(want < cap ? (want < 1 ? 1 : want) : cap);
 }
 
@@ -33,17 +39,17 @@ transcode_kernel(const uint8_t* __restrict__ mo_w, int64_t w_bytes, const uint8_
   if (tid == 0) gs_out[0] = __fmul_rn(__ldg(ws2), kGlobalScaleDivisor);
   const int64_t wv = w_bytes >> 4, sv = s_bytes >> 4;
   // Main body: 16-byte chunks of the weight plane then the scale plane;
-  // four independent loads in flight per thread.
+  // kU independent loads in flight per thread.
+  constexpr int kU = 8;
   const uint4* wi = reinterpret_cast<const uint4*>(mo_w);
   uint4* wo = reinterpret_cast<uint4*>(w_out);
   int64_t i = tid;
-  for (; i + 3 * stride < wv; i += 4 * stride) {
-    const uint4 a = ld_stream_v4(wi + i), b = ld_stream_v4(wi + i + stride);
-    const uint4 c = ld_stream_v4(wi + i + 2 * stride), d = ld_stream_v4(wi + i + 3 * stride);
-    __stcs(wo + i, a);
-    __stcs(wo + i + stride, b);
-    __stcs(wo + i + 2 * stride, c);
-    __stcs(wo + i + 3 * stride, d);
+  for (; i + (kU - 1) * stride < wv; i += kU * stride) {
+    uint4 v[kU];
+#pragma unroll
+    for (int u = 0; u < kU; ++u) v[u] = ld_stream_v4(wi + i + u * stride);
+#pragma unroll
+    for (int u = 0; u < kU; ++u) __stcs(wo + i + u * stride, v[u]);
   }
   for (; i < wv; i += stride) __stcs(wo + i, ld_stream_v4(wi + i));
   const uint4* si = reinterpret_cast<const uint4*>(mo_ws);
@@ -134,7 +140,30 @@ dequantize_kernel(const uint32_t* __restrict__ w, const uint8_t* __restrict__ sc
     const float fac = global_factor(gs, e);
     const bool has_gs = gs != nullptr;
     const int64_t base = e * groups_per_expert;
-    for (int64_t gi = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; gi < groups_per_expert; gi += stride) {
+    // kU groups per thread and iteration, all loads issued before any decode
+    // so that their latencies overlap.
+    constexpr int kU = 4;
+    int64_t gi = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    for (; gi + (kU - 1) * stride < groups_per_expert; gi += kU * stride) {
+      uint2 ww[kU];
+      uint32_t sb[kU];
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int64_t g = base + gi + u * stride;
+        ww[u] = ld_stream_v2(w + 2 * g);
+        sb[u] = __ldcs(scales + g);
+      }
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int64_t g = base + gi + u * stride;
+        const uint32_t sc = e4m3_to_f16x2_bcast(sb[u]);
+        uint32_t h[8];
+        decode8_scaled_f16(ww[u].x, sc, *reinterpret_cast<uint32_t(*)[4]>(&h[0]));
+        decode8_scaled_f16(ww[u].y, sc, *reinterpret_cast<uint32_t(*)[4]>(&h[4]));
+        store16<OutT>(out + 16 * g, h, fac, has_gs);
+      }
+    }
+    for (; gi < groups_per_expert; gi += stride) {
       const int64_t g = base + gi;
       const uint2 ww = ld_stream_v2(w + 2 * g);
       const uint32_t sc = e4m3_to_f16x2_bcast(__ldcs(scales + g));
@@ -151,8 +180,8 @@ dequantize_kernel(const uint32_t* __restrict__ w, const uint8_t* __restrict__ sc
 cudaError_t launch_transcode(const uint8_t* mo_w, int64_t w_bytes, const uint8_t* mo_ws, int64_t s_bytes,
                              const float* ws2, uint32_t* w_out, uint8_t* s_out, float* gs_out,
                              cudaStream_t st) {
-  const int64_t units = (w_bytes >> 4) / 4 + 16;
-  transcode_kernel<<<stream_grid(units), kStreamThreads, 0, st>>>(
+  const int64_t units = (w_bytes >> 4) / 8 + 16;
+  transcode_kernel<<<stream_grid(transcode_kernel, units), kStreamThreads, 0, st>>>(
       mo_w, w_bytes, mo_ws, s_bytes, ws2, reinterpret_cast<uint8_t*>(w_out), s_out, gs_out);
   return cudaGetLastError();
 }
@@ -160,21 +189,25 @@ cudaError_t launch_transcode(const uint8_t* mo_w, int64_t w_bytes, const uint8_t
 cudaError_t launch_dequantize(const uint32_t* w, const uint8_t* scales, const float* gs, int64_t E,
                               int64_t N, int64_t K, int out_dtype, void* out, cudaStream_t st) {
   const int64_t gpe = N * (K / 16);
-  int gx = stream_grid(gpe * E);
-  const int64_t per_expert = (gpe + kStreamThreads - 1) / kStreamThreads;
-  if (gx > per_expert) gx = (int)(per_expert < 1 ? 1 : per_expert);
-  int gy = (int)(E < 65535 ? E : 65535);
-  const dim3 grid(gx, gy);
+  auto grid_of = [&](auto kern) {
+    int gx = stream_grid(kern, (gpe * E + 3) / 4);
+    const int64_t per_expert = (gpe + kStreamThreads - 1) / kStreamThreads;
+    if (gx > per_expert) gx = (int)(per_expert < 1 ? 1 : per_expert);
+    const int gy = (int)(E < 65535 ? E : 65535);
+    return dim3(gx, gy);
+  };
   switch (out_dtype) {
     case kF32:
-      dequantize_kernel<float><<<grid, kStreamThreads, 0, st>>>(w, scales, gs, E, gpe, (float*)out);
+      dequantize_kernel<float><<<grid_of(dequantize_kernel<float>), kStreamThreads, 0, st>>>(w, scales, gs, E, gpe,
+                                                                                            (float*)out);
       break;
     case kF16:
-      dequantize_kernel<__half><<<grid, kStreamThreads, 0, st>>>(w, scales, gs, E, gpe, (__half*)out);
+      dequantize_kernel<__half><<<grid_of(dequantize_kernel<__half>), kStreamThreads, 0, st>>>(w, scales, gs, E, gpe,
+                                                                                              (__half*)out);
       break;
     default:
-      dequantize_kernel<__nv_bfloat16><<<grid, kStreamThreads, 0, st>>>(w, scales, gs, E, gpe,
-                                                                          (__nv_bfloat16*)out);
+      dequantize_kernel<__nv_bfloat16><<<grid_of(dequantize_kernel<__nv_bfloat16>), kStreamThreads, 0, st>>>(
+          w, scales, gs, E, gpe, (__nv_bfloat16*)out);
       break;
   }
   return cudaGetLastError();
