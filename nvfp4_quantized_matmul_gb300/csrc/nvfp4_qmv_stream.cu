@@ -19,11 +19,11 @@
 //    one, and no cluster or inter-CTA wait is involved.
 //  * A row tile covered by one CTA is finished in place. A row tile split
 //    between CTAs (by the even division or by the K groups) is finished by
-//    whichever contributor arrives last: each adds its partial sums to a f32
-//    workspace row block with vector atomics, then adds its chunk count to the
-//    tile's counter; the one that completes the count (K / 256 chunks) reads
-//    the sums, writes y and zeroes the workspace rows and the counter for the
-//    next call. Nobody waits on another CTA.
+//    whichever contributor arrives last: each adds its partial sums to the
+//    tile's f32 workspace block with one bulk reduce-add of the copy engine,
+//    then adds its chunk count to the tile's counter; the one that completes
+//    the count (K / 256 chunks) reads the sums back, writes y and zeroes the
+//    block and the counter for the next call. Nobody waits on another CTA.
 //  * Math (shared with the other decode kernels): each weight word is decoded
 //    exactly into f16 pairs that feed mma.sync m16n8k16 A fragments (weights
 //    are the 16-row A operand, token rows the 8-wide B operand, f32
@@ -50,20 +50,25 @@ namespace {
 using namespace qmv;
 using namespace pipe;
 
-constexpr int kCW = 16;                      // consumer warps, 16 weight rows each
-constexpr int kProducer = kCW;               // warp issuing the TMA copies
-constexpr int kEpilogue = kCW + 1;           // warp finishing row tiles
-constexpr int kSThreads = (kCW + 2) * 32;    // 576
-constexpr int kTileRows = kCW * 16;          // 256 weight rows per tile
+constexpr int kTileRows = 256;               // weight rows per tile
+// Warp roles for RT row tiles (16 rows each) per consumer warp: 16 / RT
+// consumer warps, then the TMA producer warp, then the epilogue warp.
+template <int RT> struct Geo {
+  static constexpr int kCW = kTileRows / (16 * RT);
+  static constexpr int kProducer = kCW;
+  static constexpr int kEpilogue = kCW + 1;
+  static constexpr int kThreads = (kCW + 2) * 32;
+};
 constexpr uint32_t kWBox = kTileRows * 128;  // one chunk of words: 256 rows x 128 B
 constexpr int kSChunks = 4;                  // chunks per scale block
 constexpr uint32_t kSBox = kTileRows * 64;   // one scale block: 256 rows x 64 B
 constexpr int kMaxStages = 6;
 constexpr int kAccSlots = 16;  // workspace floats per weight row (token slots)
 // A partial-sum buffer holds, per token slot, the 256 row sums of a tile
-// (1 KB, contiguous for the bulk copies) at a stride of 260 floats, which
-// spreads the consumers' stores over the banks.
-constexpr uint32_t kPStride = 260;
+// (1 KB); the slots follow one another, so a tile's sums for M token rows are
+// M KB contiguous, as in the workspace (tile-major: tile r's block is
+// [16 slots][256 rows] floats at r * 16 KB), and move with one bulk copy.
+constexpr uint32_t kPStride = kTileRows;
 // barriers: full[kMaxStages] empty[kMaxStages] sfull[2] sempty[2] pfull[2]
 // pempty[2] back[1], rounded to 16 bytes (what follows is read 16 B at a time)
 constexpr uint32_t kBarBytes = ((2 * kMaxStages + 9) * 8 + 15) / 16 * 16;
@@ -327,23 +332,82 @@ __device__ void produce(const SPlan& p, int grp, Work wk, const CUtensorMap* wma
   for (uint32_t v = sfirst; v < su; ++v) wait_bar_quiet(bar.sfull(v & 1u), (v >> 1) & 1u);
 }
 
-template <typename T, int MT>
+// Accumulator sets per (row tile, token tile): consecutive k-steps rotate over
+// them so that the MMAs form several dependency chains; two row tiles per warp
+// already give two chains each.
+template <int MT, int RT> struct NAccS {
+  static constexpr int value = RT == 1 ? NAcc<MT>::value : (MT == 1 ? 2 : 1);
+};
+
+// One chunk for RT row tiles of 16 rows: the activation fragments of each
+// half-chunk are loaded once and feed the MMAs of every row tile (same lane
+// layout as compute_chunk: lane t's word j holds columns 64t+8j..+7, k-step s
+// uses columns 64t+4s+0..3).
+template <typename T, int MT, int RT, int NA>
+__device__ __forceinline__ void compute_rt(const Chunk (&ch)[RT], const uint32_t (&xaddr)[MT],
+                                           float (&acc)[NA][RT][MT][4], uint32_t lut_bf) {
+#pragma unroll
+  for (int half = 0; half < 2; ++half) {
+    uint4 xv[MT][4];
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+      for (int q = 0; q < 4; ++q) xv[mt][q] = lds128(xaddr[mt] + 64 * (4 * half + q));
+#pragma unroll
+    for (int rt = 0; rt < RT; ++rt) {
+      const uint4& wa = half ? ch[rt].a1 : ch[rt].a0;
+      const uint4& wb = half ? ch[rt].b1 : ch[rt].b0;
+      uint32_t sa0, sa1, sb0, sb1;
+      scale_pair<T>(ch[rt].sa, half, lut_bf, sa0, sa1);
+      scale_pair<T>(ch[rt].sb, half, lut_bf, sb0, sb1);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        uint32_t da[4], db[4];
+        Dt<T>::decode(u4get(wa, j), j < 2 ? sa0 : sa1, da);
+        Dt<T>::decode(u4get(wb, j), j < 2 ? sb0 : sb1, db);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int sl = 2 * j + h;
+#pragma unroll
+          for (int mt = 0; mt < MT; ++mt) {
+            const uint32_t b0 = u4get(xv[mt][sl >> 1], 2 * (sl & 1));
+            const uint32_t b1 = u4get(xv[mt][sl >> 1], 2 * (sl & 1) + 1);
+            MmaOp<T>::run(acc[(8 * half + sl) % NA][rt][mt], da[2 * h], db[2 * h], da[2 * h + 1], db[2 * h + 1], b0,
+                          b1);
+          }
+        }
+      }
+    }
+  }
+}
+
+// Consumer warp: RT row tiles of 16 rows (rows 16 RT w .. 16 RT w + 16 RT - 1
+// of the 256-row tile) over every chunk of the CTA's walk.
+template <typename T, int MT, int RT>
 __device__ void consume(const SPlan& p, int grp, Work wk, XRun run, uint32_t wst, uint32_t sst,
                         uint32_t pbuf, uint32_t pbuf_bytes, const Bars& bar, volatile int* abort_flag,
                         uint32_t xs_base, uint32_t zero_base, uint32_t lut_bf, const Corr* corr, int ncorr) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
-  const int rg = warp * 16 + g, rg8 = rg + 8;
   // 128-byte swizzle of the word stage: 16-byte granule j of row r sits at
-  // j ^ (r & 7). This lane reads granules 2t and 2t+1 of rows rg and rg8.
-  const uint32_t oa0 = (uint32_t)rg * 128u + ((uint32_t)((2 * t) ^ (rg & 7)) << 4);
-  const uint32_t oa1 = (uint32_t)rg * 128u + ((uint32_t)((2 * t + 1) ^ (rg & 7)) << 4);
-  const uint32_t ob0 = (uint32_t)rg8 * 128u + ((uint32_t)((2 * t) ^ (rg8 & 7)) << 4);
-  const uint32_t ob1 = (uint32_t)rg8 * 128u + ((uint32_t)((2 * t + 1) ^ (rg8 & 7)) << 4);
+  // j ^ (r & 7); this lane reads granules 2t and 2t+1 of rows rg and rg + 8.
   // 64-byte swizzle of a scale block: granule kb (chunk kb of the block) of
   // row r sits at kb ^ ((r >> 1) & 3); this lane reads its word t (groups
   // 4t..4t+3 of the chunk).
-  const uint32_t osa = (uint32_t)rg * 64u + 4u * t, osb = (uint32_t)rg8 * 64u + 4u * t;
-  const uint32_t swa = (uint32_t)((rg >> 1) & 3), swb = (uint32_t)((rg8 >> 1) & 3);
+  int rg[RT];
+  uint32_t oa0[RT], oa1[RT], ob0[RT], ob1[RT], osa[RT], osb[RT], swa[RT], swb[RT];
+#pragma unroll
+  for (int rt = 0; rt < RT; ++rt) {
+    rg[rt] = warp * 16 * RT + 16 * rt + g;
+    const int ra = rg[rt], rb = ra + 8;
+    oa0[rt] = (uint32_t)ra * 128u + ((uint32_t)((2 * t) ^ (ra & 7)) << 4);
+    oa1[rt] = (uint32_t)ra * 128u + ((uint32_t)((2 * t + 1) ^ (ra & 7)) << 4);
+    ob0[rt] = (uint32_t)rb * 128u + ((uint32_t)((2 * t) ^ (rb & 7)) << 4);
+    ob1[rt] = (uint32_t)rb * 128u + ((uint32_t)((2 * t + 1) ^ (rb & 7)) << 4);
+    osa[rt] = (uint32_t)ra * 64u + 4u * t;
+    osb[rt] = (uint32_t)rb * 64u + 4u * t;
+    swa[rt] = (uint32_t)((ra >> 1) & 3);
+    swb[rt] = (uint32_t)((rb >> 1) & 3);
+  }
 
   uint32_t xa[MT], xstep[MT];
 #pragma unroll
@@ -354,17 +418,19 @@ __device__ void consume(const SPlan& p, int grp, Work wk, XRun run, uint32_t wst
     xstep[mt] = in ? 2u * kChunkCols : 0u;
   }
 
-  constexpr int NA = NAcc<MT>::value;
-  float acc[NA][MT][4];
+  constexpr int NA = NAccS<MT, RT>::value;
+  float acc[NA][RT][MT][4];
   uint32_t s = 0, ph = 0, su = 0, pc = 0;  // word stage and its phase, scale blocks, partial buffers
   Seg sg;
   while (wk.next(sg)) {
 #pragma unroll
     for (int k = 0; k < NA; ++k)
 #pragma unroll
-      for (int mt = 0; mt < MT; ++mt)
+      for (int rt = 0; rt < RT; ++rt)
 #pragma unroll
-        for (int i = 0; i < 4; ++i) acc[k][mt][i] = 0.f;
+        for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) acc[k][rt][mt][i] = 0.f;
     int cur = 0;  // next residual correction (sorted by column)
     while (cur < ncorr && corr[cur].col < sg.c0 * kChunkCols) ++cur;
     for (int c = sg.c0; c < sg.c1; ++c) {
@@ -381,19 +447,24 @@ __device__ void consume(const SPlan& p, int grp, Work wk, XRun run, uint32_t wst
       if (first_of_block && !wait_bar_warp(bar.sfull(sb), sph, abort_flag, 23, &g_stream_error)) continue;
       if (!wait_bar_warp(bar.full(cs), cph, abort_flag, 24, &g_stream_error)) continue;
       const uint32_t w = wst + cs * kWBox, q = sst + sb * kSBox;
-      const uint32_t qa = q + osa + (((uint32_t)kb ^ swa) << 4), qb = q + osb + (((uint32_t)kb ^ swb) << 4);
-      Chunk chk;
-      chk.a0 = lds128(w + oa0);
-      chk.a1 = lds128(w + oa1);
-      chk.b0 = lds128(w + ob0);
-      chk.b1 = lds128(w + ob1);
-      chk.sa = lds32(qa);
-      chk.sb = lds32(qb);
+      Chunk chk[RT];
+      uint32_t qa[RT], qb[RT];
+#pragma unroll
+      for (int rt = 0; rt < RT; ++rt) {
+        qa[rt] = q + osa[rt] + (((uint32_t)kb ^ swa[rt]) << 4);
+        qb[rt] = q + osb[rt] + (((uint32_t)kb ^ swb[rt]) << 4);
+        chk[rt].a0 = lds128(w + oa0[rt]);
+        chk[rt].a1 = lds128(w + oa1[rt]);
+        chk[rt].b0 = lds128(w + ob0[rt]);
+        chk[rt].b1 = lds128(w + ob1[rt]);
+        chk[rt].sa = lds32(qa[rt]);
+        chk[rt].sb = lds32(qb[rt]);
+      }
       uint32_t xc[MT];
       const int jx = c >= run.first ? c - run.first : c - run.first + p.ncg;  // staged chunk
 #pragma unroll
       for (int mt = 0; mt < MT; ++mt) xc[mt] = xa[mt] + xstep[mt] * (uint32_t)jx;
-      compute_chunk<T, MT>(chk, xc, acc, lut_bf);
+      compute_rt<T, MT, RT, NA>(chk, xc, acc, lut_bf);
       // residuals of activations that f16 could not hold exactly
       const int cend = (c + 1) * kChunkCols;
       for (; cur < ncorr && corr[cur].col < cend; ++cur) {
@@ -401,23 +472,27 @@ __device__ void consume(const SPlan& p, int grp, Work wk, XRun run, uint32_t wst
         if (((e.slot & 7) >> 1) != t) continue;
         const int kc = e.col - c * kChunkCols;  // column within the chunk
         const uint32_t wq = (uint32_t)(kc >> 5), wi = (uint32_t)((kc >> 3) & 3), sh = 4u * (uint32_t)(kc & 7);
-        const uint32_t wa = lds32(w + (uint32_t)rg * 128u + ((wq ^ (uint32_t)(rg & 7)) << 4) + 4u * wi);
-        const uint32_t wb = lds32(w + (uint32_t)rg8 * 128u + ((wq ^ (uint32_t)(rg8 & 7)) << 4) + 4u * wi);
         const uint32_t grpb = (uint32_t)(kc >> 4);  // 16-column group within the chunk: byte of the granule
-        const uint32_t sa_w = lds32(qa - 4u * t + 4u * (grpb >> 2));
-        const uint32_t sb_w = lds32(qb - 4u * t + 4u * (grpb >> 2));
         const uint32_t sbyte = 8u * (grpb & 3u);
-        // fp4 * e4m3 * residual is exact in f32 (at most 6 + 8 significant bits)
-        const float da = e2m1_to_f32((wa >> sh) & 0xF) * e4m3_to_f32((sa_w >> sbyte) & 0xFF) * e.r;
-        const float db = e2m1_to_f32((wb >> sh) & 0xF) * e4m3_to_f32((sb_w >> sbyte) & 0xFF) * e.r;
         const bool odd = e.slot & 1;
 #pragma unroll
-        for (int mt = 0; mt < MT; ++mt) {  // selects, not indexing: the accumulators stay in registers
-          const bool on = (e.slot >> 3) == mt;
-          acc[0][mt][0] += on && !odd ? da : 0.f;
-          acc[0][mt][1] += on && odd ? da : 0.f;
-          acc[0][mt][2] += on && !odd ? db : 0.f;
-          acc[0][mt][3] += on && odd ? db : 0.f;
+        for (int rt = 0; rt < RT; ++rt) {
+          const int ra = rg[rt], rb = ra + 8;
+          const uint32_t wa = lds32(w + (uint32_t)ra * 128u + ((wq ^ (uint32_t)(ra & 7)) << 4) + 4u * wi);
+          const uint32_t wb = lds32(w + (uint32_t)rb * 128u + ((wq ^ (uint32_t)(rb & 7)) << 4) + 4u * wi);
+          const uint32_t sa_w = lds32(qa[rt] - 4u * t + 4u * (grpb >> 2));
+          const uint32_t sb_w = lds32(qb[rt] - 4u * t + 4u * (grpb >> 2));
+          // fp4 * e4m3 * residual is exact in f32 (at most 6 + 8 significant bits)
+          const float da = e2m1_to_f32((wa >> sh) & 0xF) * e4m3_to_f32((sa_w >> sbyte) & 0xFF) * e.r;
+          const float db = e2m1_to_f32((wb >> sh) & 0xF) * e4m3_to_f32((sb_w >> sbyte) & 0xFF) * e.r;
+#pragma unroll
+          for (int mt = 0; mt < MT; ++mt) {  // selects, not indexing: the accumulators stay in registers
+            const bool on = (e.slot >> 3) == mt;
+            acc[0][rt][mt][0] += on && !odd ? da : 0.f;
+            acc[0][rt][mt][1] += on && odd ? da : 0.f;
+            acc[0][rt][mt][2] += on && !odd ? db : 0.f;
+            acc[0][rt][mt][3] += on && odd ? db : 0.f;
+          }
         }
       }
       __syncwarp();
@@ -432,16 +507,18 @@ __device__ void consume(const SPlan& p, int grp, Work wk, XRun run, uint32_t wst
     if (!wait_bar_warp(bar.pempty(b), bph ^ 1u, abort_flag, 25, &g_stream_error)) continue;
     const uint32_t pb = pbuf + b * pbuf_bytes;
 #pragma unroll
-    for (int mt = 0; mt < MT; ++mt)
+    for (int rt = 0; rt < RT; ++rt)
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int row = rg + ((i & 2) ? 8 : 0);
-        const int slot = 8 * mt + 2 * t + (i & 1);
-        float v = 0.f;
+      for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
-        for (int k = 0; k < NA; ++k) v += acc[k][mt][i];
-        sts_f32(pb + 4u * ((uint32_t)slot * kPStride + (uint32_t)row), v);
-      }
+        for (int i = 0; i < 4; ++i) {
+          const int row = rg[rt] + ((i & 2) ? 8 : 0);
+          const int slot = 8 * mt + 2 * t + (i & 1);
+          float v = 0.f;
+#pragma unroll
+          for (int k = 0; k < NA; ++k) v += acc[k][rt][mt][i];
+          sts_f32(pb + 4u * ((uint32_t)slot * kPStride + (uint32_t)row), v);
+        }
     mbar_arrive(bar.pfull(b));  // every lane: releases its own stores
   }
 }
@@ -465,10 +542,6 @@ __device__ __forceinline__ void bulk_add_s2g(float* dst, uint32_t src, uint32_t 
                "r"(bytes)
                : "memory");
 }
-__device__ __forceinline__ void bulk_s2g(void* dst, uint32_t src, uint32_t bytes) {
-  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(src), "r"(bytes)
-               : "memory");
-}
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
@@ -489,19 +562,17 @@ __device__ __forceinline__ void store_out8(void* y, int is_bf16, int64_t idx, co
 }
 
 // Epilogue warp: finishes each segment the consumers hand over. The
-// workspace holds, per token slot, one float per weight row (slot-major, so
-// that a tile's sums for one slot are 1 KB contiguous).
+// workspace is tile-major: row tile r owns a block of 16 slots x 256 rows of
+// float sums, of which a call with M token rows uses the first M KB.
 __device__ void finish(const QmvArgs& a, const SPlan& p, Work wk, uint32_t pbuf, uint32_t pbuf_bytes,
-                       const Bars& bar, volatile int* abort_flag, uint32_t zero_base, float* __restrict__ acc,
+                       const Bars& bar, volatile int* abort_flag, float* __restrict__ acc,
                        uint32_t* __restrict__ cnt) {
   const int lane = threadIdx.x & 31;
   const float factor = global_factor(a.gs, 0);
   const bool has_gs = a.gs != nullptr;
   const int M = p.M;
-  const int64_t npad = p.nrt * kTileRows;
   constexpr uint32_t kSlotBytes = kTileRows * 4u;
-  // the zero block (written by generic stores at set-up) is a bulk-copy source
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  const uint32_t tile_bytes = (uint32_t)M * kSlotBytes;  // this call's part of a tile block
   uint32_t pc = 0, bc = 0;
   Seg sg;
   while (wk.next(sg)) {
@@ -512,13 +583,13 @@ __device__ void finish(const QmvArgs& a, const SPlan& p, Work wk, uint32_t pbuf,
     const int64_t n0 = sg.r * kTileRows;
     const int rows = (int)(a.N - n0 < kTileRows ? a.N - n0 : kTileRows);
     bool own = p.S == 1 && sg.c0 == 0 && sg.c1 == p.ncg;  // the whole row tile is this CTA's
+    float* blk = acc + sg.r * (int64_t)(kAccSlots * kTileRows);  // the tile's workspace block
     if (!own) {
-      // Add this piece to the tile's workspace sums (one bulk add per slot;
-      // rows past N add zeros), then count its chunks in.
+      // Add this piece to the tile's workspace sums with one bulk add (rows
+      // past N add zeros), then count its chunks in.
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // consumers' stores -> copy engine
       if (lane == 0) {
-        for (int slot = 0; slot < M; ++slot)
-          bulk_add_s2g(acc + slot * npad + n0, pb + (uint32_t)slot * kPStride * 4u, kSlotBytes);
+        bulk_add_s2g(blk, pb, tile_bytes);
         bulk_commit();
         bulk_wait_all();
         asm volatile("fence.proxy.async.global;" ::: "memory");
@@ -533,9 +604,8 @@ __device__ void finish(const QmvArgs& a, const SPlan& p, Work wk, uint32_t pbuf,
         __threadfence();
         asm volatile("fence.proxy.async.global;" ::: "memory");
         if (lane == 0) {
-          mbar_arrive_tx(bar.back(), (uint32_t)M * kSlotBytes);
-          for (int slot = 0; slot < M; ++slot)
-            bulk_g2s(pb + (uint32_t)slot * kPStride * 4u, acc + slot * npad + n0, kSlotBytes, bar.back());
+          mbar_arrive_tx(bar.back(), tile_bytes);
+          bulk_g2s(pb, blk, tile_bytes, bar.back());
         }
         const bool ok = wait_bar_warp(bar.back(), bc & 1u, abort_flag, 27, &g_stream_error);
         ++bc;
@@ -543,14 +613,10 @@ __device__ void finish(const QmvArgs& a, const SPlan& p, Work wk, uint32_t pbuf,
           wait_bar_quiet(bar.back(), (bc - 1) & 1u);  // the copies must land before the CTA leaves
           break;
         }
-        if (lane == 0) {
-          for (int slot = 0; slot < M; ++slot) {
-            bulk_s2g(acc + slot * npad + n0, zero_base, kSlotBytes / 2);
-            bulk_s2g(acc + slot * npad + n0 + kTileRows / 2, zero_base, kSlotBytes / 2);
-          }
-          bulk_commit();
-          atomicExch(cnt + sg.r, 0u);
-        }
+        for (int i = lane; i < (int)(tile_bytes / 16); i += 32)
+          __stcg(reinterpret_cast<float4*>(blk) + i, make_float4(0.f, 0.f, 0.f, 0.f));
+        __syncwarp();
+        if (lane == 0) atomicExch(cnt + sg.r, 0u);
       }
     }
     if (own) {  // write y = factor * sum for the tile's rows
@@ -577,12 +643,11 @@ __device__ void finish(const QmvArgs& a, const SPlan& p, Work wk, uint32_t pbuf,
         }
       }
     }
-    // The buffer is free: its bulk add completed before the count, its
-    // read-back landed, and the zeroing copies read the zero block instead.
+    // The buffer is free: its bulk add completed before the count and its
+    // read-back landed.
     __syncwarp();
     if (lane == 0) mbar_arrive(bar.pempty(b));
   }
-  if (lane == 0) bulk_wait_all();  // the zeroing copies finish before the CTA exits
 }
 
 // Dynamic shared memory: [1024-aligned] word stages | scale blocks | partial
@@ -594,8 +659,8 @@ size_t stream_smem_bytes(const SPlan& p) {
   return 1024 + (size_t)p.stages * kWBox + 2 * kSBox + pbuf + kBarBytes + 16 + 256 + 1024 + 512 + 64 + xs;
 }
 
-template <int MT>
-__global__ void __launch_bounds__(kSThreads, 1)
+template <int MT, int RT>
+__global__ void __launch_bounds__(Geo<RT>::kThreads, 1)
 qmv_stream_kernel(const QmvArgs a, const SPlan p, float* __restrict__ acc, uint32_t* __restrict__ cnt,
                   const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap smap) {
   extern __shared__ uint8_t smem_raw[];
@@ -625,12 +690,12 @@ qmv_stream_kernel(const QmvArgs a, const SPlan p, float* __restrict__ acc, uint3
   if (threadIdx.x == 0) {
     for (int s = 0; s < p.stages; ++s) {
       mbar_init(bar.full(s), 1);     // producer arrive + TMA bytes
-      mbar_init(bar.empty(s), kCW);  // one arrive per consumer warp
+      mbar_init(bar.empty(s), Geo<RT>::kCW);  // one arrive per consumer warp
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(bar.sfull(b), 1);
-      mbar_init(bar.sempty(b), kCW);
-      mbar_init(bar.pfull(b), kCW * 32);  // every consumer lane
+      mbar_init(bar.sempty(b), Geo<RT>::kCW);
+      mbar_init(bar.pfull(b), Geo<RT>::kCW * 32);  // every consumer lane
       mbar_init(bar.pempty(b), 1);
     }
     mbar_init(bar.back(), 1);
@@ -638,7 +703,7 @@ qmv_stream_kernel(const QmvArgs a, const SPlan p, float* __restrict__ acc, uint3
     s_ncorr = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  if (threadIdx.x == kProducer * 32) {
+  if (threadIdx.x == Geo<RT>::kProducer * 32) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&wmap)) : "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&smap)) : "memory");
   }
@@ -658,25 +723,25 @@ qmv_stream_kernel(const QmvArgs a, const SPlan p, float* __restrict__ acc, uint3
   const int grp = blockIdx.x / p.gs, gi = blockIdx.x % p.gs;
   const Work wk = Work::of(p, gi);
 
-  if (warp == kProducer) {
+  if (warp == Geo<RT>::kProducer) {
     if ((threadIdx.x & 31) == 0) produce(p, grp, wk, &wmap, &smap, wst, sst, bar, abort_flag);
     return;
   }
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  if (warp == kEpilogue) {
-    finish(a, p, wk, pbuf, pbuf_bytes, bar, abort_flag, zero_base, acc, cnt);
+  if (warp == Geo<RT>::kEpilogue) {
+    finish(a, p, wk, pbuf, pbuf_bytes, bar, abort_flag, acc, cnt);
     return;
   }
   // Consumers: stage the activation columns this CTA visits (named barrier
   // 1, 512 threads), then stream.
   const XRun run = x_run(p, wk);
-  const int mode = stage_run<kCW * 32>(a, p, grp * p.ncg, run, xs_base, s_corr, &s_ncorr);
+  const int mode = stage_run<Geo<RT>::kCW * 32>(a, p, grp * p.ncg, run, xs_base, s_corr, &s_ncorr);
   if (mode == 2)
-    consume<__nv_bfloat16, MT>(p, grp, wk, run, wst, sst, pbuf, pbuf_bytes, bar, abort_flag, xs_base, zero_base,
-                               lut_bf, s_corr, 0);
+    consume<__nv_bfloat16, MT, RT>(p, grp, wk, run, wst, sst, pbuf, pbuf_bytes, bar, abort_flag, xs_base, zero_base,
+                                   lut_bf, s_corr, 0);
   else
-    consume<__half, MT>(p, grp, wk, run, wst, sst, pbuf, pbuf_bytes, bar, abort_flag, xs_base, zero_base, lut_bf,
-                        s_corr, mode == 1 ? s_ncorr : 0);
+    consume<__half, MT, RT>(p, grp, wk, run, wst, sst, pbuf, pbuf_bytes, bar, abort_flag, xs_base, zero_base, lut_bf,
+                            s_corr, mode == 1 ? s_ncorr : 0);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -794,11 +859,11 @@ bool make_plan(SPlan& p, int sms, int64_t max_dyn) {
   return found;
 }
 
-template <int MT>
+template <int MT, int RT>
 cudaError_t launch_mt(const QmvArgs& a, int xdt, cudaStream_t st, const Ws* given = nullptr) {
   auto enc = encode_fn();
   if (!enc) return cudaErrorNotSupported;
-  auto kern = qmv_stream_kernel<MT>;
+  auto kern = qmv_stream_kernel<MT, RT>;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -886,7 +951,7 @@ cudaError_t launch_mt(const QmvArgs& a, int xdt, cudaStream_t st, const Ws* give
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(p.S * p.gs), 1, 1);
-  cfg.blockDim = dim3(kSThreads, 1, 1);
+  cfg.blockDim = dim3(Geo<RT>::kThreads, 1, 1);
   cfg.dynamicSmemBytes = stream_smem_bytes(p);
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
@@ -895,6 +960,17 @@ cudaError_t launch_mt(const QmvArgs& a, int xdt, cudaStream_t st, const Ws* give
   cfg.attrs = attr;
   cfg.numAttrs = launch_overlap() ? 1 : 0;
   return cudaLaunchKernelEx(&cfg, kern, a, p, ws.acc, ws.cnt, wmap, smap);
+}
+
+// One launch for up to 16 token rows: eight token slots per MMA tile (MT),
+// and RT weight row tiles per consumer warp (RT = 2 shares each activation
+// fragment between two row tiles; NVFP4_QMV_RT=1/2 overrides the choice).
+cudaError_t launch_rows(const QmvArgs& a, int xdt, cudaStream_t st, const Ws* ws) {
+  int rt = a.R > 8 ? 2 : 1;
+  if (const char* ev = std::getenv("NVFP4_QMV_RT"))
+    if (ev[0] == '1' || ev[0] == '2') rt = ev[0] - '0';
+  if (a.R > 8) return rt == 2 ? launch_mt<2, 2>(a, xdt, st, ws) : launch_mt<2, 1>(a, xdt, st, ws);
+  return rt == 2 ? launch_mt<1, 2>(a, xdt, st, ws) : launch_mt<1, 1>(a, xdt, st, ws);
 }
 
 }  // namespace
@@ -914,7 +990,7 @@ cudaError_t launch_qmv_stream(const QmvArgs& a, int xdt, cudaStream_t st) {
     b.R = b.B = a.R - r0 < 16 ? a.R - r0 : 16;
     b.x = static_cast<const uint16_t*>(a.x) + r0 * a.K;
     b.y = static_cast<uint16_t*>(a.y) + r0 * a.N;
-    const cudaError_t e = b.R > 8 ? launch_mt<2>(b, xdt, st) : launch_mt<1>(b, xdt, st);
+    const cudaError_t e = launch_rows(b, xdt, st, nullptr);
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;
@@ -996,8 +1072,9 @@ cudaError_t launch_qmv_stream_noalloc(const QmvArgs& a, int xdt, cudaStream_t st
   // The kernel indexes the sums as [slot][nrt * 256]: clear the slots this
   // call uses and its tile counters (a previous call may have been cut short).
   if ((e = cudaMemsetAsync(ws.cnt, 0, (size_t)nrt * sizeof(uint32_t), st)) != cudaSuccess) return e;
-  if ((e = cudaMemsetAsync(ws.acc, 0, (size_t)a.R * nrt * kTileRows * sizeof(float), st)) != cudaSuccess) return e;
-  return a.R > 8 ? launch_mt<2>(a, xdt, st, &ws) : launch_mt<1>(a, xdt, st, &ws);
+  if ((e = cudaMemsetAsync(ws.acc, 0, (size_t)nrt * kAccSlots * kTileRows * sizeof(float), st)) != cudaSuccess)
+    return e;
+  return launch_rows(a, xdt, st, &ws);
 }
 
 void release_stream_workspaces() {

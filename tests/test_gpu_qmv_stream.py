@@ -56,6 +56,20 @@ def test_stream_route_parity(nv, nk, M, dt):
             assert guards_intact(backing, guard)
 
 
+@pytest.mark.parametrize("M", [3, 16])
+def test_stream_route_two_row_tiles_per_warp(nv, monkeypatch, M):
+    """NVFP4_QMV_RT=2 selects eight consumer warps of 32 weight rows each."""
+    monkeypatch.setenv("NVFP4_QMV_RT", "2")
+    N, K = 1000, 4096
+    w, s = weights(5 + M, N, K)
+    x = synth.activations(synth.rng(M), (M, K), "bf16").cuda()
+    for rep in range(2):
+        y = nv.qmm(x, u32_to_dev(w), u8_to_dev(s), route="qmv")
+        torch.cuda.synchronize()
+        assert nv.take_device_error() == 0
+        assert rel_err(y, O.qmm(x.cpu().double().numpy(), w, s, None)) <= TOL["bf16"]
+
+
 def test_stream_route_alternating_shapes_and_streams(nv):
     """Calls of different shapes interleaved on two streams; each stream has
     its own workspace."""
