@@ -91,7 +91,15 @@ def _cuda(*ts):
                 raise ValueError("nvfp4 ops take contiguous tensors")
 
 
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
 def _stream(t):
+    """The current CUDA stream of t's device, as a raw handle (the cheap
+    accessor when this torch has it: building a Stream object per call costs
+    several microseconds)."""
+    if _raw_stream is not None:
+        return _raw_stream(t.device.index)
     return torch.cuda.current_stream(t.device).cuda_stream
 
 
@@ -102,7 +110,7 @@ def _gs_tensor(gs, device):
         gs = torch.tensor([float(gs)], dtype=torch.float32, device=device)
     if gs.dtype != torch.float32:
         raise ValueError("gs must be float32")
-    return gs.reshape(-1)
+    return gs if gs.dim() == 1 else gs.reshape(-1)
 
 
 def transcode(mo_weight, mo_weight_scale, weight_scale_2, out=None):

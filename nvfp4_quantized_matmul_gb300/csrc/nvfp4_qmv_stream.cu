@@ -859,10 +859,58 @@ bool make_plan(SPlan& p, int sms, int64_t max_dyn) {
   return found;
 }
 
-template <int MT, int RT>
-cudaError_t launch_mt(const QmvArgs& a, int xdt, cudaStream_t st, const Ws* given = nullptr) {
+// TMA descriptors of a weight plane and its scale plane (words: 256-row x
+// 128-byte boxes, 128-byte swizzle; scales: 256-row x 64-byte boxes, 64-byte
+// swizzle). Encoding costs host time on every call, and decode-step weights
+// are the same few planes call after call, so the pair is kept per (planes,
+// shape).
+cudaError_t plane_maps(const QmvArgs& a, CUtensorMap* wmap, CUtensorMap* smap) {
+  using Key = std::tuple<const void*, const void*, int64_t, int64_t>;
+  struct Maps {
+    CUtensorMap w, s;
+  };
+  static std::mutex mu;
+  static std::map<Key, Maps> cache;
+  const Key key{a.w, a.scales, a.N, a.K};
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = cache.find(key);
+    if (it != cache.end()) {
+      *wmap = it->second.w;
+      *smap = it->second.s;
+      return cudaSuccess;
+    }
+  }
   auto enc = encode_fn();
   if (!enc) return cudaErrorNotSupported;
+  {
+    const cuuint64_t dims[2] = {(cuuint64_t)(a.K / 8), (cuuint64_t)a.N};
+    const cuuint64_t strides[1] = {(cuuint64_t)(a.K / 2)};
+    const cuuint32_t box[2] = {kChunkWords, kTileRows};
+    const cuuint32_t es[2] = {1, 1};
+    if (enc(wmap, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<uint32_t*>(a.w), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  {
+    const cuuint64_t dims[2] = {(cuuint64_t)(a.K / 16), (cuuint64_t)a.N};
+    const cuuint64_t strides[1] = {(cuuint64_t)(a.K / 16)};
+    const cuuint32_t box[2] = {kSChunks * 16, kTileRows};
+    const cuuint32_t es[2] = {1, 1};
+    if (enc(smap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(a.scales), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  if (cache.size() >= 1024) cache.clear();  // bound the table (weights are few; this never triggers in practice)
+  cache[key] = Maps{*wmap, *smap};
+  return cudaSuccess;
+}
+
+template <int MT, int RT>
+cudaError_t launch_mt(const QmvArgs& a, int xdt, cudaStream_t st, const Ws* given = nullptr) {
   auto kern = qmv_stream_kernel<MT, RT>;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -929,26 +977,7 @@ cudaError_t launch_mt(const QmvArgs& a, int xdt, cudaStream_t st, const Ws* give
   else if ((e = get_workspace(dev, st, p.nrt, &ws)) != cudaSuccess)
     return e;
   CUtensorMap wmap, smap;
-  {
-    const cuuint64_t dims[2] = {(cuuint64_t)(a.K / 8), (cuuint64_t)a.N};
-    const cuuint64_t strides[1] = {(cuuint64_t)(a.K / 2)};
-    const cuuint32_t box[2] = {kChunkWords, kTileRows};
-    const cuuint32_t es[2] = {1, 1};
-    if (enc(&wmap, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<uint32_t*>(a.w), dims, strides, box, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-      return cudaErrorInvalidValue;
-  }
-  {
-    const cuuint64_t dims[2] = {(cuuint64_t)(a.K / 16), (cuuint64_t)a.N};
-    const cuuint64_t strides[1] = {(cuuint64_t)(a.K / 16)};
-    const cuuint32_t box[2] = {kSChunks * 16, kTileRows};
-    const cuuint32_t es[2] = {1, 1};
-    if (enc(&smap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(a.scales), dims, strides, box, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-      return cudaErrorInvalidValue;
-  }
+  if ((e = plane_maps(a, &wmap, &smap)) != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(p.S * p.gs), 1, 1);
   cfg.blockDim = dim3(Geo<RT>::kThreads, 1, 1);
