@@ -142,7 +142,12 @@ int64_t nvfp4_qmm_crossover(nvfp4_dtype x_dtype, int64_t N, int64_t K);
  *   rhs_indices uint32 [R]; w [E, N, K/8]; scales [E, N, K/16];
  *   gs NULL (gs_len 0) or [E] (gs_len E); y [R, N] of x_dtype.
  * A row whose expert index is >= E, or whose activation index is >= B, is
- * written as exact +0.0 (no read outside x or w). `sorted_indices` != 0
+ * written as exact +0.0 (no read outside x or w). Calls with 16-bit
+ * activations, K % 256 == 0 and at most one row per SM group the rows by
+ * expert (eight to a group, in row order) and stream each group's expert
+ * plane once, split over the SMs; they use the decode route's workspace (see
+ * nvfp4_qmm). NVFP4_QMV_GROUP=0 sends them to the per-row kernel instead.
+ * `sorted_indices` != 0
  * promises expert indices in non-decreasing order (a sorted MoE prefill) and
  * lets 16-bit calls with enough rows per expert (R >= 512 and R >= 16 E, E <=
  * 1024, K % 32 == 0) take the expert-batched tensor-core route; the

@@ -46,6 +46,11 @@ bool qmv_stream_supported(const QmvArgs& a, int xdt);
 cudaError_t launch_qmv_stream(const QmvArgs& a, int xdt, cudaStream_t st);
 int read_stream_error();
 void release_stream_workspaces();
+// The same kernel for GatherQMM with at most one row per SM (16-bit
+// activations, K % 256 == 0): rows grouped by expert, eight to a group, each
+// group's expert plane streamed once and split over its share of the SMs.
+bool qmv_group_supported(const QmvArgs& a, int xdt);
+cudaError_t launch_qmv_group(const QmvArgs& a, int xdt, cudaStream_t st);
 // The same route with its scratch in a fixed array inside the library (no
 // allocation); at most kNoAllocMaxRows weight rows.
 constexpr int64_t kNoAllocMaxRows = 65536;

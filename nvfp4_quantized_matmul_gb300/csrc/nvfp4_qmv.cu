@@ -480,6 +480,7 @@ cudaError_t launch_qmv(const QmvArgs& a, int xdt, cudaStream_t st) {
     return cudaGetLastError();
   }
   if (qmv_stream_supported(a, xdt)) return launch_qmv_stream(a, xdt, st);
+  if (qmv_group_supported(a, xdt)) return launch_qmv_group(a, xdt, st);
   if (qmv_tma_supported(a, xdt)) return launch_qmv_tma(a, xdt, st);
   Plan pl{};
   pl.nchunk = (int)((a.K + kChunkCols - 1) / kChunkCols);

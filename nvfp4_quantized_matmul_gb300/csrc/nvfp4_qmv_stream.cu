@@ -158,10 +158,11 @@ __device__ __forceinline__ XRun x_run(const SPlan& p, const Work& wk) {
 // sorted); otherwise the bf16 values are staged. Returns 0 (f16), 1 (f16 with
 // residuals) or 2 (bf16). Threads 0 .. kN-1 (the consumer warps) take part;
 // *n_corr must be zero and visible on entry. Loads are issued four at a time
-// per thread so that their latencies overlap.
-template <int kN>
+// per thread so that their latencies overlap. Token slot s reads activation
+// row s, or xrow[s] for an expert group (kGrp).
+template <int kN, bool kGrp>
 __device__ int stage_run(const QmvArgs& a, const SPlan& p, int chunk0, XRun run, uint32_t xs_base, Corr* corr,
-                         int* n_corr) {
+                         int* n_corr, const int64_t* xrow) {
   constexpr int kBatch = 4;
   const int per_slot = run.count * (kChunkCols / 8), units = p.M * per_slot;
   const int tid = (int)threadIdx.x;
@@ -171,7 +172,7 @@ __device__ int stage_run(const QmvArgs& a, const SPlan& p, int chunk0, XRun run,
     int gc = run.first + j;
     if (gc >= p.ncg) gc -= p.ncg;
     gcol = gc * kChunkCols + 8 * w8;  // group-relative column
-    src = (int64_t)slot * a.K + (int64_t)chunk0 * kChunkCols + gcol;
+    src = (kGrp ? xrow[slot] : (int64_t)slot) * a.K + (int64_t)chunk0 * kChunkCols + gcol;
     dst = xs_base + 2u * (uint32_t)(slot * p.xs_stride + j * kChunkCols + (4 * (w8 & 7) + (w8 >> 3)) * 8);
   };
   int hard = 0;
@@ -299,10 +300,12 @@ struct ChunkPos {
 
 // Producer (lane 0 of the producer warp): the same chunk walk as the
 // consumers; a scale block at the start of each segment and at every fourth
-// chunk, a word stage per chunk.
+// chunk, a word stage per chunk. An expert group (kGrp) reads its expert's
+// plane through 3-D maps ([E, N, K] planes, rows past N zero-filled).
+template <bool kGrp>
 __device__ void produce(const SPlan& p, int grp, Work wk, const CUtensorMap* wmap,
                         const CUtensorMap* smap, uint32_t wst, uint32_t sst, const Bars& bar,
-                        volatile int* abort_flag) {
+                        volatile int* abort_flag, int expert) {
   uint32_t u = 0, s = 0, ph = 0, su = 0;  // copies issued, next stage and its phase, scale blocks
   ChunkPos pos;
   pos.start(wk);
@@ -314,12 +317,18 @@ __device__ void produce(const SPlan& p, int grp, Work wk, const CUtensorMap* wma
       if (!wait_bar(bar.sempty(b), bph ^ 1u, abort_flag, 21, &g_stream_error)) break;
       ++su;
       mbar_arrive_tx(bar.sfull(b), kSBox);
-      tma_load_2d(sst + b * kSBox, smap, (ac / kSChunks) * (kSChunks * 16), row, bar.sfull(b));
+      if (kGrp)
+        tma_load_3d(sst + b * kSBox, smap, (ac / kSChunks) * (kSChunks * 16), row, expert, bar.sfull(b));
+      else
+        tma_load_2d(sst + b * kSBox, smap, (ac / kSChunks) * (kSChunks * 16), row, bar.sfull(b));
     }
     if (!wait_bar(bar.empty(s), ph ^ 1u, abort_flag, 22, &g_stream_error)) break;
     ++u;
     mbar_arrive_tx(bar.full(s), kWBox);
-    tma_load_2d(wst + s * kWBox, wmap, ac * kChunkWords, row, bar.full(s));
+    if (kGrp)
+      tma_load_3d(wst + s * kWBox, wmap, ac * kChunkWords, row, expert, bar.full(s));
+    else
+      tma_load_2d(wst + s * kWBox, wmap, ac * kChunkWords, row, bar.full(s));
     if (++s == (uint32_t)p.stages) {
       s = 0;
       ph ^= 1u;
@@ -562,13 +571,19 @@ __device__ __forceinline__ void store_out8(void* y, int is_bf16, int64_t idx, co
 }
 
 // Epilogue warp: finishes each segment the consumers hand over. The
-// workspace is tile-major: row tile r owns a block of 16 slots x 256 rows of
-// float sums, of which a call with M token rows uses the first M KB.
+// workspace is tile-major: a split row tile owns a block of 16 slots x 256
+// rows of float sums, of which a call with M token rows uses the first M KB.
+// A dense call's row tile r uses block r. An expert group (kGrp) uses blocks
+// wsbase .. wsbase + gs - 1, one per row tile left over after the whole rows
+// are dealt out (there are fewer than gs), and writes token slot s to output
+// row yrow[s] with the expert's global scale.
+template <bool kGrp>
 __device__ void finish(const QmvArgs& a, const SPlan& p, Work wk, uint32_t pbuf, uint32_t pbuf_bytes,
                        const Bars& bar, volatile int* abort_flag, float* __restrict__ acc,
-                       uint32_t* __restrict__ cnt) {
+                       uint32_t* __restrict__ cnt, int expert, int wsbase, const int64_t* yrow) {
   const int lane = threadIdx.x & 31;
-  const float factor = global_factor(a.gs, 0);
+  const float factor = global_factor(a.gs, kGrp ? expert : 0);
+  const int64_t first_split = (p.nrt / p.gs) * p.gs;  // row tiles from here on may be split
   const bool has_gs = a.gs != nullptr;
   const int M = p.M;
   constexpr uint32_t kSlotBytes = kTileRows * 4u;
@@ -583,7 +598,8 @@ __device__ void finish(const QmvArgs& a, const SPlan& p, Work wk, uint32_t pbuf,
     const int64_t n0 = sg.r * kTileRows;
     const int rows = (int)(a.N - n0 < kTileRows ? a.N - n0 : kTileRows);
     bool own = p.S == 1 && sg.c0 == 0 && sg.c1 == p.ncg;  // the whole row tile is this CTA's
-    float* blk = acc + sg.r * (int64_t)(kAccSlots * kTileRows);  // the tile's workspace block
+    const int64_t wt = kGrp ? wsbase + (sg.r - first_split) : sg.r;  // the tile's workspace block
+    float* blk = acc + wt * (int64_t)(kAccSlots * kTileRows);
     if (!own) {
       // Add this piece to the tile's workspace sums with one bulk add (rows
       // past N add zeros), then count its chunks in.
@@ -595,7 +611,7 @@ __device__ void finish(const QmvArgs& a, const SPlan& p, Work wk, uint32_t pbuf,
         asm volatile("fence.proxy.async.global;" ::: "memory");
         __threadfence();
         const uint32_t add = (uint32_t)(sg.c1 - sg.c0);
-        own = atomicAdd(cnt + sg.r, add) + add == (uint32_t)p.nc;  // the last contribution finishes the tile
+        own = atomicAdd(cnt + wt, add) + add == (uint32_t)p.nc;  // the last contribution finishes the tile
       }
       own = __shfl_sync(0xffffffffu, (int)own, 0) != 0;
       if (own) {
@@ -616,7 +632,7 @@ __device__ void finish(const QmvArgs& a, const SPlan& p, Work wk, uint32_t pbuf,
         for (int i = lane; i < (int)(tile_bytes / 16); i += 32)
           __stcg(reinterpret_cast<float4*>(blk) + i, make_float4(0.f, 0.f, 0.f, 0.f));
         __syncwarp();
-        if (lane == 0) atomicExch(cnt + sg.r, 0u);
+        if (lane == 0) atomicExch(cnt + wt, 0u);
       }
     }
     if (own) {  // write y = factor * sum for the tile's rows
@@ -632,14 +648,15 @@ __device__ void finish(const QmvArgs& a, const SPlan& p, Work wk, uint32_t pbuf,
             v[i] = lds_f32(pb + 4u * ((uint32_t)slot * kPStride + (uint32_t)(r8 + i)));
             if (has_gs) v[i] = __fmul_rn(v[i], factor);
           }
-          store_out8(a.y, p.x_is_bf16, (int64_t)slot * a.N + n0 + r8, v);
+          store_out8(a.y, p.x_is_bf16, (kGrp ? yrow[slot] : (int64_t)slot) * a.N + n0 + r8, v);
         }
       } else {
         for (int idx = lane; idx < M * kTileRows; idx += 32) {
           const int slot = idx / kTileRows, row = idx % kTileRows;
           if (row >= rows) continue;
           const float v = lds_f32(pb + 4u * ((uint32_t)slot * kPStride + (uint32_t)row));
-          store_out(a.y, p.x_is_bf16, (int64_t)slot * a.N + n0 + row, has_gs ? __fmul_rn(v, factor) : v);
+          store_out(a.y, p.x_is_bf16, (kGrp ? yrow[slot] : (int64_t)slot) * a.N + n0 + row,
+                    has_gs ? __fmul_rn(v, factor) : v);
         }
       }
     }
@@ -647,6 +664,112 @@ __device__ void finish(const QmvArgs& a, const SPlan& p, Work wk, uint32_t pbuf,
     // read-back landed.
     __syncwarp();
     if (lane == 0) mbar_arrive(bar.pempty(b));
+  }
+}
+
+// ---- expert groups (GatherQMM) ----
+//
+// A GatherQMM call with at most one row per CTA is run as expert groups:
+// rows are grouped by expert index, in row order, at most kGroupRows to a
+// group (one MMA token tile), and group ids follow the order in which the
+// experts first appear. Every CTA derives the same grouping from the index
+// arrays and serves one group: group g owns CTAs [g C / G, (g + 1) C / G) of
+// the C in the grid (G <= R <= C, so every group has one), which split its
+// expert's weight plane exactly as a dense call splits its plane. Each
+// expert's weights are then streamed once per group instead of once per row.
+constexpr int kGroupRows = 8;
+constexpr uint32_t kNoExpert = 0xFFFFFFFFu;
+
+struct GroupInfo {
+  int G;       // groups in the call
+  int expert;  // this CTA's group: expert index,
+  int n;       // rows (1 .. kGroupRows),
+  int gs, gi;  // CTAs serving it and this CTA's index among them,
+  int wsbase;  // first of its workspace blocks
+};
+
+// Grouping, by all kT threads of the CTA; `scratch` holds 16 R bytes of
+// shared memory. A row whose expert index is >= E or whose activation index
+// is >= B belongs to no group: it is written as zeros, by CTA (row mod C).
+// On return (after a barrier) info->G is set; when it is non-zero, info's
+// other fields and yrow / xrow (output and activation row of each token slot)
+// are written but not yet visible to other threads. info->n must be zero and
+// visible on entry.
+template <int kT>
+__device__ void group_rows(const QmvArgs& a, uint8_t* scratch, int64_t* yrow, int64_t* xrow, GroupInfo* info) {
+  const int R = (int)a.R, tid = (int)threadIdx.x, C = (int)gridDim.x, bid = (int)blockIdx.x;
+  uint32_t* key = reinterpret_cast<uint32_t*>(scratch);  // expert of each row, or kNoExpert
+  int* rank = reinterpret_cast<int*>(key + R);           // rows of the same expert before it
+  int* lead = rank + R;                                  // first row of its expert
+  int* base = lead + R;                                  // on a first row: the expert's first group id
+  for (int t = tid; t < R; t += kT) {
+    const uint32_t e = __ldg(a.rhs + t);
+    const uint32_t xr = a.lhs ? __ldg(a.lhs + t) : (uint32_t)t;
+    key[t] = (int64_t)e < a.E && (int64_t)xr < a.B ? e : kNoExpert;
+  }
+  __syncthreads();
+  for (int t = tid; t < R; t += kT) {
+    const uint32_t e = key[t];
+    int rk = 0, total = 0, ld = t;
+    if (e != kNoExpert) {
+      for (int j = 0; j < R; ++j) {
+        const bool same = key[j] == e;
+        total += same ? 1 : 0;
+        if (same && j < t) {
+          if (rk == 0) ld = j;
+          ++rk;
+        }
+      }
+    }
+    rank[t] = rk;
+    lead[t] = ld;
+    base[t] = e != kNoExpert && rk == 0 ? (total + kGroupRows - 1) / kGroupRows : 0;
+  }
+  __syncthreads();
+  if (tid < 32) {  // exclusive prefix sum over rows of the groups each expert needs
+    const int per = (R + 31) / 32, lo = tid * per, hi = min(R, lo + per);
+    int sum = 0;
+    for (int i = lo; i < hi; ++i) sum += base[i];
+    int inc = sum;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, inc, off);
+      if (tid >= off) inc += v;
+    }
+    int run = inc - sum;
+    for (int i = lo; i < hi; ++i) {
+      const int v = base[i];
+      base[i] = run;
+      run += v;
+    }
+    if (tid == 31) info->G = inc;
+  }
+  __syncthreads();
+  for (int t = bid; t < R; t += C) {  // rows without a group: exact +0.0
+    if (key[t] != kNoExpert) continue;
+    uint16_t* yr = static_cast<uint16_t*>(a.y) + (int64_t)t * a.N;
+    if ((a.N & 7) == 0)
+      for (int64_t i = tid; i < a.N / 8; i += kT) reinterpret_cast<uint4*>(yr)[i] = make_uint4(0, 0, 0, 0);
+    else
+      for (int64_t i = tid; i < a.N; i += kT) yr[i] = 0;
+  }
+  const int G = info->G;
+  if (G == 0) return;
+  const int g = (int)(((int64_t)(bid + 1) * G - 1) / C);  // the g with g C / G <= bid < (g + 1) C / G
+  const int s0 = (int)((int64_t)g * C / G), s1 = (int)((int64_t)(g + 1) * C / G);
+  for (int t = tid; t < R; t += kT) {
+    const uint32_t e = key[t];
+    if (e == kNoExpert || base[lead[t]] + rank[t] / kGroupRows != g) continue;
+    const int slot = rank[t] % kGroupRows;
+    yrow[slot] = t;
+    xrow[slot] = a.lhs ? (int64_t)__ldg(a.lhs + t) : (int64_t)t;
+    if (slot == 0) info->expert = (int)e;
+    atomicAdd(&info->n, 1);
+  }
+  if (tid == 0) {
+    info->gs = s1 - s0;
+    info->gi = bid - s0;
+    info->wsbase = s0;
   }
 }
 
@@ -659,7 +782,7 @@ size_t stream_smem_bytes(const SPlan& p) {
   return 1024 + (size_t)p.stages * kWBox + 2 * kSBox + pbuf + kBarBytes + 16 + 256 + 1024 + 512 + 64 + xs;
 }
 
-template <int MT, int RT>
+template <int MT, int RT, bool kGrp>
 __global__ void __launch_bounds__(Geo<RT>::kThreads, 1)
 qmv_stream_kernel(const QmvArgs a, const SPlan p, float* __restrict__ acc, uint32_t* __restrict__ cnt,
                   const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap smap) {
@@ -674,8 +797,8 @@ qmv_stream_kernel(const QmvArgs a, const SPlan p, float* __restrict__ acc, uint3
   const Bars bar{pbuf + 2 * pbuf_bytes, p.stages};
   uint8_t* after_bars = bp + (bar.base - base) + kBarBytes;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(after_bars);
-  int64_t* s_e = reinterpret_cast<int64_t*>(after_bars + 16);  // 16 slots: expert (0 or -1 = no row)
-  int64_t* s_xr = s_e + 16;                                     // and activation row
+  int64_t* s_yrow = reinterpret_cast<int64_t*>(after_bars + 16);  // expert group: output row of each token slot
+  int64_t* s_xrow = s_yrow + 16;                                     // and its activation row
   uint32_t* lut = reinterpret_cast<uint32_t*>(after_bars + 16 + 256);
   const uint32_t lut_bf = smem_addr(lut);
   // 512 zero bytes stand in for the activations of absent token slots; they
@@ -685,6 +808,7 @@ qmv_stream_kernel(const QmvArgs a, const SPlan p, float* __restrict__ acc, uint3
   const uint32_t xs_base = zero_base + 512 + 64;
   __shared__ Corr s_corr[kMaxCorr];
   __shared__ int s_ncorr;
+  __shared__ GroupInfo s_ginfo;
 
   const int warp = threadIdx.x >> 5;
   if (threadIdx.x == 0) {
@@ -701,6 +825,7 @@ qmv_stream_kernel(const QmvArgs a, const SPlan p, float* __restrict__ acc, uint3
     mbar_init(bar.back(), 1);
     *abort_flag = 0;
     s_ncorr = 0;
+    s_ginfo.n = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (threadIdx.x == Geo<RT>::kProducer * 32) {
@@ -709,10 +834,6 @@ qmv_stream_kernel(const QmvArgs a, const SPlan p, float* __restrict__ acc, uint3
   }
   if (threadIdx.x < 256) lut[threadIdx.x] = e4m3_to_bf16x2_bcast_x2p112(threadIdx.x);
   if (threadIdx.x < 128) lut[256 + threadIdx.x] = 0u;  // the zero block
-  if (threadIdx.x < 16) {
-    s_e[threadIdx.x] = threadIdx.x < p.M ? 0 : -1;
-    s_xr[threadIdx.x] = threadIdx.x;
-  }
   // Launched with launch overlap on, this grid may start while the previous
   // kernel on the stream finishes: the weight planes are streamed at once
   // (the caller guarantees no running kernel writes them); activations,
@@ -720,27 +841,47 @@ qmv_stream_kernel(const QmvArgs a, const SPlan p, float* __restrict__ acc, uint3
   if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   __syncthreads();
 
-  const int grp = blockIdx.x / p.gs, gi = blockIdx.x % p.gs;
-  const Work wk = Work::of(p, gi);
+  // A dense call: CTA b serves K group b / gs. An expert group: the CTA's
+  // plan is the host's with the group's rows and CTA count.
+  SPlan q = p;
+  int grp = 0, gi = 0, expert = 0, wsbase = 0;
+  if (kGrp) {
+    // The indices may come from the kernel before: group after it completes,
+    // in word stage 0, which the producer fills only afterwards.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    group_rows<Geo<RT>::kThreads>(a, bp, s_yrow, s_xrow, &s_ginfo);
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    __syncthreads();
+    if (s_ginfo.G == 0) return;
+    q.M = s_ginfo.n;
+    q.gs = s_ginfo.gs;
+    gi = s_ginfo.gi;
+    expert = s_ginfo.expert;
+    wsbase = s_ginfo.wsbase;
+  } else {
+    grp = blockIdx.x / p.gs;
+    gi = blockIdx.x % p.gs;
+  }
+  const Work wk = Work::of(q, gi);
 
   if (warp == Geo<RT>::kProducer) {
-    if ((threadIdx.x & 31) == 0) produce(p, grp, wk, &wmap, &smap, wst, sst, bar, abort_flag);
+    if ((threadIdx.x & 31) == 0) produce<kGrp>(q, grp, wk, &wmap, &smap, wst, sst, bar, abort_flag, expert);
     return;
   }
   asm volatile("griddepcontrol.wait;" ::: "memory");
   if (warp == Geo<RT>::kEpilogue) {
-    finish(a, p, wk, pbuf, pbuf_bytes, bar, abort_flag, acc, cnt);
+    finish<kGrp>(a, q, wk, pbuf, pbuf_bytes, bar, abort_flag, acc, cnt, expert, wsbase, s_yrow);
     return;
   }
   // Consumers: stage the activation columns this CTA visits (named barrier
   // 1, 512 threads), then stream.
-  const XRun run = x_run(p, wk);
-  const int mode = stage_run<Geo<RT>::kCW * 32>(a, p, grp * p.ncg, run, xs_base, s_corr, &s_ncorr);
+  const XRun run = x_run(q, wk);
+  const int mode = stage_run<Geo<RT>::kCW * 32, kGrp>(a, q, grp * q.ncg, run, xs_base, s_corr, &s_ncorr, s_xrow);
   if (mode == 2)
-    consume<__nv_bfloat16, MT, RT>(p, grp, wk, run, wst, sst, pbuf, pbuf_bytes, bar, abort_flag, xs_base, zero_base,
+    consume<__nv_bfloat16, MT, RT>(q, grp, wk, run, wst, sst, pbuf, pbuf_bytes, bar, abort_flag, xs_base, zero_base,
                                    lut_bf, s_corr, 0);
   else
-    consume<__half, MT, RT>(p, grp, wk, run, wst, sst, pbuf, pbuf_bytes, bar, abort_flag, xs_base, zero_base, lut_bf,
+    consume<__half, MT, RT>(q, grp, wk, run, wst, sst, pbuf, pbuf_bytes, bar, abort_flag, xs_base, zero_base, lut_bf,
                             s_corr, mode == 1 ? s_ncorr : 0);
 }
 
@@ -863,15 +1004,16 @@ bool make_plan(SPlan& p, int sms, int64_t max_dyn) {
 // 128-byte boxes, 128-byte swizzle; scales: 256-row x 64-byte boxes, 64-byte
 // swizzle). Encoding costs host time on every call, and decode-step weights
 // are the same few planes call after call, so the pair is kept per (planes,
-// shape).
-cudaError_t plane_maps(const QmvArgs& a, CUtensorMap* wmap, CUtensorMap* smap) {
-  using Key = std::tuple<const void*, const void*, int64_t, int64_t>;
+// shape). With `experts` the maps are 3-D over all E planes ([E, N, K], box
+// depth 1), so that a box never runs into the next expert's rows.
+cudaError_t plane_maps(const QmvArgs& a, CUtensorMap* wmap, CUtensorMap* smap, bool experts = false) {
+  using Key = std::tuple<const void*, const void*, int64_t, int64_t, int64_t>;
   struct Maps {
     CUtensorMap w, s;
   };
   static std::mutex mu;
   static std::map<Key, Maps> cache;
-  const Key key{a.w, a.scales, a.N, a.K};
+  const Key key{a.w, a.scales, a.N, a.K, experts ? a.E : 0};
   {
     std::lock_guard<std::mutex> lock(mu);
     auto it = cache.find(key);
@@ -883,22 +1025,23 @@ cudaError_t plane_maps(const QmvArgs& a, CUtensorMap* wmap, CUtensorMap* smap) {
   }
   auto enc = encode_fn();
   if (!enc) return cudaErrorNotSupported;
+  const cuuint32_t rank = experts ? 3 : 2;
   {
-    const cuuint64_t dims[2] = {(cuuint64_t)(a.K / 8), (cuuint64_t)a.N};
-    const cuuint64_t strides[1] = {(cuuint64_t)(a.K / 2)};
-    const cuuint32_t box[2] = {kChunkWords, kTileRows};
-    const cuuint32_t es[2] = {1, 1};
-    if (enc(wmap, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<uint32_t*>(a.w), dims, strides, box, es,
+    const cuuint64_t dims[3] = {(cuuint64_t)(a.K / 8), (cuuint64_t)a.N, (cuuint64_t)a.E};
+    const cuuint64_t strides[2] = {(cuuint64_t)(a.K / 2), (cuuint64_t)(a.K / 2) * (cuuint64_t)a.N};
+    const cuuint32_t box[3] = {kChunkWords, kTileRows, 1};
+    const cuuint32_t es[3] = {1, 1, 1};
+    if (enc(wmap, CU_TENSOR_MAP_DATA_TYPE_UINT32, rank, const_cast<uint32_t*>(a.w), dims, strides, box, es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
   {
-    const cuuint64_t dims[2] = {(cuuint64_t)(a.K / 16), (cuuint64_t)a.N};
-    const cuuint64_t strides[1] = {(cuuint64_t)(a.K / 16)};
-    const cuuint32_t box[2] = {kSChunks * 16, kTileRows};
-    const cuuint32_t es[2] = {1, 1};
-    if (enc(smap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(a.scales), dims, strides, box, es,
+    const cuuint64_t dims[3] = {(cuuint64_t)(a.K / 16), (cuuint64_t)a.N, (cuuint64_t)a.E};
+    const cuuint64_t strides[2] = {(cuuint64_t)(a.K / 16), (cuuint64_t)(a.K / 16) * (cuuint64_t)a.N};
+    const cuuint32_t box[3] = {kSChunks * 16, kTileRows, 1};
+    const cuuint32_t es[3] = {1, 1, 1};
+    if (enc(smap, CU_TENSOR_MAP_DATA_TYPE_UINT8, rank, const_cast<uint8_t*>(a.scales), dims, strides, box, es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
@@ -911,7 +1054,7 @@ cudaError_t plane_maps(const QmvArgs& a, CUtensorMap* wmap, CUtensorMap* smap) {
 
 template <int MT, int RT>
 cudaError_t launch_mt(const QmvArgs& a, int xdt, cudaStream_t st, const Ws* given = nullptr) {
-  auto kern = qmv_stream_kernel<MT, RT>;
+  auto kern = qmv_stream_kernel<MT, RT, false>;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -1002,7 +1145,89 @@ cudaError_t launch_rows(const QmvArgs& a, int xdt, cudaStream_t st, const Ws* ws
   return rt == 2 ? launch_mt<1, 2>(a, xdt, st, ws) : launch_mt<1, 1>(a, xdt, st, ws);
 }
 
+// Expert-group launch (GatherQMM): one K group, so that a CTA stages the
+// whole activation rows of its group once; the deepest ring that fits next to
+// them. Shared-memory limit per device, looked up once.
+bool group_plan(const QmvArgs& a, int xdt, int dev, SPlan* out) {
+  static std::mutex mu;
+  static std::map<int, int64_t> max_dyn_of_dev;
+  int64_t max_dyn = 0;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    auto md = max_dyn_of_dev.find(dev);
+    if (md == max_dyn_of_dev.end()) {
+      auto kern = qmv_stream_kernel<1, 1, true>;
+      int optin = 0;
+      cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+      cudaFuncAttributes fa;
+      if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess) return false;
+      max_dyn = optin - (int64_t)fa.sharedSizeBytes;
+      if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)max_dyn) != cudaSuccess)
+        return false;
+      max_dyn_of_dev[dev] = max_dyn;
+    } else {
+      max_dyn = md->second;
+    }
+  }
+  SPlan p{};
+  p.M = kGroupRows;
+  p.pslots = kGroupRows;
+  p.nc = (int)(a.K / kChunkCols);
+  p.nrt = (a.N + kTileRows - 1) / kTileRows;
+  p.x_is_bf16 = xdt == kBF16;
+  p.S = 1;
+  p.ncg = p.nc;
+  p.gs = 1;  // per group, set by each CTA
+  p.xs_chunks = p.nc;
+  p.xs_stride = p.nc * kChunkCols + 32;
+  for (int stages = kMaxStages; stages >= 3; --stages) {
+    p.stages = stages;
+    if ((int64_t)stream_smem_bytes(p) <= max_dyn) {
+      *out = p;
+      return true;
+    }
+  }
+  return false;
+}
+
 }  // namespace
+
+bool qmv_group_supported(const QmvArgs& a, int xdt) {
+  if (const char* ev = std::getenv("NVFP4_QMV_GROUP"))
+    if (ev[0] == '0') return false;
+  if (xdt == kF32 || a.rhs == nullptr || a.R < 1 || a.K % kChunkCols != 0 || a.K <= 0 || a.N <= 0 ||
+      a.N >= (1ll << 31) || a.K / kChunkCols > 4096 || a.E < 1 || a.E >= (1ll << 31))
+    return false;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  SPlan p;
+  return a.R <= sms_of(dev) && group_plan(a, xdt, dev, &p);
+}
+
+// One CTA per SM; every CTA groups the rows itself (no planning launch).
+cudaError_t launch_qmv_group(const QmvArgs& a, int xdt, cudaStream_t st) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  SPlan p;
+  const int C = sms_of(dev);
+  if (a.R > C || !group_plan(a, xdt, dev, &p)) return cudaErrorInvalidConfiguration;
+  Ws ws;
+  if ((e = get_workspace(dev, st, C, &ws)) != cudaSuccess) return e;
+  CUtensorMap wmap, smap;
+  if ((e = plane_maps(a, &wmap, &smap, true)) != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)C, 1, 1);
+  cfg.blockDim = dim3(Geo<1>::kThreads, 1, 1);
+  cfg.dynamicSmemBytes = stream_smem_bytes(p);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = launch_overlap() ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, qmv_stream_kernel<1, 1, true>, a, p, ws.acc, ws.cnt, wmap, smap);
+}
 
 bool qmv_stream_supported(const QmvArgs& a, int xdt) {
   if (const char* ev = std::getenv("NVFP4_QMV_STREAM"))
@@ -1098,8 +1323,8 @@ cudaError_t launch_qmv_stream_noalloc(const QmvArgs& a, int xdt, cudaStream_t st
   ws.cnt = reinterpret_cast<uint32_t*>(base + kNoAllocAccFloats);
   ws.acc_floats = kNoAllocAccFloats;
   ws.cnt_words = kNoAllocCounters;
-  // The kernel indexes the sums as [slot][nrt * 256]: clear the slots this
-  // call uses and its tile counters (a previous call may have been cut short).
+  // Row tile r's sums are block r (16 slots x 256 floats): clear the blocks
+  // and tile counters this call uses (a previous call may have been cut short).
   if ((e = cudaMemsetAsync(ws.cnt, 0, (size_t)nrt * sizeof(uint32_t), st)) != cudaSuccess) return e;
   if ((e = cudaMemsetAsync(ws.acc, 0, (size_t)nrt * kAccSlots * kTileRows * sizeof(float), st)) != cudaSuccess)
     return e;
