@@ -152,6 +152,10 @@ int64_t nvfp4_qmm_crossover(nvfp4_dtype x_dtype, int64_t N, int64_t K);
  * lets 16-bit calls with enough rows per expert (R >= 512 and R >= 16 E, E <=
  * 1024, K % 32 == 0) take the expert-batched tensor-core route; the
  * environment variable NVFP4_GATHER_TC (1/0) forces or disables that route.
+ * With lhs_indices that route first copies the activation rows into output
+ * order, in a buffer of R * K * 2 bytes that the library keeps per (device,
+ * stream) until nvfp4_shutdown() (made outside any capture, as the decode
+ * workspace); NVFP4_GATHER_ROWS=tma fetches the rows per tile instead.
  * If the promise is broken on that route, every output row is still written
  * once and nothing outside the inputs is read, but rows are computed with
  * the expert of the sorted segment they fall in.
@@ -184,7 +188,8 @@ int32_t nvfp4_take_device_error(void);
  * decode-step matmuls, whose weights are constant. */
 int nvfp4_set_launch_overlap(int enable);
 
-/* Frees the decode route's workspaces on every device. Call only when no
+/* Frees the decode route's workspaces and the gathered-row buffers of the
+ * expert-batched route on every device. Call only when no
  * library work is queued or running; a later call allocates again. Not part
  * of the pages' interface. */
 void nvfp4_shutdown(void);

@@ -149,7 +149,10 @@ int32_t nvfp4_take_device_error(void) {
   return a ? a : b ? b : c;
 }
 
-void nvfp4_shutdown(void) { nvfp4::release_stream_workspaces(); }
+void nvfp4_shutdown(void) {
+  nvfp4::release_stream_workspaces();
+  nvfp4::release_gather_workspaces();
+}
 
 nvfp4_status nvfp4_transcode(const uint8_t* mo_weight, int64_t mo_weight_len, const uint8_t* mo_weight_scale,
                              int64_t mo_weight_scale_len, const float* weight_scale_2, int64_t N, int64_t K,

@@ -69,6 +69,8 @@ bool gather_tc_supported(int64_t B, int64_t K, int64_t R, int64_t E, int64_t N);
 cudaError_t launch_gather_tc(const void* x, int xdt, int64_t B, int64_t K, const uint32_t* lhs, const uint32_t* rhs,
                              int64_t R, const uint32_t* w, const uint8_t* scales, const float* gs, int64_t E, int64_t N,
                              void* y, cudaStream_t st);
+// Frees the gathered-activation buffers of the expert-batched route.
+void release_gather_workspaces();
 // Reads and clears the error code left by a bounded wait in the tensor-core
 // kernels (synchronises with the device); 0 = none, -1 = read failed.
 int read_tc_error();

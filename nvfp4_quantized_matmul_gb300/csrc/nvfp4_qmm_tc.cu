@@ -32,8 +32,11 @@
 #include <cmath>
 #include <cstdlib>
 #include <cstring>
+#include <map>
 #include <mutex>
 #include <type_traits>
+#include <utility>
+#include <vector>
 
 #include "nvfp4_common.cuh"
 #include "nvfp4_internal.h"
@@ -83,8 +86,10 @@ struct TcParams {
   // r is x[lhs[r]] (x[r] without lhs) times expert rhs[r]'s weights.
   const uint32_t* lhs;
   const uint32_t* rhs;
-  int64_t B;  // activation rows
-  int E;      // experts
+  int64_t B;    // activation rows
+  int E;        // experts
+  int xcontig;  // gather: the activations of output row r are row r of the
+                // mapped x (x itself, or x gathered into output-row order)
 };
 
 // One output tile: expert, weight tile, first output row and row count.
@@ -526,14 +531,39 @@ qmm_tc_kernel(const __grid_constant__ CUtensorMap xmap, const TcParams p) {
           }
         }
       }
-    } else {
-      // Each lane fetches four activation rows of every 128-row half with one
-      // tile::gather4 copy per k-block; rows past the tile's end or with an
-      // out-of-range activation index read row 0 (their outputs are not
-      // taken from the accumulator).
+    } else if (p.xcontig) {
+      // The tile's activations are rows m0 .. m0 + rows - 1 of the mapped x:
+      // one 128-row box per M half that holds rows of the tile (rows past
+      // them belong to the next expert or lie beyond x; they are computed but
+      // not stored).
       bool ok = true;
       for (int i = 0; i < my_tiles && ok; ++i) {
         const Tile tl = tile_of<true, BM>(p, (int)blockIdx.x + i * (int)gridDim.x, seg, pre);
+        const int mh = (tl.rows + 127) / 128;
+        for (int kb = 0; kb < p.num_kb; ++kb, ++u) {
+          const int s = (int)(u % STAGES);
+          const uint32_t ph = (u / STAGES) & 1;
+          if (!wait_bar_warp(emptyB(s), ph ^ 1, abort_flag, 1, &g_tc_error)) { ok = false; break; }
+          if (lane == 0) {
+            mbar_arrive_tx(fullA(s), (uint32_t)mh * kHalfA);
+#pragma unroll
+            for (int h = 0; h < MH; ++h)
+              if (h < mh)
+                tma_load_2d(sA + (uint32_t)s * C::A_BYTES + (uint32_t)h * kHalfA, &xmap, kb * BK,
+                            (int)(tl.m0 + 128 * h), fullA(s));
+          }
+          __syncwarp();
+        }
+      }
+    } else {
+      // Each lane fetches four activation rows of every 128-row half that
+      // holds rows of the tile with one tile::gather4 copy per k-block; rows
+      // past the tile's end or with an out-of-range activation index read row
+      // 0 (their outputs are not taken from the accumulator).
+      bool ok = true;
+      for (int i = 0; i < my_tiles && ok; ++i) {
+        const Tile tl = tile_of<true, BM>(p, (int)blockIdx.x + i * (int)gridDim.x, seg, pre);
+        const int mh = (tl.rows + 127) / 128;
         int xr[MH][4];
 #pragma unroll
         for (int h = 0; h < MH; ++h)
@@ -552,12 +582,13 @@ qmm_tc_kernel(const __grid_constant__ CUtensorMap xmap, const TcParams p) {
           const int s = (int)(u % STAGES);
           const uint32_t ph = (u / STAGES) & 1;
           if (!wait_bar_warp(emptyB(s), ph ^ 1, abort_flag, 1, &g_tc_error)) { ok = false; break; }
-          if (lane == 0) mbar_arrive_tx(fullA(s), C::A_BYTES);
+          if (lane == 0) mbar_arrive_tx(fullA(s), (uint32_t)mh * kHalfA);
           __syncwarp();
 #pragma unroll
           for (int h = 0; h < MH; ++h)
-            tma_gather4(sA + (uint32_t)s * C::A_BYTES + (uint32_t)h * kHalfA + 512u * (uint32_t)lane, &xmap, kb * BK,
-                        xr[h][0], xr[h][1], xr[h][2], xr[h][3], fullA(s));
+            if (h < mh)
+              tma_gather4(sA + (uint32_t)s * C::A_BYTES + (uint32_t)h * kHalfA + 512u * (uint32_t)lane, &xmap,
+                          kb * BK, xr[h][0], xr[h][1], xr[h][2], xr[h][3], fullA(s));
         }
       }
     }
@@ -578,6 +609,8 @@ qmm_tc_kernel(const __grid_constant__ CUtensorMap xmap, const TcParams p) {
       bool ok = true;
       for (int i = 0; i < my_tiles && ok; ++i) {
         const int b = i % NBUF;
+        int mh = MH;  // M halves holding rows of the tile (a gather tile may fill one)
+        if (GATHER) mh = (tile_of<true, BM>(p, (int)blockIdx.x + i * (int)gridDim.x, seg, pre).rows + 127) / 128;
         if (!wait_bar(accEmpty(b), ((i / NBUF) & 1) ^ 1, abort_flag, 4)) break;
         tc_fence_after();
         const uint32_t d = tmem + (uint32_t)(b * MH * BN);
@@ -591,6 +624,7 @@ qmm_tc_kernel(const __grid_constant__ CUtensorMap xmap, const TcParams p) {
           for (int j = 0; j < BK / 16; ++j)
 #pragma unroll
             for (int h = 0; h < MH; ++h) {
+              if (h >= mh) continue;
               const uint64_t ad = sw128_desc(sA + (uint32_t)s * C::A_BYTES + (uint32_t)h * kHalfA);
               umma_f16(d + (uint32_t)(h * BN), ad + (uint64_t)(2 * j), bd + (uint64_t)(2 * j), idesc, (kb | j) != 0);
             }
@@ -720,6 +754,7 @@ cudaError_t launch_cfg(const void* x, int64_t M, int64_t K, const uint32_t* w, c
   p.rhs = nullptr;
   p.B = M;
   p.E = 1;
+  p.xcontig = 1;
   const int grid = p.num_tiles < sms ? p.num_tiles : sms;
   auto kern = qmm_tc_kernel<T, C, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
@@ -775,24 +810,103 @@ cudaError_t launch_tc(const void* x, int64_t M, int64_t K, const uint32_t* w, co
   }
 }
 
-// Expert-batched GatherQMM: 128-row tiles (expert segments are short enough
-// that 256-row tiles would mostly compute padding), persistent grid of one
-// CTA per SM; the tile count is known only on the device.
-template <typename T>
+// Activation rows in output-row order for the expert-batched route: xg[r] =
+// x[lhs[r]], zeros where lhs[r] >= B; kv 16-byte units per row. One warp per
+// row, four loads in flight per lane.
+__global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restrict__ x, const uint32_t* __restrict__ lhs,
+                                                          int64_t B, int64_t R, int kv, uint4* __restrict__ xg) {
+  const int lane = threadIdx.x & 31;
+  const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
+  for (int64_t r = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < R; r += nwarps) {
+    const int64_t src = (int64_t)__ldg(lhs + r);
+    uint4* dst = xg + r * kv;
+    if (src >= B) {
+      for (int j = lane; j < kv; j += 32) dst[j] = make_uint4(0, 0, 0, 0);
+      continue;
+    }
+    const uint4* row = x + src * kv;
+    for (int j0 = lane; j0 < kv; j0 += 128) {
+      uint4 v[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int j = j0 + 32 * q;
+        v[q] = j < kv ? __ldg(row + j) : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int j = j0 + 32 * q;
+        if (j < kv) dst[j] = v[q];
+      }
+    }
+  }
+}
+
+// Buffer for the gathered activations, one per (device, stream), grown on
+// demand and kept until release_gather_workspaces(). Allocated with the
+// thread's capture mode relaxed, so a call captured into a CUDA graph gets it
+// outside the capture (as the decode route's workspace).
+std::mutex g_xg_mu;
+std::map<std::pair<int, uintptr_t>, std::pair<void*, size_t>> g_xg;
+std::vector<void*> g_xg_retired;
+
+cudaError_t gather_buffer(int dev, cudaStream_t st, size_t bytes, void** out) {
+  std::lock_guard<std::mutex> lock(g_xg_mu);
+  auto& slot = g_xg[{dev, reinterpret_cast<uintptr_t>(st)}];
+  if (slot.second < bytes) {
+    cudaStreamCaptureMode mode = cudaStreamCaptureModeRelaxed;
+    cudaError_t e = cudaThreadExchangeStreamCaptureMode(&mode);
+    if (e != cudaSuccess) return e;
+    void* ptr = nullptr;
+    e = cudaMalloc(&ptr, bytes);
+    cudaStreamCaptureMode back = mode;
+    cudaThreadExchangeStreamCaptureMode(&back);
+    if (e != cudaSuccess) return e;
+    if (slot.first) g_xg_retired.push_back(slot.first);
+    slot = {ptr, bytes};
+  }
+  *out = slot.first;
+  return cudaSuccess;
+}
+
+// Expert-batched GatherQMM, persistent grid of one CTA per SM; the tile count
+// is known only on the device. A tile covers up to C::BM rows of one expert's
+// segment; a tile whose rows fit one 128-row half computes only that half.
+// With activation indices the rows are first gathered into output-row order,
+// so that every activation tile is a plain 128-row TMA box (a tile::gather4
+// copy moves four rows, and at 32 of them per box the copy engine, not the
+// tensor core, set the pace); NVFP4_GATHER_ROWS=tma keeps the per-row copies.
+template <typename T, typename C>
 cudaError_t launch_gather(const void* x, int64_t B, int64_t K, const uint32_t* lhs, const uint32_t* rhs, int64_t R,
                           const uint32_t* w, const uint8_t* scales, const float* gs, int64_t E, int64_t N, void* y,
                           cudaStream_t st) {
-  using C = Tile128x256;
   auto enc = encode_fn();
   if (!enc) return cudaErrorNotSupported;
+  int dev = 0, sms = 152;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const char* rows_env = std::getenv("NVFP4_GATHER_ROWS");
+  const bool per_row = lhs && rows_env && !std::strcmp(rows_env, "tma");
+  const void* xa = x;
+  int64_t xrows = B;
+  if (lhs && !per_row) {
+    void* xg = nullptr;
+    cudaError_t e = gather_buffer(dev, st, (size_t)R * (size_t)K * 2, &xg);
+    if (e != cudaSuccess) return e;
+    const int64_t blocks = (R + 7) / 8;
+    gather_rows_kernel<<<(unsigned)(blocks < 4 * sms ? blocks : 4 * sms), 256, 0, st>>>(
+        static_cast<const uint4*>(x), lhs, B, R, (int)(K / 8), static_cast<uint4*>(xg));
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    xa = xg;
+    xrows = R;
+  }
   CUtensorMap map;
-  const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)B};
+  const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)xrows};
   const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
-  const cuuint32_t box[2] = {BK, 1};  // tile::gather4 takes a one-row box
+  const cuuint32_t box[2] = {BK, per_row ? 1u : 128u};  // tile::gather4 takes a one-row box
   const cuuint32_t estr[2] = {1, 1};
   const CUtensorMapDataType dt =
       std::is_same<T, __nv_bfloat16>::value ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-  CUresult r = enc(&map, dt, 2, const_cast<void*>(x), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+  CUresult r = enc(&map, dt, 2, const_cast<void*>(xa), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
   TcParams p;
@@ -807,13 +921,11 @@ cudaError_t launch_gather(const void* x, int64_t B, int64_t K, const uint32_t* l
   p.num_n_tiles = (int)((N + C::BN - 1) / C::BN);
   p.num_tiles = 0;  // counted on the device
   p.num_kb = (int)((K + BK - 1) / BK);
-  p.lhs = lhs;
+  p.lhs = lhs;  // still read by the epilogue: rows with an index >= B are +0
   p.rhs = rhs;
   p.B = B;
   p.E = (int)E;
-  int dev = 0, sms = 152;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  p.xcontig = per_row ? 0 : 1;
   const size_t smem = C::SMEM + kGatherSmem;
   auto kern = qmm_tc_kernel<T, C, true>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -822,19 +934,33 @@ cudaError_t launch_gather(const void* x, int64_t B, int64_t K, const uint32_t* l
   return cudaGetLastError();
 }
 
+// Gather tile: 256 rows (two halves) by default, NVFP4_GATHER_TILE = "128x256"
+// or "256x128" to override.
+template <typename T>
+cudaError_t launch_gather_t(const void* x, int64_t B, int64_t K, const uint32_t* lhs, const uint32_t* rhs, int64_t R,
+                            const uint32_t* w, const uint8_t* scales, const float* gs, int64_t E, int64_t N, void* y,
+                            cudaStream_t st) {
+  const char* t = std::getenv("NVFP4_GATHER_TILE");
+  if (t && !std::strcmp(t, "128x256"))
+    return launch_gather<T, Tile128x256>(x, B, K, lhs, rhs, R, w, scales, gs, E, N, y, st);
+  if (t && !std::strcmp(t, "256x128"))
+    return launch_gather<T, Tile256x128>(x, B, K, lhs, rhs, R, w, scales, gs, E, N, y, st);
+  return launch_gather<T, Tile256x256>(x, B, K, lhs, rhs, R, w, scales, gs, E, N, y, st);
+}
+
 }  // namespace
 
 bool gather_tc_supported(int64_t B, int64_t K, int64_t R, int64_t E, int64_t N) {
   // 32-bit activation-row coordinates and row counts; K as for the dense route
   return B > 0 && B < (1ll << 31) && R > 0 && R < (1ll << 31) && E >= 1 && E <= kGatherMaxE && N > 0 && K >= 32 &&
-         K % 32 == 0 && K < (1ll << 31) && ((R + 127) / 128 + E) * ((N + 255) / 256) < (1ll << 31);
+         K % 32 == 0 && K < (1ll << 31) && ((R + 127) / 128 + E) * ((N + 127) / 128) < (1ll << 31);
 }
 
 cudaError_t launch_gather_tc(const void* x, int xdt, int64_t B, int64_t K, const uint32_t* lhs, const uint32_t* rhs,
                              int64_t R, const uint32_t* w, const uint8_t* scales, const float* gs, int64_t E, int64_t N,
                              void* y, cudaStream_t st) {
-  if (xdt == kBF16) return launch_gather<__nv_bfloat16>(x, B, K, lhs, rhs, R, w, scales, gs, E, N, y, st);
-  return launch_gather<__half>(x, B, K, lhs, rhs, R, w, scales, gs, E, N, y, st);
+  if (xdt == kBF16) return launch_gather_t<__nv_bfloat16>(x, B, K, lhs, rhs, R, w, scales, gs, E, N, y, st);
+  return launch_gather_t<__half>(x, B, K, lhs, rhs, R, w, scales, gs, E, N, y, st);
 }
 
 bool qmm_tc_supported(int64_t M, int64_t N, int64_t K) {
@@ -848,6 +974,14 @@ cudaError_t launch_qmm_tc(const void* x, int xdt, int64_t M, int64_t K, const ui
                           const float* gs, int64_t N, void* y, cudaStream_t st) {
   if (xdt == kBF16) return launch_tc<__nv_bfloat16>(x, M, K, w, scales, gs, N, y, st);
   return launch_tc<__half>(x, M, K, w, scales, gs, N, y, st);
+}
+
+void release_gather_workspaces() {
+  std::lock_guard<std::mutex> lock(g_xg_mu);
+  for (auto& kv : g_xg) cudaFree(kv.second.first);
+  g_xg.clear();
+  for (void* ptr : g_xg_retired) cudaFree(ptr);
+  g_xg_retired.clear();
 }
 
 int read_tc_error() {

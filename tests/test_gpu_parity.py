@@ -376,8 +376,14 @@ GATHER_TC_CASES = [(16, 272, 96, 300, 4), (8, 1024, 64, 4096, 4), (128, 256, 256
 
 @pytest.mark.parametrize("case", GATHER_TC_CASES, ids=lambda v: "E%d_N%d_K%d_T%d_k%d" % v)
 @pytest.mark.parametrize("dt", ["f16", "bf16"])
-def test_gather_sorted_tc_route(nv, monkeypatch, case, dt):
+@pytest.mark.parametrize("tile", ["256x256", "128x256", "256x128"])
+@pytest.mark.parametrize("rows", ["gathered", "tma"])
+def test_gather_sorted_tc_route(nv, monkeypatch, case, dt, tile, rows):
+    """Every tile shape, with the activation rows gathered into output order
+    first (plain 128-row boxes) or fetched row by row (tile::gather4)."""
     monkeypatch.setenv("NVFP4_GATHER_TC", "1")
+    monkeypatch.setenv("NVFP4_GATHER_TILE", tile)
+    monkeypatch.setenv("NVFP4_GATHER_ROWS", rows)
     E, N, K, T, topk = case
     w, s = weights(7 * E + N, E, N, K)
     g = synth.rng(E + N + K + T)
@@ -435,6 +441,29 @@ def test_gather_sorted_tc_matches_decode_route(nv, monkeypatch):
     b = nv.gather_qmm(*args, sorted_indices=True).float()
     assert nv.take_device_error() == 0
     assert (a - b).abs().max().item() <= 2 * 2.0**-8 * b.abs().max().item()
+
+
+def test_gather_sorted_tc_moe_prefill_full_size(nv):
+    """The MoE gate/up prefill: 4096 tokens, top-8 Zipf(1.1) routing over 128
+    experts, rows sorted by expert; sampled rows against the oracle."""
+    E, N, K, T = 128, 1536, 2048, 4096
+    g = synth.rng(4242)
+    w = synth.packed_weight(g, E, N, K)
+    s = synth.log_uniform_scales(g, (E, N, K // 16), 2.0**-6, 4.0)
+    gs = synth.global_scales(g, E)
+    x = synth.activations(g, (T, K), "bf16")
+    lhs, rhs = synth.zipf_routing(g, T, E, 8)
+    y = nv.gather_qmm(x.cuda(), u32_to_dev(w), u8_to_dev(s), u32_to_dev(rhs), u32_to_dev(lhs), gs=f32_to_dev(gs),
+                      sorted_indices=True)
+    torch.cuda.synchronize()
+    assert nv.take_device_error() == 0
+    # first and last rows of every expert segment plus a random sample
+    starts = np.searchsorted(rhs, np.arange(E + 1))
+    pick = np.unique(np.concatenate([starts[:-1], np.maximum(starts[1:] - 1, 0),
+                                     g.choice(len(rhs), size=256, replace=False)]))
+    pick = pick[pick < len(rhs)]
+    ref = O.gather_qmm(x.double().numpy(), lhs[pick], rhs[pick], w, s, gs)
+    assert rel_err(y[torch.from_numpy(pick).cuda()], ref) <= TOL["bf16"]
 
 
 def test_gather_tc_unsorted_promise_is_memory_safe(nv, monkeypatch):
