@@ -202,9 +202,11 @@ int64_t nvfp4_qmm_crossover(nvfp4_dtype x_dtype, int64_t N, int64_t K) {
   // launch per 16 token rows, about 12 + bytes / 3.9 MB each (other K: the
   // cluster kernel, about 8 + bytes / 1.7 MB for the first 16 rows and 0.55
   // of that for each further 16). Below 256 rows the tensor-core route costs
-  // one pass of weight decoding over ceil(N / 256) tiles: about 0.55 us per
-  // 64-column k-block while the tiles fit one wave of SMs, 0.8 beyond. M* is
-  // the first multiple of 16 where the decode route is slower.
+  // one pass of weight decoding over ceil(N / 256) tiles. With the stream-K
+  // split that work is spread evenly over the SMs: about 5 + 1.3 us per
+  // 64-column k-block of each SM's share (at least 8 k-blocks). Without it,
+  // about 0.55 us per k-block while the tiles fit one wave of SMs, 0.8
+  // beyond. M* is the first multiple of 16 where the decode route is slower.
   int dev = 0, sms = 152;
   if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     sms = 152;
@@ -212,8 +214,15 @@ int64_t nvfp4_qmm_crossover(nvfp4_dtype x_dtype, int64_t N, int64_t K) {
   const bool stream = K % 256 == 0;
   const double t16 = stream ? 12.0 + bytes / 3.9e6 : 8.0 + bytes / 1.7e6;
   const int64_t tiles = (N + 255) / 256;
-  const double waves = (double)((tiles + sms - 1) / sms);
-  const double t_tc = waves * (double)((K + 63) / 64) * (tiles <= sms ? 0.55 : 0.8);
+  const double kbs = (double)((K + 63) / 64);
+  double t_tc;
+  if (nvfp4::tc_stream_k()) {
+    const double share = (double)tiles * kbs / sms;
+    t_tc = 5.0 + 1.3 * (share > 8.0 ? share : 8.0);
+  } else {
+    const double waves = (double)((tiles + sms - 1) / sms);
+    t_tc = waves * kbs * (tiles <= sms ? 0.55 : 0.8);
+  }
   auto t_qmv = [&](int64_t m) {
     const double blocks = (double)((m + 15) / 16);
     return stream ? blocks * t16 : t16 * (1.0 + 0.55 * (blocks - 1.0));

@@ -62,6 +62,9 @@ bool launch_overlap();
 
 // Prefill-shape tensor-core route (tcgen05, TMEM accumulators).
 bool qmm_tc_supported(int64_t M, int64_t N, int64_t K);
+// Whether its dense launches split the last partial wave of tiles by k-blocks
+// (stream-K; on unless NVFP4_TC_STREAMK=0).
+bool tc_stream_k();
 cudaError_t launch_qmm_tc(const void* x, int xdt, int64_t M, int64_t K, const uint32_t* w, const uint8_t* scales,
                           const float* gs, int64_t N, void* y, cudaStream_t st);
 // Expert-batched GatherQMM on the tensor cores, for rows sorted by expert.

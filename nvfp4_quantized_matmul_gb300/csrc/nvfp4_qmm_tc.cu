@@ -90,6 +90,16 @@ struct TcParams {
   int E;        // experts
   int xcontig;  // gather: the activations of output row r are row r of the
                 // mapped x (x itself, or x gathered into output-row order)
+  // Dense work split: tiles [0, dp_tiles) are dealt whole, round robin; the
+  // k-block iterations of tiles [dp_tiles, dp_tiles + sk_tiles) are divided
+  // evenly over the CTAs (stream-K). A stream-K tile shared by several CTAs
+  // is summed in ws (BM x BN floats per tile, column-major so that a warp's
+  // 32 rows of one column are 128 contiguous bytes; sk_tiles of them) and
+  // finished by the CTA whose k-blocks complete ws_cnt[tile - dp_tiles]; both
+  // are left zeroed.
+  int dp_tiles, sk_tiles;
+  float* ws;
+  uint32_t* ws_cnt;
 };
 
 // One output tile: expert, weight tile, first output row and row count.
@@ -135,6 +145,48 @@ __device__ __forceinline__ Tile tile_of(const TcParams& p, int t, const int* seg
   r.rows = left < BM ? (int)left : BM;
   return r;
 }
+
+// A run of k-blocks [kb0, kb1) of one tile.
+struct Unit {
+  int tile, kb0, kb1;
+};
+
+// A CTA's units, in the order every role walks them: its share of the
+// stream-K iterations (tile-major, k-blocks fastest, cut at tile boundaries),
+// then its data-parallel tiles (blockIdx.x, + gridDim.x, ...). Split tiles come
+// first so that finishing them overlaps the whole tiles that follow.
+struct Sched {
+  int i_dp, n_dp, num_kb, dp;
+  int64_t it, it_end;
+  __device__ __forceinline__ void init(int dp_tiles, int sk_tiles, int kbs) {
+    dp = dp_tiles;
+    num_kb = kbs;
+    n_dp = (int)blockIdx.x < dp_tiles ? (dp_tiles - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x : 0;
+    i_dp = 0;
+    const int64_t I = (int64_t)sk_tiles * kbs;
+    it = I * blockIdx.x / gridDim.x;
+    it_end = I * (blockIdx.x + 1) / gridDim.x;
+  }
+  // k-blocks this CTA will process in all
+  __device__ __forceinline__ int64_t total() const { return (int64_t)(n_dp - i_dp) * num_kb + (it_end - it); }
+  __device__ __forceinline__ bool next(Unit& u) {
+    if (it < it_end) {
+      const int64_t t = it / num_kb;
+      u.tile = dp + (int)t;
+      u.kb0 = (int)(it - t * num_kb);
+      const int64_t left = it_end - it;
+      u.kb1 = left < (int64_t)(num_kb - u.kb0) ? u.kb0 + (int)left : num_kb;
+      it += u.kb1 - u.kb0;
+      return true;
+    }
+    if (i_dp >= n_dp) return false;
+    u.tile = (int)blockIdx.x + i_dp * (int)gridDim.x;
+    u.kb0 = 0;
+    u.kb1 = num_kb;
+    ++i_dp;
+    return true;
+  }
+};
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
@@ -263,16 +315,19 @@ struct WTask {
 };
 
 struct WCursor {
-  int tile, kb;
+  Sched sc;
+  Unit un;
+  int kb;
   bool done;
-  int e, nt;  // expert and weight tile of `tile`
+  int e, nt;  // expert and weight tile of the current unit's tile
 };
 
 template <bool GATHER, int BM>
-__device__ __forceinline__ void w_seek(WCursor& cur, const TcParams& p, int num_tiles, const int* seg, const int* pre) {
-  cur.done = cur.tile >= num_tiles;
+__device__ __forceinline__ void w_seek(WCursor& cur, const TcParams& p, const int* seg, const int* pre) {
+  cur.done = !cur.sc.next(cur.un);
   if (!cur.done) {
-    const Tile t = tile_of<GATHER, BM>(p, cur.tile, seg, pre);
+    cur.kb = cur.un.kb0;
+    const Tile t = tile_of<GATHER, BM>(p, cur.un.tile, seg, pre);
     cur.e = t.e;
     cur.nt = t.nt;
   }
@@ -304,13 +359,8 @@ __device__ __forceinline__ void w_load(WTask<RPT>& t, const WCursor& cur, const 
 }
 
 template <bool GATHER, int BM>
-__device__ __forceinline__ void w_advance(WCursor& cur, const TcParams& p, int num_tiles, const int* seg,
-                                          const int* pre) {
-  if (++cur.kb >= p.num_kb) {
-    cur.kb = 0;
-    cur.tile += gridDim.x;
-    w_seek<GATHER, BM>(cur, p, num_tiles, seg, pre);
-  }
+__device__ __forceinline__ void w_advance(WCursor& cur, const TcParams& p, const int* seg, const int* pre) {
+  if (!cur.done && ++cur.kb >= cur.un.kb1) w_seek<GATHER, BM>(cur, p, seg, pre);
 }
 
 // Decode one row's four words (columns 32h..32h+31 of the k-block) and store
@@ -333,14 +383,16 @@ __device__ __forceinline__ void w_store_row(uint32_t stage_base, int row, int h,
 }
 
 template <typename T, typename C, bool GATHER>
-__device__ void producer_role(const TcParams& p, uint32_t sB, uint32_t bars, volatile int* abort_flag, int num_tiles,
+__device__ void producer_role(const TcParams& p, uint32_t sB, uint32_t bars, volatile int* abort_flag, Sched sched,
                               const int* seg, const int* pre) {
   constexpr int STAGES = C::STAGES, RPT = C::RPT, BM = C::BM;
   const int pid = threadIdx.x - C::kWarpProd0 * 32;  // 0..255
   const int r = pid >> 1, h = pid & 1;               // rows r + 128 i, words 4h..4h+3 of the k-block
   const int lane = threadIdx.x & 31;
-  WCursor ld{(int)blockIdx.x, 0, true, 0, 0};
-  w_seek<GATHER, BM>(ld, p, num_tiles, seg, pre);
+  WCursor ld;
+  ld.sc = sched;
+  const int64_t total = sched.total();
+  w_seek<GATHER, BM>(ld, p, seg, pre);
   // PF k-blocks of packed weights in flight per thread (registers), so that
   // the L2 latency of the loads is covered by PF - 1 blocks of decoding.
   constexpr int PF = C::PF;
@@ -348,10 +400,9 @@ __device__ void producer_role(const TcParams& p, uint32_t sB, uint32_t bars, vol
 #pragma unroll
   for (int j = 0; j < PF - 1; ++j) {
     w_load<C::BN>(buf[j], ld, p, r, h);
-    w_advance<GATHER, BM>(ld, p, num_tiles, seg, pre);
+    w_advance<GATHER, BM>(ld, p, seg, pre);
   }
   uint32_t u = 0;
-  const int total = ((num_tiles - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x) * p.num_kb;
   auto consume = [&](const WTask<RPT>& t) -> bool {
     const int s = (int)(u % STAGES);
     const uint32_t ph = (u / STAGES) & 1;
@@ -367,12 +418,12 @@ __device__ void producer_role(const TcParams& p, uint32_t sB, uint32_t bars, vol
   };
   // the ring of buffers is indexed by compile-time positions only (unrolled),
   // so it stays in registers
-  for (int i = 0; i < total; i += PF) {
+  for (int64_t i = 0; i < total; i += PF) {
 #pragma unroll
     for (int j = 0; j < PF; ++j) {
       if (i + j >= total) return;
       w_load<C::BN>(buf[(j + PF - 1) % PF], ld, p, r, h);
-      w_advance<GATHER, BM>(ld, p, num_tiles, seg, pre);
+      w_advance<GATHER, BM>(ld, p, seg, pre);
       if (!consume(buf[j])) return;
     }
   }
@@ -506,20 +557,24 @@ qmm_tc_kernel(const __grid_constant__ CUtensorMap xmap, const TcParams p) {
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *holder;
-  const int num_tiles = GATHER ? pre[p.E] : p.num_tiles;
-  const int my_tiles = (int)blockIdx.x < num_tiles
-                           ? (num_tiles - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x
-                           : 0;
+  // Every role walks the same units; a gather's tiles (counted on the device)
+  // are all dealt whole.
+  Sched sched;
+  if (GATHER)
+    sched.init(pre[p.E], 0, p.num_kb);
+  else
+    sched.init(p.dp_tiles, p.sk_tiles, p.num_kb);
+  __shared__ int s_fin;  // stream-K: this CTA completes the tile being finished
 
   if (warp == kWarpTma) {
     uint32_t u = 0;
+    Unit un;
     if (!GATHER) {
       if (lane == 0) {
         bool ok = true;
-        for (int i = 0; i < my_tiles && ok; ++i) {
-          const int tile = (int)blockIdx.x + i * (int)gridDim.x;
-          const int m_tile = tile % p.num_m_tiles;
-          for (int kb = 0; kb < p.num_kb; ++kb, ++u) {
+        while (ok && sched.next(un)) {
+          const int m_tile = un.tile % p.num_m_tiles;
+          for (int kb = un.kb0; kb < un.kb1; ++kb, ++u) {
             const int s = (int)(u % STAGES);
             const uint32_t ph = (u / STAGES) & 1;
             if (!wait_bar(emptyB(s), ph ^ 1, abort_flag, 1)) { ok = false; break; }
@@ -537,10 +592,10 @@ qmm_tc_kernel(const __grid_constant__ CUtensorMap xmap, const TcParams p) {
       // them belong to the next expert or lie beyond x; they are computed but
       // not stored).
       bool ok = true;
-      for (int i = 0; i < my_tiles && ok; ++i) {
-        const Tile tl = tile_of<true, BM>(p, (int)blockIdx.x + i * (int)gridDim.x, seg, pre);
+      while (ok && sched.next(un)) {
+        const Tile tl = tile_of<true, BM>(p, un.tile, seg, pre);
         const int mh = (tl.rows + 127) / 128;
-        for (int kb = 0; kb < p.num_kb; ++kb, ++u) {
+        for (int kb = un.kb0; kb < un.kb1; ++kb, ++u) {
           const int s = (int)(u % STAGES);
           const uint32_t ph = (u / STAGES) & 1;
           if (!wait_bar_warp(emptyB(s), ph ^ 1, abort_flag, 1, &g_tc_error)) { ok = false; break; }
@@ -561,8 +616,8 @@ qmm_tc_kernel(const __grid_constant__ CUtensorMap xmap, const TcParams p) {
       // past the tile's end or with an out-of-range activation index read row
       // 0 (their outputs are not taken from the accumulator).
       bool ok = true;
-      for (int i = 0; i < my_tiles && ok; ++i) {
-        const Tile tl = tile_of<true, BM>(p, (int)blockIdx.x + i * (int)gridDim.x, seg, pre);
+      while (ok && sched.next(un)) {
+        const Tile tl = tile_of<true, BM>(p, un.tile, seg, pre);
         const int mh = (tl.rows + 127) / 128;
         int xr[MH][4];
 #pragma unroll
@@ -578,7 +633,7 @@ qmm_tc_kernel(const __grid_constant__ CUtensorMap xmap, const TcParams p) {
             }
             xr[h][j] = (int)v;
           }
-        for (int kb = 0; kb < p.num_kb; ++kb, ++u) {
+        for (int kb = un.kb0; kb < un.kb1; ++kb, ++u) {
           const int s = (int)(u % STAGES);
           const uint32_t ph = (u / STAGES) & 1;
           if (!wait_bar_warp(emptyB(s), ph ^ 1, abort_flag, 1, &g_tc_error)) { ok = false; break; }
@@ -607,14 +662,15 @@ qmm_tc_kernel(const __grid_constant__ CUtensorMap xmap, const TcParams p) {
       constexpr uint32_t idesc = make_idesc<std::is_same<T, __nv_bfloat16>::value, BN>();
       uint32_t u = 0;
       bool ok = true;
-      for (int i = 0; i < my_tiles && ok; ++i) {
+      Unit un;
+      for (int i = 0; ok && sched.next(un); ++i) {
         const int b = i % NBUF;
         int mh = MH;  // M halves holding rows of the tile (a gather tile may fill one)
-        if (GATHER) mh = (tile_of<true, BM>(p, (int)blockIdx.x + i * (int)gridDim.x, seg, pre).rows + 127) / 128;
+        if (GATHER) mh = (tile_of<true, BM>(p, un.tile, seg, pre).rows + 127) / 128;
         if (!wait_bar(accEmpty(b), ((i / NBUF) & 1) ^ 1, abort_flag, 4)) break;
         tc_fence_after();
         const uint32_t d = tmem + (uint32_t)(b * MH * BN);
-        for (int kb = 0; kb < p.num_kb; ++kb, ++u) {
+        for (int kb = un.kb0; kb < un.kb1; ++kb, ++u) {
           const int s = (int)(u % STAGES);
           const uint32_t ph = (u / STAGES) & 1;
           if (!wait_bar(fullA(s), ph, abort_flag, 5) || !wait_bar(fullB(s), ph, abort_flag, 6)) { ok = false; break; }
@@ -626,7 +682,8 @@ qmm_tc_kernel(const __grid_constant__ CUtensorMap xmap, const TcParams p) {
             for (int h = 0; h < MH; ++h) {
               if (h >= mh) continue;
               const uint64_t ad = sw128_desc(sA + (uint32_t)s * C::A_BYTES + (uint32_t)h * kHalfA);
-              umma_f16(d + (uint32_t)(h * BN), ad + (uint64_t)(2 * j), bd + (uint64_t)(2 * j), idesc, (kb | j) != 0);
+              umma_f16(d + (uint32_t)(h * BN), ad + (uint64_t)(2 * j), bd + (uint64_t)(2 * j), idesc,
+                       ((kb - un.kb0) | j) != 0);
             }
           umma_commit(emptyB(s));
         }
@@ -636,19 +693,51 @@ qmm_tc_kernel(const __grid_constant__ CUtensorMap xmap, const TcParams p) {
   } else if (warp >= kWarpEpi0 && warp < kWarpEpi0 + C::EPI_WARPS) {
     const int q = warp & 3;                  // TMEM lane quarter this warp may read
     const int hm = (warp - kWarpEpi0) >> 2;  // M half it drains
+    const int etid = threadIdx.x - 32 * kWarpEpi0;
     T* y = static_cast<T*>(p.y);
     if (GATHER) {
       // rows whose expert index is out of range (sorted last) are exact +0
       const int64_t z0 = seg[p.E];
       const int64_t total = (p.M - z0) * p.N;
-      const int ethreads = 32 * C::EPI_WARPS, etid = threadIdx.x - 32 * kWarpEpi0;
+      const int ethreads = 32 * C::EPI_WARPS;
       uint16_t* yz = reinterpret_cast<uint16_t*>(y) + z0 * p.N;
       for (int64_t i = (int64_t)blockIdx.x * ethreads + etid; i < total; i += (int64_t)gridDim.x * ethreads) yz[i] = 0;
     }
-    for (int i = 0; i < my_tiles; ++i) {
-      const Tile tl = tile_of<GATHER, BM>(p, (int)blockIdx.x + i * (int)gridDim.x, seg, pre);
+    // factor, cast and store 32 consecutive outputs of row m from n0
+    auto store32 = [&](const uint32_t (&r)[32], int64_t m, int64_t n0, float fac, bool zero) {
+      uint32_t packed[16];
+#pragma unroll
+      for (int k = 0; k < 16; ++k) {
+        float v0 = __uint_as_float(r[2 * k]), v1 = __uint_as_float(r[2 * k + 1]);
+        if (p.gs) {
+          v0 = __fmul_rn(v0, fac);
+          v1 = __fmul_rn(v1, fac);
+        }
+        const T t0 = Dt<T>::from_f32(v0), t1 = Dt<T>::from_f32(v1);
+        packed[k] = zero ? 0u
+                         : (uint32_t)(*reinterpret_cast<const uint16_t*>(&t0)) |
+                               ((uint32_t)(*reinterpret_cast<const uint16_t*>(&t1)) << 16);
+      }
+      T* dst = y + m * p.N + n0;
+      if (n0 + 32 <= p.N && (p.N % 8) == 0) {
+        uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          d4[k] = make_uint4(packed[4 * k], packed[4 * k + 1], packed[4 * k + 2], packed[4 * k + 3]);
+      } else {
+        uint16_t* d16 = reinterpret_cast<uint16_t*>(dst);
+        for (int k = 0; k < 32 && n0 + k < p.N; ++k) d16[k] = (uint16_t)(packed[k >> 1] >> (16 * (k & 1)));
+      }
+    };
+    // After a wait gives up (the CTA is aborting) a warp keeps walking its
+    // units without touching TMEM or memory, so that the epilogue warps still
+    // meet at every named barrier.
+    bool dead = false;
+    Unit un;
+    for (int i = 0; sched.next(un); ++i) {
+      const Tile tl = tile_of<GATHER, BM>(p, un.tile, seg, pre);
       const int b = i % NBUF;
-      if (!wait_bar_warp(accFull(b), (i / NBUF) & 1, abort_flag, 7, &g_tc_error)) break;
+      if (!dead && !wait_bar_warp(accFull(b), (i / NBUF) & 1, abort_flag, 7, &g_tc_error)) dead = true;
       tc_fence_after();
       const int rr = 128 * hm + 32 * q + lane;  // row within the tile
       const int64_t m = tl.m0 + rr;
@@ -661,6 +750,51 @@ qmm_tc_kernel(const __grid_constant__ CUtensorMap xmap, const TcParams p) {
       const float fac = global_factor(p.gs, tl.e);
       const int64_t n_base = (int64_t)tl.nt * BN;
       const uint32_t tcol = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(b * MH * BN + hm * BN);
+      if (!GATHER && (un.kb0 != 0 || un.kb1 != p.num_kb)) {
+        // A piece of a stream-K tile: add it to the tile's sums, count its
+        // k-blocks; the piece that completes the count finishes the tile.
+        const int slot = un.tile - p.dp_tiles;
+        float* wcol = p.ws + (int64_t)slot * (BM * BN) + rr;  // + column * BM
+        if (!dead) {
+#pragma unroll 1
+          for (int c = 0; c < BN / 32; ++c) {
+            uint32_t r[32];
+            tmem_ld32(tcol + (uint32_t)(32 * c), r);
+            tmem_ld_wait();
+            if (!live || n_base + 32 * c >= p.N) continue;
+#pragma unroll
+            for (int k = 0; k < 32; ++k) atomicAdd(wcol + (int64_t)(32 * c + k) * BM, __uint_as_float(r[k]));
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(accEmpty(b));  // the accumulator is free again
+        }
+        __threadfence();
+        asm volatile("bar.sync 1, %0;" ::"n"(C::EPI_WARPS * 32) : "memory");
+        if (etid == 0) {
+          const uint32_t add = (uint32_t)(un.kb1 - un.kb0);
+          s_fin = dead ? 0 : (atomicAdd(p.ws_cnt + slot, add) + add == (uint32_t)p.num_kb);
+        }
+        asm volatile("bar.sync 1, %0;" ::"n"(C::EPI_WARPS * 32) : "memory");
+        if (s_fin && !dead) {
+          __threadfence();
+#pragma unroll 1
+          for (int c = 0; c < BN / 32; ++c) {
+            const int64_t n0 = n_base + 32 * c;
+            if (!live || n0 >= p.N) continue;
+            uint32_t r[32];
+            float* src = wcol + (int64_t)(32 * c) * BM;
+#pragma unroll
+            for (int k = 0; k < 32; ++k) r[k] = __float_as_uint(__ldcg(src + (int64_t)k * BM));
+#pragma unroll
+            for (int k = 0; k < 32; ++k) __stcg(src + (int64_t)k * BM, 0.f);
+            store32(r, m, n0, fac, false);
+          }
+          if (etid == 0) atomicExch(p.ws_cnt + slot, 0u);
+        }
+        continue;
+      }
+      if (dead) continue;
 #pragma unroll 1
       for (int c = 0; c < BN / 32; ++c) {
         uint32_t r[32];
@@ -669,37 +803,14 @@ qmm_tc_kernel(const __grid_constant__ CUtensorMap xmap, const TcParams p) {
         if (!live) continue;
         const int64_t n0 = n_base + 32 * c;
         if (n0 >= p.N) continue;
-        uint32_t packed[16];
-#pragma unroll
-        for (int k = 0; k < 16; ++k) {
-          float v0 = __uint_as_float(r[2 * k]), v1 = __uint_as_float(r[2 * k + 1]);
-          if (p.gs) {
-            v0 = __fmul_rn(v0, fac);
-            v1 = __fmul_rn(v1, fac);
-          }
-          const T t0 = Dt<T>::from_f32(v0), t1 = Dt<T>::from_f32(v1);
-          packed[k] = zero ? 0u
-                           : (uint32_t)(*reinterpret_cast<const uint16_t*>(&t0)) |
-                                 ((uint32_t)(*reinterpret_cast<const uint16_t*>(&t1)) << 16);
-        }
-        T* dst = y + m * p.N + n0;
-        if (n0 + 32 <= p.N && (p.N % 8) == 0) {
-          uint4* d4 = reinterpret_cast<uint4*>(dst);
-#pragma unroll
-          for (int k = 0; k < 4; ++k)
-            d4[k] = make_uint4(packed[4 * k], packed[4 * k + 1], packed[4 * k + 2], packed[4 * k + 3]);
-        } else {
-          uint16_t* d16 = reinterpret_cast<uint16_t*>(dst);
-          for (int k = 0; k < 32 && n0 + k < p.N; ++k)
-            d16[k] = (uint16_t)(packed[k >> 1] >> (16 * (k & 1)));
-        }
+        store32(r, m, n0, fac, zero);
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(accEmpty(b));
     }
   } else if (warp >= C::kWarpProd0) {
-    producer_role<T, C, GATHER>(p, sB, bars, abort_flag, num_tiles, seg, pre);
+    producer_role<T, C, GATHER>(p, sB, bars, abort_flag, sched, seg, pre);
   }
 
   tc_fence_before();
@@ -722,6 +833,67 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   });
   return fn;
 }
+
+// Stream-K sums and counters, one buffer pair per (device, stream), grown on
+// demand and zeroed when made (on a private stream, with the thread's capture
+// mode relaxed, so that a call captured into a CUDA graph gets them outside
+// the capture); every launch leaves them zeroed again.
+struct SkWs {
+  float* acc = nullptr;
+  uint32_t* cnt = nullptr;
+  size_t floats = 0, counters = 0;
+};
+std::mutex g_sk_mu;
+std::map<std::pair<int, uintptr_t>, SkWs> g_sk;
+std::vector<void*> g_sk_retired;
+
+cudaError_t zero_private(void* ptr, size_t bytes) {
+  cudaStream_t z = nullptr;
+  cudaError_t e = cudaStreamCreateWithFlags(&z, cudaStreamNonBlocking);
+  if (e != cudaSuccess) return e;
+  e = cudaMemsetAsync(ptr, 0, bytes, z);
+  const cudaError_t e2 = cudaStreamSynchronize(z);
+  cudaStreamDestroy(z);
+  return e != cudaSuccess ? e : e2;
+}
+
+cudaError_t sk_workspace(int dev, cudaStream_t st, size_t floats, size_t counters, SkWs* out) {
+  std::lock_guard<std::mutex> lock(g_sk_mu);
+  SkWs& w = g_sk[{dev, reinterpret_cast<uintptr_t>(st)}];
+  if (w.floats < floats || w.counters < counters) {
+    cudaStreamCaptureMode mode = cudaStreamCaptureModeRelaxed;
+    cudaError_t e = cudaThreadExchangeStreamCaptureMode(&mode);
+    if (e != cudaSuccess) return e;
+    const size_t nf = floats > w.floats ? floats : w.floats, nc = counters > w.counters ? counters : w.counters;
+    float* acc = nullptr;
+    uint32_t* cnt = nullptr;
+    e = cudaMalloc(&acc, nf * sizeof(float));
+    if (e == cudaSuccess) e = cudaMalloc(&cnt, nc * sizeof(uint32_t));
+    if (e == cudaSuccess) e = zero_private(acc, nf * sizeof(float));
+    if (e == cudaSuccess) e = zero_private(cnt, nc * sizeof(uint32_t));
+    cudaStreamCaptureMode back = mode;
+    cudaThreadExchangeStreamCaptureMode(&back);
+    if (e != cudaSuccess) {
+      cudaFree(acc);
+      cudaFree(cnt);
+      return e;
+    }
+    if (w.acc) g_sk_retired.push_back(w.acc);
+    if (w.cnt) g_sk_retired.push_back(w.cnt);
+    w.acc = acc;
+    w.cnt = cnt;
+    w.floats = nf;
+    w.counters = nc;
+  }
+  *out = w;
+  return cudaSuccess;
+}
+
+bool stream_k_on() { return tc_stream_k(); }
+
+// Fewest k-blocks a CTA takes of the stream-K tiles when they are fewer than
+// the SMs (smaller pieces cost more to combine than they save).
+constexpr int64_t kMinSkBlocks = 8;
 
 template <typename T, typename C>
 cudaError_t launch_cfg(const void* x, int64_t M, int64_t K, const uint32_t* w, const uint8_t* scales, const float* gs,
@@ -755,7 +927,35 @@ cudaError_t launch_cfg(const void* x, int64_t M, int64_t K, const uint32_t* w, c
   p.B = M;
   p.E = 1;
   p.xcontig = 1;
-  const int grid = p.num_tiles < sms ? p.num_tiles : sms;
+  // Whole waves of tiles are dealt round robin. The tiles that would make up
+  // the last, partial wave (with one full wave before them, so that every
+  // CTA's share is at least a tile) are split evenly by k-blocks instead.
+  const int T_ = p.num_tiles;
+  int grid = T_ < sms ? T_ : sms;
+  p.dp_tiles = T_;
+  p.sk_tiles = 0;
+  if (stream_k_on() && T_ % sms != 0) {
+    if (T_ > sms) {
+      p.dp_tiles = (T_ / sms - 1) * sms;
+      grid = sms;
+    } else {
+      p.dp_tiles = 0;
+      const int64_t by_blocks = (int64_t)T_ * p.num_kb / kMinSkBlocks;
+      grid = (int)(by_blocks < T_ ? T_ : (by_blocks < sms ? by_blocks : sms));
+    }
+    p.sk_tiles = T_ - p.dp_tiles;
+  }
+  p.ws = nullptr;
+  p.ws_cnt = nullptr;
+  if (p.sk_tiles > 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    SkWs ws;
+    cudaError_t e = sk_workspace(dev, st, (size_t)p.sk_tiles * C::BM * C::BN, (size_t)p.sk_tiles, &ws);
+    if (e != cudaSuccess) return e;
+    p.ws = ws.acc;
+    p.ws_cnt = ws.cnt;
+  }
   auto kern = qmm_tc_kernel<T, C, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
   if (e != cudaSuccess) return e;
@@ -767,13 +967,15 @@ using Tile256x256 = Cfg<2, 256>;
 using Tile256x128 = Cfg<2, 128>;
 using Tile128x256 = Cfg<1, 256>;
 
-// Tile shape by modelled time: whole waves of persistent tiles, each tile's
-// cost its area over the shape's relative throughput. The rates are measured
-// on GB300 with full waves (M = 8192, [21504, 5376]): 256x128 tiles run at
-// 0.81 of 256x256, whose decoded weight tile feeds twice the MMA work, and
-// 128x256 tiles at 0.54. With them the model picks the fastest shape on a
-// sweep of M = 512 .. 8192 and of K = 21504. The environment variable
-// NVFP4_TC_TILE ("256x256", "256x128" or "128x256") overrides it.
+// Tile shape. With the stream-K split there are no partial waves to avoid,
+// and 256x256 tiles, whose decoded weight tile feeds twice the MMA work, were
+// the fastest or within 4% of it on every prefill shape measured on GB300
+// (M = 64 .. 8192, K = 5376 and 21504). Without it (NVFP4_TC_STREAMK=0) the
+// shape is picked by modelled time: whole waves of persistent tiles, each
+// tile's cost its area over the shape's relative throughput (measured with
+// full waves at M = 8192, [21504, 5376]: 256x128 tiles run at 0.81 of
+// 256x256, 128x256 tiles at 0.54). The environment variable NVFP4_TC_TILE
+// ("256x256", "256x128" or "128x256") overrides either choice.
 int pick_tile(int64_t M, int64_t N, int sms) {
   const char* forced = std::getenv("NVFP4_TC_TILE");
   if (forced) {
@@ -781,6 +983,7 @@ int pick_tile(int64_t M, int64_t N, int sms) {
     if (!std::strcmp(forced, "256x128")) return 1;
     if (!std::strcmp(forced, "128x256")) return 2;
   }
+  if (stream_k_on()) return 0;
   const int bm[3] = {256, 256, 128}, bn[3] = {256, 128, 256};
   const double rate[3] = {1.0, 0.81, 0.54};
   int best = 0;
@@ -926,6 +1129,10 @@ cudaError_t launch_gather(const void* x, int64_t B, int64_t K, const uint32_t* l
   p.B = B;
   p.E = (int)E;
   p.xcontig = per_row ? 0 : 1;
+  p.dp_tiles = 0;  // set on the device from the segment table
+  p.sk_tiles = 0;
+  p.ws = nullptr;
+  p.ws_cnt = nullptr;
   const size_t smem = C::SMEM + kGatherSmem;
   auto kern = qmm_tc_kernel<T, C, true>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -963,6 +1170,11 @@ cudaError_t launch_gather_tc(const void* x, int xdt, int64_t B, int64_t K, const
   return launch_gather_t<__half>(x, B, K, lhs, rhs, R, w, scales, gs, E, N, y, st);
 }
 
+bool tc_stream_k() {
+  const char* e = std::getenv("NVFP4_TC_STREAMK");
+  return !(e && e[0] == '0');
+}
+
 bool qmm_tc_supported(int64_t M, int64_t N, int64_t K) {
   // TMA coordinates are 32-bit; K must keep each 128-bit weight load within
   // one k-block row segment (K % 32 == 0).
@@ -977,11 +1189,21 @@ cudaError_t launch_qmm_tc(const void* x, int xdt, int64_t M, int64_t K, const ui
 }
 
 void release_gather_workspaces() {
-  std::lock_guard<std::mutex> lock(g_xg_mu);
-  for (auto& kv : g_xg) cudaFree(kv.second.first);
-  g_xg.clear();
-  for (void* ptr : g_xg_retired) cudaFree(ptr);
-  g_xg_retired.clear();
+  {
+    std::lock_guard<std::mutex> lock(g_xg_mu);
+    for (auto& kv : g_xg) cudaFree(kv.second.first);
+    g_xg.clear();
+    for (void* ptr : g_xg_retired) cudaFree(ptr);
+    g_xg_retired.clear();
+  }
+  std::lock_guard<std::mutex> lock(g_sk_mu);
+  for (auto& kv : g_sk) {
+    cudaFree(kv.second.acc);
+    cudaFree(kv.second.cnt);
+  }
+  g_sk.clear();
+  for (void* ptr : g_sk_retired) cudaFree(ptr);
+  g_sk_retired.clear();
 }
 
 int read_tc_error() {

@@ -130,14 +130,21 @@ def test_crossover_env_override(nv, monkeypatch):
 
 def test_crossover_model(nv, monkeypatch):
     """The default crossover follows the route sweep on GB300: gate/up and
-    qkv switch to the tensor cores at 48 token rows (two 16-row decode
-    launches still beat them at 32), the down projection (21 weight tiles
-    for 152 SMs) only at 112; f32 never."""
+    down switch to the tensor cores at 48 token rows (two 16-row decode
+    launches still beat them at 32), qkv at 32; f32 never. Without the
+    stream-K split the tensor-core route is slower at small M and down (21
+    weight tiles for 152 SMs) switches only at 112."""
     monkeypatch.delenv("NVFP4_QMM_CROSSOVER", raising=False)
+    monkeypatch.delenv("NVFP4_TC_STREAMK", raising=False)
     lib = nv.library()
+    assert lib.nvfp4_qmm_crossover(2, 43008, 5376) == 48
+    assert lib.nvfp4_qmm_crossover(2, 8192, 5376) == 32
+    assert lib.nvfp4_qmm_crossover(2, 5376, 21504) == 48
+    monkeypatch.setenv("NVFP4_TC_STREAMK", "0")
     assert lib.nvfp4_qmm_crossover(2, 43008, 5376) == 48
     assert lib.nvfp4_qmm_crossover(2, 8192, 5376) == 48
     assert lib.nvfp4_qmm_crossover(2, 5376, 21504) == 112
+    monkeypatch.delenv("NVFP4_TC_STREAMK", raising=False)
     assert lib.nvfp4_qmm_crossover(1, 43008, 5376) == 48
     assert lib.nvfp4_qmm_crossover(0, 43008, 5376) > 2**62
     for n, k in ((256, 256), (1 << 20, 64), (64, 1 << 20)):
