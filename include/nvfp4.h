@@ -21,12 +21,16 @@
  *   - All data pointers are DEVICE pointers owned by the caller; the library
  *     keeps no reference after the call returns. Lengths are element counts.
  *   - Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL is the
- *     legacy default stream). Nothing is synchronised. The only allocation is
- *     the decode route's workspace (see nvfp4_qmm): made on the first such
- *     call on a stream, or the first that needs more, and kept until
+ *     legacy default stream). Nothing is synchronised. The library allocates
+ *     three kinds of scratch, each one per (device, stream): the decode
+ *     route's split-tile workspace (see nvfp4_qmm), the tensor-core route's
+ *     stream-K sums (up to two waves of 256 x 256 f32 tiles and a counter
+ *     each, about 78 MB on 152 SMs) and the expert-batched gather's row
+ *     buffer (see nvfp4_gather_qmm). Each is made on the first call on a
+ *     stream that needs it, or the first that needs more, and kept until
  *     nvfp4_shutdown(). Made while the stream is being captured into a CUDA
  *     graph, the allocation is done outside the capture (the thread's capture
- *     mode relaxed for it) and the graph uses that workspace on every replay.
+ *     mode relaxed for it) and the graph uses that memory on every replay.
  *   - Data pointers must be 16-byte aligned; index arrays and gs 4-byte.
  *   - K must be a multiple of 16. Any N >= 1 is accepted.
  *   - Empty outputs (M, N or R equal to 0) return NVFP4_OK without a launch.
@@ -188,8 +192,8 @@ int32_t nvfp4_take_device_error(void);
  * decode-step matmuls, whose weights are constant. */
 int nvfp4_set_launch_overlap(int enable);
 
-/* Frees the decode route's workspaces and the gathered-row buffers of the
- * expert-batched route on every device. Call only when no
+/* Frees the library's scratch (decode workspaces, stream-K sums, gathered-row
+ * buffers) on every device. Call only when no
  * library work is queued or running; a later call allocates again. Not part
  * of the pages' interface. */
 void nvfp4_shutdown(void);
