@@ -63,60 +63,59 @@ transcode_kernel(const uint8_t* __restrict__ mo_w, int64_t w_bytes, const uint8_
 
 // Exact dequantize (PR #2629 "ROCm native NVFP4", Summary: the dequantize
 // kernel expands a plane exactly; Changes during review: the grid is sized
-// from the weight plane). One thread-iteration expands one 16-column block:
-// two packed words and one scale byte in, sixteen outputs out. Element value
-// = cast(f32(fp4 * e4m3) * factor) with factor = gs[e] / 2688 (absent gs:
-// the product itself, exact in every output type).
+// from the weight plane). One thread-iteration expands one packed word (half
+// of a 16-column block): eight outputs from the word and its block's scale
+// byte, so that a warp's output store is 32 x 16 contiguous bytes (bf16/f16).
+// Element value = cast(f32(fp4 * e4m3) * factor) with factor = gs[e] / 2688
+// (absent gs: the product itself, exact in every output type).
 template <typename OutT>
-__device__ __forceinline__ void store16(OutT* dst, const uint32_t (&h)[8], float fac, bool has_gs);
+__device__ __forceinline__ void store8(OutT* dst, const uint32_t (&h)[4], float fac, bool has_gs);
 
 __device__ __forceinline__ float h_lo(uint32_t v) { return __half2float(__ushort_as_half((unsigned short)(v & 0xFFFF))); }
 __device__ __forceinline__ float h_hi(uint32_t v) { return __half2float(__ushort_as_half((unsigned short)(v >> 16))); }
 
 template <>
-__device__ __forceinline__ void store16<float>(float* dst, const uint32_t (&h)[8], float fac, bool has_gs) {
-  float v[16];
+__device__ __forceinline__ void store8<float>(float* dst, const uint32_t (&h)[4], float fac, bool has_gs) {
+  float v[8];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
+  for (int i = 0; i < 4; ++i) {
     v[2 * i] = h_lo(h[i]);
     v[2 * i + 1] = h_hi(h[i]);
   }
   if (has_gs) {
 #pragma unroll
-    for (int i = 0; i < 16; ++i) v[i] = __fmul_rn(v[i], fac);
+    for (int i = 0; i < 8; ++i) v[i] = __fmul_rn(v[i], fac);
   }
   uint4* d = reinterpret_cast<uint4*>(dst);
 #pragma unroll
-  for (int q = 0; q < 4; ++q)
+  for (int q = 0; q < 2; ++q)
     __stcs(d + q, make_uint4(__float_as_uint(v[4 * q]), __float_as_uint(v[4 * q + 1]),
                              __float_as_uint(v[4 * q + 2]), __float_as_uint(v[4 * q + 3])));
 }
 
 template <>
-__device__ __forceinline__ void store16<__half>(__half* dst, const uint32_t (&h)[8], float fac, bool has_gs) {
-  uint32_t o[8];
+__device__ __forceinline__ void store8<__half>(__half* dst, const uint32_t (&h)[4], float fac, bool has_gs) {
+  uint32_t o[4];
   if (!has_gs) {
 #pragma unroll
-    for (int i = 0; i < 8; ++i) o[i] = h[i];
+    for (int i = 0; i < 4; ++i) o[i] = h[i];
   } else {
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
+    for (int i = 0; i < 4; ++i) {
       const __half lo = __float2half_rn(__fmul_rn(h_lo(h[i]), fac));
       const __half hi = __float2half_rn(__fmul_rn(h_hi(h[i]), fac));
       o[i] = (uint32_t)__half_as_ushort(lo) | ((uint32_t)__half_as_ushort(hi) << 16);
     }
   }
-  uint4* d = reinterpret_cast<uint4*>(dst);
-  __stcs(d, make_uint4(o[0], o[1], o[2], o[3]));
-  __stcs(d + 1, make_uint4(o[4], o[5], o[6], o[7]));
+  __stcs(reinterpret_cast<uint4*>(dst), make_uint4(o[0], o[1], o[2], o[3]));
 }
 
 template <>
-__device__ __forceinline__ void store16<__nv_bfloat16>(__nv_bfloat16* dst, const uint32_t (&h)[8], float fac,
-                                                       bool has_gs) {
-  uint32_t o[8];
+__device__ __forceinline__ void store8<__nv_bfloat16>(__nv_bfloat16* dst, const uint32_t (&h)[4], float fac,
+                                                      bool has_gs) {
+  uint32_t o[4];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
+  for (int i = 0; i < 4; ++i) {
     float a = h_lo(h[i]), b = h_hi(h[i]);
     if (has_gs) {
       a = __fmul_rn(a, fac);
@@ -125,52 +124,44 @@ __device__ __forceinline__ void store16<__nv_bfloat16>(__nv_bfloat16* dst, const
     o[i] = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(a)) |
            ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(b)) << 16);
   }
-  uint4* d = reinterpret_cast<uint4*>(dst);
-  __stcs(d, make_uint4(o[0], o[1], o[2], o[3]));
-  __stcs(d + 1, make_uint4(o[4], o[5], o[6], o[7]));
+  __stcs(reinterpret_cast<uint4*>(dst), make_uint4(o[0], o[1], o[2], o[3]));
 }
 
 template <typename OutT>
 __global__ void __launch_bounds__(kStreamThreads)
 dequantize_kernel(const uint32_t* __restrict__ w, const uint8_t* __restrict__ scales,
-                  const float* __restrict__ gs, int64_t E, int64_t groups_per_expert,
+                  const float* __restrict__ gs, int64_t E, int64_t words_per_expert,
                   OutT* __restrict__ out) {
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   for (int64_t e = blockIdx.y; e < E; e += gridDim.y) {
     const float fac = global_factor(gs, e);
     const bool has_gs = gs != nullptr;
-    const int64_t base = e * groups_per_expert;
-    // kU groups per thread and iteration, all loads issued before any decode
+    const int64_t base = e * words_per_expert;  // first word of expert e
+    // kU words per thread and iteration, all loads issued before any decode
     // so that their latencies overlap.
-    constexpr int kU = 4;
-    int64_t gi = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    for (; gi + (kU - 1) * stride < groups_per_expert; gi += kU * stride) {
-      uint2 ww[kU];
-      uint32_t sb[kU];
+    constexpr int kU = 8;
+    int64_t vi = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    for (; vi + (kU - 1) * stride < words_per_expert; vi += kU * stride) {
+      uint32_t wv[kU], sb[kU];
 #pragma unroll
       for (int u = 0; u < kU; ++u) {
-        const int64_t g = base + gi + u * stride;
-        ww[u] = ld_stream_v2(w + 2 * g);
-        sb[u] = __ldcs(scales + g);
+        const int64_t v = base + vi + u * stride;
+        wv[u] = __ldcs(w + v);
+        sb[u] = __ldcs(scales + (v >> 1));
       }
 #pragma unroll
       for (int u = 0; u < kU; ++u) {
-        const int64_t g = base + gi + u * stride;
-        const uint32_t sc = e4m3_to_f16x2_bcast(sb[u]);
-        uint32_t h[8];
-        decode8_scaled_f16(ww[u].x, sc, *reinterpret_cast<uint32_t(*)[4]>(&h[0]));
-        decode8_scaled_f16(ww[u].y, sc, *reinterpret_cast<uint32_t(*)[4]>(&h[4]));
-        store16<OutT>(out + 16 * g, h, fac, has_gs);
+        const int64_t v = base + vi + u * stride;
+        uint32_t h[4];
+        decode8_scaled_f16(wv[u], e4m3_to_f16x2_bcast(sb[u]), h);
+        store8<OutT>(out + 8 * v, h, fac, has_gs);
       }
     }
-    for (; gi < groups_per_expert; gi += stride) {
-      const int64_t g = base + gi;
-      const uint2 ww = ld_stream_v2(w + 2 * g);
-      const uint32_t sc = e4m3_to_f16x2_bcast(__ldcs(scales + g));
-      uint32_t h[8];
-      decode8_scaled_f16(ww.x, sc, *reinterpret_cast<uint32_t(*)[4]>(&h[0]));
-      decode8_scaled_f16(ww.y, sc, *reinterpret_cast<uint32_t(*)[4]>(&h[4]));
-      store16<OutT>(out + 16 * g, h, fac, has_gs);
+    for (; vi < words_per_expert; vi += stride) {
+      const int64_t v = base + vi;
+      uint32_t h[4];
+      decode8_scaled_f16(__ldcs(w + v), e4m3_to_f16x2_bcast(__ldcs(scales + (v >> 1))), h);
+      store8<OutT>(out + 8 * v, h, fac, has_gs);
     }
   }
 }
@@ -188,9 +179,9 @@ cudaError_t launch_transcode(const uint8_t* mo_w, int64_t w_bytes, const uint8_t
 
 cudaError_t launch_dequantize(const uint32_t* w, const uint8_t* scales, const float* gs, int64_t E,
                               int64_t N, int64_t K, int out_dtype, void* out, cudaStream_t st) {
-  const int64_t gpe = N * (K / 16);
+  const int64_t gpe = N * (K / 8);  // words per expert
   auto grid_of = [&](auto kern) {
-    int gx = stream_grid(kern, (gpe * E + 3) / 4);
+    int gx = stream_grid(kern, (gpe * E + 7) / 8);
     const int64_t per_expert = (gpe + kStreamThreads - 1) / kStreamThreads;
     if (gx > per_expert) gx = (int)(per_expert < 1 ? 1 : per_expert);
     const int gy = (int)(E < 65535 ? E : 65535);
