@@ -202,24 +202,42 @@ __device__ int stage_run(const QmvArgs& a, const SPlan& p, int chunk0, XRun run,
       if (p.x_is_bf16) {
         const uint32_t in[4] = {v[b].x, v[b].y, v[b].z, v[b].w};
         uint32_t h2[4];
+        // Fast path, integer only: a bf16 whose exponent field e lies in
+        // f16's normal range (113 <= e <= 142) is exactly the f16 with
+        // exponent e - 112 and the same seven fraction bits (padded with
+        // zeros), i.e. its magnitude bits minus 112 << 7, shifted left by 3.
+        // The range test adds 0x8000 - 0x3880 to each 15-bit magnitude (the
+        // 0x8000 keeps a borrow from crossing halves): inside the range the
+        // result is 0x8000..0x8EFF. Any other value (zero, f16 subnormal or
+        // beyond f16, NaN) takes the exact float path below.
+        bool fast = true;
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-          const float lo = __uint_as_float(in[q] << 16), hi = __uint_as_float(in[q] & 0xFFFF0000u);
-          const __half2 h = __floats2half2_rn(lo, hi);
-          const float2 back = __half22float2(h);
-          h2[q] = *reinterpret_cast<const uint32_t*>(&h);
+          const uint32_t m = in[q] & 0x7FFF7FFFu;
+          const uint32_t d = (m | 0x80008000u) - 0x38803880u;
+          fast &= (d & 0xF000F000u) == 0x80008000u && (((d & 0x0F000F00u) + 0x01000100u) & 0x10001000u) == 0u;
+          h2[q] = (in[q] & 0x80008000u) | ((m - 0x38003800u) << 3);
+        }
+        if (!fast) {
 #pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const float xv = e ? hi : lo, bv = e ? back.y : back.x;
-            if (bv != xv) {
-              if (!(fabsf(xv) <= 65504.f)) {  // beyond f16's range, or NaN
-                hard = 1;
-              } else {
-                const int i = atomicAdd(n_corr, 1);
-                if (i < kMaxCorr)
-                  corr[i] = Corr{u / per_slot, gcol + 2 * q + e, xv - bv};
-                else
+          for (int q = 0; q < 4; ++q) {
+            const float lo = __uint_as_float(in[q] << 16), hi = __uint_as_float(in[q] & 0xFFFF0000u);
+            const __half2 h = __floats2half2_rn(lo, hi);
+            const float2 back = __half22float2(h);
+            h2[q] = *reinterpret_cast<const uint32_t*>(&h);
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const float xv = e ? hi : lo, bv = e ? back.y : back.x;
+              if (bv != xv) {
+                if (!(fabsf(xv) <= 65504.f)) {  // beyond f16's range, or NaN
                   hard = 1;
+                } else {
+                  const int i = atomicAdd(n_corr, 1);
+                  if (i < kMaxCorr)
+                    corr[i] = Corr{u / per_slot, gcol + 2 * q + e, xv - bv};
+                  else
+                    hard = 1;
+                }
               }
             }
           }
