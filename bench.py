@@ -164,6 +164,21 @@ def decode_step_calls(nv, lin, xs, ys, copy_shift=0):
     return calls
 
 
+def reduce_step_time(torch, dist, dev, ms_total):
+    """The timed region's length for the whole job: the maximum over ranks
+    (replicas run independently; the job ends with its slowest rank)."""
+    if dist is None:
+        return ms_total
+    t = torch.tensor([ms_total], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(step_bytes, world, ms_step):
+    """Whole-job throughput in GB/s: every rank moves step_bytes per step."""
+    return step_bytes * world / (ms_step * 1e-3) / 1e9
+
+
 def run_ours(args):
     import torch
 
@@ -225,13 +240,9 @@ def run_ours(args):
             ev1.record(stream)
         torch.cuda.synchronize(dev)
     barrier()
-    ms_total = ev0.elapsed_time(ev1)
-    if dist is not None:
-        t = torch.tensor([ms_total], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_total = float(t.item())
+    ms_total = reduce_step_time(torch, dist, dev, ev0.elapsed_time(ev1))
     ms_step = ms_total / args.steps
-    value = step_bytes * world / (ms_step * 1e-3) / 1e9
+    value = job_value(step_bytes, world, ms_step)
 
     # Per-call latency (µs/call) per shape: ten calls (rotating weight copies)
     # captured in one CUDA graph, replayed, device time / 10.
