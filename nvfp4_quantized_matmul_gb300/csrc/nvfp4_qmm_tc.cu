@@ -90,9 +90,9 @@ struct TcParams {
   int E;        // experts
   int xcontig;  // gather: the activations of output row r are row r of the
                 // mapped x (x itself, or x gathered into output-row order)
-  // Dense work split: tiles [0, dp_tiles) are dealt whole, round robin; the
-  // k-block iterations of tiles [dp_tiles, dp_tiles + sk_tiles) are divided
-  // evenly over the CTAs (stream-K). A stream-K tile shared by several CTAs
+  // Stream-K launches (qmm_tc_sk_kernel): tiles [0, dp_tiles) are dealt
+  // whole, round robin; the k-block iterations of tiles [dp_tiles, dp_tiles +
+  // sk_tiles) are divided evenly over the CTAs. A tile shared by several CTAs
   // is summed in ws (BM x BN floats per tile, column-major so that a warp's
   // 32 rows of one column are 128 contiguous bytes; sk_tiles of them) and
   // finished by the CTA whose k-blocks complete ws_cnt[tile - dp_tiles]; both
@@ -315,26 +315,23 @@ struct WTask {
 };
 
 struct WCursor {
-  Sched sc;
-  Unit un;
-  int kb;
+  int tile, kb;
   bool done;
-  int e, nt;  // expert and weight tile of the current unit's tile
+  int e, nt;  // expert and weight tile of `tile`
 };
 
 template <bool GATHER, int BM>
-__device__ __forceinline__ void w_seek(WCursor& cur, const TcParams& p, const int* seg, const int* pre) {
-  cur.done = !cur.sc.next(cur.un);
+__device__ __forceinline__ void w_seek(WCursor& cur, const TcParams& p, int num_tiles, const int* seg, const int* pre) {
+  cur.done = cur.tile >= num_tiles;
   if (!cur.done) {
-    cur.kb = cur.un.kb0;
-    const Tile t = tile_of<GATHER, BM>(p, cur.un.tile, seg, pre);
+    const Tile t = tile_of<GATHER, BM>(p, cur.tile, seg, pre);
     cur.e = t.e;
     cur.nt = t.nt;
   }
 }
 
-template <int BN, int RPT>
-__device__ __forceinline__ void w_load(WTask<RPT>& t, const WCursor& cur, const TcParams& p, int r, int h) {
+template <int BN, int RPT, typename Cur>
+__device__ __forceinline__ void w_load(WTask<RPT>& t, const Cur& cur, const TcParams& p, int r, int h) {
   if (cur.done) return;
   const int64_t kwords = p.K / 8, kgroups = p.K / 16;
   const uint32_t* w = p.w + (int64_t)cur.e * p.N * kwords;
@@ -359,8 +356,13 @@ __device__ __forceinline__ void w_load(WTask<RPT>& t, const WCursor& cur, const 
 }
 
 template <bool GATHER, int BM>
-__device__ __forceinline__ void w_advance(WCursor& cur, const TcParams& p, const int* seg, const int* pre) {
-  if (!cur.done && ++cur.kb >= cur.un.kb1) w_seek<GATHER, BM>(cur, p, seg, pre);
+__device__ __forceinline__ void w_advance(WCursor& cur, const TcParams& p, int num_tiles, const int* seg,
+                                          const int* pre) {
+  if (++cur.kb >= p.num_kb) {
+    cur.kb = 0;
+    cur.tile += gridDim.x;
+    w_seek<GATHER, BM>(cur, p, num_tiles, seg, pre);
+  }
 }
 
 // Decode one row's four words (columns 32h..32h+31 of the k-block) and store
@@ -383,16 +385,14 @@ __device__ __forceinline__ void w_store_row(uint32_t stage_base, int row, int h,
 }
 
 template <typename T, typename C, bool GATHER>
-__device__ void producer_role(const TcParams& p, uint32_t sB, uint32_t bars, volatile int* abort_flag, Sched sched,
+__device__ void producer_role(const TcParams& p, uint32_t sB, uint32_t bars, volatile int* abort_flag, int num_tiles,
                               const int* seg, const int* pre) {
   constexpr int STAGES = C::STAGES, RPT = C::RPT, BM = C::BM;
   const int pid = threadIdx.x - C::kWarpProd0 * 32;  // 0..255
   const int r = pid >> 1, h = pid & 1;               // rows r + 128 i, words 4h..4h+3 of the k-block
   const int lane = threadIdx.x & 31;
-  WCursor ld;
-  ld.sc = sched;
-  const int64_t total = sched.total();
-  w_seek<GATHER, BM>(ld, p, seg, pre);
+  WCursor ld{(int)blockIdx.x, 0, true, 0, 0};
+  w_seek<GATHER, BM>(ld, p, num_tiles, seg, pre);
   // PF k-blocks of packed weights in flight per thread (registers), so that
   // the L2 latency of the loads is covered by PF - 1 blocks of decoding.
   constexpr int PF = C::PF;
@@ -400,7 +400,85 @@ __device__ void producer_role(const TcParams& p, uint32_t sB, uint32_t bars, vol
 #pragma unroll
   for (int j = 0; j < PF - 1; ++j) {
     w_load<C::BN>(buf[j], ld, p, r, h);
-    w_advance<GATHER, BM>(ld, p, seg, pre);
+    w_advance<GATHER, BM>(ld, p, num_tiles, seg, pre);
+  }
+  uint32_t u = 0;
+  const int total = ((num_tiles - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x) * p.num_kb;
+  auto consume = [&](const WTask<RPT>& t) -> bool {
+    const int s = (int)(u % STAGES);
+    const uint32_t ph = (u / STAGES) & 1;
+    if (!wait_bar_warp(bars + 8 * (2 * STAGES + s), ph ^ 1, abort_flag, 3, &g_tc_error)) return false;  // stage empty
+    const uint32_t stage = sB + (uint32_t)s * C::B_BYTES;
+#pragma unroll
+    for (int i = 0; i < RPT; ++i) w_store_row<T>(stage, r + 128 * i, h, t.w[i], t.s[i]);
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bars + 8 * (STAGES + s));  // fullB
+    ++u;
+    return true;
+  };
+  // the ring of buffers is indexed by compile-time positions only (unrolled),
+  // so it stays in registers
+  for (int i = 0; i < total; i += PF) {
+#pragma unroll
+    for (int j = 0; j < PF; ++j) {
+      if (i + j >= total) return;
+      w_load<C::BN>(buf[(j + PF - 1) % PF], ld, p, r, h);
+      w_advance<GATHER, BM>(ld, p, num_tiles, seg, pre);
+      if (!consume(buf[j])) return;
+    }
+  }
+}
+
+// ---------------------------------------------------------------- stream-K variants
+//
+// The stream-K kernel walks units (tile, k-block range) instead of whole
+// tiles; its roles are kept apart from the whole-tile kernel's so that the
+// latter compiles exactly as before (sharing them cost it 6% at M = 8192).
+
+struct WCursorSK {
+  Sched sc;
+  Unit un;
+  int kb;
+  bool done;
+  int e, nt;  // expert and weight tile of the current unit's tile
+};
+
+template <bool GATHER, int BM>
+__device__ __forceinline__ void w_seek_sk(WCursorSK& cur, const TcParams& p, const int* seg, const int* pre) {
+  cur.done = !cur.sc.next(cur.un);
+  if (!cur.done) {
+    cur.kb = cur.un.kb0;
+    const Tile t = tile_of<GATHER, BM>(p, cur.un.tile, seg, pre);
+    cur.e = t.e;
+    cur.nt = t.nt;
+  }
+}
+
+template <bool GATHER, int BM>
+__device__ __forceinline__ void w_advance_sk(WCursorSK& cur, const TcParams& p, const int* seg, const int* pre) {
+  if (!cur.done && ++cur.kb >= cur.un.kb1) w_seek_sk<GATHER, BM>(cur, p, seg, pre);
+}
+
+template <typename T, typename C, bool GATHER>
+__device__ void producer_role_sk(const TcParams& p, uint32_t sB, uint32_t bars, volatile int* abort_flag, Sched sched,
+                              const int* seg, const int* pre) {
+  constexpr int STAGES = C::STAGES, RPT = C::RPT, BM = C::BM;
+  const int pid = threadIdx.x - C::kWarpProd0 * 32;  // 0..255
+  const int r = pid >> 1, h = pid & 1;               // rows r + 128 i, words 4h..4h+3 of the k-block
+  const int lane = threadIdx.x & 31;
+  WCursorSK ld;
+  ld.sc = sched;
+  const int64_t total = sched.total();
+  w_seek_sk<GATHER, BM>(ld, p, seg, pre);
+  // PF k-blocks of packed weights in flight per thread (registers), so that
+  // the L2 latency of the loads is covered by PF - 1 blocks of decoding.
+  constexpr int PF = C::PF;
+  WTask<RPT> buf[PF];
+#pragma unroll
+  for (int j = 0; j < PF - 1; ++j) {
+    w_load<C::BN>(buf[j], ld, p, r, h);
+    w_advance_sk<GATHER, BM>(ld, p, seg, pre);
   }
   uint32_t u = 0;
   auto consume = [&](const WTask<RPT>& t) -> bool {
@@ -423,7 +501,7 @@ __device__ void producer_role(const TcParams& p, uint32_t sB, uint32_t bars, vol
     for (int j = 0; j < PF; ++j) {
       if (i + j >= total) return;
       w_load<C::BN>(buf[(j + PF - 1) % PF], ld, p, r, h);
-      w_advance<GATHER, BM>(ld, p, seg, pre);
+      w_advance_sk<GATHER, BM>(ld, p, seg, pre);
       if (!consume(buf[j])) return;
     }
   }
@@ -509,6 +587,264 @@ __device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* map
 template <typename T, typename C, bool GATHER>
 __global__ void __launch_bounds__(C::THREADS, 1)
 qmm_tc_kernel(const __grid_constant__ CUtensorMap xmap, const TcParams p) {
+  constexpr int STAGES = C::STAGES, MH = C::MH, BN = C::BN, BM = C::BM, NBUF = C::ACC_BUFS;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* base_ptr = smem_raw + (base - raw);
+  const uint32_t sA = base, sB = base + STAGES * C::A_BYTES;
+  const uint32_t bars = sB + STAGES * C::B_BYTES;
+  // barriers: fullA[S] fullB[S] empty[S] accFull[NBUF] accEmpty[NBUF]
+  uint32_t* holder =
+      reinterpret_cast<uint32_t*>(base_ptr + STAGES * (C::A_BYTES + C::B_BYTES) + 8 * (3 * STAGES + 2 * NBUF));
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(holder + 1);
+  // gather tables follow the barrier block (16-byte aligned)
+  uint32_t* samp = reinterpret_cast<uint32_t*>(base_ptr + C::SMEM - 1024);
+  int* seg = reinterpret_cast<int*>(samp + kGatherSamples);
+  int* pre = seg + (kGatherMaxE + 1);
+  auto fullA = [&](int s) { return bars + 8 * s; };
+  auto fullB = [&](int s) { return bars + 8 * (STAGES + s); };
+  auto emptyB = [&](int s) { return bars + 8 * (2 * STAGES + s); };
+  auto accFull = [&](int b) { return bars + 8 * (3 * STAGES + b); };
+  auto accEmpty = [&](int b) { return bars + 8 * (3 * STAGES + NBUF + b); };
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(fullA(s), 1);
+      mbar_init(fullB(s), kProducerWarps);
+      mbar_init(emptyB(s), 1);
+    }
+    for (int b = 0; b < NBUF; ++b) {
+      mbar_init(accFull(b), 1);
+      mbar_init(accEmpty(b), C::EPI_WARPS);
+    }
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == kWarpTma && lane == 0)
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&xmap)) : "memory");
+  if (warp == kWarpAlloc) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(holder)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  if (GATHER) build_gather_tables<BM>(p, samp, seg, pre);  // ends with __syncthreads
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *holder;
+  const int num_tiles = GATHER ? pre[p.E] : p.num_tiles;
+  const int my_tiles = (int)blockIdx.x < num_tiles
+                           ? (num_tiles - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x
+                           : 0;
+
+  if (warp == kWarpTma) {
+    uint32_t u = 0;
+    if (!GATHER) {
+      if (lane == 0) {
+        bool ok = true;
+        for (int i = 0; i < my_tiles && ok; ++i) {
+          const int tile = (int)blockIdx.x + i * (int)gridDim.x;
+          const int m_tile = tile % p.num_m_tiles;
+          for (int kb = 0; kb < p.num_kb; ++kb, ++u) {
+            const int s = (int)(u % STAGES);
+            const uint32_t ph = (u / STAGES) & 1;
+            if (!wait_bar(emptyB(s), ph ^ 1, abort_flag, 1)) { ok = false; break; }
+            mbar_arrive_tx(fullA(s), C::A_BYTES);
+#pragma unroll
+            for (int h = 0; h < MH; ++h)
+              tma_load_2d(sA + (uint32_t)s * C::A_BYTES + (uint32_t)h * kHalfA, &xmap, kb * BK, m_tile * BM + 128 * h,
+                          fullA(s));
+          }
+        }
+      }
+    } else if (p.xcontig) {
+      // The tile's activations are rows m0 .. m0 + rows - 1 of the mapped x:
+      // one 128-row box per M half that holds rows of the tile (rows past
+      // them belong to the next expert or lie beyond x; they are computed but
+      // not stored).
+      bool ok = true;
+      for (int i = 0; i < my_tiles && ok; ++i) {
+        const Tile tl = tile_of<true, BM>(p, (int)blockIdx.x + i * (int)gridDim.x, seg, pre);
+        const int mh = (tl.rows + 127) / 128;
+        for (int kb = 0; kb < p.num_kb; ++kb, ++u) {
+          const int s = (int)(u % STAGES);
+          const uint32_t ph = (u / STAGES) & 1;
+          if (!wait_bar_warp(emptyB(s), ph ^ 1, abort_flag, 1, &g_tc_error)) { ok = false; break; }
+          if (lane == 0) {
+            mbar_arrive_tx(fullA(s), (uint32_t)mh * kHalfA);
+#pragma unroll
+            for (int h = 0; h < MH; ++h)
+              if (h < mh)
+                tma_load_2d(sA + (uint32_t)s * C::A_BYTES + (uint32_t)h * kHalfA, &xmap, kb * BK,
+                            (int)(tl.m0 + 128 * h), fullA(s));
+          }
+          __syncwarp();
+        }
+      }
+    } else {
+      // Each lane fetches four activation rows of every 128-row half that
+      // holds rows of the tile with one tile::gather4 copy per k-block; rows
+      // past the tile's end or with an out-of-range activation index read row
+      // 0 (their outputs are not taken from the accumulator).
+      bool ok = true;
+      for (int i = 0; i < my_tiles && ok; ++i) {
+        const Tile tl = tile_of<true, BM>(p, (int)blockIdx.x + i * (int)gridDim.x, seg, pre);
+        const int mh = (tl.rows + 127) / 128;
+        int xr[MH][4];
+#pragma unroll
+        for (int h = 0; h < MH; ++h)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int rr = 128 * h + 4 * lane + j;
+            int64_t v = 0;
+            if (rr < tl.rows) {
+              const int64_t r = tl.m0 + rr;
+              v = p.lhs ? (int64_t)__ldg(p.lhs + r) : r;
+              if (v >= p.B) v = 0;
+            }
+            xr[h][j] = (int)v;
+          }
+        for (int kb = 0; kb < p.num_kb; ++kb, ++u) {
+          const int s = (int)(u % STAGES);
+          const uint32_t ph = (u / STAGES) & 1;
+          if (!wait_bar_warp(emptyB(s), ph ^ 1, abort_flag, 1, &g_tc_error)) { ok = false; break; }
+          if (lane == 0) mbar_arrive_tx(fullA(s), (uint32_t)mh * kHalfA);
+          __syncwarp();
+#pragma unroll
+          for (int h = 0; h < MH; ++h)
+            if (h < mh)
+              tma_gather4(sA + (uint32_t)s * C::A_BYTES + (uint32_t)h * kHalfA + 512u * (uint32_t)lane, &xmap,
+                          kb * BK, xr[h][0], xr[h][1], xr[h][2], xr[h][3], fullA(s));
+        }
+      }
+    }
+    // Leave no copy in flight: wait (bounded) for the last stages issued.
+    if (lane == 0) {
+      const uint32_t first = u > (uint32_t)STAGES ? u - STAGES : 0;
+      for (uint32_t v = first; v < u; ++v) {
+        const uint32_t limit_ph = (v / STAGES) & 1;
+        const uint64_t t0 = gtimer();
+        while (!mbar_try(fullA((int)(v % STAGES)), limit_ph) && gtimer() - t0 < kWaitLimitNs) {
+        }
+      }
+    }
+  } else if (warp == kWarpMma) {
+    if (lane == 0) {
+      constexpr uint32_t idesc = make_idesc<std::is_same<T, __nv_bfloat16>::value, BN>();
+      uint32_t u = 0;
+      bool ok = true;
+      for (int i = 0; i < my_tiles && ok; ++i) {
+        const int b = i % NBUF;
+        int mh = MH;  // M halves holding rows of the tile (a gather tile may fill one)
+        if (GATHER) mh = (tile_of<true, BM>(p, (int)blockIdx.x + i * (int)gridDim.x, seg, pre).rows + 127) / 128;
+        if (!wait_bar(accEmpty(b), ((i / NBUF) & 1) ^ 1, abort_flag, 4)) break;
+        tc_fence_after();
+        const uint32_t d = tmem + (uint32_t)(b * MH * BN);
+        for (int kb = 0; kb < p.num_kb; ++kb, ++u) {
+          const int s = (int)(u % STAGES);
+          const uint32_t ph = (u / STAGES) & 1;
+          if (!wait_bar(fullA(s), ph, abort_flag, 5) || !wait_bar(fullB(s), ph, abort_flag, 6)) { ok = false; break; }
+          tc_fence_after();
+          const uint64_t bd = sw128_desc(sB + (uint32_t)s * C::B_BYTES);
+#pragma unroll
+          for (int j = 0; j < BK / 16; ++j)
+#pragma unroll
+            for (int h = 0; h < MH; ++h) {
+              if (h >= mh) continue;
+              const uint64_t ad = sw128_desc(sA + (uint32_t)s * C::A_BYTES + (uint32_t)h * kHalfA);
+              umma_f16(d + (uint32_t)(h * BN), ad + (uint64_t)(2 * j), bd + (uint64_t)(2 * j), idesc, (kb | j) != 0);
+            }
+          umma_commit(emptyB(s));
+        }
+        if (ok) umma_commit(accFull(b));
+      }
+    }
+  } else if (warp >= kWarpEpi0 && warp < kWarpEpi0 + C::EPI_WARPS) {
+    const int q = warp & 3;                  // TMEM lane quarter this warp may read
+    const int hm = (warp - kWarpEpi0) >> 2;  // M half it drains
+    T* y = static_cast<T*>(p.y);
+    if (GATHER) {
+      // rows whose expert index is out of range (sorted last) are exact +0
+      const int64_t z0 = seg[p.E];
+      const int64_t total = (p.M - z0) * p.N;
+      const int ethreads = 32 * C::EPI_WARPS, etid = threadIdx.x - 32 * kWarpEpi0;
+      uint16_t* yz = reinterpret_cast<uint16_t*>(y) + z0 * p.N;
+      for (int64_t i = (int64_t)blockIdx.x * ethreads + etid; i < total; i += (int64_t)gridDim.x * ethreads) yz[i] = 0;
+    }
+    for (int i = 0; i < my_tiles; ++i) {
+      const Tile tl = tile_of<GATHER, BM>(p, (int)blockIdx.x + i * (int)gridDim.x, seg, pre);
+      const int b = i % NBUF;
+      if (!wait_bar_warp(accFull(b), (i / NBUF) & 1, abort_flag, 7, &g_tc_error)) break;
+      tc_fence_after();
+      const int rr = 128 * hm + 32 * q + lane;  // row within the tile
+      const int64_t m = tl.m0 + rr;
+      const bool live = rr < tl.rows;
+      bool zero = false;
+      if (GATHER && live) {
+        const int64_t xr = p.lhs ? (int64_t)__ldg(p.lhs + m) : m;
+        zero = xr >= p.B;
+      }
+      const float fac = global_factor(p.gs, tl.e);
+      const int64_t n_base = (int64_t)tl.nt * BN;
+      const uint32_t tcol = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(b * MH * BN + hm * BN);
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld32(tcol + (uint32_t)(32 * c), r);
+        tmem_ld_wait();
+        if (!live) continue;
+        const int64_t n0 = n_base + 32 * c;
+        if (n0 >= p.N) continue;
+        uint32_t packed[16];
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+          float v0 = __uint_as_float(r[2 * k]), v1 = __uint_as_float(r[2 * k + 1]);
+          if (p.gs) {
+            v0 = __fmul_rn(v0, fac);
+            v1 = __fmul_rn(v1, fac);
+          }
+          const T t0 = Dt<T>::from_f32(v0), t1 = Dt<T>::from_f32(v1);
+          packed[k] = zero ? 0u
+                           : (uint32_t)(*reinterpret_cast<const uint16_t*>(&t0)) |
+                                 ((uint32_t)(*reinterpret_cast<const uint16_t*>(&t1)) << 16);
+        }
+        T* dst = y + m * p.N + n0;
+        if (n0 + 32 <= p.N && (p.N % 8) == 0) {
+          uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            d4[k] = make_uint4(packed[4 * k], packed[4 * k + 1], packed[4 * k + 2], packed[4 * k + 3]);
+        } else {
+          uint16_t* d16 = reinterpret_cast<uint16_t*>(dst);
+          for (int k = 0; k < 32 && n0 + k < p.N; ++k)
+            d16[k] = (uint16_t)(packed[k >> 1] >> (16 * (k & 1)));
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(accEmpty(b));
+    }
+  } else if (warp >= C::kWarpProd0) {
+    producer_role<T, C, GATHER>(p, sB, bars, abort_flag, num_tiles, seg, pre);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kWarpAlloc) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
+  }
+}
+
+// The stream-K kernel (dense launches of fewer than two waves of tiles): the
+// same roles as qmm_tc_kernel, walking units (tile, k-block range), with the
+// split-tile epilogue. Instantiated with GATHER = false and SK = true only.
+template <typename T, typename C, bool GATHER, bool SK>
+__global__ void __launch_bounds__(C::THREADS, 1)
+qmm_tc_sk_kernel(const __grid_constant__ CUtensorMap xmap, const TcParams p) {
   constexpr int STAGES = C::STAGES, MH = C::MH, BN = C::BN, BM = C::BM, NBUF = C::ACC_BUFS;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -750,7 +1086,7 @@ qmm_tc_kernel(const __grid_constant__ CUtensorMap xmap, const TcParams p) {
       const float fac = global_factor(p.gs, tl.e);
       const int64_t n_base = (int64_t)tl.nt * BN;
       const uint32_t tcol = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(b * MH * BN + hm * BN);
-      if (!GATHER && (un.kb0 != 0 || un.kb1 != p.num_kb)) {
+      if (SK && (un.kb0 != 0 || un.kb1 != p.num_kb)) {
         // A piece of a stream-K tile: add it to the tile's sums, count its
         // k-blocks; the piece that completes the count finishes the tile.
         const int slot = un.tile - p.dp_tiles;
@@ -810,7 +1146,7 @@ qmm_tc_kernel(const __grid_constant__ CUtensorMap xmap, const TcParams p) {
       if (lane == 0) mbar_arrive(accEmpty(b));
     }
   } else if (warp >= C::kWarpProd0) {
-    producer_role<T, C, GATHER>(p, sB, bars, abort_flag, sched, seg, pre);
+    producer_role_sk<T, C, GATHER>(p, sB, bars, abort_flag, sched, seg, pre);
   }
 
   tc_fence_before();
@@ -927,16 +1263,18 @@ cudaError_t launch_cfg(const void* x, int64_t M, int64_t K, const uint32_t* w, c
   p.B = M;
   p.E = 1;
   p.xcontig = 1;
-  // Whole waves of tiles are dealt round robin. The tiles that would make up
-  // the last, partial wave (with one full wave before them, so that every
-  // CTA's share is at least a tile) are split evenly by k-blocks instead.
+  // Tiles are dealt whole, round robin, unless they make fewer than two
+  // waves: then the partial wave would idle a large share of the SMs, and
+  // all tiles are split evenly by k-blocks instead (stream-K). From two
+  // waves on, splitting only the last wave cost more than it saved (M = 2048
+  // on [21504, 5376], 4.4 waves: 365 us whole-tile, 371 us split).
   const int T_ = p.num_tiles;
   int grid = T_ < sms ? T_ : sms;
   p.dp_tiles = T_;
   p.sk_tiles = 0;
-  if (stream_k_on() && T_ % sms != 0) {
+  if (stream_k_on() && T_ % sms != 0 && T_ < 2 * sms) {
     if (T_ > sms) {
-      p.dp_tiles = (T_ / sms - 1) * sms;
+      p.dp_tiles = 0;
       grid = sms;
     } else {
       p.dp_tiles = 0;
@@ -956,7 +1294,7 @@ cudaError_t launch_cfg(const void* x, int64_t M, int64_t K, const uint32_t* w, c
     p.ws = ws.acc;
     p.ws_cnt = ws.cnt;
   }
-  auto kern = qmm_tc_kernel<T, C, false>;
+  auto kern = p.sk_tiles > 0 ? qmm_tc_sk_kernel<T, C, false, true> : qmm_tc_kernel<T, C, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
   if (e != cudaSuccess) return e;
   kern<<<grid, C::THREADS, C::SMEM, st>>>(map, p);
@@ -967,15 +1305,16 @@ using Tile256x256 = Cfg<2, 256>;
 using Tile256x128 = Cfg<2, 128>;
 using Tile128x256 = Cfg<1, 256>;
 
-// Tile shape. With the stream-K split there are no partial waves to avoid,
-// and 256x256 tiles, whose decoded weight tile feeds twice the MMA work, were
-// the fastest or within 4% of it on every prefill shape measured on GB300
-// (M = 64 .. 8192, K = 5376 and 21504). Without it (NVFP4_TC_STREAMK=0) the
-// shape is picked by modelled time: whole waves of persistent tiles, each
-// tile's cost its area over the shape's relative throughput (measured with
-// full waves at M = 8192, [21504, 5376]: 256x128 tiles run at 0.81 of
-// 256x256, 128x256 tiles at 0.54). The environment variable NVFP4_TC_TILE
-// ("256x256", "256x128" or "128x256") overrides either choice.
+// Tile shape. Below two waves of 256x256 tiles the stream-K split leaves no
+// partial wave to avoid, and 256x256 tiles, whose decoded weight tile feeds
+// twice the MMA work, were the fastest or within 4% of it on every such shape
+// measured on GB300 (M = 64 .. 512 at K = 5376, M = 2048 at K = 21504).
+// Otherwise (or with NVFP4_TC_STREAMK=0) the shape is picked by modelled
+// time: whole waves of persistent tiles, each tile's cost its area over the
+// shape's relative throughput (measured with full waves at M = 8192,
+// [21504, 5376]: 256x128 tiles run at 0.81 of 256x256, 128x256 tiles at
+// 0.54). The environment variable NVFP4_TC_TILE ("256x256", "256x128" or
+// "128x256") overrides either choice.
 int pick_tile(int64_t M, int64_t N, int sms) {
   const char* forced = std::getenv("NVFP4_TC_TILE");
   if (forced) {
@@ -983,7 +1322,8 @@ int pick_tile(int64_t M, int64_t N, int sms) {
     if (!std::strcmp(forced, "256x128")) return 1;
     if (!std::strcmp(forced, "128x256")) return 2;
   }
-  if (stream_k_on()) return 0;
+  // fewer than two waves of 256x256 tiles: the stream-K split applies
+  if (stream_k_on() && ((M + 255) / 256) * ((N + 255) / 256) < 2 * sms) return 0;
   const int bm[3] = {256, 256, 128}, bn[3] = {256, 128, 256};
   const double rate[3] = {1.0, 0.81, 0.54};
   int best = 0;
@@ -1129,10 +1469,6 @@ cudaError_t launch_gather(const void* x, int64_t B, int64_t K, const uint32_t* l
   p.B = B;
   p.E = (int)E;
   p.xcontig = per_row ? 0 : 1;
-  p.dp_tiles = 0;  // set on the device from the segment table
-  p.sk_tiles = 0;
-  p.ws = nullptr;
-  p.ws_cnt = nullptr;
   const size_t smem = C::SMEM + kGatherSmem;
   auto kern = qmm_tc_kernel<T, C, true>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

@@ -443,6 +443,34 @@ def test_gather_sorted_tc_matches_decode_route(nv, monkeypatch):
     assert (a - b).abs().max().item() <= 2 * 2.0**-8 * b.abs().max().item()
 
 
+@pytest.mark.parametrize("rows", ["gathered", "tma"])
+def test_gather_sorted_tc_two_calls(nv, monkeypatch, rows):
+    """About 160 expert tiles of 16 k-blocks on 152 CTAs (a second, partial
+    wave), an activation index out of range inside a segment; every row
+    against the oracle, twice in a row (the row buffer is reused)."""
+    monkeypatch.setenv("NVFP4_GATHER_TC", "1")
+    monkeypatch.setenv("NVFP4_GATHER_ROWS", rows)
+    E, N, K, T, topk = 16, 1024, 1024, 2048, 4
+    w, s = weights(61, E, N, K)
+    g = synth.rng(62)
+    gs = synth.global_scales(g, E)
+    x = synth.activations(g, (T, K), "bf16")
+    lhs, rhs = synth.zipf_routing(g, T, E, topk)
+    lhs = lhs.copy()
+    lhs[5] = T  # an activation row out of range inside a segment
+    ref = O.gather_qmm(x.double().numpy(), lhs, rhs, w, s, gs)
+    args = (x.cuda(), u32_to_dev(w), u8_to_dev(s), u32_to_dev(rhs), u32_to_dev(lhs))
+    for rep in range(2):
+        y, backing, guard = guarded_empty((len(rhs), N), torch.bfloat16, fill=-7.0)
+        nv.gather_qmm(*args, gs=f32_to_dev(gs), sorted_indices=True, out=y)
+        torch.cuda.synchronize()
+        assert nv.take_device_error() == 0
+        assert rel_err(y, ref) <= TOL["bf16"], f"call {rep}"
+        assert guards_intact(backing, guard)
+        yc = y[5].float().cpu().numpy()
+        assert np.all(yc == 0.0) and not np.any(np.signbit(yc))
+
+
 def test_gather_sorted_tc_moe_prefill_full_size(nv):
     """The MoE gate/up prefill: 4096 tokens, top-8 Zipf(1.1) routing over 128
     experts, rows sorted by expert; sampled rows against the oracle."""

@@ -1,13 +1,13 @@
 """GPU parity of the tensor-core prefill route's stream-K work split.
 
-Whole waves of output tiles are dealt to the persistent CTAs one tile each;
-the tiles of the last, partial wave (with one full wave before them) are cut
-by k-blocks and spread over every CTA. A tile cut between CTAs is summed in a
-per-stream f32 workspace with vector atomics, and the CTA whose k-blocks
-complete it writes the outputs and clears its workspace block. The cases
-below make every tile split (fewer tiles than SMs), mix whole tiles with split
-ones, use ragged M and N, call twice in a row (the workspace must come back
-clean), replay a CUDA graph, agree with the plain round-robin split, and cover
+Output tiles are dealt whole to the persistent CTAs, one tile each, unless
+they make fewer than two waves: then every tile's k-blocks are spread evenly
+over all CTAs. A tile cut between CTAs is summed in a per-stream f32
+workspace with atomics, and the CTA whose k-blocks complete it writes the
+outputs and clears its workspace block. The cases below split every tile
+(fewer tiles than SMs, and between one and two waves), use ragged M and N,
+deal more than two waves whole, call twice in a row (the workspace must come
+back clean), replay a CUDA graph, agree with whole-tile scheduling, and cover
 the prefill shapes at full size on sampled outputs.
 """
 import numpy as np
@@ -38,7 +38,7 @@ def nv():
 #   (512, 2048, 2048)   16 tiles x 32 k-blocks: every tile split four ways
 #   (300, 1000, 1536)   8 ragged tiles, each split three ways
 #   (2048, 5376, 2048)  168 tiles: all stream-K, 1.1 tiles per CTA
-#   (4096, 8192, 512)   512 tiles: 304 whole, 208 stream-K
+#   (4096, 8192, 512)   512 tiles: more than two waves, dealt whole
 SK_SHAPES = [(512, 2048, 2048), (300, 1000, 1536), (2048, 5376, 2048), (4096, 8192, 512)]
 
 
