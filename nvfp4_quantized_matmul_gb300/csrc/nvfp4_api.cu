@@ -144,9 +144,10 @@ const char* nvfp4_version(void) { return "nvfp4-gb300 0.1 (sm_103a)"; }
 int nvfp4_set_launch_overlap(int enable) { return nvfp4::g_launch_overlap.exchange(enable ? 1 : 0); }
 
 int32_t nvfp4_take_device_error(void) {
-  const int a = nvfp4::read_tc_error(), b = nvfp4::read_qmv_error(), c = nvfp4::read_stream_error();
-  if (a < 0 || b < 0 || c < 0) return -1;
-  return a ? a : b ? b : c;
+  const int a = nvfp4::read_tc_error(), b = nvfp4::read_qmv_error(), c = nvfp4::read_stream_error(),
+            d = nvfp4::read_copy_error();
+  if (a < 0 || b < 0 || c < 0 || d < 0) return -1;
+  return a ? a : b ? b : c ? c : d;
 }
 
 void nvfp4_shutdown(void) {

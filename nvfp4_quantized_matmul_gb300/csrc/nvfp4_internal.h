@@ -14,6 +14,8 @@ cudaError_t launch_transcode(const uint8_t* mo_w, int64_t w_bytes, const uint8_t
 
 cudaError_t launch_dequantize(const uint32_t* w, const uint8_t* scales, const float* gs, int64_t E,
                               int64_t N, int64_t K, int out_dtype, void* out, cudaStream_t st);
+// Reads and clears the error code of the bulk-copy transcode's bounded waits.
+int read_copy_error();
 
 // Decode-shape product on the SIMT/mma.sync path. Row r of the output uses
 // activation row lhs[r] (r when lhs is null) and expert rhs[r] (0 when rhs is

@@ -1,8 +1,14 @@
 // Bandwidth-bound kernels: ModelOpt-triplet transcode and exact dequantize.
+#include <cstdlib>
+
 #include "nvfp4_common.cuh"
 #include "nvfp4_internal.h"
+#include "nvfp4_pipe.cuh"
 
 namespace nvfp4 {
+
+__device__ int g_copy_error = 0;  // first error code recorded by a bounded wait of the bulk copy
+
 namespace {
 
 constexpr int kStreamThreads = 256;
@@ -59,6 +65,99 @@ transcode_kernel(const uint8_t* __restrict__ mo_w, int64_t w_bytes, const uint8_
   const int64_t wt = w_bytes - (wv << 4), st = s_bytes - (sv << 4);
   if (tid < wt) w_out[(wv << 4) + tid] = mo_w[(wv << 4) + tid];
   if (tid < st) s_out[(sv << 4) + tid] = mo_ws[(sv << 4) + tid];
+}
+
+// The same transcode moved by the copy engine: each CTA (one per SM, one
+// thread issuing) copies a contiguous run of 32 KB chunks of both planes
+// through a ring of six shared-memory buffers, bulk loads running up to six
+// chunks ahead of the bulk stores. The copy engine then keeps the read and
+// write streams going with a handful of instructions per 32 KB instead of
+// one load and one store per 16 bytes and thread. Sizes and addresses of
+// bulk copies must be multiples of 16 bytes: the last (< 16) bytes of each
+// plane are copied by plain stores.
+constexpr uint32_t kCopyChunk = 32 * 1024;
+constexpr int kCopyBufs = 6;
+
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(bar)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_s2g(void* dst, uint32_t src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(src), "r"(bytes)
+               : "memory");
+}
+
+__global__ void __launch_bounds__(32, 1)
+transcode_bulk_kernel(const uint8_t* __restrict__ mo_w, int64_t w_bytes, const uint8_t* __restrict__ mo_ws,
+                      int64_t s_bytes, const float* __restrict__ ws2, uint8_t* __restrict__ w_out,
+                      uint8_t* __restrict__ s_out, float* __restrict__ gs_out) {
+  extern __shared__ __align__(128) uint8_t buf[];
+  __shared__ __align__(8) uint64_t bars[kCopyBufs];
+  __shared__ int abort_flag;
+  const int64_t wv = w_bytes & ~(int64_t)15, sv = s_bytes & ~(int64_t)15;
+  const int64_t n0 = (wv + kCopyChunk - 1) / kCopyChunk, n = n0 + (sv + kCopyChunk - 1) / kCopyChunk;
+  if (blockIdx.x == 0) {
+    if (threadIdx.x == 0) gs_out[0] = __fmul_rn(__ldg(ws2), kGlobalScaleDivisor);
+    if (threadIdx.x < w_bytes - wv) w_out[wv + threadIdx.x] = mo_w[wv + threadIdx.x];
+    if (threadIdx.x < s_bytes - sv) s_out[sv + threadIdx.x] = mo_ws[sv + threadIdx.x];
+  }
+  if (threadIdx.x != 0) return;
+  // chunk c: source, destination and size
+  auto chunk = [&](int64_t c, const uint8_t*& src, uint8_t*& dst, uint32_t& bytes) {
+    if (c < n0) {
+      const int64_t off = c * kCopyChunk;
+      src = mo_w + off;
+      dst = w_out + off;
+      bytes = (uint32_t)(wv - off < kCopyChunk ? wv - off : kCopyChunk);
+    } else {
+      const int64_t off = (c - n0) * kCopyChunk;
+      src = mo_ws + off;
+      dst = s_out + off;
+      bytes = (uint32_t)(sv - off < kCopyChunk ? sv - off : kCopyChunk);
+    }
+  };
+  const int64_t c0 = n * blockIdx.x / gridDim.x, c1 = n * (blockIdx.x + 1) / gridDim.x;
+  const uint32_t sbuf = pipe::smem_addr(buf), sbar = pipe::smem_addr(bars);
+  abort_flag = 0;
+  for (int k = 0; k < kCopyBufs; ++k) pipe::mbar_init(sbar + 8u * k, 1);
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  int64_t issued = c0;  // next chunk to load
+  for (; issued < c1 && issued < c0 + kCopyBufs; ++issued) {
+    const uint8_t* src;
+    uint8_t* dst;
+    uint32_t bytes;
+    chunk(issued, src, dst, bytes);
+    const int k = (int)(issued - c0);
+    pipe::mbar_arrive_tx(sbar + 8u * k, bytes);
+    bulk_g2s(sbuf + (uint32_t)k * kCopyChunk, src, bytes, sbar + 8u * k);
+  }
+  int64_t i = c0;
+  for (; i < c1; ++i) {
+    const int k = (int)((i - c0) % kCopyBufs);
+    const uint32_t ph = (uint32_t)(((i - c0) / kCopyBufs) & 1);
+    if (!pipe::wait_bar(sbar + 8u * k, ph, &abort_flag, 41, &g_copy_error)) break;
+    const uint8_t* src;
+    uint8_t* dst;
+    uint32_t bytes;
+    chunk(i, src, dst, bytes);
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    bulk_s2g(dst, sbuf + (uint32_t)k * kCopyChunk, bytes);
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+    if (issued < c1) {
+      // buffer k is reloaded once the store just issued has read it
+      asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+      chunk(issued, src, dst, bytes);
+      pipe::mbar_arrive_tx(sbar + 8u * k, bytes);
+      bulk_g2s(sbuf + (uint32_t)k * kCopyChunk, src, bytes, sbar + 8u * k);
+      ++issued;
+    }
+  }
+  // No load may still be in flight into shared memory when the CTA exits
+  // (only after a wait gave up), and the stores must have completed.
+  for (int64_t v = i; v < issued; ++v)
+    pipe::wait_bar_quiet(sbar + 8u * (uint32_t)((v - c0) % kCopyBufs), (uint32_t)(((v - c0) / kCopyBufs) & 1));
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
 // Exact dequantize (PR #2629 "ROCm native NVFP4", Summary: the dequantize
@@ -171,10 +270,30 @@ dequantize_kernel(const uint32_t* __restrict__ w, const uint8_t* __restrict__ sc
 cudaError_t launch_transcode(const uint8_t* mo_w, int64_t w_bytes, const uint8_t* mo_ws, int64_t s_bytes,
                              const float* ws2, uint32_t* w_out, uint8_t* s_out, float* gs_out,
                              cudaStream_t st) {
+  const char* ev = std::getenv("NVFP4_TRANSCODE_BULK");
+  if (!(ev && ev[0] == '0')) {
+    int dev = 0, sms = 152;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const size_t smem = (size_t)kCopyBufs * kCopyChunk;
+    cudaError_t e = cudaFuncSetAttribute(transcode_bulk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    transcode_bulk_kernel<<<sms, 32, smem, st>>>(mo_w, w_bytes, mo_ws, s_bytes, ws2,
+                                                reinterpret_cast<uint8_t*>(w_out), s_out, gs_out);
+    return cudaGetLastError();
+  }
   const int64_t units = (w_bytes >> 4) / 8 + 16;
   transcode_kernel<<<stream_grid(transcode_kernel, units), kStreamThreads, 0, st>>>(
       mo_w, w_bytes, mo_ws, s_bytes, ws2, reinterpret_cast<uint8_t*>(w_out), s_out, gs_out);
   return cudaGetLastError();
+}
+
+int read_copy_error() {
+  int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_copy_error, sizeof(int)) != cudaSuccess) return -1;
+  const int zero = 0;
+  cudaMemcpyToSymbol(g_copy_error, &zero, sizeof(int));
+  return v;
 }
 
 cudaError_t launch_dequantize(const uint32_t* w, const uint8_t* scales, const float* gs, int64_t E,

@@ -78,8 +78,13 @@ def test_dequantize_guard_bands(nv):
 
 # ------------------------------------------------------------------ transcode
 
-@pytest.mark.parametrize("nk", [(3, 16), (272, 256), (33, 5376), (1, 48)])
-def test_transcode_bit_exact(nv, nk):
+# (43008, 5376): the fused gate/up plane, about 26 copy chunks per SM (more
+# than the bulk copy's ring of six); (3, 16) and (1, 48): planes shorter than
+# a 16-byte unit at their end.
+@pytest.mark.parametrize("nk", [(3, 16), (272, 256), (33, 5376), (1, 48), (43008, 5376)])
+@pytest.mark.parametrize("path", ["bulk", "vector"])
+def test_transcode_bit_exact(nv, nk, path, monkeypatch):
+    monkeypatch.setenv("NVFP4_TRANSCODE_BULK", "1" if path == "bulk" else "0")
     N, K = nk
     g = synth.rng(N * 7 + K)
     mo_w, mo_ws, ws2 = synth.modelopt_triplet(g, N, K)
