@@ -74,7 +74,9 @@ typedef enum { NVFP4_ROUTE_AUTO = 0, NVFP4_ROUTE_QMV = 1, NVFP4_ROUTE_TC = 2 } n
  *   mo_weight_scale  uint8 [N, K/16]  E4M3
  *   weight_scale_2   float [1]        device scalar
  *   w_out [N, K/8] uint32, scales_out [N, K/16] uint8, gs_out float [1]
- * Lengths must equal N*K/2 and N*K/16 (NVFP4_ERR_PLANE otherwise).
+ * Lengths must equal N*K/2 and N*K/16 (NVFP4_ERR_PLANE otherwise). The
+ * planes are moved by bulk copies through shared memory (one CTA per SM);
+ * NVFP4_TRANSCODE_BULK=0 selects a vector-copy kernel instead.
  */
 nvfp4_status nvfp4_transcode(const uint8_t* mo_weight, int64_t mo_weight_len, const uint8_t* mo_weight_scale,
                              int64_t mo_weight_scale_len, const float* weight_scale_2, int64_t N, int64_t K,
