@@ -307,50 +307,71 @@ def run_ours(args):
 def run_e2e(nv, torch, dev, stream, lin, xs, ys, args, step_bytes):
     """The step through the public API, one call at a time (no graph), with the
     step's activations copied in from pinned host memory and its outputs copied
-    back every step. The 15 activation blocks live in one buffer and the 15
-    outputs in another (views), so a step moves its inputs and outputs with one
-    host-to-device and one device-to-host copy, as a serving loop batching
-    its tokens would."""
+    back to pinned host memory every step. The 15 activation blocks live in one
+    buffer and the 15 outputs in another (views), so a step moves its inputs
+    and outputs with one host-to-device and one device-to-host copy. As in a
+    serving loop, the copies run on their own streams, double-buffered: step
+    i + 1's inputs go in and step i - 1's outputs come out while step i
+    computes."""
     keys = list(xs.keys())
     xsz = [xs[k].numel() for k in keys]
     ysz = [ys[k].numel() for k in keys]
     host_x = torch.cat([xs[k].reshape(-1).cpu() for k in keys]).pin_memory()
-    dev_xbuf = torch.empty_like(host_x, device=dev)
-    dev_ybuf = torch.empty(sum(ysz), dtype=ys[keys[0]].dtype, device=dev)
-    host_y = torch.empty(dev_ybuf.shape, dtype=dev_ybuf.dtype).pin_memory()
-    dev_x, dev_y = {}, {}
-    ox = oy = 0
-    for k, nx, ny in zip(keys, xsz, ysz):
-        dev_x[k] = dev_xbuf[ox:ox + nx].view(xs[k].shape)
-        dev_y[k] = dev_ybuf[oy:oy + ny].view(ys[k].shape)
-        ox += nx
-        oy += ny
+    ydt = ys[keys[0]].dtype
+    dev_xbuf = [torch.empty_like(host_x, device=dev) for _ in range(2)]
+    dev_ybuf = [torch.empty(sum(ysz), dtype=ydt, device=dev) for _ in range(2)]
+    host_y = [torch.empty(sum(ysz), dtype=ydt).pin_memory() for _ in range(2)]
+    dev_x, dev_y = [{}, {}], [{}, {}]
+    for b in range(2):
+        ox = oy = 0
+        for k, nx, ny in zip(keys, xsz, ysz):
+            dev_x[b][k] = dev_xbuf[b][ox:ox + nx].view(xs[k].shape)
+            dev_y[b][k] = dev_ybuf[b][oy:oy + ny].view(ys[k].shape)
+            ox += nx
+            oy += ny
     h2d = host_x.numel() * host_x.element_size()
-    d2h = host_y.numel() * host_y.element_size()
+    d2h = host_y[0].numel() * host_y[0].element_size()
+    up, down = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    ev = lambda: torch.cuda.Event()
+    x_in, y_done, y_out = [ev(), ev()], [ev(), ev()], [ev(), ev()]
+    started = [False, False]
 
     def step(i):
-        dev_xbuf.copy_(host_x, non_blocking=True)
-        for mi, m in enumerate(DECODE_M):
-            for name, n, k, copies in lin:
-                w, s, gs = copies[(mi + i) % ROTATE]
-                nv.qmm(dev_x[(m, name)], w, s, gs=gs, out=dev_y[(m, name)])
-        host_y.copy_(dev_ybuf, non_blocking=True)
+        b = i % 2
+        with torch.cuda.stream(up):  # inputs of step i, once step i - 2 is done with the buffer
+            if started[b]:
+                up.wait_event(y_done[b])
+            dev_xbuf[b].copy_(host_x, non_blocking=True)
+            x_in[b].record(up)
+        with torch.cuda.stream(stream):
+            stream.wait_event(x_in[b])
+            if started[b]:
+                stream.wait_event(y_out[b])  # step i - 2's outputs have been copied out
+            for mi, m in enumerate(DECODE_M):
+                for name, n, k, copies in lin:
+                    w, s, gs = copies[(mi + i) % ROTATE]
+                    nv.qmm(dev_x[b][(m, name)], w, s, gs=gs, out=dev_y[b][(m, name)])
+            y_done[b].record(stream)
+        with torch.cuda.stream(down):
+            down.wait_event(y_done[b])
+            host_y[b].copy_(dev_ybuf[b], non_blocking=True)
+            y_out[b].record(down)
+        started[b] = True
 
-    with torch.cuda.stream(stream):
-        for i in range(args.warmup):
-            step(i)
-        torch.cuda.synchronize(dev)
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        for i in range(args.steps):
-            step(i)
-        b.record(stream)
+    for i in range(args.warmup):
+        step(i)
     torch.cuda.synchronize(dev)
-    ms = a.elapsed_time(b) / args.steps
+    a, z = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(up)
+    for i in range(args.steps):
+        step(args.warmup + i)
+    z.record(down)
+    torch.cuda.synchronize(dev)
+    ms = a.elapsed_time(z) / args.steps
     return {"value": round(step_bytes / (ms * 1e-3) / 1e9, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "ms_per_step": round(ms, 4),
-            "path": "nvfp4_qmm per call (no graph); the step's activations in one pinned host buffer copied in, "
-                    "its outputs in one device buffer copied out"}
+            "path": "nvfp4_qmm per call (no graph); per step one pinned-host copy in and one copy out, on their "
+                    "own streams, double-buffered so the copies of neighbouring steps overlap this step's calls"}
 
 
 def time_calls(torch, dev, stream, fn, reps):
