@@ -34,7 +34,9 @@ the activation batch yields a zero row, like an out-of-range expert.
 Parity status: every function here is pinned by ``tests/test_oracle_pins.py``
 (printed table, bit-definition vs library decode, closed-form packing,
 exact-rational brute force, sidecar identity against the ModelOpt formula,
-zero rows). The equivalence of ModelOpt's on-disk nibble order with the MLX
+zero rows; the gated-MLP activations against their symmetry identities, the
+exact erf GELU and the library sigmoid, and the gate/up halves through
+one-hot products). The equivalence of ModelOpt's on-disk nibble order with the MLX
 order is taken from the page ("likely matches") and is parity unpinned: no
 real checkpoint is available to confirm it.
 """
@@ -210,6 +212,40 @@ def modelopt_values(mo_weight, mo_weight_scale, weight_scale_2) -> np.ndarray:
     codes = np.stack([b & 0xF, b >> 4], axis=-1).reshape(b.shape[0], -1)
     s = np.repeat(e4m3_value(mo_weight_scale), 16, axis=-1)
     return e2m1_value(codes) * s * np.float64(np.float32(weight_scale_2))
+
+
+# Gated MLP (issue #705 "close native NVFP4 prefill gap", Hypothesis and
+# Activation-path follow-up: the Gemma and Llama MLP paths apply a GeGLU
+# activation to the fused gate/up projection and scale it by the global
+# factor). Readings: the fused plane holds the gate rows first and the up rows
+# after them (2 I rows for I outputs); the output is act(gate) * up, each half
+# already multiplied by the global factor; GeGLU uses GELU's tanh form (as
+# Gemma's MLP does); SiLU (x * sigmoid(x)) is the Llama-family activation.
+
+def gelu_tanh(v) -> np.ndarray:
+    """0.5 v (1 + tanh(sqrt(2 / pi) (v + 0.044715 v^3))), float64."""
+    v = np.asarray(v, dtype=np.float64)
+    return 0.5 * v * (1.0 + np.tanh(np.sqrt(2.0 / np.pi) * (v + 0.044715 * v ** 3)))
+
+
+def silu(v) -> np.ndarray:
+    """v / (1 + exp(-v)), float64."""
+    v = np.asarray(v, dtype=np.float64)
+    return v / (1.0 + np.exp(-v))
+
+
+ACTIVATIONS = {"silu": silu, "gelu_tanh": gelu_tanh}
+
+
+def qmm_glu(x, w, scales, gs=None, act="gelu_tanh") -> np.ndarray:
+    """Fused gate/up projection with its activation: ``w`` is ``[2 I, K/8]``
+    (gate rows, then up rows); ``y = act(g) * u`` with ``[g | u] = qmm(x, w)``,
+    ``y`` of shape ``[M, I]`` in float64."""
+    h = qmm(x, w, scales, gs)
+    half = h.shape[1] // 2
+    if 2 * half != h.shape[1]:
+        raise ValueError("the fused plane needs an even number of rows")
+    return ACTIVATIONS[act](h[:, :half]) * h[:, half:]
 
 
 def rel_to_max_error(y, ref) -> float:

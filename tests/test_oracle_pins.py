@@ -250,10 +250,57 @@ def pin_error_metric(orc):
     assert orc.rel_to_max_error([0.0], [0.0]) == 0.0
 
 
+def pin_gelu_tanh(orc):
+    import math
+    v = np.linspace(-8.0, 8.0, 4001)
+    g = orc.gelu_tanh(v)
+    assert orc.gelu_tanh(0.0) == 0.0
+    # 0.5 v (1 + tanh a) - 0.5 (-v) (1 + tanh(-a)) = v for the odd inner a(v)
+    assert np.max(np.abs(g - orc.gelu_tanh(-v) - v)) <= 1e-12
+    # the tanh form stays within 1e-3 of the exact x * Phi(x) everywhere
+    exact = np.array([0.5 * t * (1.0 + math.erf(t / math.sqrt(2.0))) for t in v])
+    assert np.max(np.abs(g - exact)) <= 1e-3
+    assert abs(orc.gelu_tanh(20.0) - 20.0) <= 1e-12 and abs(orc.gelu_tanh(-20.0)) <= 1e-12
+
+
+def pin_silu(orc):
+    from scipy.special import expit
+    v = np.linspace(-30.0, 30.0, 6001)
+    s = orc.silu(v)
+    assert orc.silu(0.0) == 0.0
+    assert np.max(np.abs(s - orc.silu(-v) - v)) <= 1e-12
+    assert np.max(np.abs(s - v * expit(v))) <= 1e-12 * (1.0 + np.abs(v)).max()
+
+
+def pin_glu_halves(orc):
+    # unit scales, one-hot x: the gate half and the up half of the fused plane
+    # are single table entries, so each output is act(table[g]) * table[u]
+    half, k = 8, 32
+    codes = synth.rng(705).integers(0, 16, size=(2 * half, k))
+    codes[0, :], codes[half, :] = 7, 2  # gate 6.0 and up 1.0 in row 0: swapping halves shows
+    sbytes = np.full((2 * half, k // 16), 0x38, dtype=np.uint8)
+    table = {int(c): float(v) for c, v in _read_table("e2m1_table.txt")}
+    for act in ("silu", "gelu_tanh"):
+        f = orc.ACTIVATIONS[act]
+        for col in (0, 9, 31):
+            x = np.zeros((1, k))
+            x[0, col] = 1.0
+            y = orc.qmm_glu(x, pack_codes(codes), sbytes, None, act)
+            want = [float(f(table[int(codes[j, col])])) * table[int(codes[half + j, col])] for j in range(half)]
+            assert y.shape == (1, half) and np.allclose(y[0], want, rtol=0, atol=1e-15)
+    # the global factor scales both halves before the activation
+    gs = np.float32(2688 * 2.0)
+    x = np.zeros((1, k))
+    x[0, 3] = 1.0
+    y = orc.qmm_glu(x, pack_codes(codes), sbytes, gs, "silu")
+    want = [float(orc.silu(2.0 * table[int(codes[j, 3])])) * 2.0 * table[int(codes[half + j, 3])] for j in range(half)]
+    assert np.allclose(y[0], want, rtol=0, atol=1e-15)
+
+
 PINS = [pin_e2m1_table, pin_e4m3_all_bytes, pin_packing, pin_block_scale_broadcast,
         pin_brute_force_matmul, pin_one_hot, pin_global_factor, pin_dequantize_rounding,
         pin_sidecar_identity, pin_transcode_layout, pin_gather_zero_rows, pin_plane_check,
-        pin_error_metric]
+        pin_error_metric, pin_gelu_tanh, pin_silu, pin_glu_halves]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=lambda p: p.__name__)
@@ -346,3 +393,24 @@ def test_planted_sidecar_without_2688(monkeypatch):
     _planted(monkeypatch, "transcode", bad)
     with pytest.raises(AssertionError):
         pin_sidecar_identity(O)
+
+
+def test_planted_glu_halves_swapped(monkeypatch):
+    orig = O.qmm
+
+    def swapped(x, w, scales, gs=None):
+        h = orig(x, w, scales, gs)
+        half = h.shape[1] // 2
+        return np.concatenate([h[:, half:], h[:, :half]], axis=1)
+    _planted(monkeypatch, "qmm", swapped)
+    with pytest.raises(AssertionError):
+        pin_glu_halves(O)
+
+
+def test_planted_gelu_without_cubic(monkeypatch):
+    def wrong(v):
+        v = np.asarray(v, dtype=np.float64)
+        return 0.5 * v * (1.0 + np.tanh(np.sqrt(2.0 / np.pi) * v))
+    monkeypatch.setattr(O, "gelu_tanh", wrong)
+    with pytest.raises(AssertionError):
+        pin_gelu_tanh(O)
