@@ -117,6 +117,30 @@ nvfp4_status nvfp4_qmm_routed(const void* x, nvfp4_dtype x_dtype, int64_t M, int
                               int64_t w_len, const uint8_t* scales, int64_t scales_len, const float* gs,
                               int64_t gs_len, int64_t N, void* y, nvfp4_route route, void* stream);
 
+/* Activation of the fused gate/up projection (nvfp4_qmm_glu). */
+typedef enum { NVFP4_ACT_SILU = 1, NVFP4_ACT_GELU_TANH = 2 } nvfp4_act;
+
+/*
+ * Fused gate/up projection with its activation (issue #705 "close native
+ * NVFP4 prefill gap", Hypothesis and Activation-path follow-up: the gated
+ * MLP's GeGLU activation applied to the fused, globally scaled gate/up
+ * projection, here fused into the matmul's epilogue):
+ *   [g | u] = x @ dequantize(w).T * gs / 2688,   y = act(g) * u
+ *   x [M, K] f16 or bf16; w [2 I, K/8] with the I gate rows first and the I
+ *   up rows after them; scales [2 I, K/16]; gs NULL or one float; y [M, I]
+ *   of x's dtype. act: SiLU (v * sigmoid(v)) or GELU in its tanh form
+ *   (Gemma's GeGLU), evaluated in f32 on the f32 sums.
+ * The intermediate [M, 2 I] never exists in memory. Below the crossover of
+ * the [2 I, K] plane (or with route NVFP4_ROUTE_QMV) the decode route runs
+ * (K % 256 == 0 required); otherwise the tensor-core route (K % 32 == 0),
+ * whole tiles only. f32 activations are refused (NVFP4_ERR_DTYPE). Not an
+ * interface of the pages; their follow-up names this fusion as the missing
+ * prefill piece.
+ */
+nvfp4_status nvfp4_qmm_glu(const void* x, nvfp4_dtype x_dtype, int64_t M, int64_t K, const uint32_t* w,
+                           int64_t w_len, const uint8_t* scales, int64_t scales_len, const float* gs,
+                           int64_t gs_len, int64_t I, nvfp4_act act, void* y, nvfp4_route route, void* stream);
+
 /*
  * nvfp4_qmm for callers that must not allocate device memory: a runtime whose
  * memory is planned once at start-up, or code that runs while a CUDA graph is

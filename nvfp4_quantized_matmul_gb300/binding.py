@@ -32,6 +32,7 @@ SIGNATURES = {
     "nvfp4_qmm_routed": (_INT, [_P, _INT, _I64, _I64, _P, _I64, _P, _I64, _P, _I64, _I64, _P, _INT, _P]),
     "nvfp4_qmm_crossover": (_I64, [_INT, _I64, _I64]),
     "nvfp4_qmm_noalloc": (_INT, [_P, _INT, _I64, _I64, _P, _I64, _P, _I64, _P, _I64, _I64, _P, _P]),
+    "nvfp4_qmm_glu": (_INT, [_P, _INT, _I64, _I64, _P, _I64, _P, _I64, _P, _I64, _I64, _INT, _P, _INT, _P]),
     "nvfp4_gather_qmm": (_INT, [_P, _INT, _I64, _I64, _P, _P, _I64, _INT, _P, _I64, _P, _I64, _P, _I64,
                                 _I64, _I64, _P, _P]),
     "nvfp4_last_error": (ctypes.c_char_p, []),
@@ -155,6 +156,26 @@ def qmm(x, w, scales, gs=None, route="auto", out=None):
         out = torch.empty((m, n), dtype=x.dtype, device=x.device)
     check(_lib.nvfp4_qmm_routed(_ptr(x), DTYPE_CODE[x.dtype], m, k, _ptr(w), w.numel(), _ptr(scales),
                                 scales.numel(), _ptr(gs), _n(gs), n, _ptr(out), ROUTE_CODE[route], _stream(x)))
+    return out
+
+
+ACT_CODE = {"silu": 1, "gelu_tanh": 2}
+
+
+def qmm_glu(x, w, scales, gs=None, act="gelu_tanh", route="auto", out=None):
+    """Fused gate/up with its activation: ``w`` is [2 I, K/8] (gate rows, then
+    up rows); returns act(gate) * up, [M, I] in x's dtype."""
+    _cuda(x, w, scales)
+    m, k = x.shape
+    n2 = w.shape[0]
+    if n2 % 2:
+        raise ValueError("the fused plane needs an even number of rows")
+    i = n2 // 2
+    gs = _gs_tensor(gs, x.device)
+    if out is None:
+        out = torch.empty((m, i), dtype=x.dtype, device=x.device)
+    check(_lib.nvfp4_qmm_glu(_ptr(x), DTYPE_CODE[x.dtype], m, k, _ptr(w), w.numel(), _ptr(scales), scales.numel(),
+                             _ptr(gs), _n(gs), i, ACT_CODE[act], _ptr(out), ROUTE_CODE[route], _stream(x)))
     return out
 
 

@@ -273,6 +273,50 @@ nvfp4_status nvfp4_qmm(const void* x, nvfp4_dtype x_dtype, int64_t M, int64_t K,
                           stream);
 }
 
+nvfp4_status nvfp4_qmm_glu(const void* x, nvfp4_dtype x_dtype, int64_t M, int64_t K, const uint32_t* w,
+                           int64_t w_len, const uint8_t* scales, int64_t scales_len, const float* gs,
+                           int64_t gs_len, int64_t I, nvfp4_act act, void* y, nvfp4_route route, void* stream) {
+  const char* fn = "nvfp4_qmm_glu";
+  if (x_dtype != NVFP4_F16 && x_dtype != NVFP4_BF16)
+    return fail(NVFP4_ERR_DTYPE, "%s: f16 or bf16 activations only (got %d)", fn, (int)x_dtype);
+  if (act != NVFP4_ACT_SILU && act != NVFP4_ACT_GELU_TANH)
+    return fail(NVFP4_ERR_DTYPE, "%s: unknown activation %d", fn, (int)act);
+  if (route != NVFP4_ROUTE_AUTO && route != NVFP4_ROUTE_QMV && route != NVFP4_ROUTE_TC)
+    return fail(NVFP4_ERR_DTYPE, "%s: unknown route %d", fn, (int)route);
+  if (M < 0 || I < 0) return fail(NVFP4_ERR_SHAPE, "%s: negative M or I", fn);
+  if (I > (INT64_MAX >> 2)) return fail(NVFP4_ERR_SHAPE, "%s: I too large", fn);
+  const int64_t N = 2 * I;  // gate rows, then up rows
+  nvfp4_status s = check_planes(fn, w, w_len, scales, scales_len, 1, N, K);
+  if (s) return s;
+  if ((s = check_gs(fn, gs, gs_len, 1))) return s;
+  int64_t xe;
+  if (!mul_ok(M, K, &xe) || !mul_ok(M, N, &xe)) return fail(NVFP4_ERR_SHAPE, "%s: M*K or M*N overflows", fn);
+  if (M == 0 || I == 0) return ok();
+  if (!y || (K > 0 && !x)) return fail(NVFP4_ERR_NULL, "%s: x or y is NULL", fn);
+  if (!aligned(x, 16) || !aligned(y, 16)) return fail(NVFP4_ERR_ALIGN, "%s: x and y must be 16-byte aligned", fn);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // K = 0: both halves are 0 and so is act(0) * 0
+  if (K == 0) return cuda_status(fn, cudaMemsetAsync(y, 0, (size_t)(M * I * dtype_size(x_dtype)), st));
+  const bool tc_ok = nvfp4::qmm_tc_supported(M, N, K);
+  nvfp4::QmvArgs a{x, w, scales, gs, nullptr, nullptr, M, M, K, N, 1, y};
+  a.glu_cols = I;
+  a.glu_act = (int)act;
+  const bool qmv_ok = nvfp4::qmv_stream_supported(a, (int)x_dtype) && N < (1ll << 31);
+  bool use_tc;
+  if (route == NVFP4_ROUTE_TC)
+    use_tc = true;
+  else if (route == NVFP4_ROUTE_QMV)
+    use_tc = false;
+  else
+    use_tc = !qmv_ok || M >= nvfp4_qmm_crossover(x_dtype, N, K);
+  if (use_tc && !tc_ok)
+    return fail(NVFP4_ERR_SHAPE, "%s: the tensor-core route needs K %% 32 == 0 and K >= 32 (K=%" PRId64 ")", fn, K);
+  if (!use_tc && !qmv_ok)
+    return fail(NVFP4_ERR_SHAPE, "%s: the decode route needs K %% 256 == 0 (K=%" PRId64 ")", fn, K);
+  if (use_tc) return cuda_status(fn, nvfp4::launch_qmm_tc_glu(x, (int)x_dtype, M, K, w, scales, gs, I, (int)act, y, st));
+  return cuda_status(fn, nvfp4::launch_qmv_stream_glu(a, (int)x_dtype, st));
+}
+
 nvfp4_status nvfp4_qmm_noalloc(const void* x, nvfp4_dtype x_dtype, int64_t M, int64_t K, const uint32_t* w,
                                int64_t w_len, const uint8_t* scales, int64_t scales_len, const float* gs,
                                int64_t gs_len, int64_t N, void* y, void* stream) {

@@ -28,7 +28,11 @@ struct QmvArgs {
   const uint32_t* lhs;    // null or [R]
   const uint32_t* rhs;    // null or [R]
   int64_t B, R, K, N, E;
-  void* y;                // [R, N], dtype xdt
+  void* y;                // [R, N], dtype xdt ([R, glu_cols] for a fused gate/up call)
+  // Fused gate/up: w holds N = 2 * glu_cols rows (gate, then up) and y gets
+  // act(gate) * up; glu_act 1 = SiLU, 2 = GELU (tanh form); 0 = plain call.
+  int64_t glu_cols = 0;
+  int glu_act = 0;
 };
 cudaError_t launch_qmv(const QmvArgs& a, int xdt, cudaStream_t st);
 
@@ -52,6 +56,9 @@ void release_stream_workspaces();
 // activations, K % 256 == 0): rows grouped by expert, eight to a group, each
 // group's expert plane streamed once and split over its share of the SMs.
 bool qmv_group_supported(const QmvArgs& a, int xdt);
+// The dense route for a fused gate/up call (a.glu_act != 0): same limits as
+// qmv_stream_supported.
+cudaError_t launch_qmv_stream_glu(const QmvArgs& a, int xdt, cudaStream_t st);
 cudaError_t launch_qmv_group(const QmvArgs& a, int xdt, cudaStream_t st);
 // The same route with its scratch in a fixed array inside the library (no
 // allocation); at most kNoAllocMaxRows weight rows.
@@ -69,6 +76,10 @@ bool qmm_tc_supported(int64_t M, int64_t N, int64_t K);
 bool tc_stream_k();
 cudaError_t launch_qmm_tc(const void* x, int xdt, int64_t M, int64_t K, const uint32_t* w, const uint8_t* scales,
                           const float* gs, int64_t N, void* y, cudaStream_t st);
+// Fused gate/up on the tensor cores: w is [2 cols, K/8] (gate rows, then up
+// rows), y [M, cols] = act(gate) * up; act 1 = SiLU, 2 = GELU (tanh form).
+cudaError_t launch_qmm_tc_glu(const void* x, int xdt, int64_t M, int64_t K, const uint32_t* w, const uint8_t* scales,
+                              const float* gs, int64_t cols, int act, void* y, cudaStream_t st);
 // Expert-batched GatherQMM on the tensor cores, for rows sorted by expert.
 bool gather_tc_supported(int64_t B, int64_t K, int64_t R, int64_t E, int64_t N);
 cudaError_t launch_gather_tc(const void* x, int xdt, int64_t B, int64_t K, const uint32_t* lhs, const uint32_t* rhs,

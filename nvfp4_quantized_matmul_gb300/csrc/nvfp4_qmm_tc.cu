@@ -100,6 +100,12 @@ struct TcParams {
   int dp_tiles, sk_tiles;
   float* ws;
   uint32_t* ws_cnt;
+  // Fused gate/up (qmm_tc_kernel with kGlu): the plane holds 2 * glu_cols
+  // rows (gate, then up); weight tile nt stands for gate rows [128 nt, 128 nt
+  // + 128) and the matching up rows, and y ([M, glu_cols]) gets act(gate) *
+  // up. glu_act: 1 SiLU, 2 GELU (tanh form).
+  int64_t glu_cols;
+  int glu_act;
 };
 
 // One output tile: expert, weight tile, first output row and row count.
@@ -330,7 +336,7 @@ __device__ __forceinline__ void w_seek(WCursor& cur, const TcParams& p, int num_
   }
 }
 
-template <int BN, int RPT, typename Cur>
+template <int BN, bool kGlu = false, int RPT, typename Cur>
 __device__ __forceinline__ void w_load(WTask<RPT>& t, const Cur& cur, const TcParams& p, int r, int h) {
   if (cur.done) return;
   const int64_t kwords = p.K / 8, kgroups = p.K / 16;
@@ -341,8 +347,10 @@ __device__ __forceinline__ void w_load(WTask<RPT>& t, const Cur& cur, const TcPa
   const int64_t g4 = (int64_t)cur.kb * 4;
 #pragma unroll
   for (int i = 0; i < RPT; ++i) {
-    const int64_t n = (int64_t)cur.nt * BN + r + 128 * i;
-    const bool ok = kok && n < p.N;
+    // GLU: the first 128 rows of the tile are gate rows, the next 128 the up
+    // rows of the same outputs
+    const int64_t n = kGlu ? (int64_t)cur.nt * 128 + r + (i ? p.glu_cols : 0) : (int64_t)cur.nt * BN + r + 128 * i;
+    const bool ok = kok && (kGlu ? (int64_t)cur.nt * 128 + r < p.glu_cols : n < p.N);
     t.w[i] = ok ? __ldg(reinterpret_cast<const uint4*>(w + n * kwords + kw)) : make_uint4(0, 0, 0, 0);
     if (kgroups % 4 == 0) {
       t.s[i] = ok ? __ldg(reinterpret_cast<const uint32_t*>(sc + n * kgroups + g4)) : 0u;
@@ -384,7 +392,7 @@ __device__ __forceinline__ void w_store_row(uint32_t stage_base, int row, int h,
   }
 }
 
-template <typename T, typename C, bool GATHER>
+template <typename T, typename C, bool GATHER, bool kGlu = false>
 __device__ void producer_role(const TcParams& p, uint32_t sB, uint32_t bars, volatile int* abort_flag, int num_tiles,
                               const int* seg, const int* pre) {
   constexpr int STAGES = C::STAGES, RPT = C::RPT, BM = C::BM;
@@ -399,7 +407,7 @@ __device__ void producer_role(const TcParams& p, uint32_t sB, uint32_t bars, vol
   WTask<RPT> buf[PF];
 #pragma unroll
   for (int j = 0; j < PF - 1; ++j) {
-    w_load<C::BN>(buf[j], ld, p, r, h);
+    w_load<C::BN, kGlu>(buf[j], ld, p, r, h);
     w_advance<GATHER, BM>(ld, p, num_tiles, seg, pre);
   }
   uint32_t u = 0;
@@ -423,7 +431,7 @@ __device__ void producer_role(const TcParams& p, uint32_t sB, uint32_t bars, vol
 #pragma unroll
     for (int j = 0; j < PF; ++j) {
       if (i + j >= total) return;
-      w_load<C::BN>(buf[(j + PF - 1) % PF], ld, p, r, h);
+      w_load<C::BN, kGlu>(buf[(j + PF - 1) % PF], ld, p, r, h);
       w_advance<GATHER, BM>(ld, p, num_tiles, seg, pre);
       if (!consume(buf[j])) return;
     }
@@ -584,7 +592,7 @@ __device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* map
 
 // ---------------------------------------------------------------- kernel
 
-template <typename T, typename C, bool GATHER>
+template <typename T, typename C, bool GATHER, bool kGlu = false>
 __global__ void __launch_bounds__(C::THREADS, 1)
 qmm_tc_kernel(const __grid_constant__ CUtensorMap xmap, const TcParams p) {
   constexpr int STAGES = C::STAGES, MH = C::MH, BN = C::BN, BM = C::BM, NBUF = C::ACC_BUFS;
@@ -790,6 +798,52 @@ qmm_tc_kernel(const __grid_constant__ CUtensorMap xmap, const TcParams p) {
       const float fac = global_factor(p.gs, tl.e);
       const int64_t n_base = (int64_t)tl.nt * BN;
       const uint32_t tcol = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(b * MH * BN + hm * BN);
+      if constexpr (kGlu) {
+        // columns [0, 128) hold gate sums, [128, 256) the matching up sums
+#pragma unroll 1
+        for (int c = 0; c < BN / 64; ++c) {
+          uint32_t g[32], u[32];
+          tmem_ld32(tcol + (uint32_t)(32 * c), g);
+          tmem_ld32(tcol + (uint32_t)(BN / 2 + 32 * c), u);
+          tmem_ld_wait();
+          if (!live) continue;
+          const int64_t n0 = (int64_t)tl.nt * (BN / 2) + 32 * c;
+          if (n0 >= p.glu_cols) continue;
+          uint32_t packed[16];
+#pragma unroll
+          for (int k = 0; k < 16; ++k) {
+            float o[2];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              float gv = __uint_as_float(g[2 * k + e]), uv = __uint_as_float(u[2 * k + e]);
+              if (p.gs) {
+                gv = __fmul_rn(gv, fac);
+                uv = __fmul_rn(uv, fac);
+              }
+              const float a = p.glu_act == 1 ? gv / (1.0f + expf(-gv))
+                                             : 0.5f * gv * (1.0f + tanhf(0.7978845608028654f * (gv + 0.044715f * gv * gv * gv)));
+              o[e] = a * uv;
+            }
+            const T t0 = Dt<T>::from_f32(o[0]), t1 = Dt<T>::from_f32(o[1]);
+            packed[k] = (uint32_t)(*reinterpret_cast<const uint16_t*>(&t0)) |
+                        ((uint32_t)(*reinterpret_cast<const uint16_t*>(&t1)) << 16);
+          }
+          T* dst = y + m * p.glu_cols + n0;
+          if (n0 + 32 <= p.glu_cols && (p.glu_cols % 8) == 0) {
+            uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              d4[k] = make_uint4(packed[4 * k], packed[4 * k + 1], packed[4 * k + 2], packed[4 * k + 3]);
+          } else {
+            uint16_t* d16 = reinterpret_cast<uint16_t*>(dst);
+            for (int k = 0; k < 32 && n0 + k < p.glu_cols; ++k) d16[k] = (uint16_t)(packed[k >> 1] >> (16 * (k & 1)));
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(accEmpty(b));
+        continue;
+      }
 #pragma unroll 1
       for (int c = 0; c < BN / 32; ++c) {
         uint32_t r[32];
@@ -828,7 +882,7 @@ qmm_tc_kernel(const __grid_constant__ CUtensorMap xmap, const TcParams p) {
       if (lane == 0) mbar_arrive(accEmpty(b));
     }
   } else if (warp >= C::kWarpProd0) {
-    producer_role<T, C, GATHER>(p, sB, bars, abort_flag, num_tiles, seg, pre);
+    producer_role<T, C, GATHER, kGlu>(p, sB, bars, abort_flag, num_tiles, seg, pre);
   }
 
   tc_fence_before();
@@ -1263,6 +1317,8 @@ cudaError_t launch_cfg(const void* x, int64_t M, int64_t K, const uint32_t* w, c
   p.B = M;
   p.E = 1;
   p.xcontig = 1;
+  p.glu_cols = 0;
+  p.glu_act = 0;
   // Tiles are dealt whole, round robin, unless they make fewer than two
   // waves: then the partial wave would idle a large share of the SMs, and
   // all tiles are split evenly by k-blocks instead (stream-K). From two
@@ -1304,6 +1360,55 @@ cudaError_t launch_cfg(const void* x, int64_t M, int64_t K, const uint32_t* w, c
 using Tile256x256 = Cfg<2, 256>;
 using Tile256x128 = Cfg<2, 128>;
 using Tile128x256 = Cfg<1, 256>;
+
+// Fused gate/up with its activation: weight tiles of 128 gate rows and the
+// matching 128 up rows (BN = 256), whole tiles round robin.
+template <typename T, typename C>
+cudaError_t launch_glu_cfg(const void* x, int64_t M, int64_t K, const uint32_t* w, const uint8_t* scales,
+                           const float* gs, int64_t cols, int act, void* y, int sms, cudaStream_t st) {
+  static_assert(C::BN == 256, "a GLU tile is 128 gate rows and 128 up rows");
+  auto enc = encode_fn();
+  if (!enc) return cudaErrorNotSupported;
+  CUtensorMap map;
+  const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)M};
+  const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+  const cuuint32_t box[2] = {BK, 128};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUtensorMapDataType dt =
+      std::is_same<T, __nv_bfloat16>::value ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  CUresult r = enc(&map, dt, 2, const_cast<void*>(x), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  TcParams p;
+  p.w = w;
+  p.scales = scales;
+  p.gs = gs;
+  p.y = y;
+  p.M = M;
+  p.N = 2 * cols;
+  p.K = K;
+  p.num_m_tiles = (int)((M + C::BM - 1) / C::BM);
+  p.num_n_tiles = (int)((cols + 127) / 128);
+  p.num_tiles = p.num_m_tiles * p.num_n_tiles;
+  p.num_kb = (int)((K + BK - 1) / BK);
+  p.lhs = nullptr;
+  p.rhs = nullptr;
+  p.B = M;
+  p.E = 1;
+  p.xcontig = 1;
+  p.dp_tiles = p.num_tiles;
+  p.sk_tiles = 0;
+  p.ws = nullptr;
+  p.ws_cnt = nullptr;
+  p.glu_cols = cols;
+  p.glu_act = act;
+  const int grid = p.num_tiles < sms ? p.num_tiles : sms;
+  auto kern = qmm_tc_kernel<T, C, false, true>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
+  if (e != cudaSuccess) return e;
+  kern<<<grid, C::THREADS, C::SMEM, st>>>(map, p);
+  return cudaGetLastError();
+}
 
 // Tile shape. Below two waves of 256x256 tiles the stream-K split leaves no
 // partial wave to avoid, and 256x256 tiles, whose decoded weight tile feeds
@@ -1469,6 +1574,8 @@ cudaError_t launch_gather(const void* x, int64_t B, int64_t K, const uint32_t* l
   p.B = B;
   p.E = (int)E;
   p.xcontig = per_row ? 0 : 1;
+  p.glu_cols = 0;
+  p.glu_act = 0;
   const size_t smem = C::SMEM + kGatherSmem;
   auto kern = qmm_tc_kernel<T, C, true>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -1504,6 +1611,18 @@ cudaError_t launch_gather_tc(const void* x, int xdt, int64_t B, int64_t K, const
                              void* y, cudaStream_t st) {
   if (xdt == kBF16) return launch_gather_t<__nv_bfloat16>(x, B, K, lhs, rhs, R, w, scales, gs, E, N, y, st);
   return launch_gather_t<__half>(x, B, K, lhs, rhs, R, w, scales, gs, E, N, y, st);
+}
+
+cudaError_t launch_qmm_tc_glu(const void* x, int xdt, int64_t M, int64_t K, const uint32_t* w, const uint8_t* scales,
+                              const float* gs, int64_t cols, int act, void* y, cudaStream_t st) {
+  int dev = 0, sms = 152;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (xdt == kBF16)
+    return M <= 128 ? launch_glu_cfg<__nv_bfloat16, Tile128x256>(x, M, K, w, scales, gs, cols, act, y, sms, st)
+                    : launch_glu_cfg<__nv_bfloat16, Tile256x256>(x, M, K, w, scales, gs, cols, act, y, sms, st);
+  return M <= 128 ? launch_glu_cfg<__half, Tile128x256>(x, M, K, w, scales, gs, cols, act, y, sms, st)
+                  : launch_glu_cfg<__half, Tile256x256>(x, M, K, w, scales, gs, cols, act, y, sms, st);
 }
 
 bool tc_stream_k() {

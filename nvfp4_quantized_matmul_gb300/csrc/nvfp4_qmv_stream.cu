@@ -86,6 +86,12 @@ struct SPlan {
   int xs_stride;  // staged activation row stride, elements (= 32 mod 256)
   int x_is_bf16;  // activation (and output) dtype is bf16, else f16
   int pslots;     // token slots held in a partial-sum buffer (8 per MMA tile)
+  // Fused gate/up (GLU) launches: the plane holds 2 * glu_cols rows (gate
+  // rows, then up rows); row tile r stands for gate rows [128 r, 128 r + 128)
+  // stacked on the matching up rows, and writes act(gate) * up for those
+  // glu_cols-wide output columns. glu_act: 1 SiLU, 2 GELU (tanh form).
+  int64_t glu_cols;
+  int glu_act;
 };
 
 struct Seg {
@@ -320,7 +326,7 @@ struct ChunkPos {
 // consumers; a scale block at the start of each segment and at every fourth
 // chunk, a word stage per chunk. An expert group (kGrp) reads its expert's
 // plane through 3-D maps ([E, N, K] planes, rows past N zero-filled).
-template <bool kGrp>
+template <bool kGrp, bool kGlu>
 __device__ void produce(const SPlan& p, int grp, Work wk, const CUtensorMap* wmap,
                         const CUtensorMap* smap, uint32_t wst, uint32_t sst, const Bars& bar,
                         volatile int* abort_flag, int expert) {
@@ -329,13 +335,18 @@ __device__ void produce(const SPlan& p, int grp, Work wk, const CUtensorMap* wma
   pos.start(wk);
   for (; pos.valid; pos.advance()) {
     const int ac = grp * p.ncg + pos.c;  // absolute chunk
-    const int row = (int)(pos.sg.r * kTileRows);
+    // GLU: the tile's gate half-tile; its up half-tile is glu_cols rows on
+    const int row = (int)(pos.sg.r * (kGlu ? kTileRows / 2 : kTileRows));
+    const int up_row = (int)(p.glu_cols + row);
     if (pos.block_start(ac)) {
       const uint32_t b = su & 1u, bph = (su >> 1) & 1u;
       if (!wait_bar(bar.sempty(b), bph ^ 1u, abort_flag, 21, &g_stream_error)) break;
       ++su;
       mbar_arrive_tx(bar.sfull(b), kSBox);
-      if (kGrp)
+      if (kGlu) {
+        tma_load_2d(sst + b * kSBox, smap, (ac / kSChunks) * (kSChunks * 16), row, bar.sfull(b));
+        tma_load_2d(sst + b * kSBox + kSBox / 2, smap, (ac / kSChunks) * (kSChunks * 16), up_row, bar.sfull(b));
+      } else if (kGrp)
         tma_load_3d(sst + b * kSBox, smap, (ac / kSChunks) * (kSChunks * 16), row, expert, bar.sfull(b));
       else
         tma_load_2d(sst + b * kSBox, smap, (ac / kSChunks) * (kSChunks * 16), row, bar.sfull(b));
@@ -343,7 +354,10 @@ __device__ void produce(const SPlan& p, int grp, Work wk, const CUtensorMap* wma
     if (!wait_bar(bar.empty(s), ph ^ 1u, abort_flag, 22, &g_stream_error)) break;
     ++u;
     mbar_arrive_tx(bar.full(s), kWBox);
-    if (kGrp)
+    if (kGlu) {
+      tma_load_2d(wst + s * kWBox, wmap, ac * kChunkWords, row, bar.full(s));
+      tma_load_2d(wst + s * kWBox + kWBox / 2, wmap, ac * kChunkWords, up_row, bar.full(s));
+    } else if (kGrp)
       tma_load_3d(wst + s * kWBox, wmap, ac * kChunkWords, row, expert, bar.full(s));
     else
       tma_load_2d(wst + s * kWBox, wmap, ac * kChunkWords, row, bar.full(s));
@@ -594,8 +608,15 @@ __device__ __forceinline__ void store_out8(void* y, int is_bf16, int64_t idx, co
 // A dense call's row tile r uses block r. An expert group (kGrp) uses blocks
 // wsbase .. wsbase + gs - 1, one per row tile left over after the whole rows
 // are dealt out (there are fewer than gs), and writes token slot s to output
-// row yrow[s] with the expert's global scale.
-template <bool kGrp>
+// row yrow[s] with the expert's global scale. A GLU tile (kGlu) holds gate
+// sums in rows 0..127 and the matching up sums in rows 128..255 and writes
+// act(factor * gate) * (factor * up) to output columns 128 r .. 128 r + 127.
+__device__ __forceinline__ float glu_act(int act, float v) {
+  if (act == 1) return v / (1.0f + expf(-v));                                            // SiLU
+  return 0.5f * v * (1.0f + tanhf(0.7978845608028654f * (v + 0.044715f * v * v * v)));  // GELU, tanh form
+}
+
+template <bool kGrp, bool kGlu>
 __device__ void finish(const QmvArgs& a, const SPlan& p, Work wk, uint32_t pbuf, uint32_t pbuf_bytes,
                        const Bars& bar, volatile int* abort_flag, float* __restrict__ acc,
                        uint32_t* __restrict__ cnt, int expert, int wsbase, const int64_t* yrow) {
@@ -613,8 +634,10 @@ __device__ void finish(const QmvArgs& a, const SPlan& p, Work wk, uint32_t pbuf,
     ++pc;
     if (!wait_bar_warp(bar.pfull(b), bph, abort_flag, 26, &g_stream_error)) break;
     const uint32_t pb = pbuf + b * pbuf_bytes;
-    const int64_t n0 = sg.r * kTileRows;
-    const int rows = (int)(a.N - n0 < kTileRows ? a.N - n0 : kTileRows);
+    const int64_t n0 = sg.r * (kGlu ? kTileRows / 2 : kTileRows);
+    const int64_t ncols = kGlu ? p.glu_cols : a.N;  // output columns
+    const int rows = kGlu ? (int)(ncols - n0 < kTileRows / 2 ? ncols - n0 : kTileRows / 2)
+                          : (int)(a.N - n0 < kTileRows ? a.N - n0 : kTileRows);
     bool own = p.S == 1 && sg.c0 == 0 && sg.c1 == p.ncg;  // the whole row tile is this CTA's
     const int64_t wt = kGrp ? wsbase + (sg.r - first_split) : sg.r;  // the tile's workspace block
     float* blk = acc + wt * (int64_t)(kAccSlots * kTileRows);
@@ -653,7 +676,32 @@ __device__ void finish(const QmvArgs& a, const SPlan& p, Work wk, uint32_t pbuf,
         if (lane == 0) atomicExch(cnt + wt, 0u);
       }
     }
-    if (own) {  // write y = factor * sum for the tile's rows
+    if (kGlu && own) {  // y = act(factor * gate) * (factor * up)
+      auto out = [&](int slot, int j) {
+        float g = lds_f32(pb + 4u * ((uint32_t)slot * kPStride + (uint32_t)j));
+        float u = lds_f32(pb + 4u * ((uint32_t)slot * kPStride + (uint32_t)(kTileRows / 2 + j)));
+        if (has_gs) {
+          g = __fmul_rn(g, factor);
+          u = __fmul_rn(u, factor);
+        }
+        return glu_act(p.glu_act, g) * u;
+      };
+      if ((ncols & 7) == 0) {
+        for (int idx = lane; idx < M * (kTileRows / 16); idx += 32) {
+          const int slot = idx / (kTileRows / 16), j8 = (idx % (kTileRows / 16)) * 8;
+          if (j8 >= rows) continue;
+          float v[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) v[i] = out(slot, j8 + i);
+          store_out8(a.y, p.x_is_bf16, (int64_t)slot * ncols + n0 + j8, v);
+        }
+      } else {
+        for (int idx = lane; idx < M * (kTileRows / 2); idx += 32) {
+          const int slot = idx / (kTileRows / 2), j = idx % (kTileRows / 2);
+          if (j < rows) store_out(a.y, p.x_is_bf16, (int64_t)slot * ncols + n0 + j, out(slot, j));
+        }
+      }
+    } else if (own) {  // write y = factor * sum for the tile's rows
       if ((a.N & 7) == 0) {
         // eight outputs (16 bytes) per store: a warp's narrow 2-byte stores
         // cost about as much each as a wide one
@@ -800,7 +848,7 @@ size_t stream_smem_bytes(const SPlan& p) {
   return 1024 + (size_t)p.stages * kWBox + 2 * kSBox + pbuf + kBarBytes + 16 + 256 + 1024 + 512 + 64 + xs;
 }
 
-template <int MT, int RT, bool kGrp>
+template <int MT, int RT, bool kGrp, bool kGlu = false>
 __global__ void __launch_bounds__(Geo<RT>::kThreads, 1)
 qmv_stream_kernel(const QmvArgs a, const SPlan p, float* __restrict__ acc, uint32_t* __restrict__ cnt,
                   const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap smap) {
@@ -883,12 +931,12 @@ qmv_stream_kernel(const QmvArgs a, const SPlan p, float* __restrict__ acc, uint3
   const Work wk = Work::of(q, gi);
 
   if (warp == Geo<RT>::kProducer) {
-    if ((threadIdx.x & 31) == 0) produce<kGrp>(q, grp, wk, &wmap, &smap, wst, sst, bar, abort_flag, expert);
+    if ((threadIdx.x & 31) == 0) produce<kGrp, kGlu>(q, grp, wk, &wmap, &smap, wst, sst, bar, abort_flag, expert);
     return;
   }
   asm volatile("griddepcontrol.wait;" ::: "memory");
   if (warp == Geo<RT>::kEpilogue) {
-    finish<kGrp>(a, q, wk, pbuf, pbuf_bytes, bar, abort_flag, acc, cnt, expert, wsbase, s_yrow);
+    finish<kGrp, kGlu>(a, q, wk, pbuf, pbuf_bytes, bar, abort_flag, acc, cnt, expert, wsbase, s_yrow);
     return;
   }
   // Consumers: stage the activation columns this CTA visits (named barrier
@@ -1024,14 +1072,16 @@ bool make_plan(SPlan& p, int sms, int64_t max_dyn) {
 // are the same few planes call after call, so the pair is kept per (planes,
 // shape). With `experts` the maps are 3-D over all E planes ([E, N, K], box
 // depth 1), so that a box never runs into the next expert's rows.
-cudaError_t plane_maps(const QmvArgs& a, CUtensorMap* wmap, CUtensorMap* smap, bool experts = false) {
-  using Key = std::tuple<const void*, const void*, int64_t, int64_t, int64_t>;
+// box_rows: 256 (a row tile per box), or 128 for a GLU tile's two halves.
+cudaError_t plane_maps(const QmvArgs& a, CUtensorMap* wmap, CUtensorMap* smap, bool experts = false,
+                       cuuint32_t box_rows = kTileRows) {
+  using Key = std::tuple<const void*, const void*, int64_t, int64_t, int64_t, cuuint32_t>;
   struct Maps {
     CUtensorMap w, s;
   };
   static std::mutex mu;
   static std::map<Key, Maps> cache;
-  const Key key{a.w, a.scales, a.N, a.K, experts ? a.E : 0};
+  const Key key{a.w, a.scales, a.N, a.K, experts ? a.E : 0, box_rows};
   {
     std::lock_guard<std::mutex> lock(mu);
     auto it = cache.find(key);
@@ -1047,7 +1097,7 @@ cudaError_t plane_maps(const QmvArgs& a, CUtensorMap* wmap, CUtensorMap* smap, b
   {
     const cuuint64_t dims[3] = {(cuuint64_t)(a.K / 8), (cuuint64_t)a.N, (cuuint64_t)a.E};
     const cuuint64_t strides[2] = {(cuuint64_t)(a.K / 2), (cuuint64_t)(a.K / 2) * (cuuint64_t)a.N};
-    const cuuint32_t box[3] = {kChunkWords, kTileRows, 1};
+    const cuuint32_t box[3] = {kChunkWords, box_rows, 1};
     const cuuint32_t es[3] = {1, 1, 1};
     if (enc(wmap, CU_TENSOR_MAP_DATA_TYPE_UINT32, rank, const_cast<uint32_t*>(a.w), dims, strides, box, es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -1057,7 +1107,7 @@ cudaError_t plane_maps(const QmvArgs& a, CUtensorMap* wmap, CUtensorMap* smap, b
   {
     const cuuint64_t dims[3] = {(cuuint64_t)(a.K / 16), (cuuint64_t)a.N, (cuuint64_t)a.E};
     const cuuint64_t strides[2] = {(cuuint64_t)(a.K / 16), (cuuint64_t)(a.K / 16) * (cuuint64_t)a.N};
-    const cuuint32_t box[3] = {kSChunks * 16, kTileRows, 1};
+    const cuuint32_t box[3] = {kSChunks * 16, box_rows, 1};
     const cuuint32_t es[3] = {1, 1, 1};
     if (enc(smap, CU_TENSOR_MAP_DATA_TYPE_UINT8, rank, const_cast<uint8_t*>(a.scales), dims, strides, box, es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -1070,20 +1120,20 @@ cudaError_t plane_maps(const QmvArgs& a, CUtensorMap* wmap, CUtensorMap* smap, b
   return cudaSuccess;
 }
 
-template <int MT, int RT>
+template <int MT, int RT, bool kGlu = false>
 cudaError_t launch_mt(const QmvArgs& a, int xdt, cudaStream_t st, const Ws* given = nullptr) {
-  auto kern = qmv_stream_kernel<MT, RT, false>;
+  auto kern = qmv_stream_kernel<MT, RT, false, kGlu>;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  using Key = std::tuple<int, int64_t, int64_t, int64_t, int>;
+  using Key = std::tuple<int, int64_t, int64_t, int64_t, int, int>;
   static std::mutex mu;
   static std::map<Key, SPlan> cache;
   static std::map<int, int64_t> max_dyn_of_dev;
   SPlan p{};
   {
     std::lock_guard<std::mutex> lock(mu);
-    const Key key{dev, a.N, a.K, a.R, xdt};
+    const Key key{dev, a.N, a.K, a.R, xdt, a.glu_act};
     auto it = cache.find(key);
     if (it != cache.end()) {
       p = it->second;
@@ -1104,8 +1154,10 @@ cudaError_t launch_mt(const QmvArgs& a, int xdt, cudaStream_t st, const Ws* give
       }
       p.M = (int)a.R;
       p.nc = (int)(a.K / kChunkCols);
-      p.nrt = (a.N + kTileRows - 1) / kTileRows;
+      p.nrt = kGlu ? (a.glu_cols + kTileRows / 2 - 1) / (kTileRows / 2) : (a.N + kTileRows - 1) / kTileRows;
       p.x_is_bf16 = xdt == kBF16;
+      p.glu_cols = a.glu_cols;
+      p.glu_act = a.glu_act;
       if (!make_plan(p, sms_of(dev), max_dyn)) return cudaErrorInvalidConfiguration;
       cache[key] = p;
       if (std::getenv("NVFP4_QMV_PLAN_LOG"))
@@ -1138,7 +1190,7 @@ cudaError_t launch_mt(const QmvArgs& a, int xdt, cudaStream_t st, const Ws* give
   else if ((e = get_workspace(dev, st, p.nrt, &ws)) != cudaSuccess)
     return e;
   CUtensorMap wmap, smap;
-  if ((e = plane_maps(a, &wmap, &smap)) != cudaSuccess) return e;
+  if ((e = plane_maps(a, &wmap, &smap, false, kGlu ? kTileRows / 2 : kTileRows)) != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(p.S * p.gs), 1, 1);
   cfg.blockDim = dim3(Geo<RT>::kThreads, 1, 1);
@@ -1263,6 +1315,20 @@ cudaError_t launch_qmv_stream(const QmvArgs& a, int xdt, cudaStream_t st) {
     b.x = static_cast<const uint16_t*>(a.x) + r0 * a.K;
     b.y = static_cast<uint16_t*>(a.y) + r0 * a.N;
     const cudaError_t e = launch_rows(b, xdt, st, nullptr);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+// Fused gate/up: 16 token rows per launch as for a plain call; y has
+// glu_cols columns.
+cudaError_t launch_qmv_stream_glu(const QmvArgs& a, int xdt, cudaStream_t st) {
+  for (int64_t r0 = 0; r0 < a.R; r0 += 16) {
+    QmvArgs b = a;
+    b.R = b.B = a.R - r0 < 16 ? a.R - r0 : 16;
+    b.x = static_cast<const uint16_t*>(a.x) + r0 * a.K;
+    b.y = static_cast<uint16_t*>(a.y) + r0 * a.glu_cols;
+    const cudaError_t e = b.R > 8 ? launch_mt<2, 2, true>(b, xdt, st) : launch_mt<1, 1, true>(b, xdt, st);
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;

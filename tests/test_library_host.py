@@ -76,6 +76,40 @@ def test_qmm_refusals(nv, kw, status):
     assert nv.library().nvfp4_last_error()
 
 
+def glu_call(nv, **kw):
+    args = dict(x=A, xdt=2, M=4, K=256, w=A, w_len=2 * 256 * 32, s=A, s_len=2 * 256 * 16, gs=None, gs_len=0,
+                I=256, act=2, y=A, route=0)
+    args.update(kw)
+    return nv.library().nvfp4_qmm_glu(args["x"], args["xdt"], args["M"], args["K"], args["w"], args["w_len"],
+                                      args["s"], args["s_len"], args["gs"], args["gs_len"], args["I"], args["act"],
+                                      args["y"], args["route"], None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(xdt=0), "ERR_DTYPE"),                                   # f32 activations
+    (dict(act=0), "ERR_DTYPE"),
+    (dict(act=3), "ERR_DTYPE"),
+    (dict(route=5), "ERR_DTYPE"),
+    (dict(w_len=256 * 32), "ERR_PLANE"),                          # plane of I rows, not 2 I
+    (dict(s_len=2 * 256 * 16 - 1), "ERR_PLANE"),
+    (dict(gs=A, gs_len=2), "ERR_GSCALE"),
+    (dict(I=-1), "ERR_SHAPE"),
+    (dict(K=24, w_len=2 * 256 * 3, s_len=2 * 256), "ERR_SHAPE"),  # K % 16 != 0
+    (dict(K=48, w_len=2 * 256 * 6, s_len=2 * 256 * 3, route=1), "ERR_SHAPE"),  # decode route needs K % 256
+    (dict(K=48, w_len=2 * 256 * 6, s_len=2 * 256 * 3, route=2), "ERR_SHAPE"),  # tensor cores need K % 32
+    (dict(y=U), "ERR_ALIGN"),
+    (dict(y=None), "ERR_NULL"),
+])
+def test_qmm_glu_refusals(nv, kw, status):
+    st = glu_call(nv, **kw)
+    assert nv.STATUS[st] == status, (st, nv.library().nvfp4_last_error())
+
+
+def test_qmm_glu_empty_returns_ok(nv):
+    assert glu_call(nv, M=0) == 0
+    assert glu_call(nv, I=0, w_len=0, s_len=0) == 0
+
+
 def test_empty_outputs_return_ok_without_launch(nv):
     assert qmm_call(nv, M=0) == 0
     assert qmm_call(nv, N=0, w_len=0, s_len=0) == 0
