@@ -482,6 +482,32 @@ def run_routes(nv, synth, torch, dev, stream, args):
                         "60_layers_ms_est": round(60 * ms_layer, 2)}
     del trip
 
+    # Fused gate/up with GeGLU on the gate/up plane [43008, 5376] (I = 21504):
+    # decode at M = 1 and 16 (bytes as for the plain call, output I wide) and
+    # prefill at M = 2048 (flops of the whole projection), beside the plain
+    # projection of the same plane.
+    n, k = 43008, 5376
+    (w, s), = rand_w(n, k, 1, seed=7)
+    gs = torch.from_numpy(synth.global_scales(g, 1)).to(dev)
+    glu = {}
+    for m in (1, 16, 2048):
+        x = synth.activations(g, (m, k), "bf16").to(dev)
+        yg = torch.empty((m, n // 2), dtype=torch.bfloat16, device=dev)
+        yp = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
+        ms_g = time_calls(torch, dev, stream, lambda i: nv.qmm_glu(x, w, s, gs=gs, act="gelu_tanh", out=yg), 5)
+        ms_p = time_calls(torch, dev, stream, lambda i: nv.qmm(x, w, s, gs=gs, out=yp), 5)
+        entry = {"us": round(ms_g * 1e3, 1), "plain_qmm_us": round(ms_p * 1e3, 1)}
+        if m >= 128:
+            tf = 2.0 * m * n * k / (ms_g * 1e-3) / 1e12
+            entry.update(TFLOPs=round(tf, 1), frac_bf16=round(tf / bf16_peak, 4))
+        else:
+            b = 0.5625 * n * k + 2 * m * k + 2 * m * (n // 2)
+            entry.update(GBps=round(b / (ms_g * 1e-3) / 1e9, 1), frac_hbm=round(b / (ms_g * 1e-3) / 1e9 / hbm_peak, 4))
+        glu[f"M{m}"] = entry
+        del x, yg, yp
+    out["gate_up_geglu_43008x5376"] = glu
+    del w, s
+
     # Dequantize the gate/up weight to bf16.
     n, k = 43008, 5376
     (w, s), = rand_w(n, k, 1, seed=5)

@@ -820,9 +820,9 @@ qmm_tc_kernel(const __grid_constant__ CUtensorMap xmap, const TcParams p) {
                 gv = __fmul_rn(gv, fac);
                 uv = __fmul_rn(uv, fac);
               }
-              const float a = p.glu_act == 1 ? gv / (1.0f + expf(-gv))
-                                             : 0.5f * gv * (1.0f + tanhf(0.7978845608028654f * (gv + 0.044715f * gv * gv * gv)));
-              o[e] = a * uv;
+              // SiLU: v sigmoid(v); GELU (tanh form): v sigmoid(2 sqrt(2/pi) (v + 0.044715 v^3))
+              const float z = p.glu_act == 1 ? gv : 1.5957691216057308f * (gv + 0.044715f * gv * gv * gv);
+              o[e] = __fdividef(gv, 1.0f + __expf(-z)) * uv;
             }
             const T t0 = Dt<T>::from_f32(o[0]), t1 = Dt<T>::from_f32(o[1]);
             packed[k] = (uint32_t)(*reinterpret_cast<const uint16_t*>(&t0)) |

@@ -611,9 +611,14 @@ __device__ __forceinline__ void store_out8(void* y, int is_bf16, int64_t idx, co
 // row yrow[s] with the expert's global scale. A GLU tile (kGlu) holds gate
 // sums in rows 0..127 and the matching up sums in rows 128..255 and writes
 // act(factor * gate) * (factor * up) to output columns 128 r .. 128 r + 127.
+// SiLU: v * sigmoid(v). GELU, tanh form: 0.5 v (1 + tanh(a)) with a =
+// sqrt(2/pi) (v + 0.044715 v^3), written as v * sigmoid(2 a) (the same value:
+// 0.5 (1 + tanh(a)) = 1 / (1 + exp(-2 a))). The fast exponential and divide
+// keep the single epilogue warp's per-output cost low; their error (a few
+// f32 ulp) is far below the output's 16-bit rounding.
 __device__ __forceinline__ float glu_act(int act, float v) {
-  if (act == 1) return v / (1.0f + expf(-v));                                            // SiLU
-  return 0.5f * v * (1.0f + tanhf(0.7978845608028654f * (v + 0.044715f * v * v * v)));  // GELU, tanh form
+  const float z = act == 1 ? v : 1.5957691216057308f * (v + 0.044715f * v * v * v);
+  return __fdividef(v, 1.0f + __expf(-z));
 }
 
 template <bool kGrp, bool kGlu>
