@@ -508,6 +508,27 @@ def run_routes(nv, synth, torch, dev, stream, args):
     out["gate_up_geglu_43008x5376"] = glu
     del w, s
 
+    # Batched weights: 8 MoE-expert gate/up planes [1536, 2048], 4 token rows
+    # each, as one expert-group launch and as one call per batch.
+    bt, m, n, k = 8, 4, 1536, 2048
+    wb = torch.randint(-2**31, 2**31 - 1, (bt, n, k // 8), dtype=torch.int32, device=dev)
+    sb = torch.from_numpy(synth.log_uniform_scales(g, (bt, n, k // 16), 2.0**-6, 4.0)).to(dev)
+    gsb = torch.from_numpy(synth.global_scales(g, bt)).to(dev)
+    xb = synth.activations(g, (bt * m, k), "bf16").reshape(bt, m, k).to(dev)
+    yb = torch.empty((bt, m, n), dtype=torch.bfloat16, device=dev)
+    ms_one = time_calls(torch, dev, stream, lambda i: nv.qmm_batched(xb, wb, sb, gs=gsb, out=yb), 10)
+    prev = os.environ.get("NVFP4_QMV_GROUP")
+    os.environ["NVFP4_QMV_GROUP"] = "0"
+    ms_loop = time_calls(torch, dev, stream, lambda i: nv.qmm_batched(xb, wb, sb, gs=gsb, out=yb), 10)
+    if prev is None:
+        os.environ.pop("NVFP4_QMV_GROUP")
+    else:
+        os.environ["NVFP4_QMV_GROUP"] = prev
+    bb = bt * (0.5625 * n * k + 2 * m * k + 2 * m * n)
+    out["qmm_batched_8x1536x2048_M4"] = {"us": round(ms_one * 1e3, 1), "GBps": round(bb / (ms_one * 1e-3) / 1e9, 1),
+                                          "per_batch_calls_us": round(ms_loop * 1e3, 1)}
+    del wb, sb, xb, yb
+
     # Dequantize the gate/up weight to bf16.
     n, k = 43008, 5376
     (w, s), = rand_w(n, k, 1, seed=5)

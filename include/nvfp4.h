@@ -117,6 +117,21 @@ nvfp4_status nvfp4_qmm_routed(const void* x, nvfp4_dtype x_dtype, int64_t M, int
                               int64_t w_len, const uint8_t* scales, int64_t scales_len, const float* gs,
                               int64_t gs_len, int64_t N, void* y, nvfp4_route route, void* stream);
 
+/*
+ * QuantizedMatmul with batched weights (PR #2629 "ROCm native NVFP4",
+ * Numerical results: "qmm batched w"): y[b] = x[b] @ dequantize(w[b]).T *
+ * gs[b] / 2688 for b < batches.
+ *   x [batches, M, K] of x_dtype; w [batches, N, K/8]; scales [batches, N,
+ *   K/16]; gs NULL (gs_len 0) or [batches]; y [batches, M, N] of x_dtype.
+ * Below the crossover (16-bit x, K % 256 == 0, batches * M at most one row
+ * per SM) all batches go out as one launch of the expert-group decode route;
+ * otherwise one nvfp4_qmm per batch. Same refusals as nvfp4_qmm, with the
+ * plane lengths and gs_len checked per batch count.
+ */
+nvfp4_status nvfp4_qmm_batched(const void* x, nvfp4_dtype x_dtype, int64_t batches, int64_t M, int64_t K,
+                               const uint32_t* w, int64_t w_len, const uint8_t* scales, int64_t scales_len,
+                               const float* gs, int64_t gs_len, int64_t N, void* y, void* stream);
+
 /* Activation of the fused gate/up projection (nvfp4_qmm_glu). */
 typedef enum { NVFP4_ACT_SILU = 1, NVFP4_ACT_GELU_TANH = 2 } nvfp4_act;
 

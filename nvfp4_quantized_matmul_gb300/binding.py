@@ -33,6 +33,7 @@ SIGNATURES = {
     "nvfp4_qmm_crossover": (_I64, [_INT, _I64, _I64]),
     "nvfp4_qmm_noalloc": (_INT, [_P, _INT, _I64, _I64, _P, _I64, _P, _I64, _P, _I64, _I64, _P, _P]),
     "nvfp4_qmm_glu": (_INT, [_P, _INT, _I64, _I64, _P, _I64, _P, _I64, _P, _I64, _I64, _INT, _P, _INT, _P]),
+    "nvfp4_qmm_batched": (_INT, [_P, _INT, _I64, _I64, _I64, _P, _I64, _P, _I64, _P, _I64, _I64, _P, _P]),
     "nvfp4_gather_qmm": (_INT, [_P, _INT, _I64, _I64, _P, _P, _I64, _INT, _P, _I64, _P, _I64, _P, _I64,
                                 _I64, _I64, _P, _P]),
     "nvfp4_last_error": (ctypes.c_char_p, []),
@@ -156,6 +157,20 @@ def qmm(x, w, scales, gs=None, route="auto", out=None):
         out = torch.empty((m, n), dtype=x.dtype, device=x.device)
     check(_lib.nvfp4_qmm_routed(_ptr(x), DTYPE_CODE[x.dtype], m, k, _ptr(w), w.numel(), _ptr(scales),
                                 scales.numel(), _ptr(gs), _n(gs), n, _ptr(out), ROUTE_CODE[route], _stream(x)))
+    return out
+
+
+def qmm_batched(x, w, scales, gs=None, out=None):
+    """QuantizedMatmul with batched weights: ``x`` [B, M, K], ``w`` [B, N, K/8],
+    ``scales`` [B, N, K/16], ``gs`` None or [B] -> [B, M, N] in x's dtype."""
+    _cuda(x, w, scales)
+    bt, m, k = x.shape
+    n = w.shape[1]
+    gs = _gs_tensor(gs, x.device)
+    if out is None:
+        out = torch.empty((bt, m, n), dtype=x.dtype, device=x.device)
+    check(_lib.nvfp4_qmm_batched(_ptr(x), DTYPE_CODE[x.dtype], bt, m, k, _ptr(w), w.numel(), _ptr(scales),
+                                 scales.numel(), _ptr(gs), _n(gs), n, _ptr(out), _stream(x)))
     return out
 
 

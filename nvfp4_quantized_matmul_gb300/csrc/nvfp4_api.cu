@@ -317,6 +317,42 @@ nvfp4_status nvfp4_qmm_glu(const void* x, nvfp4_dtype x_dtype, int64_t M, int64_
   return cuda_status(fn, nvfp4::launch_qmv_stream_glu(a, (int)x_dtype, st));
 }
 
+nvfp4_status nvfp4_qmm_batched(const void* x, nvfp4_dtype x_dtype, int64_t batches, int64_t M, int64_t K,
+                               const uint32_t* w, int64_t w_len, const uint8_t* scales, int64_t scales_len,
+                               const float* gs, int64_t gs_len, int64_t N, void* y, void* stream) {
+  const char* fn = "nvfp4_qmm_batched";
+  if (!dtype_ok(x_dtype)) return fail(NVFP4_ERR_DTYPE, "%s: unknown activation dtype %d", fn, (int)x_dtype);
+  if (batches < 0 || M < 0) return fail(NVFP4_ERR_SHAPE, "%s: negative batch count or M", fn);
+  nvfp4_status s = check_planes(fn, w, w_len, scales, scales_len, batches, N, K);
+  if (s) return s;
+  if ((s = check_gs(fn, gs, gs_len, batches))) return s;
+  int64_t rows, xe;
+  if (!mul_ok(batches, M, &rows) || !mul_ok(rows, K, &xe) || !mul_ok(rows, N, &xe))
+    return fail(NVFP4_ERR_SHAPE, "%s: batches*M*K or batches*M*N overflows", fn);
+  if (rows == 0 || N == 0) return ok();
+  if (!y || (K > 0 && !x)) return fail(NVFP4_ERR_NULL, "%s: x or y is NULL", fn);
+  if (!aligned(x, 16) || !aligned(y, 16)) return fail(NVFP4_ERR_ALIGN, "%s: x and y must be 16-byte aligned", fn);
+  if (batches > INT32_MAX) return fail(NVFP4_ERR_LIMIT, "%s: more than 2^31-1 batches", fn);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (K == 0) return cuda_status(fn, cudaMemsetAsync(y, 0, (size_t)(rows * N * dtype_size(x_dtype)), st));
+  // Decode-size batches go out as one launch of the expert-group route: row
+  // r of the flattened [batches * M, K] activations uses batch r / M's plane.
+  if (x_dtype != NVFP4_F32 && M < nvfp4_qmm_crossover(x_dtype, N, K)) {
+    nvfp4::QmvArgs a{x, w, scales, gs, nullptr, nullptr, rows, rows, K, N, batches, y};
+    a.rows_per_expert = M;
+    if (nvfp4::qmv_group_supported(a, (int)x_dtype)) return cuda_status(fn, nvfp4::launch_qmv_group(a, (int)x_dtype, st));
+  }
+  // Otherwise one QuantizedMatmul per batch, each on its own route.
+  const int64_t xs = dtype_size(x_dtype);
+  for (int64_t b = 0; b < batches; ++b) {
+    s = nvfp4_qmm(static_cast<const char*>(x) + b * M * K * xs, x_dtype, M, K, w + b * N * (K / 8), N * (K / 8),
+                  scales + b * N * (K / 16), N * (K / 16), gs ? gs + b : nullptr, gs ? 1 : 0, N,
+                  static_cast<char*>(y) + b * M * N * xs, stream);
+    if (s) return s;
+  }
+  return ok();
+}
+
 nvfp4_status nvfp4_qmm_noalloc(const void* x, nvfp4_dtype x_dtype, int64_t M, int64_t K, const uint32_t* w,
                                int64_t w_len, const uint8_t* scales, int64_t scales_len, const float* gs,
                                int64_t gs_len, int64_t N, void* y, void* stream) {

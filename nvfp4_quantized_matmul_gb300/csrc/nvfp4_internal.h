@@ -33,6 +33,9 @@ struct QmvArgs {
   // act(gate) * up; glu_act 1 = SiLU, 2 = GELU (tanh form); 0 = plain call.
   int64_t glu_cols = 0;
   int glu_act = 0;
+  // Batched weights: with rhs null, row r uses expert r / rows_per_expert
+  // (the expert-group route only).
+  int64_t rows_per_expert = 0;
 };
 cudaError_t launch_qmv(const QmvArgs& a, int xdt, cudaStream_t st);
 

@@ -774,7 +774,8 @@ __device__ void group_rows(const QmvArgs& a, uint8_t* scratch, int64_t* yrow, in
   int* lead = rank + R;                                  // first row of its expert
   int* base = lead + R;                                  // on a first row: the expert's first group id
   for (int t = tid; t < R; t += kT) {
-    const uint32_t e = __ldg(a.rhs + t);
+    // batched weights: consecutive runs of rows_per_expert rows per expert
+    const uint32_t e = a.rows_per_expert > 0 ? (uint32_t)(t / a.rows_per_expert) : __ldg(a.rhs + t);
     const uint32_t xr = a.lhs ? __ldg(a.lhs + t) : (uint32_t)t;
     key[t] = (int64_t)e < a.E && (int64_t)xr < a.B ? e : kNoExpert;
   }
@@ -1270,7 +1271,8 @@ bool group_plan(const QmvArgs& a, int xdt, int dev, SPlan* out) {
 bool qmv_group_supported(const QmvArgs& a, int xdt) {
   if (const char* ev = std::getenv("NVFP4_QMV_GROUP"))
     if (ev[0] == '0') return false;
-  if (xdt == kF32 || a.rhs == nullptr || a.R < 1 || a.K % kChunkCols != 0 || a.K <= 0 || a.N <= 0 ||
+  if (xdt == kF32 || (a.rhs == nullptr && a.rows_per_expert <= 0) || a.R < 1 || a.K % kChunkCols != 0 || a.K <= 0 ||
+      a.N <= 0 ||
       a.N >= (1ll << 31) || a.K / kChunkCols > 4096 || a.E < 1 || a.E >= (1ll << 31))
     return false;
   int dev = 0;

@@ -105,6 +105,21 @@ def test_qmm_glu_refusals(nv, kw, status):
     assert nv.STATUS[st] == status, (st, nv.library().nvfp4_last_error())
 
 
+def test_qmm_batched_refusals(nv):
+    lib = nv.library()
+    ST = nv.STATUS
+    # 3 batches of [64, 256]: planes of 3 * 64 * 32 words and 3 * 64 * 16 bytes
+    call = lambda **kw: lib.nvfp4_qmm_batched(
+        A, kw.get("xdt", 2), 3, 4, 256, A, kw.get("w_len", 3 * 64 * 32), A, kw.get("s_len", 3 * 64 * 16),
+        kw.get("gs", None), kw.get("gs_len", 0), 64, kw.get("y", A), None)
+    assert ST[call(w_len=2 * 64 * 32)] == "ERR_PLANE"
+    assert ST[call(s_len=3 * 64 * 16 + 1)] == "ERR_PLANE"
+    assert ST[call(gs=A, gs_len=1)] == "ERR_GSCALE"       # one scale per batch
+    assert ST[call(xdt=5)] == "ERR_DTYPE"
+    assert ST[call(y=U)] == "ERR_ALIGN"
+    assert lib.nvfp4_qmm_batched(A, 2, 0, 4, 256, A, 0, A, 0, None, 0, 64, A, None) == 0  # no batches
+
+
 def test_qmm_glu_empty_returns_ok(nv):
     assert glu_call(nv, M=0) == 0
     assert glu_call(nv, I=0, w_len=0, s_len=0) == 0
