@@ -47,8 +47,8 @@ METRIC = "qmv HBM GB/s & µs/call, qmm TFLOP/s; fraction of GB300 roofline (1 GP
 # step, from the ncu capture summarised in
 # profiles/qmv_stream_kernel_decode_step.md (`--case decode_step`); reported
 # per launch, and only while the kernel sources still hash to kernel_sha.
-TRAFFIC = {"source": "profiles/qmv_stream_kernel_decode_step.md", "kernel_sha": "e04151b079be5df7",
-           "bytes_per_step": 1123782400}
+TRAFFIC = {"source": "profiles/qmv_stream_kernel_decode_step.md", "kernel_sha": "ad82ae626227d1a3",
+           "bytes_per_step": 1124401408}
 TRAFFIC_FILES = ("nvfp4_qmv_stream.cu", "nvfp4_qmv_common.cuh", "nvfp4_common.cuh", "nvfp4_pipe.cuh")
 
 
