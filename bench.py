@@ -529,6 +529,31 @@ def run_routes(nv, synth, torch, dev, stream, args):
                                           "per_batch_calls_us": round(ms_loop * 1e3, 1)}
     del wb, sb, xb, yb
 
+    # Non-transposed weights: the MLP up projection's sizes (K = 5376 inputs,
+    # N = 21504 outputs) stored [K, N/8] and quantized along N, beside the
+    # transposed plane of the same sizes through nv.qmm.
+    k, n = 5376, 21504
+    wt = torch.randint(-2**31, 2**31 - 1, (k, n // 8), dtype=torch.int32, device=dev)
+    stt = torch.from_numpy(synth.log_uniform_scales(g, (k, n // 16), 2.0**-6, 4.0)).to(dev)
+    (w, s), = rand_w(n, k, 1, seed=9)
+    ntr = {}
+    for m in (1, 16, 2048):
+        x = synth.activations(g, (m, k), "bf16").to(dev)
+        y = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
+        ms_nt = time_calls(torch, dev, stream, lambda i: nv.qmm_nontransposed(x, wt, stt, out=y), 5)
+        ms_t = time_calls(torch, dev, stream, lambda i: nv.qmm(x, w, s, out=y), 5)
+        entry = {"us": round(ms_nt * 1e3, 1), "transposed_qmm_us": round(ms_t * 1e3, 1)}
+        if m >= 128:
+            tf = 2.0 * m * n * k / (ms_nt * 1e-3) / 1e12
+            entry.update(TFLOPs=round(tf, 1), frac_bf16=round(tf / bf16_peak, 4))
+        else:
+            b = 0.5625 * n * k + 2 * m * k + 2 * m * n
+            entry.update(GBps=round(b / (ms_nt * 1e-3) / 1e9, 1), frac_hbm=round(b / (ms_nt * 1e-3) / 1e9 / hbm_peak, 4))
+        ntr[f"M{m}"] = entry
+        del x, y
+    out["qmm_nontransposed_5376x21504"] = ntr
+    del wt, stt, w, s
+
     # Dequantize the gate/up weight to bf16.
     n, k = 43008, 5376
     (w, s), = rand_w(n, k, 1, seed=5)

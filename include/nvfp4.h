@@ -118,6 +118,29 @@ nvfp4_status nvfp4_qmm_routed(const void* x, nvfp4_dtype x_dtype, int64_t M, int
                               int64_t gs_len, int64_t N, void* y, nvfp4_route route, void* stream);
 
 /*
+ * QuantizedMatmul with a non-transposed weight (PR #2629, Changes during
+ * review and Review findings: the quantized axis of such a weight is N, so
+ * the multiple-of-16 rule moves from K to N and x [1, 17] against a [17, 32]
+ * weight is valid): y = x @ dequantize(w) * gs / 2688.
+ *   x [M, K] of x_dtype (f16 or bf16; f32 is refused with ERR_DTYPE), any
+ *   K >= 0; w [K, N/8] uint32 words, word j of row k holding outputs
+ *   8j..8j+7 of input k (low nibble first); scales [K, N/16] E4M3 bytes, one
+ *   per 16 outputs of an input; gs NULL (gs_len 0) or one float; y [M, N] of
+ *   x_dtype. N % 16 == 0 (ERR_SHAPE otherwise). x, y, w and scales 16-byte
+ *   aligned (ERR_ALIGN). M == 0 or N == 0 returns OK without a launch; K == 0
+ *   writes zeros.
+ * One route for every M, as on the pages (the dequantize + GEMM route): the
+ * tcgen05 tensor-core kernel, whose producer warps decode and transpose the
+ * weight tiles into shared memory. With K % 8 != 0 the activations are first
+ * copied, rows padded with zeros to a multiple of 8 elements, into the
+ * per-stream buffer of the gathered activations (grown on demand, freed by
+ * nvfp4_shutdown()).
+ */
+nvfp4_status nvfp4_qmm_nontransposed(const void* x, nvfp4_dtype x_dtype, int64_t M, int64_t K, const uint32_t* w,
+                                     int64_t w_len, const uint8_t* scales, int64_t scales_len, const float* gs,
+                                     int64_t gs_len, int64_t N, void* y, void* stream);
+
+/*
  * QuantizedMatmul with batched weights (PR #2629 "ROCm native NVFP4",
  * Numerical results: "qmm batched w"): y[b] = x[b] @ dequantize(w[b]).T *
  * gs[b] / 2688 for b < batches.

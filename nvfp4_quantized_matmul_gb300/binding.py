@@ -34,6 +34,7 @@ SIGNATURES = {
     "nvfp4_qmm_noalloc": (_INT, [_P, _INT, _I64, _I64, _P, _I64, _P, _I64, _P, _I64, _I64, _P, _P]),
     "nvfp4_qmm_glu": (_INT, [_P, _INT, _I64, _I64, _P, _I64, _P, _I64, _P, _I64, _I64, _INT, _P, _INT, _P]),
     "nvfp4_qmm_batched": (_INT, [_P, _INT, _I64, _I64, _I64, _P, _I64, _P, _I64, _P, _I64, _I64, _P, _P]),
+    "nvfp4_qmm_nontransposed": (_INT, [_P, _INT, _I64, _I64, _P, _I64, _P, _I64, _P, _I64, _I64, _P, _P]),
     "nvfp4_gather_qmm": (_INT, [_P, _INT, _I64, _I64, _P, _P, _I64, _INT, _P, _I64, _P, _I64, _P, _I64,
                                 _I64, _I64, _P, _P]),
     "nvfp4_last_error": (ctypes.c_char_p, []),
@@ -171,6 +172,21 @@ def qmm_batched(x, w, scales, gs=None, out=None):
         out = torch.empty((bt, m, n), dtype=x.dtype, device=x.device)
     check(_lib.nvfp4_qmm_batched(_ptr(x), DTYPE_CODE[x.dtype], bt, m, k, _ptr(w), w.numel(), _ptr(scales),
                                  scales.numel(), _ptr(gs), _n(gs), n, _ptr(out), _stream(x)))
+    return out
+
+
+def qmm_nontransposed(x, w, scales, gs=None, out=None):
+    """QuantizedMatmul with a non-transposed weight: ``w`` [K, N/8] quantized
+    along N, ``scales`` [K, N/16]; returns x @ dequantize(w) * gs/2688, [M, N]
+    in x's dtype."""
+    _cuda(x, w, scales)
+    m, k = x.shape
+    n = w.shape[1] * 8
+    gs = _gs_tensor(gs, x.device)
+    if out is None:
+        out = torch.empty((m, n), dtype=x.dtype, device=x.device)
+    check(_lib.nvfp4_qmm_nontransposed(_ptr(x), DTYPE_CODE[x.dtype], m, k, _ptr(w), w.numel(), _ptr(scales),
+                                       scales.numel(), _ptr(gs), _n(gs), n, _ptr(out), _stream(x)))
     return out
 
 

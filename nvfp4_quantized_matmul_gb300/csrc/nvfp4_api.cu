@@ -317,6 +317,30 @@ nvfp4_status nvfp4_qmm_glu(const void* x, nvfp4_dtype x_dtype, int64_t M, int64_
   return cuda_status(fn, nvfp4::launch_qmv_stream_glu(a, (int)x_dtype, st));
 }
 
+nvfp4_status nvfp4_qmm_nontransposed(const void* x, nvfp4_dtype x_dtype, int64_t M, int64_t K, const uint32_t* w,
+                                     int64_t w_len, const uint8_t* scales, int64_t scales_len, const float* gs,
+                                     int64_t gs_len, int64_t N, void* y, void* stream) {
+  const char* fn = "nvfp4_qmm_nontransposed";
+  if (x_dtype != NVFP4_F16 && x_dtype != NVFP4_BF16)
+    return fail(NVFP4_ERR_DTYPE, "%s: f16 or bf16 activations only (got %d)", fn, (int)x_dtype);
+  if (M < 0 || K < 0 || N < 0) return fail(NVFP4_ERR_SHAPE, "%s: negative size", fn);
+  // the quantized axis of a non-transposed plane is N
+  if (N % 16) return fail(NVFP4_ERR_SHAPE, "%s: N=%" PRId64 " (the quantized axis) is not a multiple of 16", fn, N);
+  nvfp4_status s = check_planes(fn, w, w_len, scales, scales_len, 1, K, N);  // [K, N/8] words, [K, N/16] scales
+  if (s) return s;
+  if ((s = check_gs(fn, gs, gs_len, 1))) return s;
+  int64_t xe;
+  if (!mul_ok(M, K, &xe) || !mul_ok(M, N, &xe)) return fail(NVFP4_ERR_SHAPE, "%s: M*K or M*N overflows", fn);
+  if (M == 0 || N == 0) return ok();
+  if (!y || (K > 0 && !x)) return fail(NVFP4_ERR_NULL, "%s: x or y is NULL", fn);
+  if (!aligned(x, 16) || !aligned(y, 16)) return fail(NVFP4_ERR_ALIGN, "%s: x and y must be 16-byte aligned", fn);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (K == 0) return cuda_status(fn, cudaMemsetAsync(y, 0, (size_t)(M * N * dtype_size(x_dtype)), st));
+  if (!nvfp4::qmm_tc_nt_supported(M, N, K))
+    return fail(NVFP4_ERR_LIMIT, "%s: M or K of 2^31 or more, or too many tiles", fn);
+  return cuda_status(fn, nvfp4::launch_qmm_tc_nt(x, (int)x_dtype, M, K, w, scales, gs, N, y, st));
+}
+
 nvfp4_status nvfp4_qmm_batched(const void* x, nvfp4_dtype x_dtype, int64_t batches, int64_t M, int64_t K,
                                const uint32_t* w, int64_t w_len, const uint8_t* scales, int64_t scales_len,
                                const float* gs, int64_t gs_len, int64_t N, void* y, void* stream) {

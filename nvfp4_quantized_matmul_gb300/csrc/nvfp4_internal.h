@@ -83,6 +83,11 @@ cudaError_t launch_qmm_tc(const void* x, int xdt, int64_t M, int64_t K, const ui
 // rows), y [M, cols] = act(gate) * up; act 1 = SiLU, 2 = GELU (tanh form).
 cudaError_t launch_qmm_tc_glu(const void* x, int xdt, int64_t M, int64_t K, const uint32_t* w, const uint8_t* scales,
                               const float* gs, int64_t cols, int act, void* y, cudaStream_t st);
+// Non-transposed weights: w is [K, N/8] words quantized along N (N % 16 ==
+// 0, any K >= 1), y = x @ dequantize(w) * gs/2688; f16 or bf16 x.
+bool qmm_tc_nt_supported(int64_t M, int64_t N, int64_t K);
+cudaError_t launch_qmm_tc_nt(const void* x, int xdt, int64_t M, int64_t K, const uint32_t* w, const uint8_t* scales,
+                             const float* gs, int64_t N, void* y, cudaStream_t st);
 // Expert-batched GatherQMM on the tensor cores, for rows sorted by expert.
 bool gather_tc_supported(int64_t B, int64_t K, int64_t R, int64_t E, int64_t N);
 cudaError_t launch_gather_tc(const void* x, int xdt, int64_t B, int64_t K, const uint32_t* lhs, const uint32_t* rhs,

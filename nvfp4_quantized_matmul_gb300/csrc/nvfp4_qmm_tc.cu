@@ -438,6 +438,109 @@ __device__ void producer_role(const TcParams& p, uint32_t sB, uint32_t bars, vol
   }
 }
 
+// ---------------------------------------------------------------- non-transposed weights
+//
+// A non-transposed plane is quantized along the output axis (mlx PR #2629,
+// Changes during review: the K-multiple-of-16 rule applies to N when the
+// weight is not transposed): word w[k][j] holds outputs 8j..8j+7 of input k,
+// one scale byte per 16 outputs of an input, and y = x @ dequantize(w). The
+// tensor cores still take K-major weight tiles, so the producer transposes
+// while it decodes: producer warp v takes inputs 8v..8v+7 of the k-block and
+// lane j word column j of the tile; per output it then holds eight
+// consecutive k values, which is one 16-byte chunk of the output's swizzled
+// B row. Lane j starts at output (j & 7) of its word (the word is rotated by
+// that many nibbles before decoding), so the eight lanes of a quarter-warp
+// store to eight different 16-byte bank groups.
+
+struct WTaskNT {
+  uint32_t w[8];  // inputs k0..k0+7 of the lane's word column
+  uint32_t s[2];  // their scale bytes (four per word, lowest input first)
+};
+
+template <int BM>
+__device__ __forceinline__ void w_load_nt(WTaskNT& t, const WCursor& cur, const TcParams& p, int v, int j) {
+  if (cur.done) return;
+  const int64_t nwords = p.N / 8, ngroups = p.N / 16;
+  const int64_t col = (int64_t)cur.nt * 32 + j;
+  const bool cok = col < nwords;
+  const int64_t k0 = (int64_t)cur.kb * BK + 8 * v;
+  uint32_t s0 = 0, s1 = 0;
+#pragma unroll
+  for (int kk = 0; kk < 8; ++kk) {
+    const int64_t k = k0 + kk;
+    const bool ok = cok && k < p.K;  // inputs past K decode to +0
+    t.w[kk] = ok ? __ldg(p.w + k * nwords + col) : 0u;
+    const uint32_t sb = ok ? (uint32_t)__ldg(p.scales + k * ngroups + (col >> 1)) : 0u;
+    if (kk < 4) s0 |= sb << (8 * kk); else s1 |= sb << (8 * (kk - 4));
+  }
+  t.s[0] = s0;
+  t.s[1] = s1;
+}
+
+template <typename T>
+__device__ __forceinline__ void w_store_nt(uint32_t stage_base, int v, int j, const WTaskNT& t) {
+  const int rot = j & 7;
+  uint32_t o[8][4];
+#pragma unroll
+  for (int kk = 0; kk < 8; ++kk) {
+    const uint32_t sb = (t.s[kk >> 2] >> (8 * (kk & 3))) & 0xFFu;
+    Dt<T>::decode(__funnelshift_r(t.w[kk], t.w[kk], 4 * rot), Dt<T>::scale(sb), o[kk]);
+  }
+  const uint32_t rows = stage_base + (uint32_t)j * 1024u;  // B rows 8j..8j+7
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    const uint32_t oc = (uint32_t)((c + rot) & 7);  // output 8j + oc of the tile
+    const uint32_t sel = (c & 1) ? 0x7632u : 0x5410u;
+    uint32_t q[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) q[i] = __byte_perm(o[2 * i][c >> 1], o[2 * i + 1][c >> 1], sel);
+    const uint32_t addr = rows + oc * 128u + (((uint32_t)v ^ oc) * 16u);
+    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(q[0]), "r"(q[1]), "r"(q[2]), "r"(q[3])
+                 : "memory");
+  }
+}
+
+template <typename T, typename C>
+__device__ void producer_role_nt(const TcParams& p, uint32_t sB, uint32_t bars, volatile int* abort_flag,
+                                 int num_tiles) {
+  static_assert(C::BN == 256 && kProducerWarps * 8 == BK, "one word column per lane, eight inputs per warp");
+  // three k-blocks of words in flight (ten registers each); four spill in the
+  // 640-thread configuration
+  constexpr int STAGES = C::STAGES, PF = 3, BM = C::BM;
+  const int v = (int)(threadIdx.x >> 5) - C::kWarpProd0;
+  const int j = threadIdx.x & 31;
+  WCursor ld{(int)blockIdx.x, 0, true, 0, 0};
+  w_seek<false, BM>(ld, p, num_tiles, nullptr, nullptr);
+  WTaskNT buf[PF];
+#pragma unroll
+  for (int i = 0; i < PF - 1; ++i) {
+    w_load_nt<BM>(buf[i], ld, p, v, j);
+    w_advance<false, BM>(ld, p, num_tiles, nullptr, nullptr);
+  }
+  uint32_t u = 0;
+  const int total = ((num_tiles - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x) * p.num_kb;
+  auto consume = [&](const WTaskNT& t) -> bool {
+    const int s = (int)(u % STAGES);
+    const uint32_t ph = (u / STAGES) & 1;
+    if (!wait_bar_warp(bars + 8 * (2 * STAGES + s), ph ^ 1, abort_flag, 3, &g_tc_error)) return false;  // stage empty
+    w_store_nt<T>(sB + (uint32_t)s * C::B_BYTES, v, j, t);
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    __syncwarp();
+    if (j == 0) mbar_arrive(bars + 8 * (STAGES + s));  // fullB
+    ++u;
+    return true;
+  };
+  for (int i = 0; i < total; i += PF) {
+#pragma unroll
+    for (int q = 0; q < PF; ++q) {
+      if (i + q >= total) return;
+      w_load_nt<BM>(buf[(q + PF - 1) % PF], ld, p, v, j);
+      w_advance<false, BM>(ld, p, num_tiles, nullptr, nullptr);
+      if (!consume(buf[q])) return;
+    }
+  }
+}
+
 // ---------------------------------------------------------------- stream-K variants
 //
 // The stream-K kernel walks units (tile, k-block range) instead of whole
@@ -592,7 +695,7 @@ __device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* map
 
 // ---------------------------------------------------------------- kernel
 
-template <typename T, typename C, bool GATHER, bool kGlu = false>
+template <typename T, typename C, bool GATHER, bool kGlu = false, bool kNT = false>
 __global__ void __launch_bounds__(C::THREADS, 1)
 qmm_tc_kernel(const __grid_constant__ CUtensorMap xmap, const TcParams p) {
   constexpr int STAGES = C::STAGES, MH = C::MH, BN = C::BN, BM = C::BM, NBUF = C::ACC_BUFS;
@@ -882,7 +985,10 @@ qmm_tc_kernel(const __grid_constant__ CUtensorMap xmap, const TcParams p) {
       if (lane == 0) mbar_arrive(accEmpty(b));
     }
   } else if (warp >= C::kWarpProd0) {
-    producer_role<T, C, GATHER, kGlu>(p, sB, bars, abort_flag, num_tiles, seg, pre);
+    if constexpr (kNT)
+      producer_role_nt<T, C>(p, sB, bars, abort_flag, num_tiles);
+    else
+      producer_role<T, C, GATHER, kGlu>(p, sB, bars, abort_flag, num_tiles, seg, pre);
   }
 
   tc_fence_before();
@@ -1598,6 +1704,81 @@ cudaError_t launch_gather_t(const void* x, int64_t B, int64_t K, const uint32_t*
   return launch_gather<T, Tile256x256>(x, B, K, lhs, rhs, R, w, scales, gs, E, N, y, st);
 }
 
+// Activations whose rows are not a multiple of 16 bytes (K % 8 != 0) cannot
+// be a TMA source: they are copied with rows of kp >= K elements, the columns
+// past K set to +0.
+__global__ void __launch_bounds__(256) pad_cols_kernel(const uint16_t* __restrict__ x, int64_t M, int64_t K, int64_t kp,
+                                                       uint16_t* __restrict__ xp) {
+  const int64_t n = M * kp;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t m = i / kp, c = i - m * kp;
+    xp[i] = c < K ? x[m * K + c] : (uint16_t)0;
+  }
+}
+
+// Non-transposed weights ([K, N/8] words, scales along N): whole tiles dealt
+// round robin to a persistent grid; 128-row tiles while M fits one.
+template <typename T, typename C>
+cudaError_t launch_nt_cfg(const void* x, int64_t M, int64_t K, const uint32_t* w, const uint8_t* scales,
+                          const float* gs, int64_t N, void* y, int sms, cudaStream_t st) {
+  auto enc = encode_fn();
+  if (!enc) return cudaErrorNotSupported;
+  const void* xa = x;
+  int64_t kx = K;
+  if (K % 8) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    kx = (K + 7) / 8 * 8;
+    void* xp = nullptr;
+    cudaError_t e = gather_buffer(dev, st, (size_t)M * (size_t)kx * 2, &xp);
+    if (e != cudaSuccess) return e;
+    const int64_t blocks = (M * kx + 255) / 256;
+    pad_cols_kernel<<<(unsigned)(blocks < 4 * sms ? blocks : 4 * sms), 256, 0, st>>>(
+        static_cast<const uint16_t*>(x), M, K, kx, static_cast<uint16_t*>(xp));
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    xa = xp;
+  }
+  CUtensorMap map;
+  const cuuint64_t dims[2] = {(cuuint64_t)kx, (cuuint64_t)M};
+  const cuuint64_t strides[1] = {(cuuint64_t)kx * 2};
+  const cuuint32_t box[2] = {BK, 128};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUtensorMapDataType dt =
+      std::is_same<T, __nv_bfloat16>::value ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  CUresult r = enc(&map, dt, 2, const_cast<void*>(xa), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  TcParams p;
+  p.w = w;
+  p.scales = scales;
+  p.gs = gs;
+  p.y = y;
+  p.M = M;
+  p.N = N;
+  p.K = K;
+  p.num_m_tiles = (int)((M + C::BM - 1) / C::BM);
+  p.num_n_tiles = (int)((N + C::BN - 1) / C::BN);
+  p.num_tiles = p.num_m_tiles * p.num_n_tiles;
+  p.num_kb = (int)((K + BK - 1) / BK);
+  p.lhs = nullptr;
+  p.rhs = nullptr;
+  p.B = M;
+  p.E = 1;
+  p.xcontig = 1;
+  p.dp_tiles = p.num_tiles;
+  p.sk_tiles = 0;
+  p.ws = nullptr;
+  p.ws_cnt = nullptr;
+  p.glu_cols = 0;
+  p.glu_act = 0;
+  const int grid = p.num_tiles < sms ? p.num_tiles : sms;
+  auto kern = qmm_tc_kernel<T, C, false, false, true>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
+  if (e != cudaSuccess) return e;
+  kern<<<grid, C::THREADS, C::SMEM, st>>>(map, p);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 bool gather_tc_supported(int64_t B, int64_t K, int64_t R, int64_t E, int64_t N) {
@@ -1623,6 +1804,23 @@ cudaError_t launch_qmm_tc_glu(const void* x, int xdt, int64_t M, int64_t K, cons
                     : launch_glu_cfg<__nv_bfloat16, Tile256x256>(x, M, K, w, scales, gs, cols, act, y, sms, st);
   return M <= 128 ? launch_glu_cfg<__half, Tile128x256>(x, M, K, w, scales, gs, cols, act, y, sms, st)
                   : launch_glu_cfg<__half, Tile256x256>(x, M, K, w, scales, gs, cols, act, y, sms, st);
+}
+
+bool qmm_tc_nt_supported(int64_t M, int64_t N, int64_t K) {
+  return M > 0 && N > 0 && N % 16 == 0 && K > 0 && M < (1ll << 31) && K < (1ll << 31) &&
+         (M + 127) / 128 * ((N + 255) / 256) < (1ll << 31);
+}
+
+cudaError_t launch_qmm_tc_nt(const void* x, int xdt, int64_t M, int64_t K, const uint32_t* w, const uint8_t* scales,
+                             const float* gs, int64_t N, void* y, cudaStream_t st) {
+  int dev = 0, sms = 152;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (xdt == kBF16)
+    return M <= 128 ? launch_nt_cfg<__nv_bfloat16, Tile128x256>(x, M, K, w, scales, gs, N, y, sms, st)
+                    : launch_nt_cfg<__nv_bfloat16, Tile256x256>(x, M, K, w, scales, gs, N, y, sms, st);
+  return M <= 128 ? launch_nt_cfg<__half, Tile128x256>(x, M, K, w, scales, gs, N, y, sms, st)
+                  : launch_nt_cfg<__half, Tile256x256>(x, M, K, w, scales, gs, N, y, sms, st);
 }
 
 bool tc_stream_k() {

@@ -36,7 +36,8 @@ Parity status: every function here is pinned by ``tests/test_oracle_pins.py``
 exact-rational brute force, sidecar identity against the ModelOpt formula,
 zero rows; the gated-MLP activations against their symmetry identities, the
 exact erf GELU and the library sigmoid, and the gate/up halves through
-one-hot products). The equivalence of ModelOpt's on-disk nibble order with the MLX
+one-hot products; the non-transposed product against an exact-rational
+brute force indexed [input, output] and through identity activations). The equivalence of ModelOpt's on-disk nibble order with the MLX
 order is taken from the page ("likely matches") and is parity unpinned: no
 real checkpoint is available to confirm it.
 """
@@ -145,6 +146,30 @@ def qmm(x, w, scales, gs=None) -> np.ndarray:
     deq = block_values(w, scales)
     y = xd @ deq.T
     return y * np.float64(global_factor(gs))
+
+
+def qmm_nontransposed(x, w, scales, gs=None) -> np.ndarray:
+    """QuantizedMatmul with a non-transposed weight: ``w`` is ``[K, N/8]``,
+    quantized along its last axis N (PR #2629, Changes during review: the
+    multiple-of-16 rule applies to N when the weight is not transposed), and
+    ``y = factor * (x @ (fp4 * e4m3))``, ``[M, N]`` in float64."""
+    xd = np.asarray(x, dtype=np.float64)
+    deq = block_values(w, scales)  # [K, N]
+    y = xd @ deq
+    return y * np.float64(global_factor(gs))
+
+
+def qmm_nontransposed_entries(x, w, scales, gs, rows, cols) -> np.ndarray:
+    """Selected outputs ``y[rows[i], cols[i]]`` of :func:`qmm_nontransposed`,
+    one dot product each (output n reads word column n // 8 of every input)."""
+    xd = np.asarray(x, dtype=np.float64)
+    fac = np.float64(global_factor(gs))
+    out = np.empty(len(rows), dtype=np.float64)
+    for i, (m, n) in enumerate(zip(rows, cols)):
+        g = int(n) // 16  # the 16-output block: two words, one scale byte per input
+        deq = block_values(w[:, 2 * g:2 * g + 2], scales[:, g:g + 1])[:, int(n) - 16 * g]
+        out[i] = float(np.dot(xd[m], deq)) * fac
+    return out
 
 
 def qmm_entries(x, w, scales, gs, rows, cols) -> np.ndarray:

@@ -120,6 +120,27 @@ def test_qmm_batched_refusals(nv):
     assert lib.nvfp4_qmm_batched(A, 2, 0, 4, 256, A, 0, A, 0, None, 0, 64, A, None) == 0  # no batches
 
 
+def test_qmm_nontransposed_refusals(nv):
+    lib = nv.library()
+    ST = nv.STATUS
+    # x [4, 17] against a [17, 32] weight: 17 * 4 words, 17 * 2 scale bytes
+    def call(**kw):
+        a = dict(x=A, xdt=2, M=4, K=17, w=A, w_len=17 * 4, s=A, s_len=17 * 2, gs=None, gs_len=0, N=32, y=A)
+        a.update(kw)
+        return ST[lib.nvfp4_qmm_nontransposed(a["x"], a["xdt"], a["M"], a["K"], a["w"], a["w_len"], a["s"],
+                                              a["s_len"], a["gs"], a["gs_len"], a["N"], a["y"], None)]
+    assert call(N=24, w_len=17 * 3, s_len=17) == "ERR_SHAPE"   # the quantized axis N % 16 != 0
+    assert call(xdt=0) == "ERR_DTYPE"                          # f32 activations
+    assert call(w_len=17 * 4 - 1) == "ERR_PLANE"
+    assert call(s_len=32 * 2) == "ERR_PLANE"                   # a plane laid out [N, K/16]
+    assert call(gs=A, gs_len=2) == "ERR_GSCALE"
+    assert call(y=U) == "ERR_ALIGN"
+    assert call(x=None) == "ERR_NULL"
+    assert call(M=-1) == "ERR_SHAPE"
+    assert call(M=0) == "OK"
+    assert call(N=0, w_len=0, s_len=0) == "OK"
+
+
 def test_qmm_glu_empty_returns_ok(nv):
     assert glu_call(nv, M=0) == 0
     assert glu_call(nv, I=0, w_len=0, s_len=0) == 0

@@ -297,10 +297,54 @@ def pin_glu_halves(orc):
     assert np.allclose(y[0], want, rtol=0, atol=1e-15)
 
 
+def _brute_force_qmm_nt(x, codes, sbytes, gs):
+    """Exact-rational y = factor * x @ (fp4 * e4m3) for a weight indexed
+    [input k, output n], one scale byte per 16 outputs of an input."""
+    m_, k = x.shape
+    n = codes.shape[1]
+    fac = Fraction(1) if gs is None else Fraction(float(np.float32(np.float32(gs) / np.float32(2688))))
+    y = np.empty((m_, n), dtype=np.float64)
+    for m in range(m_):
+        for j in range(n):
+            acc = Fraction(0)
+            for c in range(k):
+                acc += Fraction(float(x[m, c])) * frac_e2m1(int(codes[c, j])) * frac_e4m3(int(sbytes[c, j // 16]))
+            y[m, j] = float(acc * fac)
+    return y
+
+
+def pin_nontransposed_brute_force(orc):
+    # x [1, 17] against a [17, 32] weight (the shape PR #2629 names), a square
+    # plane on which a transposed operand would not fail on shape, and a
+    # partial last word column of a 16-output block
+    g = synth.rng(8)
+    for (m, k, n), gs in (((1, 17, 32), None), ((2, 32, 32), np.float32(26.88)), ((3, 5, 48), np.float32(4.0))):
+        codes = g.integers(0, 16, size=(k, n))
+        sbytes = synth.log_uniform_scales(g, (k, n // 16), 2.0**-4, 2.0**4)
+        x = synth.activations(g, (m, k), "bf16").double().numpy()
+        got = orc.qmm_nontransposed(x, pack_codes(codes), sbytes, gs)
+        ref = _brute_force_qmm_nt(x, codes, sbytes, gs)
+        assert got.shape == (m, n)
+        assert np.max(np.abs(got - ref)) <= 1e-12 * max(1.0, np.max(np.abs(ref)))
+        ent = orc.qmm_nontransposed_entries(x, pack_codes(codes), sbytes, gs, [m - 1, 0], [n - 1, 17 % n])
+        assert np.max(np.abs(ent - ref[[m - 1, 0], [n - 1, 17 % n]])) <= 1e-12 * max(1.0, np.max(np.abs(ref)))
+
+
+def pin_nontransposed_identity(orc):
+    # identity activations return the dequantized plane itself, row k = input k
+    k = n = 32
+    codes = np.arange(k * n).reshape(k, n) * 7 % 16
+    sbytes = np.full((k, n // 16), 0x38, dtype=np.uint8)
+    table = {int(c): float(v) for c, v in _read_table("e2m1_table.txt")}
+    y = orc.qmm_nontransposed(np.eye(k), pack_codes(codes), sbytes, None)
+    assert y.tolist() == [[table[int(codes[r, c])] for c in range(n)] for r in range(k)]
+
+
 PINS = [pin_e2m1_table, pin_e4m3_all_bytes, pin_packing, pin_block_scale_broadcast,
         pin_brute_force_matmul, pin_one_hot, pin_global_factor, pin_dequantize_rounding,
         pin_sidecar_identity, pin_transcode_layout, pin_gather_zero_rows, pin_plane_check,
-        pin_error_metric, pin_gelu_tanh, pin_silu, pin_glu_halves]
+        pin_error_metric, pin_gelu_tanh, pin_silu, pin_glu_halves, pin_nontransposed_brute_force,
+        pin_nontransposed_identity]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=lambda p: p.__name__)
@@ -414,3 +458,21 @@ def test_planted_gelu_without_cubic(monkeypatch):
     monkeypatch.setattr(O, "gelu_tanh", wrong)
     with pytest.raises(AssertionError):
         pin_gelu_tanh(O)
+
+
+def test_planted_nontransposed_as_transposed(monkeypatch):
+    def transposed(x, w, scales, gs=None):
+        return np.asarray(x, dtype=np.float64) @ O.block_values(w, scales).T * np.float64(O.global_factor(gs))
+    _planted(monkeypatch, "qmm_nontransposed", transposed)
+    with pytest.raises(AssertionError):
+        pin_nontransposed_identity(O)
+    with pytest.raises((AssertionError, ValueError)):
+        pin_nontransposed_brute_force(O)
+
+
+def test_planted_nontransposed_scale_row_shifted(monkeypatch):
+    # each input's outputs scaled by the previous input's scale bytes
+    orig = O.qmm_nontransposed
+    _planted(monkeypatch, "qmm_nontransposed", lambda x, w, s, gs=None: orig(x, w, np.roll(s, 1, axis=0), gs))
+    with pytest.raises(AssertionError):
+        pin_nontransposed_brute_force(O)
