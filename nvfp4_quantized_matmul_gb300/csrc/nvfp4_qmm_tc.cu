@@ -454,27 +454,35 @@ __device__ void producer_role(const TcParams& p, uint32_t sB, uint32_t bars, vol
 
 struct WTaskNT {
   uint32_t w[8];  // inputs k0..k0+7 of the lane's word column
-  uint32_t s[2];  // their scale bytes (four per word, lowest input first)
+  uint32_t s;     // scale bytes 4 (lane & 3) .. + 3 of the tile's 16 for input k0 + (lane >> 2)
 };
 
-template <int BM>
-__device__ __forceinline__ void w_load_nt(WTaskNT& t, const WCursor& cur, const TcParams& p, int v, int j) {
+// Loaded values are only stored in registers here (no arithmetic on them),
+// so issuing the loads of later k-blocks never waits for their data.
+template <typename Cur>
+__device__ __forceinline__ void w_load_nt(WTaskNT& t, const Cur& cur, const TcParams& p, int v, int j) {
   if (cur.done) return;
   const int64_t nwords = p.N / 8, ngroups = p.N / 16;
   const int64_t col = (int64_t)cur.nt * 32 + j;
   const bool cok = col < nwords;
   const int64_t k0 = (int64_t)cur.kb * BK + 8 * v;
-  uint32_t s0 = 0, s1 = 0;
 #pragma unroll
   for (int kk = 0; kk < 8; ++kk) {
     const int64_t k = k0 + kk;
-    const bool ok = cok && k < p.K;  // inputs past K decode to +0
-    t.w[kk] = ok ? __ldg(p.w + k * nwords + col) : 0u;
-    const uint32_t sb = ok ? (uint32_t)__ldg(p.scales + k * ngroups + (col >> 1)) : 0u;
-    if (kk < 4) s0 |= sb << (8 * kk); else s1 |= sb << (8 * (kk - 4));
+    t.w[kk] = cok && k < p.K ? __ldg(p.w + k * nwords + col) : 0u;  // inputs past K decode to +0
   }
-  t.s[0] = s0;
-  t.s[1] = s1;
+  const int64_t ks = k0 + (j >> 2), g0 = (int64_t)cur.nt * 16 + 4 * (j & 3);
+  uint32_t sv = 0;
+  if (ks < p.K) {
+    const uint8_t* row = p.scales + ks * ngroups;
+    if ((ngroups & 3) == 0) {
+      if (g0 < ngroups) sv = __ldg(reinterpret_cast<const uint32_t*>(row + g0));
+    } else {
+      for (int q = 0; q < 4; ++q)
+        if (g0 + q < ngroups) sv |= (uint32_t)__ldg(row + g0 + q) << (8 * q);
+    }
+  }
+  t.s = sv;
 }
 
 template <typename T>
@@ -483,7 +491,9 @@ __device__ __forceinline__ void w_store_nt(uint32_t stage_base, int v, int j, co
   uint32_t o[8][4];
 #pragma unroll
   for (int kk = 0; kk < 8; ++kk) {
-    const uint32_t sb = (t.s[kk >> 2] >> (8 * (kk & 3))) & 0xFFu;
+    // the scale byte of the lane's 16-output block (j / 2) for input kk
+    const uint32_t quad = __shfl_sync(0xffffffffu, t.s, kk * 4 + (j >> 3));
+    const uint32_t sb = (quad >> (8 * ((j >> 1) & 3))) & 0xFFu;
     Dt<T>::decode(__funnelshift_r(t.w[kk], t.w[kk], 4 * rot), Dt<T>::scale(sb), o[kk]);
   }
   const uint32_t rows = stage_base + (uint32_t)j * 1024u;  // B rows 8j..8j+7
@@ -504,9 +514,10 @@ template <typename T, typename C>
 __device__ void producer_role_nt(const TcParams& p, uint32_t sB, uint32_t bars, volatile int* abort_flag,
                                  int num_tiles) {
   static_assert(C::BN == 256 && kProducerWarps * 8 == BK, "one word column per lane, eight inputs per warp");
-  // three k-blocks of words in flight (ten registers each); four spill in the
-  // 640-thread configuration
-  constexpr int STAGES = C::STAGES, PF = 3, BM = C::BM;
+  // one k-block of words loaded ahead (nine registers): on GB300 this ran
+  // faster than two or three ahead (M = 8192 on [5376, 21504]: 1683 us
+  // against 2131 and 1880), whose registers the 640-thread CTA cannot spare
+  constexpr int STAGES = C::STAGES, PF = 2, BM = C::BM;
   const int v = (int)(threadIdx.x >> 5) - C::kWarpProd0;
   const int j = threadIdx.x & 31;
   WCursor ld{(int)blockIdx.x, 0, true, 0, 0};
@@ -514,7 +525,7 @@ __device__ void producer_role_nt(const TcParams& p, uint32_t sB, uint32_t bars, 
   WTaskNT buf[PF];
 #pragma unroll
   for (int i = 0; i < PF - 1; ++i) {
-    w_load_nt<BM>(buf[i], ld, p, v, j);
+    w_load_nt(buf[i], ld, p, v, j);
     w_advance<false, BM>(ld, p, num_tiles, nullptr, nullptr);
   }
   uint32_t u = 0;
@@ -534,7 +545,7 @@ __device__ void producer_role_nt(const TcParams& p, uint32_t sB, uint32_t bars, 
 #pragma unroll
     for (int q = 0; q < PF; ++q) {
       if (i + q >= total) return;
-      w_load_nt<BM>(buf[(q + PF - 1) % PF], ld, p, v, j);
+      w_load_nt(buf[(q + PF - 1) % PF], ld, p, v, j);
       w_advance<false, BM>(ld, p, num_tiles, nullptr, nullptr);
       if (!consume(buf[q])) return;
     }
@@ -614,6 +625,48 @@ __device__ void producer_role_sk(const TcParams& p, uint32_t sB, uint32_t bars, 
       w_load<C::BN>(buf[(j + PF - 1) % PF], ld, p, r, h);
       w_advance_sk<GATHER, BM>(ld, p, seg, pre);
       if (!consume(buf[j])) return;
+    }
+  }
+}
+
+// Non-transposed weights in the stream-K kernel: the units of the stream-K
+// schedule, the decode and transpose of producer_role_nt.
+template <typename T, typename C>
+__device__ void producer_role_sk_nt(const TcParams& p, uint32_t sB, uint32_t bars, volatile int* abort_flag,
+                                    Sched sched) {
+  static_assert(C::BN == 256 && kProducerWarps * 8 == BK, "one word column per lane, eight inputs per warp");
+  constexpr int STAGES = C::STAGES, PF = 2, BM = C::BM;  // as in producer_role_nt
+  const int v = (int)(threadIdx.x >> 5) - C::kWarpProd0;
+  const int j = threadIdx.x & 31;
+  WCursorSK ld;
+  ld.sc = sched;
+  const int64_t total = sched.total();
+  w_seek_sk<false, BM>(ld, p, nullptr, nullptr);
+  WTaskNT buf[PF];
+#pragma unroll
+  for (int i = 0; i < PF - 1; ++i) {
+    w_load_nt(buf[i], ld, p, v, j);
+    w_advance_sk<false, BM>(ld, p, nullptr, nullptr);
+  }
+  uint32_t u = 0;
+  auto consume = [&](const WTaskNT& t) -> bool {
+    const int s = (int)(u % STAGES);
+    const uint32_t ph = (u / STAGES) & 1;
+    if (!wait_bar_warp(bars + 8 * (2 * STAGES + s), ph ^ 1, abort_flag, 3, &g_tc_error)) return false;  // stage empty
+    w_store_nt<T>(sB + (uint32_t)s * C::B_BYTES, v, j, t);
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    __syncwarp();
+    if (j == 0) mbar_arrive(bars + 8 * (STAGES + s));  // fullB
+    ++u;
+    return true;
+  };
+  for (int64_t i = 0; i < total; i += PF) {
+#pragma unroll
+    for (int q = 0; q < PF; ++q) {
+      if (i + q >= total) return;
+      w_load_nt(buf[(q + PF - 1) % PF], ld, p, v, j);
+      w_advance_sk<false, BM>(ld, p, nullptr, nullptr);
+      if (!consume(buf[q])) return;
     }
   }
 }
@@ -1002,7 +1055,7 @@ qmm_tc_kernel(const __grid_constant__ CUtensorMap xmap, const TcParams p) {
 // The stream-K kernel (dense launches of fewer than two waves of tiles): the
 // same roles as qmm_tc_kernel, walking units (tile, k-block range), with the
 // split-tile epilogue. Instantiated with GATHER = false and SK = true only.
-template <typename T, typename C, bool GATHER, bool SK>
+template <typename T, typename C, bool GATHER, bool SK, bool kNT = false>
 __global__ void __launch_bounds__(C::THREADS, 1)
 qmm_tc_sk_kernel(const __grid_constant__ CUtensorMap xmap, const TcParams p) {
   constexpr int STAGES = C::STAGES, MH = C::MH, BN = C::BN, BM = C::BM, NBUF = C::ACC_BUFS;
@@ -1306,7 +1359,10 @@ qmm_tc_sk_kernel(const __grid_constant__ CUtensorMap xmap, const TcParams p) {
       if (lane == 0) mbar_arrive(accEmpty(b));
     }
   } else if (warp >= C::kWarpProd0) {
-    producer_role_sk<T, C, GATHER>(p, sB, bars, abort_flag, sched, seg, pre);
+    if constexpr (kNT)
+      producer_role_sk_nt<T, C>(p, sB, bars, abort_flag, sched);
+    else
+      producer_role_sk<T, C, GATHER>(p, sB, bars, abort_flag, sched, seg, pre);
   }
 
   tc_fence_before();
@@ -1765,14 +1821,34 @@ cudaError_t launch_nt_cfg(const void* x, int64_t M, int64_t K, const uint32_t* w
   p.B = M;
   p.E = 1;
   p.xcontig = 1;
-  p.dp_tiles = p.num_tiles;
+  p.glu_cols = 0;
+  p.glu_act = 0;
+  // the dense route's rule: below two waves of tiles (and not whole waves)
+  // every tile's k-blocks are split evenly over the CTAs
+  const int T_ = p.num_tiles;
+  int grid = T_ < sms ? T_ : sms;
+  p.dp_tiles = T_;
   p.sk_tiles = 0;
   p.ws = nullptr;
   p.ws_cnt = nullptr;
-  p.glu_cols = 0;
-  p.glu_act = 0;
-  const int grid = p.num_tiles < sms ? p.num_tiles : sms;
-  auto kern = qmm_tc_kernel<T, C, false, false, true>;
+  if (stream_k_on() && T_ % sms != 0 && T_ < 2 * sms) {
+    p.dp_tiles = 0;
+    p.sk_tiles = T_;
+    if (T_ > sms) {
+      grid = sms;
+    } else {
+      const int64_t by_blocks = (int64_t)T_ * p.num_kb / kMinSkBlocks;
+      grid = (int)(by_blocks < T_ ? T_ : (by_blocks < sms ? by_blocks : sms));
+    }
+    int dev = 0;
+    cudaGetDevice(&dev);
+    SkWs ws;
+    cudaError_t e = sk_workspace(dev, st, (size_t)p.sk_tiles * C::BM * C::BN, (size_t)p.sk_tiles, &ws);
+    if (e != cudaSuccess) return e;
+    p.ws = ws.acc;
+    p.ws_cnt = ws.cnt;
+  }
+  auto kern = p.sk_tiles > 0 ? qmm_tc_sk_kernel<T, C, false, true, true> : qmm_tc_kernel<T, C, false, false, true>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
   if (e != cudaSuccess) return e;
   kern<<<grid, C::THREADS, C::SMEM, st>>>(map, p);

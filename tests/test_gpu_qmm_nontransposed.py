@@ -8,7 +8,8 @@ pages name (x [1, 17] against a [17, 32] weight), K not a multiple of 8 (the
 activations are padded into a scratch buffer first) or of the 64-input
 k-block, N ending inside a weight tile and inside a word pair, one and two
 128-row halves, both dtypes, the global scale, back-to-back calls, a CUDA
-graph replay and the prefill shape at full size on sampled outputs.
+graph replay and the prefill shape at full size on sampled outputs, with
+the stream-K split of the k-blocks and with whole tiles.
 """
 import numpy as np
 import pytest
@@ -42,7 +43,11 @@ NT_SHAPES = [(1, 17, 32), (3, 64, 272), (130, 100, 512), (257, 300, 1008), (600,
 @pytest.mark.parametrize("mkn", NT_SHAPES, ids=lambda v: "M%d_K%d_N%d" % v)
 @pytest.mark.parametrize("dt", ["f16", "bf16"])
 @pytest.mark.parametrize("with_gs", [False, True])
-def test_nontransposed_parity(nv, mkn, dt, with_gs):
+@pytest.mark.parametrize("split", ["1", "0"], ids=["streamk", "whole_tiles"])
+def test_nontransposed_parity(nv, monkeypatch, mkn, dt, with_gs, split):
+    # below two waves of tiles the k-blocks are split over the CTAs unless
+    # NVFP4_TC_STREAMK=0 deals whole tiles
+    monkeypatch.setenv("NVFP4_TC_STREAMK", split)
     M, K, N = mkn
     w, s = weights(M + 7 * K + N, K, N)  # [K, N/8] words, [K, N/16] scales
     g = synth.rng(3 * M + K + 5 * N)
