@@ -554,6 +554,17 @@ def run_routes(nv, synth, torch, dev, stream, args):
     out["qmm_nontransposed_5376x21504"] = ntr
     del wt, stt, w, s
 
+    # Quantize a dense bf16 gate/up plane [43008, 5376] with gs = its amax.
+    n, k = 43008, 5376
+    xq = (torch.randn((n, k), device=dev, generator=torch.Generator(device=dev).manual_seed(11)) * 0.02).to(torch.bfloat16)
+    gq = xq.abs().max().float().reshape(1)
+    oq = (torch.empty((n, k // 8), dtype=torch.int32, device=dev), torch.empty((n, k // 16), dtype=torch.uint8, device=dev))
+    ms = time_calls(torch, dev, stream, lambda i: nv.quantize(xq, gs=gq, out=oq), 5)
+    b = 2 * n * k + 0.5625 * n * k
+    out["quantize_bf16_43008x5376"] = {"us": round(ms * 1e3, 1), "GBps": round(b / (ms * 1e-3) / 1e9, 1),
+                                       "frac_hbm": round(b / (ms * 1e-3) / 1e9 / hbm_peak, 4)}
+    del xq, gq, oq
+
     # Dequantize the gate/up weight to bf16.
     n, k = 43008, 5376
     (w, s), = rand_w(n, k, 1, seed=5)

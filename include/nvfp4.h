@@ -93,6 +93,30 @@ nvfp4_status nvfp4_dequantize(const uint32_t* w, int64_t w_len, const uint8_t* s
                               nvfp4_dtype out_dtype, void* out, void* stream);
 
 /*
+ * Dense -> NVFP4 quantize, the encoding half of MLX's global-scale convention
+ * (PR #2629, Implementation Review Summary: fp_quantize encodes block scales
+ * times 448 * 6 / global_scale; issue #693, Context: the dense f16 -> MLX
+ * quantize(mode="nvfp4") repair path). For each run of 16 columns, in IEEE
+ * float32 with round to nearest even:
+ *   amax = max |x|;  s = amax / 6, times 2688 / gs[e] when gs is given;
+ *   scale byte = the E4M3 value nearest to s, ties to even, saturating at 448;
+ *   d = e4m3(scale byte) * gs[e] / 2688 (the multiplier dequantize applies);
+ *   code = the E2M1 value nearest to x * (1 / d), ties to even, saturating at
+ *          +-6, +0 where the magnitude rounds to 0, every code 0 where d == 0.
+ * The rounding and saturation rules are this library's reading; the pages
+ * do not state them. NaN or infinite inputs give unspecified codes (no
+ * fault). With gs[e] = max |x[e]| every block scale is at most 448 and
+ * nothing saturates; without gs a block whose amax exceeds 2688 saturates.
+ *   x [E, N, K] of x_dtype (16-byte aligned), gs NULL (gs_len 0) or E floats
+ *   on the device (positive and finite), w [E, N, K/8] uint32 and scales
+ *   [E, N, K/16] uint8 written (lengths as for nvfp4_dequantize;
+ *   NVFP4_ERR_PLANE otherwise). K % 16 == 0.
+ */
+nvfp4_status nvfp4_quantize(const void* x, nvfp4_dtype x_dtype, int64_t E, int64_t N, int64_t K, const float* gs,
+                            int64_t gs_len, uint32_t* w, int64_t w_len, uint8_t* scales, int64_t scales_len,
+                            void* stream);
+
+/*
  * QuantizedMatmul (PR #2629, Summary): y = x @ dequantize(w).T, with the
  * global factor gs / 2688 applied once per output after the f32 sum.
  *   x [M, K] of x_dtype (f32, f16 or bf16), w [N, K/8], scales [N, K/16],

@@ -35,6 +35,7 @@ SIGNATURES = {
     "nvfp4_qmm_glu": (_INT, [_P, _INT, _I64, _I64, _P, _I64, _P, _I64, _P, _I64, _I64, _INT, _P, _INT, _P]),
     "nvfp4_qmm_batched": (_INT, [_P, _INT, _I64, _I64, _I64, _P, _I64, _P, _I64, _P, _I64, _I64, _P, _P]),
     "nvfp4_qmm_nontransposed": (_INT, [_P, _INT, _I64, _I64, _P, _I64, _P, _I64, _P, _I64, _I64, _P, _P]),
+    "nvfp4_quantize": (_INT, [_P, _INT, _I64, _I64, _I64, _P, _I64, _P, _I64, _P, _I64, _P]),
     "nvfp4_gather_qmm": (_INT, [_P, _INT, _I64, _I64, _P, _P, _I64, _INT, _P, _I64, _P, _I64, _P, _I64,
                                 _I64, _I64, _P, _P]),
     "nvfp4_last_error": (ctypes.c_char_p, []),
@@ -173,6 +174,26 @@ def qmm_batched(x, w, scales, gs=None, out=None):
     check(_lib.nvfp4_qmm_batched(_ptr(x), DTYPE_CODE[x.dtype], bt, m, k, _ptr(w), w.numel(), _ptr(scales),
                                  scales.numel(), _ptr(gs), _n(gs), n, _ptr(out), _stream(x)))
     return out
+
+
+def quantize(x, gs=None, out=None):
+    """Dense ``x`` [E?, N, K] (f32, f16 or bf16) -> ``(w [E?, N, K/8] int32,
+    scales [E?, N, K/16] uint8)``; ``gs`` None, a float or a device tensor with
+    one value per expert (block scales encoded times 2688 / gs)."""
+    _cuda(x)
+    if x.dim() not in (2, 3):
+        raise ValueError("x must be [N, K] or [E, N, K]")
+    e = x.shape[0] if x.dim() == 3 else 1
+    n, k = x.shape[-2], x.shape[-1]
+    gs = _gs_tensor(gs, x.device)
+    if out is None:
+        lead = tuple(x.shape[:-1])
+        out = (torch.empty(lead + (k // 8,), dtype=torch.int32, device=x.device),
+               torch.empty(lead + (k // 16,), dtype=torch.uint8, device=x.device))
+    w, s = out
+    check(_lib.nvfp4_quantize(_ptr(x), DTYPE_CODE[x.dtype], e, n, k, _ptr(gs), _n(gs), _ptr(w), w.numel(), _ptr(s),
+                              s.numel(), _stream(x)))
+    return w, s
 
 
 def qmm_nontransposed(x, w, scales, gs=None, out=None):

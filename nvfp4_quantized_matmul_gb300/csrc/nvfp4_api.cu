@@ -193,6 +193,21 @@ nvfp4_status nvfp4_dequantize(const uint32_t* w, int64_t w_len, const uint8_t* s
                                                   static_cast<cudaStream_t>(stream)));
 }
 
+nvfp4_status nvfp4_quantize(const void* x, nvfp4_dtype x_dtype, int64_t E, int64_t N, int64_t K, const float* gs,
+                            int64_t gs_len, uint32_t* w, int64_t w_len, uint8_t* scales, int64_t scales_len,
+                            void* stream) {
+  const char* fn = "nvfp4_quantize";
+  if (!dtype_ok(x_dtype)) return fail(NVFP4_ERR_DTYPE, "%s: unknown input dtype %d", fn, (int)x_dtype);
+  nvfp4_status s = check_planes(fn, w, w_len, scales, scales_len, E, N, K);
+  if (s) return s;
+  if ((s = check_gs(fn, gs, gs_len, E))) return s;
+  if (w_len == 0) return ok();
+  if (!x) return fail(NVFP4_ERR_NULL, "%s: x is NULL", fn);
+  if (!aligned(x, 16)) return fail(NVFP4_ERR_ALIGN, "%s: x must be 16-byte aligned", fn);
+  return cuda_status(fn, nvfp4::launch_quantize(x, (int)x_dtype, gs, E, N, K, w, scales,
+                                                static_cast<cudaStream_t>(stream)));
+}
+
 int64_t nvfp4_qmm_crossover(nvfp4_dtype x_dtype, int64_t N, int64_t K) {
   const int64_t env = env_crossover();
   if (env >= 0) return env;

@@ -14,6 +14,9 @@ cudaError_t launch_transcode(const uint8_t* mo_w, int64_t w_bytes, const uint8_t
 
 cudaError_t launch_dequantize(const uint32_t* w, const uint8_t* scales, const float* gs, int64_t E,
                               int64_t N, int64_t K, int out_dtype, void* out, cudaStream_t st);
+// Dense x [E, N, K] (f32, f16 or bf16) -> packed words and E4M3 block scales.
+cudaError_t launch_quantize(const void* x, int x_dtype, const float* gs, int64_t E, int64_t N, int64_t K,
+                            uint32_t* w, uint8_t* scales, cudaStream_t st);
 // Reads and clears the error code of the bulk-copy transcode's bounded waits.
 int read_copy_error();
 

@@ -37,7 +37,10 @@ exact-rational brute force, sidecar identity against the ModelOpt formula,
 zero rows; the gated-MLP activations against their symmetry identities, the
 exact erf GELU and the library sigmoid, and the gate/up halves through
 one-hot products; the non-transposed product against an exact-rational
-brute force indexed [input, output] and through identity activations). The equivalence of ModelOpt's on-disk nibble order with the MLX
+brute force indexed [input, output] and through identity activations; the
+quantizer's encoders against a brute-force nearest search and hand-worked
+ties, the quantizer through its round trip with dequantize and a worked
+global-scale case). The equivalence of ModelOpt's on-disk nibble order with the MLX
 order is taken from the page ("likely matches") and is parity unpinned: no
 real checkpoint is available to confirm it.
 """
@@ -271,6 +274,88 @@ def qmm_glu(x, w, scales, gs=None, act="gelu_tanh") -> np.ndarray:
     if 2 * half != h.shape[1]:
         raise ValueError("the fused plane needs an even number of rows")
     return ACTIVATIONS[act](h[:, :half]) * h[:, half:]
+
+
+def pack_codes(codes) -> np.ndarray:
+    """Pack codes ``[..., K]`` into words ``[..., K/8]``: column ``8*j + i``
+    into nibble ``i`` of word ``j``, least significant nibble first (the
+    inverse of :func:`unpack_codes`)."""
+    c = np.asarray(codes).astype(np.uint64) & 0xF
+    k = c.shape[-1]
+    if k % 8:
+        raise ValueError("the packed axis needs a multiple of 8 columns")
+    c = c.reshape(*c.shape[:-1], k // 8, 8)
+    words = np.zeros(c.shape[:-1], dtype=np.uint64)
+    for i in range(8):
+        words |= c[..., i] << np.uint64(4 * i)
+    return words.astype(np.uint32)
+
+
+def _round_to_grid(v, grid) -> np.ndarray:
+    """Index of the grid entry nearest to each v >= 0 (``grid`` increasing,
+    index i the code of entry i). A tie goes to the even index; v beyond the
+    last entry gives the last (saturation). Exact: every comparison is
+    against a midpoint of two grid entries, which float64 holds exactly."""
+    v = np.asarray(v, dtype=np.float64)
+    g = np.asarray(grid, dtype=np.float64)
+    i = np.clip(np.searchsorted(g, v, side="right") - 1, 0, len(g) - 1)  # g[i] <= v < g[i + 1]
+    j = np.minimum(i + 1, len(g) - 1)
+    mid = (g[i] + g[j]) / 2.0
+    up = (v > mid) | ((v == mid) & (j % 2 == 0) & (j != i))
+    return np.where(up, j, i)
+
+
+# The finite non-negative E4M3 values, byte b at index b (0x00 .. 0x7E).
+def _e4m3_grid() -> np.ndarray:
+    return e4m3_value(np.arange(0x7F))
+
+
+def e4m3_encode(v) -> np.ndarray:
+    """Byte of the E4M3FN value nearest to each v >= 0: round to nearest,
+    ties to the even byte (the even mantissa), saturating at 448 (0x7E)."""
+    return _round_to_grid(v, _e4m3_grid()).astype(np.uint8)
+
+
+def e2m1_encode(v) -> np.ndarray:
+    """Magnitude code (0..7) of the E2M1 value nearest to each v >= 0: ties to
+    the even code, saturating at 6 (code 7)."""
+    return _round_to_grid(v, E2M1_MAGNITUDES).astype(np.int64)
+
+
+def quantize(x, gs=None):
+    """Dense -> NVFP4 planes ``(w [..., K/8] uint32, scales [..., K/16] uint8)``.
+
+    The encoding half of MLX's global-scale convention (PR #2629,
+    Implementation Review Summary: fp_quantize encodes block scales times
+    448 * 6 / global_scale), with the rounding and saturation the pages leave
+    open read as follows, every step in IEEE float32 with round to nearest
+    even, per 16-column block:
+
+    * amax = max |x|; s = amax / 6, then s * (2688 / gs) when gs is given;
+    * scale byte = :func:`e4m3_encode` (s);
+    * d = e4m3(byte) * (gs / 2688), the multiplier the dequantization
+      applies, and its reciprocal r = 1 / d;
+    * code = :func:`e2m1_encode` (|x| * r) with the sign bit of x, +0 where
+      the magnitude code is 0, and every code 0 where d == 0.
+    """
+    xf = np.asarray(x, dtype=np.float32)
+    k = xf.shape[-1]
+    if k % 16:
+        raise ValueError("K must be a multiple of 16")
+    blocks = xf.reshape(*xf.shape[:-1], k // 16, 16)
+    amax = np.max(np.abs(blocks), axis=-1)
+    s = (amax / np.float32(6.0)).astype(np.float32)
+    if gs is not None:
+        inv = np.float32(np.float32(GLOBAL_SCALE_DIVISOR) / np.float32(gs))
+        s = (s * inv).astype(np.float32)
+    sbytes = e4m3_encode(s)
+    d = (e4m3_value(sbytes).astype(np.float32) * global_factor(gs)).astype(np.float32)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        r = (np.float32(1.0) / d).astype(np.float32)
+        v = (np.abs(blocks) * r[..., None]).astype(np.float32)
+    mag = np.where(d[..., None] > 0, e2m1_encode(np.where(d[..., None] > 0, v, 0.0)), 0)
+    codes = np.where((blocks < 0) & (mag != 0), mag | 8, mag).reshape(xf.shape)
+    return pack_codes(codes), sbytes
 
 
 def rel_to_max_error(y, ref) -> float:

@@ -141,6 +141,26 @@ def test_qmm_nontransposed_refusals(nv):
     assert call(N=0, w_len=0, s_len=0) == "OK"
 
 
+def test_quantize_refusals(nv):
+    lib = nv.library()
+    ST = nv.STATUS
+    # x [2, 8, 64] -> w [2, 8, 8] words, scales [2, 8, 4]
+    def call(**kw):
+        a = dict(x=A, xdt=2, E=2, N=8, K=64, gs=None, gs_len=0, w=A, w_len=2 * 8 * 8, s=A, s_len=2 * 8 * 4)
+        a.update(kw)
+        return ST[lib.nvfp4_quantize(a["x"], a["xdt"], a["E"], a["N"], a["K"], a["gs"], a["gs_len"], a["w"],
+                                     a["w_len"], a["s"], a["s_len"], None)]
+    assert call(K=40, w_len=2 * 8 * 5, s_len=2 * 8 * 2) == "ERR_SHAPE"  # K % 16
+    assert call(w_len=2 * 8 * 8 - 1) == "ERR_PLANE"
+    assert call(s_len=2 * 8 * 4 + 8) == "ERR_PLANE"
+    assert call(gs=A, gs_len=1) == "ERR_GSCALE"                         # one per expert
+    assert call(xdt=4) == "ERR_DTYPE"
+    assert call(x=U) == "ERR_ALIGN"
+    assert call(x=None) == "ERR_NULL"
+    assert call(w=U) == "ERR_ALIGN"
+    assert call(N=0, w_len=0, s_len=0) == "OK"
+
+
 def test_qmm_glu_empty_returns_ok(nv):
     assert glu_call(nv, M=0) == 0
     assert glu_call(nv, I=0, w_len=0, s_len=0) == 0

@@ -340,11 +340,90 @@ def pin_nontransposed_identity(orc):
     assert y.tolist() == [[table[int(codes[r, c])] for c in range(n)] for r in range(k)]
 
 
+def pin_pack_codes(orc):
+    # packing is the inverse of the pinned unpacking, and puts column 8j+i in nibble i
+    g = synth.rng(21)
+    w = synth.packed_weight(g, 5, 64)
+    assert np.array_equal(orc.pack_codes(orc.unpack_codes(w)), w)
+    assert orc.pack_codes(np.arange(8))[0] == 0x76543210
+
+
+def pin_e2m1_encode(orc):
+    # hand-worked from the grid 0, .5, 1, 1.5, 2, 3, 4, 6 (codes 0..7): a
+    # midpoint goes to the even code, anything past 6 to 6
+    cases = [(0.0, 0), (0.2499, 0), (0.25, 0), (0.2501, 1), (0.75, 2), (1.25, 2), (1.2501, 3), (1.75, 4),
+             (2.5, 4), (2.5001, 5), (3.5, 6), (4.9999, 6), (5.0, 6), (5.0001, 7), (6.0, 7), (7.0, 7), (1e30, 7)]
+    got = orc.e2m1_encode(np.array([v for v, _ in cases], dtype=np.float32))
+    assert got.tolist() == [c for _, c in cases]
+    # brute force: the code's value is at least as near as every other value
+    v = synth.rng(22).uniform(0, 8, size=4000).astype(np.float32).astype(np.float64)
+    code = orc.e2m1_encode(v)
+    grid = np.array([0, 0.5, 1, 1.5, 2, 3, 4, 6])
+    dist = np.abs(v[:, None] - grid[None, :])
+    assert np.all(dist[np.arange(v.size), code] <= dist.min(axis=1))
+
+
+def pin_e4m3_encode(orc):
+    # identity on the 127 finite non-negative values (bytes 0x00..0x7E, by the
+    # bit definition pinned above), ties to the even byte, saturation at 448
+    vals = orc.e4m3_value(np.arange(0x7F))
+    assert orc.e4m3_encode(vals).tolist() == list(range(0x7F))
+    mids = (vals[:-1] + vals[1:]) / 2
+    assert orc.e4m3_encode(mids).tolist() == [b + (b & 1) for b in range(0x7E)]
+    assert orc.e4m3_encode(np.array([448.0, 460.0, 1e9])).tolist() == [0x7E] * 3
+    assert orc.e4m3_encode(np.array([2.0**-10, 2.0**-10 * 1.0001])).tolist() == [0, 1]
+
+
+def _plane_with_a_six_per_block(g, n, k):
+    codes = g.integers(0, 16, size=(n, k))
+    codes[codes == 8] = 0  # -0 requantizes as +0
+    pos = g.integers(0, 16, size=(n, k // 16))
+    for b in range(k // 16):
+        codes[np.arange(n), 16 * b + pos[:, b]] = g.choice([7, 15], size=n)
+    return codes
+
+
+def pin_quantize_round_trip(orc):
+    # a plane whose every block holds a +-6 is its own quantization: amax = 6
+    # e4m3, so the scale comes back exactly and every x * (1 / d) lies within
+    # float32 rounding of a grid value, far from any midpoint;
+    # gs = 2688 * 2^k keeps both global factors exact
+    g = synth.rng(23)
+    codes = _plane_with_a_six_per_block(g, 6, 64)
+    w = pack_codes(codes)
+    s = synth.log_uniform_scales(g, (6, 4), 2.0**-8, 2.0**8)
+    for gs in (None, np.float32(2688.0), np.float32(2688.0 * 8)):
+        x = orc.block_values(w, s) * (1.0 if gs is None else float(gs) / 2688.0)
+        w2, s2 = orc.quantize(x.astype(np.float32), gs)
+        assert np.array_equal(w2, w) and np.array_equal(s2, s)
+
+
+def pin_quantize_worked_cases(orc):
+    # a block [6, 0, ...] with gs = 4 * 2688: s = 1 / 4 -> byte 0x28, d = 1,
+    # code 7; a zero block: scale 0, codes 0; a negative value rounding to
+    # zero: +0; beyond range: saturation at 448 and 6
+    x = np.zeros((4, 16), dtype=np.float32)
+    x[0, 0] = 6.0
+    x[2, :2] = [-0.1, 600.0]
+    x[3, :3] = [3000.0, -3000.0, 2.9]
+    w, s = orc.quantize(x, np.float32(4 * 2688.0))
+    assert s[0, 0] == 0x28 and w[0, 0] == 0x7 and w[0, 1] == 0
+    assert s[1, 0] == 0 and w[1].tolist() == [0, 0]
+    # row 2: amax 600 -> s = 100 / 4 = 25 -> byte of 24 (0x5C, ties 25 to 24),
+    # d = 24 * 4 = 96; 600 / 96 = 6.25 -> 6; -0.1 / 96 -> +0
+    assert s[2, 0] == 0x5C and w[2, 0] == 0x70
+    # row 3 with no global scale: s = 500 -> 448 (0x7E); 3000 / 448 > 6 -> 6;
+    # 2.9 / 448 -> 0
+    w3, s3 = orc.quantize(x[3:], None)
+    assert s3[0, 0] == 0x7E and w3[0, 0] == 0xF7
+
+
 PINS = [pin_e2m1_table, pin_e4m3_all_bytes, pin_packing, pin_block_scale_broadcast,
         pin_brute_force_matmul, pin_one_hot, pin_global_factor, pin_dequantize_rounding,
         pin_sidecar_identity, pin_transcode_layout, pin_gather_zero_rows, pin_plane_check,
         pin_error_metric, pin_gelu_tanh, pin_silu, pin_glu_halves, pin_nontransposed_brute_force,
-        pin_nontransposed_identity]
+        pin_nontransposed_identity, pin_pack_codes, pin_e2m1_encode, pin_e4m3_encode, pin_quantize_round_trip,
+        pin_quantize_worked_cases]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=lambda p: p.__name__)
@@ -476,3 +555,27 @@ def test_planted_nontransposed_scale_row_shifted(monkeypatch):
     _planted(monkeypatch, "qmm_nontransposed", lambda x, w, s, gs=None: orig(x, w, np.roll(s, 1, axis=0), gs))
     with pytest.raises(AssertionError):
         pin_nontransposed_brute_force(O)
+
+
+def test_planted_e2m1_ties_away_from_zero(monkeypatch):
+    grid = np.array([0, 0.5, 1, 1.5, 2, 3, 4, 6])
+    mids = (grid[:-1] + grid[1:]) / 2
+    _planted(monkeypatch, "e2m1_encode", lambda v: np.searchsorted(mids, np.asarray(v, dtype=np.float64), side="right"))
+    with pytest.raises(AssertionError):
+        pin_e2m1_encode(O)
+
+
+def test_planted_quantize_without_global_scale(monkeypatch):
+    orig = O.quantize
+    _planted(monkeypatch, "quantize", lambda x, gs=None: orig(x, None))
+    with pytest.raises(AssertionError):
+        pin_quantize_worked_cases(O)
+
+
+def test_planted_quantize_scale_off_by_constant(monkeypatch):
+    # every block scale 1.5 times too large (as if amax were divided by 4
+    # instead of 6)
+    orig = O.quantize
+    _planted(monkeypatch, "quantize", lambda x, gs=None: orig(np.asarray(x, dtype=np.float32) * np.float32(1.5), gs))
+    with pytest.raises(AssertionError):
+        pin_quantize_round_trip(O)
