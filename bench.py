@@ -674,6 +674,10 @@ def run_case(args):
     128 experts), one warm-up call then one call.
     prefill: the tensor-core route at M = 2048 on the [21504, 5376] plane, one
     warm-up call then one call.
+    nontransposed_prefill: nvfp4_qmm_nontransposed at M = 2048 on a [5376,
+    21504 / 8] plane (whole tiles), one warm-up call then one call.
+    quantize: nvfp4_quantize of a dense bf16 [43008, 5376] plane with gs =
+    max |x|, one warm-up call then one call.
     """
     import torch
 
@@ -693,6 +697,28 @@ def run_case(args):
             nv.qmm(x, w, s, gs=gs, route="tc")
         torch.cuda.synchronize(dev)
         print("case prefill ok")
+        return
+    if args.case == "nontransposed_prefill":
+        g = synth.rng(5400)
+        k, n, m = 5376, 21504, 2048
+        w = torch.randint(-2**31, 2**31 - 1, (k, n // 8), dtype=torch.int32, device=dev,
+                          generator=torch.Generator(device=dev).manual_seed(9))
+        s = torch.from_numpy(synth.log_uniform_scales(g, (k, n // 16), 2.0**-6, 4.0)).to(dev)
+        x = synth.activations(g, (m, k), "bf16").to(dev)
+        for _ in range(2):
+            nv.qmm_nontransposed(x, w, s)
+        torch.cuda.synchronize(dev)
+        print("case nontransposed_prefill ok")
+        return
+    if args.case == "quantize":
+        n, k = 43008, 5376
+        x = (torch.randn((n, k), device=dev, generator=torch.Generator(device=dev).manual_seed(11)) * 0.02).to(
+            torch.bfloat16)
+        gs = x.abs().max().float().reshape(1)
+        for _ in range(2):
+            nv.quantize(x, gs=gs)
+        torch.cuda.synchronize(dev)
+        print("case quantize ok")
         return
     if args.case == "gather_prefill":
         g = synth.rng(5300)
@@ -790,7 +816,8 @@ def main():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-rows", type=int, default=6144)
     ap.add_argument("--ref-rows", type=int, default=32)
-    ap.add_argument("--case", choices=["qmv_small", "qmv_shapes", "decode_step", "prefill", "gather_prefill"],
+    ap.add_argument("--case", choices=["qmv_small", "qmv_shapes", "decode_step", "prefill", "gather_prefill",
+                                       "nontransposed_prefill", "quantize"],
                     default=None,
                     help="run one small profiling case instead of the benchmark")
     args = ap.parse_args()
