@@ -565,6 +565,34 @@ def run_routes(nv, synth, torch, dev, stream, args):
                                        "frac_hbm": round(b / (ms * 1e-3) / 1e9 / hbm_peak, 4)}
     del xq, gq, oq
 
+    # Folded-scale transcode (the variant the sidecar replaces): a ModelOpt-
+    # convention triplet of the same plane (made by the quantizer, gs = amax,
+    # ws2 = amax / 2688), folded, then both dequantized and compared: blocks
+    # whose folded scale flushed to 0, and the error against the sidecar
+    # values (the sidecar dequantization is exact).
+    xq = (torch.randn((n, k), device=dev, generator=torch.Generator(device=dev).manual_seed(11)) * 0.02).to(torch.bfloat16)
+    gq = xq.abs().max().float().reshape(1)
+    wq, sq = nv.quantize(xq, gs=gq)
+    del xq
+    ws2 = gq / 2688.0
+    mo_w = wq.view(torch.uint8).reshape(n, k // 2)
+    of = (torch.empty_like(wq), torch.empty_like(sq))
+    ms = time_calls(torch, dev, stream, lambda i: nv.transcode_folded(mo_w, sq, ws2, out=of), 5)
+    b = 2 * (0.5625 * n * k)
+    ref = nv.dequantize(wq, sq, gq, torch.float32)
+    fold = nv.dequantize(of[0], of[1], None, torch.float32)
+    nzr = ref != 0
+    rel = ((fold - ref).abs()[nzr] / ref.abs()[nzr])
+    flushed = int(((sq != 0) & (of[1] == 0)).sum())
+    out["transcode_folded_43008x5376"] = {
+        "us": round(ms * 1e3, 1), "GBps": round(b / (ms * 1e-3) / 1e9, 1),
+        "blocks": int(sq.numel()), "blocks_flushed_to_zero": flushed,
+        "blocks_saturated": int((of[1] == 0x7E).sum()),
+        "max_abs_err_rel_to_max": round(float((fold - ref).abs().max() / ref.abs().max()), 6),
+        "median_rel_err_nonzero": round(float(rel.median()), 6), "max_rel_err_nonzero": round(float(rel.max()), 6),
+        "elements_zeroed": int(((fold == 0) & nzr).sum()), "elements_nonzero": int(nzr.sum())}
+    del wq, sq, of, ref, fold, nzr, rel, mo_w
+
     # Dequantize the gate/up weight to bf16.
     n, k = 43008, 5376
     (w, s), = rand_w(n, k, 1, seed=5)

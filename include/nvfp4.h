@@ -83,6 +83,23 @@ nvfp4_status nvfp4_transcode(const uint8_t* mo_weight, int64_t mo_weight_len, co
                              uint32_t* w_out, uint8_t* scales_out, float* gs_out, void* stream);
 
 /*
+ * Folded-scale transcode, the alternative issue #693 (Technical notes)
+ * rejects: weight_scale * weight_scale_2 folded into every E4M3 block scale
+ * and no sidecar, built to measure the overflow and rounding drift that the
+ * sidecar avoids (dequantize the result with gs NULL and compare it with the
+ * sidecar transcode). Weight bytes as nvfp4_transcode; each scale byte
+ * becomes the E4M3 value nearest to f32(e4m3(b) * ws2), ties to even,
+ * saturating at 448, products below 2^-10 flushed to 0. Non-negative finite
+ * scale bytes only (others give unspecified bytes, no fault).
+ *   mo_weight uint8 [N, K/2], mo_weight_scale uint8 [N, K/16],
+ *   weight_scale_2 float [1] on the device; w_out [N, K/8], scales_out
+ *   [N, K/16]. Lengths and refusals as nvfp4_transcode.
+ */
+nvfp4_status nvfp4_transcode_folded(const uint8_t* mo_weight, int64_t mo_weight_len, const uint8_t* mo_weight_scale,
+                                    int64_t mo_weight_scale_len, const float* weight_scale_2, int64_t N, int64_t K,
+                                    uint32_t* w_out, uint8_t* scales_out, void* stream);
+
+/*
  * Exact dequantize (PR #2629, Summary; Changes during review: sized from the
  * weight plane). out[e, n, k] = cast_rne(f32(fp4 * e4m3) * f32(gs[e] / 2688)),
  * or the exact product when gs is NULL. out is [E, N, K] of out_dtype.

@@ -6,7 +6,8 @@ first use, so ``synth`` can be imported on machines without the library.
 """
 _LAZY = ("transcode", "dequantize", "qmm", "gather_qmm", "library", "qmm_crossover", "take_device_error",
          "set_launch_overlap", "shutdown", "qmm_noalloc", "qmm_glu", "qmm_batched",
-         "qmm_nontransposed", "quantize")
+         "qmm_nontransposed", "quantize",
+         "transcode_folded")
 
 
 def __getattr__(name):

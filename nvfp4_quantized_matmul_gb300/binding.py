@@ -36,6 +36,7 @@ SIGNATURES = {
     "nvfp4_qmm_batched": (_INT, [_P, _INT, _I64, _I64, _I64, _P, _I64, _P, _I64, _P, _I64, _I64, _P, _P]),
     "nvfp4_qmm_nontransposed": (_INT, [_P, _INT, _I64, _I64, _P, _I64, _P, _I64, _P, _I64, _I64, _P, _P]),
     "nvfp4_quantize": (_INT, [_P, _INT, _I64, _I64, _I64, _P, _I64, _P, _I64, _P, _I64, _P]),
+    "nvfp4_transcode_folded": (_INT, [_P, _I64, _P, _I64, _P, _I64, _I64, _P, _P, _P]),
     "nvfp4_gather_qmm": (_INT, [_P, _INT, _I64, _I64, _P, _P, _I64, _INT, _P, _I64, _P, _I64, _P, _I64,
                                 _I64, _I64, _P, _P]),
     "nvfp4_last_error": (ctypes.c_char_p, []),
@@ -132,6 +133,23 @@ def transcode(mo_weight, mo_weight_scale, weight_scale_2, out=None):
     check(_lib.nvfp4_transcode(_ptr(mo_weight), mo_weight.numel(), _ptr(mo_weight_scale), mo_weight_scale.numel(),
                                _ptr(ws2), n, k, _ptr(w), _ptr(s), _ptr(gs), _stream(mo_weight)))
     return w, s, gs
+
+
+def transcode_folded(mo_weight, mo_weight_scale, weight_scale_2, out=None):
+    """ModelOpt triplet -> (w uint32 [N,K/8] as int32 storage, folded E4M3
+    scales uint8 [N,K/16]); no sidecar (dequantize with gs=None)."""
+    _cuda(mo_weight, mo_weight_scale)
+    n, half_k = mo_weight.shape
+    k = half_k * 2
+    ws2 = _gs_tensor(weight_scale_2, mo_weight.device)
+    if out is None:
+        w = torch.empty((n, k // 8), dtype=torch.int32, device=mo_weight.device)
+        s = torch.empty((n, k // 16), dtype=torch.uint8, device=mo_weight.device)
+    else:
+        w, s = out
+    check(_lib.nvfp4_transcode_folded(_ptr(mo_weight), mo_weight.numel(), _ptr(mo_weight_scale),
+                                      mo_weight_scale.numel(), _ptr(ws2), n, k, _ptr(w), _ptr(s), _stream(mo_weight)))
+    return w, s
 
 
 def dequantize(w, scales, gs=None, out_dtype=torch.bfloat16, out=None):

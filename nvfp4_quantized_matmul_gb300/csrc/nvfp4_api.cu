@@ -178,6 +178,29 @@ nvfp4_status nvfp4_transcode(const uint8_t* mo_weight, int64_t mo_weight_len, co
                                                  scales_out, gs_out, static_cast<cudaStream_t>(stream)));
 }
 
+nvfp4_status nvfp4_transcode_folded(const uint8_t* mo_weight, int64_t mo_weight_len, const uint8_t* mo_weight_scale,
+                                    int64_t mo_weight_scale_len, const float* weight_scale_2, int64_t N, int64_t K,
+                                    uint32_t* w_out, uint8_t* scales_out, void* stream) {
+  const char* fn = "nvfp4_transcode_folded";
+  if (N < 0 || K < 0) return fail(NVFP4_ERR_SHAPE, "%s: negative size", fn);
+  if (K % 16) return fail(NVFP4_ERR_SHAPE, "%s: K=%" PRId64 " is not a multiple of 16", fn, K);
+  int64_t wb, sb;
+  if (!mul_ok(N, K / 2, &wb) || !mul_ok(N, K / 16, &sb)) return fail(NVFP4_ERR_SHAPE, "%s: N*K overflows", fn);
+  if (mo_weight_len != wb)
+    return fail(NVFP4_ERR_PLANE, "%s: weight has %" PRId64 " bytes, expected N*K/2 = %" PRId64, fn, mo_weight_len, wb);
+  if (mo_weight_scale_len != sb)
+    return fail(NVFP4_ERR_PLANE, "%s: weight_scale has %" PRId64 " bytes, expected N*K/16 = %" PRId64, fn,
+                mo_weight_scale_len, sb);
+  if (!weight_scale_2) return fail(NVFP4_ERR_NULL, "%s: weight_scale_2 is required", fn);
+  if (wb == 0) return ok();
+  if (!mo_weight || !mo_weight_scale || !w_out || !scales_out) return fail(NVFP4_ERR_NULL, "%s: a plane pointer is NULL", fn);
+  if (!aligned(mo_weight, 16) || !aligned(mo_weight_scale, 16) || !aligned(w_out, 16) || !aligned(scales_out, 16) ||
+      !aligned(weight_scale_2, 4))
+    return fail(NVFP4_ERR_ALIGN, "%s: planes must be 16-byte aligned, the scalar 4-byte", fn);
+  return cuda_status(fn, nvfp4::launch_transcode_folded(mo_weight, wb, mo_weight_scale, sb, weight_scale_2, w_out,
+                                                        scales_out, static_cast<cudaStream_t>(stream)));
+}
+
 nvfp4_status nvfp4_dequantize(const uint32_t* w, int64_t w_len, const uint8_t* scales, int64_t scales_len,
                               const float* gs, int64_t gs_len, int64_t E, int64_t N, int64_t K,
                               nvfp4_dtype out_dtype, void* out, void* stream) {

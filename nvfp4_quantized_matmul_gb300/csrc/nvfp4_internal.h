@@ -17,6 +17,9 @@ cudaError_t launch_dequantize(const uint32_t* w, const uint8_t* scales, const fl
 // Dense x [E, N, K] (f32, f16 or bf16) -> packed words and E4M3 block scales.
 cudaError_t launch_quantize(const void* x, int x_dtype, const float* gs, int64_t E, int64_t N, int64_t K,
                             uint32_t* w, uint8_t* scales, cudaStream_t st);
+// ModelOpt triplet -> packed words and folded E4M3 scales (no sidecar).
+cudaError_t launch_transcode_folded(const uint8_t* mo_w, int64_t w_bytes, const uint8_t* mo_ws, int64_t s_bytes,
+                                    const float* ws2, uint32_t* w_out, uint8_t* s_out, cudaStream_t st);
 // Reads and clears the error code of the bulk-copy transcode's bounded waits.
 int read_copy_error();
 

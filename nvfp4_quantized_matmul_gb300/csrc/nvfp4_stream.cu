@@ -392,6 +392,54 @@ quantize_kernel(const T* __restrict__ x, const float* __restrict__ gs, int64_t E
   }
 }
 
+// ---------------------------------------------------------------- folded-scale transcode
+//
+// The alternative that issue #693 (Technical notes) rejects, built to measure
+// what it loses: weight_scale * weight_scale_2 folded into each E4M3 byte, no
+// sidecar. Weight bytes are copied as they are (the word plane is the byte
+// stream); each scale byte becomes the E4M3 nearest to f32(e4m3(b) * ws2),
+// ties to even, saturating at 448, small products flushed to 0 or a
+// subnormal.
+
+__device__ __forceinline__ uint32_t fold_byte(uint32_t b, float ws2) {
+  return f32_to_e4m3_satfinite(__fmul_rn(e4m3_to_f32(b & 0xFFu), ws2));
+}
+
+__device__ __forceinline__ uint32_t fold_word(uint32_t v, float ws2) {
+  return fold_byte(v, ws2) | (fold_byte(v >> 8, ws2) << 8) | (fold_byte(v >> 16, ws2) << 16) |
+         (fold_byte(v >> 24, ws2) << 24);
+}
+
+__global__ void __launch_bounds__(kStreamThreads)
+transcode_folded_kernel(const uint8_t* __restrict__ mo_w, int64_t w_bytes, const uint8_t* __restrict__ mo_ws,
+                        int64_t s_bytes, const float* __restrict__ ws2p, uint8_t* __restrict__ w_out,
+                        uint8_t* __restrict__ s_out) {
+  const float ws2 = __ldg(ws2p);
+  const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  const int64_t wv = w_bytes >> 4, sv = s_bytes >> 4;
+  const uint4* wi = reinterpret_cast<const uint4*>(mo_w);
+  uint4* wo = reinterpret_cast<uint4*>(w_out);
+  constexpr int kU = 4;  // loads in flight per thread
+  int64_t i = tid;
+  for (; i + (kU - 1) * stride < wv; i += kU * stride) {
+    uint4 v[kU];
+#pragma unroll
+    for (int u = 0; u < kU; ++u) v[u] = __ldcs(wi + i + u * stride);
+#pragma unroll
+    for (int u = 0; u < kU; ++u) __stcs(wo + i + u * stride, v[u]);
+  }
+  for (; i < wv; i += stride) __stcs(wo + i, __ldcs(wi + i));
+  const uint4* si = reinterpret_cast<const uint4*>(mo_ws);
+  uint4* so = reinterpret_cast<uint4*>(s_out);
+  for (int64_t j = tid; j < sv; j += stride) {
+    const uint4 v = __ldcs(si + j);
+    __stcs(so + j, make_uint4(fold_word(v.x, ws2), fold_word(v.y, ws2), fold_word(v.z, ws2), fold_word(v.w, ws2)));
+  }
+  for (int64_t j = (wv << 4) + tid; j < w_bytes; j += stride) w_out[j] = mo_w[j];
+  for (int64_t j = (sv << 4) + tid; j < s_bytes; j += stride) s_out[j] = (uint8_t)fold_byte(mo_ws[j], ws2);
+}
+
 }  // namespace
 
 cudaError_t launch_transcode(const uint8_t* mo_w, int64_t w_bytes, const uint8_t* mo_ws, int64_t s_bytes,
@@ -439,6 +487,14 @@ cudaError_t launch_quantize(const void* x, int x_dtype, const float* gs, int64_t
           static_cast<const __nv_bfloat16*>(x), gs, E, wpe, w, scales);
       break;
   }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_transcode_folded(const uint8_t* mo_w, int64_t w_bytes, const uint8_t* mo_ws, int64_t s_bytes,
+                                    const float* ws2, uint32_t* w_out, uint8_t* s_out, cudaStream_t st) {
+  const int64_t units = (w_bytes >> 4) / 4 + (s_bytes >> 4) + 16;
+  transcode_folded_kernel<<<stream_grid(transcode_folded_kernel, units), kStreamThreads, 0, st>>>(
+      mo_w, w_bytes, mo_ws, s_bytes, ws2, reinterpret_cast<uint8_t*>(w_out), s_out);
   return cudaGetLastError();
 }
 

@@ -230,6 +230,24 @@ def transcode(mo_weight, mo_weight_scale, weight_scale_2):
     return words.astype(np.uint32), scales, np.float32(gs)
 
 
+def fold_scales(mo_weight_scale, weight_scale_2) -> np.ndarray:
+    """The folded-scale alternative that issue #693 (Technical notes) rejects:
+    weight_scale * weight_scale_2 folded into each E4M3 byte, with no
+    sidecar. Byte = :func:`e4m3_encode` (f32(e4m3(b) * f32(ws2))): round to
+    nearest, ties to even, saturating at 448; products below half the
+    smallest subnormal become 0. Non-negative, finite scale bytes only."""
+    b = np.asarray(mo_weight_scale, dtype=np.uint8)
+    v = (e4m3_value(b).astype(np.float32) * np.float32(weight_scale_2)).astype(np.float32)
+    return e4m3_encode(v)
+
+
+def transcode_folded(mo_weight, mo_weight_scale, weight_scale_2):
+    """ModelOpt triplet -> (packed uint32 [N, K/8], folded E4M3 bytes [N, K/16]):
+    the words of :func:`transcode` and the scales of :func:`fold_scales`."""
+    words, _, _ = transcode(mo_weight, mo_weight_scale, weight_scale_2)
+    return words, fold_scales(mo_weight_scale, weight_scale_2)
+
+
 def modelopt_values(mo_weight, mo_weight_scale, weight_scale_2) -> np.ndarray:
     """ModelOpt's own dequantization fp4 * e4m3(weight_scale) * weight_scale_2 (float64).
 

@@ -161,6 +161,19 @@ def test_quantize_refusals(nv):
     assert call(N=0, w_len=0, s_len=0) == "OK"
 
 
+def test_transcode_folded_refusals(nv):
+    lib = nv.library()
+    ST = nv.STATUS
+    N, K = 8, 64
+    call = lambda **kw: ST[lib.nvfp4_transcode_folded(A, kw.get("wl", N * K // 2), A, kw.get("sl", N * K // 16),
+                                                      kw.get("ws2", A), N, kw.get("K", K), kw.get("wo", A), A, None)]
+    assert call(K=40, wl=N * 20, sl=N * 2) == "ERR_SHAPE"
+    assert call(wl=N * K // 2 + 16) == "ERR_PLANE"
+    assert call(sl=N * K // 16 - 1) == "ERR_PLANE"
+    assert call(ws2=None) == "ERR_NULL"
+    assert call(wo=U) == "ERR_ALIGN"
+
+
 def test_qmm_glu_empty_returns_ok(nv):
     assert glu_call(nv, M=0) == 0
     assert glu_call(nv, I=0, w_len=0, s_len=0) == 0

@@ -418,12 +418,33 @@ def pin_quantize_worked_cases(orc):
     assert s3[0, 0] == 0x7E and w3[0, 0] == 0xF7
 
 
+def pin_fold_scales(orc):
+    # ws2 = 1 leaves every finite non-negative byte as it is; ws2 = 2^k shifts
+    # the normal values' exponent field by k while they stay normal and finite;
+    # beyond 448 saturates; below half the smallest subnormal (2^-10) is 0
+    b = np.arange(0x7F, dtype=np.uint8)
+    assert orc.fold_scales(b, np.float32(1.0)).tolist() == list(range(0x7F))
+    normal = np.arange(0x08, 0x70, dtype=np.uint8)  # exponent fields 1..13
+    assert orc.fold_scales(normal, np.float32(2.0)).tolist() == [int(v) + 8 for v in normal]
+    assert orc.fold_scales(normal[8:], np.float32(0.5)).tolist() == [int(v) - 8 for v in normal[8:]]
+    assert orc.fold_scales(np.array([0x7E, 0x70]), np.float32(4.0)).tolist() == [0x7E, 0x7E]  # 448 * 4, 256 * 4
+    # 0x38 is 1.0: 1.0 * 2^-10 ties to 0, a little more rounds up to the smallest subnormal
+    assert orc.fold_scales(np.array([0x38, 0x38]), np.float32(2.0**-10)).tolist() == [0, 0]
+    assert orc.fold_scales(np.array([0x39]), np.float32(2.0**-10)).tolist() == [1]
+    # the words are those of the sidecar transcode
+    g = synth.rng(31)
+    mo_w, mo_ws, ws2 = synth.modelopt_triplet(g, 4, 64)
+    w, s = orc.transcode_folded(mo_w, mo_ws, ws2)
+    assert np.array_equal(w, orc.transcode(mo_w, mo_ws, ws2)[0])
+    assert np.array_equal(s, orc.fold_scales(mo_ws, ws2))
+
+
 PINS = [pin_e2m1_table, pin_e4m3_all_bytes, pin_packing, pin_block_scale_broadcast,
         pin_brute_force_matmul, pin_one_hot, pin_global_factor, pin_dequantize_rounding,
         pin_sidecar_identity, pin_transcode_layout, pin_gather_zero_rows, pin_plane_check,
         pin_error_metric, pin_gelu_tanh, pin_silu, pin_glu_halves, pin_nontransposed_brute_force,
         pin_nontransposed_identity, pin_pack_codes, pin_e2m1_encode, pin_e4m3_encode, pin_quantize_round_trip,
-        pin_quantize_worked_cases]
+        pin_quantize_worked_cases, pin_fold_scales]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=lambda p: p.__name__)
@@ -579,3 +600,10 @@ def test_planted_quantize_scale_off_by_constant(monkeypatch):
     _planted(monkeypatch, "quantize", lambda x, gs=None: orig(np.asarray(x, dtype=np.float32) * np.float32(1.5), gs))
     with pytest.raises(AssertionError):
         pin_quantize_round_trip(O)
+
+
+def test_planted_fold_without_ws2(monkeypatch):
+    orig = O.fold_scales
+    _planted(monkeypatch, "fold_scales", lambda b, ws2: orig(b, np.float32(1.0)))
+    with pytest.raises(AssertionError):
+        pin_fold_scales(O)
