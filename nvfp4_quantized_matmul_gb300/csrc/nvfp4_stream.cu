@@ -277,9 +277,76 @@ dequantize_kernel(const uint32_t* __restrict__ w, const uint8_t* __restrict__ sc
 // the hardware conversions (cvt.rn.satfinite); one reciprocal per block
 // instead of a division per element keeps the kernel bound by HBM.
 
-// x0 -> low nibble, x1 -> high nibble of each byte (cvt puts its first
-// source operand in the high nibble).
-__device__ __forceinline__ uint32_t f32x8_to_e2m1x8(const float (&q)[8]) {
+__device__ __forceinline__ uint32_t f32_to_e4m3_satfinite(float v) {
+  unsigned short h;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(h) : "f"(0.0f), "f"(v));
+  return (uint32_t)h & 0xFFu;
+}
+
+// One 16-column block's inputs as raw 16-byte words (four for f32).
+template <typename T> struct Raw16 { uint4 q[sizeof(T) == 4 ? 4 : 2]; };
+
+template <typename T>
+__device__ __forceinline__ void load_raw16(const T* p, Raw16<T>& r) {
+#pragma unroll
+  for (int i = 0; i < (int)(sizeof(r.q) / sizeof(uint4)); ++i) r.q[i] = __ldcs(reinterpret_cast<const uint4*>(p) + i);
+}
+
+__device__ __forceinline__ uint32_t u4get(const uint4& v, int i) { return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w; }
+
+// The block's sixteen values as eight f32 pairs (columns 2i, 2i + 1), and
+// max |x| over them. For 16-bit inputs the maximum is taken on the packed
+// halves (|x| by clearing the sign bits, then a packed max: exact), one
+// widening at the end.
+template <typename T> __device__ __forceinline__ float widen16(const Raw16<T>& r, float (&lo)[8], float (&hi)[8]);
+template <> __device__ __forceinline__ float widen16<float>(const Raw16<float>& r, float (&lo)[8], float (&hi)[8]) {
+  float am = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    lo[i] = __uint_as_float(u4get(r.q[i >> 1], 2 * (i & 1)));
+    hi[i] = __uint_as_float(u4get(r.q[i >> 1], 2 * (i & 1) + 1));
+    am = fmaxf(am, fmaxf(fabsf(lo[i]), fabsf(hi[i])));
+  }
+  return am;
+}
+template <> __device__ __forceinline__ float widen16<__nv_bfloat16>(const Raw16<__nv_bfloat16>& r, float (&lo)[8],
+                                                                   float (&hi)[8]) {
+  uint32_t m = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const uint32_t u = u4get(r.q[i >> 2], i & 3);
+    lo[i] = __uint_as_float(u << 16);
+    hi[i] = __uint_as_float(u & 0xFFFF0000u);
+    asm("max.bf16x2 %0, %0, %1;" : "+r"(m) : "r"(u & 0x7FFF7FFFu));
+  }
+  return fmaxf(__uint_as_float(m << 16), __uint_as_float(m & 0xFFFF0000u));
+}
+template <> __device__ __forceinline__ float widen16<__half>(const Raw16<__half>& r, float (&lo)[8], float (&hi)[8]) {
+  uint32_t m = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const uint32_t u = u4get(r.q[i >> 2], i & 3);
+    lo[i] = __half2float(__ushort_as_half((unsigned short)(u & 0xFFFFu)));
+    hi[i] = __half2float(__ushort_as_half((unsigned short)(u >> 16)));
+    asm("max.f16x2 %0, %0, %1;" : "+r"(m) : "r"(u & 0x7FFF7FFFu));
+  }
+  return fmaxf(__half2float(__ushort_as_half((unsigned short)(m & 0xFFFFu))),
+               __half2float(__ushort_as_half((unsigned short)(m >> 16))));
+}
+
+// (a, b) * (r, r), each product rounded to nearest (one packed multiply).
+__device__ __forceinline__ void mul2_rn(float& a, float& b, float r) {
+  uint64_t p, q, d;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(p) : "f"(a), "f"(b));
+  asm("mov.b64 %0, {%1, %1};" : "=l"(q) : "f"(r));
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(p), "l"(q));
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(d));
+}
+
+// Four (low, high) pairs -> one word of eight E2M1 codes, low column in the
+// low nibble (cvt puts its first source in the high nibble); +0 for a zero
+// magnitude (a negative value that rounds to zero).
+__device__ __forceinline__ uint32_t pack_e2m1x8(const float* lo, const float* hi) {
   uint32_t r;
   asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
       "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n\t"
@@ -288,105 +355,52 @@ __device__ __forceinline__ uint32_t f32x8_to_e2m1x8(const float (&q)[8]) {
       "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n\t"
       "mov.b32 %0, {b0, b1, b2, b3};\n\t}"
       : "=r"(r)
-      : "f"(q[0]), "f"(q[1]), "f"(q[2]), "f"(q[3]), "f"(q[4]), "f"(q[5]), "f"(q[6]), "f"(q[7]));
-  return r;
+      : "f"(lo[0]), "f"(hi[0]), "f"(lo[1]), "f"(hi[1]), "f"(lo[2]), "f"(hi[2]), "f"(lo[3]), "f"(hi[3]));
+  const uint32_t nz = (r | (r >> 1) | (r >> 2)) & 0x11111111u;
+  return (r & 0x77777777u) | (r & (nz << 3));
 }
 
-__device__ __forceinline__ uint32_t f32_to_e4m3_satfinite(float v) {
-  unsigned short h;
-  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(h) : "f"(0.0f), "f"(v));
-  return (uint32_t)h & 0xFFu;
-}
-
-// Eight input values as raw 16-byte words (two for f32), widened to f32 once
-// the loads of a step have all been issued.
-template <typename T> struct Raw8 { uint4 q[sizeof(T) == 4 ? 2 : 1]; };
-
-template <typename T>
-__device__ __forceinline__ void load_raw8(const T* p, Raw8<T>& r) {
-#pragma unroll
-  for (int i = 0; i < (int)(sizeof(r.q) / sizeof(uint4)); ++i) r.q[i] = __ldcs(reinterpret_cast<const uint4*>(p) + i);
-}
-
-template <typename T> __device__ __forceinline__ void widen8(const Raw8<T>& r, float (&v)[8]);
-template <> __device__ __forceinline__ void widen8<float>(const Raw8<float>& r, float (&v)[8]) {
-  const uint32_t u[8] = {r.q[0].x, r.q[0].y, r.q[0].z, r.q[0].w, r.q[1].x, r.q[1].y, r.q[1].z, r.q[1].w};
-#pragma unroll
-  for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(u[i]);
-}
-template <> __device__ __forceinline__ void widen8<__half>(const Raw8<__half>& r, float (&v)[8]) {
-  const uint32_t u[4] = {r.q[0].x, r.q[0].y, r.q[0].z, r.q[0].w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    v[2 * i] = __half2float(__ushort_as_half((unsigned short)(u[i] & 0xFFFFu)));
-    v[2 * i + 1] = __half2float(__ushort_as_half((unsigned short)(u[i] >> 16)));
-  }
-}
-template <> __device__ __forceinline__ void widen8<__nv_bfloat16>(const Raw8<__nv_bfloat16>& r, float (&v)[8]) {
-  const uint32_t u[4] = {r.q[0].x, r.q[0].y, r.q[0].z, r.q[0].w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    v[2 * i] = __uint_as_float(u[i] << 16);
-    v[2 * i + 1] = __uint_as_float(u[i] & 0xFFFF0000u);
-  }
-}
-
-// One output word (eight columns, half a scale block) per lane and step:
-// lanes 2b and 2b + 1 hold block b and exchange their maxima; the even lane
-// writes the scale byte. A warp's loads and word stores are contiguous.
+// One 16-column block (two output words and a scale byte) per thread and
+// step, two blocks in flight (64 or 128 bytes of loads a thread).
 template <typename T>
 __global__ void __launch_bounds__(kStreamThreads)
-quantize_kernel(const T* __restrict__ x, const float* __restrict__ gs, int64_t E, int64_t words_per_expert,
+quantize_kernel(const T* __restrict__ x, const float* __restrict__ gs, int64_t E, int64_t blocks_per_expert,
                 uint32_t* __restrict__ w, uint8_t* __restrict__ scales) {
-  const int lane = threadIdx.x & 31;
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-  const int64_t first = (int64_t)blockIdx.x * blockDim.x + (threadIdx.x & ~31);
+  const int64_t first = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   for (int64_t e = blockIdx.y; e < E; e += gridDim.y) {
     const bool has_gs = gs != nullptr;
     const float fac = global_factor(gs, e);
     const float inv = has_gs ? __fdiv_rn(kGlobalScaleDivisor, __ldg(gs + e)) : 1.0f;
-    const int64_t base = e * words_per_expert;
-    constexpr int kU = sizeof(T) == 4 ? 2 : 4;  // 32 or 16 bytes a lane per step in flight, times kU
-    for (int64_t u0 = first; u0 < words_per_expert; u0 += kU * stride) {  // warp-uniform
-      Raw8<T> raw[kU];
+    const int64_t base = e * blocks_per_expert;
+    constexpr int kU = 2;
+    for (int64_t b0 = first; b0 < blocks_per_expert; b0 += kU * stride) {
+      Raw16<T> raw[kU];
 #pragma unroll
       for (int k = 0; k < kU; ++k) {
-        const int64_t u = u0 + k * stride + lane;
-        if (u < words_per_expert) {
-          load_raw8<T>(x + 8 * (base + u), raw[k]);
-        } else {
-#pragma unroll
-          for (int i = 0; i < (int)(sizeof(raw[k].q) / sizeof(uint4)); ++i) raw[k].q[i] = make_uint4(0, 0, 0, 0);
-        }
+        const int64_t b = b0 + k * stride;
+        if (b < blocks_per_expert) load_raw16<T>(x + 16 * (base + b), raw[k]);
       }
 #pragma unroll
       for (int k = 0; k < kU; ++k) {
-        const int64_t u = u0 + k * stride + lane;  // words per expert is even: pairs are valid together
-        float v[8];
-        widen8<T>(raw[k], v);
-        float am = 0.0f;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) am = fmaxf(am, fabsf(v[i]));
-        am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 1));
+        const int64_t b = b0 + k * stride;
+        if (b >= blocks_per_expert) break;
+        float lo[8], hi[8];
+        const float am = widen16<T>(raw[k], lo, hi);
         float sc = __fdiv_rn(am, 6.0f);
         if (has_gs) sc = __fmul_rn(sc, inv);
         const uint32_t sbyte = f32_to_e4m3_satfinite(sc);
         const float d = __fmul_rn(e4m3_to_f32(sbyte), fac);
-        uint32_t word = 0;
+        uint2 out = make_uint2(0u, 0u);
         if (d > 0.0f) {
           const float r = __frcp_rn(d);
-          float q[8];
 #pragma unroll
-          for (int i = 0; i < 8; ++i) q[i] = __fmul_rn(v[i], r);
-          word = f32x8_to_e2m1x8(q);
-          // +0 for a zero magnitude (a negative value that rounds to zero)
-          const uint32_t nz = (word | (word >> 1) | (word >> 2)) & 0x11111111u;
-          word = (word & 0x77777777u) | (word & (nz << 3));
+          for (int i = 0; i < 8; ++i) mul2_rn(lo[i], hi[i], r);
+          out.x = pack_e2m1x8(lo, hi);
+          out.y = pack_e2m1x8(lo + 4, hi + 4);
         }
-        if (u < words_per_expert) {
-          __stcs(w + base + u, word);
-          if ((lane & 1) == 0) scales[(base + u) >> 1] = (uint8_t)sbyte;
-        }
+        __stcs(reinterpret_cast<uint2*>(w) + base + b, out);
+        scales[base + b] = (uint8_t)sbyte;
       }
     }
   }
@@ -465,10 +479,10 @@ cudaError_t launch_transcode(const uint8_t* mo_w, int64_t w_bytes, const uint8_t
 
 cudaError_t launch_quantize(const void* x, int x_dtype, const float* gs, int64_t E, int64_t N, int64_t K,
                             uint32_t* w, uint8_t* scales, cudaStream_t st) {
-  const int64_t wpe = N * (K / 8);  // output words per expert
+  const int64_t bpe = N * (K / 16);  // 16-column blocks per expert
   auto grid_of = [&](auto kern) {
-    int gx = stream_grid(kern, (wpe * E + 3) / 4);
-    const int64_t per_expert = (wpe + kStreamThreads - 1) / kStreamThreads;
+    int gx = stream_grid(kern, (bpe * E + 1) / 2);
+    const int64_t per_expert = (bpe + kStreamThreads - 1) / kStreamThreads;
     if (gx > per_expert) gx = (int)(per_expert < 1 ? 1 : per_expert);
     const int gy = (int)(E < 65535 ? E : 65535);
     return dim3(gx, gy);
@@ -476,15 +490,15 @@ cudaError_t launch_quantize(const void* x, int x_dtype, const float* gs, int64_t
   switch (x_dtype) {
     case kF32:
       quantize_kernel<float><<<grid_of(quantize_kernel<float>), kStreamThreads, 0, st>>>(
-          static_cast<const float*>(x), gs, E, wpe, w, scales);
+          static_cast<const float*>(x), gs, E, bpe, w, scales);
       break;
     case kF16:
       quantize_kernel<__half><<<grid_of(quantize_kernel<__half>), kStreamThreads, 0, st>>>(
-          static_cast<const __half*>(x), gs, E, wpe, w, scales);
+          static_cast<const __half*>(x), gs, E, bpe, w, scales);
       break;
     default:
       quantize_kernel<__nv_bfloat16><<<grid_of(quantize_kernel<__nv_bfloat16>), kStreamThreads, 0, st>>>(
-          static_cast<const __nv_bfloat16*>(x), gs, E, wpe, w, scales);
+          static_cast<const __nv_bfloat16*>(x), gs, E, bpe, w, scales);
       break;
   }
   return cudaGetLastError();
