@@ -603,7 +603,10 @@ def run_routes(nv, synth, torch, dev, stream, args):
                                          "frac_hbm": round(b / (ms * 1e-3) / 1e9 / hbm_peak, 4)}
     del d, w, s
 
-    # MoE GatherQMM: 128 experts, gate/up [1536, 2048], down [2048, 768].
+    # MoE GatherQMM: 128 experts, gate/up [1536, 2048], down [2048, 768]. The
+    # routing comes from its own generator, so the drawn experts do not depend
+    # on what the entries above drew.
+    g = synth.rng(3100)
     E = 128
     moe = {}
     for name, n, k in (("gate_up", 1536, 2048), ("down", 2048, 768)):
