@@ -170,12 +170,15 @@ nvfp4_status nvfp4_qmm_routed(const void* x, nvfp4_dtype x_dtype, int64_t M, int
  *   x_dtype. N % 16 == 0 (ERR_SHAPE otherwise). x, y, w and scales 16-byte
  *   aligned (ERR_ALIGN). M == 0 or N == 0 returns OK without a launch; K == 0
  *   writes zeros.
- * One route for every M, as on the pages (the dequantize + GEMM route): the
- * tcgen05 tensor-core kernel, whose producer warps decode and transpose the
- * weight tiles into shared memory. With K % 8 != 0 the activations are first
- * copied, rows padded with zeros to a multiple of 8 elements, into the
- * per-stream buffer of the gathered activations (grown on demand, freed by
- * nvfp4_shutdown()).
+ * One or two token rows: one streaming pass over the plane (a warp per 256
+ * outputs x 128 inputs), partial sums added into a float workspace [2, N]
+ * owned by the library, one per (device, stream), returned to zero by every
+ * call; then y. More rows (or NVFP4_NT_DECODE=0): the tcgen05 tensor-core
+ * kernel, whose producer warps decode and transpose the weight tiles into
+ * shared memory (the pages send every M to dequantize + GEMM). With
+ * K % 8 != 0 the tensor-core route first copies the activations, rows padded
+ * with zeros to a multiple of 8 elements, into the per-stream buffer of the
+ * gathered activations (grown on demand, freed by nvfp4_shutdown()).
  */
 nvfp4_status nvfp4_qmm_nontransposed(const void* x, nvfp4_dtype x_dtype, int64_t M, int64_t K, const uint32_t* w,
                                      int64_t w_len, const uint8_t* scales, int64_t scales_len, const float* gs,

@@ -20,7 +20,8 @@ LIB = os.path.join(PKG, "libnvfp4.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-O2", "--expt-relaxed-constexpr",
          "-I", os.path.join(ROOT, "include")]
-SOURCES = ["nvfp4_api.cu", "nvfp4_stream.cu", "nvfp4_qmv.cu", "nvfp4_qmv_tma.cu", "nvfp4_qmv_stream.cu", "nvfp4_qmm_tc.cu"]
+SOURCES = ["nvfp4_api.cu", "nvfp4_stream.cu", "nvfp4_qmv.cu", "nvfp4_qmv_tma.cu", "nvfp4_qmv_stream.cu", "nvfp4_qmm_tc.cu",
+           "nvfp4_qmv_nt.cu"]
 
 
 def _nvcc() -> str:

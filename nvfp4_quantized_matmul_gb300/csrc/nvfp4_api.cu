@@ -153,6 +153,7 @@ int32_t nvfp4_take_device_error(void) {
 void nvfp4_shutdown(void) {
   nvfp4::release_stream_workspaces();
   nvfp4::release_gather_workspaces();
+  nvfp4::release_nt_workspaces();
 }
 
 nvfp4_status nvfp4_transcode(const uint8_t* mo_weight, int64_t mo_weight_len, const uint8_t* mo_weight_scale,
@@ -374,6 +375,10 @@ nvfp4_status nvfp4_qmm_nontransposed(const void* x, nvfp4_dtype x_dtype, int64_t
   if (!aligned(x, 16) || !aligned(y, 16)) return fail(NVFP4_ERR_ALIGN, "%s: x and y must be 16-byte aligned", fn);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (K == 0) return cuda_status(fn, cudaMemsetAsync(y, 0, (size_t)(M * N * dtype_size(x_dtype)), st));
+  // one or two token rows: one streaming pass (NVFP4_NT_DECODE=0 sends every M to the tensor cores)
+  const char* dec = std::getenv("NVFP4_NT_DECODE");
+  if (!(dec && dec[0] == '0') && nvfp4::qmv_nt_supported(M, N, K))
+    return cuda_status(fn, nvfp4::launch_qmv_nt(x, (int)x_dtype, M, K, w, scales, gs, N, y, st));
   if (!nvfp4::qmm_tc_nt_supported(M, N, K))
     return fail(NVFP4_ERR_LIMIT, "%s: M or K of 2^31 or more, or too many tiles", fn);
   return cuda_status(fn, nvfp4::launch_qmm_tc_nt(x, (int)x_dtype, M, K, w, scales, gs, N, y, st));

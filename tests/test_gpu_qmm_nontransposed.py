@@ -9,7 +9,9 @@ activations are padded into a scratch buffer first) or of the 64-input
 k-block, N ending inside a weight tile and inside a word pair, one and two
 128-row halves, both dtypes, the global scale, back-to-back calls, a CUDA
 graph replay and the prefill shape at full size on sampled outputs, with
-the stream-K split of the k-blocks and with whole tiles.
+the stream-K split of the k-blocks and with whole tiles; and the decode
+route (one or two token rows: one streaming pass, partial sums in a float
+workspace) on its own shapes, against the tensor cores and in a graph.
 """
 import numpy as np
 import pytest
@@ -45,8 +47,10 @@ NT_SHAPES = [(1, 17, 32), (3, 64, 272), (130, 100, 512), (257, 300, 1008), (600,
 @pytest.mark.parametrize("with_gs", [False, True])
 @pytest.mark.parametrize("split", ["1", "0"], ids=["streamk", "whole_tiles"])
 def test_nontransposed_parity(nv, monkeypatch, mkn, dt, with_gs, split):
-    # below two waves of tiles the k-blocks are split over the CTAs unless
-    # NVFP4_TC_STREAMK=0 deals whole tiles
+    # the tensor-core route for every M here (the decode route has its own
+    # tests below); below two waves of tiles the k-blocks are split over the
+    # CTAs unless NVFP4_TC_STREAMK=0 deals whole tiles
+    monkeypatch.setenv("NVFP4_NT_DECODE", "0")
     monkeypatch.setenv("NVFP4_TC_STREAMK", split)
     M, K, N = mkn
     w, s = weights(M + 7 * K + N, K, N)  # [K, N/8] words, [K, N/16] scales
@@ -121,7 +125,68 @@ def test_nontransposed_zero_k_and_empty(nv):
     assert y.shape == (5, 64) and bool((y == 0).all())
 
 
-@pytest.mark.parametrize("M", [1, 2048])
+# (M, K, N) for the decode route (M <= 2): K inside one 128-input task, across
+# tasks with a ragged last one, not a multiple of 8; N ending inside a
+# 256-output slab and inside a word pair
+NT_DECODE = [(1, 17, 32), (2, 100, 272), (1, 128, 1008), (2, 300, 256), (1, 2048, 2560), (2, 5376, 4096),
+             (1, 777, 528), (2, 21504, 512)]
+
+
+@pytest.mark.parametrize("mkn", NT_DECODE, ids=lambda v: "M%d_K%d_N%d" % v)
+@pytest.mark.parametrize("dt", ["f16", "bf16"])
+@pytest.mark.parametrize("with_gs", [False, True])
+def test_nontransposed_decode_route(nv, mkn, dt, with_gs):
+    M, K, N = mkn
+    w, s = weights(5 * M + 3 * K + N, K, N)
+    g = synth.rng(7 * M + K + 3 * N)
+    x = synth.activations(g, (M, K), dt)
+    gs = np.float32(2688 * 0.71) if with_gs else None
+    ref = O.qmm_nontransposed(x.double().numpy(), w, s, gs)
+    dx, dw, ds = x.cuda(), u32_to_dev(w), u8_to_dev(s)
+    for rep in range(2):  # the second call finds the workspace as the first left it
+        y, backing, guard = guarded_empty((M, N), TORCH[dt], fill=-7.0)
+        nv.qmm_nontransposed(dx, dw, ds, gs=None if gs is None else float(gs), out=y)
+        torch.cuda.synchronize()
+        assert nv.take_device_error() == 0
+        err = rel_err(y, ref)
+        assert err <= TOL[dt], f"call {rep}: rel-to-max error {err:.3g} > {TOL[dt]}"
+        assert guards_intact(backing, guard)
+
+
+def test_nontransposed_decode_routes_agree(nv, monkeypatch):
+    """The streaming route and the tensor cores compute the same sums."""
+    M, K, N = 2, 2048, 4096
+    w, s = weights(123, K, N)
+    x = synth.activations(synth.rng(124), (M, K), "bf16").cuda()
+    dw, ds = u32_to_dev(w), u8_to_dev(s)
+    a = nv.qmm_nontransposed(x, dw, ds).float()
+    monkeypatch.setenv("NVFP4_NT_DECODE", "0")
+    b = nv.qmm_nontransposed(x, dw, ds).float()
+    torch.cuda.synchronize()
+    assert nv.take_device_error() == 0
+    assert (a - b).abs().max().item() <= 2 * 2.0**-8 * b.abs().max().item()
+
+
+def test_nontransposed_decode_graph_replay(nv):
+    M, K, N = 2, 1000, 2048
+    w, s = weights(131, K, N)
+    x = synth.activations(synth.rng(132), (M, K), "bf16").cuda()
+    dw, ds = u32_to_dev(w), u8_to_dev(s)
+    y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    gs = torch.tensor([2688.0 * 0.5], dtype=torch.float32, device="cuda")  # made before the capture
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        nv.qmm_nontransposed(x, dw, ds, gs=gs, out=y)
+    ref = O.qmm_nontransposed(x.cpu().double().numpy(), w, s, np.float32(2688.0 * 0.5))
+    for _ in range(3):
+        y.fill_(-7.0)
+        graph.replay()
+        torch.cuda.synchronize()
+        assert nv.take_device_error() == 0
+        assert rel_err(y, ref) <= TOL["bf16"]
+
+
+@pytest.mark.parametrize("M", [1, 8, 2048])
 def test_nontransposed_prefill_shape_sampled(nv, M):
     """The MLP up shape with the weight stored non-transposed: [5376, 21504 / 8]
     words; sampled outputs against the oracle's per-entry dot products."""
