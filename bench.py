@@ -707,6 +707,8 @@ def run_case(args):
     warm-up call then one call.
     nontransposed_prefill: nvfp4_qmm_nontransposed at M = 2048 on a [5376,
     21504 / 8] plane (whole tiles), one warm-up call then one call.
+    nontransposed_decode: the same plane at M = 1 (the streaming kernel), one
+    warm-up call then one call.
     quantize: nvfp4_quantize of a dense bf16 [43008, 5376] plane with gs =
     max |x|, one warm-up call then one call.
     """
@@ -740,6 +742,18 @@ def run_case(args):
             nv.qmm_nontransposed(x, w, s)
         torch.cuda.synchronize(dev)
         print("case nontransposed_prefill ok")
+        return
+    if args.case == "nontransposed_decode":
+        g = synth.rng(5500)
+        k, n = 5376, 21504
+        w = torch.randint(-2**31, 2**31 - 1, (k, n // 8), dtype=torch.int32, device=dev,
+                          generator=torch.Generator(device=dev).manual_seed(9))
+        s = torch.from_numpy(synth.log_uniform_scales(g, (k, n // 16), 2.0**-6, 4.0)).to(dev)
+        x = synth.activations(g, (1, k), "bf16").to(dev)
+        for _ in range(2):
+            nv.qmm_nontransposed(x, w, s)
+        torch.cuda.synchronize(dev)
+        print("case nontransposed_decode ok")
         return
     if args.case == "quantize":
         n, k = 43008, 5376
@@ -848,7 +862,7 @@ def main():
     ap.add_argument("--cpu-rows", type=int, default=6144)
     ap.add_argument("--ref-rows", type=int, default=32)
     ap.add_argument("--case", choices=["qmv_small", "qmv_shapes", "decode_step", "prefill", "gather_prefill",
-                                       "nontransposed_prefill", "quantize"],
+                                       "nontransposed_prefill", "nontransposed_decode", "quantize"],
                     default=None,
                     help="run one small profiling case instead of the benchmark")
     args = ap.parse_args()
