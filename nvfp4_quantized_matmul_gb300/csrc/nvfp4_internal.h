@@ -94,7 +94,7 @@ cudaError_t launch_qmm_tc_glu(const void* x, int xdt, int64_t M, int64_t K, cons
 bool qmm_tc_nt_supported(int64_t M, int64_t N, int64_t K);
 // Up to kQmvNtMaxM token rows of a non-transposed weight: one streaming pass
 // over the plane, partial sums in a per-stream float workspace, then y. On
-// GB300 it beat the tensor cores at one and two rows ([5376, 21504]: 33 / 54
+// GB300 it beat the tensor cores at one and two rows ([5376, 21504]: 30 / 52
 // µs against 86 / 66) and lost from three on (74 against 67).
 constexpr int64_t kQmvNtMaxM = 2;
 bool qmv_nt_supported(int64_t M, int64_t N, int64_t K);

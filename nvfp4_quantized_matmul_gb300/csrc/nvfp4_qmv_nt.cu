@@ -86,14 +86,29 @@ template <> __device__ __forceinline__ float x_at<__half>(const uint4& v, int kk
   return __half2float(__ushort_as_half((unsigned short)((kk & 1) ? (u >> 16) : (u & 0xFFFFu))));
 }
 
+// (c0, c1) += (a, a) * (b0, b1), each an IEEE fma (one packed instruction).
+__device__ __forceinline__ void fma2(float& c0, float& c1, float a, float b0, float b1) {
+  asm("{\n\t.reg .b64 pa, pb, pc;\n\t"
+      "mov.b64 pa, {%2, %2};\n\t"
+      "mov.b64 pb, {%3, %4};\n\t"
+      "mov.b64 pc, {%0, %1};\n\t"
+      "fma.rn.f32x2 pc, pa, pb, pc;\n\t"
+      "mov.b64 {%0, %1}, pc;\n\t}"
+      : "+f"(c0), "+f"(c1)
+      : "f"(a), "f"(b0), "f"(b1));
+}
+
+// The block scale goes into the activation (x * e4m3 has at most 15
+// significant bits, exact in f32), so each code needs only its E2M1 value;
+// every product x * e4m3 * fp4 is exact as before.
 template <typename T, int MT>
 __device__ __forceinline__ void nt_accumulate(const NtGroup<MT>& g, int lane, float (&acc)[MT][8]) {
 #pragma unroll
   for (int kk = 0; kk < 8; ++kk) {
     const uint32_t quad = __shfl_sync(0xffffffffu, g.s, kk * 4 + (lane >> 3));
-    const uint32_t sb = (quad >> (8 * ((lane >> 1) & 3))) & 0xFFu;
+    const float sf = e4m3_to_f32((quad >> (8 * ((lane >> 1) & 3))) & 0xFFu);
     uint32_t h[4];
-    decode8_scaled_f16(g.w[kk], e4m3_to_f16x2_bcast(sb), h);  // exact products
+    e2m1x8_to_f16x2(g.w[kk], h);
     float v[8];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -103,9 +118,9 @@ __device__ __forceinline__ void nt_accumulate(const NtGroup<MT>& g, int lane, fl
     }
 #pragma unroll
     for (int m = 0; m < MT; ++m) {
-      const float xm = x_at<T>(g.x[m], kk);
+      const float xs = __fmul_rn(x_at<T>(g.x[m], kk), sf);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) acc[m][i] = fmaf(xm, v[i], acc[m][i]);
+      for (int i = 0; i < 4; ++i) fma2(acc[m][2 * i], acc[m][2 * i + 1], xs, v[2 * i], v[2 * i + 1]);
     }
   }
 }
