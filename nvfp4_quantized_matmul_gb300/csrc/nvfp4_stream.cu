@@ -286,10 +286,14 @@ __device__ __forceinline__ uint32_t f32_to_e4m3_satfinite(float v) {
 // One 16-column block's inputs as raw 16-byte words (four for f32).
 template <typename T> struct Raw16 { uint4 q[sizeof(T) == 4 ? 4 : 2]; };
 
+// Cached loads: a warp's 16-byte loads each cover every other 16 (or 48)
+// bytes of its span, and the lines they bring into L1 serve the thread's
+// next load (with evict-first loads: 91.9 against 90.3 us on the bf16
+// gate/up plane, 172 against 167 with f32 input).
 template <typename T>
 __device__ __forceinline__ void load_raw16(const T* p, Raw16<T>& r) {
 #pragma unroll
-  for (int i = 0; i < (int)(sizeof(r.q) / sizeof(uint4)); ++i) r.q[i] = __ldcs(reinterpret_cast<const uint4*>(p) + i);
+  for (int i = 0; i < (int)(sizeof(r.q) / sizeof(uint4)); ++i) r.q[i] = __ldg(reinterpret_cast<const uint4*>(p) + i);
 }
 
 __device__ __forceinline__ uint32_t u4get(const uint4& v, int i) { return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w; }
