@@ -485,8 +485,10 @@ __device__ __forceinline__ void w_load_nt(WTaskNT& t, const Cur& cur, const TcPa
   t.s = sv;
 }
 
+// lut: shared-memory table of Dt<T>::scale for the 256 scale bytes (a lane
+// converts eight scale bytes per k-block, one per input row).
 template <typename T>
-__device__ __forceinline__ void w_store_nt(uint32_t stage_base, int v, int j, const WTaskNT& t) {
+__device__ __forceinline__ void w_store_nt(uint32_t stage_base, int v, int j, const WTaskNT& t, uint32_t lut) {
   const int rot = j & 7;
   uint32_t o[8][4];
 #pragma unroll
@@ -494,7 +496,9 @@ __device__ __forceinline__ void w_store_nt(uint32_t stage_base, int v, int j, co
     // the scale byte of the lane's 16-output block (j / 2) for input kk
     const uint32_t quad = __shfl_sync(0xffffffffu, t.s, kk * 4 + (j >> 3));
     const uint32_t sb = (quad >> (8 * ((j >> 1) & 3))) & 0xFFu;
-    Dt<T>::decode(__funnelshift_r(t.w[kk], t.w[kk], 4 * rot), Dt<T>::scale(sb), o[kk]);
+    uint32_t sc;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(sc) : "r"(lut + 4u * sb));
+    Dt<T>::decode(__funnelshift_r(t.w[kk], t.w[kk], 4 * rot), sc, o[kk]);
   }
   const uint32_t rows = stage_base + (uint32_t)j * 1024u;  // B rows 8j..8j+7
 #pragma unroll
@@ -512,7 +516,7 @@ __device__ __forceinline__ void w_store_nt(uint32_t stage_base, int v, int j, co
 
 template <typename T, typename C>
 __device__ void producer_role_nt(const TcParams& p, uint32_t sB, uint32_t bars, volatile int* abort_flag,
-                                 int num_tiles) {
+                                 int num_tiles, uint32_t lut) {
   static_assert(C::BN == 256 && kProducerWarps * 8 == BK, "one word column per lane, eight inputs per warp");
   // one k-block of words loaded ahead (nine registers): on GB300 this ran
   // faster than two or three ahead (M = 8192 on [5376, 21504]: 1683 us
@@ -534,7 +538,7 @@ __device__ void producer_role_nt(const TcParams& p, uint32_t sB, uint32_t bars, 
     const int s = (int)(u % STAGES);
     const uint32_t ph = (u / STAGES) & 1;
     if (!wait_bar_warp(bars + 8 * (2 * STAGES + s), ph ^ 1, abort_flag, 3, &g_tc_error)) return false;  // stage empty
-    w_store_nt<T>(sB + (uint32_t)s * C::B_BYTES, v, j, t);
+    w_store_nt<T>(sB + (uint32_t)s * C::B_BYTES, v, j, t, lut);
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     __syncwarp();
     if (j == 0) mbar_arrive(bars + 8 * (STAGES + s));  // fullB
@@ -633,7 +637,7 @@ __device__ void producer_role_sk(const TcParams& p, uint32_t sB, uint32_t bars, 
 // schedule, the decode and transpose of producer_role_nt.
 template <typename T, typename C>
 __device__ void producer_role_sk_nt(const TcParams& p, uint32_t sB, uint32_t bars, volatile int* abort_flag,
-                                    Sched sched) {
+                                    Sched sched, uint32_t lut) {
   static_assert(C::BN == 256 && kProducerWarps * 8 == BK, "one word column per lane, eight inputs per warp");
   constexpr int STAGES = C::STAGES, PF = 2, BM = C::BM;  // as in producer_role_nt
   const int v = (int)(threadIdx.x >> 5) - C::kWarpProd0;
@@ -653,7 +657,7 @@ __device__ void producer_role_sk_nt(const TcParams& p, uint32_t sB, uint32_t bar
     const int s = (int)(u % STAGES);
     const uint32_t ph = (u / STAGES) & 1;
     if (!wait_bar_warp(bars + 8 * (2 * STAGES + s), ph ^ 1, abort_flag, 3, &g_tc_error)) return false;  // stage empty
-    w_store_nt<T>(sB + (uint32_t)s * C::B_BYTES, v, j, t);
+    w_store_nt<T>(sB + (uint32_t)s * C::B_BYTES, v, j, t, lut);
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     __syncwarp();
     if (j == 0) mbar_arrive(bars + 8 * (STAGES + s));  // fullB
@@ -795,6 +799,9 @@ qmm_tc_kernel(const __grid_constant__ CUtensorMap xmap, const TcParams p) {
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
   if (GATHER) build_gather_tables<BM>(p, samp, seg, pre);  // ends with __syncthreads
+  if constexpr (kNT) {  // the scale table of the non-transposed producer (1 KB past the barriers)
+    if (threadIdx.x < 256) samp[threadIdx.x] = Dt<T>::scale(threadIdx.x);
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -1039,7 +1046,7 @@ qmm_tc_kernel(const __grid_constant__ CUtensorMap xmap, const TcParams p) {
     }
   } else if (warp >= C::kWarpProd0) {
     if constexpr (kNT)
-      producer_role_nt<T, C>(p, sB, bars, abort_flag, num_tiles);
+      producer_role_nt<T, C>(p, sB, bars, abort_flag, num_tiles, smem_u32(samp));
     else
       producer_role<T, C, GATHER, kGlu>(p, sB, bars, abort_flag, num_tiles, seg, pre);
   }
@@ -1102,6 +1109,9 @@ qmm_tc_sk_kernel(const __grid_constant__ CUtensorMap xmap, const TcParams p) {
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
   if (GATHER) build_gather_tables<BM>(p, samp, seg, pre);  // ends with __syncthreads
+  if constexpr (kNT) {  // the scale table of the non-transposed producer (1 KB past the barriers)
+    if (threadIdx.x < 256) samp[threadIdx.x] = Dt<T>::scale(threadIdx.x);
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -1360,7 +1370,7 @@ qmm_tc_sk_kernel(const __grid_constant__ CUtensorMap xmap, const TcParams p) {
     }
   } else if (warp >= C::kWarpProd0) {
     if constexpr (kNT)
-      producer_role_sk_nt<T, C>(p, sB, bars, abort_flag, sched);
+      producer_role_sk_nt<T, C>(p, sB, bars, abort_flag, sched, smem_u32(samp));
     else
       producer_role_sk<T, C, GATHER>(p, sB, bars, abort_flag, sched, seg, pre);
   }
@@ -1849,9 +1859,10 @@ cudaError_t launch_nt_cfg(const void* x, int64_t M, int64_t K, const uint32_t* w
     p.ws_cnt = ws.cnt;
   }
   auto kern = p.sk_tiles > 0 ? qmm_tc_sk_kernel<T, C, false, true, true> : qmm_tc_kernel<T, C, false, false, true>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
+  const size_t smem = C::SMEM + 1024;  // + the producer's scale table
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  kern<<<grid, C::THREADS, C::SMEM, st>>>(map, p);
+  kern<<<grid, C::THREADS, smem, st>>>(map, p);
   return cudaGetLastError();
 }
 
