@@ -40,9 +40,13 @@ one-hot products; the non-transposed product against an exact-rational
 brute force indexed [input, output] and through identity activations; the
 quantizer's encoders against a brute-force nearest search and hand-worked
 ties, the quantizer through its round trip with dequantize and a worked
-global-scale case). The equivalence of ModelOpt's on-disk nibble order with the MLX
-order is taken from the page ("likely matches") and is parity unpinned: no
-real checkpoint is available to confirm it.
+global-scale case; the folded scales against the identity at ws2 = 1, exact
+power-of-two shifts, saturation and underflow). The quantizer's and the
+folded scales' rounding rules (nearest, ties to even, saturating) are this
+module's reading, pinned to their own definitions: the pages name the
+conventions, not the rounding. The equivalence of ModelOpt's on-disk nibble
+order with the MLX order is taken from the page ("likely matches") and is
+parity unpinned: no real checkpoint is available to confirm it.
 """
 from __future__ import annotations
 
