@@ -131,6 +131,22 @@ def pin_brute_force_matmul(orc):
         assert np.max(np.abs(got - ref)) <= 1e-12 * max(1.0, np.max(np.abs(ref)))
 
 
+def pin_qmm_entries(orc):
+    # the per-entry products used for sampled full-size checks equal the
+    # exact-rational brute force at the same (row, column) pairs
+    g = synth.rng(6)
+    m, n, k = 4, 7, 64
+    codes = g.integers(0, 16, size=(n, k))
+    sbytes = synth.log_uniform_scales(g, (n, k // 16), 2.0**-4, 2.0**4)
+    x = synth.activations(g, (m, k), "bf16").double().numpy()
+    gs = np.float32(123.0)
+    ref = _brute_force_qmm(x, codes, sbytes, gs)
+    rows = np.array([0, 3, 2, 1, 3])
+    cols = np.array([6, 0, 3, 5, 6])
+    got = orc.qmm_entries(x, pack_codes(codes), sbytes, gs, rows, cols)
+    assert np.max(np.abs(got - ref[rows, cols])) <= 1e-12 * max(1.0, np.max(np.abs(ref)))
+
+
 def pin_one_hot(orc):
     # unit scales and one-hot activations pick out single table entries
     n, k = 16, 32
@@ -440,7 +456,7 @@ def pin_fold_scales(orc):
 
 
 PINS = [pin_e2m1_table, pin_e4m3_all_bytes, pin_packing, pin_block_scale_broadcast,
-        pin_brute_force_matmul, pin_one_hot, pin_global_factor, pin_dequantize_rounding,
+        pin_brute_force_matmul, pin_qmm_entries, pin_one_hot, pin_global_factor, pin_dequantize_rounding,
         pin_sidecar_identity, pin_transcode_layout, pin_gather_zero_rows, pin_plane_check,
         pin_error_metric, pin_gelu_tanh, pin_silu, pin_glu_halves, pin_nontransposed_brute_force,
         pin_nontransposed_identity, pin_pack_codes, pin_e2m1_encode, pin_e4m3_encode, pin_quantize_round_trip,
