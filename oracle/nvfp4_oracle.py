@@ -40,8 +40,10 @@ one-hot products; the non-transposed product against an exact-rational
 brute force indexed [input, output] and through identity activations; the
 quantizer's encoders against a brute-force nearest search and hand-worked
 ties, the quantizer through its round trip with dequantize and a worked
-global-scale case; the folded scales against the identity at ws2 = 1, exact
-power-of-two shifts, saturation and underflow). The quantizer's and the
+global-scale case, the quantizer's code choice against exact rational
+arithmetic at, above and below every midpoint for block multipliers whose
+reciprocal is inexact; the folded scales against the identity at ws2 = 1,
+exact power-of-two shifts, saturation and underflow). The quantizer's and the
 folded scales' rounding rules (nearest, ties to even, saturating) are this
 module's reading, pinned to their own definitions: the pages name the
 conventions, not the rounding. The equivalence of ModelOpt's on-disk nibble
@@ -344,21 +346,44 @@ def e2m1_encode(v) -> np.ndarray:
     return _round_to_grid(v, E2M1_MAGNITUDES).astype(np.int64)
 
 
+def e2m1_encode_quotient(a, d) -> np.ndarray:
+    """Magnitude code (0..7) of the E2M1 value nearest to the exact quotient
+    ``a / d`` (a >= 0, d > 0, both float32 values): ties to the even code,
+    saturating at 6 (code 7).
+
+    The quotient is never formed. For each midpoint m of two neighbouring
+    grid values, ``a`` is compared with ``m * d`` in float64, where the product
+    is exact (m has at most three significant bits, d at most 24), so every
+    decision is the exact one; the code is the number of midpoints the
+    quotient lies above, a quotient equal to a midpoint counting it only when
+    the code above it is even.
+    """
+    a = np.asarray(a, dtype=np.float64)
+    d = np.asarray(d, dtype=np.float64)
+    code = np.zeros(np.broadcast(a, d).shape, dtype=np.int64)
+    for i in range(len(E2M1_MAGNITUDES) - 1):
+        m = (E2M1_MAGNITUDES[i] + E2M1_MAGNITUDES[i + 1]) / 2.0
+        md = m * d
+        code += (a > md) | ((a == md) & ((i + 1) % 2 == 0))
+    return code
+
+
 def quantize(x, gs=None):
     """Dense -> NVFP4 planes ``(w [..., K/8] uint32, scales [..., K/16] uint8)``.
 
     The encoding half of MLX's global-scale convention (PR #2629,
     Implementation Review Summary: fp_quantize encodes block scales times
     448 * 6 / global_scale), with the rounding and saturation the pages leave
-    open read as follows, every step in IEEE float32 with round to nearest
-    even, per 16-column block:
+    open read as follows, per 16-column block:
 
-    * amax = max |x|; s = amax / 6, then s * (2688 / gs) when gs is given;
+    * amax = max |x|; s = amax / 6, then s * (2688 / gs) when gs is given
+      (each step an IEEE float32 operation, round to nearest even);
     * scale byte = :func:`e4m3_encode` (s);
-    * d = e4m3(byte) * (gs / 2688), the multiplier the dequantization
-      applies, and its reciprocal r = 1 / d;
-    * code = :func:`e2m1_encode` (|x| * r) with the sign bit of x, +0 where
-      the magnitude code is 0, and every code 0 where d == 0.
+    * d = float32(e4m3(byte) * (gs / 2688)), the multiplier the
+      dequantization applies to the block;
+    * code = the E2M1 value nearest to the exact |x| / d
+      (:func:`e2m1_encode_quotient`), with the sign bit of x; +0 where the
+      magnitude code is 0, and every code 0 where d == 0.
     """
     xf = np.asarray(x, dtype=np.float32)
     k = xf.shape[-1]
@@ -372,10 +397,8 @@ def quantize(x, gs=None):
         s = (s * inv).astype(np.float32)
     sbytes = e4m3_encode(s)
     d = (e4m3_value(sbytes).astype(np.float32) * global_factor(gs)).astype(np.float32)
-    with np.errstate(divide="ignore", invalid="ignore"):
-        r = (np.float32(1.0) / d).astype(np.float32)
-        v = (np.abs(blocks) * r[..., None]).astype(np.float32)
-    mag = np.where(d[..., None] > 0, e2m1_encode(np.where(d[..., None] > 0, v, 0.0)), 0)
+    live = d[..., None] > 0
+    mag = np.where(live, e2m1_encode_quotient(np.abs(blocks), np.where(live, d[..., None], 1.0)), 0)
     codes = np.where((blocks < 0) & (mag != 0), mag | 8, mag).reshape(xf.shape)
     return pack_codes(codes), sbytes
 

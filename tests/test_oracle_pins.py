@@ -401,8 +401,7 @@ def _plane_with_a_six_per_block(g, n, k):
 
 def pin_quantize_round_trip(orc):
     # a plane whose every block holds a +-6 is its own quantization: amax = 6
-    # e4m3, so the scale comes back exactly and every x * (1 / d) lies within
-    # float32 rounding of a grid value, far from any midpoint;
+    # e4m3, so the scale comes back exactly and every x / d is a grid value;
     # gs = 2688 * 2^k keeps both global factors exact
     g = synth.rng(23)
     codes = _plane_with_a_six_per_block(g, 6, 64)
@@ -434,6 +433,59 @@ def pin_quantize_worked_cases(orc):
     assert s3[0, 0] == 0x7E and w3[0, 0] == 0xF7
 
 
+def _nearest_code_exact(a: float, d: float) -> int:
+    """E2M1 magnitude code nearest to a / d in exact rational arithmetic, ties to the even code."""
+    q = Fraction(a) / Fraction(d)
+    best = None
+    for c in range(8):
+        dist = abs(q - frac_e2m1(c))
+        if best is None or dist < best[0] or (dist == best[0] and c % 2 == 0):
+            best = (dist, c)
+    return best[1]
+
+
+def _unpack(w: np.ndarray) -> np.ndarray:
+    w = np.asarray(w, dtype=np.int64)
+    return np.stack([(w >> (4 * i)) & 0xF for i in range(8)], axis=-1).reshape(*w.shape[:-1], -1)
+
+
+def pin_quantize_midpoints(orc):
+    # Blocks whose multiplier d has an inexact reciprocal: gs absent (d is the
+    # E4M3 scale itself) and gs = 268.8 (a global factor near 0.1). A row holds
+    # two blocks, each led by its amax (6 d, so the scale byte is b), then the
+    # values at, just above and just below m * d for every midpoint m of the
+    # E2M1 grid, and the negatives of some. Every code must be the one exact
+    # rational arithmetic gives for |x| / d, a tie going to the even code.
+    grid = [frac_e2m1(c) for c in range(8)]
+    mids = [(grid[i] + grid[i + 1]) / 2 for i in range(7)]
+    for gs in (None, np.float32(268.8)):
+        fac = np.float32(1.0) if gs is None else np.float32(np.float32(gs) / np.float32(2688.0))
+        rows, ds, bs = [], [], []
+        for b in list(range(1, 8)) + list(range(0x08, 0x7F, 3)):
+            d = np.float32(np.float32(float(frac_e4m3(b))) * fac)
+            amax = np.float32(6.0 * float(frac_e4m3(b))) if gs is None else np.float32(6.0 * float(d))
+            vals = []
+            for m in mids:
+                c = np.float32(float(m) * float(d))
+                vals += [c, np.nextafter(c, np.float32(np.inf)), np.nextafter(c, np.float32(0.0))]
+            vals = [v for v in vals if v < amax][:21]
+            vals += [np.float32(0.0)] * (21 - len(vals))
+            row = [amax] + vals[:15] + [amax] + vals[15:] + [-v for v in vals[:9]]
+            rows.append(row)
+            ds.append(d)
+            bs.append(b)
+        x = np.array(rows, dtype=np.float32)
+        w, s = orc.quantize(x, gs)
+        assert s.tolist() == [[b, b] for b in bs]
+        got = _unpack(w)
+        for r, d in enumerate(ds):
+            for k in range(32):
+                a = float(x[r, k])
+                mag = _nearest_code_exact(abs(a), float(d))
+                want = mag | 8 if a < 0 and mag else mag
+                assert got[r, k] == want, (gs, bs[r], k, a, float(d), int(got[r, k]), want)
+
+
 def pin_fold_scales(orc):
     # ws2 = 1 leaves every finite non-negative byte as it is; ws2 = 2^k shifts
     # the normal values' exponent field by k while they stay normal and finite;
@@ -460,7 +512,7 @@ PINS = [pin_e2m1_table, pin_e4m3_all_bytes, pin_packing, pin_block_scale_broadca
         pin_sidecar_identity, pin_transcode_layout, pin_gather_zero_rows, pin_plane_check,
         pin_error_metric, pin_gelu_tanh, pin_silu, pin_glu_halves, pin_nontransposed_brute_force,
         pin_nontransposed_identity, pin_pack_codes, pin_e2m1_encode, pin_e4m3_encode, pin_quantize_round_trip,
-        pin_quantize_worked_cases, pin_fold_scales]
+        pin_quantize_worked_cases, pin_quantize_midpoints, pin_fold_scales]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=lambda p: p.__name__)
@@ -623,3 +675,14 @@ def test_planted_fold_without_ws2(monkeypatch):
     _planted(monkeypatch, "fold_scales", lambda b, ws2: orig(b, np.float32(1.0)))
     with pytest.raises(AssertionError):
         pin_fold_scales(O)
+
+
+def test_planted_quantize_by_reciprocal(monkeypatch):
+    # the code taken from the float32 product |x| * float32(1 / d), which
+    # rounds twice: it picks the other code beside some midpoints
+    def by_reciprocal(a, d):
+        r = (np.float32(1.0) / np.asarray(d, dtype=np.float32)).astype(np.float32)
+        return O.e2m1_encode((np.asarray(a, dtype=np.float32) * r).astype(np.float32))
+    monkeypatch.setattr(O, "e2m1_encode_quotient", by_reciprocal)
+    with pytest.raises(AssertionError):
+        pin_quantize_midpoints(O)
