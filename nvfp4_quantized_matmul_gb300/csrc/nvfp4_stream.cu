@@ -348,9 +348,8 @@ __device__ __forceinline__ void mul2_rn(float& a, float& b, float r) {
 }
 
 // Four (low, high) pairs -> one word of eight E2M1 codes, low column in the
-// low nibble (cvt puts its first source in the high nibble); +0 for a zero
-// magnitude (a negative value that rounds to zero).
-__device__ __forceinline__ uint32_t pack_e2m1x8(const float* lo, const float* hi) {
+// low nibble (cvt puts its first source in the high nibble).
+__device__ __forceinline__ uint32_t cvt_e2m1x8(const float* lo, const float* hi) {
   uint32_t r;
   asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
       "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n\t"
@@ -360,12 +359,121 @@ __device__ __forceinline__ uint32_t pack_e2m1x8(const float* lo, const float* hi
       "mov.b32 %0, {b0, b1, b2, b3};\n\t}"
       : "=r"(r)
       : "f"(lo[0]), "f"(hi[0]), "f"(lo[1]), "f"(hi[1]), "f"(lo[2]), "f"(hi[2]), "f"(lo[3]), "f"(hi[3]));
+  return r;
+}
+// +0 for every zero magnitude (a negative value that rounds to zero).
+__device__ __forceinline__ uint32_t plus_zero(uint32_t r) {
   const uint32_t nz = (r | (r >> 1) | (r >> 2)) & 0x11111111u;
   return (r & 0x77777777u) | (r & (nz << 3));
 }
 
+// Magnitude code of the E2M1 value nearest to the exact quotient a / d, for
+// a >= 0 and d in [1, 2) (both scaled by the same power of two, which leaves
+// the quotient as it is): a is compared with each midpoint m of the grid
+// times d. fmaf forms a - m * d with one rounding, and with d in [1, 2) and
+// a near m * d no result is small enough to underflow, so its sign is the
+// exact comparison; a tie (+0) goes to the even code (up at 0.75, 1.75 and
+// 3.5, down at the others). A quotient past 5 saturates at code 7 (6.0); a
+// NaN compares false everywhere and gives 0.
+__device__ __forceinline__ uint32_t e2m1_code_exact(float a, float d) {
+  uint32_t c = 0;
+  c += fmaf(-0.25f, d, a) > 0.0f;
+  c += fmaf(-0.75f, d, a) >= 0.0f;
+  c += fmaf(-1.25f, d, a) > 0.0f;
+  c += fmaf(-1.75f, d, a) >= 0.0f;
+  c += fmaf(-2.5f, d, a) > 0.0f;
+  c += fmaf(-3.5f, d, a) >= 0.0f;
+  c += fmaf(-5.0f, d, a) > 0.0f;
+  return c;
+}
+
+// Element e (0..15, a run-time index) of a block's raw 16-byte words, as
+// float.
+__device__ __forceinline__ uint32_t u4sel(const uint4& v, int i) {
+  const uint32_t a = (i & 1) ? v.y : v.x, b = (i & 1) ? v.w : v.z;
+  return (i & 2) ? b : a;
+}
+template <typename T> __device__ __forceinline__ float raw_elem(const Raw16<T>& r, int e);
+template <> __device__ __forceinline__ float raw_elem<float>(const Raw16<float>& r, int e) {
+  const uint4 q = (e & 8) ? ((e & 4) ? r.q[3] : r.q[2]) : ((e & 4) ? r.q[1] : r.q[0]);
+  return __uint_as_float(u4sel(q, e & 3));
+}
+template <> __device__ __forceinline__ float raw_elem<__nv_bfloat16>(const Raw16<__nv_bfloat16>& r, int e) {
+  const uint32_t u = u4sel((e & 8) ? r.q[1] : r.q[0], (e & 7) >> 1);
+  return __uint_as_float((e & 1) ? (u & 0xFFFF0000u) : (u << 16));
+}
+template <> __device__ __forceinline__ float raw_elem<__half>(const Raw16<__half>& r, int e) {
+  const uint32_t u = u4sel((e & 8) ? r.q[1] : r.q[0], (e & 7) >> 1);
+  return __half2float(__ushort_as_half((unsigned short)((e & 1) ? (u >> 16) : (u & 0xFFFFu))));
+}
+
+// Power-of-two scaling of a block's comparisons: |x| and d are multiplied by
+// 2^-E, d = dn 2^E with dn in [1, 2), which leaves every quotient as it is.
+// It is exact, except that an |x| far below d may lose bits (it stays below
+// every midpoint) and one far above may become infinite (it stays above). A
+// d below 2^-126 (a float32 subnormal) is first scaled by 2^126, and |x| with
+// it, one power of two after the other.
+struct Scaled {
+  float pre, p, dn;
+  __device__ __forceinline__ explicit Scaled(float d) {
+    pre = d < 0x1p-126f ? 0x1p126f : 1.0f;
+    const uint32_t db = __float_as_uint(d * pre);
+    dn = __uint_as_float((db & 0x007FFFFFu) | 0x3F800000u);
+    p = __uint_as_float((254u - (db >> 23)) << 23);  // 2^-E of d * pre, in [2^-125, 2^126]
+  }
+  __device__ __forceinline__ float operator()(float x) const { return (fabsf(x) * pre) * p; }
+};
+
+// The midpoint of E2M1 codes c and c + 1 (0.25, 0.75, 1.25, 1.75, 2.5, 3.5,
+// 5 for c = 0..6): the float32 bits 0x3E800000 + (v << 21) with v = 0, 6, 9,
+// 11, 13, 15, 17, five bits each in one 64-bit constant.
+__device__ __forceinline__ float e2m1_midpoint(uint32_t c) {
+  constexpr uint64_t kV = 0ull | (6ull << 5) | (9ull << 10) | (11ull << 15) | (13ull << 20) | (15ull << 25) |
+                          (17ull << 30);
+  return __uint_as_float(0x3E800000u + ((((uint32_t)(kV >> (5 * c))) & 31u) << 21));
+}
+
+// The values whose two conversions disagree (set nibbles of dm, elements e0
+// .. e0 + 7 of the block, codes of the upper products in hw). The products
+// lie within a factor 1 + 2^-20 of each other and the midpoints at least a
+// factor 1.4 apart, so exactly one midpoint m separates the two codes (c from
+// the lower product, c + 1 from the upper one): the sign of |x| - m d picks
+// one of them, and a tie the even one. fmaf forms |x| - m d with one
+// rounding; for d >= 2^-100 (callers send smaller d to exact_block) no
+// nonzero result of it underflows to zero, so its sign is the exact
+// comparison. The result still needs plus_zero.
+template <typename T>
+__device__ __forceinline__ uint32_t fix_codes(uint32_t hw, uint32_t dm, const Raw16<T>& r, int e0, float d) {
+  const uint32_t lw = hw ^ dm;
+  while (dm) {
+    const int sh = (__ffs(dm) - 1) & ~3;
+    dm &= ~(0xFu << sh);
+    const uint32_t c = (lw >> sh) & 7u;
+    const float t = fmaf(-e2m1_midpoint(c), d, fabsf(raw_elem<T>(r, e0 + (sh >> 2))));
+    const bool up = t > 0.0f || (t == 0.0f && (c & 1u));
+    hw = (hw & ~(0xFu << sh)) | ((((up ? hw : lw) >> sh) & 0xFu) << sh);
+  }
+  return hw;
+}
+
+// Every code of a block by the full comparisons (a d whose reciprocal
+// overflows float32). A zero magnitude gets +0.
+template <typename T>
+__device__ __forceinline__ uint2 exact_block(const Raw16<T>& r, float d) {
+  const Scaled sc(d);
+  uint32_t wd[2] = {0u, 0u};
+  for (int e = 0; e < 16; ++e) {
+    const float x = raw_elem<T>(r, e);
+    const uint32_t c = e2m1_code_exact(sc(x), sc.dn);
+    const uint32_t nib = c | (c != 0u && x < 0.0f ? 8u : 0u);
+    wd[e >> 3] |= nib << (4 * (e & 7));
+  }
+  return make_uint2(wd[0], wd[1]);
+}
+
 // One 16-column block (two output words and a scale byte) per thread and
-// step, two blocks in flight (64 or 128 bytes of loads a thread).
+// step, four blocks in flight (128 or 256 bytes of loads a thread). The code
+// of each value is the E2M1 value nearest to the exact |x| / d.
 template <typename T>
 __global__ void __launch_bounds__(kStreamThreads)
 quantize_kernel(const T* __restrict__ x, const float* __restrict__ gs, int64_t E, int64_t blocks_per_expert,
@@ -377,7 +485,7 @@ quantize_kernel(const T* __restrict__ x, const float* __restrict__ gs, int64_t E
     const float fac = global_factor(gs, e);
     const float inv = has_gs ? __fdiv_rn(kGlobalScaleDivisor, __ldg(gs + e)) : 1.0f;
     const int64_t base = e * blocks_per_expert;
-    constexpr int kU = 2;
+    constexpr int kU = 4;
     for (int64_t b0 = first; b0 < blocks_per_expert; b0 += kU * stride) {
       Raw16<T> raw[kU];
 #pragma unroll
@@ -397,11 +505,31 @@ quantize_kernel(const T* __restrict__ x, const float* __restrict__ gs, int64_t E
         const float d = __fmul_rn(e4m3_to_f32(sbyte), fac);
         uint2 out = make_uint2(0u, 0u);
         if (d > 0.0f) {
+          // Each value is converted twice, from x * r (1 - 2^-21) and
+          // x * r (1 + 2^-21): the product x * r is within two roundings
+          // (2^-23 relative) of the quotient x / d, so the quotient lies
+          // between the two products, and where both convert to the same
+          // code (the nearest-value code is monotone) that code is the one
+          // of the quotient. Codes that differ (a midpoint lies between the
+          // products) take the exact comparisons.
           const float r = __frcp_rn(d);
+          const float rl = __fmul_rn(r, 1.0f - 0x1p-21f), rh = __fmul_rn(r, 1.0f + 0x1p-21f);
+          float ll[8], lh[8];
 #pragma unroll
-          for (int i = 0; i < 8; ++i) mul2_rn(lo[i], hi[i], r);
-          out.x = pack_e2m1x8(lo, hi);
-          out.y = pack_e2m1x8(lo + 4, hi + 4);
+          for (int i = 0; i < 8; ++i) {
+            ll[i] = lo[i];
+            lh[i] = hi[i];
+            mul2_rn(lo[i], hi[i], rh);
+            mul2_rn(ll[i], lh[i], rl);
+          }
+          uint32_t hx = cvt_e2m1x8(lo, hi), hy = cvt_e2m1x8(lo + 4, hi + 4);
+          const uint32_t dx = hx ^ cvt_e2m1x8(ll, lh), dy = hy ^ cvt_e2m1x8(ll + 4, lh + 4);
+          if (dx) hx = fix_codes<T>(hx, dx, raw[k], 0, d);
+          if (dy) hy = fix_codes<T>(hy, dy, raw[k], 8, d);
+          out = make_uint2(plus_zero(hx), plus_zero(hy));
+          // d below 2^-100: the comparisons need scaling (and below 2^-127
+          // the reciprocal overflows)
+          if (d < 0x1p-100f) out = exact_block<T>(raw[k], d);
         }
         __stcs(reinterpret_cast<uint2*>(w) + base + b, out);
         scales[base + b] = (uint8_t)sbyte;

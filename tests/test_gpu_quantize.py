@@ -1,13 +1,14 @@
 """GPU parity of the dense -> NVFP4 quantizer (``nvfp4_quantize``) against the
 oracle's ``quantize``: packed words and scale bytes must match bit for bit.
 
-Both sides take every rounding decision in IEEE float32 with the same order
-of operations (amax / 6, times 2688 / gs; the E4M3 byte nearest to that,
-ties to even, saturating; x times the reciprocal of e4m3 * gs / 2688 to the
-nearest E2M1 code, ties to even, saturating; +0 for a zero magnitude). The cases cover the
-three input dtypes, with and without a global scale (per expert), zero
-blocks, values that tie exactly on both grids, saturation of both, the
-round trip through dequantize, and planes with experts.
+The block scale is decided in IEEE float32 (amax / 6, times 2688 / gs; the
+E4M3 byte nearest to that, ties to even, saturating) and each code is the
+E2M1 value nearest to the exact |x| / d, d = e4m3 * gs / 2688 (ties to even,
+saturating; +0 for a zero magnitude). The cases cover the three input dtypes,
+with and without a global scale (per expert), zero blocks, values that tie
+exactly on both grids, values one float32 step beside every midpoint for
+multipliers whose reciprocal is inexact, saturation of both, the round trip
+through dequantize, and planes with experts.
 """
 import numpy as np
 import pytest
@@ -102,6 +103,51 @@ def test_quantize_exact_ties(nv):
     for dt in ("f32", "bf16"):
         check(nv, torch.from_numpy(x).to(TORCH[dt]), None)
     check(nv, torch.from_numpy(xs), None)
+
+
+def test_quantize_beside_midpoints(nv):
+    """Blocks led by amax = 6 d whose other values sit at, one float32 step
+    above and one below m * d for every midpoint m, for d = every fourth E4M3
+    value (gs absent) and the same values times a global factor near 0.1:
+    the quotients |x| / d land on or within two roundings of a midpoint,
+    where the code taken from |x| * (1 / d) can differ from the nearest one."""
+    mids = [0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0]
+    for gs in (None, np.array([268.8], dtype=np.float32)):
+        fac = np.float32(1.0) if gs is None else np.float32(np.float32(268.8) / np.float32(2688.0))
+        rows = []
+        for b in range(1, 0x7F, 4):
+            d = np.float32(np.float32(O.e4m3_value(b)) * fac)
+            amax = np.float32(6.0 * float(O.e4m3_value(b))) if gs is None else np.float32(6.0 * float(d))
+            vals = []
+            for m in mids:
+                c = np.float32(m * float(d))
+                vals += [c, np.nextafter(c, np.float32(np.inf)), np.nextafter(c, np.float32(0.0))]
+            vals = [v for v in vals if v < amax][:21]
+            vals += [np.float32(0.0)] * (21 - len(vals))
+            rows.append([amax] + vals[:15] + [amax] + vals[15:] + [-v for v in vals[:9]])
+        check(nv, torch.from_numpy(np.array(rows, dtype=np.float32)), gs)
+
+
+def test_quantize_subnormal_multiplier(nv):
+    """gs = 2688 * 2^-120 and blocks whose scale is the E4M3 subnormal 3 *
+    2^-9: d = 3 * 2^-129 is a float32 subnormal, whose reciprocal overflows.
+    Values at and one float32 step beside m * d for every midpoint m still
+    take the nearest code."""
+    gs = np.array([np.float32(2688.0 * 2.0**-120)], dtype=np.float32)
+    d = np.float32(3 * 2.0**-129)
+    amax = np.float32(6.0 * float(d))
+    vals = []
+    for m in [0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0]:
+        c = np.float32(m * float(d))
+        vals += [c, np.nextafter(c, np.float32(np.inf)), np.nextafter(c, np.float32(0.0))]
+    x = np.zeros((1, 48), dtype=np.float32)
+    x[0, 0], x[0, 16], x[0, 32] = amax, amax, -amax
+    x[0, 1:16] = vals[:15]
+    x[0, 17:23] = vals[15:21]
+    x[0, 33:48] = [-v for v in vals[:15]]
+    w_ref, s_ref = O.quantize(x, gs[0])
+    assert s_ref.tolist() == [[0x03, 0x03, 0x03]]
+    check(nv, torch.from_numpy(x), gs)
 
 
 def test_quantize_saturation(nv):
