@@ -231,17 +231,66 @@ nvfp4_status nvfp4_qmm_glu(const void* x, nvfp4_dtype x_dtype, int64_t M, int64_
  * scratch is a fixed array inside the library (4 MB plus 1 KB, held on every
  * GPU that loads the library until the process exits). Limits: f16 or bf16
  * activations, 1 <= M <= 16, K a multiple of 256 (at most 2^20), N at most
- * 65536; other shapes are refused (NVFP4_ERR_DTYPE / _SHAPE / _LIMIT) before
- * anything is queued. Nothing is allocated: the first call on a device looks
- * up the array's device address (make that call before any stream capture),
- * and every call clears the part of the array it uses on `stream` before its
- * kernel. All calls share the one array, so calls whose work overlaps on the
- * GPU (on different streams) race and give wrong results: order them. The
- * pages have no counterpart of this entry point.
+ * 65536; other shapes, and shapes for which the decode kernel has no launch
+ * plan, are refused (NVFP4_ERR_DTYPE / _SHAPE / _LIMIT) before anything is
+ * queued. Nothing is allocated: the first call on a device looks up the
+ * array's device address (make that call before any stream capture), and
+ * every call clears the part of the array it uses on `stream` before its
+ * kernel (the tile counters and, per 256-row tile, the M token slots of
+ * sums: two memset nodes). All calls share the one array, so calls whose
+ * work overlaps on the GPU (on different streams) race and give wrong
+ * results: order them. nvfp4_shutdown() forgets the looked-up addresses;
+ * call it before resetting a device's context, since an address from the
+ * old context would be stale. The pages have no counterpart of this entry
+ * point.
  */
 nvfp4_status nvfp4_qmm_noalloc(const void* x, nvfp4_dtype x_dtype, int64_t M, int64_t K, const uint32_t* w,
                                int64_t w_len, const uint8_t* scales, int64_t scales_len, const float* gs,
                                int64_t gs_len, int64_t N, void* y, void* stream);
+
+/* One QuantizedMatmul of a sequence (nvfp4_qmm_sequence): the arguments of
+ * nvfp4_qmm for one call, y [M, N] = x [M, K] @ dequantize(w).T * gs / 2688. */
+typedef struct {
+  const void* x;          /* [M, K], the sequence's activation dtype */
+  int64_t M, K, N;
+  const uint32_t* w;      /* [N, K/8] packed E2M1 words */
+  int64_t w_len;          /* words in w */
+  const uint8_t* scales;  /* [N, K/16] E4M3 block scales */
+  int64_t scales_len;     /* bytes in scales */
+  const float* gs;        /* NULL (gs_len 0) or one float (gs_len 1) */
+  int64_t gs_len;
+  void* y;                /* [M, N], the activation dtype */
+  /* Nonzero: this call reads x only once every earlier call of the sequence
+   * has finished (set it when x is, or depends on, an earlier call's y). */
+  int32_t after_previous;
+  int32_t reserved;       /* set to 0 */
+} nvfp4_qmm_call;
+
+/*
+ * A sequence of decode-shape QuantizedMatmuls (PR #2629, Summary: qmv for
+ * small M, the global scale applied once per output) run in order by one
+ * persistent launch on `stream`; the result is that of calling nvfp4_qmm on
+ * each in turn. The calls of a decode step (the projections of a layer, at
+ * one or several token counts) then share one weight-streaming pipeline:
+ * the next call's weights stream while the current call's last tiles finish,
+ * so the start and end of a launch are paid once per sequence instead of
+ * once per call. Every call: f16 or bf16 activations (x_dtype, all calls),
+ * 1 <= M <= 16 (M = 0 or N = 0 calls are skipped), K a positive multiple of
+ * 256 (at most 2^20), N < 2^31; at most 32 calls. Other shapes are refused
+ * (NVFP4_ERR_DTYPE / _SHAPE / _LIMIT / _PLANE / _GSCALE / _NULL / _ALIGN, the
+ * message naming the call) before anything is queued.
+ * Calls without after_previous must not read what earlier calls of the
+ * sequence write (their activations are read while those calls may still
+ * run). A call with after_previous waits, on the device, until every CTA has
+ * finished every earlier call; the launch is then cooperative (all CTAs
+ * resident at once) and each such wait gives up after 2 s with the error
+ * code that nvfp4_take_device_error() reports. The weight planes of all
+ * calls are read while earlier calls run: no call may write them. Scratch is
+ * the stream's decode workspace (see nvfp4_qmm), grown on the first call
+ * that needs more. Not an interface of the pages: it is this library's way
+ * to run the several small-M matmuls of a decode step.
+ */
+nvfp4_status nvfp4_qmm_sequence(const nvfp4_qmm_call* calls, int32_t ncalls, nvfp4_dtype x_dtype, void* stream);
 
 /* Smallest M routed to the tensor-core path for this shape and dtype. The
  * environment variable NVFP4_QMM_CROSSOVER overrides it. */

@@ -24,6 +24,14 @@ _P = ctypes.c_void_p
 _I64 = ctypes.c_int64
 _INT = ctypes.c_int
 
+class QmmCall(ctypes.Structure):
+    """nvfp4_qmm_call (include/nvfp4.h)."""
+
+    _fields_ = [("x", _P), ("M", _I64), ("K", _I64), ("N", _I64), ("w", _P), ("w_len", _I64), ("scales", _P),
+                ("scales_len", _I64), ("gs", _P), ("gs_len", _I64), ("y", _P), ("after_previous", ctypes.c_int32),
+                ("reserved", ctypes.c_int32)]
+
+
 # name -> (restype, argtypes); mirrors include/nvfp4.h
 SIGNATURES = {
     "nvfp4_transcode": (_INT, [_P, _I64, _P, _I64, _P, _I64, _I64, _P, _P, _P, _P]),
@@ -32,6 +40,7 @@ SIGNATURES = {
     "nvfp4_qmm_routed": (_INT, [_P, _INT, _I64, _I64, _P, _I64, _P, _I64, _P, _I64, _I64, _P, _INT, _P]),
     "nvfp4_qmm_crossover": (_I64, [_INT, _I64, _I64]),
     "nvfp4_qmm_noalloc": (_INT, [_P, _INT, _I64, _I64, _P, _I64, _P, _I64, _P, _I64, _I64, _P, _P]),
+    "nvfp4_qmm_sequence": (_INT, [_P, ctypes.c_int32, _INT, _P]),
     "nvfp4_qmm_glu": (_INT, [_P, _INT, _I64, _I64, _P, _I64, _P, _I64, _P, _I64, _I64, _INT, _P, _INT, _P]),
     "nvfp4_qmm_batched": (_INT, [_P, _INT, _I64, _I64, _I64, _P, _I64, _P, _I64, _P, _I64, _I64, _P, _P]),
     "nvfp4_qmm_nontransposed": (_INT, [_P, _INT, _I64, _I64, _P, _I64, _P, _I64, _P, _I64, _I64, _P, _P]),
@@ -262,6 +271,39 @@ def qmm_noalloc(x, w, scales, gs=None, out=None):
     check(_lib.nvfp4_qmm_noalloc(_ptr(x), DTYPE_CODE[x.dtype], m, k, _ptr(w), w.numel(), _ptr(scales),
                                  scales.numel(), _ptr(gs), _n(gs), n, _ptr(out), _stream(x)))
     return out
+
+
+def qmm_sequence(calls, stream_of=None):
+    """Several decode-shape QuantizedMatmuls in one launch, in order.
+
+    ``calls`` holds tuples ``(x, w, scales, gs, out, after_previous)``: x [M, K]
+    (f16 or bf16, the same dtype for all), w [N, K/8], scales [N, K/16], gs
+    None or a float32 tensor of one element, out [M, N] of x's dtype (or None
+    to allocate it), and after_previous: read x only after every earlier call
+    has finished (x is an earlier call's output). Returns the outputs."""
+    n = len(calls)
+    arr = (QmmCall * max(n, 1))()
+    outs, keep = [], []
+    dtype = None
+    for i, (x, w, scales, gs, out, after) in enumerate(calls):
+        _cuda(x, w, scales)
+        m, k = x.shape
+        nrow = w.shape[0]
+        gs = _gs_tensor(gs, x.device)
+        if out is None:
+            out = torch.empty((m, nrow), dtype=x.dtype, device=x.device)
+        _cuda(out)
+        dtype = x.dtype if dtype is None else dtype
+        if x.dtype != dtype or out.dtype != dtype:
+            raise ValueError("all calls of a sequence take activations and outputs of one dtype")
+        arr[i] = QmmCall(_ptr(x), m, k, nrow, _ptr(w), w.numel(), _ptr(scales), scales.numel(), _ptr(gs), _n(gs),
+                         _ptr(out), 1 if after else 0, 0)
+        outs.append(out)
+        keep.append(gs)
+    if n == 0:
+        return outs
+    check(_lib.nvfp4_qmm_sequence(ctypes.addressof(arr), n, DTYPE_CODE[dtype], _stream(calls[0][0])))
+    return outs
 
 
 def gather_qmm(x, w, scales, rhs, lhs=None, gs=None, sorted_indices=False, out=None):

@@ -154,6 +154,7 @@ void nvfp4_shutdown(void) {
   nvfp4::release_stream_workspaces();
   nvfp4::release_gather_workspaces();
   nvfp4::release_nt_workspaces();
+  nvfp4::release_noalloc_addresses();
 }
 
 nvfp4_status nvfp4_transcode(const uint8_t* mo_weight, int64_t mo_weight_len, const uint8_t* mo_weight_scale,
@@ -444,7 +445,53 @@ nvfp4_status nvfp4_qmm_noalloc(const void* x, nvfp4_dtype x_dtype, int64_t M, in
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (K == 0) return cuda_status(fn, cudaMemsetAsync(y, 0, (size_t)(M * N * dtype_size(x_dtype)), st));
   nvfp4::QmvArgs a{x, w, scales, gs, nullptr, nullptr, M, M, K, N, 1, y};
-  return cuda_status(fn, nvfp4::launch_qmv_stream_noalloc(a, (int)x_dtype, st));
+  const cudaError_t e = nvfp4::launch_qmv_stream_noalloc(a, (int)x_dtype, st);
+  if (e == cudaErrorInvalidConfiguration)
+    return fail(NVFP4_ERR_LIMIT, "%s: no launch plan of the decode kernel fits this shape (N=%" PRId64 ", K=%" PRId64
+                ", M=%" PRId64 ")", fn, N, K, M);
+  return cuda_status(fn, e);
+}
+
+nvfp4_status nvfp4_qmm_sequence(const nvfp4_qmm_call* calls, int32_t ncalls, nvfp4_dtype x_dtype, void* stream) {
+  const char* fn = "nvfp4_qmm_sequence";
+  if (x_dtype != NVFP4_F16 && x_dtype != NVFP4_BF16)
+    return fail(NVFP4_ERR_DTYPE, "%s: takes f16 or bf16 activations (dtype %d)", fn, (int)x_dtype);
+  if (ncalls < 0 || ncalls > nvfp4::kSeqMaxCallsApi)
+    return fail(NVFP4_ERR_LIMIT, "%s: ncalls=%d outside 0..%d", fn, (int)ncalls, nvfp4::kSeqMaxCallsApi);
+  if (ncalls > 0 && !calls) return fail(NVFP4_ERR_NULL, "%s: calls is NULL", fn);
+  nvfp4::QmvArgs args[nvfp4::kSeqMaxCallsApi];
+  int deps[nvfp4::kSeqMaxCallsApi];
+  int n = 0;
+  char name[64];
+  for (int32_t c = 0; c < ncalls; ++c) {
+    const nvfp4_qmm_call& q = calls[c];
+    snprintf(name, sizeof(name), "%s: call %d", fn, (int)c);
+    if (q.M < 0) return fail(NVFP4_ERR_SHAPE, "%s: negative M", name);
+    nvfp4_status s = check_planes(name, q.w, q.w_len, q.scales, q.scales_len, 1, q.N, q.K);
+    if (s) return s;
+    if ((s = check_gs(name, q.gs, q.gs_len, 1))) return s;
+    int64_t xe;
+    if (!mul_ok(q.M, q.K, &xe) || !mul_ok(q.M, q.N, &xe)) return fail(NVFP4_ERR_SHAPE, "%s: M*K or M*N overflows", name);
+    if (q.M == 0 || q.N == 0) continue;  // empty output: nothing to run
+    if (!q.y || !q.x) return fail(NVFP4_ERR_NULL, "%s: x or y is NULL", name);
+    if (!aligned(q.x, 16) || !aligned(q.y, 16))
+      return fail(NVFP4_ERR_ALIGN, "%s: x and y must be 16-byte aligned", name);
+    if (q.M > 16) return fail(NVFP4_ERR_LIMIT, "%s: M=%" PRId64 " exceeds 16 token rows", name, q.M);
+    if (q.K == 0 || q.K % 256)
+      return fail(NVFP4_ERR_SHAPE, "%s: K=%" PRId64 " is not a positive multiple of 256", name, q.K);
+    if (q.K > (int64_t)1 << 20) return fail(NVFP4_ERR_LIMIT, "%s: K=%" PRId64 " exceeds 2^20", name, q.K);
+    if (q.N >= ((int64_t)1 << 31)) return fail(NVFP4_ERR_LIMIT, "%s: N=%" PRId64 " exceeds 2^31-1", name, q.N);
+    args[n] = nvfp4::QmvArgs{q.x, q.w, q.scales, q.gs, nullptr, nullptr, q.M, q.M, q.K, q.N, 1, q.y};
+    // a call whose predecessors were all empty has nothing to wait for
+    deps[n] = n > 0 && q.after_previous != 0 ? 1 : 0;
+    ++n;
+  }
+  if (n == 0) return ok();
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const cudaError_t e = nvfp4::launch_qmv_seq(args, deps, n, (int)x_dtype, st);
+  if (e == cudaErrorInvalidConfiguration)
+    return fail(NVFP4_ERR_LIMIT, "%s: no launch plan of the decode kernel fits these %d calls", fn, n);
+  return cuda_status(fn, e);
 }
 
 nvfp4_status nvfp4_gather_qmm(const void* x, nvfp4_dtype x_dtype, int64_t B, int64_t K, const uint32_t* lhs_indices,

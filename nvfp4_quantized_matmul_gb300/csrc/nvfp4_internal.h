@@ -72,7 +72,20 @@ cudaError_t launch_qmv_group(const QmvArgs& a, int xdt, cudaStream_t st);
 // The same route with its scratch in a fixed array inside the library (no
 // allocation); at most kNoAllocMaxRows weight rows.
 constexpr int64_t kNoAllocMaxRows = 65536;
+// cudaErrorInvalidConfiguration (nothing queued) when the decode kernel has
+// no launch plan for the shape.
 cudaError_t launch_qmv_stream_noalloc(const QmvArgs& a, int xdt, cudaStream_t st);
+// Forgets the fixed array's device addresses (looked up again on next use).
+void release_noalloc_addresses();
+
+// A sequence of decode calls (16-bit x of dtype xdt, 1 <= M <= 16 rows each,
+// K % 256 == 0) run by one persistent launch of the decode kernel, in order;
+// call c with depends[c] != 0 (c > 0) reads its activations only after every
+// earlier call has finished (cooperative launch). At most kSeqMaxCallsApi
+// calls; the split-tile workspace is the stream's decode workspace.
+constexpr int kSeqMaxCallsApi = 32;
+bool qmv_seq_call_supported(const QmvArgs& a, int xdt);
+cudaError_t launch_qmv_seq(const QmvArgs* calls, const int* depends, int n, int xdt, cudaStream_t st);
 
 // Whether weight-streaming launches may overlap the previous kernel on the
 // stream (programmatic dependent launch; see nvfp4_set_launch_overlap).

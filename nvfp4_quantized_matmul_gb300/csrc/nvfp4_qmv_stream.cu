@@ -33,7 +33,10 @@
 
 #include <cstdio>
 #include <cstdlib>
+#include <algorithm>
+#include <cstring>
 #include <map>
+#include <memory>
 #include <mutex>
 #include <tuple>
 #include <utility>
@@ -165,8 +168,9 @@ __device__ __forceinline__ XRun x_run(const SPlan& p, const Work& wk) {
 // residuals) or 2 (bf16). Threads 0 .. kN-1 (the consumer warps) take part;
 // *n_corr must be zero and visible on entry. Loads are issued four at a time
 // per thread so that their latencies overlap. Token slot s reads activation
-// row s, or xrow[s] for an expert group (kGrp).
-template <int kN, bool kGrp>
+// row s, or xrow[s] for an expert group (kGrp). kCoherent loads through L2
+// only (activations written earlier in the same launch).
+template <int kN, bool kGrp, bool kCoherent = false>
 __device__ int stage_run(const QmvArgs& a, const SPlan& p, int chunk0, XRun run, uint32_t xs_base, Corr* corr,
                          int* n_corr, const int64_t* xrow) {
   constexpr int kBatch = 4;
@@ -193,7 +197,8 @@ __device__ int stage_run(const QmvArgs& a, const SPlan& p, int chunk0, XRun run,
         uint32_t dst;
         int gcol;
         locate(u, src, dst, gcol);
-        v[b] = __ldg(reinterpret_cast<const uint4*>(xg + src));
+        v[b] = kCoherent ? __ldcg(reinterpret_cast<const uint4*>(xg + src))
+                         : __ldg(reinterpret_cast<const uint4*>(xg + src));
       }
     }
 #pragma unroll
@@ -265,7 +270,8 @@ __device__ int stage_run(const QmvArgs& a, const SPlan& p, int chunk0, XRun run,
           uint32_t dst;
           int gcol;
           locate(u, src, dst, gcol);
-          v[b] = __ldg(reinterpret_cast<const uint4*>(xg + src));
+          v[b] = kCoherent ? __ldcg(reinterpret_cast<const uint4*>(xg + src))
+                           : __ldg(reinterpret_cast<const uint4*>(xg + src));
         }
       }
 #pragma unroll
@@ -322,15 +328,23 @@ struct ChunkPos {
   __device__ __forceinline__ bool block_start(int ac) const { return c == sg.c0 || ac % kSChunks == 0; }
 };
 
+// Ring positions of the producer (copies issued, next word stage and its
+// phase, scale blocks issued). A launch that runs several calls keeps one
+// across them: the ring never drains between calls.
+struct ProdState {
+  uint32_t u = 0, s = 0, ph = 0, su = 0;
+};
+
 // Producer (lane 0 of the producer warp): the same chunk walk as the
 // consumers; a scale block at the start of each segment and at every fourth
 // chunk, a word stage per chunk. An expert group (kGrp) reads its expert's
 // plane through 3-D maps ([E, N, K] planes, rows past N zero-filled).
+// Returns false once a wait gave up.
 template <bool kGrp, bool kGlu>
-__device__ void produce(const SPlan& p, int grp, Work wk, const CUtensorMap* wmap,
+__device__ bool produce(const SPlan& p, int grp, Work wk, const CUtensorMap* wmap,
                         const CUtensorMap* smap, uint32_t wst, uint32_t sst, const Bars& bar,
-                        volatile int* abort_flag, int expert) {
-  uint32_t u = 0, s = 0, ph = 0, su = 0;  // copies issued, next stage and its phase, scale blocks
+                        volatile int* abort_flag, int expert, ProdState& st, int stages) {
+  uint32_t &u = st.u, &s = st.s, &ph = st.ph, &su = st.su;
   ChunkPos pos;
   pos.start(wk);
   for (; pos.valid; pos.advance()) {
@@ -340,7 +354,7 @@ __device__ void produce(const SPlan& p, int grp, Work wk, const CUtensorMap* wma
     const int up_row = (int)(p.glu_cols + row);
     if (pos.block_start(ac)) {
       const uint32_t b = su & 1u, bph = (su >> 1) & 1u;
-      if (!wait_bar(bar.sempty(b), bph ^ 1u, abort_flag, 21, &g_stream_error)) break;
+      if (!wait_bar(bar.sempty(b), bph ^ 1u, abort_flag, 21, &g_stream_error)) return false;
       ++su;
       mbar_arrive_tx(bar.sfull(b), kSBox);
       if (kGlu) {
@@ -351,7 +365,7 @@ __device__ void produce(const SPlan& p, int grp, Work wk, const CUtensorMap* wma
       else
         tma_load_2d(sst + b * kSBox, smap, (ac / kSChunks) * (kSChunks * 16), row, bar.sfull(b));
     }
-    if (!wait_bar(bar.empty(s), ph ^ 1u, abort_flag, 22, &g_stream_error)) break;
+    if (!wait_bar(bar.empty(s), ph ^ 1u, abort_flag, 22, &g_stream_error)) return false;
     ++u;
     mbar_arrive_tx(bar.full(s), kWBox);
     if (kGlu) {
@@ -361,16 +375,21 @@ __device__ void produce(const SPlan& p, int grp, Work wk, const CUtensorMap* wma
       tma_load_3d(wst + s * kWBox, wmap, ac * kChunkWords, row, expert, bar.full(s));
     else
       tma_load_2d(wst + s * kWBox, wmap, ac * kChunkWords, row, bar.full(s));
-    if (++s == (uint32_t)p.stages) {
+    if (++s == (uint32_t)stages) {
       s = 0;
       ph ^= 1u;
     }
   }
-  // No copy may still be in flight when the CTA exits.
-  const uint32_t first = u > (uint32_t)p.stages ? u - p.stages : 0;
-  for (uint32_t v = first; v < u; ++v) wait_bar_quiet(bar.full(v % p.stages), (v / p.stages) & 1u);
-  const uint32_t sfirst = su > 2u ? su - 2u : 0;
-  for (uint32_t v = sfirst; v < su; ++v) wait_bar_quiet(bar.sfull(v & 1u), (v >> 1) & 1u);
+  return true;
+}
+
+// No copy may still be in flight when the CTA exits: waits (bounded) for the
+// last ring's worth of copies the producer issued.
+__device__ __forceinline__ void drain_copies(const ProdState& st, const Bars& bar, int stages) {
+  const uint32_t first = st.u > (uint32_t)stages ? st.u - stages : 0;
+  for (uint32_t v = first; v < st.u; ++v) wait_bar_quiet(bar.full(v % stages), (v / stages) & 1u);
+  const uint32_t sfirst = st.su > 2u ? st.su - 2u : 0;
+  for (uint32_t v = sfirst; v < st.su; ++v) wait_bar_quiet(bar.sfull(v & 1u), (v >> 1) & 1u);
 }
 
 // Accumulator sets per (row tile, token tile): consecutive k-steps rotate over
@@ -422,12 +441,19 @@ __device__ __forceinline__ void compute_rt(const Chunk (&ch)[RT], const uint32_t
   }
 }
 
+// Ring positions of a consumer warp (word stage and its phase, scale
+// blocks, partial buffers handed over), kept across the calls of a launch.
+struct ConsState {
+  uint32_t s = 0, ph = 0, su = 0, pc = 0;
+};
+
 // Consumer warp: RT row tiles of 16 rows (rows 16 RT w .. 16 RT w + 16 RT - 1
 // of the 256-row tile) over every chunk of the CTA's walk.
 template <typename T, int MT, int RT>
 __device__ void consume(const SPlan& p, int grp, Work wk, XRun run, uint32_t wst, uint32_t sst,
                         uint32_t pbuf, uint32_t pbuf_bytes, const Bars& bar, volatile int* abort_flag,
-                        uint32_t xs_base, uint32_t zero_base, uint32_t lut_bf, const Corr* corr, int ncorr) {
+                        uint32_t xs_base, uint32_t zero_base, uint32_t lut_bf, const Corr* corr, int ncorr,
+                        ConsState& cst, int stages) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
   // 128-byte swizzle of the word stage: 16-byte granule j of row r sits at
   // j ^ (r & 7); this lane reads granules 2t and 2t+1 of rows rg and rg + 8.
@@ -461,7 +487,7 @@ __device__ void consume(const SPlan& p, int grp, Work wk, XRun run, uint32_t wst
 
   constexpr int NA = NAccS<MT, RT>::value;
   float acc[NA][RT][MT][4];
-  uint32_t s = 0, ph = 0, su = 0, pc = 0;  // word stage and its phase, scale blocks, partial buffers
+  uint32_t &s = cst.s, &ph = cst.ph, &su = cst.su, &pc = cst.pc;
   Seg sg;
   while (wk.next(sg)) {
 #pragma unroll
@@ -477,7 +503,7 @@ __device__ void consume(const SPlan& p, int grp, Work wk, XRun run, uint32_t wst
     for (int c = sg.c0; c < sg.c1; ++c) {
       const int ac = grp * p.ncg + c, kb = ac % kSChunks;
       const uint32_t cs = s, cph = ph;  // this chunk's stage
-      if (++s == (uint32_t)p.stages) {
+      if (++s == (uint32_t)stages) {
         s = 0;
         ph ^= 1u;
       }
@@ -621,10 +647,16 @@ __device__ __forceinline__ float glu_act(int act, float v) {
   return __fdividef(v, 1.0f + __expf(-z));
 }
 
+// Positions of the epilogue warp (partial buffers taken, read-backs), kept
+// across the calls of a launch.
+struct FinState {
+  uint32_t pc = 0, bc = 0;
+};
+
 template <bool kGrp, bool kGlu>
 __device__ void finish(const QmvArgs& a, const SPlan& p, Work wk, uint32_t pbuf, uint32_t pbuf_bytes,
                        const Bars& bar, volatile int* abort_flag, float* __restrict__ acc,
-                       uint32_t* __restrict__ cnt, int expert, int wsbase, const int64_t* yrow) {
+                       uint32_t* __restrict__ cnt, int expert, int wsbase, const int64_t* yrow, FinState& fst) {
   const int lane = threadIdx.x & 31;
   const float factor = global_factor(a.gs, kGrp ? expert : 0);
   const int64_t first_split = (p.nrt / p.gs) * p.gs;  // row tiles from here on may be split
@@ -632,7 +664,7 @@ __device__ void finish(const QmvArgs& a, const SPlan& p, Work wk, uint32_t pbuf,
   const int M = p.M;
   constexpr uint32_t kSlotBytes = kTileRows * 4u;
   const uint32_t tile_bytes = (uint32_t)M * kSlotBytes;  // this call's part of a tile block
-  uint32_t pc = 0, bc = 0;
+  uint32_t &pc = fst.pc, &bc = fst.bc;
   Seg sg;
   while (wk.next(sg)) {
     const uint32_t b = pc & 1u, bph = (pc >> 1) & 1u;
@@ -937,24 +969,228 @@ qmv_stream_kernel(const QmvArgs a, const SPlan p, float* __restrict__ acc, uint3
   const Work wk = Work::of(q, gi);
 
   if (warp == Geo<RT>::kProducer) {
-    if ((threadIdx.x & 31) == 0) produce<kGrp, kGlu>(q, grp, wk, &wmap, &smap, wst, sst, bar, abort_flag, expert);
+    if ((threadIdx.x & 31) == 0) {
+      ProdState pst;
+      produce<kGrp, kGlu>(q, grp, wk, &wmap, &smap, wst, sst, bar, abort_flag, expert, pst, q.stages);
+      drain_copies(pst, bar, q.stages);
+    }
     return;
   }
   asm volatile("griddepcontrol.wait;" ::: "memory");
   if (warp == Geo<RT>::kEpilogue) {
-    finish<kGrp, kGlu>(a, q, wk, pbuf, pbuf_bytes, bar, abort_flag, acc, cnt, expert, wsbase, s_yrow);
+    FinState fst;
+    finish<kGrp, kGlu>(a, q, wk, pbuf, pbuf_bytes, bar, abort_flag, acc, cnt, expert, wsbase, s_yrow, fst);
     return;
   }
   // Consumers: stage the activation columns this CTA visits (named barrier
   // 1, 512 threads), then stream.
   const XRun run = x_run(q, wk);
   const int mode = stage_run<Geo<RT>::kCW * 32, kGrp>(a, q, grp * q.ncg, run, xs_base, s_corr, &s_ncorr, s_xrow);
+  ConsState cst;
   if (mode == 2)
     consume<__nv_bfloat16, MT, RT>(q, grp, wk, run, wst, sst, pbuf, pbuf_bytes, bar, abort_flag, xs_base, zero_base,
-                                   lut_bf, s_corr, 0);
+                                   lut_bf, s_corr, 0, cst, q.stages);
   else
     consume<__half, MT, RT>(q, grp, wk, run, wst, sst, pbuf, pbuf_bytes, bar, abort_flag, xs_base, zero_base, lut_bf,
-                            s_corr, mode == 1 ? s_ncorr : 0);
+                            s_corr, mode == 1 ? s_ncorr : 0, cst, q.stages);
+}
+
+// ---- a sequence of decode calls in one launch ----
+//
+// The calls of a decode step (the projections of a layer, at one or several
+// token counts) run back to back in one persistent launch: each CTA walks its
+// share of call 0's plane, then of call 1's, and so on, through one ring of
+// word stages and one set of barriers. The producer streams call i + 1's
+// weights while the consumers finish call i and the epilogue warp finishes
+// call i's split tiles, so what a single call pays at its start (barrier
+// set-up, the first TMA round trip, the ring filling) and at its end (the
+// split-tile reduction, the last stores) is paid once per launch. A call may
+// read outputs of earlier calls of the launch: its consumers then wait
+// (bounded) until every CTA has finished every earlier call, which needs all
+// CTAs resident at once (a cooperative launch); the producer keeps streaming
+// its weights meanwhile.
+constexpr int kSeqMaxCalls = 32;
+
+struct SeqCall {
+  CUtensorMap wmap, smap;  // first: 64-byte aligned
+  QmvArgs a;
+  SPlan p;
+  int64_t ws_block;  // first workspace block (256-row tile) of this call
+  int depends;       // wait for every earlier call before reading x
+};
+struct SeqArgs {
+  SeqCall call[kSeqMaxCalls];
+  int ncalls;
+  int stages;    // word stages in the ring (all calls)
+  int pslots;    // token slots of a partial buffer (8 or 16)
+  int signal;    // some call depends on earlier ones: count finished calls
+  int64_t done;  // counter words: done[c] at cnt[done + c], then the exit count
+};
+
+__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Bounded wait by one thread until *ctr >= target (release by the CTAs that
+// counted in, acquire here); false once the limit passes (abort flag set,
+// error code 28 recorded) or another warp has aborted.
+__device__ bool wait_count(const uint32_t* ctr, uint32_t target, volatile int* abort_flag) {
+  const uint64_t t0 = gtimer();
+  for (;;) {
+    if (ld_acquire_u32(ctr) >= target) return true;
+    if (*abort_flag) return false;
+    if (gtimer() - t0 > kWaitLimitNs) {
+      *abort_flag = 1;
+      atomicCAS(&g_stream_error, 0, 28);
+      return false;
+    }
+    __nanosleep(64);
+  }
+}
+
+// Dynamic shared memory of the sequence kernel: the single-call layout with
+// a common ring depth, partial buffers of pslots token slots and room for the
+// largest staged activation slice of any call.
+size_t seq_smem_bytes(int stages, int pslots, size_t xs) {
+  const size_t pbuf = (size_t)2 * pslots * kPStride * 4;
+  return 1024 + (size_t)stages * kWBox + 2 * kSBox + pbuf + kBarBytes + 16 + 256 + 1024 + 512 + 64 +
+         ((xs + 15) & ~(size_t)15);
+}
+
+__global__ void __launch_bounds__(Geo<1>::kThreads, 1)
+qmv_seq_kernel(const __grid_constant__ SeqArgs sa, float* __restrict__ acc, uint32_t* __restrict__ cnt) {
+  using G = Geo<1>;
+  constexpr int kN = G::kCW * 32;  // consumer threads
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_addr(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* bp = smem_raw + (base - raw);
+  const int stages = sa.stages;
+  const uint32_t wst = base;
+  const uint32_t sst = wst + stages * kWBox;
+  const uint32_t pbuf = sst + 2 * kSBox;
+  const uint32_t pbuf_bytes = (uint32_t)(sa.pslots * kPStride * 4);
+  const Bars bar{pbuf + 2 * pbuf_bytes, stages};
+  uint8_t* after_bars = bp + (bar.base - base) + kBarBytes;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(after_bars);
+  uint32_t* lut = reinterpret_cast<uint32_t*>(after_bars + 16 + 256);
+  const uint32_t lut_bf = smem_addr(lut);
+  const uint32_t zero_base = lut_bf + 1024;
+  const uint32_t xs_base = zero_base + 512 + 64;
+  __shared__ Corr s_corr[kMaxCorr];
+  __shared__ int s_ncorr;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int st = 0; st < stages; ++st) {
+      mbar_init(bar.full(st), 1);
+      mbar_init(bar.empty(st), G::kCW);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar.sfull(b), 1);
+      mbar_init(bar.sempty(b), G::kCW);
+      mbar_init(bar.pfull(b), G::kCW * 32);
+      mbar_init(bar.pempty(b), 1);
+    }
+    mbar_init(bar.back(), 1);
+    *abort_flag = 0;
+    s_ncorr = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == G::kProducer && lane == 0)
+    for (int c = 0; c < sa.ncalls; ++c) {
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&sa.call[c].wmap)) : "memory");
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&sa.call[c].smap)) : "memory");
+    }
+  if (threadIdx.x < 256) lut[threadIdx.x] = e4m3_to_bf16x2_bcast_x2p112(threadIdx.x);
+  if (threadIdx.x < 128) lut[256 + threadIdx.x] = 0u;  // the zero block
+  // With launch overlap the weights stream at once; activations, outputs and
+  // the workspace are touched only after griddepcontrol.wait.
+  if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  __syncthreads();
+
+  const int b = (int)blockIdx.x;
+  if (warp == G::kProducer) {
+    if (lane == 0) {
+      ProdState pst;
+      for (int c = 0; c < sa.ncalls; ++c) {
+        const SeqCall& C = sa.call[c];
+        if (b >= C.p.S * C.p.gs) continue;
+        if (!produce<false, false>(C.p, b / C.p.gs, Work::of(C.p, b % C.p.gs), &C.wmap, &C.smap, wst, sst, bar,
+                                   abort_flag, 0, pst, stages))
+          break;
+      }
+      drain_copies(pst, bar, stages);
+    }
+    return;
+  }
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (warp == G::kEpilogue) {
+    FinState fst;
+    for (int c = 0; c < sa.ncalls; ++c) {
+      const SeqCall& C = sa.call[c];
+      if (b < C.p.S * C.p.gs)
+        finish<false, false>(C.a, C.p, Work::of(C.p, b % C.p.gs), pbuf, pbuf_bytes, bar, abort_flag,
+                             acc + C.ws_block * (int64_t)(kAccSlots * kTileRows), cnt + C.ws_block, 0, 0, nullptr,
+                             fst);
+      if (sa.signal) {  // this CTA has written all it writes of calls 0..c
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) atomicAdd(cnt + sa.done + c, 1u);
+      }
+    }
+    if (sa.signal && lane == 0) {
+      // The last CTA out returns the counters to zero for the next launch
+      // (every CTA has passed all its waits before it counts out).
+      __threadfence();
+      if (atomicAdd(cnt + sa.done + sa.ncalls, 1u) == gridDim.x - 1) {
+        for (int c = 0; c < sa.ncalls; ++c) atomicExch(cnt + sa.done + c, 0u);
+        atomicExch(cnt + sa.done + sa.ncalls, 0u);
+      }
+    }
+    return;
+  }
+  // Consumers: per call, stage its activation columns (after the previous
+  // call's last chunk, and after the calls it depends on have finished
+  // everywhere), then stream.
+  ConsState cst;
+  bool staged = false;
+  for (int c = 0; c < sa.ncalls; ++c) {
+    const SeqCall& C = sa.call[c];
+    if (b >= C.p.S * C.p.gs) continue;
+    const int grp = b / C.p.gs;
+    const Work wk = Work::of(C.p, b % C.p.gs);
+    if (staged) {  // every consumer is done with the previous activations
+      sync_all<kN>();
+      if (threadIdx.x == 0) s_ncorr = 0;
+      sync_all<kN>();
+    }
+    staged = true;
+    if (C.depends) {
+      if (threadIdx.x == 0) wait_count(cnt + sa.done + c - 1, gridDim.x, abort_flag);
+      sync_all<kN>();
+    }
+    const XRun run = x_run(C.p, wk);
+    const int mode = stage_run<kN, false, true>(C.a, C.p, grp * C.p.ncg, run, xs_base, s_corr, &s_ncorr, nullptr);
+    const int ncorr = mode == 1 ? s_ncorr : 0;
+    if (C.p.M > 8) {
+      if (mode == 2)
+        consume<__nv_bfloat16, 2, 1>(C.p, grp, wk, run, wst, sst, pbuf, pbuf_bytes, bar, abort_flag, xs_base,
+                                     zero_base, lut_bf, s_corr, 0, cst, stages);
+      else
+        consume<__half, 2, 1>(C.p, grp, wk, run, wst, sst, pbuf, pbuf_bytes, bar, abort_flag, xs_base, zero_base,
+                              lut_bf, s_corr, ncorr, cst, stages);
+    } else {
+      if (mode == 2)
+        consume<__nv_bfloat16, 1, 1>(C.p, grp, wk, run, wst, sst, pbuf, pbuf_bytes, bar, abort_flag, xs_base,
+                                     zero_base, lut_bf, s_corr, 0, cst, stages);
+      else
+        consume<__half, 1, 1>(C.p, grp, wk, run, wst, sst, pbuf, pbuf_bytes, bar, abort_flag, xs_base, zero_base,
+                              lut_bf, s_corr, ncorr, cst, stages);
+    }
+  }
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -1126,70 +1362,58 @@ cudaError_t plane_maps(const QmvArgs& a, CUtensorMap* wmap, CUtensorMap* smap, b
   return cudaSuccess;
 }
 
+// The launch plan of a decode call, made once per (device, shape, M) and
+// cached; cudaErrorInvalidConfiguration when no plan fits the SM's shared
+// memory. `out` may be null (a check only).
 template <int MT, int RT, bool kGlu = false>
-cudaError_t launch_mt(const QmvArgs& a, int xdt, cudaStream_t st, const Ws* given = nullptr) {
+cudaError_t stream_plan(const QmvArgs& a, int xdt, int dev, SPlan* out) {
   auto kern = qmv_stream_kernel<MT, RT, false, kGlu>;
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
   using Key = std::tuple<int, int64_t, int64_t, int64_t, int, int>;
   static std::mutex mu;
   static std::map<Key, SPlan> cache;
   static std::map<int, int64_t> max_dyn_of_dev;
+  std::lock_guard<std::mutex> lock(mu);
+  const Key key{dev, a.N, a.K, a.R, xdt, a.glu_act};
+  auto it = cache.find(key);
+  if (it != cache.end()) {
+    if (out) *out = it->second;
+    return cudaSuccess;
+  }
+  auto md = max_dyn_of_dev.find(dev);
+  int64_t max_dyn;
+  if (md == max_dyn_of_dev.end()) {
+    int optin = 0;
+    cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    cudaFuncAttributes fa;
+    cudaError_t e = cudaFuncGetAttributes(&fa, kern);
+    if (e != cudaSuccess) return e;
+    max_dyn = optin - (int64_t)fa.sharedSizeBytes;
+    if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)max_dyn)) != cudaSuccess)
+      return e;
+    max_dyn_of_dev[dev] = max_dyn;
+  } else {
+    max_dyn = md->second;
+  }
   SPlan p{};
-  {
-    std::lock_guard<std::mutex> lock(mu);
-    const Key key{dev, a.N, a.K, a.R, xdt, a.glu_act};
-    auto it = cache.find(key);
-    if (it != cache.end()) {
-      p = it->second;
-    } else {
-      auto md = max_dyn_of_dev.find(dev);
-      int64_t max_dyn;
-      if (md == max_dyn_of_dev.end()) {
-        int optin = 0;
-        cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-        cudaFuncAttributes fa;
-        if ((e = cudaFuncGetAttributes(&fa, kern)) != cudaSuccess) return e;
-        max_dyn = optin - (int64_t)fa.sharedSizeBytes;
-        if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)max_dyn)) != cudaSuccess)
-          return e;
-        max_dyn_of_dev[dev] = max_dyn;
-      } else {
-        max_dyn = md->second;
-      }
-      p.M = (int)a.R;
-      p.nc = (int)(a.K / kChunkCols);
-      p.nrt = kGlu ? (a.glu_cols + kTileRows / 2 - 1) / (kTileRows / 2) : (a.N + kTileRows - 1) / kTileRows;
-      p.x_is_bf16 = xdt == kBF16;
-      p.glu_cols = a.glu_cols;
-      p.glu_act = a.glu_act;
-      if (!make_plan(p, sms_of(dev), max_dyn)) return cudaErrorInvalidConfiguration;
-      cache[key] = p;
-      if (std::getenv("NVFP4_QMV_PLAN_LOG"))
-        std::fprintf(stderr, "nvfp4 qmv stream plan N=%lld K=%lld M=%d: stages=%d S=%d CTAs/group=%d tiles/group=%lld\n",
-                     (long long)a.N, (long long)a.K, p.M, p.stages, p.S, p.gs, (long long)(p.nrt * p.ncg));
-    }
-  }
-  // NVFP4_QMV_STREAM_PLAN="stages,groups" overrides the plan (tuning).
-  if (const char* ev = std::getenv("NVFP4_QMV_STREAM_PLAN")) {
-    int stages = 0, S = 0;
-    if (std::sscanf(ev, "%d,%d", &stages, &S) == 2 && stages >= 2 && stages <= kMaxStages && S >= 1 && S <= p.nc &&
-        p.nc % S == 0) {
-      SPlan q = p;
-      q.stages = stages;
-      q.S = S;
-      q.ncg = p.nc / S;
-      const int64_t per = sms_of(dev) / S, tg = q.nrt * q.ncg;
-      q.gs = (int)(per < tg ? per : tg);
-      const int64_t run = q.gs > 0 ? (tg + q.gs - 1) / q.gs : 0;
-      q.xs_chunks = q.gs > 0 && (q.nrt / q.gs >= 1 || run >= q.ncg) ? q.ncg : (int)run;
-      q.xs_stride = q.xs_chunks * kChunkCols + 32;
-      std::lock_guard<std::mutex> lock(mu);
-      if (q.gs < 1 || (int64_t)stream_smem_bytes(q) > max_dyn_of_dev[dev]) return cudaErrorInvalidConfiguration;
-      p = q;
-    }
-  }
+  p.M = (int)a.R;
+  p.nc = (int)(a.K / kChunkCols);
+  p.nrt = kGlu ? (a.glu_cols + kTileRows / 2 - 1) / (kTileRows / 2) : (a.N + kTileRows - 1) / kTileRows;
+  p.x_is_bf16 = xdt == kBF16;
+  p.glu_cols = a.glu_cols;
+  p.glu_act = a.glu_act;
+  if (!make_plan(p, sms_of(dev), max_dyn)) return cudaErrorInvalidConfiguration;
+  cache[key] = p;
+  if (out) *out = p;
+  return cudaSuccess;
+}
+
+template <int MT, int RT, bool kGlu = false>
+cudaError_t launch_mt(const QmvArgs& a, int xdt, cudaStream_t st, const Ws* given = nullptr) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  SPlan p{};
+  if ((e = stream_plan<MT, RT, kGlu>(a, xdt, dev, &p)) != cudaSuccess) return e;
   Ws ws;
   if (given)
     ws = *given;
@@ -1207,7 +1431,7 @@ cudaError_t launch_mt(const QmvArgs& a, int xdt, cudaStream_t st, const Ws* give
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = launch_overlap() ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, kern, a, p, ws.acc, ws.cnt, wmap, smap);
+  return cudaLaunchKernelEx(&cfg, qmv_stream_kernel<MT, RT, false, kGlu>, a, p, ws.acc, ws.cnt, wmap, smap);
 }
 
 // One launch for up to 16 token rows: eight token slots per MMA tile (MT),
@@ -1341,6 +1565,141 @@ cudaError_t launch_qmv_stream_glu(const QmvArgs& a, int xdt, cudaStream_t st) {
   return cudaSuccess;
 }
 
+// ---- host side of the call sequence ----
+namespace {
+
+// A call's plan for a given ring depth: the fewest K groups whose staged
+// activation slice fits in `xs_budget` bytes (as make_plan); false if none.
+bool seq_call_plan(SPlan& p, int sms, int64_t xs_budget) {
+  for (int S = 1; S <= p.nc && S <= sms; ++S) {
+    if (p.nc % S) continue;
+    SPlan q = p;
+    q.S = S;
+    q.ncg = p.nc / S;
+    const int64_t tg = q.nrt * q.ncg;
+    const int64_t per = sms / S;
+    q.gs = (int)(per < tg ? per : tg);
+    if (q.gs < 1) continue;
+    const int64_t run = (tg + q.gs - 1) / q.gs;
+    q.xs_chunks = q.nrt / q.gs >= 1 || run >= q.ncg ? q.ncg : (int)run;
+    q.xs_stride = q.xs_chunks * kChunkCols + 32;
+    if ((int64_t)q.M * q.xs_stride * 2 > xs_budget) continue;
+    p = q;
+    return true;
+  }
+  return false;
+}
+
+int64_t seq_max_dyn(int dev) {
+  static std::mutex mu;
+  static std::map<int, int64_t> of_dev;
+  std::lock_guard<std::mutex> lock(mu);
+  auto it = of_dev.find(dev);
+  if (it != of_dev.end()) return it->second;
+  int optin = 0;
+  cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  cudaFuncAttributes fa;
+  if (cudaFuncGetAttributes(&fa, qmv_seq_kernel) != cudaSuccess) return -1;
+  const int64_t max_dyn = optin - (int64_t)fa.sharedSizeBytes;
+  if (cudaFuncSetAttribute(qmv_seq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)max_dyn) != cudaSuccess)
+    return -1;
+  of_dev[dev] = max_dyn;
+  return max_dyn;
+}
+
+}  // namespace
+
+bool qmv_seq_call_supported(const QmvArgs& a, int xdt) {
+  return xdt != kF32 && a.rhs == nullptr && a.lhs == nullptr && a.E == 1 && a.R >= 1 && a.R <= 16 &&
+         a.K % kChunkCols == 0 && a.K > 0 && a.N > 0 && a.N < (1ll << 31) && a.K / kChunkCols <= 4096;
+}
+
+cudaError_t launch_qmv_seq(const QmvArgs* calls, const int* depends, int n, int xdt, cudaStream_t st) {
+  if (n < 1 || n > kSeqMaxCalls) return cudaErrorInvalidValue;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const int64_t max_dyn = seq_max_dyn(dev);
+  if (max_dyn < 0) return cudaErrorInvalidConfiguration;
+  const int sms = sms_of(dev);
+  static_assert(sizeof(SeqArgs) + 2 * sizeof(void*) <= 32764, "kernel parameters exceed the launch limit");
+  auto sa = std::make_unique<SeqArgs>();
+  std::memset(sa.get(), 0, sizeof(SeqArgs));
+  int pslots = 8;
+  bool any_dep = false;
+  for (int c = 0; c < n; ++c) {
+    if (calls[c].R > 8) pslots = 16;
+    any_dep = any_dep || (c > 0 && depends[c]);
+  }
+  // One ring depth for every call: the depth whose calls need the fewest K
+  // groups in all (fewer row tiles finished through the workspace), ties to
+  // the deeper ring; each call takes the fewest groups its slice allows.
+  int best_stages = 0;
+  int64_t best_groups = 0;
+  std::vector<SPlan> best(n), cur(n);
+  for (int stages = kMaxStages; stages >= 3; --stages) {
+    const int64_t budget = max_dyn - (int64_t)seq_smem_bytes(stages, pslots, 0);
+    if (budget < 0) continue;
+    int64_t groups = 0;
+    bool ok = true;
+    for (int c = 0; c < n && ok; ++c) {
+      SPlan p{};
+      p.M = (int)calls[c].R;
+      p.nc = (int)(calls[c].K / kChunkCols);
+      p.nrt = (calls[c].N + kTileRows - 1) / kTileRows;
+      p.x_is_bf16 = xdt == kBF16;
+      p.stages = stages;
+      p.pslots = pslots;
+      ok = seq_call_plan(p, sms, budget);
+      cur[c] = p;
+      groups += p.S;
+    }
+    if (ok && (best_stages == 0 || groups < best_groups)) {
+      best_stages = stages;
+      best_groups = groups;
+      best = cur;
+    }
+  }
+  if (best_stages == 0) return cudaErrorInvalidConfiguration;
+  int64_t blocks = 0;
+  size_t xs = 0;
+  for (int c = 0; c < n; ++c) {
+    SeqCall& C = sa->call[c];
+    C.a = calls[c];
+    C.p = best[c];
+    C.ws_block = blocks;
+    C.depends = c > 0 && depends[c] ? 1 : 0;
+    blocks += C.p.nrt;
+    xs = std::max(xs, (size_t)C.p.M * C.p.xs_stride * 2);
+    if ((e = plane_maps(C.a, &C.wmap, &C.smap)) != cudaSuccess) return e;
+  }
+  sa->ncalls = n;
+  sa->stages = best_stages;
+  sa->pslots = pslots;
+  sa->signal = any_dep ? 1 : 0;
+  sa->done = blocks;  // the counter words after the tile counters
+  Ws ws;
+  // blocks tile blocks of sums and counters, plus n + 1 counter words
+  if ((e = get_workspace(dev, st, blocks + kSeqMaxCalls + 1, &ws)) != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)sms, 1, 1);
+  cfg.blockDim = dim3(Geo<1>::kThreads, 1, 1);
+  cfg.dynamicSmemBytes = seq_smem_bytes(best_stages, pslots, xs);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  if (any_dep) {
+    // the dependent waits need every CTA resident at once
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+  } else {
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = any_dep || launch_overlap() ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, qmv_seq_kernel, *sa, ws.acc, ws.cnt);
+}
+
 int read_stream_error() {
   int v = 0;
   if (cudaMemcpyFromSymbol(&v, g_stream_error, sizeof(int)) != cudaSuccess) return -1;
@@ -1400,12 +1759,22 @@ cudaError_t noalloc_base(int dev, float** out) {
   *out = d.base;
   return cudaSuccess;
 }
+
+// Whether the decode kernel has a launch plan for this shape (the plan the
+// launch itself will use, cached the same way).
+bool noalloc_plan_ok(const QmvArgs& a, int xdt, int dev) {
+  if (a.R > 8) return stream_plan<2, 2>(a, xdt, dev, nullptr) == cudaSuccess;
+  return stream_plan<1, 1>(a, xdt, dev, nullptr) == cudaSuccess;
+}
 }  // namespace
 
 cudaError_t launch_qmv_stream_noalloc(const QmvArgs& a, int xdt, cudaStream_t st) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
+  // Resolve the launch plan first, so that a shape the kernel cannot take is
+  // refused before anything is queued on the stream.
+  if (!noalloc_plan_ok(a, xdt, dev)) return cudaErrorInvalidConfiguration;
   float* base = nullptr;
   if ((e = noalloc_base(dev, &base)) != cudaSuccess) return e;
   const int64_t nrt = (a.N + kTileRows - 1) / kTileRows;
@@ -1414,12 +1783,19 @@ cudaError_t launch_qmv_stream_noalloc(const QmvArgs& a, int xdt, cudaStream_t st
   ws.cnt = reinterpret_cast<uint32_t*>(base + kNoAllocAccFloats);
   ws.acc_floats = kNoAllocAccFloats;
   ws.cnt_words = kNoAllocCounters;
-  // Row tile r's sums are block r (16 slots x 256 floats): clear the blocks
-  // and tile counters this call uses (a previous call may have been cut short).
+  // Row tile r's sums are block r (16 slots x 256 floats), of which a call
+  // with M token rows uses the first M slots: clear those and the tile
+  // counters (a previous call may have been cut short and left them dirty).
   if ((e = cudaMemsetAsync(ws.cnt, 0, (size_t)nrt * sizeof(uint32_t), st)) != cudaSuccess) return e;
-  if ((e = cudaMemsetAsync(ws.acc, 0, (size_t)nrt * kAccSlots * kTileRows * sizeof(float), st)) != cudaSuccess)
+  if ((e = cudaMemset2DAsync(ws.acc, (size_t)kAccSlots * kTileRows * sizeof(float), 0,
+                             (size_t)a.R * kTileRows * sizeof(float), (size_t)nrt, st)) != cudaSuccess)
     return e;
   return launch_rows(a, xdt, st, &ws);
+}
+
+void release_noalloc_addresses() {
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  g_noalloc.clear();
 }
 
 void release_stream_workspaces() {

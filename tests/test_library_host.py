@@ -262,3 +262,48 @@ def test_binding_rejects_cpu_tensors(nv):
     s = torch.zeros(4, 2, dtype=torch.uint8)
     with pytest.raises(ValueError):
         nv.qmm(x, w, s)
+
+
+def seq_calls(nv, n, **kw):
+    """n calls of [512, 256] at M = 4 with fake aligned addresses; kw
+    overrides fields of call 1 (or of the only call)."""
+    arr = (nv.QmmCall * n)()
+    for i in range(n):
+        c = dict(x=A, M=4, K=256, N=512, w=A, w_len=512 * 32, scales=A, scales_len=512 * 16, gs=None, gs_len=0,
+                 y=A, after_previous=0, reserved=0)
+        if i == min(1, n - 1):
+            c.update(kw)
+        arr[i] = nv.QmmCall(**c)
+    return arr
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(M=17), "ERR_LIMIT"),                                    # more than 16 token rows
+    (dict(K=272, w_len=512 * 34, scales_len=512 * 17), "ERR_SHAPE"),  # K % 256 != 0
+    (dict(w_len=512 * 32 - 1), "ERR_PLANE"),
+    (dict(scales_len=512 * 16 + 1), "ERR_PLANE"),
+    (dict(gs=A, gs_len=2), "ERR_GSCALE"),
+    (dict(x=U), "ERR_ALIGN"),
+    (dict(y=None), "ERR_NULL"),
+    (dict(M=-1), "ERR_SHAPE"),
+])
+def test_qmm_sequence_refusals(nv, kw, status):
+    lib = nv.library()
+    arr = seq_calls(nv, 3, **kw)
+    st = lib.nvfp4_qmm_sequence(ctypes.addressof(arr), 3, 2, None)
+    assert nv.STATUS[st] == status, (st, lib.nvfp4_last_error())
+    assert b"call 1" in lib.nvfp4_last_error()
+
+
+def test_qmm_sequence_refusals_of_the_whole(nv):
+    lib = nv.library()
+    arr = seq_calls(nv, 33)
+    assert nv.STATUS[lib.nvfp4_qmm_sequence(ctypes.addressof(arr), 33, 2, None)] == "ERR_LIMIT"
+    assert nv.STATUS[lib.nvfp4_qmm_sequence(ctypes.addressof(arr), -1, 2, None)] == "ERR_LIMIT"
+    assert nv.STATUS[lib.nvfp4_qmm_sequence(ctypes.addressof(arr), 2, 0, None)] == "ERR_DTYPE"  # f32
+    assert nv.STATUS[lib.nvfp4_qmm_sequence(None, 2, 2, None)] == "ERR_NULL"
+    # nothing to run: no calls, or only empty outputs (M = 0 or N = 0)
+    assert lib.nvfp4_qmm_sequence(None, 0, 2, None) == 0
+    empty = seq_calls(nv, 2, M=0)
+    empty[0] = nv.QmmCall(A, 4, 256, 0, A, 0, A, 0, None, 0, A, 0, 0)
+    assert lib.nvfp4_qmm_sequence(ctypes.addressof(empty), 2, 2, None) == 0
