@@ -1050,6 +1050,21 @@ __device__ bool wait_count(const uint32_t* ctr, uint32_t target, volatile int* a
   }
 }
 
+// Asks L2 for this CTA's 1/C share of a call's activations x (M K 16-bit
+// values, contiguous; a multiple of 512 bytes), so that when the consumers
+// stage the call they read L2 instead of waiting behind the weight stream in
+// HBM.
+__device__ __forceinline__ void prefetch_x_share(const QmvArgs& a, int b, int C) {
+  const uint64_t bytes = (uint64_t)a.R * (uint64_t)a.K * 2u;
+  const uint64_t share = ((bytes + (uint64_t)C - 1) / (uint64_t)C + 15u) & ~(uint64_t)15u;
+  const uint64_t start = (uint64_t)b * share;
+  if (start >= bytes) return;
+  const uint64_t len = bytes - start < share ? bytes - start : share;
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(static_cast<const char*>(a.x) + start),
+               "r"((uint32_t)len)
+               : "memory");
+}
+
 // Dynamic shared memory of the sequence kernel: the single-call layout with
 // a common ring depth, partial buffers of pslots token slots and room for the
 // largest staged activation slice of any call.
@@ -1118,6 +1133,8 @@ qmv_seq_kernel(const __grid_constant__ SeqArgs sa, float* __restrict__ acc, uint
       for (int c = 0; c < sa.ncalls; ++c) {
         const SeqCall& C = sa.call[c];
         if (b >= C.p.S * C.p.gs) continue;
+        // the consumers are still a ring's depth behind, on the previous call
+        if (c > 0 && !C.depends) prefetch_x_share(C.a, b, (int)gridDim.x);
         if (!produce<false, false>(C.p, b / C.p.gs, Work::of(C.p, b % C.p.gs), &C.wmap, &C.smap, wst, sst, bar,
                                    abort_flag, 0, pst, stages))
           break;
