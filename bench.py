@@ -4,12 +4,14 @@ Step (the headline): one decode-layer pass of the decode-shape workload. For
 each token count M in {1, 2, 4, 8, 16}, bf16 activations x [M, K] go through
 the three NVFP4 linears of a 31B-class layer (fused gate/up [43008, 5376],
 down [5376, 21504], qkv [8192, 5376]), each with an E4M3/16 scale plane and a
-per-linear float32 global scale: 15 `nvfp4_qmm` calls (the public API, route
-chosen by the library: all of them are on the decode-shape qmv route).
-`value` is the algorithmic HBM traffic of those calls (9/16 byte per weight
-element + activations + outputs + one global scale) divided by the step time,
-in GB/s. Five rotating weight copies (1.1 GB per step) keep every call's
-weights out of L2.
+per-linear float32 global scale: 15 QuantizedMatmuls, run by the public API
+as one `nvfp4_qmm_sequence` call (one persistent decode launch for the whole
+step). `value` is the algorithmic HBM traffic of those calls (9/16 byte per
+weight element + activations + outputs + one global scale) divided by the
+step time, in GB/s. Five rotating weight copies (1.1 GB per step) keep every
+call's weights out of L2. The same 15 calls as single `nvfp4_qmm` calls (15
+launches) are timed beside it (`step_single_calls`), and per call
+(`us_per_call`).
 
 `routes` reports the other configurations measured the same way (prefill
 QuantizedMatmul TFLOP/s, MoE GatherQMM, transcode, dequantize) for context.
@@ -43,12 +45,10 @@ WORKLOAD = ("decode-shape qmv: bf16 x [M in {1,2,4,8,16}, K] through NVFP4 gate/
             "per-linear f32 global scale in [0.5,2]*2688; bf16 out, f32 accumulate")
 METRIC = "qmv HBM GB/s & µs/call, qmm TFLOP/s; fraction of GB300 roofline (1 GPU)"
 
-# DRAM bytes (read + write) of the decode kernel over the 15 launches of one
-# step, from the ncu capture summarised in
-# profiles/qmv_stream_kernel_decode_step.md (`--case decode_step`); reported
-# per launch, and only while the kernel sources still hash to kernel_sha.
-TRAFFIC = {"source": "profiles/qmv_stream_kernel_decode_step.md", "kernel_sha": "ad82ae626227d1a3",
-           "bytes_per_step": 1124401408}
+# DRAM bytes (read + write) of the decode kernel over one step, from an ncu
+# capture of `--case decode_step`; reported per launch, and only while the
+# kernel sources still hash to kernel_sha.
+TRAFFIC = {"kernel_sha": "ad82ae626227d1a3", "bytes_per_step": 1124401408}
 TRAFFIC_FILES = ("nvfp4_qmv_stream.cu", "nvfp4_qmv_common.cuh", "nvfp4_common.cuh", "nvfp4_pipe.cuh")
 
 
@@ -203,23 +203,32 @@ def run_ours(args):
     nv.set_launch_overlap(args.launch_overlap == "on")
     lin, xs, ys = build_decode(nv, synth, torch, dev, rank)
     step_bytes = sum(qmv_bytes(m, n, k) for m in DECODE_M for _, n, k, _ in lin)
-    launches_per_step = len(DECODE_M) * len(LINEARS)
+    launches_per_step = 1
 
-    # One CUDA graph per rotation phase: the 15 calls of a step, weights
-    # rotated so consecutive steps never touch the same copy.
+    def step_sequence(shift):
+        return [(x, w, s, gs, y, False) for (m, n, k, x, w, s, gs, y) in decode_step_calls(nv, lin, xs, ys, shift)]
+
+    # One CUDA graph per rotation phase: the step's one sequence launch,
+    # weights rotated so consecutive steps never touch the same copy; and the
+    # same step as 15 single calls.
     stream = torch.cuda.Stream(device=dev)
-    graphs = []
+    graphs, single_graphs = [], []
     with torch.cuda.stream(stream):
         for shift in range(ROTATE):
+            nv.qmm_sequence(step_sequence(shift))  # warm the path outside capture
             for (m, n, k, x, w, s, gs, y) in decode_step_calls(nv, lin, xs, ys, shift):
-                nv.qmm(x, w, s, gs=gs, out=y)  # warm the path outside capture
+                nv.qmm(x, w, s, gs=gs, out=y)
         torch.cuda.synchronize(dev)
         for shift in range(ROTATE):
             gph = torch.cuda.CUDAGraph()
             with torch.cuda.graph(gph, stream=stream):
+                nv.qmm_sequence(step_sequence(shift))
+            graphs.append(gph)
+            gph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gph, stream=stream):
                 for (m, n, k, x, w, s, gs, y) in decode_step_calls(nv, lin, xs, ys, shift):
                     nv.qmm(x, w, s, gs=gs, out=y)
-            graphs.append(gph)
+            single_graphs.append(gph)
     torch.cuda.synchronize(dev)
 
     def barrier():
@@ -231,18 +240,39 @@ def run_ours(args):
         for i in range(args.warmup):
             graphs[i % ROTATE].replay()
     barrier()
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with ClockSampler(local) as clk:
+
+    def window(gs_list):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         with torch.cuda.stream(stream):
-            ev0.record(stream)
+            a.record(stream)
             for i in range(args.steps):
-                graphs[i % ROTATE].replay()
-            ev1.record(stream)
+                gs_list[i % ROTATE].replay()
+            b.record(stream)
         torch.cuda.synchronize(dev)
+        return a.elapsed_time(b)
+
+    with ClockSampler(local) as clk:
+        ms_window = window(graphs)  # the timed region: exactly K steps
+        barrier()
+        # further windows of K steps, for the spread of the step rate
+        extra = [window(graphs) for _ in range(args.windows - 1)]
     barrier()
-    ms_total = reduce_step_time(torch, dist, dev, ev0.elapsed_time(ev1))
+    ms_total = reduce_step_time(torch, dist, dev, ms_window)
     ms_step = ms_total / args.steps
     value = job_value(step_bytes, world, ms_step)
+    rates = sorted(step_bytes / (ms / args.steps * 1e-3) / 1e9 for ms in [ms_window] + extra)
+    spread = {"windows": len(rates), "steps_per_window": args.steps, "GBps_min": round(rates[0], 1),
+              "GBps_median": round(statistics.median(rates), 1), "GBps_max": round(rates[-1], 1)}
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            single_graphs[i % ROTATE].replay()
+    torch.cuda.synchronize(dev)
+    ms_single = window(single_graphs) / args.steps
+    step_single = {"ms_per_step": round(ms_single, 5),
+                   "GBps": round(step_bytes / (ms_single * 1e-3) / 1e9, 1),
+                   "launches_per_step": len(DECODE_M) * len(LINEARS),
+                   "path": "the same 15 calls as single nvfp4_qmm calls (one launch each, launch overlap as "
+                           "configured), one CUDA graph per step"}
 
     # Per-call latency (µs/call) per shape: ten calls (rotating weight copies)
     # captured in one CUDA graph, replayed, device time / 10.
@@ -271,6 +301,7 @@ def run_ours(args):
     # End to end through the public API: pinned host activations in, bf16
     # outputs back to pinned host memory, every step.
     e2e = run_e2e(nv, torch, dev, stream, lin, xs, ys, args, step_bytes)
+    del single_graphs
 
     routes = {} if args.no_routes else run_routes(nv, synth, torch, dev, stream, args)
     kernel_sha = source_sha(TRAFFIC_FILES)
@@ -283,15 +314,18 @@ def run_ours(args):
             "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "M": list(DECODE_M), "calls_per_step": launches_per_step,
+            "config": {"workload": WORKLOAD, "M": list(DECODE_M), "calls_per_step": len(DECODE_M) * len(LINEARS),
+                       "launches_per_step": launches_per_step, "api": "nvfp4_qmm_sequence (15 calls, one launch)",
                        "bytes_per_step": step_bytes, "l2": "inputs larger than L2: 5 rotating weight copies "
                        "(1.1 GB per step)", "graph": "one CUDA graph per step",
                        "launch_overlap": args.launch_overlap == "on"},
+            "spread": spread,
+            "step_single_calls": step_single,
             "us_per_call": per_call,
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
                          "frac": round(achieved / hbm_peak, 4), "peak_kind": f"{peak_kind} copy bandwidth",
                          "frac_of_8TBps": round(achieved / 8000.0, 4),
-                         "kernel": "qmv_stream_kernel (all 15 launches of the step)",
+                         "kernel": "qmv_seq_kernel (one launch per step)",
                          "traffic": None if traffic is None else round(traffic / launches_per_step)},
             "gpu_launches": launches_per_step * args.steps,
             "e2e": e2e,
@@ -305,9 +339,9 @@ def run_ours(args):
 
 
 def run_e2e(nv, torch, dev, stream, lin, xs, ys, args, step_bytes):
-    """The step through the public API, one call at a time (no graph), with the
-    step's activations copied in from pinned host memory and its outputs copied
-    back to pinned host memory every step. The 15 activation blocks live in one
+    """The step through the public API, one nvfp4_qmm_sequence call per step
+    (no graph), with the step's activations copied in from pinned host memory
+    and its outputs copied back to pinned host memory every step. The 15 activation blocks live in one
     buffer and the 15 outputs in another (views), so a step moves its inputs
     and outputs with one host-to-device and one device-to-host copy. As in a
     serving loop, the copies run on their own streams, double-buffered: step
@@ -347,10 +381,12 @@ def run_e2e(nv, torch, dev, stream, lin, xs, ys, args, step_bytes):
             stream.wait_event(x_in[b])
             if started[b]:
                 stream.wait_event(y_out[b])  # step i - 2's outputs have been copied out
+            calls = []
             for mi, m in enumerate(DECODE_M):
                 for name, n, k, copies in lin:
                     w, s, gs = copies[(mi + i) % ROTATE]
-                    nv.qmm(dev_x[b][(m, name)], w, s, gs=gs, out=dev_y[b][(m, name)])
+                    calls.append((dev_x[b][(m, name)], w, s, gs, dev_y[b][(m, name)], False))
+            nv.qmm_sequence(calls)
             y_done[b].record(stream)
         with torch.cuda.stream(down):
             down.wait_event(y_done[b])
@@ -370,8 +406,9 @@ def run_e2e(nv, torch, dev, stream, lin, xs, ys, args, step_bytes):
     ms = a.elapsed_time(z) / args.steps
     return {"value": round(step_bytes / (ms * 1e-3) / 1e9, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "ms_per_step": round(ms, 4),
-            "path": "nvfp4_qmm per call (no graph); per step one pinned-host copy in and one copy out, on their "
-                    "own streams, double-buffered so the copies of neighbouring steps overlap this step's calls"}
+            "path": "one nvfp4_qmm_sequence call per step (no graph); per step one pinned-host copy in and one copy "
+                    "out, on their own streams, double-buffered so the copies of neighbouring steps overlap this "
+                    "step's launch"}
 
 
 def time_calls(torch, dev, stream, fn, reps):
@@ -427,20 +464,22 @@ def run_routes(nv, synth, torch, dev, stream, args):
     out["qmm_prefill"] = pre
 
     # Route crossover: the decode-shape route against the tensor-core route
-    # for growing M on each decode linear (two weight copies alternate, so the
-    # weights come from HBM); M* is the first M where the tensor cores win.
+    # for M = 16 .. 8192 on each decode linear (two weight copies alternate,
+    # so the weights come from HBM); M* is the first M where the tensor cores
+    # win.
     cross = {}
     for name, n, k in LINEARS:
         ws = rand_w(n, k, 2, seed=7 * n + k)
         row = {"M": [], "qmv_us": [], "tc_us": []}
         first = None
-        for m in (16, 24, 32, 48, 64, 96, 128, 192, 256):
+        for m in (16, 24, 32, 48, 64, 96, 128, 192, 256, 512, 1024, 2048, 4096, 8192):
             x = synth.activations(g, (m, k), "bf16").to(dev)
             y = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
             t = {}
             for route in ("qmv", "tc"):
                 t[route] = time_calls(torch, dev, stream,
-                                      lambda i: nv.qmm(x, ws[i % 2][0], ws[i % 2][1], route=route, out=y), 6)
+                                      lambda i: nv.qmm(x, ws[i % 2][0], ws[i % 2][1], route=route, out=y),
+                                      6 if m <= 256 else 2)
             row["M"].append(m)
             row["qmv_us"].append(round(t["qmv"] * 1e3, 1))
             row["tc_us"].append(round(t["tc"] * 1e3, 1))
@@ -476,11 +515,32 @@ def run_routes(nv, synth, torch, dev, stream, args):
     _, n0, k0, w0, s0, g0, o0 = trip[0]
     ms_gu = time_calls(torch, dev, stream, lambda i: nv.transcode(w0, s0, g0, out=o0), 5)
     b_gu = 2 * 0.5625 * n0 * k0 + 8
+    del trip
+    # The whole 60-layer workload: every layer's three triplets resident on
+    # the device (13.2 GB in, 13.2 GB out), the 180 transcodes in one pass.
+    layers = []
+    for layer in range(60):
+        for j, (_, n, k) in enumerate(LINEARS):
+            mo_w, mo_s, ws2 = synth.device_modelopt_triplet(9000 + 3 * layer + j, n, k, dev)
+            outp = (torch.empty((n, k // 8), dtype=torch.int32, device=dev),
+                    torch.empty((n, k // 16), dtype=torch.uint8, device=dev),
+                    torch.empty((1,), dtype=torch.float32, device=dev))
+            layers.append((mo_w, mo_s, torch.tensor([float(ws2)], dtype=torch.float32, device=dev), outp))
+
+    def all_layers(i):
+        for (mo_w, mo_s, ws2, outp) in layers:
+            nv.transcode(mo_w, mo_s, ws2, out=outp)
+
+    ms_60 = time_calls(torch, dev, stream, all_layers, 1)
+    b_60 = 60 * layer_b
     out["transcode"] = {"layer_us": round(ms_layer * 1e3, 1), "layer_GBps": round(layer_b / (ms_layer * 1e-3) / 1e9, 1),
                         "layer_frac_hbm": round(layer_b / (ms_layer * 1e-3) / 1e9 / hbm_peak, 4),
                         "gate_up": {"us": round(ms_gu * 1e3, 1), "GBps": round(b_gu / (ms_gu * 1e-3) / 1e9, 1)},
-                        "60_layers_ms_est": round(60 * ms_layer, 2)}
-    del trip
+                        "60_layers_ms": round(ms_60, 3), "60_layers_GBps": round(b_60 / (ms_60 * 1e-3) / 1e9, 1),
+                        "60_layers_frac_hbm": round(b_60 / (ms_60 * 1e-3) / 1e9 / hbm_peak, 4),
+                        "60_layers_bytes": b_60}
+    del layers
+    torch.cuda.empty_cache()
 
     # Fused gate/up with GeGLU on the gate/up plane [43008, 5376] (I = 21504):
     # decode at M = 1 and 16 (bytes as for the plain call, output I wide) and
@@ -517,13 +577,9 @@ def run_routes(nv, synth, torch, dev, stream, args):
     xb = synth.activations(g, (bt * m, k), "bf16").reshape(bt, m, k).to(dev)
     yb = torch.empty((bt, m, n), dtype=torch.bfloat16, device=dev)
     ms_one = time_calls(torch, dev, stream, lambda i: nv.qmm_batched(xb, wb, sb, gs=gsb, out=yb), 10)
-    prev = os.environ.get("NVFP4_QMV_GROUP")
-    os.environ["NVFP4_QMV_GROUP"] = "0"
+    nv.set_option("gather_group", 0)  # one call per batch instead of one launch
     ms_loop = time_calls(torch, dev, stream, lambda i: nv.qmm_batched(xb, wb, sb, gs=gsb, out=yb), 10)
-    if prev is None:
-        os.environ.pop("NVFP4_QMV_GROUP")
-    else:
-        os.environ["NVFP4_QMV_GROUP"] = prev
+    nv.set_option("gather_group", 1)
     bb = bt * (0.5625 * n * k + 2 * m * k + 2 * m * n)
     out["qmm_batched_8x1536x2048_M4"] = {"us": round(ms_one * 1e3, 1), "GBps": round(bb / (ms_one * 1e-3) / 1e9, 1),
                                           "per_batch_calls_us": round(ms_loop * 1e3, 1)}
@@ -699,8 +755,9 @@ def run_case(args):
     three warm-up calls then one call each at M = 1, 8 and 16.
     qmv_shapes: each decode linear (gate/up, down, qkv; 220 MB) once at M = 1
     and once at M = 16, after one warm-up call each.
-    decode_step: the 15 calls of one decode step (one weight copy per linear),
-    once as warm-up and once more.
+    decode_step: the 15 calls of one decode step (one weight copy per linear)
+    as one nvfp4_qmm_sequence launch, once as warm-up and once more.
+    decode_step_single: the same 15 calls as single nvfp4_qmm calls.
     gather_prefill: the sorted MoE gate/up GatherQMM (4096 tokens, top-8 of
     128 experts), one warm-up call then one call.
     prefill: the tensor-core route at M = 2048 on the [21504, 5376] plane, one
@@ -783,11 +840,19 @@ def run_case(args):
         return
     if args.case == "decode_step":
         lin, xs, ys = build_decode(nv, synth, torch, dev, 0, copies=1)
+        calls = [(x, w, s, gs, y, False) for (m, n, k, x, w, s, gs, y) in decode_step_calls(nv, lin, xs, ys, 0)]
+        for _ in range(2):
+            nv.qmm_sequence(calls)
+        torch.cuda.synchronize(dev)
+        print("case decode_step ok")
+        return
+    if args.case == "decode_step_single":
+        lin, xs, ys = build_decode(nv, synth, torch, dev, 0, copies=1)
         for _ in range(2):
             for (m, n, k, x, w, s, gs, y) in decode_step_calls(nv, lin, xs, ys, 0):
                 nv.qmm(x, w, s, gs=gs, out=y)
         torch.cuda.synchronize(dev)
-        print("case decode_step ok")
+        print("case decode_step_single ok")
         return
     if args.case == "qmv_shapes":
         g = synth.rng(5100)
@@ -859,9 +924,12 @@ def main():
     ap.add_argument("--launch-overlap", choices=["on", "off"], default="on",
                     help="let each decode call start while the previous one finishes (weights are constant)")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--windows", type=int, default=5,
+                    help="timed windows of --steps steps; the first is the reported value, all give the spread")
     ap.add_argument("--cpu-rows", type=int, default=6144)
     ap.add_argument("--ref-rows", type=int, default=32)
-    ap.add_argument("--case", choices=["qmv_small", "qmv_shapes", "decode_step", "prefill", "gather_prefill",
+    ap.add_argument("--case", choices=["qmv_small", "qmv_shapes", "decode_step", "decode_step_single", "prefill",
+                                       "gather_prefill",
                                        "nontransposed_prefill", "nontransposed_decode", "quantize"],
                     default=None,
                     help="run one small profiling case instead of the benchmark")

@@ -75,8 +75,7 @@ typedef enum { NVFP4_ROUTE_AUTO = 0, NVFP4_ROUTE_QMV = 1, NVFP4_ROUTE_TC = 2 } n
  *   weight_scale_2   float [1]        device scalar
  *   w_out [N, K/8] uint32, scales_out [N, K/16] uint8, gs_out float [1]
  * Lengths must equal N*K/2 and N*K/16 (NVFP4_ERR_PLANE otherwise). The
- * planes are moved by bulk copies through shared memory (one CTA per SM);
- * NVFP4_TRANSCODE_BULK=0 selects a vector-copy kernel instead.
+ * planes are moved by bulk copies through shared memory (one CTA per SM).
  */
 nvfp4_status nvfp4_transcode(const uint8_t* mo_weight, int64_t mo_weight_len, const uint8_t* mo_weight_scale,
                              int64_t mo_weight_scale_len, const float* weight_scale_2, int64_t N, int64_t K,
@@ -145,9 +144,7 @@ nvfp4_status nvfp4_quantize(const void* x, nvfp4_dtype x_dtype, int64_t E, int64
  * computed by several CTAs is summed in a float32 workspace owned by the
  * library, one per (device, stream): 64 bytes per weight row plus a counter
  * per 256 rows, returned to zero by every call that completes. Calls on one
- * stream are ordered, so they never share it concurrently. The environment
- * variable NVFP4_QMV_STREAM=0 selects the cluster-split decode kernel instead
- * (no workspace).
+ * stream are ordered, so they never share it concurrently.
  */
 nvfp4_status nvfp4_qmm(const void* x, nvfp4_dtype x_dtype, int64_t M, int64_t K, const uint32_t* w,
                        int64_t w_len, const uint8_t* scales, int64_t scales_len, const float* gs,
@@ -173,7 +170,8 @@ nvfp4_status nvfp4_qmm_routed(const void* x, nvfp4_dtype x_dtype, int64_t M, int
  * One or two token rows: one streaming pass over the plane (a warp per 256
  * outputs x 128 inputs), partial sums added into a float workspace [2, N]
  * owned by the library, one per (device, stream), returned to zero by every
- * call; then y. More rows (or NVFP4_NT_DECODE=0): the tcgen05 tensor-core
+ * call; then y. More rows (or the NVFP4_OPT_NT_DECODE option set to 0): the
+ * tcgen05 tensor-core
  * kernel, whose producer warps decode and transpose the weight tiles into
  * shared memory (the pages send every M to dequantize + GEMM). With
  * K % 8 != 0 the tensor-core route first copies the activations, rows padded
@@ -307,16 +305,17 @@ int64_t nvfp4_qmm_crossover(nvfp4_dtype x_dtype, int64_t N, int64_t K);
  * activations, K % 256 == 0 and at most one row per SM group the rows by
  * expert (eight to a group, in row order) and stream each group's expert
  * plane once, split over the SMs; they use the decode route's workspace (see
- * nvfp4_qmm). NVFP4_QMV_GROUP=0 sends them to the per-row kernel instead.
+ * nvfp4_qmm). The NVFP4_OPT_GATHER_GROUP option set to 0 sends them to the
+ * per-row kernel instead.
  * `sorted_indices` != 0
  * promises expert indices in non-decreasing order (a sorted MoE prefill) and
  * lets 16-bit calls with enough rows per expert (R >= 512 and R >= 16 E, E <=
  * 1024, K % 32 == 0) take the expert-batched tensor-core route; the
- * environment variable NVFP4_GATHER_TC (1/0) forces or disables that route.
+ * NVFP4_OPT_GATHER_TC option forces (1) or disables (0) that route.
  * With lhs_indices that route first copies the activation rows into output
  * order, in a buffer of R * K * 2 bytes that the library keeps per (device,
  * stream) until nvfp4_shutdown() (made outside any capture, as the decode
- * workspace); NVFP4_GATHER_ROWS=tma fetches the rows per tile instead.
+ * workspace).
  * If the promise is broken on that route, every output row is still written
  * once and nothing outside the inputs is read, but rows are computed with
  * the expert of the sorted segment they fall in.
@@ -348,6 +347,30 @@ int32_t nvfp4_take_device_error(void);
  * part of the pages' interface: it removes the idle gap between consecutive
  * decode-step matmuls, whose weights are constant. */
 int nvfp4_set_launch_overlap(int enable);
+
+/* Process-wide choices between equivalent kernels, for tests and tuning; the
+ * defaults are the automatic choices and results agree to the stated
+ * tolerances whatever is set. Not part of the pages' interface. */
+typedef enum {
+  NVFP4_OPT_TC_TILE = 1,        /* prefill tile: 0 automatic (default), 1 256x256, 2 256x128, 3 128x256 */
+  NVFP4_OPT_TC_STREAMK = 2,     /* 1 (default): fewer than two waves of prefill tiles are split by k-blocks
+                                   over all SMs; 0: whole tiles only */
+  NVFP4_OPT_NT_DECODE = 3,      /* 1 (default): one or two rows of a non-transposed weight take the streaming
+                                   kernel; 0: the tensor cores */
+  NVFP4_OPT_QMV_ROW_TILES = 4,  /* 16-row weight tiles per decode consumer warp: 0 automatic (default), 1, 2 */
+  NVFP4_OPT_GATHER_GROUP = 5,   /* 1 (default): decode-shape gathers grouped by expert; 0: the per-row kernel */
+  NVFP4_OPT_GATHER_TC = 6,      /* -1 automatic (default); 1: sorted gathers take the expert-batched
+                                   tensor-core route wherever supported; 0: never */
+  NVFP4_OPT_GATHER_TILE = 7     /* expert-batched route's tile: 0 automatic (default, 256x256), 1 256x256,
+                                   2 256x128, 3 128x256 */
+} nvfp4_option;
+
+/* Sets an option: NVFP4_ERR_DTYPE for an unknown option, NVFP4_ERR_LIMIT
+ * for a value outside its range (nothing changed). Takes effect for calls
+ * made afterwards (a CUDA graph keeps the kernels it captured). */
+nvfp4_status nvfp4_set_option(nvfp4_option option, int32_t value);
+/* The option's current value (INT32_MIN for an unknown option). */
+int32_t nvfp4_get_option(nvfp4_option option);
 
 /* Frees the library's scratch (decode workspaces, stream-K sums, gathered-row
  * buffers) on every device. Call only when no

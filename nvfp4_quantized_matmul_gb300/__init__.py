@@ -5,7 +5,7 @@ The compute path lives in ``libnvfp4.so`` (CUDA kernels behind a C ABI); the
 first use, so ``synth`` can be imported on machines without the library.
 """
 _LAZY = ("transcode", "dequantize", "qmm", "gather_qmm", "library", "qmm_crossover", "take_device_error",
-         "set_launch_overlap", "shutdown", "qmm_noalloc", "qmm_sequence", "qmm_glu", "qmm_batched",
+         "set_launch_overlap", "set_option", "get_option", "shutdown", "qmm_noalloc", "qmm_sequence", "qmm_glu", "qmm_batched",
          "qmm_nontransposed", "quantize",
          "transcode_folded")
 

@@ -52,6 +52,8 @@ SIGNATURES = {
     "nvfp4_version": (ctypes.c_char_p, []),
     "nvfp4_take_device_error": (ctypes.c_int32, []),
     "nvfp4_set_launch_overlap": (_INT, [_INT]),
+    "nvfp4_set_option": (_INT, [_INT, ctypes.c_int32]),
+    "nvfp4_get_option": (ctypes.c_int32, [_INT]),
     "nvfp4_shutdown": (None, []),
 }
 
@@ -331,6 +333,23 @@ def set_launch_overlap(enable):
     finishes (the weight planes must not be written by a kernel still running).
     Returns the previous setting."""
     return bool(_lib.nvfp4_set_launch_overlap(int(bool(enable))))
+
+
+OPTION_CODE = {"tc_tile": 1, "tc_streamk": 2, "nt_decode": 3, "qmv_row_tiles": 4, "gather_group": 5,
+               "gather_tc": 6, "gather_tile": 7}
+TILE_CODE = {"auto": 0, "256x256": 1, "256x128": 2, "128x256": 3}
+
+
+def set_option(name, value):
+    """Sets one of the library's process-wide kernel choices (nvfp4_set_option);
+    tile options also take "256x256", "256x128" or "128x256"."""
+    if isinstance(value, str):
+        value = TILE_CODE[value]
+    check(_lib.nvfp4_set_option(OPTION_CODE[name], int(value)))
+
+
+def get_option(name):
+    return int(_lib.nvfp4_get_option(OPTION_CODE[name]))
 
 
 def shutdown():

@@ -133,6 +133,15 @@ int64_t env_crossover() {
 namespace nvfp4 {
 std::atomic<int> g_launch_overlap{0};
 bool launch_overlap() { return g_launch_overlap.load(std::memory_order_relaxed) != 0; }
+
+namespace {
+// Index: nvfp4_option value (0 unused). Defaults: automatic choices.
+std::atomic<int> g_options[kOptEnd] = {0, 0, 1, 1, 0, 1, -1, 0};
+constexpr int kOptMin[kOptEnd] = {0, 0, 0, 0, 0, 0, -1, 0};
+constexpr int kOptMax[kOptEnd] = {0, 3, 1, 1, 2, 1, 1, 3};
+}  // namespace
+
+int option(int opt) { return g_options[opt].load(std::memory_order_relaxed); }
 }  // namespace nvfp4
 
 extern "C" {
@@ -148,6 +157,23 @@ int32_t nvfp4_take_device_error(void) {
             d = nvfp4::read_copy_error();
   if (a < 0 || b < 0 || c < 0 || d < 0) return -1;
   return a ? a : b ? b : c ? c : d;
+}
+
+nvfp4_status nvfp4_set_option(nvfp4_option option, int32_t value) {
+  const int o = (int)option;
+  if (o <= 0 || o >= nvfp4::kOptEnd)
+    return fail(NVFP4_ERR_DTYPE, "nvfp4_set_option: unknown option %d", o);
+  if (value < nvfp4::kOptMin[o] || value > nvfp4::kOptMax[o])
+    return fail(NVFP4_ERR_LIMIT, "nvfp4_set_option: value %d of option %d outside %d..%d", (int)value, o,
+                nvfp4::kOptMin[o], nvfp4::kOptMax[o]);
+  nvfp4::g_options[o].store((int)value, std::memory_order_relaxed);
+  return ok();
+}
+
+int32_t nvfp4_get_option(nvfp4_option option) {
+  const int o = (int)option;
+  if (o <= 0 || o >= nvfp4::kOptEnd) return INT32_MIN;
+  return nvfp4::option(o);
 }
 
 void nvfp4_shutdown(void) {
@@ -376,9 +402,9 @@ nvfp4_status nvfp4_qmm_nontransposed(const void* x, nvfp4_dtype x_dtype, int64_t
   if (!aligned(x, 16) || !aligned(y, 16)) return fail(NVFP4_ERR_ALIGN, "%s: x and y must be 16-byte aligned", fn);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (K == 0) return cuda_status(fn, cudaMemsetAsync(y, 0, (size_t)(M * N * dtype_size(x_dtype)), st));
-  // one or two token rows: one streaming pass (NVFP4_NT_DECODE=0 sends every M to the tensor cores)
-  const char* dec = std::getenv("NVFP4_NT_DECODE");
-  if (!(dec && dec[0] == '0') && nvfp4::qmv_nt_supported(M, N, K))
+  // one or two token rows: one streaming pass (the NVFP4_OPT_NT_DECODE option
+  // set to 0 sends every M to the tensor cores)
+  if (nvfp4::option(nvfp4::kOptNtDecode) != 0 && nvfp4::qmv_nt_supported(M, N, K))
     return cuda_status(fn, nvfp4::launch_qmv_nt(x, (int)x_dtype, M, K, w, scales, gs, N, y, st));
   if (!nvfp4::qmm_tc_nt_supported(M, N, K))
     return fail(NVFP4_ERR_LIMIT, "%s: M or K of 2^31 or more, or too many tiles", fn);
@@ -520,11 +546,11 @@ nvfp4_status nvfp4_gather_qmm(const void* x, nvfp4_dtype x_dtype, int64_t B, int
   if (K == 0) return cuda_status(fn, cudaMemsetAsync(y, 0, (size_t)(R * N * dtype_size(x_dtype)), st));
   // Sorted rows with enough of them per expert take the expert-batched
   // tensor-core route (128-row tiles; below about 16 rows per expert the tiles
-  // would mostly be padding). NVFP4_GATHER_TC=1 forces it where supported,
-  // =0 disables it.
+  // would mostly be padding). The NVFP4_OPT_GATHER_TC option forces (1) or
+  // disables (0) it.
   if (sorted_indices && x_dtype != NVFP4_F32 && nvfp4::gather_tc_supported(B, K, R, E, N)) {
-    const char* force = std::getenv("NVFP4_GATHER_TC");
-    const bool use = force ? force[0] == '1' : (R >= 512 && R >= 16 * E);
+    const int force = nvfp4::option(nvfp4::kOptGatherTc);
+    const bool use = force >= 0 ? force == 1 : (R >= 512 && R >= 16 * E);
     if (use)
       return cuda_status(fn, nvfp4::launch_gather_tc(x, (int)x_dtype, B, K, lhs_indices, rhs_indices, R, w, scales, gs,
                                                      E, N, y, st));

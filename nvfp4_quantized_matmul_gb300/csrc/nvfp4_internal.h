@@ -87,6 +87,21 @@ constexpr int kSeqMaxCallsApi = 32;
 bool qmv_seq_call_supported(const QmvArgs& a, int xdt);
 cudaError_t launch_qmv_seq(const QmvArgs* calls, const int* depends, int n, int xdt, cudaStream_t st);
 
+// Process-wide options set through nvfp4_set_option (include/nvfp4.h); each
+// kernel family reads its own with option(). The values are those of the
+// header's nvfp4_option enumeration.
+enum Option : int {
+  kOptTcTile = 1,
+  kOptTcStreamK = 2,
+  kOptNtDecode = 3,
+  kOptQmvRowTiles = 4,
+  kOptGatherGroup = 5,
+  kOptGatherTc = 6,
+  kOptGatherTile = 7,
+  kOptEnd = 8
+};
+int option(int opt);
+
 // Whether weight-streaming launches may overlap the previous kernel on the
 // stream (programmatic dependent launch; see nvfp4_set_launch_overlap).
 bool launch_overlap();
@@ -94,7 +109,7 @@ bool launch_overlap();
 // Prefill-shape tensor-core route (tcgen05, TMEM accumulators).
 bool qmm_tc_supported(int64_t M, int64_t N, int64_t K);
 // Whether its dense launches split the last partial wave of tiles by k-blocks
-// (stream-K; on unless NVFP4_TC_STREAMK=0).
+// (stream-K; on unless the NVFP4_OPT_TC_STREAMK option is 0).
 bool tc_stream_k();
 cudaError_t launch_qmm_tc(const void* x, int xdt, int64_t M, int64_t K, const uint32_t* w, const uint8_t* scales,
                           const float* gs, int64_t N, void* y, cudaStream_t st);

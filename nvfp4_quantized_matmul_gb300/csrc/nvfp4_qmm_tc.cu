@@ -88,8 +88,6 @@ struct TcParams {
   const uint32_t* rhs;
   int64_t B;    // activation rows
   int E;        // experts
-  int xcontig;  // gather: the activations of output row r are row r of the
-                // mapped x (x itself, or x gathered into output-row order)
   // Stream-K launches (qmm_tc_sk_kernel): tiles [0, dp_tiles) are dealt
   // whole, round robin; the k-block iterations of tiles [dp_tiles, dp_tiles +
   // sk_tiles) are divided evenly over the CTAs. A tile shared by several CTAs
@@ -741,15 +739,6 @@ __device__ void build_gather_tables(const TcParams& p, uint32_t* samp, int* seg,
   __syncthreads();
 }
 
-__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* map, int c0, int r0, int r1, int r2, int r3,
-                                            uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, "
-      "%4, %5, %6}], [%7];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(bar)
-      : "memory");
-}
-
 // ---------------------------------------------------------------- kernel
 
 template <typename T, typename C, bool GATHER, bool kGlu = false, bool kNT = false>
@@ -831,7 +820,7 @@ qmm_tc_kernel(const __grid_constant__ CUtensorMap xmap, const TcParams p) {
           }
         }
       }
-    } else if (p.xcontig) {
+    } else {
       // The tile's activations are rows m0 .. m0 + rows - 1 of the mapped x:
       // one 128-row box per M half that holds rows of the tile (rows past
       // them belong to the next expert or lie beyond x; they are computed but
@@ -853,42 +842,6 @@ qmm_tc_kernel(const __grid_constant__ CUtensorMap xmap, const TcParams p) {
                             (int)(tl.m0 + 128 * h), fullA(s));
           }
           __syncwarp();
-        }
-      }
-    } else {
-      // Each lane fetches four activation rows of every 128-row half that
-      // holds rows of the tile with one tile::gather4 copy per k-block; rows
-      // past the tile's end or with an out-of-range activation index read row
-      // 0 (their outputs are not taken from the accumulator).
-      bool ok = true;
-      for (int i = 0; i < my_tiles && ok; ++i) {
-        const Tile tl = tile_of<true, BM>(p, (int)blockIdx.x + i * (int)gridDim.x, seg, pre);
-        const int mh = (tl.rows + 127) / 128;
-        int xr[MH][4];
-#pragma unroll
-        for (int h = 0; h < MH; ++h)
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const int rr = 128 * h + 4 * lane + j;
-            int64_t v = 0;
-            if (rr < tl.rows) {
-              const int64_t r = tl.m0 + rr;
-              v = p.lhs ? (int64_t)__ldg(p.lhs + r) : r;
-              if (v >= p.B) v = 0;
-            }
-            xr[h][j] = (int)v;
-          }
-        for (int kb = 0; kb < p.num_kb; ++kb, ++u) {
-          const int s = (int)(u % STAGES);
-          const uint32_t ph = (u / STAGES) & 1;
-          if (!wait_bar_warp(emptyB(s), ph ^ 1, abort_flag, 1, &g_tc_error)) { ok = false; break; }
-          if (lane == 0) mbar_arrive_tx(fullA(s), (uint32_t)mh * kHalfA);
-          __syncwarp();
-#pragma unroll
-          for (int h = 0; h < MH; ++h)
-            if (h < mh)
-              tma_gather4(sA + (uint32_t)s * C::A_BYTES + (uint32_t)h * kHalfA + 512u * (uint32_t)lane, &xmap,
-                          kb * BK, xr[h][0], xr[h][1], xr[h][2], xr[h][3], fullA(s));
         }
       }
     }
@@ -1145,7 +1098,7 @@ qmm_tc_sk_kernel(const __grid_constant__ CUtensorMap xmap, const TcParams p) {
           }
         }
       }
-    } else if (p.xcontig) {
+    } else {
       // The tile's activations are rows m0 .. m0 + rows - 1 of the mapped x:
       // one 128-row box per M half that holds rows of the tile (rows past
       // them belong to the next expert or lie beyond x; they are computed but
@@ -1167,42 +1120,6 @@ qmm_tc_sk_kernel(const __grid_constant__ CUtensorMap xmap, const TcParams p) {
                             (int)(tl.m0 + 128 * h), fullA(s));
           }
           __syncwarp();
-        }
-      }
-    } else {
-      // Each lane fetches four activation rows of every 128-row half that
-      // holds rows of the tile with one tile::gather4 copy per k-block; rows
-      // past the tile's end or with an out-of-range activation index read row
-      // 0 (their outputs are not taken from the accumulator).
-      bool ok = true;
-      while (ok && sched.next(un)) {
-        const Tile tl = tile_of<true, BM>(p, un.tile, seg, pre);
-        const int mh = (tl.rows + 127) / 128;
-        int xr[MH][4];
-#pragma unroll
-        for (int h = 0; h < MH; ++h)
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const int rr = 128 * h + 4 * lane + j;
-            int64_t v = 0;
-            if (rr < tl.rows) {
-              const int64_t r = tl.m0 + rr;
-              v = p.lhs ? (int64_t)__ldg(p.lhs + r) : r;
-              if (v >= p.B) v = 0;
-            }
-            xr[h][j] = (int)v;
-          }
-        for (int kb = un.kb0; kb < un.kb1; ++kb, ++u) {
-          const int s = (int)(u % STAGES);
-          const uint32_t ph = (u / STAGES) & 1;
-          if (!wait_bar_warp(emptyB(s), ph ^ 1, abort_flag, 1, &g_tc_error)) { ok = false; break; }
-          if (lane == 0) mbar_arrive_tx(fullA(s), (uint32_t)mh * kHalfA);
-          __syncwarp();
-#pragma unroll
-          for (int h = 0; h < MH; ++h)
-            if (h < mh)
-              tma_gather4(sA + (uint32_t)s * C::A_BYTES + (uint32_t)h * kHalfA + 512u * (uint32_t)lane, &xmap,
-                          kb * BK, xr[h][0], xr[h][1], xr[h][2], xr[h][3], fullA(s));
         }
       }
     }
@@ -1488,7 +1405,6 @@ cudaError_t launch_cfg(const void* x, int64_t M, int64_t K, const uint32_t* w, c
   p.rhs = nullptr;
   p.B = M;
   p.E = 1;
-  p.xcontig = 1;
   p.glu_cols = 0;
   p.glu_act = 0;
   // Tiles are dealt whole, round robin, unless they make fewer than two
@@ -1567,7 +1483,6 @@ cudaError_t launch_glu_cfg(const void* x, int64_t M, int64_t K, const uint32_t* 
   p.rhs = nullptr;
   p.B = M;
   p.E = 1;
-  p.xcontig = 1;
   p.dp_tiles = p.num_tiles;
   p.sk_tiles = 0;
   p.ws = nullptr;
@@ -1586,19 +1501,14 @@ cudaError_t launch_glu_cfg(const void* x, int64_t M, int64_t K, const uint32_t* 
 // partial wave to avoid, and 256x256 tiles, whose decoded weight tile feeds
 // twice the MMA work, were the fastest or within 4% of it on every such shape
 // measured on GB300 (M = 64 .. 512 at K = 5376, M = 2048 at K = 21504).
-// Otherwise (or with NVFP4_TC_STREAMK=0) the shape is picked by modelled
-// time: whole waves of persistent tiles, each tile's cost its area over the
-// shape's relative throughput (measured with full waves at M = 8192,
+// Otherwise (or with the stream-K option off) the shape is picked by
+// modelled time: whole waves of persistent tiles, each tile's cost its area
+// over the shape's relative throughput (measured with full waves at M = 8192,
 // [21504, 5376]: 256x128 tiles run at 0.81 of 256x256, 128x256 tiles at
-// 0.54). The environment variable NVFP4_TC_TILE ("256x256", "256x128" or
-// "128x256") overrides either choice.
+// 0.54). The NVFP4_OPT_TC_TILE option overrides either choice.
 int pick_tile(int64_t M, int64_t N, int sms) {
-  const char* forced = std::getenv("NVFP4_TC_TILE");
-  if (forced) {
-    if (!std::strcmp(forced, "256x256")) return 0;
-    if (!std::strcmp(forced, "256x128")) return 1;
-    if (!std::strcmp(forced, "128x256")) return 2;
-  }
+  const int forced = option(kOptTcTile);  // 1 256x256, 2 256x128, 3 128x256
+  if (forced >= 1 && forced <= 3) return forced - 1;
   // fewer than two waves of 256x256 tiles: the stream-K split applies
   if (stream_k_on() && ((M + 255) / 256) * ((N + 255) / 256) < 2 * sms) return 0;
   const int bm[3] = {256, 256, 128}, bn[3] = {256, 128, 256};
@@ -1692,9 +1602,9 @@ cudaError_t gather_buffer(int dev, cudaStream_t st, size_t bytes, void** out) {
 // is known only on the device. A tile covers up to C::BM rows of one expert's
 // segment; a tile whose rows fit one 128-row half computes only that half.
 // With activation indices the rows are first gathered into output-row order,
-// so that every activation tile is a plain 128-row TMA box (a tile::gather4
-// copy moves four rows, and at 32 of them per box the copy engine, not the
-// tensor core, set the pace); NVFP4_GATHER_ROWS=tma keeps the per-row copies.
+// so that every activation tile is a plain 128-row TMA box (per-row
+// tile::gather4 copies, four rows each and 32 per box, left the copy engine,
+// not the tensor core, setting the pace).
 template <typename T, typename C>
 cudaError_t launch_gather(const void* x, int64_t B, int64_t K, const uint32_t* lhs, const uint32_t* rhs, int64_t R,
                           const uint32_t* w, const uint8_t* scales, const float* gs, int64_t E, int64_t N, void* y,
@@ -1704,11 +1614,9 @@ cudaError_t launch_gather(const void* x, int64_t B, int64_t K, const uint32_t* l
   int dev = 0, sms = 152;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const char* rows_env = std::getenv("NVFP4_GATHER_ROWS");
-  const bool per_row = lhs && rows_env && !std::strcmp(rows_env, "tma");
   const void* xa = x;
   int64_t xrows = B;
-  if (lhs && !per_row) {
+  if (lhs) {
     void* xg = nullptr;
     cudaError_t e = gather_buffer(dev, st, (size_t)R * (size_t)K * 2, &xg);
     if (e != cudaSuccess) return e;
@@ -1722,7 +1630,7 @@ cudaError_t launch_gather(const void* x, int64_t B, int64_t K, const uint32_t* l
   CUtensorMap map;
   const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)xrows};
   const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
-  const cuuint32_t box[2] = {BK, per_row ? 1u : 128u};  // tile::gather4 takes a one-row box
+  const cuuint32_t box[2] = {BK, 128u};
   const cuuint32_t estr[2] = {1, 1};
   const CUtensorMapDataType dt =
       std::is_same<T, __nv_bfloat16>::value ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
@@ -1745,7 +1653,6 @@ cudaError_t launch_gather(const void* x, int64_t B, int64_t K, const uint32_t* l
   p.rhs = rhs;
   p.B = B;
   p.E = (int)E;
-  p.xcontig = per_row ? 0 : 1;
   p.glu_cols = 0;
   p.glu_act = 0;
   const size_t smem = C::SMEM + kGatherSmem;
@@ -1756,17 +1663,15 @@ cudaError_t launch_gather(const void* x, int64_t B, int64_t K, const uint32_t* l
   return cudaGetLastError();
 }
 
-// Gather tile: 256 rows (two halves) by default, NVFP4_GATHER_TILE = "128x256"
-// or "256x128" to override.
+// Gather tile: 256 rows (two halves) by default; the NVFP4_OPT_GATHER_TILE
+// option selects 256x128 or 128x256 instead.
 template <typename T>
 cudaError_t launch_gather_t(const void* x, int64_t B, int64_t K, const uint32_t* lhs, const uint32_t* rhs, int64_t R,
                             const uint32_t* w, const uint8_t* scales, const float* gs, int64_t E, int64_t N, void* y,
                             cudaStream_t st) {
-  const char* t = std::getenv("NVFP4_GATHER_TILE");
-  if (t && !std::strcmp(t, "128x256"))
-    return launch_gather<T, Tile128x256>(x, B, K, lhs, rhs, R, w, scales, gs, E, N, y, st);
-  if (t && !std::strcmp(t, "256x128"))
-    return launch_gather<T, Tile256x128>(x, B, K, lhs, rhs, R, w, scales, gs, E, N, y, st);
+  const int t = option(kOptGatherTile);  // 0 or 1 256x256, 2 256x128, 3 128x256
+  if (t == 3) return launch_gather<T, Tile128x256>(x, B, K, lhs, rhs, R, w, scales, gs, E, N, y, st);
+  if (t == 2) return launch_gather<T, Tile256x128>(x, B, K, lhs, rhs, R, w, scales, gs, E, N, y, st);
   return launch_gather<T, Tile256x256>(x, B, K, lhs, rhs, R, w, scales, gs, E, N, y, st);
 }
 
@@ -1830,7 +1735,6 @@ cudaError_t launch_nt_cfg(const void* x, int64_t M, int64_t K, const uint32_t* w
   p.rhs = nullptr;
   p.B = M;
   p.E = 1;
-  p.xcontig = 1;
   p.glu_cols = 0;
   p.glu_act = 0;
   // the dense route's rule: below two waves of tiles (and not whole waves)
@@ -1910,10 +1814,7 @@ cudaError_t launch_qmm_tc_nt(const void* x, int xdt, int64_t M, int64_t K, const
                   : launch_nt_cfg<__half, Tile256x256>(x, M, K, w, scales, gs, N, y, sms, st);
 }
 
-bool tc_stream_k() {
-  const char* e = std::getenv("NVFP4_TC_STREAMK");
-  return !(e && e[0] == '0');
-}
+bool tc_stream_k() { return option(kOptTcStreamK) != 0; }
 
 bool qmm_tc_supported(int64_t M, int64_t N, int64_t K) {
   // TMA coordinates are 32-bit; K must keep each 128-bit weight load within

@@ -1453,11 +1453,12 @@ cudaError_t launch_mt(const QmvArgs& a, int xdt, cudaStream_t st, const Ws* give
 
 // One launch for up to 16 token rows: eight token slots per MMA tile (MT),
 // and RT weight row tiles per consumer warp (RT = 2 shares each activation
-// fragment between two row tiles; NVFP4_QMV_RT=1/2 overrides the choice).
+// fragment between two row tiles; the NVFP4_OPT_QMV_ROW_TILES option
+// overrides the choice).
 cudaError_t launch_rows(const QmvArgs& a, int xdt, cudaStream_t st, const Ws* ws) {
   int rt = a.R > 8 ? 2 : 1;
-  if (const char* ev = std::getenv("NVFP4_QMV_RT"))
-    if (ev[0] == '1' || ev[0] == '2') rt = ev[0] - '0';
+  const int forced = option(kOptQmvRowTiles);
+  if (forced == 1 || forced == 2) rt = forced;
   if (a.R > 8) return rt == 2 ? launch_mt<2, 2>(a, xdt, st, ws) : launch_mt<2, 1>(a, xdt, st, ws);
   return rt == 2 ? launch_mt<1, 2>(a, xdt, st, ws) : launch_mt<1, 1>(a, xdt, st, ws);
 }
@@ -1510,8 +1511,7 @@ bool group_plan(const QmvArgs& a, int xdt, int dev, SPlan* out) {
 }  // namespace
 
 bool qmv_group_supported(const QmvArgs& a, int xdt) {
-  if (const char* ev = std::getenv("NVFP4_QMV_GROUP"))
-    if (ev[0] == '0') return false;
+  if (option(kOptGatherGroup) == 0) return false;
   if (xdt == kF32 || (a.rhs == nullptr && a.rows_per_expert <= 0) || a.R < 1 || a.K % kChunkCols != 0 || a.K <= 0 ||
       a.N <= 0 ||
       a.N >= (1ll << 31) || a.K / kChunkCols > 4096 || a.E < 1 || a.E >= (1ll << 31))
@@ -1548,8 +1548,6 @@ cudaError_t launch_qmv_group(const QmvArgs& a, int xdt, cudaStream_t st) {
 }
 
 bool qmv_stream_supported(const QmvArgs& a, int xdt) {
-  if (const char* ev = std::getenv("NVFP4_QMV_STREAM"))
-    if (ev[0] == '0') return false;
   return xdt != kF32 && a.rhs == nullptr && a.lhs == nullptr && a.E == 1 && a.R >= 1 && a.K % kChunkCols == 0 &&
          a.K > 0 && a.N > 0 && a.N < (1ll << 31) && a.K / kChunkCols <= 4096;
 }

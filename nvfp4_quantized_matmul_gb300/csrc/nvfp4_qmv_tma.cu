@@ -605,32 +605,6 @@ cudaError_t launch_mt(const QmvArgs& a, Plan pl, int64_t row_tiles, cudaStream_t
       };
       pl = tma_plan(pl, row_tiles, capacity);
       cache[key] = pl;
-      if (std::getenv("NVFP4_QMV_PLAN_LOG")) {
-        std::fprintf(stderr, "nvfp4 qmv plan N=%lld K=%lld E=%lld rows=%lld: C=%d slabs/cluster=%d stages=%d; resident CTAs by C:",
-                     (long long)a.N, (long long)a.K, (long long)a.E, (long long)a.R, pl.C, pl.spc, pl.stages);
-        for (int C = 1; C <= 16 && C <= pl.nchunk; ++C) {
-          Plan q = pl;
-          q.C = C;
-          q.xs_stride = ((pl.nchunk + C - 1) / C) * kChunkCols + 32;
-          std::fprintf(stderr, " %d:%lld", C, (long long)capacity(C, tma_smem_bytes(q)));
-        }
-        std::fprintf(stderr, "\n");
-      }
-    }
-  }
-  // NVFP4_QMV_PLAN="C,slabs_per_cluster,stages" overrides the plan (tuning).
-  if (const char* ev = std::getenv("NVFP4_QMV_PLAN")) {
-    int C = 0, spc = 0, stages = 0;
-    if (std::sscanf(ev, "%d,%d,%d", &C, &spc, &stages) == 3 && C >= 1 && C <= 16 && C <= pl.nchunk && spc >= 1 &&
-        stages >= 2 && stages <= kMaxStages) {
-      Plan q = pl;
-      q.C = C;
-      q.spc = spc;
-      q.stages = stages;
-      q.xs_stride = ((pl.nchunk + C - 1) / C) * kChunkCols + 32;
-      std::lock_guard<std::mutex> lock(mu);
-      if (tma_smem_bytes(q) > (size_t)max_dyn_of_dev[dev]) return cudaErrorInvalidConfiguration;
-      pl = q;
     }
   }
   if (pl.C == 0) return cudaErrorInvalidValue;

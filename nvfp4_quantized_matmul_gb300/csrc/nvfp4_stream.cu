@@ -32,49 +32,19 @@ int stream_grid(Kern kern, int64_t units) {
 // Implementation plan step 3). ModelOpt's U8 plane stores column 2j in the
 // low nibble of byte j; packing four consecutive bytes little-endian into one
 // uint32 therefore yields the native word with column 8i+k in nibble k. That
-// repack is the identity on the byte stream, so the kernel is a 16-byte
-// vectorised copy of both planes; the E4M3 block scales are kept byte for
-// byte and the sidecar is f32(ws2) * 2688 so that gs / 2688 stands for ws2.
-// Both planes are read and written exactly once; no dense intermediate.
-__global__ void __launch_bounds__(kStreamThreads)
-transcode_kernel(const uint8_t* __restrict__ mo_w, int64_t w_bytes, const uint8_t* __restrict__ mo_ws,
-                 int64_t s_bytes, const float* __restrict__ ws2, uint8_t* __restrict__ w_out,
-                 uint8_t* __restrict__ s_out, float* __restrict__ gs_out) {
-  const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-  if (tid == 0) gs_out[0] = __fmul_rn(__ldg(ws2), kGlobalScaleDivisor);
-  const int64_t wv = w_bytes >> 4, sv = s_bytes >> 4;
-  // Main body: 16-byte chunks of the weight plane then the scale plane;
-  // kU independent loads in flight per thread.
-  constexpr int kU = 8;
-  const uint4* wi = reinterpret_cast<const uint4*>(mo_w);
-  uint4* wo = reinterpret_cast<uint4*>(w_out);
-  int64_t i = tid;
-  for (; i + (kU - 1) * stride < wv; i += kU * stride) {
-    uint4 v[kU];
-#pragma unroll
-    for (int u = 0; u < kU; ++u) v[u] = ld_stream_v4(wi + i + u * stride);
-#pragma unroll
-    for (int u = 0; u < kU; ++u) __stcs(wo + i + u * stride, v[u]);
-  }
-  for (; i < wv; i += stride) __stcs(wo + i, ld_stream_v4(wi + i));
-  const uint4* si = reinterpret_cast<const uint4*>(mo_ws);
-  uint4* so = reinterpret_cast<uint4*>(s_out);
-  for (int64_t j = tid; j < sv; j += stride) __stcs(so + j, ld_stream_v4(si + j));
-  // Byte tails (fewer than 16 bytes each).
-  const int64_t wt = w_bytes - (wv << 4), st = s_bytes - (sv << 4);
-  if (tid < wt) w_out[(wv << 4) + tid] = mo_w[(wv << 4) + tid];
-  if (tid < st) s_out[(sv << 4) + tid] = mo_ws[(sv << 4) + tid];
-}
-
-// The same transcode moved by the copy engine: each CTA (one per SM, one
-// thread issuing) copies a contiguous run of 32 KB chunks of both planes
-// through a ring of six shared-memory buffers, bulk loads running up to six
-// chunks ahead of the bulk stores. The copy engine then keeps the read and
-// write streams going with a handful of instructions per 32 KB instead of
-// one load and one store per 16 bytes and thread. Sizes and addresses of
-// bulk copies must be multiples of 16 bytes: the last (< 16) bytes of each
-// plane are copied by plain stores.
+// repack is the identity on the byte stream, so the kernel copies both planes
+// as they are; the E4M3 block scales are kept byte for byte and the sidecar is
+// f32(ws2) * 2688 so that gs / 2688 stands for ws2. Both planes are read and
+// written exactly once; no dense intermediate.
+//
+// The copy engine moves the bytes: each CTA (one per SM, one thread issuing)
+// copies a contiguous run of 32 KB chunks of both planes through a ring of
+// six shared-memory buffers, bulk loads running up to six chunks ahead of the
+// bulk stores, a handful of instructions per 32 KB (a 16-byte vector copy
+// with eight loads in flight per thread took 80 us for a layer's three
+// triplets, this one 75). Sizes and addresses of bulk copies must be
+// multiples of 16 bytes: the last (< 16) bytes of each plane are copied by
+// plain stores.
 constexpr uint32_t kCopyChunk = 32 * 1024;
 constexpr int kCopyBufs = 6;
 
@@ -591,21 +561,14 @@ transcode_folded_kernel(const uint8_t* __restrict__ mo_w, int64_t w_bytes, const
 cudaError_t launch_transcode(const uint8_t* mo_w, int64_t w_bytes, const uint8_t* mo_ws, int64_t s_bytes,
                              const float* ws2, uint32_t* w_out, uint8_t* s_out, float* gs_out,
                              cudaStream_t st) {
-  const char* ev = std::getenv("NVFP4_TRANSCODE_BULK");
-  if (!(ev && ev[0] == '0')) {
-    int dev = 0, sms = 152;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    const size_t smem = (size_t)kCopyBufs * kCopyChunk;
-    cudaError_t e = cudaFuncSetAttribute(transcode_bulk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    transcode_bulk_kernel<<<sms, 32, smem, st>>>(mo_w, w_bytes, mo_ws, s_bytes, ws2,
-                                                reinterpret_cast<uint8_t*>(w_out), s_out, gs_out);
-    return cudaGetLastError();
-  }
-  const int64_t units = (w_bytes >> 4) / 8 + 16;
-  transcode_kernel<<<stream_grid(transcode_kernel, units), kStreamThreads, 0, st>>>(
-      mo_w, w_bytes, mo_ws, s_bytes, ws2, reinterpret_cast<uint8_t*>(w_out), s_out, gs_out);
+  int dev = 0, sms = 152;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const size_t smem = (size_t)kCopyBufs * kCopyChunk;
+  cudaError_t e = cudaFuncSetAttribute(transcode_bulk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  transcode_bulk_kernel<<<sms, 32, smem, st>>>(mo_w, w_bytes, mo_ws, s_bytes, ws2, reinterpret_cast<uint8_t*>(w_out),
+                                              s_out, gs_out);
   return cudaGetLastError();
 }
 

@@ -95,3 +95,17 @@ def zipf_experts(g: np.random.Generator, rows: int, experts: int, a: float = 1.1
     p = (np.arange(experts, dtype=np.float64) + 1.0) ** -a
     p /= p.sum()
     return g.choice(experts, size=rows, p=p).astype(np.uint32)
+
+
+def device_modelopt_triplet(seed: int, n: int, k: int, device, lo: float = 2.0**-6, hi: float = 4.0):
+    """The ModelOpt triplet of :func:`modelopt_triplet`, drawn on the device
+    (for planes too large to draw on the host quickly): weight bytes uniform
+    over 0..255 and weight_scale the E4M3 (round to nearest even) of
+    2**U(log2 lo, log2 hi), from a torch generator seeded with `seed`;
+    weight_scale_2 U(1e-4, 1e-2) from rng(seed)."""
+    gen = torch.Generator(device=device).manual_seed(seed)
+    weight = torch.randint(0, 256, (n, k // 2), dtype=torch.uint8, device=device, generator=gen)
+    e = torch.rand((n, k // 16), device=device, generator=gen) * (np.log2(hi) - np.log2(lo)) + np.log2(lo)
+    scale = torch.exp2(e).to(torch.float8_e4m3fn).view(torch.uint8)
+    ws2 = np.float32(rng(seed).uniform(1e-4, 1e-2))
+    return weight, scale, ws2

@@ -8,3 +8,24 @@ if ROOT not in sys.path:
 
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (GB300, sm_103a)")
+
+
+import pytest
+
+
+@pytest.fixture
+def opt():
+    """Sets library options (nvfp4_set_option) for one test and puts back the
+    previous values afterwards."""
+    from nvfp4_quantized_matmul_gb300 import binding
+
+    saved = {}
+
+    def set_(name, value):
+        if name not in saved:
+            saved[name] = binding.get_option(name)
+        binding.set_option(name, value)
+
+    yield set_
+    for name, value in saved.items():
+        binding.set_option(name, value)

@@ -117,7 +117,7 @@ def test_group_route_no_valid_rows(nv):
     assert np.all(yc == 0.0) and not np.any(np.signbit(yc))
 
 
-def test_group_route_matches_row_route(nv, monkeypatch):
+def test_group_route_matches_row_route(nv, opt):
     """The expert-group and the per-row decode kernels compute the same sums."""
     E, N, K, R, B = 32, 1536, 2048, 64, 64
     w, s = weights(8, E, N, K)
@@ -127,7 +127,7 @@ def test_group_route_matches_row_route(nv, monkeypatch):
     gs = f32_to_dev(synth.global_scales(g, E))
     args = (x, u32_to_dev(w), u8_to_dev(s), u32_to_dev(rhs), u32_to_dev(lhs))
     a = nv.gather_qmm(*args, gs=gs).float()
-    monkeypatch.setenv("NVFP4_QMV_GROUP", "0")
+    opt("gather_group", 0)
     b = nv.gather_qmm(*args, gs=gs).float()
     torch.cuda.synchronize()
     scale = b.abs().max().item()

@@ -82,9 +82,7 @@ def test_dequantize_guard_bands(nv):
 # than the bulk copy's ring of six); (3, 16) and (1, 48): planes shorter than
 # a 16-byte unit at their end.
 @pytest.mark.parametrize("nk", [(3, 16), (272, 256), (33, 5376), (1, 48), (43008, 5376)])
-@pytest.mark.parametrize("path", ["bulk", "vector"])
-def test_transcode_bit_exact(nv, nk, path, monkeypatch):
-    monkeypatch.setenv("NVFP4_TRANSCODE_BULK", "1" if path == "bulk" else "0")
+def test_transcode_bit_exact(nv, nk):
     N, K = nk
     g = synth.rng(N * 7 + K)
     mo_w, mo_ws, ws2 = synth.modelopt_triplet(g, N, K)
@@ -213,9 +211,9 @@ TC_SHAPES = [(1, 256, 64), (100, 272, 96), (128, 512, 256), (129, 40, 64), (300,
 @pytest.mark.parametrize("tile", ["auto", "256x256", "256x128", "128x256"])
 @pytest.mark.parametrize("mnk", TC_SHAPES, ids=lambda v: "M%d_N%d_K%d" % v)
 @pytest.mark.parametrize("dt", ["f16", "bf16"])
-def test_qmm_tc_route(nv, mnk, dt, tile, monkeypatch):
+def test_qmm_tc_route(nv, mnk, dt, tile, opt):
     if tile != "auto":
-        monkeypatch.setenv("NVFP4_TC_TILE", tile)
+        opt("tc_tile", tile)
     M, N, K = mnk
     w, s = weights(M + 7 * N + K, N, K, lo=2.0**-4, hi=16.0)
     g = synth.rng(M * 77 + N + K)
@@ -382,13 +380,11 @@ GATHER_TC_CASES = [(16, 272, 96, 300, 4), (8, 1024, 64, 4096, 4), (128, 256, 256
 @pytest.mark.parametrize("case", GATHER_TC_CASES, ids=lambda v: "E%d_N%d_K%d_T%d_k%d" % v)
 @pytest.mark.parametrize("dt", ["f16", "bf16"])
 @pytest.mark.parametrize("tile", ["256x256", "128x256", "256x128"])
-@pytest.mark.parametrize("rows", ["gathered", "tma"])
-def test_gather_sorted_tc_route(nv, monkeypatch, case, dt, tile, rows):
-    """Every tile shape, with the activation rows gathered into output order
-    first (plain 128-row boxes) or fetched row by row (tile::gather4)."""
-    monkeypatch.setenv("NVFP4_GATHER_TC", "1")
-    monkeypatch.setenv("NVFP4_GATHER_TILE", tile)
-    monkeypatch.setenv("NVFP4_GATHER_ROWS", rows)
+def test_gather_sorted_tc_route(nv, opt, case, dt, tile):
+    """Every tile shape (the activation rows gathered into output order first,
+    then plain 128-row boxes)."""
+    opt("gather_tc", 1)
+    opt("gather_tile", tile)
     E, N, K, T, topk = case
     w, s = weights(7 * E + N, E, N, K)
     g = synth.rng(E + N + K + T)
@@ -415,9 +411,9 @@ def test_gather_sorted_tc_route(nv, monkeypatch, case, dt, tile, rows):
     assert guards_intact(backing, guard)
 
 
-def test_gather_sorted_tc_identity_lhs(nv, monkeypatch):
+def test_gather_sorted_tc_identity_lhs(nv, opt):
     """Without lhs, row r reads x[r]; rows at or past B are +0.0."""
-    monkeypatch.setenv("NVFP4_GATHER_TC", "1")
+    opt("gather_tc", 1)
     E, N, K, R = 32, 256, 128, 2048
     w, s = weights(81, E, N, K)
     g = synth.rng(82)
@@ -432,7 +428,7 @@ def test_gather_sorted_tc_identity_lhs(nv, monkeypatch):
     assert np.all(y[B:].float().cpu().numpy() == 0.0)
 
 
-def test_gather_sorted_tc_matches_decode_route(nv, monkeypatch):
+def test_gather_sorted_tc_matches_decode_route(nv, opt):
     """The expert-batched and the decode-shape gather compute the same sums."""
     E, N, K, T, topk = 64, 512, 512, 1024, 4
     w, s = weights(91, E, N, K)
@@ -440,21 +436,19 @@ def test_gather_sorted_tc_matches_decode_route(nv, monkeypatch):
     x = synth.activations(g, (T, K), "bf16").cuda()
     lhs, rhs = synth.zipf_routing(g, T, E, topk)
     args = (x, u32_to_dev(w), u8_to_dev(s), u32_to_dev(rhs), u32_to_dev(lhs))
-    monkeypatch.setenv("NVFP4_GATHER_TC", "1")
+    opt("gather_tc", 1)
     a = nv.gather_qmm(*args, sorted_indices=True).float()
-    monkeypatch.setenv("NVFP4_GATHER_TC", "0")
+    opt("gather_tc", 0)
     b = nv.gather_qmm(*args, sorted_indices=True).float()
     assert nv.take_device_error() == 0
     assert (a - b).abs().max().item() <= 2 * 2.0**-8 * b.abs().max().item()
 
 
-@pytest.mark.parametrize("rows", ["gathered", "tma"])
-def test_gather_sorted_tc_two_calls(nv, monkeypatch, rows):
+def test_gather_sorted_tc_two_calls(nv, opt):
     """About 160 expert tiles of 16 k-blocks on 152 CTAs (a second, partial
     wave), an activation index out of range inside a segment; every row
     against the oracle, twice in a row (the row buffer is reused)."""
-    monkeypatch.setenv("NVFP4_GATHER_TC", "1")
-    monkeypatch.setenv("NVFP4_GATHER_ROWS", rows)
+    opt("gather_tc", 1)
     E, N, K, T, topk = 16, 1024, 1024, 2048, 4
     w, s = weights(61, E, N, K)
     g = synth.rng(62)
@@ -499,10 +493,94 @@ def test_gather_sorted_tc_moe_prefill_full_size(nv):
     assert rel_err(y[torch.from_numpy(pick).cuda()], ref) <= TOL["bf16"]
 
 
-def test_gather_tc_unsorted_promise_is_memory_safe(nv, monkeypatch):
+def test_gather_sorted_tc_moe_down_prefill_full_size(nv):
+    """The MoE down prefill: the 32768 gate/up output rows (4096 tokens, top-8
+    Zipf(1.1) over 128 experts, sorted by expert) taken in order (identity
+    activation indices) through [128, 2048, 768]; sampled rows against the
+    oracle."""
+    E, N, K, T = 128, 2048, 768, 4096
+    g = synth.rng(4343)
+    w = synth.packed_weight(g, E, N, K)
+    s = synth.log_uniform_scales(g, (E, N, K // 16), 2.0**-6, 4.0)
+    gs = synth.global_scales(g, E)
+    _, rhs = synth.zipf_routing(g, T, E, 8)
+    x = synth.activations(g, (rhs.size, K), "bf16")
+    y = nv.gather_qmm(x.cuda(), u32_to_dev(w), u8_to_dev(s), u32_to_dev(rhs), None, gs=f32_to_dev(gs),
+                      sorted_indices=True)
+    torch.cuda.synchronize()
+    assert nv.take_device_error() == 0
+    starts = np.searchsorted(rhs, np.arange(E + 1))
+    pick = np.unique(np.concatenate([starts[:-1], np.maximum(starts[1:] - 1, 0),
+                                     g.choice(len(rhs), size=256, replace=False)]))
+    pick = pick[pick < len(rhs)]
+    ref = O.gather_qmm(x.double().numpy(), pick.astype(np.uint32), rhs[pick], w, s, gs)
+    assert rel_err(y[torch.from_numpy(pick).cuda()], ref) <= TOL["bf16"]
+
+
+# The prefill configuration at full size, through the automatic route (whole
+# tensor-core tiles: 17.7 and 4.4 waves of 256 x 256 tiles on 152 SMs):
+# M = 8192 and M = 2048 on [21504, 5376]; sampled outputs against the oracle.
+@pytest.mark.parametrize("mnk", [(8192, 21504, 5376), (2048, 21504, 5376)], ids=lambda v: "M%d_N%d_K%d" % v)
+def test_prefill_full_size_sampled(nv, mnk):
+    M, N, K = mnk
+    g = synth.rng(M + 2 * N)
+    w = synth.packed_weight(g, N, K)
+    s = synth.log_uniform_scales(g, (N, K // 16), 2.0**-6, 4.0)
+    gs = synth.global_scales(g, 1)[0]
+    x = synth.activations(g, (M, K), "bf16")
+    y = nv.qmm(x.cuda(), u32_to_dev(w), u8_to_dev(s), gs=float(gs))
+    torch.cuda.synchronize()
+    assert nv.take_device_error() == 0
+    yc = y.double().cpu().numpy()
+    assert np.isfinite(yc).all()
+    pick = synth.rng(N + M + 3)
+    rows = np.concatenate([pick.integers(0, M, size=700), np.arange(M - 10, M), np.zeros(10, dtype=np.int64)])
+    cols = np.concatenate([pick.integers(0, N, size=700), np.arange(N - 10, N), np.arange(10)])
+    ref = O.qmm_entries(x.double().numpy(), w, s, gs, rows, cols)
+    assert np.max(np.abs(yc[rows, cols] - ref)) <= TOL["bf16"] * np.max(np.abs(ref))
+
+
+def test_transcode_sixty_layers(nv):
+    """The 60-layer transcode workload: every layer's three ModelOpt triplets
+    ([43008, 5376], [5376, 21504], [8192, 5376]; 13.2 GB in all) resident on
+    the device and transcoded in one pass; then, layer by layer, each native
+    plane and sidecar compared bit for bit with the oracle's transcode of the
+    same input bytes, and the first 64 rows of each plane dequantized (bf16)
+    bit for bit against the oracle."""
+    dev = torch.device("cuda")
+    lin = [(43008, 5376), (5376, 21504), (8192, 5376)]
+    layers = []
+    for layer in range(60):
+        trip = []
+        for j, (n, k) in enumerate(lin):
+            mo_w, mo_s, ws2 = synth.device_modelopt_triplet(5000 + 3 * layer + j, n, k, dev)
+            out = (torch.empty((n, k // 8), dtype=torch.int32, device=dev),
+                   torch.empty((n, k // 16), dtype=torch.uint8, device=dev),
+                   torch.empty((1,), dtype=torch.float32, device=dev))
+            trip.append((mo_w, mo_s, ws2, f32_to_dev(ws2), out))
+        layers.append(trip)
+    for trip in layers:
+        for (mo_w, mo_s, _, ws2_d, out) in trip:
+            nv.transcode(mo_w, mo_s, ws2_d, out=out)
+    torch.cuda.synchronize()
+    assert nv.take_device_error() == 0
+    for layer, trip in enumerate(layers):
+        for j, (mo_w, mo_s, ws2, _, out) in enumerate(trip):
+            hw, hs = mo_w.cpu().numpy(), mo_s.cpu().numpy()
+            rw, rs, rg = O.transcode(hw, hs, ws2)
+            assert np.array_equal(out[0].cpu().numpy().view(np.uint32), rw), (layer, j)
+            assert np.array_equal(out[1].cpu().numpy(), rs), (layer, j)
+            assert out[2].cpu().numpy()[0] == rg, (layer, j)
+            deq = nv.dequantize(out[0][:64], out[1][:64], out[2], torch.bfloat16)
+            ref = O.dequantize(rw[:64], rs[:64], rg, "bf16")
+            assert torch.equal(deq.cpu().view(torch.int16), ref.view(torch.int16)), (layer, j)
+        layers[layer] = None  # frees the layer's device planes
+
+
+def test_gather_tc_unsorted_promise_is_memory_safe(nv, opt):
     """Indices that break the sorted promise still write every row once and
     read nothing out of range (values are then unspecified)."""
-    monkeypatch.setenv("NVFP4_GATHER_TC", "1")
+    opt("gather_tc", 1)
     E, N, K, T = 8, 256, 64, 600
     w, s = weights(95, E, N, K)
     g = synth.rng(96)

@@ -63,14 +63,14 @@ def test_batched_parity(nv, case, dt, with_gs):
         assert guards_intact(backing, guard)
 
 
-def test_batched_group_launch_matches_per_batch_calls(nv, monkeypatch):
+def test_batched_group_launch_matches_per_batch_calls(nv, opt):
     """The one-launch route and one call per batch compute the same sums."""
     bt, M, N, K = 16, 2, 2048, 768
     w, s = weights(5, bt, N, K)
     x = synth.activations(synth.rng(6), (bt * M, K), "bf16").reshape(bt, M, K).cuda()
     args = (x, u32_to_dev(w), u8_to_dev(s))
     a = nv.qmm_batched(*args).float()
-    monkeypatch.setenv("NVFP4_QMV_GROUP", "0")
+    opt("gather_group", 0)
     b = nv.qmm_batched(*args).float()
     torch.cuda.synchronize()
     assert (a - b).abs().max().item() <= 2 * 2.0**-8 * b.abs().max().item()

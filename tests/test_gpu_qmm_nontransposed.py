@@ -46,12 +46,12 @@ NT_SHAPES = [(1, 17, 32), (3, 64, 272), (130, 100, 512), (257, 300, 1008), (600,
 @pytest.mark.parametrize("dt", ["f16", "bf16"])
 @pytest.mark.parametrize("with_gs", [False, True])
 @pytest.mark.parametrize("split", ["1", "0"], ids=["streamk", "whole_tiles"])
-def test_nontransposed_parity(nv, monkeypatch, mkn, dt, with_gs, split):
+def test_nontransposed_parity(nv, opt, mkn, dt, with_gs, split):
     # the tensor-core route for every M here (the decode route has its own
     # tests below); below two waves of tiles the k-blocks are split over the
-    # CTAs unless NVFP4_TC_STREAMK=0 deals whole tiles
-    monkeypatch.setenv("NVFP4_NT_DECODE", "0")
-    monkeypatch.setenv("NVFP4_TC_STREAMK", split)
+    # CTAs unless the stream-K option is off (whole tiles)
+    opt("nt_decode", 0)
+    opt("tc_streamk", int(split))
     M, K, N = mkn
     w, s = weights(M + 7 * K + N, K, N)  # [K, N/8] words, [K, N/16] scales
     g = synth.rng(3 * M + K + 5 * N)
@@ -153,14 +153,14 @@ def test_nontransposed_decode_route(nv, mkn, dt, with_gs):
         assert guards_intact(backing, guard)
 
 
-def test_nontransposed_decode_routes_agree(nv, monkeypatch):
+def test_nontransposed_decode_routes_agree(nv, opt):
     """The streaming route and the tensor cores compute the same sums."""
     M, K, N = 2, 2048, 4096
     w, s = weights(123, K, N)
     x = synth.activations(synth.rng(124), (M, K), "bf16").cuda()
     dw, ds = u32_to_dev(w), u8_to_dev(s)
     a = nv.qmm_nontransposed(x, dw, ds).float()
-    monkeypatch.setenv("NVFP4_NT_DECODE", "0")
+    opt("nt_decode", 0)
     b = nv.qmm_nontransposed(x, dw, ds).float()
     torch.cuda.synchronize()
     assert nv.take_device_error() == 0

@@ -45,8 +45,8 @@ SK_SHAPES = [(512, 2048, 2048), (300, 1000, 1536), (2048, 5376, 2048), (4096, 81
 @pytest.mark.parametrize("mnk", SK_SHAPES, ids=lambda v: "M%d_N%d_K%d" % v)
 @pytest.mark.parametrize("tile", ["256x256", "256x128", "128x256"])
 @pytest.mark.parametrize("dt", ["f16", "bf16"])
-def test_stream_k_parity(nv, monkeypatch, mnk, tile, dt):
-    monkeypatch.setenv("NVFP4_TC_TILE", tile)
+def test_stream_k_parity(nv, opt, mnk, tile, dt):
+    opt("tc_tile", tile)
     M, N, K = mnk
     w, s = weights(M + 3 * N + K, N, K)
     g = synth.rng(M + 5 * N + K)
@@ -64,7 +64,7 @@ def test_stream_k_parity(nv, monkeypatch, mnk, tile, dt):
         assert guards_intact(backing, guard)
 
 
-def test_stream_k_matches_round_robin(nv, monkeypatch):
+def test_stream_k_matches_round_robin(nv, opt):
     """Stream-K and whole-tile scheduling compute the same sums (only the
     order of the f32 additions of split tiles differs)."""
     M, N, K = 2048, 5376, 2048
@@ -72,7 +72,7 @@ def test_stream_k_matches_round_robin(nv, monkeypatch):
     x = synth.activations(synth.rng(13), (M, K), "bf16").cuda()
     dw, ds = u32_to_dev(w), u8_to_dev(s)
     a = nv.qmm(x, dw, ds, route="tc").float()
-    monkeypatch.setenv("NVFP4_TC_STREAMK", "0")
+    opt("tc_streamk", 0)
     b = nv.qmm(x, dw, ds, route="tc").float()
     torch.cuda.synchronize()
     assert nv.take_device_error() == 0

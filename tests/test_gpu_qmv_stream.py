@@ -57,9 +57,10 @@ def test_stream_route_parity(nv, nk, M, dt):
 
 
 @pytest.mark.parametrize("M", [3, 16])
-def test_stream_route_two_row_tiles_per_warp(nv, monkeypatch, M):
-    """NVFP4_QMV_RT=2 selects eight consumer warps of 32 weight rows each."""
-    monkeypatch.setenv("NVFP4_QMV_RT", "2")
+def test_stream_route_two_row_tiles_per_warp(nv, opt, M):
+    """Two row tiles per consumer warp: eight consumer warps of 32 weight rows
+    each."""
+    opt("qmv_row_tiles", 2)
     N, K = 1000, 4096
     w, s = weights(5 + M, N, K)
     x = synth.activations(synth.rng(M), (M, K), "bf16").cuda()
@@ -130,15 +131,14 @@ def test_stream_route_graph_replay(nv, capture):
         nv.set_launch_overlap(prev)
 
 
-def test_stream_route_matches_cluster_route(nv, monkeypatch):
-    """The persistent route and the cluster-split route compute the same sums."""
+def test_stream_route_matches_tensor_core_route(nv):
+    """The decode route and the tensor-core route compute the same sums."""
     N, K, M = 3000, 5376, 8
     w, s = weights(88, N, K)
     x = synth.activations(synth.rng(89), (M, K), "bf16").cuda()
     dw, ds = u32_to_dev(w), u8_to_dev(s)
     a = nv.qmm(x, dw, ds, route="qmv").float()
-    monkeypatch.setenv("NVFP4_QMV_STREAM", "0")
-    b = nv.qmm(x, dw, ds, route="qmv").float()
+    b = nv.qmm(x, dw, ds, route="tc").float()
     assert nv.take_device_error() == 0
     assert (a - b).abs().max().item() <= 2 * 2.0**-8 * b.abs().max().item()
 

@@ -231,23 +231,22 @@ def test_crossover_env_override(nv, monkeypatch):
     assert nv.library().nvfp4_qmm_crossover(2, 21504, 5376) == 96
 
 
-def test_crossover_model(nv, monkeypatch):
+def test_crossover_model(nv, monkeypatch, opt):
     """The default crossover follows the route sweep on GB300: gate/up and
     down switch to the tensor cores at 48 token rows (two 16-row decode
     launches still beat them at 32), qkv at 32; f32 never. Without the
     stream-K split the tensor-core route is slower at small M and down (21
     weight tiles for 152 SMs) switches only at 112."""
     monkeypatch.delenv("NVFP4_QMM_CROSSOVER", raising=False)
-    monkeypatch.delenv("NVFP4_TC_STREAMK", raising=False)
     lib = nv.library()
     assert lib.nvfp4_qmm_crossover(2, 43008, 5376) == 48
     assert lib.nvfp4_qmm_crossover(2, 8192, 5376) == 32
     assert lib.nvfp4_qmm_crossover(2, 5376, 21504) == 48
-    monkeypatch.setenv("NVFP4_TC_STREAMK", "0")
+    opt("tc_streamk", 0)
     assert lib.nvfp4_qmm_crossover(2, 43008, 5376) == 48
     assert lib.nvfp4_qmm_crossover(2, 8192, 5376) == 48
     assert lib.nvfp4_qmm_crossover(2, 5376, 21504) == 112
-    monkeypatch.delenv("NVFP4_TC_STREAMK", raising=False)
+    opt("tc_streamk", 1)
     assert lib.nvfp4_qmm_crossover(1, 43008, 5376) == 48
     assert lib.nvfp4_qmm_crossover(0, 43008, 5376) > 2**62
     for n, k in ((256, 256), (1 << 20, 64), (64, 1 << 20)):
@@ -307,3 +306,16 @@ def test_qmm_sequence_refusals_of_the_whole(nv):
     empty = seq_calls(nv, 2, M=0)
     empty[0] = nv.QmmCall(A, 4, 256, 0, A, 0, A, 0, None, 0, A, 0, 0)
     assert lib.nvfp4_qmm_sequence(ctypes.addressof(empty), 2, 2, None) == 0
+
+
+def test_options_set_get_and_refusals(nv, opt):
+    lib = nv.library()
+    assert nv.get_option("tc_streamk") == 1 and nv.get_option("gather_tc") == -1
+    opt("tc_tile", "256x128")
+    assert nv.get_option("tc_tile") == 2
+    assert nv.STATUS[lib.nvfp4_set_option(1, 4)] == "ERR_LIMIT"      # tile code out of range
+    assert nv.get_option("tc_tile") == 2                              # unchanged
+    assert nv.STATUS[lib.nvfp4_set_option(6, -2)] == "ERR_LIMIT"
+    assert nv.STATUS[lib.nvfp4_set_option(0, 0)] == "ERR_DTYPE"       # unknown option
+    assert nv.STATUS[lib.nvfp4_set_option(99, 0)] == "ERR_DTYPE"
+    assert lib.nvfp4_get_option(99) == -2**31
