@@ -361,8 +361,15 @@ typedef enum {
   NVFP4_OPT_GATHER_GROUP = 5,   /* 1 (default): decode-shape gathers grouped by expert; 0: the per-row kernel */
   NVFP4_OPT_GATHER_TC = 6,      /* -1 automatic (default); 1: sorted gathers take the expert-batched
                                    tensor-core route wherever supported; 0: never */
-  NVFP4_OPT_GATHER_TILE = 7     /* expert-batched route's tile: 0 automatic (default, 256x256), 1 256x256,
+  NVFP4_OPT_GATHER_TILE = 7,    /* expert-batched route's tile: 0 automatic (default, 256x256), 1 256x256,
                                    2 256x128, 3 128x256 */
+  NVFP4_OPT_WAIT_LIMIT_US = 8,  /* decode-route calls of nvfp4_qmm: limit of each bounded wait in
+                                   microseconds, 0 (default) for 2 s; for tests of the stall path */
+  NVFP4_OPT_TEST_WITHHOLD = 9   /* tests of the stall path only: 1 makes the first CTA of the next
+                                   decode-route nvfp4_qmm launches withhold the release of one
+                                   pipeline stage, so that a bounded wait runs out (the call then
+                                   reports its error code through nvfp4_take_device_error and
+                                   leaves no copy in flight); 0 (default) off */
 } nvfp4_option;
 
 /* Sets an option: NVFP4_ERR_DTYPE for an unknown option, NVFP4_ERR_LIMIT

@@ -336,7 +336,7 @@ def set_launch_overlap(enable):
 
 
 OPTION_CODE = {"tc_tile": 1, "tc_streamk": 2, "nt_decode": 3, "qmv_row_tiles": 4, "gather_group": 5,
-               "gather_tc": 6, "gather_tile": 7}
+               "gather_tc": 6, "gather_tile": 7, "wait_limit_us": 8, "test_withhold": 9}
 TILE_CODE = {"auto": 0, "256x256": 1, "256x128": 2, "128x256": 3}
 
 

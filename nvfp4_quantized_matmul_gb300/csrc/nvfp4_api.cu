@@ -136,9 +136,9 @@ bool launch_overlap() { return g_launch_overlap.load(std::memory_order_relaxed) 
 
 namespace {
 // Index: nvfp4_option value (0 unused). Defaults: automatic choices.
-std::atomic<int> g_options[kOptEnd] = {0, 0, 1, 1, 0, 1, -1, 0};
-constexpr int kOptMin[kOptEnd] = {0, 0, 0, 0, 0, 0, -1, 0};
-constexpr int kOptMax[kOptEnd] = {0, 3, 1, 1, 2, 1, 1, 3};
+std::atomic<int> g_options[kOptEnd] = {0, 0, 1, 1, 0, 1, -1, 0, 0, 0};
+constexpr int kOptMin[kOptEnd] = {0, 0, 0, 0, 0, 0, -1, 0, 0, 0};
+constexpr int kOptMax[kOptEnd] = {0, 3, 1, 1, 2, 1, 1, 3, 2000000, 1};
 }  // namespace
 
 int option(int opt) { return g_options[opt].load(std::memory_order_relaxed); }

@@ -98,7 +98,9 @@ enum Option : int {
   kOptGatherGroup = 5,
   kOptGatherTc = 6,
   kOptGatherTile = 7,
-  kOptEnd = 8
+  kOptWaitLimitUs = 8,
+  kOptTestWithhold = 9,
+  kOptEnd = 10
 };
 int option(int opt);
 

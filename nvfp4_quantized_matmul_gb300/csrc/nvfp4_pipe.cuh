@@ -52,14 +52,15 @@ __device__ __forceinline__ uint64_t gtimer() {
 
 // Bounded wait by one thread; false once the limit passes (abort flag set,
 // `code` recorded in *err) or another warp has aborted.
-__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag, int code, int* err) {
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag, int code, int* err,
+                                         uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try(bar, parity)) return true;
   const uint64_t t0 = gtimer();
   for (uint32_t n = 1;; ++n) {
     if (mbar_try(bar, parity)) return true;
     if ((n & 63) == 0) {
       if (*abort_flag) return false;
-      if (gtimer() - t0 > kWaitLimitNs) {
+      if (gtimer() - t0 > limit_ns) {
         *abort_flag = 1;
         atomicCAS(err, 0, code);
         return false;
@@ -71,13 +72,13 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
 // Bounded wait by all 32 lanes of a warp together: every lane polls (so each
 // has acquired the phase) and the decision to stop is taken warp-wide.
 __device__ __forceinline__ bool wait_bar_warp(uint32_t bar, uint32_t parity, volatile int* abort_flag, int code,
-                                              int* err) {
+                                              int* err, uint64_t limit_ns = kWaitLimitNs) {
   if (__all_sync(0xffffffffu, mbar_try(bar, parity))) return true;
   const uint64_t t0 = gtimer();
   for (uint32_t n = 1;; ++n) {
     if (__all_sync(0xffffffffu, mbar_try(bar, parity))) return true;
     if ((n & 63) == 0) {
-      const bool stop = __any_sync(0xffffffffu, *abort_flag != 0 || gtimer() - t0 > kWaitLimitNs);
+      const bool stop = __any_sync(0xffffffffu, *abort_flag != 0 || gtimer() - t0 > limit_ns);
       if (stop) {
         if ((threadIdx.x & 31) == 0) {
           if (!*abort_flag) atomicCAS(err, 0, code);

@@ -95,6 +95,12 @@ struct SPlan {
   // glu_cols-wide output columns. glu_act: 1 SiLU, 2 GELU (tanh form).
   int64_t glu_cols;
   int glu_act;
+  // Limit of every bounded wait of the launch (2 s unless a test shortens
+  // it), and, for tests of that limit only, a flag that makes consumer warp 0
+  // of CTA 0 withhold its release of its first stage, so that the producer's
+  // wait for that stage runs out.
+  uint64_t wait_ns;
+  int withhold;
 };
 
 struct Seg {
@@ -354,7 +360,7 @@ __device__ bool produce(const SPlan& p, int grp, Work wk, const CUtensorMap* wma
     const int up_row = (int)(p.glu_cols + row);
     if (pos.block_start(ac)) {
       const uint32_t b = su & 1u, bph = (su >> 1) & 1u;
-      if (!wait_bar(bar.sempty(b), bph ^ 1u, abort_flag, 21, &g_stream_error)) return false;
+      if (!wait_bar(bar.sempty(b), bph ^ 1u, abort_flag, 21, &g_stream_error, p.wait_ns)) return false;
       ++su;
       mbar_arrive_tx(bar.sfull(b), kSBox);
       if (kGlu) {
@@ -365,7 +371,7 @@ __device__ bool produce(const SPlan& p, int grp, Work wk, const CUtensorMap* wma
       else
         tma_load_2d(sst + b * kSBox, smap, (ac / kSChunks) * (kSChunks * 16), row, bar.sfull(b));
     }
-    if (!wait_bar(bar.empty(s), ph ^ 1u, abort_flag, 22, &g_stream_error)) return false;
+    if (!wait_bar(bar.empty(s), ph ^ 1u, abort_flag, 22, &g_stream_error, p.wait_ns)) return false;
     ++u;
     mbar_arrive_tx(bar.full(s), kWBox);
     if (kGlu) {
@@ -488,6 +494,7 @@ __device__ void consume(const SPlan& p, int grp, Work wk, XRun run, uint32_t wst
   constexpr int NA = NAccS<MT, RT>::value;
   float acc[NA][RT][MT][4];
   uint32_t &s = cst.s, &ph = cst.ph, &su = cst.su, &pc = cst.pc;
+  bool hold = p.withhold && blockIdx.x == 0 && warp == 0;  // tests of the bounded waits only
   Seg sg;
   while (wk.next(sg)) {
 #pragma unroll
@@ -511,8 +518,8 @@ __device__ void consume(const SPlan& p, int grp, Work wk, XRun run, uint32_t wst
       const bool first_of_block = c == sg.c0 || kb == 0;
       const bool last_of_block = c + 1 == sg.c1 || kb == kSChunks - 1;
       if (last_of_block) ++su;
-      if (first_of_block && !wait_bar_warp(bar.sfull(sb), sph, abort_flag, 23, &g_stream_error)) continue;
-      if (!wait_bar_warp(bar.full(cs), cph, abort_flag, 24, &g_stream_error)) continue;
+      if (first_of_block && !wait_bar_warp(bar.sfull(sb), sph, abort_flag, 23, &g_stream_error, p.wait_ns)) continue;
+      if (!wait_bar_warp(bar.full(cs), cph, abort_flag, 24, &g_stream_error, p.wait_ns)) continue;
       const uint32_t w = wst + cs * kWBox, q = sst + sb * kSBox;
       Chunk chk[RT];
       uint32_t qa[RT], qb[RT];
@@ -564,14 +571,15 @@ __device__ void consume(const SPlan& p, int grp, Work wk, XRun run, uint32_t wst
       }
       __syncwarp();
       if (lane == 0) {
-        mbar_arrive_relaxed(bar.empty(cs));
+        if (!hold) mbar_arrive_relaxed(bar.empty(cs));
         if (last_of_block) mbar_arrive_relaxed(bar.sempty(sb));
       }
+      hold = false;
     }
     // hand the segment's sums to the epilogue warp
     const uint32_t b = pc & 1u, bph = (pc >> 1) & 1u;
     ++pc;
-    if (!wait_bar_warp(bar.pempty(b), bph ^ 1u, abort_flag, 25, &g_stream_error)) continue;
+    if (!wait_bar_warp(bar.pempty(b), bph ^ 1u, abort_flag, 25, &g_stream_error, p.wait_ns)) continue;
     const uint32_t pb = pbuf + b * pbuf_bytes;
 #pragma unroll
     for (int rt = 0; rt < RT; ++rt)
@@ -669,7 +677,7 @@ __device__ void finish(const QmvArgs& a, const SPlan& p, Work wk, uint32_t pbuf,
   while (wk.next(sg)) {
     const uint32_t b = pc & 1u, bph = (pc >> 1) & 1u;
     ++pc;
-    if (!wait_bar_warp(bar.pfull(b), bph, abort_flag, 26, &g_stream_error)) break;
+    if (!wait_bar_warp(bar.pfull(b), bph, abort_flag, 26, &g_stream_error, p.wait_ns)) break;
     const uint32_t pb = pbuf + b * pbuf_bytes;
     const int64_t n0 = sg.r * (kGlu ? kTileRows / 2 : kTileRows);
     const int64_t ncols = kGlu ? p.glu_cols : a.N;  // output columns
@@ -701,7 +709,7 @@ __device__ void finish(const QmvArgs& a, const SPlan& p, Work wk, uint32_t pbuf,
           mbar_arrive_tx(bar.back(), tile_bytes);
           bulk_g2s(pb, blk, tile_bytes, bar.back());
         }
-        const bool ok = wait_bar_warp(bar.back(), bc & 1u, abort_flag, 27, &g_stream_error);
+        const bool ok = wait_bar_warp(bar.back(), bc & 1u, abort_flag, 27, &g_stream_error, p.wait_ns);
         ++bc;
         if (!ok) {
           wait_bar_quiet(bar.back(), (bc - 1) & 1u);  // the copies must land before the CTA leaves
@@ -1419,6 +1427,8 @@ cudaError_t stream_plan(const QmvArgs& a, int xdt, int dev, SPlan* out) {
   p.glu_cols = a.glu_cols;
   p.glu_act = a.glu_act;
   if (!make_plan(p, sms_of(dev), max_dyn)) return cudaErrorInvalidConfiguration;
+  p.wait_ns = kWaitLimitNs;
+  p.withhold = 0;
   cache[key] = p;
   if (out) *out = p;
   return cudaSuccess;
@@ -1431,6 +1441,9 @@ cudaError_t launch_mt(const QmvArgs& a, int xdt, cudaStream_t st, const Ws* give
   if (e != cudaSuccess) return e;
   SPlan p{};
   if ((e = stream_plan<MT, RT, kGlu>(a, xdt, dev, &p)) != cudaSuccess) return e;
+  // tests of the bounded waits: a shorter limit, and a withheld stage release
+  if (const int us = option(kOptWaitLimitUs)) p.wait_ns = (uint64_t)us * 1000u;
+  p.withhold = option(kOptTestWithhold);
   Ws ws;
   if (given)
     ws = *given;
@@ -1498,6 +1511,8 @@ bool group_plan(const QmvArgs& a, int xdt, int dev, SPlan* out) {
   p.gs = 1;  // per group, set by each CTA
   p.xs_chunks = p.nc;
   p.xs_stride = p.nc * kChunkCols + 32;
+  p.wait_ns = kWaitLimitNs;
+  p.withhold = 0;
   for (int stages = kMaxStages; stages >= 3; --stages) {
     p.stages = stages;
     if ((int64_t)stream_smem_bytes(p) <= max_dyn) {
@@ -1682,6 +1697,8 @@ cudaError_t launch_qmv_seq(const QmvArgs* calls, const int* depends, int n, int 
     SeqCall& C = sa->call[c];
     C.a = calls[c];
     C.p = best[c];
+    C.p.wait_ns = kWaitLimitNs;
+    C.p.withhold = 0;
     C.ws_block = blocks;
     C.depends = c > 0 && depends[c] ? 1 : 0;
     blocks += C.p.nrt;
