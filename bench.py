@@ -48,7 +48,7 @@ METRIC = "qmv HBM GB/s & µs/call, qmm TFLOP/s; fraction of GB300 roofline (1 GP
 # DRAM bytes (read + write) of the decode kernel over one step, from an ncu
 # capture of `--case decode_step`; reported per launch, and only while the
 # kernel sources still hash to kernel_sha.
-TRAFFIC = {"kernel_sha": "ad82ae626227d1a3", "bytes_per_step": 1124401408}
+TRAFFIC = {"kernel_sha": "76df51d916a49058", "bytes_per_step": 1128138240}
 TRAFFIC_FILES = ("nvfp4_qmv_stream.cu", "nvfp4_qmv_common.cuh", "nvfp4_common.cuh", "nvfp4_pipe.cuh")
 
 
