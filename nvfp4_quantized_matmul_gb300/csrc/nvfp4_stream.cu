@@ -256,56 +256,50 @@ __device__ __forceinline__ uint32_t f32_to_e4m3_satfinite(float v) {
 // One 16-column block's inputs as raw 16-byte words (four for f32).
 template <typename T> struct Raw16 { uint4 q[sizeof(T) == 4 ? 4 : 2]; };
 
-// Cached loads: a warp's 16-byte loads each cover every other 16 (or 48)
-// bytes of its span, and the lines they bring into L1 serve the thread's
-// next load (with evict-first loads: 91.9 against 90.3 us on the bf16
-// gate/up plane, 172 against 167 with f32 input).
-template <typename T>
-__device__ __forceinline__ void load_raw16(const T* p, Raw16<T>& r) {
-#pragma unroll
-  for (int i = 0; i < (int)(sizeof(r.q) / sizeof(uint4)); ++i) r.q[i] = __ldg(reinterpret_cast<const uint4*>(p) + i);
-}
-
 __device__ __forceinline__ uint32_t u4get(const uint4& v, int i) { return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w; }
 
-// The block's sixteen values as eight f32 pairs (columns 2i, 2i + 1), and
-// max |x| over them. For 16-bit inputs the maximum is taken on the packed
-// halves (|x| by clearing the sign bits, then a packed max: exact), one
-// widening at the end.
-template <typename T> __device__ __forceinline__ float widen16(const Raw16<T>& r, float (&lo)[8], float (&hi)[8]);
-template <> __device__ __forceinline__ float widen16<float>(const Raw16<float>& r, float (&lo)[8], float (&hi)[8]) {
+// max |x| over a block. For 16-bit inputs the maximum is taken on the packed
+// halves: max.xorsign.abs gives max(|a|, |b|) (exact) with some sign, which
+// the next step ignores and the end clears; one widening at the end.
+template <typename T> __device__ __forceinline__ float amax16(const Raw16<T>& r);
+template <> __device__ __forceinline__ float amax16<float>(const Raw16<float>& r) {
   float am = 0.0f;
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    lo[i] = __uint_as_float(u4get(r.q[i >> 1], 2 * (i & 1)));
-    hi[i] = __uint_as_float(u4get(r.q[i >> 1], 2 * (i & 1) + 1));
-    am = fmaxf(am, fmaxf(fabsf(lo[i]), fabsf(hi[i])));
-  }
+  for (int i = 0; i < 16; ++i) am = fmaxf(am, fabsf(__uint_as_float(u4get(r.q[i >> 2], i & 3))));
   return am;
 }
-template <> __device__ __forceinline__ float widen16<__nv_bfloat16>(const Raw16<__nv_bfloat16>& r, float (&lo)[8],
-                                                                   float (&hi)[8]) {
+template <> __device__ __forceinline__ float amax16<__nv_bfloat16>(const Raw16<__nv_bfloat16>& r) {
   uint32_t m = 0;
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const uint32_t u = u4get(r.q[i >> 2], i & 3);
-    lo[i] = __uint_as_float(u << 16);
-    hi[i] = __uint_as_float(u & 0xFFFF0000u);
-    asm("max.bf16x2 %0, %0, %1;" : "+r"(m) : "r"(u & 0x7FFF7FFFu));
-  }
+  for (int i = 0; i < 8; ++i) asm("max.xorsign.abs.bf16x2 %0, %0, %1;" : "+r"(m) : "r"(u4get(r.q[i >> 2], i & 3)));
+  m &= 0x7FFF7FFFu;
   return fmaxf(__uint_as_float(m << 16), __uint_as_float(m & 0xFFFF0000u));
 }
-template <> __device__ __forceinline__ float widen16<__half>(const Raw16<__half>& r, float (&lo)[8], float (&hi)[8]) {
+template <> __device__ __forceinline__ float amax16<__half>(const Raw16<__half>& r) {
   uint32_t m = 0;
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const uint32_t u = u4get(r.q[i >> 2], i & 3);
-    lo[i] = __half2float(__ushort_as_half((unsigned short)(u & 0xFFFFu)));
-    hi[i] = __half2float(__ushort_as_half((unsigned short)(u >> 16)));
-    asm("max.f16x2 %0, %0, %1;" : "+r"(m) : "r"(u & 0x7FFF7FFFu));
-  }
+  for (int i = 0; i < 8; ++i) asm("max.xorsign.abs.f16x2 %0, %0, %1;" : "+r"(m) : "r"(u4get(r.q[i >> 2], i & 3)));
+  m &= 0x7FFF7FFFu;
   return fmaxf(__half2float(__ushort_as_half((unsigned short)(m & 0xFFFFu))),
                __half2float(__ushort_as_half((unsigned short)(m >> 16))));
+}
+
+// Columns 2i and 2i + 1 of a block as f32 (i = 0..7).
+template <typename T> __device__ __forceinline__ void pair_at(const Raw16<T>& r, int i, float& lo, float& hi);
+template <> __device__ __forceinline__ void pair_at<float>(const Raw16<float>& r, int i, float& lo, float& hi) {
+  lo = __uint_as_float(u4get(r.q[i >> 1], 2 * (i & 1)));
+  hi = __uint_as_float(u4get(r.q[i >> 1], 2 * (i & 1) + 1));
+}
+template <> __device__ __forceinline__ void pair_at<__nv_bfloat16>(const Raw16<__nv_bfloat16>& r, int i, float& lo,
+                                                                 float& hi) {
+  const uint32_t u = u4get(r.q[i >> 2], i & 3);
+  lo = __uint_as_float(u << 16);
+  hi = __uint_as_float(u & 0xFFFF0000u);
+}
+template <> __device__ __forceinline__ void pair_at<__half>(const Raw16<__half>& r, int i, float& lo, float& hi) {
+  const uint32_t u = u4get(r.q[i >> 2], i & 3);
+  lo = __half2float(__ushort_as_half((unsigned short)(u & 0xFFFFu)));
+  hi = __half2float(__ushort_as_half((unsigned short)(u >> 16)));
 }
 
 // (a, b) * (r, r), each product rounded to nearest (one packed multiply).
@@ -331,10 +325,12 @@ __device__ __forceinline__ uint32_t cvt_e2m1x8(const float* lo, const float* hi)
       : "f"(lo[0]), "f"(hi[0]), "f"(lo[1]), "f"(hi[1]), "f"(lo[2]), "f"(hi[2]), "f"(lo[3]), "f"(hi[3]));
   return r;
 }
-// +0 for every zero magnitude (a negative value that rounds to zero).
+// +0 for every zero magnitude (a negative value that rounds to zero): a
+// nibble keeps its sign bit only where its magnitude m is nonzero, i.e.
+// where m + 7 (at most 14: no carry between nibbles) reaches bit 3.
 __device__ __forceinline__ uint32_t plus_zero(uint32_t r) {
-  const uint32_t nz = (r | (r >> 1) | (r >> 2)) & 0x11111111u;
-  return (r & 0x77777777u) | (r & (nz << 3));
+  const uint32_t m = r & 0x77777777u;
+  return m | (r & (m + 0x77777777u) & 0x88888888u);
 }
 
 // Magnitude code of the E2M1 value nearest to the exact quotient a / d, for
@@ -357,24 +353,24 @@ __device__ __forceinline__ uint32_t e2m1_code_exact(float a, float d) {
   return c;
 }
 
-// Element e (0..15, a run-time index) of a block's raw 16-byte words, as
-// float.
-__device__ __forceinline__ uint32_t u4sel(const uint4& v, int i) {
-  const uint32_t a = (i & 1) ? v.y : v.x, b = (i & 1) ? v.w : v.z;
-  return (i & 2) ? b : a;
+// Element e of a block, read again from its copy in shared memory (at
+// address blk) as float: the fix-up paths below are rare, and keeping the
+// block's values in registers until then would cost registers everywhere.
+template <typename T> __device__ __forceinline__ float elem_at(uint32_t blk, int e);
+template <> __device__ __forceinline__ float elem_at<float>(uint32_t blk, int e) {
+  float v;
+  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(blk + 4u * (uint32_t)e));
+  return v;
 }
-template <typename T> __device__ __forceinline__ float raw_elem(const Raw16<T>& r, int e);
-template <> __device__ __forceinline__ float raw_elem<float>(const Raw16<float>& r, int e) {
-  const uint4 q = (e & 8) ? ((e & 4) ? r.q[3] : r.q[2]) : ((e & 4) ? r.q[1] : r.q[0]);
-  return __uint_as_float(u4sel(q, e & 3));
+template <> __device__ __forceinline__ float elem_at<__nv_bfloat16>(uint32_t blk, int e) {
+  unsigned short v;
+  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(blk + 2u * (uint32_t)e));
+  return __uint_as_float((uint32_t)v << 16);
 }
-template <> __device__ __forceinline__ float raw_elem<__nv_bfloat16>(const Raw16<__nv_bfloat16>& r, int e) {
-  const uint32_t u = u4sel((e & 8) ? r.q[1] : r.q[0], (e & 7) >> 1);
-  return __uint_as_float((e & 1) ? (u & 0xFFFF0000u) : (u << 16));
-}
-template <> __device__ __forceinline__ float raw_elem<__half>(const Raw16<__half>& r, int e) {
-  const uint32_t u = u4sel((e & 8) ? r.q[1] : r.q[0], (e & 7) >> 1);
-  return __half2float(__ushort_as_half((unsigned short)((e & 1) ? (u >> 16) : (u & 0xFFFFu))));
+template <> __device__ __forceinline__ float elem_at<__half>(uint32_t blk, int e) {
+  unsigned short v;
+  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(blk + 2u * (uint32_t)e));
+  return __half2float(__ushort_as_half(v));
 }
 
 // Power-of-two scaling of a block's comparisons: |x| and d are multiplied by
@@ -396,44 +392,53 @@ struct Scaled {
 
 // The midpoint of E2M1 codes c and c + 1 (0.25, 0.75, 1.25, 1.75, 2.5, 3.5,
 // 5 for c = 0..6): the float32 bits 0x3E800000 + (v << 21) with v = 0, 6, 9,
-// 11, 13, 15, 17, five bits each in one 64-bit constant.
+// 11, 13, 15, 17, byte c of a pair of 32-bit constants.
 __device__ __forceinline__ float e2m1_midpoint(uint32_t c) {
-  constexpr uint64_t kV = 0ull | (6ull << 5) | (9ull << 10) | (11ull << 15) | (13ull << 20) | (15ull << 25) |
-                          (17ull << 30);
-  return __uint_as_float(0x3E800000u + ((((uint32_t)(kV >> (5 * c))) & 31u) << 21));
+  const uint32_t v = __byte_perm(0x0B090600u, 0x00110F0Du, c) & 0xFFu;
+  return __uint_as_float(0x3E800000u + (v << 21));
 }
 
-// The values whose two conversions disagree (set nibbles of dm, elements e0
-// .. e0 + 7 of the block, codes of the upper products in hw). The products
-// lie within a factor 1 + 2^-20 of each other and the midpoints at least a
-// factor 1.4 apart, so exactly one midpoint m separates the two codes (c from
-// the lower product, c + 1 from the upper one): the sign of |x| - m d picks
-// one of them, and a tie the even one. fmaf forms |x| - m d with one
-// rounding; for d >= 2^-100 (callers send smaller d to exact_block) no
-// nonzero result of it underflows to zero, so its sign is the exact
-// comparison. The result still needs plus_zero.
+// The values whose two conversions disagree (set nibbles of dm0 and dm1 for
+// the words hw0 and hw1, elements 0..7 and 8..15 of the block; the codes in
+// hw are those of the upper products). The products lie within a factor
+// 1 + 2^-21 of each other and the midpoints at least a factor 1.4 apart, so
+// exactly one midpoint m separates the two codes (c from the lower product,
+// c + 1 from the upper one): the sign of |x| - m d picks one of them, and a
+// tie the even one. fmaf forms |x| - m d with one rounding; for d >= 2^-100
+// (callers send smaller d to exact_block) no nonzero result of it underflows
+// to zero, so its sign is the exact comparison. Both words in one loop, so
+// that a warp runs as many rounds as its lane with the most such values. The
+// results still need plus_zero.
 template <typename T>
-__device__ __forceinline__ uint32_t fix_codes(uint32_t hw, uint32_t dm, const Raw16<T>& r, int e0, float d) {
-  const uint32_t lw = hw ^ dm;
-  while (dm) {
+__device__ __forceinline__ void fix_codes(uint32_t& hw0, uint32_t& hw1, uint32_t dm0, uint32_t dm1, uint32_t blk,
+                                          float d) {
+  while (dm0 | dm1) {
+    const bool first = dm0 != 0;
+    const uint32_t dm = first ? dm0 : dm1;
+    const uint32_t hw = first ? hw0 : hw1;
     const int sh = (__ffs(dm) - 1) & ~3;
-    dm &= ~(0xFu << sh);
-    const uint32_t c = (lw >> sh) & 7u;
-    const float t = fmaf(-e2m1_midpoint(c), d, fabsf(raw_elem<T>(r, e0 + (sh >> 2))));
-    const bool up = t > 0.0f || (t == 0.0f && (c & 1u));
-    hw = (hw & ~(0xFu << sh)) | ((((up ? hw : lw) >> sh) & 0xFu) << sh);
+    const uint32_t nib = dm & (0xFu << sh);
+    const uint32_t c = ((hw ^ nib) >> sh) & 7u;  // the lower product's code
+    const float t = fmaf(-e2m1_midpoint(c), d, fabsf(elem_at<T>(blk, (first ? 0 : 8) + (sh >> 2))));
+    const uint32_t flip = (t < 0.0f || (t == 0.0f && !(c & 1u))) ? nib : 0u;  // down to c
+    if (first) {
+      hw0 ^= flip;
+      dm0 ^= nib;
+    } else {
+      hw1 ^= flip;
+      dm1 ^= nib;
+    }
   }
-  return hw;
 }
 
 // Every code of a block by the full comparisons (a d whose reciprocal
 // overflows float32). A zero magnitude gets +0.
 template <typename T>
-__device__ __forceinline__ uint2 exact_block(const Raw16<T>& r, float d) {
+__device__ __forceinline__ uint2 exact_block(uint32_t blk, float d) {
   const Scaled sc(d);
   uint32_t wd[2] = {0u, 0u};
   for (int e = 0; e < 16; ++e) {
-    const float x = raw_elem<T>(r, e);
+    const float x = elem_at<T>(blk, e);
     const uint32_t c = e2m1_code_exact(sc(x), sc.dn);
     const uint32_t nib = c | (c != 0u && x < 0.0f ? 8u : 0u);
     wd[e >> 3] |= nib << (4 * (e & 7));
@@ -441,69 +446,138 @@ __device__ __forceinline__ uint2 exact_block(const Raw16<T>& r, float d) {
   return make_uint2(wd[0], wd[1]);
 }
 
-// One 16-column block (two output words and a scale byte) per thread and
-// step, four blocks in flight (128 or 256 bytes of loads a thread). The code
-// of each value is the E2M1 value nearest to the exact |x| / d.
+// One 16-column block: its scale byte (returned in *sbyte) and its two
+// output words. blk is the block's shared-memory address (read again only by
+// the rare fix-up paths). The code of each value is the E2M1 value nearest to
+// the exact |x| / d.
 template <typename T>
-__global__ void __launch_bounds__(kStreamThreads)
-quantize_kernel(const T* __restrict__ x, const float* __restrict__ gs, int64_t E, int64_t blocks_per_expert,
-                uint32_t* __restrict__ w, uint8_t* __restrict__ scales) {
-  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-  const int64_t first = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+__device__ __forceinline__ uint2 quantize_block(const Raw16<T>& raw, uint32_t blk, bool has_gs, float inv, float fac,
+                                                uint32_t* sbyte) {
+  const float am = amax16<T>(raw);
+  float sc = __fdiv_rn(am, 6.0f);
+  if (has_gs) sc = __fmul_rn(sc, inv);
+  *sbyte = f32_to_e4m3_satfinite(sc);
+  const float d = __fmul_rn(e4m3_to_f32(*sbyte), fac);
+  if (!(d > 0.0f)) return make_uint2(0u, 0u);
+  // d below 2^-100: the comparisons need scaling (and below 2^-127 the
+  // reciprocal overflows)
+  if (d < 0x1p-100f) return exact_block<T>(blk, d);
+  // Each value is converted twice, from x * r (1 - 2^-22) and x * r (1 +
+  // 2^-22), r = 1 / d rounded: x * r is within two roundings (2^-23
+  // relative) of the quotient x / d, and each bracketing product within two
+  // more of x * r (1 -+ 2^-22), so the quotient lies strictly between them.
+  // Where both convert to the same code (the nearest-value code is monotone)
+  // that code is the one of the quotient. Codes that differ (a midpoint lies
+  // between the products, or on one of them) take the exact comparisons. One
+  // output word (eight values) at a time, to keep few values live.
+  const float r = __frcp_rn(d);
+  const float rl = __fmul_rn(r, 1.0f - 0x1p-22f), rh = __fmul_rn(r, 1.0f + 0x1p-22f);
+  uint32_t hw[2], dm[2];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    float ul[4], uh[4], vl[4], vh[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      pair_at<T>(raw, 4 * h + i, ul[i], uh[i]);
+      vl[i] = ul[i];
+      vh[i] = uh[i];
+      mul2_rn(ul[i], uh[i], rh);
+      mul2_rn(vl[i], vh[i], rl);
+    }
+    hw[h] = cvt_e2m1x8(ul, uh);
+    dm[h] = hw[h] ^ cvt_e2m1x8(vl, vh);
+  }
+  if (dm[0] | dm[1]) fix_codes<T>(hw[0], hw[1], dm[0], dm[1], blk, d);
+  return make_uint2(plus_zero(hw[0]), plus_zero(hw[1]));
+}
+
+// The quantizer: the copy engine streams the activations into shared memory, so that the bytes in flight no longer depend on registers. Chunks
+// of kQBlocks blocks of one expert's plane go through a ring of stages; one
+// producer thread issues the bulk loads, eight consumer warps quantize each
+// chunk (two blocks per thread) and store the words and scale bytes
+// directly (a warp's stores are 256 and 32 contiguous bytes). CTA (bx, by)
+// takes chunks bx, bx + gx, ... of experts by, by + gy, ...
+constexpr int kQBlocks = 512;
+constexpr int kQConsumers = 256;
+constexpr int kQThreads = kQConsumers + 32;
+template <typename T> struct QRing {
+  static constexpr int kStages = sizeof(T) == 4 ? 3 : 4;
+  static constexpr uint32_t kStage = kQBlocks * 16 * (uint32_t)sizeof(T);
+};
+
+template <typename T>
+__global__ void __launch_bounds__(kQThreads)
+quantize_kernel(const T* __restrict__ x, const float* __restrict__ gs, int64_t E, int64_t bpe,
+                     uint32_t* __restrict__ w, uint8_t* __restrict__ scales) {
+  using R = QRing<T>;
+  extern __shared__ __align__(128) uint8_t qbuf[];
+  __shared__ __align__(8) uint64_t bars[2 * R::kStages];  // full[s], then empty[s]
+  __shared__ int abort_flag;
+  const int warp = (int)threadIdx.x >> 5, lane = (int)threadIdx.x & 31;
+  const uint32_t sbuf = pipe::smem_addr(qbuf), sbar = pipe::smem_addr(bars);
+  auto full = [&](int st) { return sbar + 8u * (uint32_t)st; };
+  auto empty = [&](int st) { return sbar + 8u * (uint32_t)(R::kStages + st); };
+  if (threadIdx.x == 0) {
+    for (int st = 0; st < R::kStages; ++st) {
+      pipe::mbar_init(full(st), 1);
+      pipe::mbar_init(empty(st), kQConsumers / 32);
+    }
+    abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  const int64_t nch = (bpe + kQBlocks - 1) / kQBlocks;  // chunks per expert
+  if (warp == kQConsumers / 32) {
+    if (lane == 0) {
+      int64_t it = 0;
+      bool ok = true;
+      for (int64_t e = blockIdx.y; e < E && ok; e += gridDim.y)
+        for (int64_t c = blockIdx.x; c < nch; c += gridDim.x, ++it) {
+          const int st = (int)(it % R::kStages);
+          const uint32_t ph = (uint32_t)((it / R::kStages) & 1);
+          // stage st is free once every consumer warp released its last use
+          if (it >= R::kStages && !pipe::wait_bar(empty(st), ph ^ 1u, &abort_flag, 43, &g_copy_error)) {
+            ok = false;
+            break;
+          }
+          const int64_t b0 = c * kQBlocks;
+          const uint32_t bytes = (uint32_t)((bpe - b0 < kQBlocks ? bpe - b0 : kQBlocks) * 16 * (int64_t)sizeof(T));
+          pipe::mbar_arrive_tx(full(st), bytes);
+          bulk_g2s(sbuf + (uint32_t)st * R::kStage, x + 16 * (e * bpe + b0), bytes, full(st));
+        }
+      // no copy may still be landing when the CTA exits
+      for (int64_t i = it > R::kStages ? it - R::kStages : 0; i < it; ++i)
+        pipe::wait_bar_quiet(full((int)(i % R::kStages)), (uint32_t)((i / R::kStages) & 1));
+    }
+    return;
+  }
+  const bool has_gs = gs != nullptr;
+  int64_t it = 0;
   for (int64_t e = blockIdx.y; e < E; e += gridDim.y) {
-    const bool has_gs = gs != nullptr;
     const float fac = global_factor(gs, e);
     const float inv = has_gs ? __fdiv_rn(kGlobalScaleDivisor, __ldg(gs + e)) : 1.0f;
-    const int64_t base = e * blocks_per_expert;
-    constexpr int kU = 4;
-    for (int64_t b0 = first; b0 < blocks_per_expert; b0 += kU * stride) {
-      Raw16<T> raw[kU];
+    for (int64_t c = blockIdx.x; c < nch; c += gridDim.x, ++it) {
+      const int st = (int)(it % R::kStages);
+      const uint32_t ph = (uint32_t)((it / R::kStages) & 1);
+      if (!pipe::wait_bar_warp(full(st), ph, &abort_flag, 42, &g_copy_error)) return;
+      const int64_t b0 = c * kQBlocks, g0 = e * bpe + b0;
+      const int nb = (int)(bpe - b0 < kQBlocks ? bpe - b0 : kQBlocks);
+      const uint32_t src = sbuf + (uint32_t)st * R::kStage;
+      for (int j = (int)threadIdx.x; j < nb; j += kQConsumers) {
+        const uint32_t blk = src + (uint32_t)j * (16u * (uint32_t)sizeof(T));
+        Raw16<T> raw;
 #pragma unroll
-      for (int k = 0; k < kU; ++k) {
-        const int64_t b = b0 + k * stride;
-        if (b < blocks_per_expert) load_raw16<T>(x + 16 * (base + b), raw[k]);
+        for (int i = 0; i < (int)(sizeof(raw.q) / sizeof(uint4)); ++i)
+          asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                       : "=r"(raw.q[i].x), "=r"(raw.q[i].y), "=r"(raw.q[i].z), "=r"(raw.q[i].w)
+                       : "r"(blk + 16u * (uint32_t)i));
+        uint32_t sbyte;
+        const uint2 out = quantize_block<T>(raw, blk, has_gs, inv, fac, &sbyte);
+        __stcs(reinterpret_cast<uint2*>(w) + g0 + j, out);
+        scales[g0 + j] = (uint8_t)sbyte;
       }
-#pragma unroll
-      for (int k = 0; k < kU; ++k) {
-        const int64_t b = b0 + k * stride;
-        if (b >= blocks_per_expert) break;
-        float lo[8], hi[8];
-        const float am = widen16<T>(raw[k], lo, hi);
-        float sc = __fdiv_rn(am, 6.0f);
-        if (has_gs) sc = __fmul_rn(sc, inv);
-        const uint32_t sbyte = f32_to_e4m3_satfinite(sc);
-        const float d = __fmul_rn(e4m3_to_f32(sbyte), fac);
-        uint2 out = make_uint2(0u, 0u);
-        if (d > 0.0f) {
-          // Each value is converted twice, from x * r (1 - 2^-21) and
-          // x * r (1 + 2^-21): the product x * r is within two roundings
-          // (2^-23 relative) of the quotient x / d, so the quotient lies
-          // between the two products, and where both convert to the same
-          // code (the nearest-value code is monotone) that code is the one
-          // of the quotient. Codes that differ (a midpoint lies between the
-          // products) take the exact comparisons.
-          const float r = __frcp_rn(d);
-          const float rl = __fmul_rn(r, 1.0f - 0x1p-21f), rh = __fmul_rn(r, 1.0f + 0x1p-21f);
-          float ll[8], lh[8];
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            ll[i] = lo[i];
-            lh[i] = hi[i];
-            mul2_rn(lo[i], hi[i], rh);
-            mul2_rn(ll[i], lh[i], rl);
-          }
-          uint32_t hx = cvt_e2m1x8(lo, hi), hy = cvt_e2m1x8(lo + 4, hi + 4);
-          const uint32_t dx = hx ^ cvt_e2m1x8(ll, lh), dy = hy ^ cvt_e2m1x8(ll + 4, lh + 4);
-          if (dx) hx = fix_codes<T>(hx, dx, raw[k], 0, d);
-          if (dy) hy = fix_codes<T>(hy, dy, raw[k], 8, d);
-          out = make_uint2(plus_zero(hx), plus_zero(hy));
-          // d below 2^-100: the comparisons need scaling (and below 2^-127
-          // the reciprocal overflows)
-          if (d < 0x1p-100f) out = exact_block<T>(raw[k], d);
-        }
-        __stcs(reinterpret_cast<uint2*>(w) + base + b, out);
-        scales[base + b] = (uint8_t)sbyte;
-      }
+      __syncwarp();
+      if (lane == 0) pipe::mbar_arrive(empty(st));
     }
   }
 }
@@ -574,29 +648,38 @@ cudaError_t launch_transcode(const uint8_t* mo_w, int64_t w_bytes, const uint8_t
 
 cudaError_t launch_quantize(const void* x, int x_dtype, const float* gs, int64_t E, int64_t N, int64_t K,
                             uint32_t* w, uint8_t* scales, cudaStream_t st) {
+  // x is 16-byte aligned (the API checks), so every chunk is a legal bulk copy
   const int64_t bpe = N * (K / 16);  // 16-column blocks per expert
-  auto grid_of = [&](auto kern) {
-    int gx = stream_grid(kern, (bpe * E + 1) / 2);
-    const int64_t per_expert = (bpe + kStreamThreads - 1) / kStreamThreads;
-    if (gx > per_expert) gx = (int)(per_expert < 1 ? 1 : per_expert);
-    const int gy = (int)(E < 65535 ? E : 65535);
-    return dim3(gx, gy);
+  const int gy = (int)(E < 65535 ? E : 65535);
+  int dev = 0, sms = 152;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  // as many CTAs as are resident at once, spread over the experts, at most
+  // one per chunk of an expert
+  auto launch = [&](auto kern, auto* xt, uint32_t smem) -> cudaError_t {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    int per_sm = 1;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kQThreads, smem) != cudaSuccess || per_sm < 1)
+      per_sm = 1;
+    const int64_t nch = (bpe + kQBlocks - 1) / kQBlocks;
+    int64_t gx = ((int64_t)sms * per_sm + gy - 1) / gy;
+    if (gx > nch) gx = nch;
+    if (gx < 1) gx = 1;
+    kern<<<dim3((unsigned)gx, (unsigned)gy), kQThreads, smem, st>>>(xt, gs, E, bpe, w, scales);
+    return cudaGetLastError();
   };
   switch (x_dtype) {
     case kF32:
-      quantize_kernel<float><<<grid_of(quantize_kernel<float>), kStreamThreads, 0, st>>>(
-          static_cast<const float*>(x), gs, E, bpe, w, scales);
-      break;
+      return launch(quantize_kernel<float>, static_cast<const float*>(x),
+                    QRing<float>::kStages * QRing<float>::kStage);
     case kF16:
-      quantize_kernel<__half><<<grid_of(quantize_kernel<__half>), kStreamThreads, 0, st>>>(
-          static_cast<const __half*>(x), gs, E, bpe, w, scales);
-      break;
+      return launch(quantize_kernel<__half>, static_cast<const __half*>(x),
+                    QRing<__half>::kStages * QRing<__half>::kStage);
     default:
-      quantize_kernel<__nv_bfloat16><<<grid_of(quantize_kernel<__nv_bfloat16>), kStreamThreads, 0, st>>>(
-          static_cast<const __nv_bfloat16*>(x), gs, E, bpe, w, scales);
-      break;
+      return launch(quantize_kernel<__nv_bfloat16>, static_cast<const __nv_bfloat16*>(x),
+                    QRing<__nv_bfloat16>::kStages * QRing<__nv_bfloat16>::kStage);
   }
-  return cudaGetLastError();
 }
 
 cudaError_t launch_transcode_folded(const uint8_t* mo_w, int64_t w_bytes, const uint8_t* mo_ws, int64_t s_bytes,

@@ -89,6 +89,17 @@ def test_quantize_experts(nv, dt):
     check(nv, x, None)
 
 
+def test_quantize_experts_partial_chunks(nv):
+    """Experts whose block count is not a multiple of the bulk kernel's chunk
+    (512 blocks): 5 experts of 37 x 2064 (4773 blocks each), and more experts
+    (70) than one CTA per expert would give."""
+    x = dense(93, (5, 37, 2064), "bf16")
+    gs = np.abs(x.float().numpy()).reshape(5, -1).max(axis=1).astype(np.float32)
+    check(nv, x, gs)
+    x = dense(94, (70, 3, 64), "f16")
+    check(nv, x, None)
+
+
 def test_quantize_exact_ties(nv):
     """Codes at the midpoints of the E2M1 grid (d = 1) and block scales at the
     midpoints of the E4M3 grid: both roundings must go to the even code."""
