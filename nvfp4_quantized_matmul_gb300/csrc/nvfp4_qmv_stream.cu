@@ -1018,6 +1018,8 @@ qmv_stream_kernel(const QmvArgs a, const SPlan p, float* __restrict__ acc, uint3
 // CTAs resident at once (a cooperative launch); the producer keeps streaming
 // its weights meanwhile.
 constexpr int kSeqMaxCalls = 32;
+// Largest grid whose CTAs the host reassigns per call (one byte per CTA).
+constexpr int kSeqMaxGrid = 256;
 
 struct SeqCall {
   CUtensorMap wmap, smap;  // first: 64-byte aligned
@@ -1025,6 +1027,12 @@ struct SeqCall {
   SPlan p;
   int64_t ws_block;  // first workspace block (256-row tile) of this call
   int depends;       // wait for every earlier call before reading x
+  // CTA b takes share pos[b] of this call's split (shares >= S * gs have no
+  // work): the host deals the heavier shares of each call to the CTAs with
+  // the least work so far, so that the per-call rounding of the split does
+  // not pile up on the same CTAs. Identity when `permuted` is 0.
+  int permuted;
+  uint8_t pos[kSeqMaxGrid];
 };
 struct SeqArgs {
   SeqCall call[kSeqMaxCalls];
@@ -1057,6 +1065,8 @@ __device__ bool wait_count(const uint32_t* ctr, uint32_t target, volatile int* a
     __nanosleep(64);
   }
 }
+
+__device__ __forceinline__ int share_of(const SeqCall& C, int b) { return C.permuted ? (int)C.pos[b] : b; }
 
 // Asks L2 for this CTA's 1/C share of a call's activations x (M K 16-bit
 // values, contiguous; a multiple of 512 bytes), so that when the consumers
@@ -1140,10 +1150,11 @@ qmv_seq_kernel(const __grid_constant__ SeqArgs sa, float* __restrict__ acc, uint
       ProdState pst;
       for (int c = 0; c < sa.ncalls; ++c) {
         const SeqCall& C = sa.call[c];
-        if (b >= C.p.S * C.p.gs) continue;
+        const int bc = share_of(C, b);
+        if (bc >= C.p.S * C.p.gs) continue;
         // the consumers are still a ring's depth behind, on the previous call
         if (c > 0 && !C.depends) prefetch_x_share(C.a, b, (int)gridDim.x);
-        if (!produce<false, false>(C.p, b / C.p.gs, Work::of(C.p, b % C.p.gs), &C.wmap, &C.smap, wst, sst, bar,
+        if (!produce<false, false>(C.p, bc / C.p.gs, Work::of(C.p, bc % C.p.gs), &C.wmap, &C.smap, wst, sst, bar,
                                    abort_flag, 0, pst, stages))
           break;
       }
@@ -1156,8 +1167,9 @@ qmv_seq_kernel(const __grid_constant__ SeqArgs sa, float* __restrict__ acc, uint
     FinState fst;
     for (int c = 0; c < sa.ncalls; ++c) {
       const SeqCall& C = sa.call[c];
-      if (b < C.p.S * C.p.gs)
-        finish<false, false>(C.a, C.p, Work::of(C.p, b % C.p.gs), pbuf, pbuf_bytes, bar, abort_flag,
+      const int bc = share_of(C, b);
+      if (bc < C.p.S * C.p.gs)
+        finish<false, false>(C.a, C.p, Work::of(C.p, bc % C.p.gs), pbuf, pbuf_bytes, bar, abort_flag,
                              acc + C.ws_block * (int64_t)(kAccSlots * kTileRows), cnt + C.ws_block, 0, 0, nullptr,
                              fst);
       if (sa.signal) {  // this CTA has written all it writes of calls 0..c
@@ -1184,9 +1196,10 @@ qmv_seq_kernel(const __grid_constant__ SeqArgs sa, float* __restrict__ acc, uint
   bool staged = false;
   for (int c = 0; c < sa.ncalls; ++c) {
     const SeqCall& C = sa.call[c];
-    if (b >= C.p.S * C.p.gs) continue;
-    const int grp = b / C.p.gs;
-    const Work wk = Work::of(C.p, b % C.p.gs);
+    const int bc = share_of(C, b);
+    if (bc >= C.p.S * C.p.gs) continue;
+    const int grp = bc / C.p.gs;
+    const Work wk = Work::of(C.p, bc % C.p.gs);
     if (staged) {  // every consumer is done with the previous activations
       sync_all<kN>();
       if (threadIdx.x == 0) s_ncorr = 0;
@@ -1704,6 +1717,35 @@ cudaError_t launch_qmv_seq(const QmvArgs* calls, const int* depends, int n, int 
     blocks += C.p.nrt;
     xs = std::max(xs, (size_t)C.p.M * C.p.xs_stride * 2);
     if ((e = plane_maps(C.a, &C.wmap, &C.smap)) != cudaSuccess) return e;
+  }
+  // Deal each call's shares: the heaviest (most chunks, a 16-token chunk
+  // counted 1.3 times) to the CTAs with the least work so far.
+  if (sms <= kSeqMaxGrid) {
+    std::vector<double> load(sms, 0.0);
+    std::vector<int> by_load(sms), by_share(sms);
+    std::vector<double> share(sms);
+    for (int c = 0; c < n; ++c) {
+      SeqCall& C = sa->call[c];
+      const SPlan& p = C.p;
+      const double wgt = p.M > 8 ? 1.3 : 1.0;
+      const int64_t W = p.nrt / p.gs, rest = (p.nrt - W * p.gs) * p.ncg;
+      for (int i = 0; i < sms; ++i) {
+        if (i >= p.S * p.gs) {
+          share[i] = 0.0;
+          continue;
+        }
+        const int64_t gi = i % p.gs;
+        share[i] = wgt * (double)(W * p.ncg + rest * (gi + 1) / p.gs - rest * gi / p.gs);
+      }
+      for (int i = 0; i < sms; ++i) by_load[i] = by_share[i] = i;
+      std::stable_sort(by_load.begin(), by_load.end(), [&](int x, int y) { return load[x] < load[y]; });
+      std::stable_sort(by_share.begin(), by_share.end(), [&](int x, int y) { return share[x] > share[y]; });
+      for (int k = 0; k < sms; ++k) {
+        C.pos[by_load[k]] = (uint8_t)by_share[k];
+        load[by_load[k]] += share[by_share[k]];
+      }
+      C.permuted = 1;
+    }
   }
   sa->ncalls = n;
   sa->stages = best_stages;
