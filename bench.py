@@ -587,17 +587,20 @@ def run_routes(nv, synth, torch, dev, stream, args):
 
     # Non-transposed weights: the MLP up projection's sizes (K = 5376 inputs,
     # N = 21504 outputs) stored [K, N/8] and quantized along N, beside the
-    # transposed plane of the same sizes through nv.qmm.
+    # transposed plane of the same sizes through nv.qmm. Four copies of each
+    # plane (260 MB, twice what L2 holds) take turns, so that no call finds
+    # its weights left in L2 by an earlier one.
     k, n = 5376, 21504
-    wt = torch.randint(-2**31, 2**31 - 1, (k, n // 8), dtype=torch.int32, device=dev)
-    stt = torch.from_numpy(synth.log_uniform_scales(g, (k, n // 16), 2.0**-6, 4.0)).to(dev)
-    (w, s), = rand_w(n, k, 1, seed=9)
+    wts = [torch.randint(-2**31, 2**31 - 1, (k, n // 8), dtype=torch.int32, device=dev) for _ in range(4)]
+    stts = [torch.from_numpy(synth.log_uniform_scales(g, (k, n // 16), 2.0**-6, 4.0)).to(dev) for _ in range(4)]
+    wst = rand_w(n, k, 4, seed=9)
     ntr = {}
-    for m in (1, 16, 2048):
+    for m in (1, 8, 16, 2048):
         x = synth.activations(g, (m, k), "bf16").to(dev)
         y = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
-        ms_nt = time_calls(torch, dev, stream, lambda i: nv.qmm_nontransposed(x, wt, stt, out=y), 5)
-        ms_t = time_calls(torch, dev, stream, lambda i: nv.qmm(x, w, s, out=y), 5)
+        reps = 24 if m < 128 else 4
+        ms_nt = time_calls(torch, dev, stream, lambda i: nv.qmm_nontransposed(x, wts[i % 4], stts[i % 4], out=y), reps)
+        ms_t = time_calls(torch, dev, stream, lambda i: nv.qmm(x, wst[i % 4][0], wst[i % 4][1], out=y), reps)
         entry = {"us": round(ms_nt * 1e3, 1), "transposed_qmm_us": round(ms_t * 1e3, 1)}
         if m >= 128:
             tf = 2.0 * m * n * k / (ms_nt * 1e-3) / 1e12
@@ -608,7 +611,7 @@ def run_routes(nv, synth, torch, dev, stream, args):
         ntr[f"M{m}"] = entry
         del x, y
     out["qmm_nontransposed_5376x21504"] = ntr
-    del wt, stt, w, s
+    del wts, stts, wst
 
     # Quantize a dense bf16 gate/up plane [43008, 5376] with gs = its amax.
     n, k = 43008, 5376

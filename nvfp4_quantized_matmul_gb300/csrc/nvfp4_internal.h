@@ -123,10 +123,10 @@ cudaError_t launch_qmm_tc_glu(const void* x, int xdt, int64_t M, int64_t K, cons
 // 0, any K >= 1), y = x @ dequantize(w) * gs/2688; f16 or bf16 x.
 bool qmm_tc_nt_supported(int64_t M, int64_t N, int64_t K);
 // Up to kQmvNtMaxM token rows of a non-transposed weight: one streaming pass
-// over the plane, partial sums in a per-stream float workspace, then y. On
-// GB300 it beat the tensor cores at one and two rows ([5376, 21504]: 30 / 52
-// µs against 86 / 66) and lost from three on (74 against 67).
-constexpr int64_t kQmvNtMaxM = 2;
+// over the plane (the eight token rows are the eight columns of an m16n8k16
+// MMA's B operand, so any M up to 8 costs the same), partial sums in a
+// per-stream float workspace, then y.
+constexpr int64_t kQmvNtMaxM = 8;
 bool qmv_nt_supported(int64_t M, int64_t N, int64_t K);
 cudaError_t launch_qmv_nt(const void* x, int xdt, int64_t M, int64_t K, const uint32_t* w, const uint8_t* scales,
                           const float* gs, int64_t N, void* y, cudaStream_t st);

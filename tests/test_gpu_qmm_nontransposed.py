@@ -10,8 +10,9 @@ k-block, N ending inside a weight tile and inside a word pair, one and two
 128-row halves, both dtypes, the global scale, back-to-back calls, a CUDA
 graph replay and the prefill shape at full size on sampled outputs, with
 the stream-K split of the k-blocks and with whole tiles; and the decode
-route (one or two token rows: one streaming pass, partial sums in a float
-workspace) on its own shapes, against the tensor cores and in a graph.
+route (up to eight token rows: one streaming pass through m16n8k16 MMAs,
+partial sums in a float workspace) on its own shapes, with activations
+beyond f16's range, against the tensor cores and in a graph.
 """
 import numpy as np
 import pytest
@@ -125,11 +126,13 @@ def test_nontransposed_zero_k_and_empty(nv):
     assert y.shape == (5, 64) and bool((y == 0).all())
 
 
-# (M, K, N) for the decode route (M <= 2): K inside one 128-input task, across
-# tasks with a ragged last one, not a multiple of 8; N ending inside a
-# 256-output slab and inside a word pair
+# (M, K, N) for the decode route (M <= 8): K inside one 16-input step, across
+# steps with a ragged last one, not a multiple of 4 or 8; N ending inside a
+# 256-output slab and inside a word pair; planes that take the copy ring
+# (N % 128 == 0, K % 4 == 0) and planes that take plain loads
 NT_DECODE = [(1, 17, 32), (2, 100, 272), (1, 128, 1008), (2, 300, 256), (1, 2048, 2560), (2, 5376, 4096),
-             (1, 777, 528), (2, 21504, 512)]
+             (1, 777, 528), (2, 21504, 512), (3, 1000, 1024), (5, 260, 384), (8, 513, 640), (7, 4096, 2048),
+             (4, 64, 16), (6, 18, 2304)]
 
 
 @pytest.mark.parametrize("mkn", NT_DECODE, ids=lambda v: "M%d_K%d_N%d" % v)
@@ -151,6 +154,34 @@ def test_nontransposed_decode_route(nv, mkn, dt, with_gs):
         err = rel_err(y, ref)
         assert err <= TOL[dt], f"call {rep}: rel-to-max error {err:.3g} > {TOL[dt]}"
         assert guards_intact(backing, guard)
+
+
+@pytest.mark.parametrize("aligned", [True, False], ids=["ring", "plain"])
+def test_nontransposed_decode_bf16_beyond_f16(nv, aligned):
+    """bf16 activations that f16 cannot hold (above its range, or below its
+    normal range with more bits than its subnormals keep) take the bf16 MMA
+    for the steps that hold them; the other steps keep the f16 MMA. Each token
+    row is checked against its own largest output."""
+    M, N = 4, 512 if aligned else 528
+    K = 1024 if aligned else 1022
+    w, s = weights(211 + K, K, N)
+    g = synth.rng(212)
+    x = torch.from_numpy(g.standard_normal(size=(M, K)).astype(np.float32))
+    x[0] *= 2.0**20            # every value overflows f16
+    x[1] *= 2.0**-30           # every value below f16's subnormals
+    x[2, 300:310] *= 2.0**18   # a few steps of row 2 overflow f16
+    x[3, 700] = 2.0**-20 * (1 + 2.0**-7)  # one value f16 rounds
+    x = x.to(torch.bfloat16)
+    ref = O.qmm_nontransposed(x.double().numpy(), w, s, None)
+    y = nv.qmm_nontransposed(x.cuda(), u32_to_dev(w), u8_to_dev(s))
+    torch.cuda.synchronize()
+    assert nv.take_device_error() == 0
+    yc = y.double().cpu().numpy()
+    for m in range(M):
+        scale = np.max(np.abs(ref[m]))
+        assert scale > 0
+        err = np.max(np.abs(yc[m] - ref[m])) / scale
+        assert err <= TOL["bf16"], f"row {m}: rel-to-max error {err:.3g}"
 
 
 def test_nontransposed_decode_routes_agree(nv, opt):
