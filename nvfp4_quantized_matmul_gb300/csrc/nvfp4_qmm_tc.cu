@@ -104,7 +104,28 @@ struct TcParams {
   // up. glu_act: 1 SiLU, 2 GELU (tanh form).
   int64_t glu_cols;
   int glu_act;
+  // bf16 activations served by the f16 kernel (rows_to_f16_kernel, output
+  // type bf16): row m of the f16 activations is the bf16 row times 1 /
+  // row_scale[m], so each sum is multiplied by row_scale[m] (a power of two).
+  const float* row_scale = nullptr;
 };
+
+// Output bits of one value in the output type. The f16 kernels that serve
+// bf16 rows (output type bf16) scale each row's sums by row_scale; the others
+// have no scaling code at all.
+template <typename T, typename TO>
+__device__ __forceinline__ float row_factor(const TcParams& p, int64_t m) {
+  if constexpr (std::is_same<T, TO>::value) {
+    return 1.0f;
+  } else {
+    return __ldg(p.row_scale + m);  // an exact power of two
+  }
+}
+template <typename TO>
+__device__ __forceinline__ uint32_t out_bits(float v) {
+  const TO t = Dt<TO>::from_f32(v);
+  return *reinterpret_cast<const uint16_t*>(&t);
+}
 
 // One output tile: expert, weight tile, first output row and row count.
 struct Tile {
@@ -741,7 +762,8 @@ __device__ void build_gather_tables(const TcParams& p, uint32_t* samp, int* seg,
 
 // ---------------------------------------------------------------- kernel
 
-template <typename T, typename C, bool GATHER, bool kGlu = false, bool kNT = false>
+// TO: the output type (T, or bf16 when the f16 kernel serves bf16 rows).
+template <typename T, typename C, bool GATHER, bool kGlu = false, bool kNT = false, typename TO = T>
 __global__ void __launch_bounds__(C::THREADS, 1)
 qmm_tc_kernel(const __grid_constant__ CUtensorMap xmap, const TcParams p) {
   constexpr int STAGES = C::STAGES, MH = C::MH, BN = C::BN, BM = C::BM, NBUF = C::ACC_BUFS;
@@ -889,7 +911,7 @@ qmm_tc_kernel(const __grid_constant__ CUtensorMap xmap, const TcParams p) {
   } else if (warp >= kWarpEpi0 && warp < kWarpEpi0 + C::EPI_WARPS) {
     const int q = warp & 3;                  // TMEM lane quarter this warp may read
     const int hm = (warp - kWarpEpi0) >> 2;  // M half it drains
-    T* y = static_cast<T*>(p.y);
+    TO* y = static_cast<TO*>(p.y);
     if (GATHER) {
       // rows whose expert index is out of range (sorted last) are exact +0
       const int64_t z0 = seg[p.E];
@@ -912,6 +934,8 @@ qmm_tc_kernel(const __grid_constant__ CUtensorMap xmap, const TcParams p) {
         zero = xr >= p.B;
       }
       const float fac = global_factor(p.gs, tl.e);
+      constexpr bool kRowScale = !std::is_same<T, TO>::value;
+      const float rsc = kRowScale && live ? row_factor<T, TO>(p, m) : 1.0f;
       const int64_t n_base = (int64_t)tl.nt * BN;
       const uint32_t tcol = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(b * MH * BN + hm * BN);
       if constexpr (kGlu) {
@@ -932,6 +956,10 @@ qmm_tc_kernel(const __grid_constant__ CUtensorMap xmap, const TcParams p) {
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
               float gv = __uint_as_float(g[2 * k + e]), uv = __uint_as_float(u[2 * k + e]);
+              if (kRowScale) {
+                gv *= rsc;
+                uv *= rsc;
+              }
               if (p.gs) {
                 gv = __fmul_rn(gv, fac);
                 uv = __fmul_rn(uv, fac);
@@ -940,11 +968,9 @@ qmm_tc_kernel(const __grid_constant__ CUtensorMap xmap, const TcParams p) {
               const float z = p.glu_act == 1 ? gv : 1.5957691216057308f * (gv + 0.044715f * gv * gv * gv);
               o[e] = __fdividef(gv, 1.0f + __expf(-z)) * uv;
             }
-            const T t0 = Dt<T>::from_f32(o[0]), t1 = Dt<T>::from_f32(o[1]);
-            packed[k] = (uint32_t)(*reinterpret_cast<const uint16_t*>(&t0)) |
-                        ((uint32_t)(*reinterpret_cast<const uint16_t*>(&t1)) << 16);
+            packed[k] = out_bits<TO>(o[0]) | (out_bits<TO>(o[1]) << 16);
           }
-          T* dst = y + m * p.glu_cols + n0;
+          TO* dst = y + m * p.glu_cols + n0;
           if (n0 + 32 <= p.glu_cols && (p.glu_cols % 8) == 0) {
             uint4* d4 = reinterpret_cast<uint4*>(dst);
 #pragma unroll
@@ -972,16 +998,17 @@ qmm_tc_kernel(const __grid_constant__ CUtensorMap xmap, const TcParams p) {
 #pragma unroll
         for (int k = 0; k < 16; ++k) {
           float v0 = __uint_as_float(r[2 * k]), v1 = __uint_as_float(r[2 * k + 1]);
+          if (kRowScale) {
+            v0 *= rsc;
+            v1 *= rsc;
+          }
           if (p.gs) {
             v0 = __fmul_rn(v0, fac);
             v1 = __fmul_rn(v1, fac);
           }
-          const T t0 = Dt<T>::from_f32(v0), t1 = Dt<T>::from_f32(v1);
-          packed[k] = zero ? 0u
-                           : (uint32_t)(*reinterpret_cast<const uint16_t*>(&t0)) |
-                                 ((uint32_t)(*reinterpret_cast<const uint16_t*>(&t1)) << 16);
+          packed[k] = zero ? 0u : out_bits<TO>(v0) | (out_bits<TO>(v1) << 16);
         }
-        T* dst = y + m * p.N + n0;
+        TO* dst = y + m * p.N + n0;
         if (n0 + 32 <= p.N && (p.N % 8) == 0) {
           uint4* d4 = reinterpret_cast<uint4*>(dst);
 #pragma unroll
@@ -1015,7 +1042,7 @@ qmm_tc_kernel(const __grid_constant__ CUtensorMap xmap, const TcParams p) {
 // The stream-K kernel (dense launches of fewer than two waves of tiles): the
 // same roles as qmm_tc_kernel, walking units (tile, k-block range), with the
 // split-tile epilogue. Instantiated with GATHER = false and SK = true only.
-template <typename T, typename C, bool GATHER, bool SK, bool kNT = false>
+template <typename T, typename C, bool GATHER, bool SK, bool kNT = false, typename TO = T>
 __global__ void __launch_bounds__(C::THREADS, 1)
 qmm_tc_sk_kernel(const __grid_constant__ CUtensorMap xmap, const TcParams p) {
   constexpr int STAGES = C::STAGES, MH = C::MH, BN = C::BN, BM = C::BM, NBUF = C::ACC_BUFS;
@@ -1170,7 +1197,7 @@ qmm_tc_sk_kernel(const __grid_constant__ CUtensorMap xmap, const TcParams p) {
     const int q = warp & 3;                  // TMEM lane quarter this warp may read
     const int hm = (warp - kWarpEpi0) >> 2;  // M half it drains
     const int etid = threadIdx.x - 32 * kWarpEpi0;
-    T* y = static_cast<T*>(p.y);
+    TO* y = static_cast<TO*>(p.y);
     if (GATHER) {
       // rows whose expert index is out of range (sorted last) are exact +0
       const int64_t z0 = seg[p.E];
@@ -1181,20 +1208,23 @@ qmm_tc_sk_kernel(const __grid_constant__ CUtensorMap xmap, const TcParams p) {
     }
     // factor, cast and store 32 consecutive outputs of row m from n0
     auto store32 = [&](const uint32_t (&r)[32], int64_t m, int64_t n0, float fac, bool zero) {
+      constexpr bool kRowScale = !std::is_same<T, TO>::value;
+      const float rsc = row_factor<T, TO>(p, m);
       uint32_t packed[16];
 #pragma unroll
       for (int k = 0; k < 16; ++k) {
         float v0 = __uint_as_float(r[2 * k]), v1 = __uint_as_float(r[2 * k + 1]);
+        if (kRowScale) {
+          v0 *= rsc;
+          v1 *= rsc;
+        }
         if (p.gs) {
           v0 = __fmul_rn(v0, fac);
           v1 = __fmul_rn(v1, fac);
         }
-        const T t0 = Dt<T>::from_f32(v0), t1 = Dt<T>::from_f32(v1);
-        packed[k] = zero ? 0u
-                         : (uint32_t)(*reinterpret_cast<const uint16_t*>(&t0)) |
-                               ((uint32_t)(*reinterpret_cast<const uint16_t*>(&t1)) << 16);
+        packed[k] = zero ? 0u : out_bits<TO>(v0) | (out_bits<TO>(v1) << 16);
       }
-      T* dst = y + m * p.N + n0;
+      TO* dst = y + m * p.N + n0;
       if (n0 + 32 <= p.N && (p.N % 8) == 0) {
         uint4* d4 = reinterpret_cast<uint4*>(dst);
 #pragma unroll
@@ -1374,9 +1404,9 @@ bool stream_k_on() { return tc_stream_k(); }
 // the SMs (smaller pieces cost more to combine than they save).
 constexpr int64_t kMinSkBlocks = 8;
 
-template <typename T, typename C>
+template <typename T, typename C, typename TO = T>
 cudaError_t launch_cfg(const void* x, int64_t M, int64_t K, const uint32_t* w, const uint8_t* scales, const float* gs,
-                       int64_t N, void* y, int sms, cudaStream_t st) {
+                       int64_t N, void* y, int sms, cudaStream_t st, const float* row_scale = nullptr) {
   auto enc = encode_fn();
   if (!enc) return cudaErrorNotSupported;
   CUtensorMap map;
@@ -1407,6 +1437,7 @@ cudaError_t launch_cfg(const void* x, int64_t M, int64_t K, const uint32_t* w, c
   p.E = 1;
   p.glu_cols = 0;
   p.glu_act = 0;
+  p.row_scale = row_scale;
   // Tiles are dealt whole, round robin, unless they make fewer than two
   // waves: then the partial wave would idle a large share of the SMs, and
   // all tiles are split evenly by k-blocks instead (stream-K). From two
@@ -1438,7 +1469,7 @@ cudaError_t launch_cfg(const void* x, int64_t M, int64_t K, const uint32_t* w, c
     p.ws = ws.acc;
     p.ws_cnt = ws.cnt;
   }
-  auto kern = p.sk_tiles > 0 ? qmm_tc_sk_kernel<T, C, false, true> : qmm_tc_kernel<T, C, false>;
+  auto kern = p.sk_tiles > 0 ? qmm_tc_sk_kernel<T, C, false, true, false, TO> : qmm_tc_kernel<T, C, false, false, false, TO>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
   if (e != cudaSuccess) return e;
   kern<<<grid, C::THREADS, C::SMEM, st>>>(map, p);
@@ -1451,9 +1482,10 @@ using Tile128x256 = Cfg<1, 256>;
 
 // Fused gate/up with its activation: weight tiles of 128 gate rows and the
 // matching 128 up rows (BN = 256), whole tiles round robin.
-template <typename T, typename C>
+template <typename T, typename C, typename TO = T>
 cudaError_t launch_glu_cfg(const void* x, int64_t M, int64_t K, const uint32_t* w, const uint8_t* scales,
-                           const float* gs, int64_t cols, int act, void* y, int sms, cudaStream_t st) {
+                           const float* gs, int64_t cols, int act, void* y, int sms, cudaStream_t st,
+                           const float* row_scale = nullptr) {
   static_assert(C::BN == 256, "a GLU tile is 128 gate rows and 128 up rows");
   auto enc = encode_fn();
   if (!enc) return cudaErrorNotSupported;
@@ -1489,8 +1521,9 @@ cudaError_t launch_glu_cfg(const void* x, int64_t M, int64_t K, const uint32_t* 
   p.ws_cnt = nullptr;
   p.glu_cols = cols;
   p.glu_act = act;
+  p.row_scale = row_scale;
   const int grid = p.num_tiles < sms ? p.num_tiles : sms;
-  auto kern = qmm_tc_kernel<T, C, false, true>;
+  auto kern = qmm_tc_kernel<T, C, false, true, false, TO>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
   if (e != cudaSuccess) return e;
   kern<<<grid, C::THREADS, C::SMEM, st>>>(map, p);
@@ -1527,16 +1560,162 @@ int pick_tile(int64_t M, int64_t N, int sms) {
   return best;
 }
 
+cudaError_t gather_buffer(int dev, cudaStream_t st, size_t bytes, void** out);
+
+// bf16 activation rows as f16, for the f16 kernels: output row r takes x row
+// lhs[r] (row r without lhs; an index >= B gives a zero row), scaled by 2^s,
+// the power of two that brings the row's largest finite magnitude into
+// [2^14, 2^15), and rounded to f16; rs[r] = 2^-s undoes the scaling on the
+// row's sums. A bf16 value keeps 8 significant bits and f16 11 down to
+// 2^-14, so every value of at least 2^-29 times the row's largest converts
+// exactly; smaller ones round to a multiple of 2^-24 (after scaling), an
+// error below 2^-39 of the row's largest value. Infinities and NaNs pass
+// through. One warp per row, kv 16-byte units per row.
+__device__ __forceinline__ int f16_row_shift(uint32_t mx) {  // mx: largest finite |value| as bf16 bits
+  int sh = mx == 0 ? 0 : 141 - (int)(mx >> 7);                 // largest * 2^sh in [2^14, 2^15)
+  return sh > 126 ? 126 : sh;                                  // (subnormal maxima)
+}
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2_scaled(uint32_t w, float up) {
+  const __half2 h = __floats2half2_rn(__uint_as_float(w << 16) * up, __uint_as_float(w & 0xFFFF0000u) * up);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+__device__ __forceinline__ uint32_t finite_abs_max(uint32_t mx, uint32_t w) {
+  const uint32_t lo = w & 0x7FFFu, hi = (w >> 16) & 0x7FFFu;
+  if (lo < 0x7F80u) mx = lo > mx ? lo : mx;
+  if (hi < 0x7F80u) mx = hi > mx ? hi : mx;
+  return mx;
+}
+
+// One CTA per row; a row of up to 256 * kRowRegUnits 16-byte units is read
+// once and kept in registers between the maximum and the conversion,
+// longer rows are read twice.
+constexpr int kRowThreads = 256, kRowRegUnits = 12;
+__global__ void __launch_bounds__(kRowThreads) rows_to_f16_kernel(const uint4* __restrict__ x,
+                                                                  const uint32_t* __restrict__ lhs, int64_t B,
+                                                                  int64_t R, int kv, uint4* __restrict__ xh,
+                                                                  float* __restrict__ rs) {
+  __shared__ uint32_t s_max[kRowThreads / 32];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  for (int64_t r = blockIdx.x; r < R; r += gridDim.x) {
+    const int64_t src = lhs ? (int64_t)__ldg(lhs + r) : r;
+    uint4* out = xh + r * kv;
+    if (src >= B) {  // block-uniform
+      for (int j = tid; j < kv; j += kRowThreads) out[j] = make_uint4(0, 0, 0, 0);
+      if (tid == 0) rs[r] = 1.0f;
+      continue;
+    }
+    const uint4* row = x + src * kv;
+    const bool in_regs = kv <= kRowThreads * kRowRegUnits;
+    uint4 v[kRowRegUnits];
+    uint32_t mx = 0;
+    if (in_regs) {
+#pragma unroll
+      for (int i = 0; i < kRowRegUnits; ++i) {
+        const int j = tid + i * kRowThreads;
+        v[i] = j < kv ? __ldg(row + j) : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int i = 0; i < kRowRegUnits; ++i)
+        mx = finite_abs_max(finite_abs_max(finite_abs_max(finite_abs_max(mx, v[i].x), v[i].y), v[i].z), v[i].w);
+    } else {
+      for (int j = tid; j < kv; j += kRowThreads) {
+        const uint4 u = __ldg(row + j);
+        mx = finite_abs_max(finite_abs_max(finite_abs_max(finite_abs_max(mx, u.x), u.y), u.z), u.w);
+      }
+    }
+    mx = __reduce_max_sync(0xffffffffu, mx);
+    if (lane == 0) s_max[warp] = mx;
+    __syncthreads();
+    mx = s_max[0];
+#pragma unroll
+    for (int w = 1; w < kRowThreads / 32; ++w) mx = s_max[w] > mx ? s_max[w] : mx;
+    __syncthreads();  // s_max is rewritten for the next row
+    const int sh = f16_row_shift(mx);
+    const float up = __uint_as_float((uint32_t)(sh + 127) << 23);
+    if (tid == 0) rs[r] = __uint_as_float((uint32_t)(127 - sh) << 23);
+    if (in_regs) {
+#pragma unroll
+      for (int i = 0; i < kRowRegUnits; ++i) {
+        const int j = tid + i * kRowThreads;
+        if (j < kv)
+          out[j] = make_uint4(bf16x2_to_f16x2_scaled(v[i].x, up), bf16x2_to_f16x2_scaled(v[i].y, up),
+                              bf16x2_to_f16x2_scaled(v[i].z, up), bf16x2_to_f16x2_scaled(v[i].w, up));
+      }
+    } else {
+      for (int j = tid; j < kv; j += kRowThreads) {
+        const uint4 u = __ldg(row + j);
+        out[j] = make_uint4(bf16x2_to_f16x2_scaled(u.x, up), bf16x2_to_f16x2_scaled(u.y, up),
+                            bf16x2_to_f16x2_scaled(u.z, up), bf16x2_to_f16x2_scaled(u.w, up));
+      }
+    }
+  }
+}
+
+// The same for rows of any length K, written with kp >= K elements (columns
+// past K are +0), for activations that are no TMA source as they are.
+__global__ void __launch_bounds__(256) rows_to_f16_pad_kernel(const uint16_t* __restrict__ x, int64_t M, int64_t K,
+                                                              int64_t kp, uint16_t* __restrict__ xh,
+                                                              float* __restrict__ rs) {
+  const int lane = threadIdx.x & 31;
+  const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
+  for (int64_t r = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < M; r += nwarps) {
+    const uint16_t* row = x + r * K;
+    uint32_t mx = 0;
+    for (int64_t c = lane; c < K; c += 32) mx = finite_abs_max(mx, __ldg(row + c));
+    const int sh = f16_row_shift(__reduce_max_sync(0xffffffffu, mx));
+    const float up = __uint_as_float((uint32_t)(sh + 127) << 23);
+    if (lane == 0) rs[r] = __uint_as_float((uint32_t)(127 - sh) << 23);
+    for (int64_t c = lane; c < kp; c += 32) {
+      const uint32_t v = c < K ? (uint32_t)__ldg(row + c) : 0u;
+      xh[r * kp + c] = (uint16_t)bf16x2_to_f16x2_scaled(v, up);
+    }
+  }
+}
+
+// bf16 activations take the f16 kernels (their weight decode costs about a
+// third of the bf16 one: there is no E2M1 -> bf16 conversion): R rows (row r
+// from x row lhs[r], or r) are first converted into the stream's scratch
+// buffer, rows of kp elements (kp = K when K % 8 == 0), each with a
+// power-of-two scale that the kernels undo on its sums.
+cudaError_t rows_to_f16(const void* x, int64_t R, int64_t K, const uint32_t* lhs, int64_t B, int sms, cudaStream_t st,
+                        const void** xh, const float** rs, int64_t* kp_out = nullptr) {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  const int64_t kp = (K + 7) / 8 * 8;
+  const size_t xb = ((size_t)R * (size_t)kp * 2 + 255) / 256 * 256;
+  void* buf = nullptr;
+  cudaError_t e = gather_buffer(dev, st, xb + (size_t)R * 4, &buf);
+  if (e != cudaSuccess) return e;
+  float* scale = reinterpret_cast<float*>(static_cast<char*>(buf) + xb);
+  if (kp == K) {
+    rows_to_f16_kernel<<<(unsigned)(R < 16 * sms ? R : 16 * sms), kRowThreads, 0, st>>>(
+        static_cast<const uint4*>(x), lhs, B, R, (int)(K / 8), static_cast<uint4*>(buf), scale);
+  } else {  // (no row gather with K % 8 != 0: the gather route needs K % 16 == 0)
+    const int64_t blocks = (R + 7) / 8;
+    rows_to_f16_pad_kernel<<<(unsigned)(blocks < 8 * sms ? blocks : 8 * sms), 256, 0, st>>>(
+        static_cast<const uint16_t*>(x), R, K, kp, static_cast<uint16_t*>(buf), scale);
+  }
+  *xh = buf;
+  *rs = scale;
+  if (kp_out) *kp_out = kp;
+  return cudaGetLastError();
+}
+
 template <typename T>
 cudaError_t launch_tc(const void* x, int64_t M, int64_t K, const uint32_t* w, const uint8_t* scales, const float* gs,
                       int64_t N, void* y, cudaStream_t st) {
   int dev = 0, sms = 152;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  switch (pick_tile(M, N, sms)) {
-    case 0: return launch_cfg<T, Tile256x256>(x, M, K, w, scales, gs, N, y, sms, st);
-    case 1: return launch_cfg<T, Tile256x128>(x, M, K, w, scales, gs, N, y, sms, st);
-    default: return launch_cfg<T, Tile128x256>(x, M, K, w, scales, gs, N, y, sms, st);
+  const float* rs = nullptr;
+  if (std::is_same<T, __nv_bfloat16>::value) {
+    cudaError_t e = rows_to_f16(x, M, K, nullptr, M, sms, st, &x, &rs);
+    if (e != cudaSuccess) return e;
+  }
+  switch (pick_tile(M, N, sms)) {  // T here is the output type; the kernels decode and multiply in f16
+    case 0: return launch_cfg<__half, Tile256x256, T>(x, M, K, w, scales, gs, N, y, sms, st, rs);
+    case 1: return launch_cfg<__half, Tile256x128, T>(x, M, K, w, scales, gs, N, y, sms, st, rs);
+    default: return launch_cfg<__half, Tile128x256, T>(x, M, K, w, scales, gs, N, y, sms, st, rs);
   }
 }
 
@@ -1605,7 +1784,7 @@ cudaError_t gather_buffer(int dev, cudaStream_t st, size_t bytes, void** out) {
 // so that every activation tile is a plain 128-row TMA box (per-row
 // tile::gather4 copies, four rows each and 32 per box, left the copy engine,
 // not the tensor core, setting the pace).
-template <typename T, typename C>
+template <typename T, typename C, typename TO = T>
 cudaError_t launch_gather(const void* x, int64_t B, int64_t K, const uint32_t* lhs, const uint32_t* rhs, int64_t R,
                           const uint32_t* w, const uint8_t* scales, const float* gs, int64_t E, int64_t N, void* y,
                           cudaStream_t st) {
@@ -1616,7 +1795,12 @@ cudaError_t launch_gather(const void* x, int64_t B, int64_t K, const uint32_t* l
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const void* xa = x;
   int64_t xrows = B;
-  if (lhs) {
+  const float* rs = nullptr;
+  if (!std::is_same<T, TO>::value) {  // bf16 rows, gathered and converted in one pass
+    cudaError_t e = rows_to_f16(x, R, K, lhs, B, sms, st, &xa, &rs);
+    if (e != cudaSuccess) return e;
+    xrows = R;
+  } else if (lhs) {
     void* xg = nullptr;
     cudaError_t e = gather_buffer(dev, st, (size_t)R * (size_t)K * 2, &xg);
     if (e != cudaSuccess) return e;
@@ -1655,8 +1839,9 @@ cudaError_t launch_gather(const void* x, int64_t B, int64_t K, const uint32_t* l
   p.E = (int)E;
   p.glu_cols = 0;
   p.glu_act = 0;
+  p.row_scale = rs;
   const size_t smem = C::SMEM + kGatherSmem;
-  auto kern = qmm_tc_kernel<T, C, true>;
+  auto kern = qmm_tc_kernel<T, C, true, false, false, TO>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   kern<<<sms, C::THREADS, smem, st>>>(map, p);
@@ -1669,10 +1854,11 @@ template <typename T>
 cudaError_t launch_gather_t(const void* x, int64_t B, int64_t K, const uint32_t* lhs, const uint32_t* rhs, int64_t R,
                             const uint32_t* w, const uint8_t* scales, const float* gs, int64_t E, int64_t N, void* y,
                             cudaStream_t st) {
+  // T is the activation (and output) type; the kernels decode and multiply in f16
   const int t = option(kOptGatherTile);  // 0 or 1 256x256, 2 256x128, 3 128x256
-  if (t == 3) return launch_gather<T, Tile128x256>(x, B, K, lhs, rhs, R, w, scales, gs, E, N, y, st);
-  if (t == 2) return launch_gather<T, Tile256x128>(x, B, K, lhs, rhs, R, w, scales, gs, E, N, y, st);
-  return launch_gather<T, Tile256x256>(x, B, K, lhs, rhs, R, w, scales, gs, E, N, y, st);
+  if (t == 3) return launch_gather<__half, Tile128x256, T>(x, B, K, lhs, rhs, R, w, scales, gs, E, N, y, st);
+  if (t == 2) return launch_gather<__half, Tile256x128, T>(x, B, K, lhs, rhs, R, w, scales, gs, E, N, y, st);
+  return launch_gather<__half, Tile256x256, T>(x, B, K, lhs, rhs, R, w, scales, gs, E, N, y, st);
 }
 
 // Activations whose rows are not a multiple of 16 bytes (K % 8 != 0) cannot
@@ -1689,14 +1875,18 @@ __global__ void __launch_bounds__(256) pad_cols_kernel(const uint16_t* __restric
 
 // Non-transposed weights ([K, N/8] words, scales along N): whole tiles dealt
 // round robin to a persistent grid; 128-row tiles while M fits one.
-template <typename T, typename C>
+template <typename T, typename C, typename TO = T>
 cudaError_t launch_nt_cfg(const void* x, int64_t M, int64_t K, const uint32_t* w, const uint8_t* scales,
                           const float* gs, int64_t N, void* y, int sms, cudaStream_t st) {
   auto enc = encode_fn();
   if (!enc) return cudaErrorNotSupported;
   const void* xa = x;
   int64_t kx = K;
-  if (K % 8) {
+  const float* rs = nullptr;
+  if (!std::is_same<T, TO>::value) {  // bf16 rows: converted (and padded) in one pass
+    cudaError_t e = rows_to_f16(x, M, K, nullptr, M, sms, st, &xa, &rs, &kx);
+    if (e != cudaSuccess) return e;
+  } else if (K % 8) {
     int dev = 0;
     cudaGetDevice(&dev);
     kx = (K + 7) / 8 * 8;
@@ -1737,6 +1927,7 @@ cudaError_t launch_nt_cfg(const void* x, int64_t M, int64_t K, const uint32_t* w
   p.E = 1;
   p.glu_cols = 0;
   p.glu_act = 0;
+  p.row_scale = rs;
   // the dense route's rule: below two waves of tiles (and not whole waves)
   // every tile's k-blocks are split evenly over the CTAs
   const int T_ = p.num_tiles;
@@ -1762,7 +1953,7 @@ cudaError_t launch_nt_cfg(const void* x, int64_t M, int64_t K, const uint32_t* w
     p.ws = ws.acc;
     p.ws_cnt = ws.cnt;
   }
-  auto kern = p.sk_tiles > 0 ? qmm_tc_sk_kernel<T, C, false, true, true> : qmm_tc_kernel<T, C, false, false, true>;
+  auto kern = p.sk_tiles > 0 ? qmm_tc_sk_kernel<T, C, false, true, true, TO> : qmm_tc_kernel<T, C, false, false, true, TO>;
   const size_t smem = C::SMEM + 1024;  // + the producer's scale table
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
@@ -1790,9 +1981,14 @@ cudaError_t launch_qmm_tc_glu(const void* x, int xdt, int64_t M, int64_t K, cons
   int dev = 0, sms = 152;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  if (xdt == kBF16)
-    return M <= 128 ? launch_glu_cfg<__nv_bfloat16, Tile128x256>(x, M, K, w, scales, gs, cols, act, y, sms, st)
-                    : launch_glu_cfg<__nv_bfloat16, Tile256x256>(x, M, K, w, scales, gs, cols, act, y, sms, st);
+  if (xdt == kBF16) {  // through the f16 kernel (rows_to_f16)
+    const float* rs = nullptr;
+    cudaError_t e = rows_to_f16(x, M, K, nullptr, M, sms, st, &x, &rs);
+    if (e != cudaSuccess) return e;
+    return M <= 128
+               ? launch_glu_cfg<__half, Tile128x256, __nv_bfloat16>(x, M, K, w, scales, gs, cols, act, y, sms, st, rs)
+               : launch_glu_cfg<__half, Tile256x256, __nv_bfloat16>(x, M, K, w, scales, gs, cols, act, y, sms, st, rs);
+  }
   return M <= 128 ? launch_glu_cfg<__half, Tile128x256>(x, M, K, w, scales, gs, cols, act, y, sms, st)
                   : launch_glu_cfg<__half, Tile256x256>(x, M, K, w, scales, gs, cols, act, y, sms, st);
 }
@@ -1807,9 +2003,9 @@ cudaError_t launch_qmm_tc_nt(const void* x, int xdt, int64_t M, int64_t K, const
   int dev = 0, sms = 152;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  if (xdt == kBF16)
-    return M <= 128 ? launch_nt_cfg<__nv_bfloat16, Tile128x256>(x, M, K, w, scales, gs, N, y, sms, st)
-                    : launch_nt_cfg<__nv_bfloat16, Tile256x256>(x, M, K, w, scales, gs, N, y, sms, st);
+  if (xdt == kBF16)  // through the f16 kernels (rows_to_f16)
+    return M <= 128 ? launch_nt_cfg<__half, Tile128x256, __nv_bfloat16>(x, M, K, w, scales, gs, N, y, sms, st)
+                    : launch_nt_cfg<__half, Tile256x256, __nv_bfloat16>(x, M, K, w, scales, gs, N, y, sms, st);
   return M <= 128 ? launch_nt_cfg<__half, Tile128x256>(x, M, K, w, scales, gs, N, y, sms, st)
                   : launch_nt_cfg<__half, Tile256x256>(x, M, K, w, scales, gs, N, y, sms, st);
 }
