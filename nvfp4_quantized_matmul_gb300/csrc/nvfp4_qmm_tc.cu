@@ -1586,11 +1586,13 @@ __device__ __forceinline__ uint32_t finite_abs_max(uint32_t mx, uint32_t w) {
   return mx;
 }
 
-// One CTA per row; a row of up to 256 * kRowRegUnits 16-byte units is read
-// once and kept in registers between the maximum and the conversion,
-// longer rows are read twice.
-constexpr int kRowThreads = 256, kRowRegUnits = 12;
-__global__ void __launch_bounds__(kRowThreads) rows_to_f16_kernel(const uint4* __restrict__ x,
+// One CTA of kRowThreads per row; a row of up to kRowThreads * kRowRegUnits
+// 16-byte units is read once and kept in registers between the maximum and
+// the conversion, longer rows are read twice. Short rows take the small
+// instance (128 x 6: about 40 registers, so every row of a 2048-row call is
+// resident at once), long ones 256 x 12.
+template <int kRowThreads, int kRowRegUnits, int kMinBlocks>
+__global__ void __launch_bounds__(kRowThreads, kMinBlocks) rows_to_f16_kernel(const uint4* __restrict__ x,
                                                                   const uint32_t* __restrict__ lhs, int64_t B,
                                                                   int64_t R, int kv, uint4* __restrict__ xh,
                                                                   float* __restrict__ rs) {
@@ -1687,8 +1689,11 @@ cudaError_t rows_to_f16(const void* x, int64_t R, int64_t K, const uint32_t* lhs
   cudaError_t e = gather_buffer(dev, st, xb + (size_t)R * 4, &buf);
   if (e != cudaSuccess) return e;
   float* scale = reinterpret_cast<float*>(static_cast<char*>(buf) + xb);
-  if (kp == K) {
-    rows_to_f16_kernel<<<(unsigned)(R < 16 * sms ? R : 16 * sms), kRowThreads, 0, st>>>(
+  if (kp == K && K / 8 <= 128 * 6) {
+    rows_to_f16_kernel<128, 6, 10><<<(unsigned)(R < 16 * sms ? R : 16 * sms), 128, 0, st>>>(
+        static_cast<const uint4*>(x), lhs, B, R, (int)(K / 8), static_cast<uint4*>(buf), scale);
+  } else if (kp == K) {
+    rows_to_f16_kernel<256, 12, 3><<<(unsigned)(R < 8 * sms ? R : 8 * sms), 256, 0, st>>>(
         static_cast<const uint4*>(x), lhs, B, R, (int)(K / 8), static_cast<uint4*>(buf), scale);
   } else {  // (no row gather with K % 8 != 0: the gather route needs K % 16 == 0)
     const int64_t blocks = (R + 7) / 8;
