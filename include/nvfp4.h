@@ -167,10 +167,10 @@ nvfp4_status nvfp4_qmm_routed(const void* x, nvfp4_dtype x_dtype, int64_t M, int
  *   x_dtype. N % 16 == 0 (ERR_SHAPE otherwise). x, y, w and scales 16-byte
  *   aligned (ERR_ALIGN). M == 0 or N == 0 returns OK without a launch; K == 0
  *   writes zeros.
- * Up to eight token rows: one streaming pass over the plane (m16n8k16 MMAs
- * on nibble-interleaved pairs of input rows; each warp a run of 16-input
- * steps of one 256-output slab), partial sums added into a float workspace
- * [8, N] owned by the library, one per (device, stream), returned to zero by
+ * Up to sixteen token rows: one streaming pass over the plane per eight rows
+ * (m16n8k16 MMAs on nibble-interleaved pairs of input rows; each warp a run
+ * of 16-input steps of one 256-output slab), partial sums added into a float
+ * workspace [16, N] owned by the library, one per (device, stream), returned to zero by
  * every call; then y. More rows (or the NVFP4_OPT_NT_DECODE option set to
  * 0): the tcgen05 tensor-core
  * kernel, whose producer warps decode and transpose the weight tiles into
@@ -356,7 +356,7 @@ typedef enum {
   NVFP4_OPT_TC_TILE = 1,        /* prefill tile: 0 automatic (default), 1 256x256, 2 256x128, 3 128x256 */
   NVFP4_OPT_TC_STREAMK = 2,     /* 1 (default): fewer than two waves of prefill tiles are split by k-blocks
                                    over all SMs; 0: whole tiles only */
-  NVFP4_OPT_NT_DECODE = 3,      /* 1 (default): up to eight rows of a non-transposed weight take the streaming
+  NVFP4_OPT_NT_DECODE = 3,      /* 1 (default): up to sixteen rows of a non-transposed weight take the streaming
                                    kernel; 0: the tensor cores */
   NVFP4_OPT_QMV_ROW_TILES = 4,  /* 16-row weight tiles per decode consumer warp: 0 automatic (default), 1, 2 */
   NVFP4_OPT_GATHER_GROUP = 5,   /* 1 (default): decode-shape gathers grouped by expert; 0: the per-row kernel */

@@ -402,7 +402,7 @@ nvfp4_status nvfp4_qmm_nontransposed(const void* x, nvfp4_dtype x_dtype, int64_t
   if (!aligned(x, 16) || !aligned(y, 16)) return fail(NVFP4_ERR_ALIGN, "%s: x and y must be 16-byte aligned", fn);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (K == 0) return cuda_status(fn, cudaMemsetAsync(y, 0, (size_t)(M * N * dtype_size(x_dtype)), st));
-  // up to eight token rows: one streaming pass (the NVFP4_OPT_NT_DECODE option
+  // up to sixteen token rows: streaming passes (the NVFP4_OPT_NT_DECODE option
   // set to 0 sends every M to the tensor cores)
   if (nvfp4::option(nvfp4::kOptNtDecode) != 0 && nvfp4::qmv_nt_supported(M, N, K))
     return cuda_status(fn, nvfp4::launch_qmv_nt(x, (int)x_dtype, M, K, w, scales, gs, N, y, st));

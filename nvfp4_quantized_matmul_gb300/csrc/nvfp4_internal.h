@@ -123,10 +123,11 @@ cudaError_t launch_qmm_tc_glu(const void* x, int xdt, int64_t M, int64_t K, cons
 // 0, any K >= 1), y = x @ dequantize(w) * gs/2688; f16 or bf16 x.
 bool qmm_tc_nt_supported(int64_t M, int64_t N, int64_t K);
 // Up to kQmvNtMaxM token rows of a non-transposed weight: one streaming pass
-// over the plane (the eight token rows are the eight columns of an m16n8k16
-// MMA's B operand, so any M up to 8 costs the same), partial sums in a
-// per-stream float workspace, then y.
-constexpr int64_t kQmvNtMaxM = 8;
+// over the plane per eight rows (the eight token rows are the eight columns
+// of an m16n8k16 MMA's B operand, so any M up to 8 costs the same), partial
+// sums in a per-stream float workspace, then y. Two passes (M = 9..16) still
+// beat the tensor cores ([5376, 21504]: about 62 against 71 µs at M = 16).
+constexpr int64_t kQmvNtMaxM = 16;
 bool qmv_nt_supported(int64_t M, int64_t N, int64_t K);
 cudaError_t launch_qmv_nt(const void* x, int xdt, int64_t M, int64_t K, const uint32_t* w, const uint8_t* scales,
                           const float* gs, int64_t N, void* y, cudaStream_t st);

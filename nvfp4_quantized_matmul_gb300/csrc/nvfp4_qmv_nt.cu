@@ -1,6 +1,7 @@
 // Decode-size QuantizedMatmul with a non-transposed weight (mlx PR #2629,
 // Changes during review: the quantized axis of such a weight is N): y = x @
-// dequantize(w) * gs / 2688 for up to eight token rows, w [K, N/8] words
+// dequantize(w) * gs / 2688 for up to sixteen token rows (one pass over the
+// plane per eight), w [K, N/8] words
 // (word j of row k holds outputs 8j..8j+7 of input k, nibble i output 8j+i),
 // one E4M3 byte per 16 outputs of an input.
 //
@@ -459,15 +460,20 @@ cudaError_t launch_t(const void* x, int64_t M, int64_t K, const uint32_t* w, con
   float* ws = nullptr;
   cudaError_t e = nt_workspace(dev, st, (size_t)kQmvNtMaxM * (size_t)N, &ws);
   if (e != cudaSuccess) return e;
-  NtArgs a{x, (int)M, K, w, scales, N, ws, (K + 15) / 16, 0, 0};
-  a.steps = (N / 8 + kNtSlabWords - 1) / kNtSlabWords * a.ksteps;
   // copies need 16-byte word rows in whole 4-word units, 8-byte scale rows in
   // whole 8-byte units and 8-byte activation units
   const bool aligned = N % 128 == 0 && K % 4 == 0 && N < (1ll << 31) && K < (1ll << 30) &&
                        reinterpret_cast<uintptr_t>(w) % 16 == 0 && reinterpret_cast<uintptr_t>(scales) % 8 == 0 &&
                        reinterpret_cast<uintptr_t>(x) % 8 == 0;
-  e = aligned ? launch_kernel<T, true>(a, sms, st) : launch_kernel<T, false>(a, sms, st);
-  if (e != cudaSuccess) return e;
+  // one pass per eight token rows (the MMA's eight B columns); a second pass
+  // reads the plane again
+  for (int64_t m0 = 0; m0 < M; m0 += 8) {
+    const int64_t mp = M - m0 < 8 ? M - m0 : 8;
+    NtArgs a{static_cast<const T*>(x) + m0 * K, (int)mp, K, w, scales, N, ws + m0 * N, (K + 15) / 16, 0, 0};
+    a.steps = (N / 8 + kNtSlabWords - 1) / kNtSlabWords * a.ksteps;
+    e = aligned ? launch_kernel<T, true>(a, sms, st) : launch_kernel<T, false>(a, sms, st);
+    if (e != cudaSuccess) return e;
+  }
   const int64_t n = M * N, fb = (n + 255) / 256;
   qmv_nt_finish<T><<<(unsigned)(fb < 4 * sms ? fb : 4 * sms), 256, 0, st>>>(ws, n, gs, static_cast<T*>(y));
   return cudaGetLastError();

@@ -126,13 +126,13 @@ def test_nontransposed_zero_k_and_empty(nv):
     assert y.shape == (5, 64) and bool((y == 0).all())
 
 
-# (M, K, N) for the decode route (M <= 8): K inside one 16-input step, across
+# (M, K, N) for the decode route (M <= 16, eight rows per pass): K inside one 16-input step, across
 # steps with a ragged last one, not a multiple of 4 or 8; N ending inside a
 # 256-output slab and inside a word pair; planes that take the copy ring
 # (N % 128 == 0, K % 4 == 0) and planes that take plain loads
 NT_DECODE = [(1, 17, 32), (2, 100, 272), (1, 128, 1008), (2, 300, 256), (1, 2048, 2560), (2, 5376, 4096),
              (1, 777, 528), (2, 21504, 512), (3, 1000, 1024), (5, 260, 384), (8, 513, 640), (7, 4096, 2048),
-             (4, 64, 16), (6, 18, 2304)]
+             (4, 64, 16), (6, 18, 2304), (9, 77, 640), (12, 1000, 1024), (16, 300, 256)]
 
 
 @pytest.mark.parametrize("mkn", NT_DECODE, ids=lambda v: "M%d_K%d_N%d" % v)
