@@ -1586,66 +1586,73 @@ __device__ __forceinline__ uint32_t finite_abs_max(uint32_t mx, uint32_t w) {
   return mx;
 }
 
-// One CTA of kRowThreads per row; a row of up to kRowThreads * kRowRegUnits
-// 16-byte units is read once and kept in registers between the maximum and
-// the conversion, longer rows are read twice. Short rows take the small
-// instance (128 x 6: about 40 registers, so every row of a 2048-row call is
-// resident at once), long ones 256 x 12.
-template <int kRowThreads, int kRowRegUnits, int kMinBlocks>
-__global__ void __launch_bounds__(kRowThreads, kMinBlocks) rows_to_f16_kernel(const uint4* __restrict__ x,
-                                                                  const uint32_t* __restrict__ lhs, int64_t B,
-                                                                  int64_t R, int kv, uint4* __restrict__ xh,
-                                                                  float* __restrict__ rs) {
-  __shared__ uint32_t s_max[kRowThreads / 32];
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  for (int64_t r = blockIdx.x; r < R; r += gridDim.x) {
-    const int64_t src = lhs ? (int64_t)__ldg(lhs + r) : r;
-    uint4* out = xh + r * kv;
-    if (src >= B) {  // block-uniform
-      for (int j = tid; j < kv; j += kRowThreads) out[j] = make_uint4(0, 0, 0, 0);
-      if (tid == 0) rs[r] = 1.0f;
-      continue;
-    }
-    const uint4* row = x + src * kv;
-    const bool in_regs = kv <= kRowThreads * kRowRegUnits;
-    uint4 v[kRowRegUnits];
+// kTPR threads per row (a warp, or several warps of a 256-thread CTA); a row
+// of up to kTPR * kUnits 16-byte units is read once and kept in registers
+// between the maximum and the conversion, longer rows are read twice. The
+// launch picks the smallest group that holds the row: a warp per row up to
+// 2048 elements (eight rows per CTA), 128 threads up to 6144, 256 threads up
+// to 24576; every row of a 2048-row call with K = 5376 is then resident at
+// once, and 32768 short rows do not queue behind each other in one CTA.
+template <int kTPR, int kUnits, int kMinBlocks>
+__global__ void __launch_bounds__(256, kMinBlocks) rows_to_f16_kernel(const uint4* __restrict__ x,
+                                                                      const uint32_t* __restrict__ lhs, int64_t B,
+                                                                      int64_t R, int kv, uint4* __restrict__ xh,
+                                                                      float* __restrict__ rs) {
+  constexpr int kGroups = 256 / kTPR, kWarpsPerRow = kTPR / 32;
+  __shared__ uint32_t s_max[8];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, grp = tid / kTPR, gtid = tid % kTPR;
+  // every thread of the CTA takes the same number of turns (the barriers)
+  for (int64_t base = (int64_t)blockIdx.x * kGroups; base < R; base += (int64_t)gridDim.x * kGroups) {
+    const int64_t r = base + grp;
+    const bool has = r < R;
+    const int64_t src = has ? (lhs ? (int64_t)__ldg(lhs + r) : r) : B;
+    const bool live = src < B;  // uniform over the row's group
+    const uint4* row = x + (live ? src : 0) * kv;
+    const bool in_regs = kv <= kTPR * kUnits;
+    uint4 v[kUnits];
     uint32_t mx = 0;
     if (in_regs) {
 #pragma unroll
-      for (int i = 0; i < kRowRegUnits; ++i) {
-        const int j = tid + i * kRowThreads;
-        v[i] = j < kv ? __ldg(row + j) : make_uint4(0, 0, 0, 0);
+      for (int i = 0; i < kUnits; ++i) {
+        const int j = gtid + i * kTPR;
+        v[i] = live && j < kv ? __ldg(row + j) : make_uint4(0, 0, 0, 0);
       }
 #pragma unroll
-      for (int i = 0; i < kRowRegUnits; ++i)
+      for (int i = 0; i < kUnits; ++i)
         mx = finite_abs_max(finite_abs_max(finite_abs_max(finite_abs_max(mx, v[i].x), v[i].y), v[i].z), v[i].w);
-    } else {
-      for (int j = tid; j < kv; j += kRowThreads) {
+    } else if (live) {
+      for (int j = gtid; j < kv; j += kTPR) {
         const uint4 u = __ldg(row + j);
         mx = finite_abs_max(finite_abs_max(finite_abs_max(finite_abs_max(mx, u.x), u.y), u.z), u.w);
       }
     }
-    mx = __reduce_max_sync(0xffffffffu, mx);
-    if (lane == 0) s_max[warp] = mx;
-    __syncthreads();
-    mx = s_max[0];
+    mx = __reduce_max_sync(0xffffffffu, mx);  // a warp never spans two rows
+    if constexpr (kWarpsPerRow > 1) {
+      if (lane == 0) s_max[warp] = mx;
+      __syncthreads();
 #pragma unroll
-    for (int w = 1; w < kRowThreads / 32; ++w) mx = s_max[w] > mx ? s_max[w] : mx;
-    __syncthreads();  // s_max is rewritten for the next row
-    const int sh = f16_row_shift(mx);
+      for (int w = 0; w < kWarpsPerRow; ++w) {
+        const uint32_t o = s_max[grp * kWarpsPerRow + w];
+        mx = o > mx ? o : mx;
+      }
+      __syncthreads();  // s_max is rewritten on the next turn
+    }
+    if (!has) continue;
+    const int sh = f16_row_shift(mx);  // 0 for a zero row
     const float up = __uint_as_float((uint32_t)(sh + 127) << 23);
-    if (tid == 0) rs[r] = __uint_as_float((uint32_t)(127 - sh) << 23);
+    if (gtid == 0) rs[r] = __uint_as_float((uint32_t)(127 - sh) << 23);
+    uint4* out = xh + r * kv;
     if (in_regs) {
 #pragma unroll
-      for (int i = 0; i < kRowRegUnits; ++i) {
-        const int j = tid + i * kRowThreads;
+      for (int i = 0; i < kUnits; ++i) {
+        const int j = gtid + i * kTPR;
         if (j < kv)
           out[j] = make_uint4(bf16x2_to_f16x2_scaled(v[i].x, up), bf16x2_to_f16x2_scaled(v[i].y, up),
                               bf16x2_to_f16x2_scaled(v[i].z, up), bf16x2_to_f16x2_scaled(v[i].w, up));
       }
     } else {
-      for (int j = tid; j < kv; j += kRowThreads) {
-        const uint4 u = __ldg(row + j);
+      for (int j = gtid; j < kv; j += kTPR) {
+        const uint4 u = live ? __ldg(row + j) : make_uint4(0, 0, 0, 0);
         out[j] = make_uint4(bf16x2_to_f16x2_scaled(u.x, up), bf16x2_to_f16x2_scaled(u.y, up),
                             bf16x2_to_f16x2_scaled(u.z, up), bf16x2_to_f16x2_scaled(u.w, up));
       }
@@ -1689,12 +1696,20 @@ cudaError_t rows_to_f16(const void* x, int64_t R, int64_t K, const uint32_t* lhs
   cudaError_t e = gather_buffer(dev, st, xb + (size_t)R * 4, &buf);
   if (e != cudaSuccess) return e;
   float* scale = reinterpret_cast<float*>(static_cast<char*>(buf) + xb);
-  if (kp == K && K / 8 <= 128 * 6) {
-    rows_to_f16_kernel<128, 6, 10><<<(unsigned)(R < 16 * sms ? R : 16 * sms), 128, 0, st>>>(
-        static_cast<const uint4*>(x), lhs, B, R, (int)(K / 8), static_cast<uint4*>(buf), scale);
+  const int kv = (int)(K / 8);
+  auto grid_for = [&](int64_t rows_per_cta) {
+    const int64_t b = (R + rows_per_cta - 1) / rows_per_cta;
+    return (unsigned)(b < 16 * sms ? b : 16 * sms);
+  };
+  if (kp == K && kv <= 32 * 8) {
+    rows_to_f16_kernel<32, 8, 3><<<grid_for(8), 256, 0, st>>>(static_cast<const uint4*>(x), lhs, B, R, kv,
+                                                             static_cast<uint4*>(buf), scale);
+  } else if (kp == K && kv <= 128 * 6) {
+    rows_to_f16_kernel<128, 6, 4><<<grid_for(2), 256, 0, st>>>(static_cast<const uint4*>(x), lhs, B, R, kv,
+                                                              static_cast<uint4*>(buf), scale);
   } else if (kp == K) {
-    rows_to_f16_kernel<256, 12, 3><<<(unsigned)(R < 8 * sms ? R : 8 * sms), 256, 0, st>>>(
-        static_cast<const uint4*>(x), lhs, B, R, (int)(K / 8), static_cast<uint4*>(buf), scale);
+    rows_to_f16_kernel<256, 12, 3><<<grid_for(1), 256, 0, st>>>(static_cast<const uint4*>(x), lhs, B, R, kv,
+                                                               static_cast<uint4*>(buf), scale);
   } else {  // (no row gather with K % 8 != 0: the gather route needs K % 16 == 0)
     const int64_t blocks = (R + 7) / 8;
     rows_to_f16_pad_kernel<<<(unsigned)(blocks < 8 * sms ? blocks : 8 * sms), 256, 0, st>>>(
