@@ -354,8 +354,8 @@ int nvfp4_set_launch_overlap(int enable);
  * tolerances whatever is set. Not part of the pages' interface. */
 typedef enum {
   NVFP4_OPT_TC_TILE = 1,        /* prefill tile: 0 automatic (default), 1 256x256, 2 256x128, 3 128x256 */
-  NVFP4_OPT_TC_STREAMK = 2,     /* 1 (default): fewer than two waves of prefill tiles are split by k-blocks
-                                   over all SMs; 0: whole tiles only */
+  NVFP4_OPT_TC_STREAMK = 2,     /* 1 (default): fewer than two waves of prefill tiles, the second at most 60%
+                                   full, are split by k-blocks over all SMs; 0: whole tiles only */
   NVFP4_OPT_NT_DECODE = 3,      /* 1 (default): up to sixteen rows of a non-transposed weight take the streaming
                                    kernel; 0: the tensor cores */
   NVFP4_OPT_QMV_ROW_TILES = 4,  /* 16-row weight tiles per decode consumer warp: 0 automatic (default), 1, 2 */

@@ -1400,6 +1400,16 @@ cudaError_t sk_workspace(int dev, cudaStream_t st, size_t floats, size_t counter
 
 bool stream_k_on() { return tc_stream_k(); }
 
+// The stream-K split applies to launches of fewer than two waves whose
+// partial wave would be at most 60% full. Measured on [21504, 5376] with
+// 256x256 tiles: 168 tiles (1.1 waves, M = 512) 121.6 us split against 125.0
+// whole; 252 tiles (1.66 waves, M = 768) 154.7 split against 137.3 whole;
+// 84 tiles (M = 256) 72.9 against 73.7; far fewer tiles than SMs (the decode
+// linears at M <= 128) 1.1 to 2.9x faster split.
+bool split_k(int tiles, int sms) {
+  return stream_k_on() && tiles % sms != 0 && tiles < 2 * sms && (int64_t)(tiles % sms) * 5 <= (int64_t)sms * 3;
+}
+
 // Fewest k-blocks a CTA takes of the stream-K tiles when they are fewer than
 // the SMs (smaller pieces cost more to combine than they save).
 constexpr int64_t kMinSkBlocks = 8;
@@ -1439,15 +1449,16 @@ cudaError_t launch_cfg(const void* x, int64_t M, int64_t K, const uint32_t* w, c
   p.glu_act = 0;
   p.row_scale = row_scale;
   // Tiles are dealt whole, round robin, unless they make fewer than two
-  // waves: then the partial wave would idle a large share of the SMs, and
-  // all tiles are split evenly by k-blocks instead (stream-K). From two
-  // waves on, splitting only the last wave cost more than it saved (M = 2048
-  // on [21504, 5376], 4.4 waves: 365 us whole-tile, 371 us split).
+  // waves with a mostly empty partial wave (split_k): then that wave would
+  // idle a large share of the SMs, and all tiles are split evenly by
+  // k-blocks instead (stream-K). From two waves on, splitting only the last
+  // wave cost more than it saved (M = 2048 on [21504, 5376], 4.4 waves: 365
+  // us whole-tile, 371 us split).
   const int T_ = p.num_tiles;
   int grid = T_ < sms ? T_ : sms;
   p.dp_tiles = T_;
   p.sk_tiles = 0;
-  if (stream_k_on() && T_ % sms != 0 && T_ < 2 * sms) {
+  if (split_k(T_, sms)) {
     if (T_ > sms) {
       p.dp_tiles = 0;
       grid = sms;
@@ -1530,10 +1541,11 @@ cudaError_t launch_glu_cfg(const void* x, int64_t M, int64_t K, const uint32_t* 
   return cudaGetLastError();
 }
 
-// Tile shape. Below two waves of 256x256 tiles the stream-K split leaves no
-// partial wave to avoid, and 256x256 tiles, whose decoded weight tile feeds
-// twice the MMA work, were the fastest or within 4% of it on every such shape
-// measured on GB300 (M = 64 .. 512 at K = 5376, M = 2048 at K = 21504).
+// Tile shape. Below two waves of 256x256 tiles (split by k-blocks, or one
+// wave and a mostly full second one), 256x256 tiles, whose decoded weight
+// tile feeds twice the MMA work, were the fastest or within 4% of it on every
+// such shape measured on GB300 (M = 64 .. 768 at K = 5376, M = 2048 at K =
+// 21504).
 // Otherwise (or with the stream-K option off) the shape is picked by
 // modelled time: whole waves of persistent tiles, each tile's cost its area
 // over the shape's relative throughput (measured with full waves at M = 8192,
@@ -1542,7 +1554,7 @@ cudaError_t launch_glu_cfg(const void* x, int64_t M, int64_t K, const uint32_t* 
 int pick_tile(int64_t M, int64_t N, int sms) {
   const int forced = option(kOptTcTile);  // 1 256x256, 2 256x128, 3 128x256
   if (forced >= 1 && forced <= 3) return forced - 1;
-  // fewer than two waves of 256x256 tiles: the stream-K split applies
+  // fewer than two waves of 256x256 tiles
   if (stream_k_on() && ((M + 255) / 256) * ((N + 255) / 256) < 2 * sms) return 0;
   const int bm[3] = {256, 256, 128}, bn[3] = {256, 128, 256};
   const double rate[3] = {1.0, 0.81, 0.54};
@@ -1956,7 +1968,7 @@ cudaError_t launch_nt_cfg(const void* x, int64_t M, int64_t K, const uint32_t* w
   p.sk_tiles = 0;
   p.ws = nullptr;
   p.ws_cnt = nullptr;
-  if (stream_k_on() && T_ % sms != 0 && T_ < 2 * sms) {
+  if (split_k(T_, sms)) {
     p.dp_tiles = 0;
     p.sk_tiles = T_;
     if (T_ > sms) {
