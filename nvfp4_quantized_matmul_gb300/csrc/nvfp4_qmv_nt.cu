@@ -1,20 +1,19 @@
 // Decode-size QuantizedMatmul with a non-transposed weight (mlx PR #2629,
 // Changes during review: the quantized axis of such a weight is N): y = x @
-// dequantize(w) * gs / 2688 for up to sixteen token rows (one pass over the
-// plane per eight), w [K, N/8] words
+// dequantize(w) * gs / 2688 for up to sixteen token rows, w [K, N/8] words
 // (word j of row k holds outputs 8j..8j+7 of input k, nibble i output 8j+i),
 // one E4M3 byte per 16 outputs of an input.
 //
-// The weight plane is streamed once, through m16n8k16 MMAs: A is the weight
-// (rows = outputs, columns = inputs), B the activations (eight token
-// columns). An MMA wants each register's two f16 values to be neighbours
-// along K, while a word holds neighbours along N; so the words of two input
-// rows are interleaved nibble by nibble (two shifts and two logic ops give
-// two words whose bytes are (row k, row k+1) code pairs), and one E2M1x2
-// conversion then yields the pair the MMA expects. The scale pair of those
-// two rows multiplies it (fp4 * e4m3 is exact in f16). A lane (g, t) owns
-// inputs 4t..4t+3 of every 16-input step and word columns 4g..4g+3 of its
-// warp's 32-word slab; MMA p of column c puts output 8j+2p in row g and
+// The weight plane is streamed once per eight token rows, through m16n8k16
+// MMAs: A is the weight (rows = outputs, columns = inputs), B the activations
+// (eight token columns). An MMA wants each register's two f16 values to be
+// neighbours along K, while a word holds neighbours along N; so the words of
+// two input rows are interleaved nibble by nibble (two shifts and two logic
+// ops give two words whose bytes are (row k, row k+1) code pairs), and one
+// E2M1x2 conversion then yields the pair the MMA expects. The scale pair of
+// those two rows multiplies it (fp4 * e4m3 is exact in f16). A lane (g, t)
+// owns inputs 4t..4t+3 of every 16-input step and word columns 4g..4g+3 of
+// its warp's 32-word slab; MMA p of column c puts output 8j+2p in row g and
 // 8j+2p+1 in row g+8. Every lane thus decodes each word it loads exactly
 // once, with no data exchanged between lanes.
 //
@@ -23,10 +22,9 @@
 // through its own ring of shared-memory stages filled by per-lane cp.async
 // copies (weights 2 KB, scale bytes 256 B and activations 256 B a step;
 // planes whose rows or bases do not meet the copy alignment are loaded and
-// stored instead). A
-// run that leaves a slab, or ends, adds its sums into a float workspace [M,
-// N] (red.global.add.v4.f32); a second kernel scales, rounds and writes y,
-// and returns the workspace to zero for the next call.
+// stored instead). A run that leaves a slab, or ends, adds its sums into a
+// float workspace [M, N] (red.global.add.v4.f32); a second kernel scales,
+// rounds and writes y, and returns the workspace to zero for the next call.
 //
 // bf16 activations take the f16 MMA when a step's values convert to f16
 // exactly (checked per step, warp-wide); otherwise that step decodes the
